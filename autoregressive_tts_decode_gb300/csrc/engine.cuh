@@ -1,0 +1,75 @@
+// engine.cuh -- the handle behind the C ABI and the workspace layout.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "common.cuh"
+#include "../../include/q3tts.h"
+
+namespace q3 {
+
+// Per-call description of a frame step, passed by value to the set-up kernel.
+struct StepDesc {
+  int n;
+  int sid[Q3TTS_MAX_STREAMS];       // stream id of active slot b
+  int pos[Q3TTS_MAX_STREAMS];       // Talker position the frame writes
+  int newpage[Q3TTS_MAX_STREAMS];   // page id to enter at pos / page_size, or -1
+  q3tts_sampling sp[Q3TTS_MAX_STREAMS];
+};
+
+struct FrameKernelState;  // persistent frame kernel (frame_kernel.cu)
+
+}  // namespace q3
+
+struct q3tts_handle {
+  q3tts_config c;
+  std::vector<q3tts_layer_weights> tl, cl;
+  q3tts_weights w;
+  cudaStream_t s;
+  int dev, n_sm;
+
+  // dimensions
+  int Dt, Dc, Ft, Fc, Hq, Hkv, hd, Vt, Vc, qkv_rows, pps, n_pages, chunk, m_max, esz;
+
+  // workspace carve-up
+  float* rope_cos;  // [kv_cap][hd/2]
+  float* rope_sin;
+  void* kv_pool;    // Talker KV, paged
+  int* page_table;  // [max_streams][pps]
+  float* cp_kv;     // CodePredictor KV: one 16-slot page per stream, fp32
+  int* cp_page_table;
+  float* pending_h;       // [max_streams][D_t]
+  float* pending_logits;  // [max_streams][V_t]
+  uint8_t* history;       // [max_streams][V_t]
+  int* d_sid;             // [max_streams]
+  int* d_pos;
+  q3tts_sampling* d_sp;
+  int* d_fed;             // [max_streams][16] codes fed forward
+  int* d_tok_stream;      // [m_max]
+  int* d_tok_pos;         // [m_max]
+  float *x, *hb, *qkv, *att, *gu, *act, *uin, *cpx, *logits;
+  int* d_err;
+
+  // host-side stream bookkeeping
+  std::vector<int> len;  // Talker positions held; -1 = no prompt yet
+  std::vector<std::vector<int>> pages;
+  std::vector<int> free_pages;
+
+  q3::FrameKernelState* fk;
+  uint64_t launches = 0;
+};
+
+namespace q3 {
+
+// Layered frame step (one kernel per operation), any number of streams.
+int step_layered(q3tts_handle* h, const StepDesc& d, const float* uniforms, int32_t* codes,
+                 const int32_t* forced, float* logits);
+int prefill_layered(q3tts_handle* h, int sid, const float* embeds, int len);
+
+KVDesc talker_kv(const q3tts_handle* h);
+KVDesc cp_kv(const q3tts_handle* h);
+
+}  // namespace q3

@@ -1,0 +1,46 @@
+// layers.cuh -- one-kernel-per-operation building blocks of the decoder stack.
+//
+// These kernels run the Talker prefill (many positions at once) and the
+// layer-by-layer frame step for any number of streams.  Activations are fp32,
+// weights fp32 or bf16 (template WT), the Talker KV cache fp32 or bf16 (KT).
+// A "token" m is one row of the activation buffers; tok_stream[m] names its
+// stream and tok_pos[m] its position (when tok_pos is NULL every token sits at
+// pos_const).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "../../include/q3tts.h"
+
+namespace q3 {
+
+struct TokDesc {
+  const int* tok_stream;
+  const int* tok_pos;  // NULL: every token at pos_const
+  int pos_const;
+};
+
+// Y[m, n] (+)= sum_k X[m, k] W[n, k] for m < M, n < N.
+void launch_linear(int wdt, const float* X, int ldx, const void* W, int N, int K, float* Y, int ldy,
+                   int M, bool accumulate, cudaStream_t s);
+
+// Y[m] = X[in_row(m)] / rms * g, in_row(m) = m * in_mul + in_add.
+void launch_rmsnorm(int wdt, const float* X, int ldx, int in_mul, int in_add, const void* g,
+                    float* Y, int ldy, int M, int D, float eps, cudaStream_t s);
+
+// Per token: q and k heads RMSNorm'ed (if qk_norm) and rotated at the token's
+// position; q written back in place, k and v stored into the paged cache.
+void launch_qk_rope_append(int wdt, int kdt, float* qkv, int ld, int M, TokDesc td, const void* gq,
+                           const void* gk, int qk_norm, float eps, const float* rope_cos,
+                           const float* rope_sin, KVDesc kv, int layer, int Hq, cudaStream_t s);
+
+// Single-query attention of every token over positions 0..pos of its stream.
+void launch_attention(int kdt, const float* qkv, int ld, int M, TokDesc td, KVDesc kv, int layer,
+                      int Hq, float* out, int ldo, int max_ctx, cudaStream_t s);
+
+// a[m, f] = silu(gu[m, f]) * gu[m, F + f]
+void launch_silu_mul(const float* gu, float* a, int M, int F, cudaStream_t s);
+
+}  // namespace q3

@@ -1,0 +1,259 @@
+// step.cu -- prefill and the layer-by-layer frame step (one kernel per operation).
+//
+// Frame structure ("Running Qwen3-TTS on an AMD R9700", section "Running
+// Qwen3-TTS"): the semantic token comes from the Talker's pending logits, the
+// CodePredictor then produces acoustic tokens 1..15 one pass at a time (pass 0
+// over the Talker hidden and the semantic token's embedding, pass j over the
+// embedding of token j), and the sum of the frame's 16 code embeddings
+// ("qwen3-tts-hip" README, "Python Parity Fixtures": embedding-sum parity) is
+// the input of one Talker step whose final norm and codec head leave the next
+// pending logits.
+#include "engine.cuh"
+#include "layers.cuh"
+#include "sampler.cuh"
+
+namespace q3 {
+
+KVDesc talker_kv(const q3tts_handle* h) {
+  KVDesc d;
+  d.pool = h->kv_pool;
+  d.page_table = h->page_table;
+  d.pages_per_stream = h->pps;
+  d.page_size = h->c.page_size;
+  d.n_pages = h->n_pages;
+  d.Hkv = h->Hkv;
+  d.hd = h->hd;
+  return d;
+}
+
+KVDesc cp_kv(const q3tts_handle* h) {
+  KVDesc d;
+  d.pool = h->cp_kv;
+  d.page_table = h->cp_page_table;
+  d.pages_per_stream = 1;
+  d.page_size = Q3TTS_N_CODEBOOKS;
+  d.n_pages = h->c.max_streams;
+  d.Hkv = h->Hkv;
+  d.hd = h->hd;
+  return d;
+}
+
+// ----------------------------------------------------------- small kernels
+
+__global__ void setup_kernel(StepDesc d, int* sid, int* pos, q3tts_sampling* sp, int* page_table,
+                             int pps, int page_size, int* tok_stream, int* tok_pos) {
+  for (int b = threadIdx.x; b < d.n; b += blockDim.x) {
+    sid[b] = d.sid[b];
+    pos[b] = d.pos[b];
+    sp[b] = d.sp[b];
+    if (d.newpage[b] >= 0) page_table[d.sid[b] * pps + d.pos[b] / page_size] = d.newpage[b];
+    // CodePredictor pass 0: two tokens per stream at positions 0 and 1
+    tok_stream[2 * b] = d.sid[b];
+    tok_stream[2 * b + 1] = d.sid[b];
+    tok_pos[2 * b] = 0;
+    tok_pos[2 * b + 1] = 1;
+  }
+}
+
+__global__ void fill_tokens_kernel(int* tok_stream, int* tok_pos, int T, int sid, int pos0) {
+  for (int m = blockIdx.x * blockDim.x + threadIdx.x; m < T; m += gridDim.x * blockDim.x) {
+    tok_stream[m] = sid;
+    tok_pos[m] = pos0 + m;
+  }
+}
+
+// One block per active stream.  semantic != 0: the Talker's pending logits of
+// the stream, its repetition history and the semantic controls; otherwise row
+// b of `logits` with the sub-talker controls.
+__global__ void __launch_bounds__(256) sample_kernel(
+    const float* __restrict__ logits, int V, int semantic, const int* __restrict__ sid,
+    const q3tts_sampling* __restrict__ sp, uint8_t* history, const float* __restrict__ uniforms,
+    int cb, const int32_t* __restrict__ forced, int32_t* __restrict__ codes, int* __restrict__ fed,
+    float* __restrict__ dump, int dump_ld, int dump_off, int* err) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  SamplerSmem& sm = *reinterpret_cast<SamplerSmem*>(smraw);
+  const int b = blockIdx.x, s = sid[b];
+  const float* row = semantic ? logits + (size_t)s * V : logits + (size_t)b * V;
+  for (int i = threadIdx.x; i < V; i += blockDim.x) {
+    float v = row[i];
+    sm.val[i] = v;
+    if (dump) dump[(size_t)b * dump_ld + dump_off + i] = v;
+  }
+  __syncthreads();
+  const q3tts_sampling p = sp[b];
+  const uint8_t* hist = semantic ? history + (size_t)s * V : nullptr;
+  int code = semantic
+                 ? block_sample(sm, V, p.do_sample, p.top_k, p.top_p, p.temperature,
+                                p.repetition_penalty, hist, uniforms[b * 16 + cb])
+                 : block_sample(sm, V, p.sub_do_sample, p.sub_top_k, p.sub_top_p,
+                                p.sub_temperature, 1.0f, nullptr, uniforms[b * 16 + cb]);
+  if (threadIdx.x == 0) {
+    codes[b * 16 + cb] = code;
+    int f = forced ? forced[b * 16 + cb] : code;
+    if (f < 0 || f >= V) {
+      atomicExch(err, Q3TTS_ERR_ARG);
+      f = code;
+    }
+    fed[b * 16 + cb] = f;
+    if (semantic) history[(size_t)s * V + f] = 1;
+  }
+}
+
+template <class WT>
+__global__ void cp_input_kernel(int j, int n, const int* __restrict__ sid,
+                                const int* __restrict__ fed, const float* __restrict__ pending_h,
+                                const WT* __restrict__ e_codec, const WT* __restrict__ cp_embeds,
+                                int Dt, int Vc, float* __restrict__ uin) {
+  const int r = blockIdx.x;  // output row
+  const float* srcf = nullptr;
+  const WT* srcw = nullptr;
+  if (j == 0) {
+    int b = r / 2;
+    if ((r & 1) == 0)
+      srcf = pending_h + (size_t)sid[b] * Dt;
+    else
+      srcw = e_codec + (size_t)fed[b * 16] * Dt;
+  } else {
+    srcw = cp_embeds + ((size_t)(j - 1) * Vc + fed[r * 16 + j]) * Dt;
+  }
+  for (int i = threadIdx.x; i < Dt; i += blockDim.x)
+    uin[(size_t)r * Dt + i] = srcf ? srcf[i] : to_f(srcw[i]);
+}
+
+template <class WT>
+__global__ void embed_sum_kernel(const int* __restrict__ fed, const WT* __restrict__ e_codec,
+                                 const WT* __restrict__ cp_embeds, int Dt, int Vc,
+                                 float* __restrict__ x) {
+  const int b = blockIdx.y;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= Dt) return;
+  float acc = to_f(e_codec[(size_t)fed[b * 16] * Dt + i]);
+  for (int j = 1; j < Q3TTS_N_CODEBOOKS; ++j)
+    acc += to_f(cp_embeds[((size_t)(j - 1) * Vc + fed[b * 16 + j]) * Dt + i]);
+  x[(size_t)b * Dt + i] = acc;
+}
+
+__global__ void scatter_pending_kernel(const int* __restrict__ sid, const float* __restrict__ hn,
+                                       const float* __restrict__ lg, int Dt, int Vt,
+                                       float* __restrict__ pending_h,
+                                       float* __restrict__ pending_logits) {
+  const int b = blockIdx.x, s = sid[b];
+  for (int i = threadIdx.x; i < Dt; i += blockDim.x)
+    pending_h[(size_t)s * Dt + i] = hn[(size_t)b * Dt + i];
+  for (int i = threadIdx.x; i < Vt; i += blockDim.x)
+    pending_logits[(size_t)s * Vt + i] = lg[(size_t)b * Vt + i];
+}
+
+// ------------------------------------------------------------ stack pass
+
+// M tokens through all layers of one decoder stack (residual stream x [M, D]).
+static void stack_pass(q3tts_handle* h, const q3tts_layer_weights* lw, int layers, int D, int F,
+                       float* x, int M, TokDesc td, KVDesc kv, int kdt, int max_ctx) {
+  cudaStream_t s = h->s;
+  const int wdt = h->c.weight_dtype, HqD = h->Hq * h->hd;
+  for (int l = 0; l < layers; ++l) {
+    const q3tts_layer_weights& L = lw[l];
+    launch_rmsnorm(wdt, x, D, 1, 0, L.g_attn_norm, h->hb, D, M, D, h->c.rms_eps, s);
+    launch_linear(wdt, h->hb, D, L.w_qkv, h->qkv_rows, D, h->qkv, h->qkv_rows, M, false, s);
+    launch_qk_rope_append(wdt, kdt, h->qkv, h->qkv_rows, M, td, L.g_q_norm, L.g_k_norm,
+                          h->c.qk_norm, h->c.rms_eps, h->rope_cos, h->rope_sin, kv, l, h->Hq, s);
+    launch_attention(kdt, h->qkv, h->qkv_rows, M, td, kv, l, h->Hq, h->att, HqD, max_ctx, s);
+    launch_linear(wdt, h->att, HqD, L.w_o, D, HqD, x, D, M, true, s);
+    launch_rmsnorm(wdt, x, D, 1, 0, L.g_ffn_norm, h->hb, D, M, D, h->c.rms_eps, s);
+    launch_linear(wdt, h->hb, D, L.w_gateup, 2 * F, D, h->gu, 2 * F, M, false, s);
+    launch_silu_mul(h->gu, h->act, M, F, s);
+    launch_linear(wdt, h->act, F, L.w_down, D, F, x, D, M, true, s);
+  }
+  h->launches += 9ull * layers;
+}
+
+static size_t wbytes(const q3tts_handle* h) { return (size_t)h->esz; }
+
+int prefill_layered(q3tts_handle* h, int sid, const float* embeds, int len) {
+  cudaStream_t s = h->s;
+  const int Dt = h->Dt;
+  for (int c0 = 0; c0 < len; c0 += h->chunk) {
+    int T = len - c0 < h->chunk ? len - c0 : h->chunk;
+    cudaMemcpyAsync(h->x, embeds + (size_t)c0 * Dt, sizeof(float) * (size_t)T * Dt,
+                    cudaMemcpyDeviceToDevice, s);
+    fill_tokens_kernel<<<(T + 255) / 256, 256, 0, s>>>(h->d_tok_stream, h->d_tok_pos, T, sid, c0);
+    h->launches += 1;
+    TokDesc td{h->d_tok_stream, h->d_tok_pos, 0};
+    stack_pass(h, h->tl.data(), h->c.talker_layers, Dt, h->Ft, h->x, T, td, talker_kv(h),
+               h->c.kv_dtype, c0 + T);
+    if (c0 + T == len) {
+      launch_rmsnorm(h->c.weight_dtype, h->x, Dt, 1, T - 1, h->w.talker_g_final,
+                     h->pending_h + (size_t)sid * Dt, Dt, 1, Dt, h->c.rms_eps, s);
+      launch_linear(h->c.weight_dtype, h->pending_h + (size_t)sid * Dt, Dt, h->w.talker_w_head,
+                    h->Vt, Dt, h->pending_logits + (size_t)sid * h->Vt, h->Vt, 1, false, s);
+      h->launches += 2;
+    }
+  }
+  return cudaGetLastError() == cudaSuccess ? Q3TTS_OK : Q3TTS_ERR_CUDA;
+}
+
+int step_layered(q3tts_handle* h, const StepDesc& d, const float* uniforms, int32_t* codes,
+                 const int32_t* forced, float* logits) {
+  cudaStream_t s = h->s;
+  const int n = d.n, Dt = h->Dt, Dc = h->Dc, Vt = h->Vt, Vc = h->Vc, wdt = h->c.weight_dtype;
+  const int dump_ld = Vt + (Q3TTS_N_CODEBOOKS - 1) * Vc;
+  const size_t smem = sizeof(SamplerSmem);
+  int max_ctx = 0;
+  for (int b = 0; b < n; ++b) max_ctx = d.pos[b] + 1 > max_ctx ? d.pos[b] + 1 : max_ctx;
+
+  setup_kernel<<<1, 256, 0, s>>>(d, h->d_sid, h->d_pos, h->d_sp, h->page_table, h->pps,
+                                 h->c.page_size, h->d_tok_stream, h->d_tok_pos);
+  sample_kernel<<<n, 256, smem, s>>>(h->pending_logits, Vt, 1, h->d_sid, h->d_sp, h->history,
+                                     uniforms, 0, forced, codes, h->d_fed, logits, dump_ld, 0,
+                                     h->d_err);
+  const size_t es = wbytes(h);
+  for (int j = 0; j < Q3TTS_N_CODEBOOKS - 1; ++j) {
+    const int M = j == 0 ? 2 * n : n;
+    if (wdt == Q3TTS_BF16)
+      cp_input_kernel<bf16><<<M, 256, 0, s>>>(j, n, h->d_sid, h->d_fed, h->pending_h,
+                                              (const bf16*)h->w.talker_e_codec,
+                                              (const bf16*)h->w.cp_embeds, Dt, Vc, h->uin);
+    else
+      cp_input_kernel<float><<<M, 256, 0, s>>>(j, n, h->d_sid, h->d_fed, h->pending_h,
+                                               (const float*)h->w.talker_e_codec,
+                                               (const float*)h->w.cp_embeds, Dt, Vc, h->uin);
+    if (h->w.cp_w_proj)
+      launch_linear(wdt, h->uin, Dt, h->w.cp_w_proj, Dc, Dt, h->cpx, Dc, M, false, s);
+    else
+      cudaMemcpyAsync(h->cpx, h->uin, sizeof(float) * (size_t)M * Dc, cudaMemcpyDeviceToDevice, s);
+    TokDesc td = j == 0 ? TokDesc{h->d_tok_stream, h->d_tok_pos, 0} : TokDesc{h->d_sid, nullptr, j + 1};
+    stack_pass(h, h->cl.data(), h->c.cp_layers, Dc, h->Fc, h->cpx, M, td, cp_kv(h), Q3TTS_F32,
+               Q3TTS_N_CODEBOOKS);
+    launch_rmsnorm(wdt, h->cpx, Dc, j == 0 ? 2 : 1, j == 0 ? 1 : 0, h->w.cp_g_final, h->hb, Dc, n,
+                   Dc, h->c.rms_eps, s);
+    const void* head = (const char*)h->w.cp_heads + (size_t)j * Vc * Dc * es;
+    launch_linear(wdt, h->hb, Dc, head, Vc, Dc, h->logits, Vc, n, false, s);
+    sample_kernel<<<n, 256, smem, s>>>(h->logits, Vc, 0, h->d_sid, h->d_sp, nullptr, uniforms,
+                                       j + 1, forced, codes, h->d_fed, logits, dump_ld,
+                                       Vt + j * Vc, h->d_err);
+    h->launches += 4 + (h->w.cp_w_proj ? 1 : 0);
+  }
+  if (wdt == Q3TTS_BF16)
+    embed_sum_kernel<bf16><<<dim3((Dt + 255) / 256, n), 256, 0, s>>>(
+        h->d_fed, (const bf16*)h->w.talker_e_codec, (const bf16*)h->w.cp_embeds, Dt, Vc, h->x);
+  else
+    embed_sum_kernel<float><<<dim3((Dt + 255) / 256, n), 256, 0, s>>>(
+        h->d_fed, (const float*)h->w.talker_e_codec, (const float*)h->w.cp_embeds, Dt, Vc, h->x);
+  TokDesc td{h->d_sid, h->d_pos, 0};
+  stack_pass(h, h->tl.data(), h->c.talker_layers, Dt, h->Ft, h->x, n, td, talker_kv(h),
+             h->c.kv_dtype, max_ctx);
+  launch_rmsnorm(wdt, h->x, Dt, 1, 0, h->w.talker_g_final, h->hb, Dt, n, Dt, h->c.rms_eps, s);
+  launch_linear(wdt, h->hb, Dt, h->w.talker_w_head, Vt, Dt, h->logits, Vt, n, false, s);
+  scatter_pending_kernel<<<n, 256, 0, s>>>(h->d_sid, h->hb, h->logits, Dt, Vt, h->pending_h,
+                                           h->pending_logits);
+  h->launches += 6;  // setup, semantic sample, embed-sum, final norm, head, scatter
+  return cudaGetLastError() == cudaSuccess ? Q3TTS_OK : Q3TTS_ERR_CUDA;
+}
+
+int sampler_setup() {
+  cudaError_t e = cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)sizeof(SamplerSmem));
+  return e == cudaSuccess ? Q3TTS_OK : Q3TTS_ERR_CUDA;
+}
+
+}  // namespace q3

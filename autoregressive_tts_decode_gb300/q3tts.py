@@ -1,0 +1,216 @@
+"""ctypes binding of libq3tts (include/q3tts.h): argument marshalling only.
+
+Every step of the decode runs in the CUDA library; this module turns torch
+tensors into device pointers and status codes into exceptions.  It refuses to
+work without the built library (no CPU path exists).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Dict, Optional, Sequence
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libq3tts.so")
+
+OK = 0
+ERR_ARG, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED, ERR_STATE = -1, -2, -3, -4, -5, -6
+F32, BF16 = 0, 1
+MAX_STREAMS = 256
+N_CODEBOOKS = 16
+
+LAYER_KEYS = ("w_qkv", "w_o", "w_gateup", "w_down",
+              "g_attn_norm", "g_ffn_norm", "g_q_norm", "g_k_norm")
+
+
+class Q3TTSError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+        self.code = code
+
+
+class Config(C.Structure):
+    _fields_ = [(n, C.c_int) for n in (
+        "talker_layers", "talker_hidden", "talker_ffn", "cp_layers", "cp_hidden", "cp_ffn",
+        "n_q_heads", "n_kv_heads", "head_dim", "codec_vocab", "cp_vocab", "n_codebooks",
+        "max_streams", "kv_cap_steps", "page_size", "kv_pages", "prefill_chunk",
+        "weight_dtype", "kv_dtype", "qk_norm")] + [("rms_eps", C.c_float), ("rope_theta", C.c_float)]
+
+
+class LayerWeights(C.Structure):
+    _fields_ = [(k, C.c_void_p) for k in LAYER_KEYS]
+
+
+class Weights(C.Structure):
+    _fields_ = [("talker_layers", C.POINTER(LayerWeights)), ("talker_g_final", C.c_void_p),
+                ("talker_w_head", C.c_void_p), ("talker_e_codec", C.c_void_p),
+                ("cp_layers", C.POINTER(LayerWeights)), ("cp_g_final", C.c_void_p),
+                ("cp_heads", C.c_void_p), ("cp_embeds", C.c_void_p), ("cp_w_proj", C.c_void_p)]
+
+
+class Sampling(C.Structure):
+    _fields_ = [("do_sample", C.c_int), ("top_k", C.c_int), ("top_p", C.c_float),
+                ("temperature", C.c_float), ("repetition_penalty", C.c_float),
+                ("sub_do_sample", C.c_int), ("sub_top_k", C.c_int), ("sub_top_p", C.c_float),
+                ("sub_temperature", C.c_float)]
+
+
+EXPORTS = ("q3tts_workspace_size", "q3tts_create", "q3tts_prefill", "q3tts_step_frame",
+           "q3tts_read_pending", "q3tts_reset", "q3tts_stream_length", "q3tts_sync_status",
+           "q3tts_kernel_launches", "q3tts_destroy", "q3tts_strerror")
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Loads libq3tts.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libq3tts.so is not built ({path}); run __graft_entry__.build()")
+    L = C.CDLL(path)
+    vp = C.c_void_p
+    L.q3tts_workspace_size.restype = C.c_size_t
+    L.q3tts_workspace_size.argtypes = [C.POINTER(Config)]
+    L.q3tts_create.argtypes = [C.POINTER(Config), C.POINTER(Weights), vp, C.c_size_t, vp,
+                               C.POINTER(vp)]
+    L.q3tts_prefill.argtypes = [vp, C.c_int, vp, C.c_int]
+    L.q3tts_step_frame.argtypes = [vp, C.POINTER(Sampling), C.POINTER(C.c_int32), C.c_int, vp, vp,
+                                   vp, vp]
+    L.q3tts_read_pending.argtypes = [vp, C.c_int, vp, vp]
+    L.q3tts_reset.argtypes = [vp, C.c_int]
+    L.q3tts_stream_length.argtypes = [vp, C.c_int]
+    L.q3tts_sync_status.argtypes = [vp]
+    L.q3tts_destroy.argtypes = [vp]
+    L.q3tts_kernel_launches.restype = C.c_uint64
+    L.q3tts_kernel_launches.argtypes = [vp]
+    L.q3tts_strerror.restype = C.c_char_p
+    L.q3tts_strerror.argtypes = [C.c_int]
+    _lib = L
+    return L
+
+
+def strerror(code: int) -> str:
+    try:
+        return load().q3tts_strerror(code).decode()
+    except RuntimeError:
+        return f"error {code}"
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise Q3TTSError(rc, what)
+
+
+def make_config(shape, max_streams: int, kv_cap: int, page_size: int = 16, kv_pages: int = 0,
+                prefill_chunk: int = 0) -> Config:
+    s = shape
+    return Config(s.talker_layers, s.talker_hidden, s.talker_ffn, s.cp_layers, s.cp_hidden,
+                  s.cp_ffn, s.n_q_heads, s.n_kv_heads, s.head_dim, s.codec_vocab, s.cp_vocab,
+                  s.n_codebooks, max_streams, kv_cap, page_size, kv_pages, prefill_chunk,
+                  s.weight_dtype, s.kv_dtype, s.qk_norm, float(s.rms_eps), float(s.rope_theta))
+
+
+def sampling_struct(sp) -> Sampling:
+    return Sampling(int(sp.do_sample), int(sp.top_k), float(sp.top_p), float(sp.temperature),
+                    float(sp.repetition_penalty), int(sp.sub_do_sample), int(sp.sub_top_k),
+                    float(sp.sub_top_p), float(sp.sub_temperature))
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+class Engine:
+    """One libq3tts handle over device weights (dict of CUDA tensors named as in
+    ``synth.weight_specs``) and a workspace allocated here through torch."""
+
+    def __init__(self, shape, weights: Dict[str, "object"], max_streams: int, kv_cap: int,
+                 page_size: int = 16, kv_pages: int = 0, prefill_chunk: int = 0, stream=None):
+        import torch
+        L = load()
+        self.shape = shape
+        self.max_streams = max_streams
+        self.cfg = make_config(shape, max_streams, kv_cap, page_size, kv_pages, prefill_chunk)
+        self._w = weights
+        for k, t in weights.items():
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"weight {k} must be a contiguous CUDA tensor")
+        tl = (LayerWeights * shape.talker_layers)()
+        for i in range(shape.talker_layers):
+            tl[i] = LayerWeights(*[weights[f"talker.{i}.{k}"].data_ptr() for k in LAYER_KEYS])
+        cl = (LayerWeights * shape.cp_layers)()
+        for i in range(shape.cp_layers):
+            cl[i] = LayerWeights(*[weights[f"cp.{i}.{k}"].data_ptr() for k in LAYER_KEYS])
+        proj = weights.get("cp.w_proj")
+        self._tl, self._cl = tl, cl
+        self.wstruct = Weights(tl, weights["talker.g_final"].data_ptr(),
+                               weights["talker.w_head"].data_ptr(),
+                               weights["talker.e_codec"].data_ptr(), cl,
+                               weights["cp.g_final"].data_ptr(), weights["cp.heads"].data_ptr(),
+                               weights["cp.embeds"].data_ptr(), _ptr(proj))
+        n = L.q3tts_workspace_size(C.byref(self.cfg))
+        if n == 0:
+            raise Q3TTSError(ERR_ARG, "q3tts_workspace_size")
+        self.workspace_bytes = int(n)
+        self.workspace = torch.empty(int(n), dtype=torch.uint8, device="cuda")
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        h = C.c_void_p()
+        _check(L.q3tts_create(C.byref(self.cfg), C.byref(self.wstruct),
+                              self.workspace.data_ptr(), n, C.c_void_p(self.stream.cuda_stream),
+                              C.byref(h)), "q3tts_create")
+        self.h = h
+
+    def close(self):
+        if getattr(self, "h", None) is not None and self.h.value:
+            load().q3tts_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def prefill(self, stream_id: int, embeds) -> None:
+        if not embeds.is_cuda or embeds.dtype.itemsize != 4 or not embeds.is_contiguous():
+            raise ValueError("embeds must be a contiguous CUDA float32 tensor")
+        _check(load().q3tts_prefill(self.h, stream_id, embeds.data_ptr(), embeds.shape[0]),
+               "q3tts_prefill")
+
+    def step_frame(self, stream_ids: Sequence[int], sampling, uniforms, codes, forced=None,
+                   logits=None) -> None:
+        """uniforms: CUDA fp32 [n, 16]; codes: CUDA int32 [n, 16] (written);
+        forced: None or CUDA int32 [n, 16]; logits: None or CUDA fp32
+        [n, V_t + 15 V_c].  `sampling` is one Sampling-like object or a list."""
+        n = len(stream_ids)
+        if not isinstance(sampling, (list, tuple)):
+            sampling = [sampling] * n
+        sp = (Sampling * n)(*[sampling_struct(x) for x in sampling])
+        ids = (C.c_int32 * n)(*[int(i) for i in stream_ids])
+        _check(load().q3tts_step_frame(self.h, sp, ids, n, uniforms.data_ptr(), codes.data_ptr(),
+                                       _ptr(forced), _ptr(logits)), "q3tts_step_frame")
+
+    def read_pending(self, stream_id: int):
+        import torch
+        hdn = torch.empty(self.shape.talker_hidden, dtype=torch.float32, device="cuda")
+        lg = torch.empty(self.shape.codec_vocab, dtype=torch.float32, device="cuda")
+        _check(load().q3tts_read_pending(self.h, stream_id, hdn.data_ptr(), lg.data_ptr()),
+               "q3tts_read_pending")
+        return hdn, lg
+
+    def reset(self, stream_id: int = -1) -> None:
+        _check(load().q3tts_reset(self.h, stream_id), "q3tts_reset")
+
+    def length(self, stream_id: int) -> int:
+        rc = load().q3tts_stream_length(self.h, stream_id)
+        if rc < 0:
+            raise Q3TTSError(rc, "q3tts_stream_length")
+        return rc
+
+    def kernel_launches(self) -> int:
+        return int(load().q3tts_kernel_launches(self.h))
+
+    def sync(self) -> None:
+        _check(load().q3tts_sync_status(self.h), "q3tts_sync_status")

@@ -122,14 +122,18 @@ TINY_SHAPE = ModelShape(talker_layers=2, talker_hidden=256, talker_ffn=768, cp_l
                         cp_hidden=256, cp_ffn=768, n_q_heads=4, n_kv_heads=2, head_dim=64,
                         codec_vocab=3072, cp_vocab=2048, weight_dtype=DTYPE_F32,
                         kv_dtype=DTYPE_F32)
+# The batch-1 and batched-16 workloads fix bf16 for the weights only; their
+# Talker KV cache stays fp32 (bf16 KV moves 1.7B logits by ~0.036 against the
+# fp64 oracle, over the 3e-2 tolerance).  The serving workload fixes bf16 KV.
 SHAPE_06B = ModelShape(talker_layers=28, talker_hidden=1024, talker_ffn=3072, cp_layers=5,
                        cp_hidden=1024, cp_ffn=3072, n_q_heads=16, n_kv_heads=8, head_dim=128,
                        codec_vocab=3072, cp_vocab=2048, weight_dtype=DTYPE_BF16,
-                       kv_dtype=DTYPE_BF16)
+                       kv_dtype=DTYPE_F32)
 SHAPE_17B = ModelShape(talker_layers=28, talker_hidden=2048, talker_ffn=6144, cp_layers=5,
                        cp_hidden=1024, cp_ffn=3072, n_q_heads=16, n_kv_heads=8, head_dim=128,
                        codec_vocab=3072, cp_vocab=2048, weight_dtype=DTYPE_BF16,
-                       kv_dtype=DTYPE_BF16)
+                       kv_dtype=DTYPE_F32)
+SHAPE_17B_KV16 = dataclasses.replace(SHAPE_17B, kv_dtype=DTYPE_BF16)
 
 WORKLOADS: Dict[str, Workload] = {
     "tiny": Workload("tiny", TINY_SHAPE, streams=1, frames=8, kv_cap=64, page_size=16,
@@ -141,7 +145,7 @@ WORKLOADS: Dict[str, Workload] = {
     "batched16": Workload("batched16", SHAPE_17B, streams=16, frames=240, kv_cap=512,
                           page_size=16, sampling=QWEN_DEFAULT_SAMPLING,
                           prompt_len_range=(32, 256)),
-    "serving128": Workload("serving128", SHAPE_17B, streams=128, frames=64, kv_cap=2112,
+    "serving128": Workload("serving128", SHAPE_17B_KV16, streams=128, frames=64, kv_cap=2112,
                            page_size=16, sampling=GREEDY, prompt_len_range=(256, 2048)),
 }
 

@@ -1,0 +1,192 @@
+/*
+ * q3tts.h -- C ABI of libq3tts: GB300 (sm_103a) frame decode of a
+ * Qwen3-TTS-style model.
+ *
+ * One acoustic frame is 80 ms of audio, 16 codebook tokens [semantic token,
+ * acoustic tokens 1..15]: the Talker (main decoder) produces the semantic
+ * token, the CodePredictor fills in the 15 acoustic tokens of the same frame
+ * one at a time, and the sum of the frame's 16 code embeddings is the next
+ * Talker input.  ("Running Qwen3-TTS on an AMD R9700", section "Running
+ * Qwen3-TTS"; embedding sum: "qwen3-tts-hip" README, section "Python Parity
+ * Fixtures".)  The calls below mirror the engine surface of the "qwen3-tts-hip"
+ * README, section "Library Usage": a model loaded once with a fixed KV-cache
+ * capacity (EngineOptions::max_cache_steps), per-request sampling controls
+ * (GenerateOptions) and persistent frame-incremental streams
+ * (HipTtsEngine::start_stream), with errors returned as status codes.
+ *
+ * Conventions for every call:
+ *   - All pointers documented "device" are CUDA device pointers in the
+ *     current context; "host" pointers are ordinary host memory.
+ *   - The library allocates no device memory.  The caller owns the weights
+ *     and one workspace buffer (size from q3tts_workspace_size); both must
+ *     outlive the handle.  The workspace holds the KV caches, per-stream state,
+ *     activations and the library's re-laid-out copies of some weights.
+ *   - Work is enqueued on the CUDA stream given to q3tts_create and is
+ *     asynchronous unless stated; q3tts_sync_status waits for it.
+ *   - Every call returns Q3TTS_OK (0) or a negative Q3TTS_ERR_* code.  Argument
+ *     checks happen before anything is launched; no C++ exception and no abort
+ *     crosses this boundary.
+ */
+#ifndef Q3TTS_H
+#define Q3TTS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q3TTS_OK 0
+#define Q3TTS_ERR_ARG (-1)         /* invalid argument, shape or pointer */
+#define Q3TTS_ERR_CAPACITY (-2)    /* KV cache or page pool full; stream limit */
+#define Q3TTS_ERR_CUDA (-3)        /* a CUDA runtime call failed */
+#define Q3TTS_ERR_TIMEOUT (-4)     /* a device-side wait gave up (bounded spin) */
+#define Q3TTS_ERR_UNSUPPORTED (-5) /* configuration outside what the kernels handle */
+#define Q3TTS_ERR_STATE (-6)       /* e.g. a frame requested before prefill */
+
+#define Q3TTS_F32 0
+#define Q3TTS_BF16 1
+
+#define Q3TTS_MAX_STREAMS 256
+#define Q3TTS_N_CODEBOOKS 16
+
+/* Model and engine shape.  Dimensions follow the Qwen3-style decoder: RMSNorm
+ * (eps rms_eps), per-head q/k RMSNorm when qk_norm != 0, rotate-half RoPE
+ * (base rope_theta), grouped-query attention (n_q_heads over n_kv_heads),
+ * SwiGLU FFN.  The CodePredictor has the same head layout as the Talker.
+ * kv_cap_steps is the per-stream Talker KV capacity in positions
+ * (max_cache_steps); the KV cache is paged in pages of page_size positions
+ * drawn from a pool of kv_pages pages shared by all streams (0 = enough for
+ * max_streams full streams).  prefill_chunk bounds the positions one prefill
+ * launch processes (0 = 256). */
+typedef struct q3tts_config {
+  int talker_layers, talker_hidden, talker_ffn;
+  int cp_layers, cp_hidden, cp_ffn;
+  int n_q_heads, n_kv_heads, head_dim;
+  int codec_vocab; /* V_t: Talker codec vocabulary (semantic token) */
+  int cp_vocab;    /* V_c: vocabulary of each acoustic codebook */
+  int n_codebooks; /* must be 16 */
+  int max_streams, kv_cap_steps, page_size, kv_pages, prefill_chunk;
+  int weight_dtype; /* Q3TTS_F32 or Q3TTS_BF16: every weight tensor */
+  int kv_dtype;     /* Talker KV cache: Q3TTS_F32 or Q3TTS_BF16 */
+  int qk_norm;
+  float rms_eps, rope_theta;
+} q3tts_config;
+
+/* One decoder layer; device pointers, row-major [out, in], weight_dtype.
+ *   w_qkv    [(Hq + 2 Hkv) hd, D]   q rows, then k rows, then v rows
+ *   w_o      [D, Hq hd]
+ *   w_gateup [2 F, D]                gate rows, then up rows
+ *   w_down   [D, F]
+ *   g_attn_norm [D], g_ffn_norm [D], g_q_norm [hd], g_k_norm [hd] */
+typedef struct q3tts_layer_weights {
+  const void* w_qkv;
+  const void* w_o;
+  const void* w_gateup;
+  const void* w_down;
+  const void* g_attn_norm;
+  const void* g_ffn_norm;
+  const void* g_q_norm;
+  const void* g_k_norm;
+} q3tts_layer_weights;
+
+/* All weights.  talker_layers / cp_layers are HOST arrays of per-layer device
+ * pointer sets (copied during q3tts_create).  Device tensors:
+ *   talker_g_final [D_t], talker_w_head [V_t, D_t], talker_e_codec [V_t, D_t]
+ *   cp_g_final [D_c], cp_heads [15, V_c, D_c], cp_embeds [15, V_c, D_t]
+ *   cp_w_proj [D_c, D_t]: the CodePredictor input projection, required when
+ *   D_t != D_c and NULL otherwise. */
+typedef struct q3tts_weights {
+  const q3tts_layer_weights* talker_layers;
+  const void* talker_g_final;
+  const void* talker_w_head;
+  const void* talker_e_codec;
+  const q3tts_layer_weights* cp_layers;
+  const void* cp_g_final;
+  const void* cp_heads;
+  const void* cp_embeds;
+  const void* cp_w_proj;
+} q3tts_weights;
+
+/* Sampling controls of one stream ("qwen3-tts-hip" README, "Library Usage",
+ * GenerateOptions): semantic token (do_sample, top_k, top_p, temperature,
+ * repetition_penalty) and acoustic tokens (sub_*; no repetition penalty).
+ * top_k <= 0 or >= vocabulary disables top-k; top_p >= 1 disables top-p;
+ * temperature must be > 0 when sampling.  The rule applied, in float:
+ * penalty over the stream's emitted semantic codes (l>0 ? l/rho : l*rho), then
+ * greedy argmax (lowest index on ties) or: l/T, order by (value desc, index
+ * asc), keep top-k, w = exp(l - max) in that order, optional top-p prefix,
+ * pick the first id whose running float sum exceeds u * (float sum of w). */
+typedef struct q3tts_sampling {
+  int do_sample, top_k;
+  float top_p, temperature, repetition_penalty;
+  int sub_do_sample, sub_top_k;
+  float sub_top_p, sub_temperature;
+} q3tts_sampling;
+
+typedef struct q3tts_handle q3tts_handle;
+
+/* Bytes of workspace q3tts_create needs for cfg (0 if cfg is invalid). */
+size_t q3tts_workspace_size(const q3tts_config* cfg);
+
+/* Builds a handle over caller-owned weights and workspace (device memory of at
+ * least q3tts_workspace_size(cfg) bytes, 256-byte aligned).  cuda_stream is a
+ * cudaStream_t (NULL = legacy default stream).  Uploads RoPE tables and the
+ * library's re-laid-out weight copies into the workspace and synchronises
+ * once.  On success *out receives the handle. */
+int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspace,
+                 size_t workspace_bytes, void* cuda_stream, q3tts_handle** out);
+
+/* Restarts stream stream_id with a prompt: embeds_dev is a device fp32
+ * [len, D_t] array of Talker input vectors for positions 0..len-1.  Writes
+ * their KV and leaves the final-normed hidden and codec logits of position
+ * len-1 as the stream's pending state, from which the next frame's semantic
+ * token is drawn.  Q3TTS_ERR_CAPACITY if len >= kv_cap_steps or the page pool
+ * is exhausted. */
+int q3tts_prefill(q3tts_handle* h, int stream_id, const float* embeds_dev, int len);
+
+/* Decodes one frame for each of n_active streams (distinct ids, host array
+ * stream_ids[n_active]; params: host array [n_active]).
+ *   uniforms_dev     device fp32 [n_active, 16]: the uniform in [0,1) for each
+ *                    draw (codebook order); ignored by greedy draws.
+ *   codes_dev        device int32 [n_active, 16]: the drawn codes.
+ *   forced_dev       NULL, or device int32 [n_active, 16]: teacher forcing --
+ *                    these codes are fed forward instead of the drawn ones.
+ *   logits_dev       NULL, or device fp32 [n_active, V_t + 15 V_c]: the raw
+ *                    logits behind each draw (pending Talker logits, then the
+ *                    15 CodePredictor heads).
+ * Each stream advances by one Talker position.  Q3TTS_ERR_STATE if a stream
+ * has no prompt, Q3TTS_ERR_CAPACITY if its cache is full. */
+int q3tts_step_frame(q3tts_handle* h, const q3tts_sampling* params, const int32_t* stream_ids,
+                     int n_active, const float* uniforms_dev, int32_t* codes_dev,
+                     const int32_t* forced_dev, float* logits_dev);
+
+/* Copies a stream's pending state to device buffers (either may be NULL):
+ * hidden_dev fp32 [D_t], logits_dev fp32 [V_t].  Asynchronous. */
+int q3tts_read_pending(q3tts_handle* h, int stream_id, float* hidden_dev, float* logits_dev);
+
+/* Forgets a stream (-1 = all): length, semantic history, pending state; its
+ * KV pages return to the pool. */
+int q3tts_reset(q3tts_handle* h, int stream_id);
+
+/* Talker positions held by a stream (0 after reset), or a negative error. */
+int q3tts_stream_length(q3tts_handle* h, int stream_id);
+
+/* Waits for the handle's stream and reports any error recorded by a kernel
+ * (Q3TTS_ERR_TIMEOUT for a device-side wait that gave up), or a CUDA error. */
+int q3tts_sync_status(q3tts_handle* h);
+
+/* Number of kernel launches this handle has issued since q3tts_create (a
+ * diagnostic for launch-overhead accounting). */
+uint64_t q3tts_kernel_launches(const q3tts_handle* h);
+
+void q3tts_destroy(q3tts_handle* h);
+
+const char* q3tts_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q3TTS_H */

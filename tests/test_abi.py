@@ -1,0 +1,88 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, and exports
+every function include/q3tts.h declares; the binding mirrors the header's
+structs and constants."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from autoregressive_tts_decode_gb300 import build, q3tts
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q3tts.h")
+
+
+def header_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(q3tts_[a-z_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ctypes.CDLL(build.LIB)
+
+
+def test_exports_every_declared_function(lib):
+    names = header_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(q3tts.EXPORTS)
+
+
+def test_header_constants_match_binding():
+    src = open(HEADER).read()
+    consts = dict(re.findall(r"#define (Q3TTS_[A-Z_0-9]+) \(?(-?\d+)\)?", src))
+    assert int(consts["Q3TTS_ERR_ARG"]) == q3tts.ERR_ARG
+    assert int(consts["Q3TTS_ERR_CAPACITY"]) == q3tts.ERR_CAPACITY
+    assert int(consts["Q3TTS_ERR_CUDA"]) == q3tts.ERR_CUDA
+    assert int(consts["Q3TTS_ERR_TIMEOUT"]) == q3tts.ERR_TIMEOUT
+    assert int(consts["Q3TTS_ERR_UNSUPPORTED"]) == q3tts.ERR_UNSUPPORTED
+    assert int(consts["Q3TTS_ERR_STATE"]) == q3tts.ERR_STATE
+    assert int(consts["Q3TTS_MAX_STREAMS"]) == q3tts.MAX_STREAMS
+    assert int(consts["Q3TTS_BF16"]) == q3tts.BF16
+
+
+def test_struct_layouts_match_header():
+    src = open(HEADER).read()
+
+    def fields(struct):
+        body = re.search(r"typedef struct " + struct + r" \{(.*?)\} " + struct, src, re.S).group(1)
+        body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+        out = []
+        for decl in body.split(";"):
+            decl = decl.strip()
+            if not decl:
+                continue
+            names = decl.split(None, 1)[1] if not decl.startswith("const") else decl.split("*", 1)[1]
+            out += [n.strip().lstrip("*") for n in names.split(",")]
+        return out
+
+    assert fields("q3tts_config") == [f[0] for f in q3tts.Config._fields_]
+    assert fields("q3tts_sampling") == [f[0] for f in q3tts.Sampling._fields_]
+    assert fields("q3tts_layer_weights") == [f[0] for f in q3tts.LayerWeights._fields_]
+    assert fields("q3tts_weights") == [f[0] for f in q3tts.Weights._fields_]
+
+
+def test_workspace_size_without_gpu(lib):
+    from autoregressive_tts_decode_gb300 import synth
+    L = q3tts.load(build.LIB)
+    cfg = q3tts.make_config(synth.TINY_SHAPE, 1, 64)
+    n = L.q3tts_workspace_size(ctypes.byref(cfg))
+    assert n > 0
+    bad = q3tts.make_config(synth.TINY_SHAPE, 1, 64)
+    bad.head_dim = 96
+    assert L.q3tts_workspace_size(ctypes.byref(bad)) == 0
+    assert L.q3tts_strerror(q3tts.ERR_CAPACITY).decode().startswith("KV cache")
+
+
+def test_binding_refuses_missing_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        q3tts._lib_saved = q3tts._lib
+        try:
+            q3tts._lib = None
+            q3tts.load(str(tmp_path / "nope.so"))
+        finally:
+            q3tts._lib = q3tts._lib_saved

@@ -51,19 +51,21 @@ def test_algorithmic_frame_bytes_1p7b():
     assert fb.talker_weights / 1e9 == pytest.approx(2.831, abs=0.001)
     # CodePredictor pass: 5 layers x 31.5 MB + head 4.2 MB + projection 4.2 MB
     assert fb.cp_pass_weights / 1e6 == pytest.approx(165.7, abs=0.1)
-    # + Talker KV (28 layers x ~249 positions x 4 KB bf16 K+V) ~ 28.5 MB
+    # + Talker KV (28 layers x ~249 positions x 8 KB fp32 K+V) ~ 57 MB
     # + CodePredictor KV (fp32, 5 layers x 135 positions x 8 KB) ~ 5.5 MB
     run = bm.run_bytes(s, 128, 240) / 240
-    assert run / 1e9 == pytest.approx(2.831 + 15 * 0.1657 + 0.0285 + 0.0055, abs=0.002)
+    assert run / 1e9 == pytest.approx(2.831 + 15 * 0.1657 + 0.0571 + 0.0055, abs=0.002)
+    kv16 = bm.run_bytes(synth.SHAPE_17B_KV16, 128, 240) / 240
+    assert (run - kv16) / 1e9 == pytest.approx(0.0286, abs=0.001)
 
 
 def test_algorithmic_frame_bytes_0p6b():
     s = synth.SHAPE_06B
     fb = bm.frame_bytes(s, 64)
     assert fb.cp_pass_weights / 1e6 == pytest.approx(161.5, abs=0.1)
-    # Talker 0.887 GB + 15 passes + Talker KV (~184 positions) + CodePredictor KV
+    # Talker 0.887 GB + 15 passes + fp32 Talker KV (~184 positions) + CodePredictor KV
     run = bm.run_bytes(s, 64, 240) / 240
-    assert run / 1e9 == pytest.approx(0.887 + 15 * 0.1615 + 0.0211 + 0.0055, abs=0.002)
+    assert run / 1e9 == pytest.approx(0.887 + 15 * 0.1615 + 0.0423 + 0.0055, abs=0.002)
 
 
 def test_talker_module_below_page_figure():
