@@ -2,6 +2,7 @@
 // checks, workspace layout, stream bookkeeping (lengths, KV pages, capacity),
 // and dispatch to the frame kernels.
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -14,7 +15,8 @@ namespace q3 {
 int sampler_setup();
 int frame_kernel_create(q3tts_handle* h);
 void frame_kernel_destroy(q3tts_handle* h);
-bool frame_kernel_supports(const q3tts_handle* h, int n_active);
+bool frame_kernel_supports(const q3tts_handle* h, int n_active, const q3tts_sampling* sp);
+int frame_kernel_recover(q3tts_handle* h);
 int frame_kernel_step(q3tts_handle* h, const StepDesc& d, const float* uniforms, int32_t* codes,
                       const int32_t* forced, float* logits);
 size_t frame_kernel_workspace(const q3tts_config& c, int n_sm);
@@ -190,7 +192,10 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
   h->Dt = d.Dt; h->Dc = d.Dc; h->Ft = d.Ft; h->Fc = d.Fc; h->Hq = d.Hq; h->Hkv = d.Hkv;
   h->hd = d.hd; h->Vt = d.Vt; h->Vc = d.Vc; h->qkv_rows = d.qkv_rows; h->pps = d.pps;
   h->n_pages = d.n_pages; h->chunk = d.chunk; h->m_max = d.m_max; h->esz = d.esz;
+  h->fk_base = (char*)workspace + carve(c, nullptr, nullptr);
   carve(c, workspace, h);
+  const char* env = getenv("Q3TTS_FRAME_KERNEL");
+  h->frame_kernel_off = env && env[0] == '0';
 
   // RoPE tables: angle pos * theta^(-2i/hd), computed in double, stored as float.
   const int half = d.hd / 2;
@@ -291,7 +296,7 @@ int q3tts_step_frame(q3tts_handle* h, const q3tts_sampling* params, const int32_
     }
   }
   int rc;
-  if (q3::frame_kernel_supports(h, n_active))
+  if (q3::frame_kernel_supports(h, n_active, d.sp))
     rc = q3::frame_kernel_step(h, d, uniforms_dev, codes_dev, forced_dev, logits_dev);
   else
     rc = q3::step_layered(h, d, uniforms_dev, codes_dev, forced_dev, logits_dev);
@@ -340,6 +345,8 @@ int q3tts_sync_status(q3tts_handle* h) {
     return Q3TTS_ERR_CUDA;
   if (e != 0) {
     cudaMemset(h->d_err, 0, sizeof(int));
+    q3::frame_kernel_recover(h);
+    cudaStreamSynchronize(h->s);
     return e;
   }
   return cudaGetLastError() == cudaSuccess ? Q3TTS_OK : Q3TTS_ERR_CUDA;

@@ -7,7 +7,7 @@
 #include <vector>
 
 #include "common.cuh"
-#include "../../include/q3tts.h"
+#include "q3tts.h"
 
 namespace q3 {
 
@@ -59,6 +59,8 @@ struct q3tts_handle {
   std::vector<int> free_pages;
 
   q3::FrameKernelState* fk;
+  char* fk_base;           // workspace region of the persistent frame kernel
+  bool frame_kernel_off;   // Q3TTS_FRAME_KERNEL=0: always use the layered step
   uint64_t launches = 0;
 };
 

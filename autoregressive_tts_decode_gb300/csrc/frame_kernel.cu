@@ -1,13 +1,1581 @@
-// frame_kernel.cu -- persistent whole-frame kernel (placeholder until built).
+// frame_kernel.cu -- one acoustic frame of one stream in a single persistent
+// launch.
+//
+// The frame ("Running Qwen3-TTS on an AMD R9700", section "Running Qwen3-TTS"):
+// draw the semantic token from the pending Talker logits, run 15 CodePredictor
+// passes (pass 0 over [Talker hidden, semantic embedding], pass j over the
+// embedding of acoustic token j; each ends in head j and a draw), sum the 16
+// code embeddings ("qwen3-tts-hip" README, "Python Parity Fixtures") and run
+// one Talker step whose final norm and codec head leave the next pending
+// logits.  The page's cost model -- bytes(Talker) + 15 bytes(CodePredictor)
+// per frame -- makes this a weight-streaming problem: at batch 1 every weight
+// byte is used by one multiply-add.
+//
+// Design (GB300, one CTA per SM, cooperative launch):
+//  * A producer warp walks the frame's weight schedule for its CTA -- the
+//    same row slices the consumers will need, in frame order -- and streams
+//    them through a 6-deep ring of 16 KB stages in shared memory with 1-D
+//    bulk TMA copies (cp.async.bulk + mbarrier transaction counts).  Weights do not
+//    depend on activations, so the stream runs ahead across the grid
+//    barriers that separate dependent phases and HBM stays busy.
+//  * Eight consumer warps run the phases: fused RMSNorm + GEMV on the staged
+//    rows; attention; a fused SwiGLU FFN that multiplies each CTA's gate/up
+//    rows and the matching rows of the transposed down projection and adds
+//    its partial result into the residual with float4 atomics (split-K over
+//    the FFN width, no extra phase); o_proj as a split over (head, output
+//    column) with the same atomic accumulation.  Draws are made redundantly
+//    by every CTA from the full logit vector, so a sampled code needs no
+//    extra barrier.
+//  * Residual bookkeeping: a layer's input is R + dA + dF (two alternating
+//    buffer sets); phase A folds it into the other set's R and zeroes that
+//    set's deltas, which phase B (attention) and phase C (FFN) accumulate.
+//  * Phases per layer: CodePredictor 3 (QKV | attention + o_proj | FFN) --
+//    its context is at most 16 positions, so every CTA recomputes the one or
+//    two heads it needs; Talker 4 (QKV | attention partials over position
+//    chunks | combine + o_proj | FFN).
+//  * Latency is the constraint of the short CodePredictor phases: every
+//    thread issues all of a step's global loads before using them (residual
+//    gathers, K/V rows, partial sums), draws are register-resident (per-warp
+//    radix histograms, a shuffle sort of the <= 64 candidates), and the grid
+//    barrier is a release-add / acquire-load counter.
+//  * Every wait (ring slots, grid barrier) is bounded; on expiry the kernel
+//    records Q3TTS_ERR_TIMEOUT, raises an abort flag, stops waiting, lets
+//    in-flight copies land and returns.
+#include <algorithm>
+#include <new>
+#include <vector>
+
 #include "engine.cuh"
+#include "sampler.cuh"
 
 namespace q3 {
-size_t frame_kernel_workspace(const q3tts_config&, int) { return 0; }
-int frame_kernel_create(q3tts_handle*) { return Q3TTS_OK; }
-void frame_kernel_destroy(q3tts_handle*) {}
-bool frame_kernel_supports(const q3tts_handle*, int) { return false; }
-int frame_kernel_step(q3tts_handle*, const StepDesc&, const float*, int32_t*, const int32_t*,
-                      float*) {
-  return Q3TTS_ERR_UNSUPPORTED;
+
+constexpr int FK_CONSUMER_WARPS = 8;
+constexpr int FK_CONSUMERS = FK_CONSUMER_WARPS * 32;
+constexpr int FK_PRODUCER_THREADS = 32;  // one warp; one thread issues the copies
+constexpr int FK_THREADS = FK_PRODUCER_THREADS + FK_CONSUMERS;
+constexpr int FK_STAGE = 16384;
+constexpr int FK_NSTAGE = 6;
+constexpr int FK_TMAX = 2;     // tokens per pass (CodePredictor pass 0 carries two)
+constexpr int FK_DMAX = 2048;  // widest hidden state staged in shared memory
+constexpr int FK_HDMAX = 128;
+constexpr int FK_REPMAX = 4;   // q heads per kv head
+constexpr int FK_MAXCTA = 256;
+constexpr int FK_PAIRS = 4;    // (head, token) pairs of one CTA in a CodePredictor attention
+constexpr long long FK_WAIT_CYCLES = 4000000000ll;  // ~2 s at GB300 clocks
+// Per-layer "side block" (norm gains g_attn | g_ffn | g_q | g_k, weight dtype),
+// copied into a double-buffered shared-memory slot one layer ahead.
+constexpr int FK_SIDE_BYTES = (2 * FK_DMAX + 2 * FK_HDMAX) * 4;
+constexpr int FK_MAXLAYERS = 64;  // Talker + CodePredictor layers held in shared memory
+
+static_assert(FAST_NT == FK_CONSUMERS, "the register sampler runs on the consumer warps");
+
+struct LayerDev {
+  const void* side;   // [g_attn D | g_ffn D | g_q hd | g_k hd], weight dtype, contiguous
+  const void* w_qkv;
+  const void* w_oT;   // [Hq][D][hd]: for each head, one hd-long row per output column
+  const void* w_gate;
+  const void* w_up;
+  const void* w_dT;   // [F][D]: down projection transposed
+  const void* g_attn;
+  const void* g_ffn;
+  const void* g_q;
+  const void* g_k;
+};
+
+struct FKParams {
+  int ncta;
+  int Dt, Dc, Ft, Fc, Hq, Hkv, hd, Vt, Vc, Lt, Lc, qkv_rows, has_proj, qk_norm, dmax;
+  float eps;
+  const LayerDev* tl;
+  const LayerDev* cl;
+  const void *t_head, *e_codec, *cp_heads, *cp_embeds, *cp_proj, *t_gfinal, *cp_gfinal;
+  float* pending_h;
+  float* pending_logits;
+  uint8_t* history;
+  KVDesc tkv, ckv;
+  const float* rope_cos;
+  const float* rope_sin;
+  float *R, *dA, *dF;  // [2][FK_TMAX][dmax] each
+  float* qkv;          // [FK_TMAX][qkv_rows]
+  float* part;         // [Hq][cpg][hd + 2]
+  float* cp_logits;    // [Vc]
+  float* xsum;         // [Dt]
+  unsigned* bar;
+  unsigned* done;
+  int* err;
+  int* abort_flag;
+  // this call
+  int sid, pos, newpage;
+  q3tts_sampling sp;
+  const float* uniforms;
+  int32_t* codes;
+  const int32_t* forced;
+  float* dump;
+};
+
+struct FKState {
+  void* base;
+  char* sideT;
+  char* sideC;
+  LayerDev* tl;
+  LayerDev* cl;
+  float *R, *dA, *dF, *qkv, *part, *cp_logits, *xsum;
+  unsigned *bar, *done;
+  int* abort_flag;
+  int ncta, dmax;
+  size_t smem;
+  bool ok;
+};
+
+}  // namespace q3
+
+struct q3::FrameKernelState : q3::FKState {};
+
+namespace q3 {
+
+// ------------------------------------------------------------------ PTX
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
 }
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Weight bytes are read once per use: the copy carries an L2 evict-first
+// policy so the stream does not push activations, KV rows and code out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar,
+                                         uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(FK_CONSUMERS) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_volatile(const int* p) { return *(const volatile int*)p; }
+
+__device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+
+__device__ __forceinline__ void split(int n, int parts, int i, int& lo, int& hi) {
+  lo = (int)((long long)n * i / parts);
+  hi = (int)((long long)n * (i + 1) / parts);
+}
+
+__device__ __forceinline__ int rows_per_chunk(int row_bytes) {
+  int r = FK_STAGE / row_bytes;
+  return r < 1 ? 1 : r;
+}
+
+// Activations staged for a GEMV use a "plane" layout so that lane reads of 8
+// consecutive elements are bank-conflict free: for a vector of length K,
+// float4 j of plane 0 holds elements 8j..8j+3 and float4 j of plane 1 (at
+// offset K/2) holds 8j+4..8j+7.  plane_first(p, K) is the first element of
+// plane float4 p (p < K/4).
+__device__ __forceinline__ int plane_first(int p, int K) {
+  const int half = K >> 3;
+  return p < half ? 8 * p : 8 * (p - half) + 4;
+}
+
+// ------------------------------------------------------------ shared memory
+
+struct AttnScratch {
+  float m[FK_CONSUMER_WARPS][FK_PAIRS];
+  float l[FK_CONSUMER_WARPS][FK_PAIRS];
+  float o[FK_CONSUMER_WARPS][FK_PAIRS][FK_HDMAX];
+  float q[FK_PAIRS][FK_HDMAX];
+};
+static_assert(FK_PAIRS >= FK_REPMAX, "talker attention keeps one partial per q head of a group");
+
+struct FKSmem {
+  alignas(128) unsigned char ring[FK_NSTAGE][FK_STAGE];
+  // Launch parameters and per-layer pointer tables live in shared memory: a
+  // read through a pointer to the parameter block or a global table costs a
+  // memory round trip, which the short phases cannot afford.
+  FKParams prm;
+  LayerDev lay[FK_MAXLAYERS];  // Talker layers, then CodePredictor layers
+  union {
+    float xs[FK_TMAX * FK_DMAX];  // normed activations of the current GEMV (plane layout)
+    FastSamplerSmem smp;
+    AttnScratch att;
+  } u;
+  float os[2][FK_TMAX][FK_HDMAX];  // attention outputs of the CTA's (<= 2) heads, plane layout
+  float av[2][FK_TMAX][64];        // SwiGLU values of a row group (double-buffered)
+  float red[FK_TMAX][FK_CONSUMER_WARPS];
+  float rope_c[17][FK_HDMAX / 2];  // rows 0..15: CodePredictor positions; 16: the Talker position
+  float rope_s[17][FK_HDMAX / 2];
+  alignas(128) unsigned char side[2][FK_SIDE_BYTES];
+  alignas(16) unsigned char fin[2 * FK_DMAX * 4];  // final-norm gains: CodePredictor then Talker
+  float uni[Q3TTS_N_CODEBOOKS];
+  int forced[Q3TTS_N_CODEBOOKS];
+  alignas(8) uint64_t full[FK_NSTAGE];
+  alignas(8) uint64_t empty[FK_NSTAGE];
+  alignas(8) uint64_t side_full[2];
+  alignas(8) uint64_t side_empty[2];
+  int flag;
+};
+static_assert(sizeof(FKSmem) <= 227 * 1024, "persistent kernel shared memory");
+
+// ---------------------------------------------------------------- context
+
+struct Cons {
+  const FKParams* p;
+  FKSmem* sm;
+  int cta, tid, warp, lane;
+  uint32_t n;      // ring chunks consumed
+  uint32_t phase;  // grid barriers passed in this launch
+  uint32_t layer;  // layers started in this launch (side-slot index)
+  bool aborted;
+};
+
+struct ConsGroup {
+  __device__ static int tid() { return threadIdx.x - FK_PRODUCER_THREADS; }
+  __device__ static int nt() { return FK_CONSUMERS; }
+  __device__ static void sync() { consumer_sync(); }
+};
+
+__device__ __forceinline__ void raise_abort(const FKParams& p, int code) {
+  atomicCAS(p.err, 0, code);
+  atomicExch(p.abort_flag, 1);
+}
+
+// Waits for ring chunk n (all lanes of the calling warp).
+__device__ __forceinline__ const unsigned char* acquire_at(Cons& c, uint32_t n) {
+  const int s = n % FK_NSTAGE;
+  const unsigned par = (n / FK_NSTAGE) & 1u;
+  if (!c.aborted) {
+    long long t0 = clock64();
+    unsigned it = 0;
+    while (!mbar_try_wait(&c.sm->full[s], par)) {
+      if ((++it & 255u) == 0 && (ld_volatile(c.p->abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
+        if (c.lane == 0) raise_abort(*c.p, Q3TTS_ERR_TIMEOUT);
+        c.aborted = true;
+        break;
+      }
+    }
+  }
+  return c.sm->ring[s];
+}
+
+// Bounded wait on an arbitrary mbarrier phase (all lanes of the calling warp).
+__device__ __forceinline__ void wait_bar(Cons& c, uint64_t* bar, unsigned par) {
+  if (c.aborted) return;
+  long long t0 = clock64();
+  unsigned it = 0;
+  while (!mbar_try_wait(bar, par)) {
+    if ((++it & 255u) == 0 && (ld_volatile(c.p->abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
+      if (c.lane == 0) raise_abort(*c.p, Q3TTS_ERR_TIMEOUT);
+      c.aborted = true;
+      break;
+    }
+  }
+}
+
+// The side block of the layer being started (waits for its copy).
+template <class WT>
+__device__ __forceinline__ const WT* side_begin(Cons& c) {
+  const int slot = c.layer & 1;
+  wait_bar(c, &c.sm->side_full[slot], (c.layer >> 1) & 1u);
+  return reinterpret_cast<const WT*>(c.sm->side[slot]);
+}
+
+// Done with the current layer's gains: the slot may be refilled.
+__device__ __forceinline__ void side_end(Cons& c) {
+  if (c.tid == 0) mbar_arrive(&c.sm->side_empty[c.layer & 1]);
+  c.layer++;
+}
+
+__device__ __forceinline__ void release_n(Cons& c, int count) {
+  __syncwarp();
+  if (c.lane == 0)
+    for (int i = 0; i < count; ++i) mbar_arrive(&c.sm->empty[(c.n + i) % FK_NSTAGE]);
+  c.n += count;
+}
+
+// Grid-wide barrier of all CTAs' consumers: a monotonic arrival counter,
+// release-add to arrive, acquire-load to wait (the last CTA to finish the
+// launch resets it).
+__device__ void grid_sync(Cons& c) {
+  consumer_sync();
+  if (c.tid == 0) {
+    const FKParams& p = *c.p;
+    red_release_add(p.bar, 1u);
+    c.phase++;
+    const unsigned target = c.phase * (unsigned)p.ncta;
+    int fail = c.aborted ? 1 : 0;
+    if (!fail) {
+      long long t0 = clock64();
+      unsigned it = 0;
+      while (ld_acquire(p.bar) < target) {
+        if ((++it & 63u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
+          raise_abort(p, Q3TTS_ERR_TIMEOUT);
+          fail = 1;
+          break;
+        }
+      }
+    }
+    c.sm->flag = fail;
+  }
+  consumer_sync();
+  if (c.sm->flag) c.aborted = true;
+}
+
+// -------------------------------------------------------------- GEMV core
+
+template <class WT>
+__device__ __forceinline__ void ld8_smem(const WT* p, float* w);
+template <>
+__device__ __forceinline__ void ld8_smem<bf16>(const bf16* p, float* w) {
+  unpack_bf16x8(*reinterpret_cast<const uint4*>(p), w);
+}
+template <>
+__device__ __forceinline__ void ld8_smem<float>(const float* p, float* w) {
+  float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+
+__device__ __forceinline__ float dot8(const float* w, float4 a, float4 b, float acc) {
+  acc = fmaf(w[0], a.x, acc); acc = fmaf(w[1], a.y, acc); acc = fmaf(w[2], a.z, acc);
+  acc = fmaf(w[3], a.w, acc); acc = fmaf(w[4], b.x, acc); acc = fmaf(w[5], b.y, acc);
+  acc = fmaf(w[6], b.z, acc); acc = fmaf(w[7], b.w, acc);
+  return acc;
+}
+
+// One row of the ring chunk (K weights at w) against T plane-layout vectors;
+// G lanes share the row (lane sl covers k = 8 sl + 8 G i); full-warp reduce
+// over the G-lane group.  All 32 lanes must call it.
+template <class WT>
+__device__ __forceinline__ void row_dot(const WT* w, int K, int G, int sl, bool valid, const float* x0,
+                                        const float* x1, int T, float& r0, float& r1) {
+  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+  if (valid) {
+    const float4* p0 = reinterpret_cast<const float4*>(x0);
+    const float4* q0 = reinterpret_cast<const float4*>(x0 + (K >> 1));
+    const float4* p1 = reinterpret_cast<const float4*>(x1);
+    const float4* q1 = reinterpret_cast<const float4*>(x1 + (K >> 1));
+    int k = sl * 8;
+#pragma unroll 2
+    for (; k < K; k += G * 8) {
+      float wv[8];
+      ld8_smem<WT>(w + k, wv);
+      const int j = k >> 3;
+      a0 = fmaf(wv[0], p0[j].x, a0); a0 = fmaf(wv[1], p0[j].y, a0);
+      a0 = fmaf(wv[2], p0[j].z, a0); a0 = fmaf(wv[3], p0[j].w, a0);
+      b0 = fmaf(wv[4], q0[j].x, b0); b0 = fmaf(wv[5], q0[j].y, b0);
+      b0 = fmaf(wv[6], q0[j].z, b0); b0 = fmaf(wv[7], q0[j].w, b0);
+      if (T > 1) {
+        a1 = fmaf(wv[0], p1[j].x, a1); a1 = fmaf(wv[1], p1[j].y, a1);
+        a1 = fmaf(wv[2], p1[j].z, a1); a1 = fmaf(wv[3], p1[j].w, a1);
+        b1 = fmaf(wv[4], q1[j].x, b1); b1 = fmaf(wv[5], q1[j].y, b1);
+        b1 = fmaf(wv[6], q1[j].z, b1); b1 = fmaf(wv[7], q1[j].w, b1);
+      }
+    }
+  }
+  r0 = a0 + b0;
+  r1 = a1 + b1;
+  for (int o = G / 2; o > 0; o >>= 1) {
+    r0 += __shfl_xor_sync(0xffffffffu, r0, o);
+    r1 += __shfl_xor_sync(0xffffffffu, r1, o);
+  }
+}
+
+__device__ __forceinline__ int lanes_per_row(int K) { return K >= 256 ? 32 : (K >= 128 ? 16 : 8); }
+
+// Rows [r0, r1) of a row-major [*, K] matrix, streamed from the ring: out_t(row)
+// = sum_k W[row, k] * x_t[k] for t < T.  xsel(row, t) gives the plane-layout
+// vector; epi(row, t, value) consumes each result (called by one lane per row).
+template <class WT, class XSel, class Epi>
+__device__ void gemv_rows(Cons& c, int r0, int r1, int K, int T, XSel xsel, Epi epi) {
+  const int row_bytes = K * (int)sizeof(WT);
+  const int rpc = rows_per_chunk(row_bytes);
+  const int G = lanes_per_row(K);
+  const int gpw = 32 / G, nslots = FK_CONSUMER_WARPS * gpw;
+  const int sub = c.lane / G, sl = c.lane % G;
+  for (int r = r0; r < r1; r += rpc) {
+    const int nr = min(rpc, r1 - r);
+    const WT* buf = reinterpret_cast<const WT*>(acquire_at(c, c.n));
+    for (int base = c.warp * gpw; base < nr; base += nslots) {
+      const int i = base + sub;
+      const bool valid = i < nr;
+      const int row = r + (valid ? i : 0);
+      float v0, v1;
+      row_dot<WT>(buf + (size_t)(valid ? i : 0) * K, K, G, sl, valid, xsel(row, 0),
+                  xsel(row, T > 1 ? 1 : 0), T, v0, v1);
+      if (valid && sl == 0) {
+        epi(row, 0, v0);
+        if (T > 1) epi(row, 1, v1);
+      }
+    }
+    release_n(c, 1);
+  }
+}
+
+// ------------------------------------------------------- residual helpers
+
+__device__ __forceinline__ float* rbuf(const FKParams& p, float* base, int set, int t) {
+  return base + ((size_t)set * FK_TMAX + t) * p.dmax;
+}
+
+enum { SRC_SETS = 0, SRC_SETS_NOF = 1, SRC_XS = 2 };
+
+// Builds xs[t] = RMSNorm(x_t) * g (plane layout) for t < T, where x_t is
+//   SRC_SETS:     R_s + dA_s + dF_s of token t0 + t,
+//   SRC_SETS_NOF: R_s + dA_s,
+//   SRC_XS:       already in xs (plane layout, raw).
+// All loads of a thread are issued together.  With fold, the CTA's slice of
+// each raw x_t is written to R_{1-s} and the same slices of dA_{1-s}, dF_{1-s}
+// are zeroed.  If out is given, the CTA's slice of the normed x_0 goes there.
+template <class WT>
+__device__ __noinline__ void load_norm(Cons& c, int mode, int s, int t0, int T, int D, const WT* g, bool fold,
+                          float* out) {
+  const FKParams& p = *c.p;
+  float* xs = c.sm->u.xs;
+  constexpr int PER = FK_TMAX * FK_DMAX / 4 / FK_CONSUMERS;  // float4 per thread, at most 4
+  const int nq = D / 4;                                       // float4 per token
+  float4 xv[PER];
+  float gv[PER][4];
+  float ss[FK_TMAX] = {0.f, 0.f};
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int e = c.tid + FK_CONSUMERS * u;
+    if (e < T * nq) {
+      const int t = e / nq, pq = e % nq, i = plane_first(pq, D);
+      if (mode == SRC_XS) {
+        xv[u] = reinterpret_cast<const float4*>(xs + t * D)[pq];
+      } else {
+        float4 r = ldcg4(rbuf(p, p.R, s, t0 + t) + i);
+        float4 a = ldcg4(rbuf(p, p.dA, s, t0 + t) + i);
+        float4 f = mode == SRC_SETS ? ldcg4(rbuf(p, p.dF, s, t0 + t) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        xv[u] = make_float4(r.x + a.x + f.x, r.y + a.y + f.y, r.z + a.z + f.z, r.w + a.w + f.w);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) gv[u][q] = to_f(g[i + q]);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int e = c.tid + FK_CONSUMERS * u;
+    if (e < T * nq) {
+      const int t = e / nq;
+      const float v = xv[u].x * xv[u].x + xv[u].y * xv[u].y + xv[u].z * xv[u].z + xv[u].w * xv[u].w;
+      if (t == 0) ss[0] += v; else ss[1] += v;
+    }
+  }
+  if (fold) {
+    int lo, hi;
+    split(D, p.ncta, c.cta, lo, hi);
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int e = c.tid + FK_CONSUMERS * u;
+      if (e < T * nq) {
+        const int t = e / nq, i = plane_first(e % nq, D);
+        const float vals[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (i + q >= lo && i + q < hi) {
+            rbuf(p, p.R, 1 - s, t)[i + q] = vals[q];
+            rbuf(p, p.dA, 1 - s, t)[i + q] = 0.f;
+            rbuf(p, p.dF, 1 - s, t)[i + q] = 0.f;
+          }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < FK_TMAX; ++t) {
+    const float v = warp_sum(ss[t]);
+    if (c.lane == 0) c.sm->red[t][c.warp] = v;
+  }
+  consumer_sync();
+  float inv[FK_TMAX];
+#pragma unroll
+  for (int t = 0; t < FK_TMAX; ++t) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < FK_CONSUMER_WARPS; ++w) tot += c.sm->red[t][w];
+    inv[t] = 1.0f / sqrtf(tot / (float)D + p.eps);
+  }
+  int lo = 0, hi = 0;
+  if (out) split(D, p.ncta, c.cta, lo, hi);
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int e = c.tid + FK_CONSUMERS * u;
+    if (e < T * nq) {
+      const int t = e / nq, pq = e % nq;
+      const float iv = t == 0 ? inv[0] : inv[1];
+      float4 y = make_float4(xv[u].x * iv * gv[u][0], xv[u].y * iv * gv[u][1], xv[u].z * iv * gv[u][2],
+                             xv[u].w * iv * gv[u][3]);
+      reinterpret_cast<float4*>(xs + t * D)[pq] = y;
+      if (out && t == 0) {
+        const int i = plane_first(pq, D);
+        const float vals[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (i + q >= lo && i + q < hi) out[i + q] = vals[q];
+      }
+    }
+  }
+  consumer_sync();
+}
+
+// Writes a raw vector (natural order, D floats at src) into xs token t (plane layout).
+__device__ __forceinline__ void put_plane(float* xs_t, int D, int i, float v) {
+  const int j = i >> 3, r = i & 7;
+  xs_t[r < 4 ? 4 * j + r : (D >> 1) + 4 * j + (r - 4)] = v;
+}
+
+// ----------------------------------------------- q/k head normalisation
+
+// One warp: v (hd elements, lane holds l + 32 j) <- RoPE(RMSNorm(v) * g) with
+// gains g (shared memory) and the rotation of shared-memory rope row `rr`.
+template <class WT>
+__device__ __forceinline__ void norm_rope_head(const FKParams& p, const FKSmem* sm, float (&v)[4],
+                                               const WT* g, int rr, int lane) {
+  const int hd = p.hd, J = hd / 32;
+  if (p.qk_norm) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < J) ss = fmaf(v[j], v[j], ss);
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / (float)hd + p.eps);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < J) v[j] = v[j] * inv * to_f(g[lane + 32 * j]);
+  }
+  // rotate-half pairs (i, i + hd/2): (v0, v2), (v1, v3) for hd = 128; (v0, v1) for hd = 64
+  const float c0 = sm->rope_c[rr][lane], s0 = sm->rope_s[rr][lane];
+  if (J == 4) {
+    const float c1 = sm->rope_c[rr][lane + 32], s1 = sm->rope_s[rr][lane + 32];
+    const float a0 = v[0], a2 = v[2], a1 = v[1], a3 = v[3];
+    v[0] = a0 * c0 - a2 * s0;
+    v[2] = a2 * c0 + a0 * s0;
+    v[1] = a1 * c1 - a3 * s1;
+    v[3] = a3 * c1 + a1 * s1;
+  } else {
+    const float a0 = v[0], a1 = v[1];
+    v[0] = a0 * c0 - a1 * s0;
+    v[1] = a1 * c0 + a0 * s0;
+  }
+}
+
+// Row of the shared-memory rope table for a position: CodePredictor positions
+// map to themselves, the Talker position to row 16.
+__device__ __forceinline__ int cp_rope_row(int pos) { return pos; }
+constexpr int TALKER_ROPE_ROW = 16;
+
+// ------------------------------------------------------------ the sampler
+
+// Draws code j of the frame (0: semantic from the pending Talker logits; 1..15:
+// acoustic from the last CodePredictor head) in every CTA, identically.
+// Returns the code fed forward (the forced code under teacher forcing).
+__device__ __noinline__ int draw_code(Cons& c, int j) {
+  const FKParams& p = *c.p;
+  const bool sem = j == 0;
+  const int V = sem ? p.Vt : p.Vc;
+  const float* src = sem ? p.pending_logits + (size_t)p.sid * p.Vt : p.cp_logits;
+  if (p.dump && c.cta == 0) {
+    const int off = sem ? 0 : p.Vt + (j - 1) * p.Vc;
+    for (int i = c.tid; i < V; i += FK_CONSUMERS) p.dump[off + i] = __ldcg(src + i);
+  }
+  int code = fast_sample<ConsGroup>(c.sm->u.smp, src, V, sem ? p.sp.do_sample : p.sp.sub_do_sample,
+                                    sem ? p.sp.top_k : p.sp.sub_top_k, sem ? p.sp.top_p : p.sp.sub_top_p,
+                                    sem ? p.sp.temperature : p.sp.sub_temperature,
+                                    sem ? p.sp.repetition_penalty : 1.0f,
+                                    sem ? p.history + (size_t)p.sid * p.Vt : nullptr, c.sm->uni[j]);
+  code = min(max(code, 0), V - 1);
+  int fed = code;
+  if (p.forced) {
+    fed = c.sm->forced[j];
+    if (fed < 0 || fed >= V) {
+      if (c.cta == 0 && c.tid == 0) atomicCAS(p.err, 0, Q3TTS_ERR_ARG);
+      fed = code;
+    }
+  }
+  if (c.cta == 0 && c.tid == 0) p.codes[j] = code;
+  return fed;
+}
+
+// Gains of the current layer inside its side slot.
+template <class WT>
+__device__ __forceinline__ const WT* side_cur(const Cons& c) {
+  return reinterpret_cast<const WT*>(c.sm->side[c.layer & 1]);
+}
+template <class WT>
+__device__ __forceinline__ const WT* side_gq(const Cons& c, int D) { return side_cur<WT>(c) + 2 * D; }
+template <class WT>
+__device__ __forceinline__ const WT* side_gk(const Cons& c, int D) { return side_cur<WT>(c) + 2 * D + c.p->hd; }
+
+// ---------------------------------------------------------------- phases
+
+// Phase A: residual in (or tokens already in xs), fold, RMSNorm, QKV rows out;
+// the layer's q/k norm gains go to shared memory for phase B.
+template <class WT>
+__device__ __noinline__ void phase_qkv(Cons& c, int D, int T, int s, bool from_xs) {
+  const FKParams& p = *c.p;
+  const WT* side = side_begin<WT>(c);
+  load_norm<WT>(c, from_xs ? SRC_XS : SRC_SETS, s, 0, T, D, side, true, nullptr);
+  int lo, hi;
+  split(p.qkv_rows, p.ncta, c.cta, lo, hi);
+  float* xs = c.sm->u.xs;
+  gemv_rows<WT>(
+      c, lo, hi, D, T, [&](int, int t) { return xs + t * D; },
+      [&](int row, int t, float v) { p.qkv[(size_t)t * p.qkv_rows + row] = v; });
+  grid_sync(c);
+}
+
+// o_proj over the CTA's (head, output column) range; os holds the heads' outputs.
+template <class WT>
+__device__ void oproj_cols(Cons& c, int D, int T, int s_next, int v0, int v1, int h_first) {
+  const FKParams& p = *c.p;
+  gemv_rows<WT>(
+      c, v0, v1, p.hd, T, [&](int row, int t) { return c.sm->os[row / D - h_first][t]; },
+      [&](int row, int t, float v) { atomicAdd(rbuf(p, p.dA, s_next, t) + row % D, v); });
+}
+
+// Stores a warp's head vector (lane holds l + 32 j) into plane layout.
+__device__ __forceinline__ void store_head_plane(float* dst, int hd, const float* v, int lane) {
+  for (int j = 0; j < hd / 32; ++j) put_plane(dst, hd, lane + 32 * j, v[j]);
+}
+
+// CodePredictor phase B: attention of the CTA's one or two heads for each of
+// the pass's tokens over positions 0..pos0+t (at most 16), then o_proj.
+// Positions are spread over the warps (K/V loads issued up front), partial
+// softmax sums are combined across warps.  The CTA owning column 0 of the
+// first q head of a kv group appends that group's current k, v to the cache.
+template <class WT>
+__device__ __noinline__ void phase_cp_attn(Cons& c, int layer, int T, int pos0, int s_next) {
+  const FKParams& p = *c.p;
+  const int D = p.Dc, hd = p.hd, Hq = p.Hq, Hkv = p.Hkv, rep = Hq / Hkv, J = hd / 32;
+  int v0, v1;
+  split(Hq * D, p.ncta, c.cta, v0, v1);
+  const int h_first = v0 / D, h_last = (v1 - 1) / D;
+  const int nh = v1 > v0 ? h_last - h_first + 1 : 0;
+  const int npair = nh * T;
+  const int g_first = h_first / rep;
+  const int ng = nh ? h_last / rep - g_first + 1 : 0;  // kv groups touched (<= 2)
+  AttnScratch& as = c.sm->u.att;
+  const float scale = 1.0f / sqrtf((float)hd);
+  const int S = pos0 + T;  // positions 0..S-1 exist after this pass
+  // 1) this warp's positions (warp, warp + 8): k, v of every touched kv group
+  float kk[2][2][4], vv[2][2][4];
+#pragma unroll
+  for (int np = 0; np < 2; ++np) {
+    const int sp = c.warp + FK_CONSUMER_WARPS * np;
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi) {
+      const int g = g_first + gi;
+      if (sp < S && gi < ng) {
+        const float* kc;
+        const float* vc;
+        if (sp < pos0) {
+          kc = (const float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 0, g);
+          vc = (const float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 1, g);
+        } else {
+          kc = p.qkv + (size_t)(sp - pos0) * p.qkv_rows + (Hq + g) * hd;
+          vc = p.qkv + (size_t)(sp - pos0) * p.qkv_rows + (Hq + Hkv + g) * hd;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          kk[np][gi][j] = j < J ? __ldcg(kc + c.lane + 32 * j) : 0.f;
+          vv[np][gi][j] = j < J ? __ldcg(vc + c.lane + 32 * j) : 0.f;
+        }
+      }
+    }
+  }
+  // 2) q of each (head, token) pair, normalised and rotated
+  if (c.warp < npair) {
+    const int h = h_first + c.warp / T, t = c.warp % T;
+    float q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = j < J ? __ldcg(p.qkv + (size_t)t * p.qkv_rows + h * hd + c.lane + 32 * j) : 0.f;
+    norm_rope_head(p, c.sm, q, side_gq<WT>(c, D), cp_rope_row(pos0 + t), c.lane);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < J) as.q[c.warp][c.lane + 32 * j] = q[j];
+  }
+  // 3) current-position keys: normalise, rotate, append (designated CTA)
+#pragma unroll
+  for (int np = 0; np < 2; ++np) {
+    const int sp = c.warp + FK_CONSUMER_WARPS * np;
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi) {
+      if (sp < S && sp >= pos0 && gi < ng) {
+        const int g = g_first + gi;
+        norm_rope_head(p, c.sm, kk[np][gi], side_gk<WT>(c, D), cp_rope_row(sp), c.lane);
+        const long long first = (long long)g * rep * D;
+        if (first >= v0 && first < v1) {
+          float* kc = (float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 0, g);
+          float* vc = (float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 1, g);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (j < J) { kc[c.lane + 32 * j] = kk[np][gi][j]; vc[c.lane + 32 * j] = vv[np][gi][j]; }
+        }
+      }
+    }
+  }
+  consumer_sync();
+  // 4) per-warp partial softmax over its positions, for every pair
+  for (int pr = 0; pr < npair; ++pr) {
+    const int h = h_first + pr / T, t = pr % T, gsel = h / rep - g_first;
+    float m = -INFINITY, l = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      const int sp = c.warp + FK_CONSUMER_WARPS * np;
+      if (sp <= pos0 + t) {  // causal (and sp < S)
+#pragma unroll
+        for (int gi = 0; gi < 2; ++gi) {
+          if (gi == gsel) {
+            float d = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (j < J) d = fmaf(as.q[pr][c.lane + 32 * j], kk[np][gi][j], d);
+            d = warp_sum(d) * scale;
+            const float mn = fmaxf(m, d), corr = __expf(m - mn), e = __expf(d - mn);
+            l = l * corr + e;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[j] = o[j] * corr + e * vv[np][gi][j];
+            m = mn;
+          }
+        }
+      }
+    }
+    if (c.lane == 0) { as.m[c.warp][pr] = m; as.l[c.warp][pr] = l; }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < J) as.o[c.warp][pr][c.lane + 32 * j] = o[j];
+  }
+  consumer_sync();
+  // 5) combine the warps: thread (pair, d)
+  for (int e = c.tid; e < npair * hd; e += FK_CONSUMERS) {
+    const int pr = e / hd, d = e % hd;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < FK_CONSUMER_WARPS; ++w) M = fmaxf(M, as.m[w][pr]);
+    float Ls = 0.f, Os = 0.f;
+#pragma unroll
+    for (int w = 0; w < FK_CONSUMER_WARPS; ++w) {
+      const float f = as.m[w][pr] == -INFINITY ? 0.f : __expf(as.m[w][pr] - M);
+      Ls += as.l[w][pr] * f;
+      Os += as.o[w][pr][d] * f;
+    }
+    put_plane(c.sm->os[pr / T][pr % T], hd, d, Os / Ls);
+  }
+  consumer_sync();
+  oproj_cols<WT>(c, D, T, s_next, v0, v1, h_first);
+  grid_sync(c);
+}
+
+// Talker phase B1: attention partials.  Work item = (kv group g, position
+// chunk); the q heads of the group share the K/V reads.  The item holding the
+// current position appends its k, v to the cache.
+template <class WT, class KT>
+__device__ __noinline__ void phase_talker_attn(Cons& c, int layer) {
+  const FKParams& p = *c.p;
+  const int hd = p.hd, Hq = p.Hq, Hkv = p.Hkv, rep = Hq / Hkv, J = hd / 32;
+  const int cpg = p.ncta / Hkv;
+  const int g = c.cta / cpg, ch = c.cta % cpg;
+  const int pos = p.pos, S = pos + 1;
+  AttnScratch& as = c.sm->u.att;
+  const float scale = 1.0f / sqrtf((float)hd);
+  if (g < Hkv) {
+    const int cs = (S + cpg - 1) / cpg, s0 = ch * cs, s1 = min(S, s0 + cs);
+    if (c.warp < rep) {
+      const int h = g * rep + c.warp;
+      float q[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) q[j] = j < J ? __ldcg(p.qkv + h * hd + c.lane + 32 * j) : 0.f;
+      norm_rope_head(p, c.sm, q, side_gq<WT>(c, p.Dt), TALKER_ROPE_ROW, c.lane);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j < J) as.q[c.warp][c.lane + 32 * j] = q[j];
+    }
+    consumer_sync();
+    float m[FK_REPMAX], l[FK_REPMAX], o[FK_REPMAX][4];
+#pragma unroll
+    for (int r = 0; r < FK_REPMAX; ++r) {
+      m[r] = -INFINITY; l[r] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[r][j] = 0.f;
+    }
+    constexpr int BATCH = 4;
+    for (int sb = s0 + c.warp; sb < s1; sb += BATCH * FK_CONSUMER_WARPS) {
+      float k[BATCH][4], v[BATCH][4];
+#pragma unroll
+      for (int b = 0; b < BATCH; ++b) {
+        const int sp = sb + b * FK_CONSUMER_WARPS;
+        if (sp < pos) {
+          const KT* kc = (const KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, sp, 0, g);
+          const KT* vc = (const KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, sp, 1, g);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            k[b][j] = j < J ? to_f(kc[c.lane + 32 * j]) : 0.f;
+            v[b][j] = j < J ? to_f(vc[c.lane + 32 * j]) : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            k[b][j] = (sp == pos && j < J) ? __ldcg(p.qkv + (Hq + g) * hd + c.lane + 32 * j) : 0.f;
+            v[b][j] = (sp == pos && j < J) ? __ldcg(p.qkv + (Hq + Hkv + g) * hd + c.lane + 32 * j) : 0.f;
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < BATCH; ++b) {
+        const int sp = sb + b * FK_CONSUMER_WARPS;
+        if (sp < s1) {
+          if (sp == pos) {
+            norm_rope_head(p, c.sm, k[b], side_gk<WT>(c, p.Dt), TALKER_ROPE_ROW, c.lane);
+            KT* kc = (KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, pos, 0, g);
+            KT* vc = (KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, pos, 1, g);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (j < J) { kc[c.lane + 32 * j] = from_f<KT>(k[b][j]); vc[c.lane + 32 * j] = from_f<KT>(v[b][j]); }
+          }
+#pragma unroll
+          for (int r = 0; r < FK_REPMAX; ++r) {
+            if (r < rep) {
+              float d = 0.f;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (j < J) d = fmaf(as.q[r][c.lane + 32 * j], k[b][j], d);
+              d = warp_sum(d) * scale;
+              const float mn = fmaxf(m[r], d), corr = __expf(m[r] - mn), e = __expf(d - mn);
+              l[r] = l[r] * corr + e;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) o[r][j] = o[r][j] * corr + e * v[b][j];
+              m[r] = mn;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < FK_REPMAX; ++r) {
+      if (r < rep) {
+        if (c.lane == 0) { as.m[c.warp][r] = m[r]; as.l[c.warp][r] = l[r]; }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < J) as.o[c.warp][r][c.lane + 32 * j] = o[r][j];
+      }
+    }
+    consumer_sync();
+    for (int e = c.tid; e < rep * hd; e += FK_CONSUMERS) {
+      const int r = e / hd, d = e % hd;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < FK_CONSUMER_WARPS; ++w) M = fmaxf(M, as.m[w][r]);
+      float Ls = 0.f, Os = 0.f;
+      if (M > -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < FK_CONSUMER_WARPS; ++w) {
+          const float f = as.m[w][r] == -INFINITY ? 0.f : __expf(as.m[w][r] - M);
+          Ls += as.l[w][r] * f;
+          Os += as.o[w][r][d] * f;
+        }
+      }
+      float* dst = p.part + ((size_t)(g * rep + r) * cpg + ch) * (hd + 2);
+      dst[2 + d] = Os;
+      if (d == 0) { dst[0] = M; dst[1] = Ls; }
+    }
+  }
+  grid_sync(c);
+}
+
+// Talker phase B2: combine the partials of the CTA's heads (all partial loads
+// of a thread issued together), then o_proj.
+template <class WT>
+__device__ __noinline__ void phase_talker_oproj(Cons& c, int s_next) {
+  const FKParams& p = *c.p;
+  const int D = p.Dt, hd = p.hd, Hq = p.Hq, cpg = p.ncta / p.Hkv;
+  int v0, v1;
+  split(Hq * D, p.ncta, c.cta, v0, v1);
+  const int h_first = v0 / D, h_last = (v1 - 1) / D;
+  const int nh = v1 > v0 ? h_last - h_first + 1 : 0;
+  constexpr int CMAX = 20;  // chunks per kv group handled in one batch of loads
+  for (int e = c.tid; e < nh * hd; e += FK_CONSUMERS) {
+    const int hh = e / hd, d = e % hd, h = h_first + hh;
+    const float* base = p.part + (size_t)h * cpg * (hd + 2);
+    float M = -INFINITY, Ls = 0.f, Os = 0.f;
+    for (int c0 = 0; c0 < cpg; c0 += CMAX) {
+      float mm[CMAX], ll[CMAX], oo[CMAX];
+#pragma unroll
+      for (int q = 0; q < CMAX; ++q) {
+        const int chn = c0 + q;
+        const float* pr = base + (size_t)(chn < cpg ? chn : 0) * (hd + 2);
+        mm[q] = chn < cpg ? __ldcg(pr) : -INFINITY;
+        ll[q] = chn < cpg ? __ldcg(pr + 1) : 0.f;
+        oo[q] = chn < cpg ? __ldcg(pr + 2 + d) : 0.f;
+      }
+      float Mn = M;
+#pragma unroll
+      for (int q = 0; q < CMAX; ++q) Mn = fmaxf(Mn, mm[q]);
+      const float corr = M == -INFINITY ? 0.f : __expf(M - Mn);
+      Ls *= corr;
+      Os *= corr;
+#pragma unroll
+      for (int q = 0; q < CMAX; ++q) {
+        const float f = mm[q] == -INFINITY ? 0.f : __expf(mm[q] - Mn);
+        Ls += ll[q] * f;
+        Os += oo[q] * f;
+      }
+      M = Mn;
+    }
+    put_plane(c.sm->os[hh][0], hd, d, Os / Ls);
+  }
+  consumer_sync();
+  oproj_cols<WT>(c, D, 1, s_next, v0, v1, h_first);
+  grid_sync(c);
+}
+
+// Phase C: y = R + dA (set s_next), RMSNorm, gate/up rows of the CTA's FFN
+// slice, SwiGLU, matching rows of the transposed down projection; the partial
+// D-vector is added into dF with float4 atomics.
+template <class WT>
+__device__ __noinline__ void phase_ffn(Cons& c, const LayerDev& L, int D, int F, int T, int s_next) {
+  const FKParams& p = *c.p;
+  load_norm<WT>(c, SRC_SETS_NOF, s_next, 0, T, D, side_cur<WT>(c) + D, false, nullptr);
+  side_end(c);
+  float* xs = c.sm->u.xs;
+  int f0, f1;
+  split(F, p.ncta, c.cta, f0, f1);
+  const int row_bytes = D * (int)sizeof(WT);
+  const int gpr = min(64, rows_per_chunk(row_bytes));
+  const int G = lanes_per_row(D), gpw = 32 / G, nslots = FK_CONSUMER_WARPS * gpw;
+  const int sub = c.lane / G, sl = c.lane % G;
+  float acc[FK_TMAX][8];
+#pragma unroll
+  for (int t = 0; t < FK_TMAX; ++t)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[t][q] = 0.f;
+  const int col = c.tid * 8;  // this thread's 8 output columns (D <= 2048)
+  int buf = 0;
+  for (int g = f0; g < f1; g += gpr, buf ^= 1) {
+    const int ng = min(gpr, f1 - g);
+    // gate and up rows of the group (two consecutive ring chunks)
+    const WT* wg = reinterpret_cast<const WT*>(acquire_at(c, c.n));
+    const WT* wu = reinterpret_cast<const WT*>(acquire_at(c, c.n + 1));
+    for (int base = c.warp * gpw; base < ng; base += nslots) {
+      const int i = base + sub;
+      const bool valid = i < ng;
+      const int ii = valid ? i : 0;
+      float g0, g1, u0, u1;
+      row_dot<WT>(wg + (size_t)ii * D, D, G, sl, valid, xs, xs + D, T, g0, g1);
+      row_dot<WT>(wu + (size_t)ii * D, D, G, sl, valid, xs, xs + D, T, u0, u1);
+      if (valid && sl == 0) {
+        c.sm->av[buf][0][i] = silu(g0) * u0;
+        if (T > 1) c.sm->av[buf][1][i] = silu(g1) * u1;
+      }
+    }
+    release_n(c, 2);
+    consumer_sync();
+    const WT* wd = reinterpret_cast<const WT*>(acquire_at(c, c.n));
+    if (col < D) {
+      for (int i = 0; i < ng; ++i) {
+        float w[8];
+        ld8_smem<WT>(wd + (size_t)i * D + col, w);
+        const float a0 = c.sm->av[buf][0][i];
+        const float a1 = T > 1 ? c.sm->av[buf][1][i] : 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          acc[0][q] = fmaf(a0, w[q], acc[0][q]);
+          acc[1][q] = fmaf(a1, w[q], acc[1][q]);
+        }
+      }
+    }
+    release_n(c, 1);
+  }
+  if (col < D && f1 > f0) {
+#pragma unroll
+    for (int t = 0; t < FK_TMAX; ++t) {
+      if (t < T) {
+        float* dst = rbuf(p, p.dF, s_next, t) + col;
+        atomicAdd(reinterpret_cast<float4*>(dst), make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]));
+        atomicAdd(reinterpret_cast<float4*>(dst + 4), make_float4(acc[t][4], acc[t][5], acc[t][6], acc[t][7]));
+      }
+    }
+  }
+  grid_sync(c);
+}
+
+// The CodePredictor input token(s) of pass j into xs (plane layout, D_t wide):
+// pass 0: [h_T, E_t[c0]]; pass j >= 1: E_cp[j-1][c_j].
+template <class WT>
+__device__ __noinline__ void cp_tokens(Cons& c, int j, int fed) {
+  const FKParams& p = *c.p;
+  const int Dt = p.Dt;
+  float* xs = c.sm->u.xs;
+  if (j == 0) {
+    const WT* e = (const WT*)p.e_codec + (size_t)fed * Dt;
+    for (int i = c.tid; i < Dt; i += FK_CONSUMERS) {
+      put_plane(xs, Dt, i, __ldcg(p.pending_h + (size_t)p.sid * Dt + i));
+      put_plane(xs + Dt, Dt, i, to_f(e[i]));
+    }
+  } else {
+    const WT* e = (const WT*)p.cp_embeds + ((size_t)(j - 1) * p.Vc + fed) * Dt;
+    for (int i = c.tid; i < Dt; i += FK_CONSUMERS) put_plane(xs, Dt, i, to_f(e[i]));
+  }
+  consumer_sync();
+}
+
+// The CTA's slice of the running embedding sum of the frame's codes.
+template <class WT>
+__device__ __noinline__ void xsum_add(Cons& c, int j, int fed) {
+  const FKParams& p = *c.p;
+  int lo, hi;
+  split(p.Dt, p.ncta, c.cta, lo, hi);
+  const WT* e = j == 0 ? (const WT*)p.e_codec + (size_t)fed * p.Dt
+                       : (const WT*)p.cp_embeds + ((size_t)(j - 1) * p.Vc + fed) * p.Dt;
+  for (int i = lo + c.tid; i < hi; i += FK_CONSUMERS)
+    p.xsum[i] = j == 0 ? to_f(e[i]) : p.xsum[i] + to_f(e[i]);
+}
+
+template <class WT, class KT>
+__device__ void consumer(const FKParams& p, FKSmem* sm) {
+  Cons c;
+  c.p = &p;
+  c.sm = sm;
+  c.cta = blockIdx.x;
+  c.tid = threadIdx.x - FK_PRODUCER_THREADS;
+  c.warp = c.tid >> 5;
+  c.lane = c.tid & 31;
+  c.n = 0;
+  c.phase = 0;
+  c.layer = 0;
+  c.aborted = false;
+  if (c.tid < Q3TTS_N_CODEBOOKS) {
+    sm->uni[c.tid] = p.uniforms[c.tid];
+    sm->forced[c.tid] = p.forced ? p.forced[c.tid] : 0;
+  }
+  {
+    WT* fin = reinterpret_cast<WT*>(sm->fin);
+    for (int i = c.tid; i < p.Dc; i += FK_CONSUMERS) fin[i] = ((const WT*)p.cp_gfinal)[i];
+    for (int i = c.tid; i < p.Dt; i += FK_CONSUMERS) fin[p.Dc + i] = ((const WT*)p.t_gfinal)[i];
+  }
+  if (c.cta == 0 && c.tid == 0 && p.newpage >= 0)
+    const_cast<int*>(p.tkv.page_table)[p.sid * p.tkv.pages_per_stream + p.pos / p.tkv.page_size] = p.newpage;
+  {
+    // rope rows: CodePredictor positions 0..15 and the Talker position
+    const int half = p.hd / 2;
+    for (int e = c.tid; e < 17 * half; e += FK_CONSUMERS) {
+      const int r = e / half, i = e % half, pos = r < 16 ? r : p.pos;
+      sm->rope_c[r][i] = p.rope_cos[(size_t)pos * half + i];
+      sm->rope_s[r][i] = p.rope_sin[(size_t)pos * half + i];
+    }
+  }
+  consumer_sync();
+  int fed0 = 0;
+  for (int j = 0; j < Q3TTS_N_CODEBOOKS - 1; ++j) {
+    const int T = j == 0 ? 2 : 1, pos0 = j == 0 ? 0 : j + 1;
+    const int fed = draw_code(c, j);
+    if (j == 0) fed0 = fed;
+    xsum_add<WT>(c, j, fed);
+    cp_tokens<WT>(c, j, fed);
+    int s = 0;
+    bool from_xs = true;
+    if (p.has_proj) {
+      // z = W_p u into R_0 (rows of the CTA), deltas of set 0 zeroed
+      int lo, hi;
+      split(p.Dc, p.ncta, c.cta, lo, hi);
+      float* xs = sm->u.xs;
+      gemv_rows<WT>(
+          c, lo, hi, p.Dt, T, [&](int, int t) { return xs + t * p.Dt; },
+          [&](int row, int t, float v) {
+            rbuf(p, p.R, 0, t)[row] = v;
+            rbuf(p, p.dA, 0, t)[row] = 0.f;
+            rbuf(p, p.dF, 0, t)[row] = 0.f;
+          });
+      grid_sync(c);
+      from_xs = false;
+    }
+    for (int l = 0; l < p.Lc; ++l) {
+      const LayerDev& L = sm->lay[p.Lt + l];
+      phase_qkv<WT>(c, p.Dc, T, s, from_xs);
+      from_xs = false;
+      phase_cp_attn<WT>(c, l, T, pos0, 1 - s);
+      phase_ffn<WT>(c, L, p.Dc, p.Fc, T, 1 - s);
+      s = 1 - s;
+    }
+    // final norm of the last token, head j
+    load_norm<WT>(c, SRC_SETS, s, T - 1, 1, p.Dc, reinterpret_cast<const WT*>(sm->fin), false, nullptr);
+    {
+      int lo, hi;
+      split(p.Vc, p.ncta, c.cta, lo, hi);
+      float* xs = sm->u.xs;
+      gemv_rows<WT>(
+          c, lo, hi, p.Dc, 1, [&](int, int) { return xs; },
+          [&](int row, int, float v) { p.cp_logits[row] = v; });
+    }
+    grid_sync(c);
+  }
+  // ---- Talker: input = embedding sum of the 16 codes
+  {
+    const int fed15 = draw_code(c, Q3TTS_N_CODEBOOKS - 1);
+    const WT* e = (const WT*)p.cp_embeds + ((size_t)(Q3TTS_N_CODEBOOKS - 2) * p.Vc + fed15) * p.Dt;
+    float* xs = sm->u.xs;
+    for (int i = c.tid; i < p.Dt; i += FK_CONSUMERS) put_plane(xs, p.Dt, i, __ldcg(p.xsum + i) + to_f(e[i]));
+    consumer_sync();
+  }
+  int s = 0;
+  bool from_xs = true;
+  for (int l = 0; l < p.Lt; ++l) {
+    const LayerDev& L = sm->lay[l];
+    phase_qkv<WT>(c, p.Dt, 1, s, from_xs);
+    from_xs = false;
+    phase_talker_attn<WT, KT>(c, l);
+    phase_talker_oproj<WT>(c, 1 - s);
+    phase_ffn<WT>(c, L, p.Dt, p.Ft, 1, 1 - s);
+    s = 1 - s;
+  }
+  // final norm -> pending hidden (CTA slice) and codec head rows -> pending logits
+  load_norm<WT>(c, SRC_SETS, s, 0, 1, p.Dt, reinterpret_cast<const WT*>(sm->fin) + p.Dc, false,
+                p.pending_h + (size_t)p.sid * p.Dt);
+  {
+    int lo, hi;
+    split(p.Vt, p.ncta, c.cta, lo, hi);
+    float* xs = sm->u.xs;
+    float* out = p.pending_logits + (size_t)p.sid * p.Vt;
+    gemv_rows<WT>(
+        c, lo, hi, p.Dt, 1, [&](int, int) { return xs; }, [&](int row, int, float v) { out[row] = v; });
+  }
+  if (c.cta == 0 && c.tid == 0) p.history[(size_t)p.sid * p.Vt + fed0] = 1;
+  consumer_sync();
+  if (c.tid == 0) {
+    __threadfence();
+    if (atomicAdd(p.done, 1u) == (unsigned)p.ncta - 1) {
+      *p.bar = 0u;
+      *p.done = 0u;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- producer
+
+template <class WT>
+struct Producer {
+  const FKParams& p;
+  FKSmem* sm;
+  int cta;
+  uint32_t n = 0;
+  bool stop = false;
+  uint64_t pol;
+
+  __device__ Producer(const FKParams& pp, FKSmem* s, int c) : p(pp), sm(s), cta(c) {
+    pol = l2_evict_first_policy();
+  }
+
+  __device__ void issue(const void* src, unsigned bytes) {
+    if (stop) return;
+    const int s = n % FK_NSTAGE;
+    if (n >= (uint32_t)FK_NSTAGE) {
+      const unsigned par = ((n / FK_NSTAGE) - 1) & 1u;
+      long long t0 = clock64();
+      unsigned it = 0;
+      while (!mbar_try_wait(&sm->empty[s], par)) {
+        // the ring is full most of the time: sleep between polls so this warp
+        // does not take issue slots from the consumer warps of its scheduler
+        __nanosleep(200);
+        if ((++it & 15u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
+          raise_abort(p, Q3TTS_ERR_TIMEOUT);
+          stop = true;
+          return;
+        }
+      }
+    }
+    mbar_expect_tx(&sm->full[s], bytes);
+    bulk_g2s(sm->ring[s], src, bytes, &sm->full[s], pol);
+    n++;
+  }
+
+  __device__ void rows(const void* base, int r0, int r1, int row_bytes) {
+    const int rpc = rows_per_chunk(row_bytes);
+    for (int r = r0; r < r1; r += rpc)
+      issue((const char*)base + (size_t)r * row_bytes, (unsigned)(min(rpc, r1 - r) * row_bytes));
+  }
+
+  __device__ void split_rows(const void* base, int N, int row_bytes) {
+    int lo, hi;
+    split(N, p.ncta, cta, lo, hi);
+    rows(base, lo, hi, row_bytes);
+  }
+
+  __device__ void ffn(const LayerDev& L, int D, int F) {
+    const int row_bytes = D * (int)sizeof(WT);
+    const int gpr = min(64, rows_per_chunk(row_bytes));
+    int f0, f1;
+    split(F, p.ncta, cta, f0, f1);
+    for (int g = f0; g < f1; g += gpr) {
+      const int ng = min(gpr, f1 - g);
+      rows(L.w_gate, g, g + ng, row_bytes);
+      rows(L.w_up, g, g + ng, row_bytes);
+      rows(L.w_dT, g, g + ng, row_bytes);
+    }
+  }
+
+  int nlayers = 0;  // layers in the frame (15 CodePredictor passes, then the Talker)
+  int layer_i = 0;  // next layer whose weights are streamed
+
+  __device__ const LayerDev& layer_at(int k) const {
+    const int ncp = (Q3TTS_N_CODEBOOKS - 1) * p.Lc;
+    return k < ncp ? sm->lay[p.Lt + k % p.Lc] : sm->lay[k - ncp];
+  }
+
+  // Side block of layer k into slot k & 1 (after the consumers freed it).
+  __device__ void side(int k) {
+    if (stop || k >= nlayers) return;
+    const int slot = k & 1;
+    if (k >= 2) {
+      const unsigned par = ((k >> 1) - 1) & 1u;
+      long long t0 = clock64();
+      unsigned it = 0;
+      while (!mbar_try_wait(&sm->side_empty[slot], par)) {
+        __nanosleep(200);
+        if ((++it & 15u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
+          raise_abort(p, Q3TTS_ERR_TIMEOUT);
+          stop = true;
+          return;
+        }
+      }
+    }
+    const int ncp = (Q3TTS_N_CODEBOOKS - 1) * p.Lc;
+    const int D = k < ncp ? p.Dc : p.Dt;
+    const unsigned bytes = (unsigned)((2 * D + 2 * p.hd) * (int)sizeof(WT));
+    mbar_expect_tx(&sm->side_full[slot], bytes);
+    bulk_g2s(sm->side[slot], layer_at(k).side, bytes, &sm->side_full[slot], pol);
+  }
+
+  __device__ void layer(const LayerDev& L, int D, int F) {
+    const int esz = (int)sizeof(WT);
+    // the next layer's gains go out one layer ahead
+    if (layer_i >= 1) side(layer_i + 1);
+    layer_i++;
+    split_rows(L.w_qkv, p.qkv_rows, D * esz);
+    split_rows(L.w_oT, p.Hq * D, p.hd * esz);
+    ffn(L, D, F);
+  }
+
+  __device__ void run() {
+    const int esz = (int)sizeof(WT);
+    nlayers = (Q3TTS_N_CODEBOOKS - 1) * p.Lc + p.Lt;
+    side(0);
+    side(1);
+    for (int j = 0; j < Q3TTS_N_CODEBOOKS - 1; ++j) {
+      if (p.has_proj) split_rows(p.cp_proj, p.Dc, p.Dt * esz);
+      for (int l = 0; l < p.Lc; ++l) layer(sm->lay[p.Lt + l], p.Dc, p.Fc);
+      split_rows((const char*)p.cp_heads + (size_t)j * p.Vc * p.Dc * esz, p.Vc, p.Dc * esz);
+    }
+    for (int l = 0; l < p.Lt; ++l) layer(sm->lay[l], p.Dt, p.Ft);
+    split_rows(p.t_head, p.Vt, p.Dt * esz);
+    // copies still in flight must land before the CTA may exit
+    for (int k = nlayers - 2; k < nlayers; ++k) {
+      if (k < 0) continue;
+      long long t0 = clock64();
+      while (!mbar_try_wait(&sm->side_full[k & 1], (k >> 1) & 1u))
+        if (clock64() - t0 > FK_WAIT_CYCLES) break;
+    }
+    const uint32_t first = n > (uint32_t)FK_NSTAGE ? n - FK_NSTAGE : 0;
+    for (uint32_t m = first; m < n; ++m) {
+      long long t0 = clock64();
+      while (!mbar_try_wait(&sm->full[m % FK_NSTAGE], (m / FK_NSTAGE) & 1u))
+        if (clock64() - t0 > FK_WAIT_CYCLES) break;
+    }
+  }
+};
+
+template <class WT, class KT>
+__global__ void __launch_bounds__(FK_THREADS, 1) frame_kernel(const __grid_constant__ FKParams p) {
+  extern __shared__ __align__(128) unsigned char fk_smem_raw[];
+  FKSmem* sm = reinterpret_cast<FKSmem*>(fk_smem_raw);
+  if (threadIdx.x == 0) sm->prm = p;
+  for (int i = threadIdx.x; i < p.Lt + p.Lc; i += blockDim.x)
+    sm->lay[i] = i < p.Lt ? p.tl[i] : p.cl[i - p.Lt];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < FK_NSTAGE; ++s) {
+      mbar_init(&sm->full[s], 1);
+      mbar_init(&sm->empty[s], FK_CONSUMER_WARPS);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm->side_full[s], 1);
+      mbar_init(&sm->side_empty[s], 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x < FK_PRODUCER_THREADS) {
+    if (threadIdx.x == 0) {
+      Producer<WT> pr(sm->prm, sm, blockIdx.x);
+      pr.run();
+    }
+    return;
+  }
+  consumer<WT, KT>(sm->prm, sm);
+}
+
+// ------------------------------------------------------------- host side
+
+template <class T>
+__global__ void repack_oT_kernel(const T* __restrict__ w_o, T* __restrict__ w_oT, int D, int Hq, int hd) {
+  // w_oT[h][c][d] = w_o[c][h*hd + d]
+  const size_t n = (size_t)Hq * D * hd;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
+    const size_t d = e % hd, c = (e / hd) % D, h = e / ((size_t)hd * D);
+    w_oT[e] = w_o[c * (size_t)Hq * hd + h * hd + d];
+  }
+}
+
+template <class T>
+__global__ void transpose_kernel(const T* __restrict__ in, T* __restrict__ out, int rows, int cols) {
+  // out[c][r] = in[r][c]
+  __shared__ T tile[32][33];
+  for (int r0 = blockIdx.y * 32; r0 < rows; r0 += gridDim.y * 32)
+    for (int c0 = blockIdx.x * 32; c0 < cols; c0 += gridDim.x * 32) {
+      for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int r = r0 + i, cc = c0 + threadIdx.x;
+        if (r < rows && cc < cols) tile[i][threadIdx.x] = in[(size_t)r * cols + cc];
+      }
+      __syncthreads();
+      for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int cc = c0 + i, r = r0 + threadIdx.x;
+        if (r < rows && cc < cols) out[(size_t)cc * rows + r] = tile[threadIdx.x][i];
+      }
+      __syncthreads();
+    }
+}
+
+static size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static size_t fk_layout(const q3tts_config& c, int ncta, FKState* st, char* base) {
+  const int esz = c.weight_dtype == Q3TTS_F32 ? 4 : 2;
+  const int Hq = c.n_q_heads, hd = c.head_dim, Hkv = c.n_kv_heads;
+  const int dmax = std::max(c.talker_hidden, c.cp_hidden);
+  const int qkv_rows = (Hq + 2 * Hkv) * hd;
+  const int cpg = std::max(1, ncta / Hkv);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = al256(off + bytes);
+    return base ? base + o : nullptr;
+  };
+  char* reT = take((size_t)c.talker_layers * ((size_t)Hq * hd * c.talker_hidden + (size_t)c.talker_ffn * c.talker_hidden) * esz);
+  char* reC = take((size_t)c.cp_layers * ((size_t)Hq * hd * c.cp_hidden + (size_t)c.cp_ffn * c.cp_hidden) * esz);
+  char* sideT = take((size_t)c.talker_layers * (2 * c.talker_hidden + 2 * hd) * esz);
+  char* sideC = take((size_t)c.cp_layers * (2 * c.cp_hidden + 2 * hd) * esz);
+  char* tl = take(sizeof(LayerDev) * c.talker_layers);
+  char* cl = take(sizeof(LayerDev) * c.cp_layers);
+  char* R = take(sizeof(float) * 2 * FK_TMAX * dmax);
+  char* dA = take(sizeof(float) * 2 * FK_TMAX * dmax);
+  char* dF = take(sizeof(float) * 2 * FK_TMAX * dmax);
+  char* qkv = take(sizeof(float) * FK_TMAX * qkv_rows);
+  char* part = take(sizeof(float) * (size_t)Hq * cpg * (hd + 2));
+  char* lg = take(sizeof(float) * c.cp_vocab);
+  char* xsum = take(sizeof(float) * c.talker_hidden);
+  char* sync = take(sizeof(unsigned) * 4);
+  if (st) {
+    st->base = base;
+    st->tl = (LayerDev*)tl;
+    st->cl = (LayerDev*)cl;
+    st->R = (float*)R; st->dA = (float*)dA; st->dF = (float*)dF;
+    st->qkv = (float*)qkv; st->part = (float*)part; st->cp_logits = (float*)lg; st->xsum = (float*)xsum;
+    st->bar = (unsigned*)sync;
+    st->done = st->bar + 1;
+    st->abort_flag = (int*)(st->bar + 2);
+    st->dmax = dmax;
+    st->sideT = sideT;
+    st->sideC = sideC;
+    (void)reT; (void)reC;
+  }
+  return off;
+}
+
+size_t frame_kernel_workspace(const q3tts_config& c, int) { return fk_layout(c, FK_MAXCTA, nullptr, nullptr) + 256; }
+
+template <class WT, class KT>
+static void* kernel_ptr() {
+  return (void*)frame_kernel<WT, KT>;
+}
+
+static void* pick_kernel(int wdt, int kdt) {
+  if (wdt == Q3TTS_BF16) return kdt == Q3TTS_BF16 ? kernel_ptr<bf16, bf16>() : kernel_ptr<bf16, float>();
+  return kdt == Q3TTS_BF16 ? kernel_ptr<float, bf16>() : kernel_ptr<float, float>();
+}
+
+int frame_kernel_create(q3tts_handle* h) {
+  FrameKernelState* st = new (std::nothrow) FrameKernelState();
+  if (!st) return Q3TTS_ERR_ARG;
+  st->ok = false;
+  h->fk = st;
+  const q3tts_config& c = h->c;
+  // eligibility: shapes the kernel's shared-memory layout covers
+  if (c.talker_hidden > FK_DMAX || c.cp_hidden > FK_DMAX || c.head_dim > FK_HDMAX ||
+      c.talker_layers + c.cp_layers > FK_MAXLAYERS ||
+      c.n_q_heads / c.n_kv_heads > FK_REPMAX || c.codec_vocab > SAMPLER_VMAX ||
+      c.cp_vocab > SAMPLER_VMAX || (c.talker_hidden % 4) || (c.cp_hidden % 4))
+    return Q3TTS_OK;
+  const int ncta = std::min(h->n_sm, FK_MAXCTA);
+  // every CTA's o_proj column range must touch at most two heads
+  if (ncta < c.n_kv_heads || ncta < c.n_q_heads) return Q3TTS_OK;
+  // the per-CTA FFN slice must fit the gate/up scratch of one group (<= 64 rows)
+  st->smem = sizeof(FKSmem);
+  void* k = pick_kernel(c.weight_dtype, c.kv_dtype);
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st->smem) != cudaSuccess) {
+    cudaGetLastError();
+    return Q3TTS_OK;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, FK_THREADS, st->smem) != cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    return Q3TTS_OK;
+  }
+  int coop = 0;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->dev);
+  if (!coop) return Q3TTS_OK;
+  st->ncta = ncta;
+  char* base = (char*)h->fk_base;  // workspace tail reserved by frame_kernel_workspace
+  fk_layout(c, ncta, st, base);
+  // re-laid-out weights
+  const int esz = c.weight_dtype == Q3TTS_F32 ? 4 : 2;
+  const int Hq = c.n_q_heads, hd = c.head_dim;
+  std::vector<LayerDev> tl(c.talker_layers), cl(c.cp_layers);
+  char* re = base;
+  auto fill = [&](const q3tts_layer_weights& w, LayerDev& d, int D, int F, char* side) -> bool {
+    const size_t gd = (size_t)D * esz, gh = (size_t)hd * esz;
+    if (cudaMemcpyAsync(side, w.g_attn_norm, gd, cudaMemcpyDeviceToDevice, h->s) != cudaSuccess ||
+        cudaMemcpyAsync(side + gd, w.g_ffn_norm, gd, cudaMemcpyDeviceToDevice, h->s) != cudaSuccess ||
+        (w.g_q_norm && cudaMemcpyAsync(side + 2 * gd, w.g_q_norm, gh, cudaMemcpyDeviceToDevice, h->s) != cudaSuccess) ||
+        (w.g_k_norm && cudaMemcpyAsync(side + 2 * gd + gh, w.g_k_norm, gh, cudaMemcpyDeviceToDevice, h->s) != cudaSuccess))
+      return false;
+    d.side = side;
+    d.w_qkv = w.w_qkv;
+    d.w_gate = w.w_gateup;
+    d.w_up = (const char*)w.w_gateup + (size_t)F * D * esz;
+    d.g_attn = w.g_attn_norm;
+    d.g_ffn = w.g_ffn_norm;
+    d.g_q = w.g_q_norm;
+    d.g_k = w.g_k_norm;
+    char* oT = re;
+    re += (size_t)Hq * hd * D * esz;
+    char* dT = re;
+    re += (size_t)F * D * esz;
+    d.w_oT = oT;
+    d.w_dT = dT;
+    dim3 tb(32, 8), tg((F + 31) / 32 < 1024 ? (F + 31) / 32 : 1024, (D + 31) / 32 < 1024 ? (D + 31) / 32 : 1024);
+    if (esz == 2) {
+      repack_oT_kernel<bf16><<<1024, 256, 0, h->s>>>((const bf16*)w.w_o, (bf16*)oT, D, Hq, hd);
+      transpose_kernel<bf16><<<tg, tb, 0, h->s>>>((const bf16*)w.w_down, (bf16*)dT, D, F);
+    } else {
+      repack_oT_kernel<float><<<1024, 256, 0, h->s>>>((const float*)w.w_o, (float*)oT, D, Hq, hd);
+      transpose_kernel<float><<<tg, tb, 0, h->s>>>((const float*)w.w_down, (float*)dT, D, F);
+    }
+    return cudaGetLastError() == cudaSuccess;
+  };
+  for (int l = 0; l < c.talker_layers; ++l)
+    if (!fill(h->tl[l], tl[l], c.talker_hidden, c.talker_ffn,
+              st->sideT + (size_t)l * (2 * c.talker_hidden + 2 * hd) * esz))
+      return Q3TTS_ERR_CUDA;
+  for (int l = 0; l < c.cp_layers; ++l)
+    if (!fill(h->cl[l], cl[l], c.cp_hidden, c.cp_ffn, st->sideC + (size_t)l * (2 * c.cp_hidden + 2 * hd) * esz))
+      return Q3TTS_ERR_CUDA;
+  if (cudaMemcpyAsync(st->tl, tl.data(), sizeof(LayerDev) * tl.size(), cudaMemcpyHostToDevice, h->s) != cudaSuccess ||
+      cudaMemcpyAsync(st->cl, cl.data(), sizeof(LayerDev) * cl.size(), cudaMemcpyHostToDevice, h->s) != cudaSuccess ||
+      cudaMemsetAsync(st->bar, 0, sizeof(unsigned) * 4, h->s) != cudaSuccess ||
+      cudaStreamSynchronize(h->s) != cudaSuccess)
+    return Q3TTS_ERR_CUDA;
+  st->ok = true;
+  return Q3TTS_OK;
+}
+
+void frame_kernel_destroy(q3tts_handle* h) {
+  delete h->fk;
+  h->fk = nullptr;
+}
+
+static bool sampling_ok(int do_sample, int top_k) {
+  return !do_sample || (top_k >= 1 && top_k <= SAMPLER_KSMALL);
+}
+
+// The persistent kernel takes one stream per launch and draws with top-k
+// within the sampler's small-candidate path (or greedily).
+bool frame_kernel_supports(const q3tts_handle* h, int n_active, const q3tts_sampling* sp) {
+  if (!h->fk || !h->fk->ok || n_active != 1 || h->frame_kernel_off) return false;
+  return sampling_ok(sp[0].do_sample, sp[0].top_k) && sampling_ok(sp[0].sub_do_sample, sp[0].sub_top_k);
+}
+
+int frame_kernel_step(q3tts_handle* h, const StepDesc& d, const float* uniforms, int32_t* codes,
+                      const int32_t* forced, float* logits) {
+  FrameKernelState* st = h->fk;
+  const q3tts_config& c = h->c;
+  FKParams p;
+  p.ncta = st->ncta;
+  p.Dt = c.talker_hidden; p.Dc = c.cp_hidden; p.Ft = c.talker_ffn; p.Fc = c.cp_ffn;
+  p.Hq = c.n_q_heads; p.Hkv = c.n_kv_heads; p.hd = c.head_dim; p.Vt = c.codec_vocab; p.Vc = c.cp_vocab;
+  p.Lt = c.talker_layers; p.Lc = c.cp_layers; p.qkv_rows = h->qkv_rows;
+  p.has_proj = h->w.cp_w_proj != nullptr; p.qk_norm = c.qk_norm; p.dmax = st->dmax; p.eps = c.rms_eps;
+  p.tl = st->tl; p.cl = st->cl;
+  p.t_head = h->w.talker_w_head; p.e_codec = h->w.talker_e_codec; p.cp_heads = h->w.cp_heads;
+  p.cp_embeds = h->w.cp_embeds; p.cp_proj = h->w.cp_w_proj; p.t_gfinal = h->w.talker_g_final;
+  p.cp_gfinal = h->w.cp_g_final;
+  p.pending_h = h->pending_h; p.pending_logits = h->pending_logits; p.history = h->history;
+  p.tkv = talker_kv(h); p.ckv = cp_kv(h); p.rope_cos = h->rope_cos; p.rope_sin = h->rope_sin;
+  p.R = st->R; p.dA = st->dA; p.dF = st->dF; p.qkv = st->qkv; p.part = st->part;
+  p.cp_logits = st->cp_logits; p.xsum = st->xsum;
+  p.bar = st->bar; p.done = st->done; p.err = h->d_err; p.abort_flag = st->abort_flag;
+  p.sid = d.sid[0]; p.pos = d.pos[0]; p.newpage = d.newpage[0]; p.sp = d.sp[0];
+  p.uniforms = uniforms; p.codes = codes; p.forced = forced; p.dump = logits;
+  void* args[] = {&p};
+  cudaError_t e = cudaLaunchCooperativeKernel(pick_kernel(c.weight_dtype, c.kv_dtype), dim3(st->ncta),
+                                              dim3(FK_THREADS), args, st->smem, h->s);
+  h->launches += 1;
+  return e == cudaSuccess ? Q3TTS_OK : Q3TTS_ERR_CUDA;
+}
+
+// After a device-side error: clear the barrier counters and the abort flag.
+int frame_kernel_recover(q3tts_handle* h) {
+  if (!h->fk || !h->fk->ok) return Q3TTS_OK;
+  return cudaMemsetAsync(h->fk->bar, 0, sizeof(unsigned) * 4, h->s) == cudaSuccess ? Q3TTS_OK
+                                                                                   : Q3TTS_ERR_CUDA;
+}
+
 }  // namespace q3

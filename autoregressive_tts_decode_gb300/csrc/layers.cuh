@@ -12,7 +12,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
-#include "../../include/q3tts.h"
+#include "q3tts.h"
 
 namespace q3 {
 

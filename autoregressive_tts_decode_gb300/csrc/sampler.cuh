@@ -15,7 +15,8 @@
 //   7. Z = running float sum of kept w, t = u * Z, pick the first id whose
 //      running sum > t, else the last kept id.
 // Selection (step 4) uses a radix select on order-preserving keys when k is
-// small and a bitonic sort of all ids otherwise.
+// small (ties at the k-th value resolved by lowest index) and a bitonic sort of
+// all ids otherwise.
 #pragma once
 
 #include "common.cuh"
@@ -24,7 +25,6 @@ namespace q3 {
 
 constexpr int SAMPLER_VMAX = 4096;  // largest vocabulary the block sampler takes
 constexpr int SAMPLER_KSMALL = 64;  // top-k handled by radix select + warp sort
-constexpr int SAMPLER_TIE_CAP = 256;
 
 // exp(x) for x <= 0 in float, from the Cody-Waite method (Cody and Waite,
 // "Software Manual for the Elementary Functions", 1980): k = rint(x log2 e),
@@ -61,22 +61,44 @@ struct SamplerSmem {
   uint32_t hist[256];
   float w[SAMPLER_VMAX];
   int cand[SAMPLER_VMAX];
-  int ties[SAMPLER_TIE_CAP];
-  float red[32];
-  int ired[32];
-  int n_gt, n_eq, remaining, pick, kept;
+  int wsum[32];
+  int n_gt, remaining, pick;
   uint32_t prefix;
+  static constexpr bool kFullSort = true;
 };
 
 __device__ __forceinline__ unsigned long long skey(float v, int i) {
   return ((unsigned long long)fkey(v) << 32) | (unsigned long long)(0xffffffffu - (uint32_t)i);
 }
 
+// Sampler scratch for callers that only take greedy or 1 <= top_k <= 64
+// (the persistent frame kernel): the logits plus 64-entry candidate arrays.
+struct SamplerSmemSmall {
+  float val[SAMPLER_VMAX];
+  unsigned long long sortkey[SAMPLER_KSMALL];
+  uint32_t hist[256];
+  float w[SAMPLER_KSMALL];
+  int cand[SAMPLER_KSMALL];
+  int wsum[32];
+  int n_gt, remaining, pick;
+  uint32_t prefix;
+  static constexpr bool kFullSort = false;  // callers keep top_k within SAMPLER_KSMALL
+};
+
+// Thread-group description for the block sampler: the participating threads
+// (tid in [0, nt)) and their barrier.  BlockGroup is a whole thread block.
+struct BlockGroup {
+  __device__ static int tid() { return threadIdx.x; }
+  __device__ static int nt() { return blockDim.x; }
+  __device__ static void sync() { __syncthreads(); }
+};
+
 // Bitonic sort, descending, of n (power of two) keys in shared memory.
+template <class G>
 __device__ inline void bitonic_desc(unsigned long long* a, int n) {
   for (int k = 2; k <= n; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      for (int i = G::tid(); i < n; i += G::nt()) {
         int ixj = i ^ j;
         if (ixj > i) {
           unsigned long long x = a[i], y = a[ixj];
@@ -84,16 +106,22 @@ __device__ inline void bitonic_desc(unsigned long long* a, int n) {
           if (desc ? (x < y) : (x > y)) { a[i] = y; a[ixj] = x; }
         }
       }
-      __syncthreads();
+      G::sync();
     }
   }
 }
 
-// Block-wide sample over sm.val[0..V) (already holding the logits).  All threads
-// of the block must call it; returns the token to every thread.
-__device__ inline int block_sample(SamplerSmem& sm, int V, int do_sample, int top_k, float top_p,
+template <class G, class SM>
+__device__ inline void full_sort(SM& sm, int V);
+
+// Group-wide sample over sm.val[0..V) (already holding the logits).  Every
+// thread of the group must call it; returns the token to all of them.  With
+// full_sort == false the caller guarantees 1 <= top_k <= SAMPLER_KSMALL (or
+// greedy), so sortkey/w/cand need only SAMPLER_KSMALL entries.
+template <class G, class SM>
+__device__ inline int group_sample(SM& sm, int V, int do_sample, int top_k, float top_p,
                                    float temperature, float rep, const uint8_t* history, float u) {
-  const int tid = threadIdx.x, nt = blockDim.x;
+  const int tid = G::tid(), nt = G::nt();
   if (history != nullptr && rep != 1.0f) {
     for (int i = tid; i < V; i += nt)
       if (history[i]) {
@@ -101,7 +129,7 @@ __device__ inline int block_sample(SamplerSmem& sm, int V, int do_sample, int to
         sm.val[i] = l > 0.0f ? __fdiv_rn(l, rep) : __fmul_rn(l, rep);
       }
   }
-  __syncthreads();
+  G::sync();
   if (!do_sample) {
     // argmax with lowest index on ties: max over (fkey, ~index)
     unsigned long long best = 0ull;
@@ -114,91 +142,119 @@ __device__ inline int block_sample(SamplerSmem& sm, int V, int do_sample, int to
       unsigned long long t = __shfl_xor_sync(0xffffffffu, best, o);
       best = t > best ? t : best;
     }
-    __syncthreads();
+    G::sync();
     if ((tid & 31) == 0) sm.sortkey[tid >> 5] = best;
-    __syncthreads();
+    G::sync();
     if (tid == 0) {
       unsigned long long b = 0ull;
       for (int w = 0; w < (nt + 31) / 32; ++w) b = sm.sortkey[w] > b ? sm.sortkey[w] : b;
       sm.pick = (int)(0xffffffffu - (uint32_t)(b & 0xffffffffull));
     }
-    __syncthreads();
+    G::sync();
     return sm.pick;
   }
   for (int i = tid; i < V; i += nt) sm.val[i] = __fdiv_rn(sm.val[i], temperature);
-  __syncthreads();
+  G::sync();
   const int K = (top_k <= 0 || top_k >= V) ? V : top_k;
-  bool small = K <= SAMPLER_KSMALL;
+  const bool small = K <= SAMPLER_KSMALL;
   if (small) {
     // radix select of the K-th largest key, 8 bits at a time
     if (tid == 0) { sm.prefix = 0u; sm.remaining = K; }
     uint32_t mask = 0u;
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int b = tid; b < 256; b += nt) sm.hist[b] = 0u;
-      __syncthreads();
+      G::sync();
       uint32_t prefix = sm.prefix;
       for (int i = tid; i < V; i += nt) {
         uint32_t k = fkey(sm.val[i]);
         if ((k & mask) == prefix) atomicAdd(&sm.hist[(k >> shift) & 0xffu], 1u);
       }
-      __syncthreads();
-      if (tid == 0) {
-        int rem = sm.remaining;
-        uint32_t cum = 0;
-        int b = 255;
-        for (; b > 0; --b) {
-          if (cum + sm.hist[b] >= (uint32_t)rem) break;
-          cum += sm.hist[b];
+      G::sync();
+      if (tid < 32) {
+        // warp 0: lane l holds bins 255-8l .. 248-8l (descending); find the bin
+        // where the running count from the top reaches `remaining`
+        const int rem = sm.remaining;
+        uint32_t c[8], tot = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) { c[q] = sm.hist[255 - 8 * tid - q]; tot += c[q]; }
+        uint32_t incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (tid >= o) incl += t;
         }
-        sm.remaining = rem - (int)cum;
-        sm.prefix = prefix | ((uint32_t)b << shift);
+        const uint32_t excl = incl - tot;
+        const bool mine = excl < (uint32_t)rem && incl >= (uint32_t)rem;
+        if (mine) {
+          uint32_t cum = excl;
+          int q = 0;
+          for (; q < 7; ++q) {
+            if (cum + c[q] >= (uint32_t)rem) break;
+            cum += c[q];
+          }
+          sm.remaining = rem - (int)cum;
+          sm.prefix = prefix | ((uint32_t)(255 - 8 * tid - q) << shift);
+        }
       }
       mask |= 0xffu << shift;
-      __syncthreads();
+      G::sync();
     }
-    // gather: keys above the K-th all go in; equal keys by lowest index
-    if (tid == 0) { sm.n_gt = 0; sm.n_eq = 0; }
-    __syncthreads();
+    // gather: keys above the K-th all go in (any order; sorted below); of the
+    // keys equal to the K-th, the `remaining` lowest indices, found with an
+    // ordered count over contiguous index ranges so any number of ties works.
+    if (tid == 0) sm.n_gt = 0;
+    G::sync();
     const uint32_t kth = sm.prefix;
-    for (int i = tid; i < V; i += nt) {
+    const int rem = sm.remaining;
+    const int per = (V + nt - 1) / nt, lo = tid * per, hi = min(V, lo + per);
+    int my_eq = 0;
+    for (int i = lo; i < hi; ++i) {
       uint32_t k = fkey(sm.val[i]);
       if (k > kth) {
         int slot = atomicAdd(&sm.n_gt, 1);
         sm.sortkey[slot] = skey(sm.val[i], i);
       } else if (k == kth) {
-        int slot = atomicAdd(&sm.n_eq, 1);
-        if (slot < SAMPLER_TIE_CAP) sm.ties[slot] = i;
+        ++my_eq;
       }
     }
-    __syncthreads();
-    if (sm.n_eq > SAMPLER_TIE_CAP) {
-      small = false;  // pathological ties: fall back to the full sort
-    } else {
-      // ties: the `remaining` lowest indices, each appended after the n_gt keys
-      const int n_gt = sm.n_gt, n_eq = sm.n_eq, rem = sm.remaining;
-      for (int t = tid; t < n_eq; t += nt) {
-        int idx = sm.ties[t], rank = 0;
-        for (int s = 0; s < n_eq; ++s) rank += sm.ties[s] < idx;
-        if (rank < rem) sm.sortkey[n_gt + rank] = skey(sm.val[idx], idx);
-      }
-      for (int t = n_gt + rem + tid; t < SAMPLER_KSMALL; t += nt) sm.sortkey[t] = 0ull;
-      __syncthreads();
-      bitonic_desc(sm.sortkey, SAMPLER_KSMALL);
+    // exclusive prefix of my_eq over threads in index order
+    int incl = my_eq;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if ((tid & 31) >= o) incl += t;
     }
+    if ((tid & 31) == 31) sm.wsum[tid >> 5] = incl;
+    G::sync();
+    if (tid < 32) {
+      int v = tid < (nt + 31) / 32 ? sm.wsum[tid] : 0, vi = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, vi, o);
+        if (tid >= o) vi += t;
+      }
+      sm.wsum[tid] = vi - v;  // exclusive over warps
+    }
+    G::sync();
+    int rank = sm.wsum[tid >> 5] + incl - my_eq;
+    const int n_gt = K - rem;
+    for (int i = lo; i < hi && rank < rem; ++i)
+      if (fkey(sm.val[i]) == kth) sm.sortkey[n_gt + rank++] = skey(sm.val[i], i);
+    for (int t = K + tid; t < SAMPLER_KSMALL; t += nt) sm.sortkey[t] = 0ull;
+    G::sync();
+    bitonic_desc<G>(sm.sortkey, SAMPLER_KSMALL);
   }
   if (!small) {
     int n2 = 1;
     while (n2 < V) n2 <<= 1;
-    for (int i = tid; i < n2; i += nt) sm.sortkey[i] = i < V ? skey(sm.val[i], i) : 0ull;
-    __syncthreads();
-    bitonic_desc(sm.sortkey, n2);
+    full_sort<G>(sm, V);
   }
   // sorted candidates: index = ~low32, value from val[]
   for (int i = tid; i < K; i += nt) sm.cand[i] = (int)(0xffffffffu - (uint32_t)(sm.sortkey[i] & 0xffffffffull));
-  __syncthreads();
+  G::sync();
   const float m = sm.val[sm.cand[0]];
   for (int i = tid; i < K; i += nt) sm.w[i] = exp_cw(__fsub_rn(sm.val[sm.cand[i]], m));
-  __syncthreads();
+  G::sync();
   if (tid == 0) {
     int kept = K;
     if (top_p < 1.0f) {
@@ -220,8 +276,204 @@ __device__ inline int block_sample(SamplerSmem& sm, int V, int do_sample, int to
     }
     sm.pick = pick;
   }
-  __syncthreads();
+  G::sync();
   return sm.pick;
+}
+
+template <class G, class SM>
+__device__ inline void full_sort(SM& sm, int V) {
+  int n2 = 1;
+  while (n2 < V) n2 <<= 1;
+  for (int i = G::tid(); i < n2; i += G::nt()) sm.sortkey[i] = i < V ? skey(sm.val[i], i) : 0ull;
+  G::sync();
+  bitonic_desc<G>(sm.sortkey, n2);
+}
+
+__device__ inline int block_sample(SamplerSmem& sm, int V, int do_sample, int top_k, float top_p,
+                                   float temperature, float rep, const uint8_t* history, float u) {
+  return group_sample<BlockGroup>(sm, V, do_sample, top_k, top_p, temperature, rep, history, u);
+}
+
+}  // namespace q3
+
+namespace q3 {
+
+// ---------------------------------------------------------------------------
+// Register-resident variant of the same rule for greedy or 1 <= k <= 64, run
+// by a group of 256 threads (8 warps).  Warp w owns indices [w*V8, (w+1)*V8),
+// 16 per lane, as 64-bit keys (order-preserving value key, inverted index):
+// each warp sorts its 512 keys with a shuffle bitonic network and keeps its
+// top 64; warp 0 sorts the 8 x 64 survivors and draws from the first k.
+// Keys are distinct (they carry the index), so the order is exactly
+// (value desc, index asc).  Same float operations as group_sample.
+constexpr int FAST_NT = 256;
+constexpr int FAST_VPT = SAMPLER_VMAX / FAST_NT;  // 16 logits per thread at most
+
+struct FastSamplerSmem {
+  unsigned long long cand[SAMPLER_KSMALL];
+  unsigned long long sorted[SAMPLER_KSMALL];
+  float w[SAMPLER_KSMALL];
+  int wc[2][FAST_NT / 32];
+  int wscan[FAST_NT / 32];
+  unsigned long long wbest[FAST_NT / 32];
+  int n_gt, pick;
+};
+
+__device__ __forceinline__ float key_value(unsigned long long k) {
+  const uint32_t f = (uint32_t)(k >> 32);
+  const uint32_t bits = (f & 0x80000000u) ? (f & 0x7fffffffu) : ~f;
+  return __uint_as_float(bits);
+}
+
+__device__ __forceinline__ int key_index(unsigned long long k) {
+  return (int)(0xffffffffu - (uint32_t)(k & 0xffffffffull));
+}
+
+// Group-wide sum of one int per thread; `slot` alternates between calls so a
+// single barrier suffices.
+template <class G>
+__device__ __forceinline__ int group_count(FastSamplerSmem& sm, int v, int slot) {
+  const int lane = G::tid() & 31, warp = G::tid() >> 5;
+  v = __reduce_add_sync(0xffffffffu, v);
+  if (lane == 0) sm.wc[slot][warp] = v;
+  G::sync();
+  int tot = 0;
+  for (int w = 0; w < FAST_NT / 32; ++w) tot += sm.wc[slot][w];
+  return tot;
+}
+
+// Compact variant of the same rule for greedy or 1 <= k <= 64, run by a group
+// of 256 threads: thread t keeps logits [16t, 16t + 16) in registers; the k-th
+// largest order-preserving key is found by bisection over its 32 bits (one
+// group count per bit), ties at that key go to the lowest indices (threads own
+// contiguous index ranges, so an exclusive count over threads orders them),
+// the k candidates are placed by rank, and thread 0 draws.  Loops stay rolled
+// to keep the code small.  Same float operations as group_sample.
+template <class G>
+__device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits, int V, int do_sample,
+                                        int top_k, float top_p, float temperature, float rep,
+                                        const uint8_t* history, float u) {
+  const int tid = G::tid(), lane = tid & 31, warp = tid >> 5;
+  const int per = (V + FAST_NT - 1) / FAST_NT;
+  const int i0 = tid * per;
+  float v[FAST_VPT];
+#pragma unroll
+  for (int r = 0; r < FAST_VPT; ++r) {
+    const int i = i0 + r;
+    v[r] = (r < per && i < V) ? __ldcg(logits + i) : 0.f;
+  }
+  if (history != nullptr && rep != 1.0f) {
+#pragma unroll
+    for (int r = 0; r < FAST_VPT; ++r) {
+      const int i = i0 + r;
+      if (r < per && i < V && history[i]) v[r] = v[r] > 0.0f ? __fdiv_rn(v[r], rep) : __fmul_rn(v[r], rep);
+    }
+  }
+  if (!do_sample) {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int r = 0; r < FAST_VPT; ++r) {
+      const int i = i0 + r;
+      if (r < per && i < V) {
+        const unsigned long long k = skey(v[r], i);
+        best = k > best ? k : best;
+      }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long t = __shfl_xor_sync(0xffffffffu, best, o);
+      best = t > best ? t : best;
+    }
+    if (lane == 0) sm.wbest[warp] = best;
+    G::sync();
+    unsigned long long b = 0ull;
+    for (int w = 0; w < FAST_NT / 32; ++w) b = sm.wbest[w] > b ? sm.wbest[w] : b;
+    G::sync();
+    return key_index(b);
+  }
+  uint32_t key[FAST_VPT];
+#pragma unroll
+  for (int r = 0; r < FAST_VPT; ++r) {
+    const int i = i0 + r;
+    // 0 is below the key of every float, so padding never counts
+    key[r] = (r < per && i < V) ? fkey(__fdiv_rn(v[r], temperature)) : 0u;
+  }
+  const int K = (top_k <= 0 || top_k >= V) ? V : top_k;  // caller: K <= SAMPLER_KSMALL
+  // bisection: the largest t with count(key >= t) >= K is the K-th largest key
+  uint32_t t = 0u;
+  for (int b = 31; b >= 0; --b) {
+    const uint32_t cand = t | (1u << b);
+    int cnt = 0;
+#pragma unroll
+    for (int r = 0; r < FAST_VPT; ++r) cnt += key[r] >= cand ? 1 : 0;
+    if (group_count<G>(sm, cnt, b & 1) >= K) t = cand;
+  }
+  int n_gt = 0, n_eq = 0;
+#pragma unroll
+  for (int r = 0; r < FAST_VPT; ++r) {
+    n_gt += key[r] > t ? 1 : 0;
+    n_eq += (key[r] == t && key[r] != 0u) ? 1 : 0;
+  }
+  // ties before this thread's (lower indices): warp scan + warp totals
+  int incl = n_eq;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) sm.wscan[warp] = incl;
+  if (tid == 0) sm.n_gt = 0;
+  const int above = group_count<G>(sm, n_gt, 1);  // keys above t (fewer than K)
+  int before = incl - n_eq;
+  for (int w = 0; w < warp; ++w) before += sm.wscan[w];
+  // keys above t take any of the first `above` slots; ties take slot
+  // above + (rank among ties) while that is below K
+#pragma unroll
+  for (int r = 0; r < FAST_VPT; ++r) {
+    const int i = i0 + r;
+    if (key[r] > t) {
+      sm.cand[atomicAdd(&sm.n_gt, 1)] = ((unsigned long long)key[r] << 32) | (0xffffffffu - (uint32_t)i);
+    } else if (key[r] == t && key[r] != 0u) {
+      if (above + before < K)
+        sm.cand[above + before] = ((unsigned long long)key[r] << 32) | (0xffffffffu - (uint32_t)i);
+      ++before;
+    }
+  }
+  G::sync();
+  if (tid < K) {
+    const unsigned long long my = sm.cand[tid];
+    int rank = 0;
+    for (int j = 0; j < K; ++j) rank += sm.cand[j] > my ? 1 : 0;
+    sm.sorted[rank] = my;
+  }
+  G::sync();
+  if (tid < K) sm.w[tid] = exp_cw(__fsub_rn(key_value(sm.sorted[tid]), key_value(sm.sorted[0])));
+  G::sync();
+  if (tid == 0) {
+    int kept = K;
+    if (top_p < 1.0f) {
+      float z = 0.0f;
+      for (int i = 0; i < K; ++i) z = __fadd_rn(z, sm.w[i]);
+      const float tp = __fmul_rn(top_p, z);
+      float run = 0.0f;
+      for (int i = 0; i < K; ++i) {
+        run = __fadd_rn(run, sm.w[i]);
+        if (run >= tp) { kept = i + 1; break; }
+      }
+    }
+    float z = 0.0f;
+    for (int i = 0; i < kept; ++i) z = __fadd_rn(z, sm.w[i]);
+    const float th = __fmul_rn(u, z);
+    float run = 0.0f;
+    int sel = kept - 1;
+    for (int i = 0; i < kept; ++i) {
+      run = __fadd_rn(run, sm.w[i]);
+      if (run > th) { sel = i; break; }
+    }
+    sm.pick = key_index(sm.sorted[sel]);
+  }
+  G::sync();
+  const int pick = sm.pick;
+  G::sync();
+  return pick;
 }
 
 }  // namespace q3

@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(256) sample_kernel(
                                 p.repetition_penalty, hist, uniforms[b * 16 + cb])
                  : block_sample(sm, V, p.sub_do_sample, p.sub_top_k, p.sub_top_p,
                                 p.sub_temperature, 1.0f, nullptr, uniforms[b * 16 + cb]);
+  code = min(max(code, 0), V - 1);
   if (threadIdx.x == 0) {
     codes[b * 16 + cb] = code;
     int f = forced ? forced[b * 16 + cb] : code;

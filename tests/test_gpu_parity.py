@@ -221,3 +221,47 @@ def test_errors_are_status_codes(q3, tiny_weights):
         eng.sync()
     assert e.value.code == q3.ERR_ARG
     eng.sync()
+
+
+def _with_frame_kernel(enabled: bool):
+    import contextlib
+    import os
+
+    @contextlib.contextmanager
+    def cm():
+        old = os.environ.get("Q3TTS_FRAME_KERNEL")
+        os.environ["Q3TTS_FRAME_KERNEL"] = "1" if enabled else "0"
+        try:
+            yield
+        finally:
+            if old is None:
+                del os.environ["Q3TTS_FRAME_KERNEL"]
+            else:
+                os.environ["Q3TTS_FRAME_KERNEL"] = old
+    return cm()
+
+
+@pytest.mark.parametrize("shape_name", ["tiny", "ragged"])
+def test_persistent_kernel_matches_layered_step(q3, shape_name):
+    """Batch-1 frames run as one persistent launch; the same frames through the
+    one-kernel-per-operation step give the same codes and (within fp32
+    reassociation) the same logits."""
+    shape = TINY.shape if shape_name == "tiny" else RAGGED
+    W, Wd = pu.gpu_weights(shape)
+    sp = synth.QWEN_DEFAULT_SAMPLING
+    p = synth.make_prompts(shape, [21])[0]
+    u = synth.uniforms([0], 6)
+    out = {}
+    for fk in (True, False):
+        with _with_frame_kernel(fk):
+            eng = q3.Engine(shape, Wd, max_streams=1, kv_cap=40)
+        eng.prefill(0, p.cuda())
+        eng.sync()
+        l0 = eng.kernel_launches()
+        codes, logits = pu.run_gpu(eng, [0], [p], sp, 6, uniforms=u, prefill=False)
+        out[fk] = (codes, logits, eng.kernel_launches() - l0)
+        eng.close()
+    assert out[True][2] == 6, out[True][2]        # one launch per frame
+    assert out[False][2] > 100 * 6
+    assert np.array_equal(out[True][0], out[False][0])
+    assert np.max(np.abs(out[True][1] - out[False][1])) < 2e-5
