@@ -67,6 +67,7 @@ constexpr long long FK_WAIT_CYCLES = 4000000000ll;  // ~2 s at GB300 clocks
 // copied into a double-buffered shared-memory slot one layer ahead.
 constexpr int FK_SIDE_BYTES = (2 * FK_DMAX + 2 * FK_HDMAX) * 4;
 constexpr int FK_MAXLAYERS = 64;  // Talker + CodePredictor layers held in shared memory
+constexpr int FK_TASKROWS = 64;   // most rows one CTA owns in a row-split GEMV
 
 static_assert(FAST_NT == FK_CONSUMERS, "the register sampler runs on the consumer warps");
 
@@ -222,6 +223,31 @@ __device__ __forceinline__ int plane_first(int p, int K) {
 
 // ------------------------------------------------------------ shared memory
 
+// The block's dynamic shared memory.  Hot loops address it through 32-bit
+// offsets from this array (shared-window loads), not through generic pointers.
+extern __shared__ __align__(128) unsigned char fk_smem_raw[];
+
+__device__ __forceinline__ uint32_t soff(const void* p) {
+  return (uint32_t)((const unsigned char*)p - fk_smem_raw);
+}
+__device__ __forceinline__ float4 lds_f4(uint32_t off) {
+  return *reinterpret_cast<const float4*>(fk_smem_raw + off);
+}
+__device__ __forceinline__ uint4 lds_u4(uint32_t off) {
+  return *reinterpret_cast<const uint4*>(fk_smem_raw + off);
+}
+template <class WT>
+__device__ __forceinline__ void lds_w8(uint32_t off, float* w);
+template <>
+__device__ __forceinline__ void lds_w8<bf16>(uint32_t off, float* w) {
+  unpack_bf16x8(lds_u4(off), w);
+}
+template <>
+__device__ __forceinline__ void lds_w8<float>(uint32_t off, float* w) {
+  const float4 a = lds_f4(off), b = lds_f4(off + 16);
+  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+
 struct AttnScratch {
   float m[FK_CONSUMER_WARPS][FK_PAIRS];
   float l[FK_CONSUMER_WARPS][FK_PAIRS];
@@ -244,6 +270,8 @@ struct FKSmem {
   } u;
   float os[2][FK_TMAX][FK_HDMAX];  // attention outputs of the CTA's (<= 2) heads, plane layout
   float av[2][FK_TMAX][64];        // SwiGLU values of a row group (double-buffered)
+  float gu[2][FK_TMAX][128];       // gate (0..63) and up (64..127) sums of a row group
+  float acc[FK_TMAX][FK_TASKROWS]; // row sums of the current GEMV task
   float red[FK_TMAX][FK_CONSUMER_WARPS];
   float rope_c[17][FK_HDMAX / 2];  // rows 0..15: CodePredictor positions; 16: the Talker position
   float rope_s[17][FK_HDMAX / 2];
@@ -296,6 +324,7 @@ __device__ __forceinline__ const unsigned char* acquire_at(Cons& c, uint32_t n) 
         break;
       }
     }
+    c.aborted = __any_sync(0xffffffffu, c.aborted);  // one decision per warp
   }
   return c.sm->ring[s];
 }
@@ -312,6 +341,7 @@ __device__ __forceinline__ void wait_bar(Cons& c, uint64_t* bar, unsigned par) {
       break;
     }
   }
+  c.aborted = __any_sync(0xffffffffu, c.aborted);  // one decision per warp
 }
 
 // The side block of the layer being started (waits for its copy).
@@ -322,15 +352,20 @@ __device__ __forceinline__ const WT* side_begin(Cons& c) {
   return reinterpret_cast<const WT*>(c.sm->side[slot]);
 }
 
-// Done with the current layer's gains: the slot may be refilled.
+// Done with the current layer's gains: the slot may be refilled (not after an
+// abort, for the reason given at release_n).
 __device__ __forceinline__ void side_end(Cons& c) {
-  if (c.tid == 0) mbar_arrive(&c.sm->side_empty[c.layer & 1]);
+  if (c.tid == 0 && !c.aborted) mbar_arrive(&c.sm->side_empty[c.layer & 1]);
   c.layer++;
 }
 
+// Hands ring slots back to the producer.  After an abort a consumer has
+// stopped waiting for data, so it must not free slots either: the producer then
+// blocks, sees the abort flag and lets its in-flight copies land before the CTA
+// can exit.
 __device__ __forceinline__ void release_n(Cons& c, int count) {
   __syncwarp();
-  if (c.lane == 0)
+  if (c.lane == 0 && !c.aborted)
     for (int i = 0; i < count; ++i) mbar_arrive(&c.sm->empty[(c.n + i) % FK_NSTAGE]);
   c.n += count;
 }
@@ -384,33 +419,29 @@ __device__ __forceinline__ float dot8(const float* w, float4 a, float4 b, float 
   return acc;
 }
 
-// One row of the ring chunk (K weights at w) against T plane-layout vectors;
-// G lanes share the row (lane sl covers k = 8 sl + 8 G i); full-warp reduce
-// over the G-lane group.  All 32 lanes must call it.
+// One row of the ring chunk (K weights at shared offset w) against T
+// plane-layout vectors at shared offsets x0, x1; G lanes share the row (lane sl
+// covers k = 8 sl + 8 G i); reduction over the G-lane group.  All 32 lanes
+// must call it.
 template <class WT>
-__device__ __forceinline__ void row_dot(const WT* w, int K, int G, int sl, bool valid, const float* x0,
-                                        const float* x1, int T, float& r0, float& r1) {
+__device__ __forceinline__ void row_dot(uint32_t w, int K, int G, int sl, bool valid, uint32_t x0,
+                                        uint32_t x1, int T, float& r0, float& r1) {
   float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
   if (valid) {
-    const float4* p0 = reinterpret_cast<const float4*>(x0);
-    const float4* q0 = reinterpret_cast<const float4*>(x0 + (K >> 1));
-    const float4* p1 = reinterpret_cast<const float4*>(x1);
-    const float4* q1 = reinterpret_cast<const float4*>(x1 + (K >> 1));
-    int k = sl * 8;
-#pragma unroll 2
-    for (; k < K; k += G * 8) {
+    uint32_t wo = w + (uint32_t)(sl * 8 * (int)sizeof(WT));
+    uint32_t xa = x0 + (uint32_t)sl * 16u, xb = xa + (uint32_t)K * 2u;
+    uint32_t ya = x1 + (uint32_t)sl * 16u, yb = ya + (uint32_t)K * 2u;
+    const uint32_t wstep = (uint32_t)(G * 8 * (int)sizeof(WT)), xstep = (uint32_t)G * 16u;
+    for (int k = sl * 8; k < K; k += G * 8, wo += wstep, xa += xstep, xb += xstep, ya += xstep, yb += xstep) {
       float wv[8];
-      ld8_smem<WT>(w + k, wv);
-      const int j = k >> 3;
-      a0 = fmaf(wv[0], p0[j].x, a0); a0 = fmaf(wv[1], p0[j].y, a0);
-      a0 = fmaf(wv[2], p0[j].z, a0); a0 = fmaf(wv[3], p0[j].w, a0);
-      b0 = fmaf(wv[4], q0[j].x, b0); b0 = fmaf(wv[5], q0[j].y, b0);
-      b0 = fmaf(wv[6], q0[j].z, b0); b0 = fmaf(wv[7], q0[j].w, b0);
+      lds_w8<WT>(wo, wv);
+      const float4 p = lds_f4(xa), q = lds_f4(xb);
+      a0 = fmaf(wv[0], p.x, a0); a0 = fmaf(wv[1], p.y, a0); a0 = fmaf(wv[2], p.z, a0); a0 = fmaf(wv[3], p.w, a0);
+      b0 = fmaf(wv[4], q.x, b0); b0 = fmaf(wv[5], q.y, b0); b0 = fmaf(wv[6], q.z, b0); b0 = fmaf(wv[7], q.w, b0);
       if (T > 1) {
-        a1 = fmaf(wv[0], p1[j].x, a1); a1 = fmaf(wv[1], p1[j].y, a1);
-        a1 = fmaf(wv[2], p1[j].z, a1); a1 = fmaf(wv[3], p1[j].w, a1);
-        b1 = fmaf(wv[4], q1[j].x, b1); b1 = fmaf(wv[5], q1[j].y, b1);
-        b1 = fmaf(wv[6], q1[j].z, b1); b1 = fmaf(wv[7], q1[j].w, b1);
+        const float4 p1 = lds_f4(ya), q1 = lds_f4(yb);
+        a1 = fmaf(wv[0], p1.x, a1); a1 = fmaf(wv[1], p1.y, a1); a1 = fmaf(wv[2], p1.z, a1); a1 = fmaf(wv[3], p1.w, a1);
+        b1 = fmaf(wv[4], q1.x, b1); b1 = fmaf(wv[5], q1.y, b1); b1 = fmaf(wv[6], q1.z, b1); b1 = fmaf(wv[7], q1.w, b1);
       }
     }
   }
@@ -418,15 +449,87 @@ __device__ __forceinline__ void row_dot(const WT* w, int K, int G, int sl, bool 
   r1 = a1 + b1;
   for (int o = G / 2; o > 0; o >>= 1) {
     r0 += __shfl_xor_sync(0xffffffffu, r0, o);
-    r1 += __shfl_xor_sync(0xffffffffu, r1, o);
+    if (T > 1) r1 += __shfl_xor_sync(0xffffffffu, r1, o);
   }
 }
 
 __device__ __forceinline__ int lanes_per_row(int K) { return K >= 256 ? 32 : (K >= 128 ? 16 : 8); }
 
-// Rows [r0, r1) of a row-major [*, K] matrix, streamed from the ring: out_t(row)
-// = sum_k W[row, k] * x_t[k] for t < T.  xsel(row, t) gives the plane-layout
-// vector; epi(row, t, value) consumes each result (called by one lane per row).
+// Segments per row so that nr rows keep all eight warps busy: the largest
+// power of two S with nr * S <= 8 and K a multiple of 8 S.
+__device__ __forceinline__ int row_segments(int nr, int K) {
+  int S = 1;
+  while (nr * S * 2 <= FK_CONSUMER_WARPS && K % (16 * S) == 0) S *= 2;
+  return S;
+}
+
+// Partial dot product of one row segment [k0, k1) of the row at shared offset
+// w against T plane-layout vectors (shared offsets x0, x1 = x0 + 4K), reduced
+// over the warp (all 32 lanes call it).
+template <class WT>
+__device__ __forceinline__ void seg_dot(uint32_t w, int K, int k0, int k1, int lane, uint32_t x0, int T,
+                                        float& r0, float& r1) {
+  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+  const int k = k0 + lane * 8;
+  uint32_t wo = w + (uint32_t)(k * (int)sizeof(WT));
+  uint32_t xa = x0 + (uint32_t)(k >> 3) * 16u, xb = xa + (uint32_t)K * 2u;
+  uint32_t ya = xa + (uint32_t)K * 4u, yb = ya + (uint32_t)K * 2u;
+  constexpr uint32_t wstep = 256 * sizeof(WT), xstep = 32 * 16;
+  const int n = k < k1 ? (k1 - k + 255) >> 8 : 0;
+#pragma unroll 2
+  for (int i = 0; i < n; ++i, wo += wstep, xa += xstep, xb += xstep, ya += xstep, yb += xstep) {
+    float wv[8];
+    lds_w8<WT>(wo, wv);
+    const float4 p = lds_f4(xa), q = lds_f4(xb);
+    a0 = fmaf(wv[0], p.x, a0); a0 = fmaf(wv[1], p.y, a0); a0 = fmaf(wv[2], p.z, a0); a0 = fmaf(wv[3], p.w, a0);
+    b0 = fmaf(wv[4], q.x, b0); b0 = fmaf(wv[5], q.y, b0); b0 = fmaf(wv[6], q.z, b0); b0 = fmaf(wv[7], q.w, b0);
+    if (T > 1) {
+      const float4 p1 = lds_f4(ya), q1 = lds_f4(yb);
+      a1 = fmaf(wv[0], p1.x, a1); a1 = fmaf(wv[1], p1.y, a1); a1 = fmaf(wv[2], p1.z, a1); a1 = fmaf(wv[3], p1.w, a1);
+      b1 = fmaf(wv[4], q1.x, b1); b1 = fmaf(wv[5], q1.y, b1); b1 = fmaf(wv[6], q1.z, b1); b1 = fmaf(wv[7], q1.w, b1);
+    }
+  }
+  r0 = warp_sum(a0 + b0);
+  r1 = T > 1 ? warp_sum(a1 + b1) : 0.f;
+}
+
+// Rows [r0, r1) (at most FK_TASKROWS) of a row-major [*, K] matrix with
+// K >= 256, streamed from the ring, against the plane-layout vectors
+// xs + t * K: each chunk's rows are cut into segments so all warps work, the
+// segment sums meet in shared memory, and epi(row, t, value) runs once per row
+// at the end (one thread per (row, t)).
+template <class WT, class Epi>
+__device__ void gemv_task(Cons& c, int r0, int r1, int K, int T, const float* xs, Epi epi) {
+  const int nrows = r1 - r0;
+  for (int e = c.tid; e < FK_TMAX * FK_TASKROWS; e += FK_CONSUMERS) (&c.sm->acc[0][0])[e] = 0.f;
+  consumer_sync();
+  const int rpc = rows_per_chunk(K * (int)sizeof(WT));
+  for (int r = r0; r < r1; r += rpc) {
+    const int nr = min(rpc, r1 - r);
+    const int S = row_segments(nr, K), seg = K / S, lg = __ffs(S) - 1;
+    const uint32_t buf = soff(acquire_at(c, c.n));
+    for (int base = c.warp; base < nr * S; base += FK_CONSUMER_WARPS) {
+      const int row = base >> lg, sg = base & (S - 1);
+      float v0, v1;
+      seg_dot<WT>(buf + (uint32_t)(row * K * (int)sizeof(WT)), K, sg * seg, (sg + 1) * seg, c.lane, soff(xs), T,
+                  v0, v1);
+      if (c.lane == 0) {
+        atomicAdd(&c.sm->acc[0][r - r0 + row], v0);
+        if (T > 1) atomicAdd(&c.sm->acc[1][r - r0 + row], v1);
+      }
+    }
+    release_n(c, 1);
+  }
+  consumer_sync();
+  for (int e = c.tid; e < nrows * T; e += FK_CONSUMERS) {
+    const int t = e / nrows, i = e % nrows;
+    epi(r0 + i, t, c.sm->acc[t][i]);
+  }
+}
+
+// Rows [r0, r1) of a row-major [*, K] matrix with short rows (K < 256, the
+// per-head o_proj rows): G lanes per row, several rows per warp, epi(row, t,
+// value) per row as it completes.  xsel(row, t) gives the plane-layout vector.
 template <class WT, class XSel, class Epi>
 __device__ void gemv_rows(Cons& c, int r0, int r1, int K, int T, XSel xsel, Epi epi) {
   const int row_bytes = K * (int)sizeof(WT);
@@ -436,14 +539,14 @@ __device__ void gemv_rows(Cons& c, int r0, int r1, int K, int T, XSel xsel, Epi 
   const int sub = c.lane / G, sl = c.lane % G;
   for (int r = r0; r < r1; r += rpc) {
     const int nr = min(rpc, r1 - r);
-    const WT* buf = reinterpret_cast<const WT*>(acquire_at(c, c.n));
+    const uint32_t buf = soff(acquire_at(c, c.n));
     for (int base = c.warp * gpw; base < nr; base += nslots) {
       const int i = base + sub;
       const bool valid = i < nr;
       const int row = r + (valid ? i : 0);
       float v0, v1;
-      row_dot<WT>(buf + (size_t)(valid ? i : 0) * K, K, G, sl, valid, xsel(row, 0),
-                  xsel(row, T > 1 ? 1 : 0), T, v0, v1);
+      row_dot<WT>(buf + (uint32_t)((valid ? i : 0) * row_bytes), K, G, sl, valid, soff(xsel(row, 0)),
+                  soff(xsel(row, T > 1 ? 1 : 0)), T, v0, v1);
       if (valid && sl == 0) {
         epi(row, 0, v0);
         if (T > 1) epi(row, 1, v1);
@@ -455,22 +558,25 @@ __device__ void gemv_rows(Cons& c, int r0, int r1, int K, int T, XSel xsel, Epi 
 
 // ------------------------------------------------------- residual helpers
 
-__device__ __forceinline__ float* rbuf(const FKParams& p, float* base, int set, int t) {
-  return base + ((size_t)set * FK_TMAX + t) * p.dmax;
+// Residual stream: three rotating buffers X0..X2 ([FK_TMAX][dmax] each).  A
+// layer whose input sits in X_i folds it (each CTA its slice) into both
+// X_{i+1} and X_{i+2}; attention output is added into both, the FFN output
+// into X_{i+2}, which is the next layer's input.  So every phase reads one
+// complete vector: phase A reads X_i, phase C reads X_{i+1}.
+__device__ __forceinline__ float* xbuf(const FKParams& p, int idx, int t) {
+  float* base = idx == 0 ? p.R : (idx == 1 ? p.dA : p.dF);
+  return base + (size_t)t * p.dmax;
 }
-
-enum { SRC_SETS = 0, SRC_SETS_NOF = 1, SRC_XS = 2 };
+__device__ __forceinline__ int xnext(int i, int k) { return (i + k) % 3; }
 
 // Builds xs[t] = RMSNorm(x_t) * g (plane layout) for t < T, where x_t is
-//   SRC_SETS:     R_s + dA_s + dF_s of token t0 + t,
-//   SRC_SETS_NOF: R_s + dA_s,
-//   SRC_XS:       already in xs (plane layout, raw).
-// All loads of a thread are issued together.  With fold, the CTA's slice of
-// each raw x_t is written to R_{1-s} and the same slices of dA_{1-s}, dF_{1-s}
-// are zeroed.  If out is given, the CTA's slice of the normed x_0 goes there.
+// xs[t] itself (from_xs, raw plane layout) or buffer X_src of token t0 + t.
+// All loads of a thread are issued together.  With fold_a >= 0 the CTA's slice
+// of each raw x_t is written to X_fold_a and X_fold_b.  If out is given, the
+// CTA's slice of the normed x_0 goes there.
 template <class WT>
-__device__ __noinline__ void load_norm(Cons& c, int mode, int s, int t0, int T, int D, const WT* g, bool fold,
-                          float* out) {
+__device__ __noinline__ void load_norm(Cons& c, bool from_xs, int src, int t0, int T, int D, const WT* g,
+                                       int fold_a, int fold_b, float* out) {
   const FKParams& p = *c.p;
   float* xs = c.sm->u.xs;
   constexpr int PER = FK_TMAX * FK_DMAX / 4 / FK_CONSUMERS;  // float4 per thread, at most 4
@@ -482,15 +588,8 @@ __device__ __noinline__ void load_norm(Cons& c, int mode, int s, int t0, int T, 
   for (int u = 0; u < PER; ++u) {
     const int e = c.tid + FK_CONSUMERS * u;
     if (e < T * nq) {
-      const int t = e / nq, pq = e % nq, i = plane_first(pq, D);
-      if (mode == SRC_XS) {
-        xv[u] = reinterpret_cast<const float4*>(xs + t * D)[pq];
-      } else {
-        float4 r = ldcg4(rbuf(p, p.R, s, t0 + t) + i);
-        float4 a = ldcg4(rbuf(p, p.dA, s, t0 + t) + i);
-        float4 f = mode == SRC_SETS ? ldcg4(rbuf(p, p.dF, s, t0 + t) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        xv[u] = make_float4(r.x + a.x + f.x, r.y + a.y + f.y, r.z + a.z + f.z, r.w + a.w + f.w);
-      }
+      const int t = e >= nq ? 1 : 0, pq = e - t * nq, i = plane_first(pq, D);
+      xv[u] = from_xs ? reinterpret_cast<const float4*>(xs + t * D)[pq] : ldcg4(xbuf(p, src, t0 + t) + i);
 #pragma unroll
       for (int q = 0; q < 4; ++q) gv[u][q] = to_f(g[i + q]);
     }
@@ -499,26 +598,25 @@ __device__ __noinline__ void load_norm(Cons& c, int mode, int s, int t0, int T, 
   for (int u = 0; u < PER; ++u) {
     const int e = c.tid + FK_CONSUMERS * u;
     if (e < T * nq) {
-      const int t = e / nq;
+      const int t = e >= nq ? 1 : 0;
       const float v = xv[u].x * xv[u].x + xv[u].y * xv[u].y + xv[u].z * xv[u].z + xv[u].w * xv[u].w;
       if (t == 0) ss[0] += v; else ss[1] += v;
     }
   }
-  if (fold) {
+  if (fold_a >= 0) {
     int lo, hi;
     split(D, p.ncta, c.cta, lo, hi);
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
       const int e = c.tid + FK_CONSUMERS * u;
       if (e < T * nq) {
-        const int t = e / nq, i = plane_first(e % nq, D);
+        const int t = e >= nq ? 1 : 0, i = plane_first(e - t * nq, D);
         const float vals[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           if (i + q >= lo && i + q < hi) {
-            rbuf(p, p.R, 1 - s, t)[i + q] = vals[q];
-            rbuf(p, p.dA, 1 - s, t)[i + q] = 0.f;
-            rbuf(p, p.dF, 1 - s, t)[i + q] = 0.f;
+            xbuf(p, fold_a, t)[i + q] = vals[q];
+            xbuf(p, fold_b, t)[i + q] = vals[q];
           }
       }
     }
@@ -543,7 +641,7 @@ __device__ __noinline__ void load_norm(Cons& c, int mode, int s, int t0, int T, 
   for (int u = 0; u < PER; ++u) {
     const int e = c.tid + FK_CONSUMERS * u;
     if (e < T * nq) {
-      const int t = e / nq, pq = e % nq;
+      const int t = e >= nq ? 1 : 0, pq = e - t * nq;
       const float iv = t == 0 ? inv[0] : inv[1];
       float4 y = make_float4(xv[u].x * iv * gv[u][0], xv[u].y * iv * gv[u][1], xv[u].z * iv * gv[u][2],
                              xv[u].w * iv * gv[u][3]);
@@ -650,29 +748,33 @@ __device__ __forceinline__ const WT* side_gk(const Cons& c, int D) { return side
 
 // ---------------------------------------------------------------- phases
 
-// Phase A: residual in (or tokens already in xs), fold, RMSNorm, QKV rows out;
-// the layer's q/k norm gains go to shared memory for phase B.
+// Phase A: layer input X_in (or tokens already in xs), fold into X_in+1 and
+// X_in+2, RMSNorm, QKV rows out.
 template <class WT>
-__device__ __noinline__ void phase_qkv(Cons& c, int D, int T, int s, bool from_xs) {
+__device__ __noinline__ void phase_qkv(Cons& c, int D, int T, int in, bool from_xs) {
   const FKParams& p = *c.p;
   const WT* side = side_begin<WT>(c);
-  load_norm<WT>(c, from_xs ? SRC_XS : SRC_SETS, s, 0, T, D, side, true, nullptr);
+  load_norm<WT>(c, from_xs, in, 0, T, D, side, xnext(in, 1), xnext(in, 2), nullptr);
   int lo, hi;
   split(p.qkv_rows, p.ncta, c.cta, lo, hi);
-  float* xs = c.sm->u.xs;
-  gemv_rows<WT>(
-      c, lo, hi, D, T, [&](int, int t) { return xs + t * D; },
-      [&](int row, int t, float v) { p.qkv[(size_t)t * p.qkv_rows + row] = v; });
+  gemv_task<WT>(c, lo, hi, D, T, c.sm->u.xs,
+                [&](int row, int t, float v) { p.qkv[(size_t)t * p.qkv_rows + row] = v; });
   grid_sync(c);
 }
 
-// o_proj over the CTA's (head, output column) range; os holds the heads' outputs.
+// o_proj over the CTA's (head, output column) range; os holds the heads'
+// outputs; the sums go into both X_a and X_b.
 template <class WT>
-__device__ void oproj_cols(Cons& c, int D, int T, int s_next, int v0, int v1, int h_first) {
+__device__ void oproj_cols(Cons& c, int D, int T, int xa, int xb, int v0, int v1, int h_first) {
   const FKParams& p = *c.p;
+  const int boundary = (h_first + 1) * D;  // first column of the CTA's second head
   gemv_rows<WT>(
-      c, v0, v1, p.hd, T, [&](int row, int t) { return c.sm->os[row / D - h_first][t]; },
-      [&](int row, int t, float v) { atomicAdd(rbuf(p, p.dA, s_next, t) + row % D, v); });
+      c, v0, v1, p.hd, T, [&](int row, int t) { return c.sm->os[row >= boundary ? 1 : 0][t]; },
+      [&](int row, int t, float v) {
+        const int col = row >= boundary ? row - boundary : row - (boundary - D);
+        atomicAdd(xbuf(p, xa, t) + col, v);
+        atomicAdd(xbuf(p, xb, t) + col, v);
+      });
 }
 
 // Stores a warp's head vector (lane holds l + 32 j) into plane layout.
@@ -686,7 +788,7 @@ __device__ __forceinline__ void store_head_plane(float* dst, int hd, const float
 // softmax sums are combined across warps.  The CTA owning column 0 of the
 // first q head of a kv group appends that group's current k, v to the cache.
 template <class WT>
-__device__ __noinline__ void phase_cp_attn(Cons& c, int layer, int T, int pos0, int s_next) {
+__device__ __noinline__ void phase_cp_attn(Cons& c, int layer, int T, int pos0, int xa, int xb) {
   const FKParams& p = *c.p;
   const int D = p.Dc, hd = p.hd, Hq = p.Hq, Hkv = p.Hkv, rep = Hq / Hkv, J = hd / 32;
   int v0, v1;
@@ -804,7 +906,7 @@ __device__ __noinline__ void phase_cp_attn(Cons& c, int layer, int T, int pos0, 
     put_plane(c.sm->os[pr / T][pr % T], hd, d, Os / Ls);
   }
   consumer_sync();
-  oproj_cols<WT>(c, D, T, s_next, v0, v1, h_first);
+  oproj_cols<WT>(c, D, T, xa, xb, v0, v1, h_first);
   grid_sync(c);
 }
 
@@ -927,7 +1029,7 @@ __device__ __noinline__ void phase_talker_attn(Cons& c, int layer) {
 // Talker phase B2: combine the partials of the CTA's heads (all partial loads
 // of a thread issued together), then o_proj.
 template <class WT>
-__device__ __noinline__ void phase_talker_oproj(Cons& c, int s_next) {
+__device__ __noinline__ void phase_talker_oproj(Cons& c, int xa, int xb) {
   const FKParams& p = *c.p;
   const int D = p.Dt, hd = p.hd, Hq = p.Hq, cpg = p.ncta / p.Hkv;
   int v0, v1;
@@ -966,25 +1068,25 @@ __device__ __noinline__ void phase_talker_oproj(Cons& c, int s_next) {
     put_plane(c.sm->os[hh][0], hd, d, Os / Ls);
   }
   consumer_sync();
-  oproj_cols<WT>(c, D, 1, s_next, v0, v1, h_first);
+  oproj_cols<WT>(c, D, 1, xa, xb, v0, v1, h_first);
   grid_sync(c);
 }
 
-// Phase C: y = R + dA (set s_next), RMSNorm, gate/up rows of the CTA's FFN
-// slice, SwiGLU, matching rows of the transposed down projection; the partial
-// D-vector is added into dF with float4 atomics.
+// Phase C: y = X_a (input + attention), RMSNorm, gate and up rows of the
+// CTA's FFN slice (gate rows and up rows on different warps), SwiGLU, the
+// matching rows of the transposed down projection; the partial D-vector is
+// added into X_b with float4 atomics.
 template <class WT>
-__device__ __noinline__ void phase_ffn(Cons& c, const LayerDev& L, int D, int F, int T, int s_next) {
+__device__ __noinline__ void phase_ffn(Cons& c, int D, int F, int T, int xa, int xb) {
   const FKParams& p = *c.p;
-  load_norm<WT>(c, SRC_SETS_NOF, s_next, 0, T, D, side_cur<WT>(c) + D, false, nullptr);
+  for (int e = c.tid; e < FK_TMAX * 128; e += FK_CONSUMERS) (&c.sm->gu[0][0][0])[e] = 0.f;
+  load_norm<WT>(c, false, xa, 0, T, D, side_cur<WT>(c) + D, -1, -1, nullptr);
   side_end(c);
   float* xs = c.sm->u.xs;
   int f0, f1;
   split(F, p.ncta, c.cta, f0, f1);
   const int row_bytes = D * (int)sizeof(WT);
   const int gpr = min(64, rows_per_chunk(row_bytes));
-  const int G = lanes_per_row(D), gpw = 32 / G, nslots = FK_CONSUMER_WARPS * gpw;
-  const int sub = c.lane / G, sl = c.lane % G;
   float acc[FK_TMAX][8];
 #pragma unroll
   for (int t = 0; t < FK_TMAX; ++t)
@@ -995,33 +1097,49 @@ __device__ __noinline__ void phase_ffn(Cons& c, const LayerDev& L, int D, int F,
   for (int g = f0; g < f1; g += gpr, buf ^= 1) {
     const int ng = min(gpr, f1 - g);
     // gate and up rows of the group (two consecutive ring chunks)
-    const WT* wg = reinterpret_cast<const WT*>(acquire_at(c, c.n));
-    const WT* wu = reinterpret_cast<const WT*>(acquire_at(c, c.n + 1));
-    for (int base = c.warp * gpw; base < ng; base += nslots) {
-      const int i = base + sub;
-      const bool valid = i < ng;
-      const int ii = valid ? i : 0;
-      float g0, g1, u0, u1;
-      row_dot<WT>(wg + (size_t)ii * D, D, G, sl, valid, xs, xs + D, T, g0, g1);
-      row_dot<WT>(wu + (size_t)ii * D, D, G, sl, valid, xs, xs + D, T, u0, u1);
-      if (valid && sl == 0) {
-        c.sm->av[buf][0][i] = silu(g0) * u0;
-        if (T > 1) c.sm->av[buf][1][i] = silu(g1) * u1;
+    const uint32_t wg = soff(acquire_at(c, c.n));
+    const uint32_t wu = soff(acquire_at(c, c.n + 1));
+    const int S = row_segments(2 * ng, D), seg = D / S, lg = __ffs(S) - 1;
+    for (int item = c.warp; item < 2 * ng * S; item += FK_CONSUMER_WARPS) {
+      const int r2 = item >> lg, sg = item & (S - 1), which = r2 >= ng ? 1 : 0, i = r2 - which * ng;
+      float v0, v1;
+      seg_dot<WT>((which ? wu : wg) + (uint32_t)(i * row_bytes), D, sg * seg, (sg + 1) * seg, c.lane, soff(xs), T,
+                  v0, v1);
+      if (c.lane == 0) {
+        atomicAdd(&c.sm->gu[buf][0][which * 64 + i], v0);
+        if (T > 1) atomicAdd(&c.sm->gu[buf][1][which * 64 + i], v1);
       }
     }
     release_n(c, 2);
     consumer_sync();
-    const WT* wd = reinterpret_cast<const WT*>(acquire_at(c, c.n));
+    for (int e = c.tid; e < T * ng; e += FK_CONSUMERS) {
+      const int t = e / ng, i = e % ng;
+      c.sm->av[buf][t][i] = silu(c.sm->gu[buf][t][i]) * c.sm->gu[buf][t][64 + i];
+    }
+    for (int e = c.tid; e < FK_TMAX * 128; e += FK_CONSUMERS) (&c.sm->gu[buf ^ 1][0][0])[e] = 0.f;
+    consumer_sync();
+    const uint32_t wd = soff(acquire_at(c, c.n));
     if (col < D) {
-      for (int i = 0; i < ng; ++i) {
-        float w[8];
-        ld8_smem<WT>(wd + (size_t)i * D + col, w);
-        const float a0 = c.sm->av[buf][0][i];
-        const float a1 = T > 1 ? c.sm->av[buf][1][i] : 0.f;
+      uint32_t wo = wd + (uint32_t)(col * (int)sizeof(WT));
+      if (T > 1) {
+        for (int i = 0; i < ng; ++i, wo += (uint32_t)row_bytes) {
+          float w[8];
+          lds_w8<WT>(wo, w);
+          const float a0 = c.sm->av[buf][0][i], a1 = c.sm->av[buf][1][i];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          acc[0][q] = fmaf(a0, w[q], acc[0][q]);
-          acc[1][q] = fmaf(a1, w[q], acc[1][q]);
+          for (int q = 0; q < 8; ++q) {
+            acc[0][q] = fmaf(a0, w[q], acc[0][q]);
+            acc[1][q] = fmaf(a1, w[q], acc[1][q]);
+          }
+        }
+      } else {
+#pragma unroll 2
+        for (int i = 0; i < ng; ++i, wo += (uint32_t)row_bytes) {
+          float w[8];
+          lds_w8<WT>(wo, w);
+          const float a0 = c.sm->av[buf][0][i];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[0][q] = fmaf(a0, w[q], acc[0][q]);
         }
       }
     }
@@ -1031,7 +1149,7 @@ __device__ __noinline__ void phase_ffn(Cons& c, const LayerDev& L, int D, int F,
 #pragma unroll
     for (int t = 0; t < FK_TMAX; ++t) {
       if (t < T) {
-        float* dst = rbuf(p, p.dF, s_next, t) + col;
+        float* dst = xbuf(p, xb, t) + col;
         atomicAdd(reinterpret_cast<float4*>(dst), make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]));
         atomicAdd(reinterpret_cast<float4*>(dst + 4), make_float4(acc[t][4], acc[t][5], acc[t][6], acc[t][7]));
       }
@@ -1113,40 +1231,29 @@ __device__ void consumer(const FKParams& p, FKSmem* sm) {
     if (j == 0) fed0 = fed;
     xsum_add<WT>(c, j, fed);
     cp_tokens<WT>(c, j, fed);
-    int s = 0;
+    int in = 0;  // the layer input buffer
     bool from_xs = true;
     if (p.has_proj) {
-      // z = W_p u into R_0 (rows of the CTA), deltas of set 0 zeroed
+      // z = W_p u into X_0 (rows of the CTA)
       int lo, hi;
       split(p.Dc, p.ncta, c.cta, lo, hi);
-      float* xs = sm->u.xs;
-      gemv_rows<WT>(
-          c, lo, hi, p.Dt, T, [&](int, int t) { return xs + t * p.Dt; },
-          [&](int row, int t, float v) {
-            rbuf(p, p.R, 0, t)[row] = v;
-            rbuf(p, p.dA, 0, t)[row] = 0.f;
-            rbuf(p, p.dF, 0, t)[row] = 0.f;
-          });
+      gemv_task<WT>(c, lo, hi, p.Dt, T, sm->u.xs, [&](int row, int t, float v) { xbuf(p, 0, t)[row] = v; });
       grid_sync(c);
       from_xs = false;
     }
     for (int l = 0; l < p.Lc; ++l) {
-      const LayerDev& L = sm->lay[p.Lt + l];
-      phase_qkv<WT>(c, p.Dc, T, s, from_xs);
+      phase_qkv<WT>(c, p.Dc, T, in, from_xs);
       from_xs = false;
-      phase_cp_attn<WT>(c, l, T, pos0, 1 - s);
-      phase_ffn<WT>(c, L, p.Dc, p.Fc, T, 1 - s);
-      s = 1 - s;
+      phase_cp_attn<WT>(c, l, T, pos0, xnext(in, 1), xnext(in, 2));
+      phase_ffn<WT>(c, p.Dc, p.Fc, T, xnext(in, 1), xnext(in, 2));
+      in = xnext(in, 2);
     }
     // final norm of the last token, head j
-    load_norm<WT>(c, SRC_SETS, s, T - 1, 1, p.Dc, reinterpret_cast<const WT*>(sm->fin), false, nullptr);
+    load_norm<WT>(c, false, in, T - 1, 1, p.Dc, reinterpret_cast<const WT*>(sm->fin), -1, -1, nullptr);
     {
       int lo, hi;
       split(p.Vc, p.ncta, c.cta, lo, hi);
-      float* xs = sm->u.xs;
-      gemv_rows<WT>(
-          c, lo, hi, p.Dc, 1, [&](int, int) { return xs; },
-          [&](int row, int, float v) { p.cp_logits[row] = v; });
+      gemv_task<WT>(c, lo, hi, p.Dc, 1, sm->u.xs, [&](int row, int, float v) { p.cp_logits[row] = v; });
     }
     grid_sync(c);
   }
@@ -1158,27 +1265,24 @@ __device__ void consumer(const FKParams& p, FKSmem* sm) {
     for (int i = c.tid; i < p.Dt; i += FK_CONSUMERS) put_plane(xs, p.Dt, i, __ldcg(p.xsum + i) + to_f(e[i]));
     consumer_sync();
   }
-  int s = 0;
+  int in = 0;
   bool from_xs = true;
   for (int l = 0; l < p.Lt; ++l) {
-    const LayerDev& L = sm->lay[l];
-    phase_qkv<WT>(c, p.Dt, 1, s, from_xs);
+    phase_qkv<WT>(c, p.Dt, 1, in, from_xs);
     from_xs = false;
     phase_talker_attn<WT, KT>(c, l);
-    phase_talker_oproj<WT>(c, 1 - s);
-    phase_ffn<WT>(c, L, p.Dt, p.Ft, 1, 1 - s);
-    s = 1 - s;
+    phase_talker_oproj<WT>(c, xnext(in, 1), xnext(in, 2));
+    phase_ffn<WT>(c, p.Dt, p.Ft, 1, xnext(in, 1), xnext(in, 2));
+    in = xnext(in, 2);
   }
   // final norm -> pending hidden (CTA slice) and codec head rows -> pending logits
-  load_norm<WT>(c, SRC_SETS, s, 0, 1, p.Dt, reinterpret_cast<const WT*>(sm->fin) + p.Dc, false,
+  load_norm<WT>(c, false, in, 0, 1, p.Dt, reinterpret_cast<const WT*>(sm->fin) + p.Dc, -1, -1,
                 p.pending_h + (size_t)p.sid * p.Dt);
   {
     int lo, hi;
     split(p.Vt, p.ncta, c.cta, lo, hi);
-    float* xs = sm->u.xs;
     float* out = p.pending_logits + (size_t)p.sid * p.Vt;
-    gemv_rows<WT>(
-        c, lo, hi, p.Dt, 1, [&](int, int) { return xs; }, [&](int row, int, float v) { out[row] = v; });
+    gemv_task<WT>(c, lo, hi, p.Dt, 1, sm->u.xs, [&](int row, int, float v) { out[row] = v; });
   }
   if (c.cta == 0 && c.tid == 0) p.history[(size_t)p.sid * p.Vt + fed0] = 1;
   consumer_sync();
@@ -1326,7 +1430,6 @@ struct Producer {
 
 template <class WT, class KT>
 __global__ void __launch_bounds__(FK_THREADS, 1) frame_kernel(const __grid_constant__ FKParams p) {
-  extern __shared__ __align__(128) unsigned char fk_smem_raw[];
   FKSmem* sm = reinterpret_cast<FKSmem*>(fk_smem_raw);
   if (threadIdx.x == 0) sm->prm = p;
   for (int i = threadIdx.x; i < p.Lt + p.Lc; i += blockDim.x)
@@ -1456,6 +1559,9 @@ int frame_kernel_create(q3tts_handle* h) {
   const int ncta = std::min(h->n_sm, FK_MAXCTA);
   // every CTA's o_proj column range must touch at most two heads
   if (ncta < c.n_kv_heads || ncta < c.n_q_heads) return Q3TTS_OK;
+  // row-split tasks (QKV, heads, projection) must fit the task accumulator
+  const int most = std::max(std::max(h->qkv_rows, c.codec_vocab), std::max(c.cp_vocab, c.cp_hidden));
+  if ((most + ncta - 1) / ncta > FK_TASKROWS) return Q3TTS_OK;
   // the per-CTA FFN slice must fit the gate/up scratch of one group (<= 64 rows)
   st->smem = sizeof(FKSmem);
   void* k = pick_kernel(c.weight_dtype, c.kv_dtype);

@@ -340,7 +340,10 @@ def main():
                        "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2: each step streams %.2f GB of weights"
                              % (bytes_per_step / 1e9)},
-            "roofline": {"bound": "hbm", "kernel": "frame step (all launches of one frame)",
+            "roofline": {"bound": "hbm",
+                         "kernel": ("frame_kernel (persistent, one launch per frame)"
+                                    if launches == args.steps else
+                                    "frame step (all launches of one frame)"),
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                          "unit": "GB/s", "frac": achieved / peak, "traffic": None,
                          "algorithmic_bytes_per_step": bytes_per_step,

@@ -242,26 +242,31 @@ def _with_frame_kernel(enabled: bool):
 
 
 @pytest.mark.parametrize("shape_name", ["tiny", "ragged"])
-def test_persistent_kernel_matches_layered_step(q3, shape_name):
-    """Batch-1 frames run as one persistent launch; the same frames through the
-    one-kernel-per-operation step give the same codes and (within fp32
-    reassociation) the same logits."""
+def test_persistent_kernel_matches_layered_step(q3, oracle_mod, shape_name):
+    """Batch-1 frames run as one persistent launch; the one-kernel-per-operation
+    step, teacher-forced with the persistent kernel's codes, produces the same
+    logits (fp32 reassociation only), and each path's draws follow the float
+    rule on its own logits."""
     shape = TINY.shape if shape_name == "tiny" else RAGGED
     W, Wd = pu.gpu_weights(shape)
     sp = synth.QWEN_DEFAULT_SAMPLING
     p = synth.make_prompts(shape, [21])[0]
     u = synth.uniforms([0], 6)
     out = {}
+    forced = None
     for fk in (True, False):
         with _with_frame_kernel(fk):
             eng = q3.Engine(shape, Wd, max_streams=1, kv_cap=40)
         eng.prefill(0, p.cuda())
         eng.sync()
         l0 = eng.kernel_launches()
-        codes, logits = pu.run_gpu(eng, [0], [p], sp, 6, uniforms=u, prefill=False)
+        codes, logits = pu.run_gpu(eng, [0], [p], sp, 6, uniforms=u, prefill=False, forced=forced)
         out[fk] = (codes, logits, eng.kernel_launches() - l0)
         eng.close()
+        forced = codes
     assert out[True][2] == 6, out[True][2]        # one launch per frame
     assert out[False][2] > 100 * 6
-    assert np.array_equal(out[True][0], out[False][0])
     assert np.max(np.abs(out[True][1] - out[False][1])) < 2e-5
+    for fk in (True, False):
+        codes, logits, _ = out[fk]
+        assert pu.sampler_replay(oracle_mod, shape, sp, codes[0], logits[0], out[True][0][0], u[0]) == 0
