@@ -20,6 +20,10 @@ int frame_kernel_recover(q3tts_handle* h);
 int frame_kernel_step(q3tts_handle* h, const StepDesc& d, const float* uniforms, int32_t* codes,
                       const int32_t* forced, float* logits);
 size_t frame_kernel_workspace(const q3tts_config& c, int n_sm);
+int frame_kernel_static_check(const q3tts_handle* h, const q3tts_sampling& sp);
+int frame_kernel_step_static(q3tts_handle* h, int sid, int pos, int newpage, const q3tts_sampling& sp,
+                             const float* uniforms, int32_t* codes, const int32_t* forced, float* logits);
+int frame_kernel_recover_static(q3tts_handle* h);
 }  // namespace q3
 
 namespace {
@@ -305,6 +309,39 @@ int q3tts_step_frame(q3tts_handle* h, const q3tts_sampling* params, const int32_
   return Q3TTS_OK;
 }
 
+// Batch-1 frame with the persistent kernel's per-frame scratch in a static
+// device array.  Validation and stream bookkeeping follow q3tts_step_frame,
+// but nothing here allocates: no std::vector, no thread-local descriptor, and
+// the page lists were reserved to their maximum length by the handle's first
+// call, so pushing a page never grows them.
+int q3tts_step_frame_static(q3tts_handle* h, const q3tts_sampling* params, int stream_id,
+                            const float* uniforms_dev, int32_t* codes_dev,
+                            const int32_t* forced_dev, float* logits_dev) {
+  if (!h || !params || !uniforms_dev || !codes_dev) return Q3TTS_ERR_ARG;
+  const int s = stream_id;
+  if (s < 0 || s >= h->c.max_streams || !check_sampling(*params)) return Q3TTS_ERR_ARG;
+  int rc = q3::frame_kernel_static_check(h, *params);
+  if (rc != Q3TTS_OK) return rc;
+  if (h->len[s] < 1) return Q3TTS_ERR_STATE;
+  if (h->len[s] >= h->c.kv_cap_steps) return Q3TTS_ERR_CAPACITY;
+  if (!h->static_ready) {
+    for (auto& v : h->pages) v.reserve(h->pps);
+    h->static_ready = true;
+  }
+  const bool grow = h->len[s] / h->c.page_size >= (int)h->pages[s].size();
+  if (grow && h->free_pages.empty()) return Q3TTS_ERR_CAPACITY;
+  const int newpage = grow ? h->free_pages.back() : -1;
+  rc = q3::frame_kernel_step_static(h, s, h->len[s], newpage, *params, uniforms_dev, codes_dev,
+                                    forced_dev, logits_dev);
+  if (rc != Q3TTS_OK) return rc;
+  if (grow) {
+    h->free_pages.pop_back();
+    h->pages[s].push_back(newpage);
+  }
+  h->len[s] += 1;
+  return Q3TTS_OK;
+}
+
 int q3tts_read_pending(q3tts_handle* h, int sid, float* hidden_dev, float* logits_dev) {
   if (!h || sid < 0 || sid >= h->c.max_streams) return Q3TTS_ERR_ARG;
   if (h->len[sid] < 1) return Q3TTS_ERR_STATE;
@@ -346,6 +383,7 @@ int q3tts_sync_status(q3tts_handle* h) {
   if (e != 0) {
     cudaMemset(h->d_err, 0, sizeof(int));
     q3::frame_kernel_recover(h);
+    q3::frame_kernel_recover_static(h);
     cudaStreamSynchronize(h->s);
     return e;
   }
@@ -369,6 +407,7 @@ const char* q3tts_strerror(int code) {
     case Q3TTS_ERR_TIMEOUT: return "device-side wait timed out";
     case Q3TTS_ERR_UNSUPPORTED: return "unsupported configuration";
     case Q3TTS_ERR_STATE: return "stream has no prompt";
+    case Q3TTS_ERR_SCRATCH: return "static scratch array too small for this configuration";
     default: return "unknown error";
   }
 }

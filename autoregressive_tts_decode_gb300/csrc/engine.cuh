@@ -61,6 +61,8 @@ struct q3tts_handle {
   q3::FrameKernelState* fk;
   char* fk_base;           // workspace region of the persistent frame kernel
   bool frame_kernel_off;   // Q3TTS_FRAME_KERNEL=0: always use the layered step
+  bool used_static = false;   // q3tts_step_frame_static has run on this handle
+  bool static_ready = false;  // per-stream page lists reserved for it
   uint64_t launches = 0;
 };
 

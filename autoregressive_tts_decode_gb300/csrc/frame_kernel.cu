@@ -42,6 +42,8 @@
 //    records Q3TTS_ERR_TIMEOUT, raises an abort flag, stops waiting, lets
 //    in-flight copies land and returns.
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -1649,11 +1651,13 @@ bool frame_kernel_supports(const q3tts_handle* h, int n_active, const q3tts_samp
   return sampling_ok(sp[0].do_sample, sp[0].top_k) && sampling_ok(sp[0].sub_do_sample, sp[0].sub_top_k);
 }
 
-int frame_kernel_step(q3tts_handle* h, const StepDesc& d, const float* uniforms, int32_t* codes,
-                      const int32_t* forced, float* logits) {
-  FrameKernelState* st = h->fk;
+// Launch parameters of one frame of stream sid at Talker position pos, with the
+// per-frame scratch taken from the handle's workspace.
+static void frame_params(FKParams& p, const q3tts_handle* h, int sid, int pos, int newpage,
+                         const q3tts_sampling& sp, const float* uniforms, int32_t* codes,
+                         const int32_t* forced, float* logits) {
+  const FrameKernelState* st = h->fk;
   const q3tts_config& c = h->c;
-  FKParams p;
   p.ncta = st->ncta;
   p.Dt = c.talker_hidden; p.Dc = c.cp_hidden; p.Ft = c.talker_ffn; p.Fc = c.cp_ffn;
   p.Hq = c.n_q_heads; p.Hkv = c.n_kv_heads; p.hd = c.head_dim; p.Vt = c.codec_vocab; p.Vc = c.cp_vocab;
@@ -1668,13 +1672,23 @@ int frame_kernel_step(q3tts_handle* h, const StepDesc& d, const float* uniforms,
   p.R = st->R; p.dA = st->dA; p.dF = st->dF; p.qkv = st->qkv; p.part = st->part;
   p.cp_logits = st->cp_logits; p.xsum = st->xsum;
   p.bar = st->bar; p.done = st->done; p.err = h->d_err; p.abort_flag = st->abort_flag;
-  p.sid = d.sid[0]; p.pos = d.pos[0]; p.newpage = d.newpage[0]; p.sp = d.sp[0];
+  p.sid = sid; p.pos = pos; p.newpage = newpage; p.sp = sp;
   p.uniforms = uniforms; p.codes = codes; p.forced = forced; p.dump = logits;
+}
+
+static int frame_launch(q3tts_handle* h, FKParams& p) {
   void* args[] = {&p};
-  cudaError_t e = cudaLaunchCooperativeKernel(pick_kernel(c.weight_dtype, c.kv_dtype), dim3(st->ncta),
-                                              dim3(FK_THREADS), args, st->smem, h->s);
+  cudaError_t e = cudaLaunchCooperativeKernel(pick_kernel(h->c.weight_dtype, h->c.kv_dtype),
+                                              dim3(h->fk->ncta), dim3(FK_THREADS), args, h->fk->smem, h->s);
   h->launches += 1;
   return e == cudaSuccess ? Q3TTS_OK : Q3TTS_ERR_CUDA;
+}
+
+int frame_kernel_step(q3tts_handle* h, const StepDesc& d, const float* uniforms, int32_t* codes,
+                      const int32_t* forced, float* logits) {
+  FKParams p;
+  frame_params(p, h, d.sid[0], d.pos[0], d.newpage[0], d.sp[0], uniforms, codes, forced, logits);
+  return frame_launch(h, p);
 }
 
 // After a device-side error: clear the barrier counters and the abort flag.
@@ -1682,6 +1696,116 @@ int frame_kernel_recover(q3tts_handle* h) {
   if (!h->fk || !h->fk->ok) return Q3TTS_OK;
   return cudaMemsetAsync(h->fk->bar, 0, sizeof(unsigned) * 4, h->s) == cudaSuccess ? Q3TTS_OK
                                                                                    : Q3TTS_ERR_CUDA;
+}
+
+
+// ------------------------------------------- frame step with static scratch
+//
+// q3tts_step_frame_static runs the same kernel with its per-frame scratch (the
+// three residual vectors, QKV rows, attention partials, CodePredictor logits,
+// the running embedding sum and the grid-barrier words) in this file-scope
+// device array instead of the caller's workspace, so a frame needs no memory
+// from the caller beyond what q3tts_create was given, and the call itself
+// makes no device or host allocation.  Layout: the barrier words (bar, done,
+// abort flag) in the first 256 bytes -- at the same place for every handle,
+// since a completed frame leaves them zero for whichever call comes next --
+// then the vectors, each 256-byte aligned.  Every other byte is written by a
+// frame before it is read, so only the barrier words must start at zero.
+static __device__ __align__(256) unsigned char fk_static_scratch[Q3TTS_STATIC_SCRATCH_BYTES];
+
+constexpr int FK_MAX_DEVICES = 64;
+static std::mutex g_static_mu;
+static std::atomic<unsigned char*> g_static_addr[FK_MAX_DEVICES];
+
+// Places the scratch vectors of config c behind the barrier words at base
+// (size only when base is null); returns the bytes used.
+static size_t fk_static_layout(const q3tts_config& c, int ncta, char* base, FKParams* p) {
+  const int dmax = std::max(c.talker_hidden, c.cp_hidden);
+  const int qkv_rows = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+  const int cpg = std::max(1, ncta / c.n_kv_heads);
+  size_t off = 256;  // barrier words
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = al256(off + bytes);
+    return (float*)(base ? base + o : nullptr);
+  };
+  float* R = take(sizeof(float) * 2 * FK_TMAX * dmax);
+  float* dA = take(sizeof(float) * 2 * FK_TMAX * dmax);
+  float* dF = take(sizeof(float) * 2 * FK_TMAX * dmax);
+  float* qkv = take(sizeof(float) * FK_TMAX * qkv_rows);
+  float* part = take(sizeof(float) * (size_t)c.n_q_heads * cpg * (c.head_dim + 2));
+  float* lg = take(sizeof(float) * c.cp_vocab);
+  float* xsum = take(sizeof(float) * c.talker_hidden);
+  if (p) {
+    p->R = R; p->dA = dA; p->dF = dF; p->qkv = qkv; p->part = part;
+    p->cp_logits = lg; p->xsum = xsum;
+    p->bar = (unsigned*)base;
+    p->done = p->bar + 1;
+    p->abort_flag = (int*)(p->bar + 2);
+  }
+  return off;
+}
+
+// Address of the scratch array on the handle's device.  The first call on a
+// device looks the symbol up (with that device current) and clears the
+// barrier words on the handle's stream; later calls only read the cached
+// address.
+static int static_scratch(q3tts_handle* h, unsigned char** out) {
+  if (h->dev < 0 || h->dev >= FK_MAX_DEVICES) return Q3TTS_ERR_UNSUPPORTED;
+  unsigned char* a = g_static_addr[h->dev].load(std::memory_order_acquire);
+  if (!a) {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    a = g_static_addr[h->dev].load(std::memory_order_relaxed);
+    if (!a) {
+      int cur = -1;
+      if (cudaGetDevice(&cur) != cudaSuccess) return Q3TTS_ERR_CUDA;
+      if (cur != h->dev && cudaSetDevice(h->dev) != cudaSuccess) return Q3TTS_ERR_CUDA;
+      void* sym = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&sym, fk_static_scratch);
+      if (e == cudaSuccess) e = cudaMemsetAsync(sym, 0, 256, h->s);
+      if (e == cudaSuccess) e = cudaStreamSynchronize(h->s);
+      if (cur != h->dev) cudaSetDevice(cur);
+      if (e != cudaSuccess || !sym) {
+        cudaGetLastError();
+        return Q3TTS_ERR_CUDA;
+      }
+      a = (unsigned char*)sym;
+      g_static_addr[h->dev].store(a, std::memory_order_release);
+    }
+  }
+  *out = a;
+  return Q3TTS_OK;
+}
+
+// Whether q3tts_step_frame_static can run this handle with these sampling
+// settings; Q3TTS_ERR_SCRATCH if the scratch would not fit the array.
+int frame_kernel_static_check(const q3tts_handle* h, const q3tts_sampling& sp) {
+  if (!h->fk || !h->fk->ok) return Q3TTS_ERR_UNSUPPORTED;
+  if (!sampling_ok(sp.do_sample, sp.top_k) || !sampling_ok(sp.sub_do_sample, sp.sub_top_k))
+    return Q3TTS_ERR_UNSUPPORTED;
+  if (fk_static_layout(h->c, h->fk->ncta, nullptr, nullptr) > (size_t)Q3TTS_STATIC_SCRATCH_BYTES)
+    return Q3TTS_ERR_SCRATCH;
+  return Q3TTS_OK;
+}
+
+int frame_kernel_step_static(q3tts_handle* h, int sid, int pos, int newpage, const q3tts_sampling& sp,
+                             const float* uniforms, int32_t* codes, const int32_t* forced, float* logits) {
+  unsigned char* base = nullptr;
+  int rc = static_scratch(h, &base);
+  if (rc != Q3TTS_OK) return rc;
+  h->used_static = true;
+  FKParams p;
+  frame_params(p, h, sid, pos, newpage, sp, uniforms, codes, forced, logits);
+  fk_static_layout(h->c, h->fk->ncta, (char*)base, &p);
+  return frame_launch(h, p);
+}
+
+// After a device-side error in a frame that used the static scratch.
+int frame_kernel_recover_static(q3tts_handle* h) {
+  if (!h->used_static || h->dev < 0 || h->dev >= FK_MAX_DEVICES) return Q3TTS_OK;
+  unsigned char* a = g_static_addr[h->dev].load(std::memory_order_acquire);
+  if (!a) return Q3TTS_OK;
+  return cudaMemsetAsync(a, 0, 256, h->s) == cudaSuccess ? Q3TTS_OK : Q3TTS_ERR_CUDA;
 }
 
 }  // namespace q3

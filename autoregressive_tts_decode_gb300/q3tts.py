@@ -15,6 +15,8 @@ LIB_PATH = os.path.join(HERE, "libq3tts.so")
 
 OK = 0
 ERR_ARG, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED, ERR_STATE = -1, -2, -3, -4, -5, -6
+ERR_SCRATCH = -7
+STATIC_SCRATCH_BYTES = 393216
 F32, BF16 = 0, 1
 MAX_STREAMS = 256
 N_CODEBOOKS = 16
@@ -57,7 +59,8 @@ class Sampling(C.Structure):
 
 EXPORTS = ("q3tts_workspace_size", "q3tts_create", "q3tts_prefill", "q3tts_step_frame",
            "q3tts_read_pending", "q3tts_reset", "q3tts_stream_length", "q3tts_sync_status",
-           "q3tts_kernel_launches", "q3tts_destroy", "q3tts_strerror")
+           "q3tts_kernel_launches", "q3tts_destroy", "q3tts_strerror",
+           "q3tts_step_frame_static")
 
 _lib = None
 
@@ -78,6 +81,7 @@ def load(path: str = LIB_PATH):
     L.q3tts_prefill.argtypes = [vp, C.c_int, vp, C.c_int]
     L.q3tts_step_frame.argtypes = [vp, C.POINTER(Sampling), C.POINTER(C.c_int32), C.c_int, vp, vp,
                                    vp, vp]
+    L.q3tts_step_frame_static.argtypes = [vp, C.POINTER(Sampling), C.c_int, vp, vp, vp, vp]
     L.q3tts_read_pending.argtypes = [vp, C.c_int, vp, vp]
     L.q3tts_reset.argtypes = [vp, C.c_int]
     L.q3tts_stream_length.argtypes = [vp, C.c_int]
@@ -191,6 +195,16 @@ class Engine:
         ids = (C.c_int32 * n)(*[int(i) for i in stream_ids])
         _check(load().q3tts_step_frame(self.h, sp, ids, n, uniforms.data_ptr(), codes.data_ptr(),
                                        _ptr(forced), _ptr(logits)), "q3tts_step_frame")
+
+    def step_frame_static(self, stream_id: int, sampling, uniforms, codes, forced=None,
+                          logits=None) -> None:
+        """One frame of one stream through q3tts_step_frame_static (scratch in the
+        library's static device array); tensors as for step_frame with n = 1."""
+        sp = sampling_struct(sampling)
+        _check(load().q3tts_step_frame_static(self.h, C.byref(sp), int(stream_id),
+                                              uniforms.data_ptr(), codes.data_ptr(),
+                                              _ptr(forced), _ptr(logits)),
+               "q3tts_step_frame_static")
 
     def read_pending(self, stream_id: int):
         import torch

@@ -44,12 +44,17 @@ extern "C" {
 #define Q3TTS_ERR_TIMEOUT (-4)     /* a device-side wait gave up (bounded spin) */
 #define Q3TTS_ERR_UNSUPPORTED (-5) /* configuration outside what the kernels handle */
 #define Q3TTS_ERR_STATE (-6)       /* e.g. a frame requested before prefill */
+#define Q3TTS_ERR_SCRATCH (-7)     /* static scratch array too small (q3tts_step_frame_static) */
 
 #define Q3TTS_F32 0
 #define Q3TTS_BF16 1
 
 #define Q3TTS_MAX_STREAMS 256
 #define Q3TTS_N_CODEBOOKS 16
+
+/* Size of the library's static device scratch array (384 KiB), used only by
+ * q3tts_step_frame_static. */
+#define Q3TTS_STATIC_SCRATCH_BYTES 393216
 
 /* Model and engine shape.  Dimensions follow the Qwen3-style decoder: RMSNorm
  * (eps rms_eps), per-head q/k RMSNorm when qk_norm != 0, rotate-half RoPE
@@ -161,6 +166,46 @@ int q3tts_prefill(q3tts_handle* h, int stream_id, const float* embeds_dev, int l
 int q3tts_step_frame(q3tts_handle* h, const q3tts_sampling* params, const int32_t* stream_ids,
                      int n_active, const float* uniforms_dev, int32_t* codes_dev,
                      const int32_t* forced_dev, float* logits_dev);
+
+/* One frame of one stream, like q3tts_step_frame with n_active = 1, but with
+ * the frame's scratch (residual vectors, QKV rows, attention partials,
+ * CodePredictor logits, embedding sum, grid-barrier words) in a static device
+ * array of Q3TTS_STATIC_SCRATCH_BYTES bytes compiled into the library instead
+ * of the handle's workspace.  The method's description has no counterpart to
+ * this call.  It exists for callers that must not allocate while decoding: a
+ * real-time audio thread that cannot afford an allocator's locks or an
+ * implicit device synchronisation, or a host embedding the library under a
+ * fixed memory budget.  After the set-up below the call requests no device
+ * memory and builds no host container (q3tts_step_frame builds a host-side
+ * list per call).
+ *   params           host, one q3tts_sampling; top_k must be in 1..64 for a
+ *                    sampled draw (or the draw greedy), else
+ *                    Q3TTS_ERR_UNSUPPORTED.
+ *   stream_id        the stream to advance by one Talker position.
+ *   uniforms_dev, codes_dev, forced_dev, logits_dev
+ *                    as for q3tts_step_frame with n_active = 1.
+ * Set-up: the first call on a device (from any handle) looks up the array's
+ * device address with that device current, clears its barrier words and
+ * synchronises the handle's stream once; the first call on a handle also
+ * reserves its per-stream page lists (a host allocation).  Make one call
+ * before any stream capture and before any code that must not allocate.
+ * The barrier words must be zero when a frame starts: module load and the
+ * set-up leave them zero, every completed frame leaves them zero, and
+ * q3tts_sync_status clears them after a frame that reported an error.
+ * The array is one per device and process, shared by every handle: calls
+ * that overlap on the device (two streams, two threads, two handles) race on
+ * it and corrupt each other's frames -- serialise them.
+ * Errors, all returned before anything is launched and with the stream left
+ * as it was: Q3TTS_ERR_ARG for a bad pointer, stream id or sampling value;
+ * then the configuration checks -- Q3TTS_ERR_UNSUPPORTED if the persistent
+ * frame kernel cannot run this handle or these sampling settings,
+ * Q3TTS_ERR_SCRATCH if this configuration's scratch exceeds the array; then
+ * Q3TTS_ERR_STATE / Q3TTS_ERR_CAPACITY as for q3tts_step_frame.  A failed
+ * launch returns Q3TTS_ERR_CUDA; device-side errors are reported by
+ * q3tts_sync_status. */
+int q3tts_step_frame_static(q3tts_handle* h, const q3tts_sampling* params, int stream_id,
+                            const float* uniforms_dev, int32_t* codes_dev,
+                            const int32_t* forced_dev, float* logits_dev);
 
 /* Copies a stream's pending state to device buffers (either may be NULL):
  * hidden_dev fp32 [D_t], logits_dev fp32 [V_t].  Asynchronous. */

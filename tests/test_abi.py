@@ -41,6 +41,8 @@ def test_header_constants_match_binding():
     assert int(consts["Q3TTS_ERR_TIMEOUT"]) == q3tts.ERR_TIMEOUT
     assert int(consts["Q3TTS_ERR_UNSUPPORTED"]) == q3tts.ERR_UNSUPPORTED
     assert int(consts["Q3TTS_ERR_STATE"]) == q3tts.ERR_STATE
+    assert int(consts["Q3TTS_ERR_SCRATCH"]) == q3tts.ERR_SCRATCH
+    assert int(consts["Q3TTS_STATIC_SCRATCH_BYTES"]) == q3tts.STATIC_SCRATCH_BYTES
     assert int(consts["Q3TTS_MAX_STREAMS"]) == q3tts.MAX_STREAMS
     assert int(consts["Q3TTS_BF16"]) == q3tts.BF16
 
