@@ -56,8 +56,8 @@ constexpr int FK_CONSUMER_WARPS = 8;
 constexpr int FK_CONSUMERS = FK_CONSUMER_WARPS * 32;
 constexpr int FK_PRODUCER_THREADS = 32;  // one warp; one thread issues the copies
 constexpr int FK_THREADS = FK_PRODUCER_THREADS + FK_CONSUMERS;
-constexpr int FK_STAGE = 16384;
-constexpr int FK_NSTAGE = 6;
+constexpr int FK_STAGE = 12288;  // one ring chunk: 3 rows of 2048 bf16, one 2048-wide FFN unit
+constexpr int FK_NSTAGE = 11;
 constexpr int FK_TMAX = 2;     // tokens per pass (CodePredictor pass 0 carries two)
 constexpr int FK_DMAX = 2048;  // widest hidden state staged in shared memory
 constexpr int FK_HDMAX = 128;
@@ -69,21 +69,19 @@ constexpr long long FK_WAIT_CYCLES = 4000000000ll;  // ~2 s at GB300 clocks
 // copied into a double-buffered shared-memory slot one layer ahead.
 constexpr int FK_SIDE_BYTES = (2 * FK_DMAX + 2 * FK_HDMAX) * 4;
 constexpr int FK_MAXLAYERS = 64;  // Talker + CodePredictor layers held in shared memory
-constexpr int FK_TASKROWS = 64;   // most rows one CTA owns in a row-split GEMV
+constexpr int FK_GROUP = 3;       // rows one warp keeps in registers in a row GEMV
+constexpr int FK_YCOLS = 64;      // FFN output columns of one lane over a gang (2048 / 32)
+constexpr int FK_GANG = 2;        // warps that stream one ring chunk together
+constexpr int FK_NGANG = FK_CONSUMER_WARPS / FK_GANG;
+constexpr int FK_XCH = 64;        // floats one gang exchanges per chunk (rows x tokens, or a tile's columns)
 
 static_assert(FAST_NT == FK_CONSUMERS, "the register sampler runs on the consumer warps");
 
 struct LayerDev {
   const void* side;   // [g_attn D | g_ffn D | g_q hd | g_k hd], weight dtype, contiguous
   const void* w_qkv;
-  const void* w_oT;   // [Hq][D][hd]: for each head, one hd-long row per output column
-  const void* w_gate;
-  const void* w_up;
-  const void* w_dT;   // [F][D]: down projection transposed
-  const void* g_attn;
-  const void* g_ffn;
-  const void* g_q;
-  const void* g_k;
+  const void* w_oT;   // o_proj tiles [Hq][ceil(D/32)][hd/8][32][8] (see oproj_tiles)
+  const void* w_ffn;  // [F][3][D]: FFN unit f = gate row f, up row f, column f of W_down
 };
 
 struct FKParams {
@@ -164,6 +162,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, unsigned parity) {
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// As mbar_try_wait, but the thread may be suspended up to about `ns`
+// nanoseconds while the phase is incomplete (woken early when it completes),
+// so a waiting thread issues few instructions.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* b, unsigned parity, unsigned ns) {
+  unsigned ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity), "r"(ns)
       : "memory");
   return ok != 0;
 }
@@ -266,15 +278,16 @@ struct FKSmem {
   FKParams prm;
   LayerDev lay[FK_MAXLAYERS];  // Talker layers, then CodePredictor layers
   union {
-    float xs[FK_TMAX * FK_DMAX];  // normed activations of the current GEMV (plane layout)
+    struct {
+      float xs[FK_TMAX * FK_DMAX];      // normed activations of the current GEMV (plane layout)
+      float yred[32 * FK_YCOLS];        // FFN output of the CTA, lane-transposed (see phase_ffn)
+    } g;
     FastSamplerSmem smp;
     AttnScratch att;
   } u;
   float os[2][FK_TMAX][FK_HDMAX];  // attention outputs of the CTA's (<= 2) heads, plane layout
-  float av[2][FK_TMAX][64];        // SwiGLU values of a row group (double-buffered)
-  float gu[2][FK_TMAX][128];       // gate (0..63) and up (64..127) sums of a row group
-  float acc[FK_TMAX][FK_TASKROWS]; // row sums of the current GEMV task
   float red[FK_TMAX][FK_CONSUMER_WARPS];
+  float xch[FK_NGANG][2][FK_GANG * FK_XCH];  // a gang's partial sums per warp (double-buffered by chunk)
   float rope_c[17][FK_HDMAX / 2];  // rows 0..15: CodePredictor positions; 16: the Talker position
   float rope_s[17][FK_HDMAX / 2];
   alignas(128) unsigned char side[2][FK_SIDE_BYTES];
@@ -355,21 +368,10 @@ __device__ __forceinline__ const WT* side_begin(Cons& c) {
 }
 
 // Done with the current layer's gains: the slot may be refilled (not after an
-// abort, for the reason given at release_n).
+// abort, for the reason given at release_at).
 __device__ __forceinline__ void side_end(Cons& c) {
   if (c.tid == 0 && !c.aborted) mbar_arrive(&c.sm->side_empty[c.layer & 1]);
   c.layer++;
-}
-
-// Hands ring slots back to the producer.  After an abort a consumer has
-// stopped waiting for data, so it must not free slots either: the producer then
-// blocks, sees the abort flag and lets its in-flight copies land before the CTA
-// can exit.
-__device__ __forceinline__ void release_n(Cons& c, int count) {
-  __syncwarp();
-  if (c.lane == 0 && !c.aborted)
-    for (int i = 0; i < count; ++i) mbar_arrive(&c.sm->empty[(c.n + i) % FK_NSTAGE]);
-  c.n += count;
 }
 
 // Grid-wide barrier of all CTAs' consumers: a monotonic arrival counter,
@@ -400,162 +402,206 @@ __device__ void grid_sync(Cons& c) {
   if (c.sm->flag) c.aborted = true;
 }
 
-// -------------------------------------------------------------- GEMV core
+// ------------------------------------------------------------ streaming
+//
+// Ring chunk n belongs to gang n % 4 -- a pair of consumer warps that stream
+// it together, each taking every other 256-wide block of the reduction (or
+// every other hd block of an o_proj tile), meeting once per chunk through a
+// named barrier of the pair and a small exchange buffer.  No block-wide
+// synchronisation happens inside a streaming loop.  A streaming loop keeps
+// what it touches per chunk in registers (the Stream state, hoisted pointers).
 
-template <class WT>
-__device__ __forceinline__ void ld8_smem(const WT* p, float* w);
-template <>
-__device__ __forceinline__ void ld8_smem<bf16>(const bf16* p, float* w) {
-  unpack_bf16x8(*reinterpret_cast<const uint4*>(p), w);
-}
-template <>
-__device__ __forceinline__ void ld8_smem<float>(const float* p, float* w) {
-  float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+__device__ __forceinline__ FKSmem* fk_sm() { return reinterpret_cast<FKSmem*>(fk_smem_raw); }
+
+struct Stream {
+  int lane, gang, j;  // j: the warp's place in its gang
+  bool aborted;
+  const int* abort_flag;
+  int* err;
+};
+
+__device__ __forceinline__ Stream stream_begin(const Cons& c) {
+  Stream s;
+  s.lane = c.lane;
+  s.gang = c.warp / FK_GANG;
+  s.j = c.warp % FK_GANG;
+  s.aborted = c.aborted;
+  s.abort_flag = c.p->abort_flag;
+  s.err = c.p->err;
+  return s;
 }
 
-__device__ __forceinline__ float dot8(const float* w, float4 a, float4 b, float acc) {
-  acc = fmaf(w[0], a.x, acc); acc = fmaf(w[1], a.y, acc); acc = fmaf(w[2], a.z, acc);
-  acc = fmaf(w[3], a.w, acc); acc = fmaf(w[4], b.x, acc); acc = fmaf(w[5], b.y, acc);
-  acc = fmaf(w[6], b.z, acc); acc = fmaf(w[7], b.w, acc);
-  return acc;
+// The gang's named barrier (ids 2..5; 0 is __syncthreads, 1 the consumers').
+__device__ __forceinline__ void gang_sync(const Stream& s) {
+  asm volatile("bar.sync %0, %1;" ::"r"(2 + s.gang), "n"(FK_GANG * 32) : "memory");
 }
 
-// One row of the ring chunk (K weights at shared offset w) against T
-// plane-layout vectors at shared offsets x0, x1; G lanes share the row (lane sl
-// covers k = 8 sl + 8 G i); reduction over the G-lane group.  All 32 lanes
-// must call it.
-template <class WT>
-__device__ __forceinline__ void row_dot(uint32_t w, int K, int G, int sl, bool valid, uint32_t x0,
-                                        uint32_t x1, int T, float& r0, float& r1) {
-  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-  if (valid) {
-    uint32_t wo = w + (uint32_t)(sl * 8 * (int)sizeof(WT));
-    uint32_t xa = x0 + (uint32_t)sl * 16u, xb = xa + (uint32_t)K * 2u;
-    uint32_t ya = x1 + (uint32_t)sl * 16u, yb = ya + (uint32_t)K * 2u;
-    const uint32_t wstep = (uint32_t)(G * 8 * (int)sizeof(WT)), xstep = (uint32_t)G * 16u;
-    for (int k = sl * 8; k < K; k += G * 8, wo += wstep, xa += xstep, xb += xstep, ya += xstep, yb += xstep) {
-      float wv[8];
-      lds_w8<WT>(wo, wv);
-      const float4 p = lds_f4(xa), q = lds_f4(xb);
-      a0 = fmaf(wv[0], p.x, a0); a0 = fmaf(wv[1], p.y, a0); a0 = fmaf(wv[2], p.z, a0); a0 = fmaf(wv[3], p.w, a0);
-      b0 = fmaf(wv[4], q.x, b0); b0 = fmaf(wv[5], q.y, b0); b0 = fmaf(wv[6], q.z, b0); b0 = fmaf(wv[7], q.w, b0);
-      if (T > 1) {
-        const float4 p1 = lds_f4(ya), q1 = lds_f4(yb);
-        a1 = fmaf(wv[0], p1.x, a1); a1 = fmaf(wv[1], p1.y, a1); a1 = fmaf(wv[2], p1.z, a1); a1 = fmaf(wv[3], p1.w, a1);
-        b1 = fmaf(wv[4], q1.x, b1); b1 = fmaf(wv[5], q1.y, b1); b1 = fmaf(wv[6], q1.z, b1); b1 = fmaf(wv[7], q1.w, b1);
+// The gang's first chunk at or after n0.
+__device__ __forceinline__ uint32_t first_chunk(uint32_t n0, int gang) {
+  return n0 + (uint32_t)((gang - (int)(n0 % FK_NGANG) + FK_NGANG) % FK_NGANG);
+}
+
+// Exchange buffer of chunk n for the gang (alternates between two).
+__device__ __forceinline__ float* xch_buf(const Stream& s, uint32_t n) {
+  return fk_sm()->xch[s.gang][(n / FK_NGANG) & 1];
+}
+
+// Waits (bounded) for ring chunk n; returns its shared-memory offset.
+__device__ __forceinline__ uint32_t chunk_wait(Stream& s, uint32_t n) {
+  FKSmem* sm = fk_sm();
+  const uint32_t slot = n % FK_NSTAGE;
+  if (!s.aborted) {
+    const unsigned par = (n / FK_NSTAGE) & 1u;
+    if (!__all_sync(0xffffffffu, mbar_try_wait(&sm->full[slot], par))) {
+      const long long t0 = clock64();
+      unsigned it = 0;
+      bool ab = false;
+      while (!mbar_try_wait(&sm->full[slot], par)) {
+        if ((++it & 255u) == 0 && (ld_volatile(s.abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
+          ab = true;
+          break;
+        }
+      }
+      s.aborted = __any_sync(0xffffffffu, ab);  // one decision per warp
+      if (s.aborted && s.lane == 0) {
+        atomicCAS(s.err, 0, Q3TTS_ERR_TIMEOUT);
+        atomicExch(const_cast<int*>(s.abort_flag), 1);
       }
     }
   }
-  r0 = a0 + b0;
-  r1 = a1 + b1;
-  for (int o = G / 2; o > 0; o >>= 1) {
-    r0 += __shfl_xor_sync(0xffffffffu, r0, o);
-    if (T > 1) r1 += __shfl_xor_sync(0xffffffffu, r1, o);
-  }
+  return soff(sm->ring[slot]);
 }
 
-__device__ __forceinline__ int lanes_per_row(int K) { return K >= 256 ? 32 : (K >= 128 ? 16 : 8); }
-
-// Segments per row so that nr rows keep all eight warps busy: the largest
-// power of two S with nr * S <= 8 and K a multiple of 8 S.
-__device__ __forceinline__ int row_segments(int nr, int K) {
-  int S = 1;
-  while (nr * S * 2 <= FK_CONSUMER_WARPS && K % (16 * S) == 0) S *= 2;
-  return S;
+// Hands ring chunk n back to the producer: one arrival, from the gang's first
+// warp after the gang's last barrier of the chunk (so both warps are done with
+// it).  After an abort a consumer has stopped waiting for data, so it must not
+// free slots either: the producer then blocks, sees the abort flag and lets
+// its in-flight copies land before the CTA can exit.
+__device__ __forceinline__ void chunk_release(const Stream& s, uint32_t n) {
+  if (s.j == 0 && s.lane == 0 && !s.aborted) mbar_arrive(&fk_sm()->empty[n % FK_NSTAGE]);
 }
 
-// Partial dot product of one row segment [k0, k1) of the row at shared offset
-// w against T plane-layout vectors (shared offsets x0, x1 = x0 + 4K), reduced
-// over the warp (all 32 lanes call it).
+// 8 weights at shared offset w times 8 activations (plane halves xa, xb) into
+// the two partial sums a, b.
 template <class WT>
-__device__ __forceinline__ void seg_dot(uint32_t w, int K, int k0, int k1, int lane, uint32_t x0, int T,
-                                        float& r0, float& r1) {
-  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-  const int k = k0 + lane * 8;
-  uint32_t wo = w + (uint32_t)(k * (int)sizeof(WT));
-  uint32_t xa = x0 + (uint32_t)(k >> 3) * 16u, xb = xa + (uint32_t)K * 2u;
-  uint32_t ya = xa + (uint32_t)K * 4u, yb = ya + (uint32_t)K * 2u;
-  constexpr uint32_t wstep = 256 * sizeof(WT), xstep = 32 * 16;
-  const int n = k < k1 ? (k1 - k + 255) >> 8 : 0;
-#pragma unroll 2
-  for (int i = 0; i < n; ++i, wo += wstep, xa += xstep, xb += xstep, ya += xstep, yb += xstep) {
+__device__ __forceinline__ void fma8(uint32_t w, const float4& xa, const float4& xb, float& a, float& b) {
+  float wv[8];
+  lds_w8<WT>(w, wv);
+  a = fmaf(wv[0], xa.x, a); a = fmaf(wv[1], xa.y, a); a = fmaf(wv[2], xa.z, a); a = fmaf(wv[3], xa.w, a);
+  b = fmaf(wv[4], xb.x, b); b = fmaf(wv[5], xb.y, b); b = fmaf(wv[6], xb.z, b); b = fmaf(wv[7], xb.w, b);
+}
+
+// One 256-wide block of G rows (row pitch rb) against T tokens: lane l's 8
+// weights at w + r rb, activations at xa / xb + 4 K t.
+template <class WT, int T, int G>
+__device__ __forceinline__ void rows_block(uint32_t w, int rb, uint32_t xa, uint32_t xb, int K4,
+                                           float (&a)[T][G], float (&b)[T][G]) {
+  float4 va[T], vb[T];
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    va[t] = lds_f4(xa + (uint32_t)(t * K4));
+    vb[t] = lds_f4(xb + (uint32_t)(t * K4));
+  }
+#pragma unroll
+  for (int r = 0; r < G; ++r) {
     float wv[8];
-    lds_w8<WT>(wo, wv);
-    const float4 p = lds_f4(xa), q = lds_f4(xb);
-    a0 = fmaf(wv[0], p.x, a0); a0 = fmaf(wv[1], p.y, a0); a0 = fmaf(wv[2], p.z, a0); a0 = fmaf(wv[3], p.w, a0);
-    b0 = fmaf(wv[4], q.x, b0); b0 = fmaf(wv[5], q.y, b0); b0 = fmaf(wv[6], q.z, b0); b0 = fmaf(wv[7], q.w, b0);
-    if (T > 1) {
-      const float4 p1 = lds_f4(ya), q1 = lds_f4(yb);
-      a1 = fmaf(wv[0], p1.x, a1); a1 = fmaf(wv[1], p1.y, a1); a1 = fmaf(wv[2], p1.z, a1); a1 = fmaf(wv[3], p1.w, a1);
-      b1 = fmaf(wv[4], q1.x, b1); b1 = fmaf(wv[5], q1.y, b1); b1 = fmaf(wv[6], q1.z, b1); b1 = fmaf(wv[7], q1.w, b1);
+    lds_w8<WT>(w + (uint32_t)(r * rb), wv);
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      a[t][r] = fmaf(wv[0], va[t].x, a[t][r]); a[t][r] = fmaf(wv[1], va[t].y, a[t][r]);
+      a[t][r] = fmaf(wv[2], va[t].z, a[t][r]); a[t][r] = fmaf(wv[3], va[t].w, a[t][r]);
+      b[t][r] = fmaf(wv[4], vb[t].x, b[t][r]); b[t][r] = fmaf(wv[5], vb[t].y, b[t][r]);
+      b[t][r] = fmaf(wv[6], vb[t].z, b[t][r]); b[t][r] = fmaf(wv[7], vb[t].w, b[t][r]);
     }
   }
-  r0 = warp_sum(a0 + b0);
-  r1 = T > 1 ? warp_sum(a1 + b1) : 0.f;
 }
 
-// Rows [r0, r1) (at most FK_TASKROWS) of a row-major [*, K] matrix with
-// K >= 256, streamed from the ring, against the plane-layout vectors
-// xs + t * K: each chunk's rows are cut into segments so all warps work, the
-// segment sums meet in shared memory, and epi(row, t, value) runs once per row
-// at the end (one thread per (row, t)).
+// This warp's share (256-wide blocks i = j, j + 2, ..., and the ragged tail
+// block if it falls to j) of the dot products of G consecutive rows (shared
+// offset w, pitch rb, K weights) with T plane-layout vectors at xs; the
+// warp-reduced partial sums land in every lane.
+template <class WT, int T, int G>
+__device__ __forceinline__ void rows_part(uint32_t w, int rb, int K, uint32_t xs, int lane, int j,
+                                          float (&out)[T][G]) {
+  float a[T][G], b[T][G];
+#pragma unroll
+  for (int t = 0; t < T; ++t)
+#pragma unroll
+    for (int r = 0; r < G; ++r) a[t][r] = b[t][r] = 0.f;
+  const uint32_t wl = w + (uint32_t)(lane * 8 * (int)sizeof(WT));
+  const uint32_t xa = xs + (uint32_t)lane * 16u, xb = xa + (uint32_t)K * 2u;
+  const int nfull = K >> 8, K4 = K * 4;
+#pragma unroll 2
+  for (int i = j; i < nfull; i += FK_GANG)
+    rows_block<WT, T, G>(wl + (uint32_t)(i * 256 * (int)sizeof(WT)), rb, xa + (uint32_t)(i * 512),
+                         xb + (uint32_t)(i * 512), K4, a, b);
+  if ((K & 255) && (nfull % FK_GANG) == j && lane * 8 < (K & 255))
+    rows_block<WT, T, G>(wl + (uint32_t)(nfull * 256 * (int)sizeof(WT)), rb, xa + (uint32_t)(nfull * 512),
+                         xb + (uint32_t)(nfull * 512), K4, a, b);
+#pragma unroll
+  for (int t = 0; t < T; ++t)
+#pragma unroll
+    for (int r = 0; r < G; ++r) out[t][r] = warp_sum(a[t][r] + b[t][r]);
+}
+
+// Rows [r, r + G) of a chunk: each warp posts its partial sums to its half of
+// the exchange buffer (index r T + t).
+template <class WT, int T, int G>
+__device__ __forceinline__ void rows_group(uint32_t w, int r, int rb, int K, uint32_t xs, const Stream& s, float* xb) {
+  float o[T][G];
+  rows_part<WT, T, G>(w + (uint32_t)(r * rb), rb, K, xs, s.lane, s.j, o);
+  if (s.lane == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int t = 0; t < T; ++t) xb[s.j * FK_XCH + (r + g) * T + t] = o[t][g];
+  }
+}
+
+// All R rows of a chunk (R T <= FK_XCH); after the gang barrier the first
+// warp's lane 0 passes each completed sum to epi(r, t, v).
+template <class WT, int T, class Epi>
+__device__ __forceinline__ void chunk_rows(uint32_t w, int R, int K, int rb, uint32_t xs, const Stream& s, float* xb,
+                                           Epi& epi) {
+  constexpr int G = FK_GROUP;
+  int r = 0;
+  for (; r + G <= R; r += G) rows_group<WT, T, G>(w, r, rb, K, xs, s, xb);
+  if (R - r == 2)
+    rows_group<WT, T, 2>(w, r, rb, K, xs, s, xb);
+  else if (R - r == 1)
+    rows_group<WT, T, 1>(w, r, rb, K, xs, s, xb);
+  gang_sync(s);
+  if (s.j == 0 && s.lane == 0)
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+      for (int t = 0; t < T; ++t) epi(i, t, xb[i * T + t] + xb[FK_XCH + i * T + t]);
+}
+
+// Rows [r0, r1) of a row-major [*, K] matrix streamed from the ring (the
+// chunks the producer cut them into), against the T plane-layout vectors at
+// xs; epi(row, t, value) once per row and token.  Advances c.n past the rows'
+// chunks.
 template <class WT, class Epi>
-__device__ void gemv_task(Cons& c, int r0, int r1, int K, int T, const float* xs, Epi epi) {
-  const int nrows = r1 - r0;
-  for (int e = c.tid; e < FK_TMAX * FK_TASKROWS; e += FK_CONSUMERS) (&c.sm->acc[0][0])[e] = 0.f;
-  consumer_sync();
-  const int rpc = rows_per_chunk(K * (int)sizeof(WT));
-  for (int r = r0; r < r1; r += rpc) {
-    const int nr = min(rpc, r1 - r);
-    const int S = row_segments(nr, K), seg = K / S, lg = __ffs(S) - 1;
-    const uint32_t buf = soff(acquire_at(c, c.n));
-    for (int base = c.warp; base < nr * S; base += FK_CONSUMER_WARPS) {
-      const int row = base >> lg, sg = base & (S - 1);
-      float v0, v1;
-      seg_dot<WT>(buf + (uint32_t)(row * K * (int)sizeof(WT)), K, sg * seg, (sg + 1) * seg, c.lane, soff(xs), T,
-                  v0, v1);
-      if (c.lane == 0) {
-        atomicAdd(&c.sm->acc[0][r - r0 + row], v0);
-        if (T > 1) atomicAdd(&c.sm->acc[1][r - r0 + row], v1);
-      }
-    }
-    release_n(c, 1);
+__device__ __forceinline__ void stream_rows(Cons& c, int r0, int r1, int K, int T, const float* xs, Epi epi) {
+  Stream s = stream_begin(c);
+  const int rb = K * (int)sizeof(WT);
+  const int rpc = rows_per_chunk(rb);
+  const uint32_t n0 = c.n;
+  const uint32_t nch = r1 > r0 ? (uint32_t)((r1 - r0 + rpc - 1) / rpc) : 0u;
+  const uint32_t x = soff(xs);
+  for (uint32_t n = first_chunk(n0, s.gang); n < n0 + nch; n += FK_NGANG) {
+    const uint32_t buf = chunk_wait(s, n);
+    const int base = r0 + (int)(n - n0) * rpc, R = min(rpc, r1 - base);
+    auto e = [&](int r, int t, float v) { epi(base + r, t, v); };
+    float* xb = xch_buf(s, n);
+    if (T > 1)
+      chunk_rows<WT, 2>(buf, R, K, rb, x, s, xb, e);
+    else
+      chunk_rows<WT, 1>(buf, R, K, rb, x, s, xb, e);
+    chunk_release(s, n);
   }
-  consumer_sync();
-  for (int e = c.tid; e < nrows * T; e += FK_CONSUMERS) {
-    const int t = e / nrows, i = e % nrows;
-    epi(r0 + i, t, c.sm->acc[t][i]);
-  }
-}
-
-// Rows [r0, r1) of a row-major [*, K] matrix with short rows (K < 256, the
-// per-head o_proj rows): G lanes per row, several rows per warp, epi(row, t,
-// value) per row as it completes.  xsel(row, t) gives the plane-layout vector.
-template <class WT, class XSel, class Epi>
-__device__ void gemv_rows(Cons& c, int r0, int r1, int K, int T, XSel xsel, Epi epi) {
-  const int row_bytes = K * (int)sizeof(WT);
-  const int rpc = rows_per_chunk(row_bytes);
-  const int G = lanes_per_row(K);
-  const int gpw = 32 / G, nslots = FK_CONSUMER_WARPS * gpw;
-  const int sub = c.lane / G, sl = c.lane % G;
-  for (int r = r0; r < r1; r += rpc) {
-    const int nr = min(rpc, r1 - r);
-    const uint32_t buf = soff(acquire_at(c, c.n));
-    for (int base = c.warp * gpw; base < nr; base += nslots) {
-      const int i = base + sub;
-      const bool valid = i < nr;
-      const int row = r + (valid ? i : 0);
-      float v0, v1;
-      row_dot<WT>(buf + (uint32_t)((valid ? i : 0) * row_bytes), K, G, sl, valid, soff(xsel(row, 0)),
-                  soff(xsel(row, T > 1 ? 1 : 0)), T, v0, v1);
-      if (valid && sl == 0) {
-        epi(row, 0, v0);
-        if (T > 1) epi(row, 1, v1);
-      }
-    }
-    release_n(c, 1);
-  }
+  c.aborted = s.aborted;
+  c.n = n0 + nch;
 }
 
 // ------------------------------------------------------- residual helpers
@@ -580,7 +626,7 @@ template <class WT>
 __device__ __noinline__ void load_norm(Cons& c, bool from_xs, int src, int t0, int T, int D, const WT* g,
                                        int fold_a, int fold_b, float* out) {
   const FKParams& p = *c.p;
-  float* xs = c.sm->u.xs;
+  float* xs = c.sm->u.g.xs;
   constexpr int PER = FK_TMAX * FK_DMAX / 4 / FK_CONSUMERS;  // float4 per thread, at most 4
   const int nq = D / 4;                                       // float4 per token
   float4 xv[PER];
@@ -759,24 +805,80 @@ __device__ __noinline__ void phase_qkv(Cons& c, int D, int T, int in, bool from_
   load_norm<WT>(c, from_xs, in, 0, T, D, side, xnext(in, 1), xnext(in, 2), nullptr);
   int lo, hi;
   split(p.qkv_rows, p.ncta, c.cta, lo, hi);
-  gemv_task<WT>(c, lo, hi, D, T, c.sm->u.xs,
-                [&](int row, int t, float v) { p.qkv[(size_t)t * p.qkv_rows + row] = v; });
+  float* qkv = p.qkv;
+  const int qr = p.qkv_rows;
+  stream_rows<WT>(c, lo, hi, D, T, c.sm->u.g.xs, [=](int row, int t, float v) { qkv[t * qr + row] = v; });
   grid_sync(c);
 }
 
-// o_proj over the CTA's (head, output column) range; os holds the heads'
-// outputs; the sums go into both X_a and X_b.
+// o_proj is cut into tiles of 32 output columns of one head.  A tile is
+// stored lane-interleaved, [hd/8][32][8]: lane l's 8 weights of hd block kb
+// (column 32 j + l of W_o, inputs h hd + 8 kb ..) sit at (kb 32 + l) 8, so a
+// warp reads a tile with conflict-free 16-byte loads and every lane owns one
+// output column -- no cross-lane reduction.  The CTA's tiles are [t0, t1)
+// of Hq * ceil(D / 32).
+__device__ __forceinline__ int oproj_nt(int D) { return (D + 31) >> 5; }
+__device__ __forceinline__ void oproj_tiles(const FKParams& p, int D, int cta, int& t0, int& t1) {
+  split(p.Hq * oproj_nt(D), p.ncta, cta, t0, t1);
+}
+
+// The CTA's o_proj tiles against the attention outputs of its (<= 2) heads
+// (os, plane layout; h_first is the first head); each column's sum goes into
+// both X_a and X_b.  The two warps of a gang take alternate hd blocks of a
+// tile and meet in the exchange buffer.
 template <class WT>
-__device__ void oproj_cols(Cons& c, int D, int T, int xa, int xb, int v0, int v1, int h_first) {
+__device__ void oproj_cols(Cons& c, int D, int T, int xa, int xb, int t0, int t1, int h_first) {
   const FKParams& p = *c.p;
-  const int boundary = (h_first + 1) * D;  // first column of the CTA's second head
-  gemv_rows<WT>(
-      c, v0, v1, p.hd, T, [&](int row, int t) { return c.sm->os[row >= boundary ? 1 : 0][t]; },
-      [&](int row, int t, float v) {
-        const int col = row >= boundary ? row - boundary : row - (boundary - D);
-        atomicAdd(xbuf(p, xa, t) + col, v);
-        atomicAdd(xbuf(p, xb, t) + col, v);
-      });
+  Stream s = stream_begin(c);
+  const int hd = p.hd, nt = oproj_nt(D), nkb = hd >> 3, dmax = p.dmax;
+  const int tb = 32 * hd * (int)sizeof(WT);
+  const int tpc = rows_per_chunk(tb);
+  float* XA = xbuf(p, xa, 0);
+  float* XB = xbuf(p, xb, 0);
+  FKSmem* sm = fk_sm();
+  const uint32_t os0 = soff(sm->os[0][0]);
+  constexpr uint32_t OS_HEAD = FK_TMAX * FK_HDMAX * 4, OS_TOK = FK_HDMAX * 4;
+  const uint32_t n0 = c.n;
+  const uint32_t nch = t1 > t0 ? (uint32_t)((t1 - t0 + tpc - 1) / tpc) : 0u;
+  for (uint32_t n = first_chunk(n0, s.gang); n < n0 + nch; n += FK_NGANG) {
+    const uint32_t buf = chunk_wait(s, n);
+    float* xbf = xch_buf(s, n);
+    const int tf = t0 + (int)(n - n0) * tpc, ntl = min(tpc, t1 - tf);
+    for (int jt = 0; jt < ntl; ++jt) {
+      const int ti = tf + jt, h = ti / nt, col = (ti - h * nt) * 32 + s.lane;
+      const uint32_t xo = os0 + (uint32_t)(h - h_first) * OS_HEAD;
+      const uint32_t w = buf + (uint32_t)(jt * tb + s.lane * 8 * (int)sizeof(WT));
+      float a[FK_TMAX] = {0.f, 0.f}, b[FK_TMAX] = {0.f, 0.f};
+      if (T > 1) {
+#pragma unroll 2
+        for (int kb = s.j; kb < nkb; kb += FK_GANG) {
+          const uint32_t wk = w + (uint32_t)(kb * 256 * (int)sizeof(WT));
+          fma8<WT>(wk, lds_f4(xo + (uint32_t)(kb * 16)), lds_f4(xo + (uint32_t)(2 * hd + kb * 16)), a[0], b[0]);
+          fma8<WT>(wk, lds_f4(xo + OS_TOK + (uint32_t)(kb * 16)), lds_f4(xo + OS_TOK + (uint32_t)(2 * hd + kb * 16)),
+                   a[1], b[1]);
+        }
+      } else {
+#pragma unroll 4
+        for (int kb = s.j; kb < nkb; kb += FK_GANG)
+          fma8<WT>(w + (uint32_t)(kb * 256 * (int)sizeof(WT)), lds_f4(xo + (uint32_t)(kb * 16)),
+                   lds_f4(xo + (uint32_t)(2 * hd + kb * 16)), a[0], b[0]);
+      }
+      xbf[s.j * FK_XCH + s.lane] = a[0] + b[0];
+      if (T > 1) xbf[s.j * FK_XCH + 32 + s.lane] = a[1] + b[1];
+      gang_sync(s);
+      if (s.j == 0 && col < D) {
+        for (int t = 0; t < T; ++t) {
+          const float v = xbf[t * 32 + s.lane] + xbf[FK_XCH + t * 32 + s.lane];
+          atomicAdd(XA + t * dmax + col, v);
+          atomicAdd(XB + t * dmax + col, v);
+        }
+      }
+      gang_sync(s);  // the buffer is rewritten by the next tile
+    }
+    chunk_release(s, n);
+  }
+  c.aborted = s.aborted;
+  c.n = n0 + nch;
 }
 
 // Stores a warp's head vector (lane holds l + 32 j) into plane layout.
@@ -793,9 +895,10 @@ template <class WT>
 __device__ __noinline__ void phase_cp_attn(Cons& c, int layer, int T, int pos0, int xa, int xb) {
   const FKParams& p = *c.p;
   const int D = p.Dc, hd = p.hd, Hq = p.Hq, Hkv = p.Hkv, rep = Hq / Hkv, J = hd / 32;
-  int v0, v1;
-  split(Hq * D, p.ncta, c.cta, v0, v1);
-  const int h_first = v0 / D, h_last = (v1 - 1) / D;
+  const int nt = oproj_nt(D);
+  int v0, v1;  // the CTA's o_proj tiles
+  oproj_tiles(p, D, c.cta, v0, v1);
+  const int h_first = v0 / nt, h_last = (v1 - 1) / nt;
   const int nh = v1 > v0 ? h_last - h_first + 1 : 0;
   const int npair = nh * T;
   const int g_first = h_first / rep;
@@ -849,7 +952,7 @@ __device__ __noinline__ void phase_cp_attn(Cons& c, int layer, int T, int pos0, 
       if (sp < S && sp >= pos0 && gi < ng) {
         const int g = g_first + gi;
         norm_rope_head(p, c.sm, kk[np][gi], side_gk<WT>(c, D), cp_rope_row(sp), c.lane);
-        const long long first = (long long)g * rep * D;
+        const int first = g * rep * nt;  // first o_proj tile of the group's first q head
         if (first >= v0 && first < v1) {
           float* kc = (float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 0, g);
           float* vc = (float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 1, g);
@@ -1033,10 +1136,10 @@ __device__ __noinline__ void phase_talker_attn(Cons& c, int layer) {
 template <class WT>
 __device__ __noinline__ void phase_talker_oproj(Cons& c, int xa, int xb) {
   const FKParams& p = *c.p;
-  const int D = p.Dt, hd = p.hd, Hq = p.Hq, cpg = p.ncta / p.Hkv;
-  int v0, v1;
-  split(Hq * D, p.ncta, c.cta, v0, v1);
-  const int h_first = v0 / D, h_last = (v1 - 1) / D;
+  const int D = p.Dt, hd = p.hd, cpg = p.ncta / p.Hkv, nt = oproj_nt(D);
+  int v0, v1;  // the CTA's o_proj tiles
+  oproj_tiles(p, D, c.cta, v0, v1);
+  const int h_first = v0 / nt, h_last = (v1 - 1) / nt;
   const int nh = v1 > v0 ? h_last - h_first + 1 : 0;
   constexpr int CMAX = 20;  // chunks per kv group handled in one batch of loads
   for (int e = c.tid; e < nh * hd; e += FK_CONSUMERS) {
@@ -1074,88 +1177,161 @@ __device__ __noinline__ void phase_talker_oproj(Cons& c, int xa, int xb) {
   grid_sync(c);
 }
 
-// Phase C: y = X_a (input + attention), RMSNorm, gate and up rows of the
-// CTA's FFN slice (gate rows and up rows on different warps), SwiGLU, the
-// matching rows of the transposed down projection; the partial D-vector is
-// added into X_b with float4 atomics.
+// One 256-wide block of an FFN unit's gate and up rows (at g, g + rb) against
+// T tokens.
+template <class WT, int T>
+__device__ __forceinline__ void gu_block(uint32_t g, uint32_t rb, uint32_t xa, uint32_t xb, int D4, float (&ga)[T],
+                                         float (&gb)[T], float (&ua)[T], float (&ub)[T]) {
+  float g8[8], u8[8];
+  lds_w8<WT>(g, g8);
+  lds_w8<WT>(g + rb, u8);
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    const float4 va = lds_f4(xa + (uint32_t)(t * D4)), vb = lds_f4(xb + (uint32_t)(t * D4));
+    ga[t] = fmaf(g8[0], va.x, ga[t]); ga[t] = fmaf(g8[1], va.y, ga[t]);
+    ga[t] = fmaf(g8[2], va.z, ga[t]); ga[t] = fmaf(g8[3], va.w, ga[t]);
+    gb[t] = fmaf(g8[4], vb.x, gb[t]); gb[t] = fmaf(g8[5], vb.y, gb[t]);
+    gb[t] = fmaf(g8[6], vb.z, gb[t]); gb[t] = fmaf(g8[7], vb.w, gb[t]);
+    ua[t] = fmaf(u8[0], va.x, ua[t]); ua[t] = fmaf(u8[1], va.y, ua[t]);
+    ua[t] = fmaf(u8[2], va.z, ua[t]); ua[t] = fmaf(u8[3], va.w, ua[t]);
+    ub[t] = fmaf(u8[4], vb.x, ub[t]); ub[t] = fmaf(u8[5], vb.y, ub[t]);
+    ub[t] = fmaf(u8[6], vb.z, ub[t]); ub[t] = fmaf(u8[7], vb.w, ub[t]);
+  }
+}
+
+// One FFN unit f at shared offset u (gate row, up row, down column; D weights
+// each), shared by the two warps of a gang: each takes alternate 256-wide
+// blocks of the gate/up dot products, the partial sums meet in the exchange
+// buffer slot xu (2 T floats per warp), both form a_t = silu(gate_f . x_t) *
+// (up_f . x_t), and each adds a_t W_down[:, f] into the columns of its own
+// blocks: lane l, block i = 2 ii + j holds columns 8 l + 256 i + q as
+// y[t (4 / T) + ii][q].
+template <class WT, int T>
+__device__ __forceinline__ void ffn_unit(uint32_t u, int D, uint32_t xs, const Stream& s, float* xu,
+                                         float (&y)[4][8]) {
+  constexpr int IM2 = 4 / T;  // blocks per token and warp (D <= 256 IM2 FK_GANG)
+  const uint32_t rb = (uint32_t)D * (uint32_t)sizeof(WT);
+  const uint32_t wl = u + (uint32_t)(s.lane * 8 * (int)sizeof(WT));
+  const uint32_t xa = xs + (uint32_t)s.lane * 16u, xb = xa + (uint32_t)D * 2u;
+  const int nfull = D >> 8, D4 = D * 4;
+  const bool tail = (D & 255) && (nfull % FK_GANG) == s.j && s.lane * 8 < (D & 255);
+  float ga[T], gb[T], ua[T], ub[T];
+#pragma unroll
+  for (int t = 0; t < T; ++t) ga[t] = gb[t] = ua[t] = ub[t] = 0.f;
+#pragma unroll 2
+  for (int i = s.j; i < nfull; i += FK_GANG)
+    gu_block<WT, T>(wl + (uint32_t)(i * 256 * (int)sizeof(WT)), rb, xa + (uint32_t)(i * 512), xb + (uint32_t)(i * 512),
+                    D4, ga, gb, ua, ub);
+  if (tail)
+    gu_block<WT, T>(wl + (uint32_t)(nfull * 256 * (int)sizeof(WT)), rb, xa + (uint32_t)(nfull * 512),
+                    xb + (uint32_t)(nfull * 512), D4, ga, gb, ua, ub);
+  float pg[T], pu[T];
+#pragma unroll
+  for (int t = 0; t < T; ++t) {
+    pg[t] = warp_sum(ga[t] + gb[t]);
+    pu[t] = warp_sum(ua[t] + ub[t]);
+  }
+  if (s.lane == 0) {
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+      xu[s.j * FK_XCH + 2 * t] = pg[t];
+      xu[s.j * FK_XCH + 2 * t + 1] = pu[t];
+    }
+  }
+  gang_sync(s);
+  float act[T];
+#pragma unroll
+  for (int t = 0; t < T; ++t)
+    act[t] = silu(xu[2 * t] + xu[FK_XCH + 2 * t]) * (xu[2 * t + 1] + xu[FK_XCH + 2 * t + 1]);
+  const uint32_t wd = wl + 2u * rb;
+  const bool dtail = (D & 255) && s.lane * 8 < (D & 255);
+#pragma unroll
+  for (int ii = 0; ii < IM2; ++ii) {
+    const int i = ii * FK_GANG + s.j;
+    if (i < nfull || (i == nfull && dtail)) {
+      float d8[8];
+      lds_w8<WT>(wd + (uint32_t)(i * 256 * (int)sizeof(WT)), d8);
+#pragma unroll
+      for (int t = 0; t < T; ++t)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) y[t * IM2 + ii][q] = fmaf(act[t], d8[q], y[t * IM2 + ii][q]);
+    }
+  }
+}
+
+// The gang's share of the CTA's FFN units [f0, f1) (chunks n0 .. n0 + nch),
+// its down-projection sums added into yred (layout at phase_ffn).
+template <class WT, int T>
+__device__ __noinline__ void ffn_stream(Cons& c, int D, int f0, int f1, uint32_t n0, uint32_t nch) {
+  constexpr int IM = 8 / T, IM2 = 4 / T;
+  Stream s = stream_begin(c);
+  const int ub = 3 * D * (int)sizeof(WT);
+  const int upc = rows_per_chunk(ub);
+  FKSmem* sm = fk_sm();
+  const uint32_t xs = soff(sm->u.g.xs);
+  float y[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int q = 0; q < 8; ++q) y[i][q] = 0.f;
+  bool any = false;
+  for (uint32_t n = first_chunk(n0, s.gang); n < n0 + nch; n += FK_NGANG) {
+    const uint32_t buf = chunk_wait(s, n);
+    float* xbf = xch_buf(s, n);
+    const int nu = min(upc, f1 - (f0 + (int)(n - n0) * upc));
+    for (int jj = 0; jj < nu; ++jj) ffn_unit<WT, T>(buf + (uint32_t)(jj * ub), D, xs, s, xbf + 4 * jj, y);
+    gang_sync(s);  // both warps are done with the chunk
+    chunk_release(s, n);
+    any = true;
+  }
+  c.aborted = s.aborted;
+  if (any) {
+    float* yred = sm->u.g.yred;
+    const int k0 = s.lane * 8;
+#pragma unroll
+    for (int t = 0; t < T; ++t)
+#pragma unroll
+      for (int ii = 0; ii < IM2; ++ii) {
+        const int i = ii * FK_GANG + s.j;
+        if (k0 + 256 * i < D) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) atomicAdd(&yred[((t * IM + i) * 8 + q) * 32 + s.lane], y[t * IM2 + ii][q]);
+        }
+      }
+  }
+}
+
+// Phase C: y = X_a (input + attention), RMSNorm, then the CTA's FFN units
+// (split-K over the FFN width), each warp accumulating its units' down
+// projection in registers; the warps' sums meet in shared memory and the
+// CTA's partial D-vector is added into X_b with float4 atomics.  yred holds
+// the sums lane-transposed -- element ((t IM + i) 8 + q) 32 + lane, IM = 8 / T,
+// is column 8 lane + 256 i + q of token t -- so the warps' shared-memory adds
+// are bank-conflict free.
 template <class WT>
 __device__ __noinline__ void phase_ffn(Cons& c, int D, int F, int T, int xa, int xb) {
   const FKParams& p = *c.p;
-  for (int e = c.tid; e < FK_TMAX * 128; e += FK_CONSUMERS) (&c.sm->gu[0][0][0])[e] = 0.f;
+  float* yred = c.sm->u.g.yred;
+  for (int e = c.tid; e < 32 * FK_YCOLS; e += FK_CONSUMERS) yred[e] = 0.f;  // before load_norm's barriers
   load_norm<WT>(c, false, xa, 0, T, D, side_cur<WT>(c) + D, -1, -1, nullptr);
   side_end(c);
-  float* xs = c.sm->u.xs;
   int f0, f1;
   split(F, p.ncta, c.cta, f0, f1);
-  const int row_bytes = D * (int)sizeof(WT);
-  const int gpr = min(64, rows_per_chunk(row_bytes));
-  float acc[FK_TMAX][8];
-#pragma unroll
-  for (int t = 0; t < FK_TMAX; ++t)
-#pragma unroll
-    for (int q = 0; q < 8; ++q) acc[t][q] = 0.f;
-  const int col = c.tid * 8;  // this thread's 8 output columns (D <= 2048)
-  int buf = 0;
-  for (int g = f0; g < f1; g += gpr, buf ^= 1) {
-    const int ng = min(gpr, f1 - g);
-    // gate and up rows of the group (two consecutive ring chunks)
-    const uint32_t wg = soff(acquire_at(c, c.n));
-    const uint32_t wu = soff(acquire_at(c, c.n + 1));
-    const int S = row_segments(2 * ng, D), seg = D / S, lg = __ffs(S) - 1;
-    for (int item = c.warp; item < 2 * ng * S; item += FK_CONSUMER_WARPS) {
-      const int r2 = item >> lg, sg = item & (S - 1), which = r2 >= ng ? 1 : 0, i = r2 - which * ng;
-      float v0, v1;
-      seg_dot<WT>((which ? wu : wg) + (uint32_t)(i * row_bytes), D, sg * seg, (sg + 1) * seg, c.lane, soff(xs), T,
-                  v0, v1);
-      if (c.lane == 0) {
-        atomicAdd(&c.sm->gu[buf][0][which * 64 + i], v0);
-        if (T > 1) atomicAdd(&c.sm->gu[buf][1][which * 64 + i], v1);
-      }
-    }
-    release_n(c, 2);
-    consumer_sync();
-    for (int e = c.tid; e < T * ng; e += FK_CONSUMERS) {
-      const int t = e / ng, i = e % ng;
-      c.sm->av[buf][t][i] = silu(c.sm->gu[buf][t][i]) * c.sm->gu[buf][t][64 + i];
-    }
-    for (int e = c.tid; e < FK_TMAX * 128; e += FK_CONSUMERS) (&c.sm->gu[buf ^ 1][0][0])[e] = 0.f;
-    consumer_sync();
-    const uint32_t wd = soff(acquire_at(c, c.n));
-    if (col < D) {
-      uint32_t wo = wd + (uint32_t)(col * (int)sizeof(WT));
-      if (T > 1) {
-        for (int i = 0; i < ng; ++i, wo += (uint32_t)row_bytes) {
-          float w[8];
-          lds_w8<WT>(wo, w);
-          const float a0 = c.sm->av[buf][0][i], a1 = c.sm->av[buf][1][i];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            acc[0][q] = fmaf(a0, w[q], acc[0][q]);
-            acc[1][q] = fmaf(a1, w[q], acc[1][q]);
-          }
-        }
-      } else {
-#pragma unroll 2
-        for (int i = 0; i < ng; ++i, wo += (uint32_t)row_bytes) {
-          float w[8];
-          lds_w8<WT>(wo, w);
-          const float a0 = c.sm->av[buf][0][i];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) acc[0][q] = fmaf(a0, w[q], acc[0][q]);
-        }
-      }
-    }
-    release_n(c, 1);
-  }
-  if (col < D && f1 > f0) {
-#pragma unroll
-    for (int t = 0; t < FK_TMAX; ++t) {
-      if (t < T) {
-        float* dst = xbuf(p, xb, t) + col;
-        atomicAdd(reinterpret_cast<float4*>(dst), make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]));
-        atomicAdd(reinterpret_cast<float4*>(dst + 4), make_float4(acc[t][4], acc[t][5], acc[t][6], acc[t][7]));
-      }
-    }
+  const int upc = rows_per_chunk(3 * D * (int)sizeof(WT));
+  const uint32_t n0 = c.n;
+  const uint32_t nch = f1 > f0 ? (uint32_t)((f1 - f0 + upc - 1) / upc) : 0u;
+  if (T > 1)
+    ffn_stream<WT, 2>(c, D, f0, f1, n0, nch);
+  else
+    ffn_stream<WT, 1>(c, D, f0, f1, n0, nch);
+  c.n = n0 + nch;
+  consumer_sync();
+  const int IM = 8 / T, nq = D / 4;
+  for (int e = c.tid; e < T * nq; e += FK_CONSUMERS) {
+    const int t = e / nq, col = (e % nq) * 4;
+    const int i = col >> 8, ln = (col & 255) >> 3, q = col & 7;
+    const float* src = yred + ((t * IM + i) * 8 + q) * 32 + ln;
+    atomicAdd(reinterpret_cast<float4*>(xbuf(p, xb, t) + col), make_float4(src[0], src[32], src[64], src[96]));
   }
   grid_sync(c);
 }
@@ -1166,7 +1342,7 @@ template <class WT>
 __device__ __noinline__ void cp_tokens(Cons& c, int j, int fed) {
   const FKParams& p = *c.p;
   const int Dt = p.Dt;
-  float* xs = c.sm->u.xs;
+  float* xs = c.sm->u.g.xs;
   if (j == 0) {
     const WT* e = (const WT*)p.e_codec + (size_t)fed * Dt;
     for (int i = c.tid; i < Dt; i += FK_CONSUMERS) {
@@ -1239,7 +1415,9 @@ __device__ void consumer(const FKParams& p, FKSmem* sm) {
       // z = W_p u into X_0 (rows of the CTA)
       int lo, hi;
       split(p.Dc, p.ncta, c.cta, lo, hi);
-      gemv_task<WT>(c, lo, hi, p.Dt, T, sm->u.xs, [&](int row, int t, float v) { xbuf(p, 0, t)[row] = v; });
+      float* X0 = xbuf(p, 0, 0);
+      const int dmax = p.dmax;
+      stream_rows<WT>(c, lo, hi, p.Dt, T, sm->u.g.xs, [=](int row, int t, float v) { X0[t * dmax + row] = v; });
       grid_sync(c);
       from_xs = false;
     }
@@ -1255,7 +1433,8 @@ __device__ void consumer(const FKParams& p, FKSmem* sm) {
     {
       int lo, hi;
       split(p.Vc, p.ncta, c.cta, lo, hi);
-      gemv_task<WT>(c, lo, hi, p.Dc, 1, sm->u.xs, [&](int row, int, float v) { p.cp_logits[row] = v; });
+      float* lg = p.cp_logits;
+      stream_rows<WT>(c, lo, hi, p.Dc, 1, sm->u.g.xs, [=](int row, int, float v) { lg[row] = v; });
     }
     grid_sync(c);
   }
@@ -1263,7 +1442,7 @@ __device__ void consumer(const FKParams& p, FKSmem* sm) {
   {
     const int fed15 = draw_code(c, Q3TTS_N_CODEBOOKS - 1);
     const WT* e = (const WT*)p.cp_embeds + ((size_t)(Q3TTS_N_CODEBOOKS - 2) * p.Vc + fed15) * p.Dt;
-    float* xs = sm->u.xs;
+    float* xs = sm->u.g.xs;
     for (int i = c.tid; i < p.Dt; i += FK_CONSUMERS) put_plane(xs, p.Dt, i, __ldcg(p.xsum + i) + to_f(e[i]));
     consumer_sync();
   }
@@ -1284,7 +1463,7 @@ __device__ void consumer(const FKParams& p, FKSmem* sm) {
     int lo, hi;
     split(p.Vt, p.ncta, c.cta, lo, hi);
     float* out = p.pending_logits + (size_t)p.sid * p.Vt;
-    gemv_task<WT>(c, lo, hi, p.Dt, 1, sm->u.xs, [&](int row, int, float v) { out[row] = v; });
+    stream_rows<WT>(c, lo, hi, p.Dt, 1, sm->u.g.xs, [=](int row, int, float v) { out[row] = v; });
   }
   if (c.cta == 0 && c.tid == 0) p.history[(size_t)p.sid * p.Vt + fed0] = 1;
   consumer_sync();
@@ -1319,10 +1498,9 @@ struct Producer {
       const unsigned par = ((n / FK_NSTAGE) - 1) & 1u;
       long long t0 = clock64();
       unsigned it = 0;
-      while (!mbar_try_wait(&sm->empty[s], par)) {
-        // the ring is full most of the time: sleep between polls so this warp
-        // does not take issue slots from the consumer warps of its scheduler
-        __nanosleep(200);
+      // the ring is full most of the time: wait suspended so this warp does
+      // not take issue slots from the consumer warps of its scheduler
+      while (!mbar_try_wait_sleep(&sm->empty[s], par, 2000)) {
         if ((++it & 15u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
           raise_abort(p, Q3TTS_ERR_TIMEOUT);
           stop = true;
@@ -1347,18 +1525,8 @@ struct Producer {
     rows(base, lo, hi, row_bytes);
   }
 
-  __device__ void ffn(const LayerDev& L, int D, int F) {
-    const int row_bytes = D * (int)sizeof(WT);
-    const int gpr = min(64, rows_per_chunk(row_bytes));
-    int f0, f1;
-    split(F, p.ncta, cta, f0, f1);
-    for (int g = f0; g < f1; g += gpr) {
-      const int ng = min(gpr, f1 - g);
-      rows(L.w_gate, g, g + ng, row_bytes);
-      rows(L.w_up, g, g + ng, row_bytes);
-      rows(L.w_dT, g, g + ng, row_bytes);
-    }
-  }
+  // The CTA's FFN units (gate row, up row, down column: 3 D weights each).
+  __device__ void ffn(const LayerDev& L, int D, int F) { split_rows(L.w_ffn, F, 3 * D * (int)sizeof(WT)); }
 
   int nlayers = 0;  // layers in the frame (15 CodePredictor passes, then the Talker)
   int layer_i = 0;  // next layer whose weights are streamed
@@ -1376,8 +1544,7 @@ struct Producer {
       const unsigned par = ((k >> 1) - 1) & 1u;
       long long t0 = clock64();
       unsigned it = 0;
-      while (!mbar_try_wait(&sm->side_empty[slot], par)) {
-        __nanosleep(200);
+      while (!mbar_try_wait_sleep(&sm->side_empty[slot], par, 2000)) {
         if ((++it & 15u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
           raise_abort(p, Q3TTS_ERR_TIMEOUT);
           stop = true;
@@ -1398,7 +1565,7 @@ struct Producer {
     if (layer_i >= 1) side(layer_i + 1);
     layer_i++;
     split_rows(L.w_qkv, p.qkv_rows, D * esz);
-    split_rows(L.w_oT, p.Hq * D, p.hd * esz);
+    split_rows(L.w_oT, p.Hq * oproj_nt(D), 32 * p.hd * esz);
     ffn(L, D, F);
   }
 
@@ -1439,7 +1606,7 @@ __global__ void __launch_bounds__(FK_THREADS, 1) frame_kernel(const __grid_const
   if (threadIdx.x == 0) {
     for (int s = 0; s < FK_NSTAGE; ++s) {
       mbar_init(&sm->full[s], 1);
-      mbar_init(&sm->empty[s], FK_CONSUMER_WARPS);
+      mbar_init(&sm->empty[s], 1);  // the one warp that streams the chunk
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm->side_full[s], 1);
@@ -1462,17 +1629,24 @@ __global__ void __launch_bounds__(FK_THREADS, 1) frame_kernel(const __grid_const
 
 template <class T>
 __global__ void repack_oT_kernel(const T* __restrict__ w_o, T* __restrict__ w_oT, int D, int Hq, int hd) {
-  // w_oT[h][c][d] = w_o[c][h*hd + d]
-  const size_t n = (size_t)Hq * D * hd;
-  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
-    const size_t d = e % hd, c = (e / hd) % D, h = e / ((size_t)hd * D);
-    w_oT[e] = w_o[c * (size_t)Hq * hd + h * hd + d];
+  // tile (h, j): w_oT[((h NT + j) (hd/8) + kb) 256 + 8 l + e] = w_o[32 j + l][h hd + 8 kb + e], 0 past D
+  const int NT = (D + 31) / 32, nkb = hd / 8;
+  const size_t n = (size_t)Hq * NT * 32 * hd;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int e = (int)(i % 8), l = (int)((i / 8) % 32);
+    const size_t rest = i / 256;
+    const int kb = (int)(rest % nkb);
+    const size_t tile = rest / nkb;
+    const int j = (int)(tile % NT), h = (int)(tile / NT);
+    const int col = 32 * j + l;
+    w_oT[i] = col < D ? w_o[(size_t)col * Hq * hd + (size_t)h * hd + 8 * kb + e] : T(0.f);
   }
 }
 
 template <class T>
-__global__ void transpose_kernel(const T* __restrict__ in, T* __restrict__ out, int rows, int cols) {
-  // out[c][r] = in[r][c]
+__global__ void transpose_kernel(const T* __restrict__ in, T* __restrict__ out, int rows, int cols,
+                                 size_t ostride) {
+  // out[c * ostride + r] = in[r][c]
   __shared__ T tile[32][33];
   for (int r0 = blockIdx.y * 32; r0 < rows; r0 += gridDim.y * 32)
     for (int c0 = blockIdx.x * 32; c0 < cols; c0 += gridDim.x * 32) {
@@ -1483,7 +1657,7 @@ __global__ void transpose_kernel(const T* __restrict__ in, T* __restrict__ out, 
       __syncthreads();
       for (int i = threadIdx.y; i < 32; i += blockDim.y) {
         const int cc = c0 + i, r = r0 + threadIdx.x;
-        if (r < rows && cc < cols) out[(size_t)cc * rows + r] = tile[threadIdx.x][i];
+        if (r < rows && cc < cols) out[(size_t)cc * ostride + r] = tile[threadIdx.x][i];
       }
       __syncthreads();
     }
@@ -1503,8 +1677,10 @@ static size_t fk_layout(const q3tts_config& c, int ncta, FKState* st, char* base
     off = al256(off + bytes);
     return base ? base + o : nullptr;
   };
-  char* reT = take((size_t)c.talker_layers * ((size_t)Hq * hd * c.talker_hidden + (size_t)c.talker_ffn * c.talker_hidden) * esz);
-  char* reC = take((size_t)c.cp_layers * ((size_t)Hq * hd * c.cp_hidden + (size_t)c.cp_ffn * c.cp_hidden) * esz);
+  const size_t oT_t = (size_t)Hq * hd * 32 * ((c.talker_hidden + 31) / 32);
+  const size_t oT_c = (size_t)Hq * hd * 32 * ((c.cp_hidden + 31) / 32);
+  char* reT = take((size_t)c.talker_layers * (oT_t + 3 * (size_t)c.talker_ffn * c.talker_hidden) * esz);
+  char* reC = take((size_t)c.cp_layers * (oT_c + 3 * (size_t)c.cp_ffn * c.cp_hidden) * esz);
   char* sideT = take((size_t)c.talker_layers * (2 * c.talker_hidden + 2 * hd) * esz);
   char* sideC = take((size_t)c.cp_layers * (2 * c.cp_hidden + 2 * hd) * esz);
   char* tl = take(sizeof(LayerDev) * c.talker_layers);
@@ -1559,12 +1735,21 @@ int frame_kernel_create(q3tts_handle* h) {
       c.cp_vocab > SAMPLER_VMAX || (c.talker_hidden % 4) || (c.cp_hidden % 4))
     return Q3TTS_OK;
   const int ncta = std::min(h->n_sm, FK_MAXCTA);
-  // every CTA's o_proj column range must touch at most two heads
-  if (ncta < c.n_kv_heads || ncta < c.n_q_heads) return Q3TTS_OK;
-  // row-split tasks (QKV, heads, projection) must fit the task accumulator
-  const int most = std::max(std::max(h->qkv_rows, c.codec_vocab), std::max(c.cp_vocab, c.cp_hidden));
-  if ((most + ncta - 1) / ncta > FK_TASKROWS) return Q3TTS_OK;
-  // the per-CTA FFN slice must fit the gate/up scratch of one group (<= 64 rows)
+  // every CTA's o_proj tile range must touch at most two heads (32-column
+  // tiles, at most one head's worth per CTA); Talker attention needs a CTA
+  // per kv head
+  auto tiles_ok = [&](int D) {
+    const int nt = (D + 31) / 32;
+    return (c.n_q_heads * nt + ncta - 1) / ncta <= nt;
+  };
+  if (ncta < c.n_kv_heads || !tiles_ok(c.talker_hidden) || !tiles_ok(c.cp_hidden)) return Q3TTS_OK;
+  // a ring chunk holds at least one row and one FFN unit (3 D weights); the
+  // two-token CodePredictor pass keeps 2 x (D_c / 32) FFN sums per lane
+  const int esz_w = c.weight_dtype == Q3TTS_F32 ? 4 : 2;
+  if (3 * std::max(c.talker_hidden, c.cp_hidden) * esz_w > FK_STAGE || 2 * c.cp_hidden > 32 * FK_YCOLS)
+    return Q3TTS_OK;
+  // a gang exchanges at most FK_XCH partial sums per chunk (rows x 2 tokens)
+  if (2 * (FK_STAGE / (std::min(c.talker_hidden, c.cp_hidden) * esz_w)) > FK_XCH) return Q3TTS_OK;
   st->smem = sizeof(FKSmem);
   void* k = pick_kernel(c.weight_dtype, c.kv_dtype);
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st->smem) != cudaSuccess) {
@@ -1597,25 +1782,25 @@ int frame_kernel_create(q3tts_handle* h) {
       return false;
     d.side = side;
     d.w_qkv = w.w_qkv;
-    d.w_gate = w.w_gateup;
-    d.w_up = (const char*)w.w_gateup + (size_t)F * D * esz;
-    d.g_attn = w.g_attn_norm;
-    d.g_ffn = w.g_ffn_norm;
-    d.g_q = w.g_q_norm;
-    d.g_k = w.g_k_norm;
     char* oT = re;
-    re += (size_t)Hq * hd * D * esz;
-    char* dT = re;
-    re += (size_t)F * D * esz;
+    re += (size_t)Hq * hd * 32 * ((D + 31) / 32) * esz;
+    char* ffn = re;
+    re += 3 * (size_t)F * D * esz;
     d.w_oT = oT;
-    d.w_dT = dT;
+    d.w_ffn = ffn;
+    // FFN unit f = [gate row f | up row f | column f of W_down]
+    const size_t rb = (size_t)D * esz;
+    if (cudaMemcpy2DAsync(ffn, 3 * rb, w.w_gateup, rb, rb, F, cudaMemcpyDeviceToDevice, h->s) != cudaSuccess ||
+        cudaMemcpy2DAsync(ffn + rb, 3 * rb, (const char*)w.w_gateup + (size_t)F * rb, rb, rb, F,
+                          cudaMemcpyDeviceToDevice, h->s) != cudaSuccess)
+      return false;
     dim3 tb(32, 8), tg((F + 31) / 32 < 1024 ? (F + 31) / 32 : 1024, (D + 31) / 32 < 1024 ? (D + 31) / 32 : 1024);
     if (esz == 2) {
       repack_oT_kernel<bf16><<<1024, 256, 0, h->s>>>((const bf16*)w.w_o, (bf16*)oT, D, Hq, hd);
-      transpose_kernel<bf16><<<tg, tb, 0, h->s>>>((const bf16*)w.w_down, (bf16*)dT, D, F);
+      transpose_kernel<bf16><<<tg, tb, 0, h->s>>>((const bf16*)w.w_down, (bf16*)(ffn + 2 * rb), D, F, 3 * (size_t)D);
     } else {
       repack_oT_kernel<float><<<1024, 256, 0, h->s>>>((const float*)w.w_o, (float*)oT, D, Hq, hd);
-      transpose_kernel<float><<<tg, tb, 0, h->s>>>((const float*)w.w_down, (float*)dT, D, F);
+      transpose_kernel<float><<<tg, tb, 0, h->s>>>((const float*)w.w_down, (float*)(ffn + 2 * rb), D, F, 3 * (size_t)D);
     }
     return cudaGetLastError() == cudaSuccess;
   };
