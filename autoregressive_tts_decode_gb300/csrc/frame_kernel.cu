@@ -270,6 +270,15 @@ struct AttnScratch {
 };
 static_assert(FK_PAIRS >= FK_REPMAX, "talker attention keeps one partial per q head of a group");
 
+// Per consumer warp: ring chunks consumed, grid barriers passed, layers
+// started (side-slot index), whether the warp gave up after a timeout, and
+// the position in the frame's schedule.
+struct ConsState {
+  uint32_t n, phase, layer;
+  int aborted;
+  int k, in, from_xs, fed0;  // the frame schedule's loop state
+};
+
 struct FKSmem {
   alignas(128) unsigned char ring[FK_NSTAGE][FK_STAGE];
   // Launch parameters and per-layer pointer tables live in shared memory: a
@@ -299,20 +308,38 @@ struct FKSmem {
   alignas(8) uint64_t side_full[2];
   alignas(8) uint64_t side_empty[2];
   int flag;
+  ConsState cs[FK_CONSUMER_WARPS];
 };
 static_assert(sizeof(FKSmem) <= 227 * 1024, "persistent kernel shared memory");
 
 // ---------------------------------------------------------------- context
 
-struct Cons {
-  const FKParams* p;
-  FKSmem* sm;
-  int cta, tid, warp, lane;
-  uint32_t n;      // ring chunks consumed
-  uint32_t phase;  // grid barriers passed in this launch
-  uint32_t layer;  // layers started in this launch (side-slot index)
-  bool aborted;
-};
+// The consumer warps' context.  Nothing of it lives in local memory: the
+// launch parameters and the shared-memory layout sit at fixed shared
+// addresses, thread and block indices come from special registers, and each
+// warp's mutable state (ConsState) is a shared-memory record.  A local-memory
+// context would put a dependent load -- which can miss the small L1 left
+// beside the ring -- in front of every phase.  Cons is an empty tag passed by
+// value to the phase functions.
+struct Cons {};
+
+__device__ __forceinline__ FKSmem* fk_sm() { return reinterpret_cast<FKSmem*>(fk_smem_raw); }
+__device__ __forceinline__ const FKParams* fk_prm() { return &fk_sm()->prm; }
+__device__ __forceinline__ int ctid() { return (int)threadIdx.x - FK_PRODUCER_THREADS; }
+__device__ __forceinline__ int cwarp() { return ctid() >> 5; }
+__device__ __forceinline__ int clane() { return (int)threadIdx.x & 31; }
+__device__ __forceinline__ int ccta() { return (int)blockIdx.x; }
+__device__ __forceinline__ ConsState& cst() { return fk_sm()->cs[cwarp()]; }
+
+// Updates a field of the warp's record from all 32 lanes: the new value is
+// computed (from the old one) by every lane before any lane stores it, so the
+// identical stores cannot race with a lagging lane's read.
+template <class T>
+__device__ __forceinline__ void warp_set(T& field, T v) {
+  __syncwarp();
+  field = v;
+  __syncwarp();
+}
 
 struct ConsGroup {
   __device__ static int tid() { return threadIdx.x - FK_PRODUCER_THREADS; }
@@ -325,66 +352,49 @@ __device__ __forceinline__ void raise_abort(const FKParams& p, int code) {
   atomicExch(p.abort_flag, 1);
 }
 
-// Waits for ring chunk n (all lanes of the calling warp).
-__device__ __forceinline__ const unsigned char* acquire_at(Cons& c, uint32_t n) {
-  const int s = n % FK_NSTAGE;
-  const unsigned par = (n / FK_NSTAGE) & 1u;
-  if (!c.aborted) {
-    long long t0 = clock64();
-    unsigned it = 0;
-    while (!mbar_try_wait(&c.sm->full[s], par)) {
-      if ((++it & 255u) == 0 && (ld_volatile(c.p->abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
-        if (c.lane == 0) raise_abort(*c.p, Q3TTS_ERR_TIMEOUT);
-        c.aborted = true;
-        break;
-      }
-    }
-    c.aborted = __any_sync(0xffffffffu, c.aborted);  // one decision per warp
-  }
-  return c.sm->ring[s];
-}
-
 // Bounded wait on an arbitrary mbarrier phase (all lanes of the calling warp).
-__device__ __forceinline__ void wait_bar(Cons& c, uint64_t* bar, unsigned par) {
-  if (c.aborted) return;
+__device__ __forceinline__ void wait_bar(Cons c, uint64_t* bar, unsigned par) {
+  if (cst().aborted) return;
   long long t0 = clock64();
   unsigned it = 0;
+  bool ab = false;
   while (!mbar_try_wait(bar, par)) {
-    if ((++it & 255u) == 0 && (ld_volatile(c.p->abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
-      if (c.lane == 0) raise_abort(*c.p, Q3TTS_ERR_TIMEOUT);
-      c.aborted = true;
+    if ((++it & 255u) == 0 && (ld_volatile(fk_prm()->abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
+      ab = true;
       break;
     }
   }
-  c.aborted = __any_sync(0xffffffffu, c.aborted);  // one decision per warp
+  ab = __any_sync(0xffffffffu, ab);  // one decision per warp
+  if (ab && clane() == 0) raise_abort(*fk_prm(), Q3TTS_ERR_TIMEOUT);
+  warp_set(cst().aborted, ab ? 1 : 0);
 }
 
 // The side block of the layer being started (waits for its copy).
 template <class WT>
-__device__ __forceinline__ const WT* side_begin(Cons& c) {
-  const int slot = c.layer & 1;
-  wait_bar(c, &c.sm->side_full[slot], (c.layer >> 1) & 1u);
-  return reinterpret_cast<const WT*>(c.sm->side[slot]);
+__device__ __forceinline__ const WT* side_begin(Cons c) {
+  const int slot = cst().layer & 1;
+  wait_bar(c, &fk_sm()->side_full[slot], (cst().layer >> 1) & 1u);
+  return reinterpret_cast<const WT*>(fk_sm()->side[slot]);
 }
 
 // Done with the current layer's gains: the slot may be refilled (not after an
 // abort, for the reason given at release_at).
-__device__ __forceinline__ void side_end(Cons& c) {
-  if (c.tid == 0 && !c.aborted) mbar_arrive(&c.sm->side_empty[c.layer & 1]);
-  c.layer++;
+__device__ __forceinline__ void side_end(Cons c) {
+  if (ctid() == 0 && !cst().aborted) mbar_arrive(&fk_sm()->side_empty[cst().layer & 1]);
+  warp_set(cst().layer, cst().layer + 1u);
 }
 
 // Grid-wide barrier of all CTAs' consumers: a monotonic arrival counter,
 // release-add to arrive, acquire-load to wait (the last CTA to finish the
 // launch resets it).
-__device__ void grid_sync(Cons& c) {
+__device__ void grid_sync(Cons c) {
   consumer_sync();
-  if (c.tid == 0) {
-    const FKParams& p = *c.p;
+  if (ctid() == 0) {
+    const FKParams& p = *fk_prm();
     red_release_add(p.bar, 1u);
-    c.phase++;
-    const unsigned target = c.phase * (unsigned)p.ncta;
-    int fail = c.aborted ? 1 : 0;
+    cst().phase++;
+    const unsigned target = cst().phase * (unsigned)p.ncta;
+    int fail = cst().aborted ? 1 : 0;
     if (!fail) {
       long long t0 = clock64();
       unsigned it = 0;
@@ -396,10 +406,10 @@ __device__ void grid_sync(Cons& c) {
         }
       }
     }
-    c.sm->flag = fail;
+    fk_sm()->flag = fail;
   }
   consumer_sync();
-  if (c.sm->flag) c.aborted = true;
+  if (fk_sm()->flag) warp_set(cst().aborted, 1);
 }
 
 // ------------------------------------------------------------ streaming
@@ -411,8 +421,6 @@ __device__ void grid_sync(Cons& c) {
 // synchronisation happens inside a streaming loop.  A streaming loop keeps
 // what it touches per chunk in registers (the Stream state, hoisted pointers).
 
-__device__ __forceinline__ FKSmem* fk_sm() { return reinterpret_cast<FKSmem*>(fk_smem_raw); }
-
 struct Stream {
   int lane, gang, j;  // j: the warp's place in its gang
   bool aborted;
@@ -420,14 +428,14 @@ struct Stream {
   int* err;
 };
 
-__device__ __forceinline__ Stream stream_begin(const Cons& c) {
+__device__ __forceinline__ Stream stream_begin(Cons c) {
   Stream s;
-  s.lane = c.lane;
-  s.gang = c.warp / FK_GANG;
-  s.j = c.warp % FK_GANG;
-  s.aborted = c.aborted;
-  s.abort_flag = c.p->abort_flag;
-  s.err = c.p->err;
+  s.lane = clane();
+  s.gang = cwarp() / FK_GANG;
+  s.j = cwarp() % FK_GANG;
+  s.aborted = cst().aborted;
+  s.abort_flag = fk_prm()->abort_flag;
+  s.err = fk_prm()->err;
   return s;
 }
 
@@ -491,65 +499,89 @@ __device__ __forceinline__ void fma8(uint32_t w, const float4& xa, const float4&
   b = fmaf(wv[4], xb.x, b); b = fmaf(wv[5], xb.y, b); b = fmaf(wv[6], xb.z, b); b = fmaf(wv[7], xb.w, b);
 }
 
-// One 256-wide block of G rows (row pitch rb) against T tokens: lane l's 8
-// weights at w + r rb, activations at xa / xb + 4 K t.
-template <class WT, int T, int G>
-__device__ __forceinline__ void rows_block(uint32_t w, int rb, uint32_t xa, uint32_t xb, int K4,
-                                           float (&a)[T][G], float (&b)[T][G]) {
-  float4 va[T], vb[T];
+// The activations a warp multiplies, held in registers for a whole streaming
+// loop: warp j of a gang owns the 256-wide blocks i = j, j + 2, j + 4, j + 6
+// of the reduction (K <= 2048; the block holding the ragged tail K % 256
+// included), lane l elements 8 l + 256 i .. + 7 of token t in a[t][b] (first
+// four) and c[t][b] (last four).  Lanes past a ragged tail hold zeros and are
+// masked out of the weight loads.
+constexpr int FK_XB = 4;  // blocks per warp
+template <int T>
+struct XReg {
+  float4 a[T][FK_XB], c[T][FK_XB];
+};
+
+// Which of the warp's blocks exist for a reduction of length K: bit b set if
+// block 2 b + j has weights for this lane.
+__device__ __forceinline__ unsigned xblocks(int K, int lane, int j) {
+  const int nfull = K >> 8;
+  unsigned m = 0;
 #pragma unroll
-  for (int t = 0; t < T; ++t) {
-    va[t] = lds_f4(xa + (uint32_t)(t * K4));
-    vb[t] = lds_f4(xb + (uint32_t)(t * K4));
+  for (int b = 0; b < FK_XB; ++b) {
+    const int i = FK_GANG * b + j;
+    if (i < nfull || (i == nfull && lane * 8 < (K & 255))) m |= 1u << b;
   }
-#pragma unroll
-  for (int r = 0; r < G; ++r) {
-    float wv[8];
-    lds_w8<WT>(w + (uint32_t)(r * rb), wv);
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      a[t][r] = fmaf(wv[0], va[t].x, a[t][r]); a[t][r] = fmaf(wv[1], va[t].y, a[t][r]);
-      a[t][r] = fmaf(wv[2], va[t].z, a[t][r]); a[t][r] = fmaf(wv[3], va[t].w, a[t][r]);
-      b[t][r] = fmaf(wv[4], vb[t].x, b[t][r]); b[t][r] = fmaf(wv[5], vb[t].y, b[t][r]);
-      b[t][r] = fmaf(wv[6], vb[t].z, b[t][r]); b[t][r] = fmaf(wv[7], vb[t].w, b[t][r]);
-    }
-  }
+  return m;
 }
 
-// This warp's share (256-wide blocks i = j, j + 2, ..., and the ragged tail
-// block if it falls to j) of the dot products of G consecutive rows (shared
-// offset w, pitch rb, K weights) with T plane-layout vectors at xs; the
-// warp-reduced partial sums land in every lane.
+// Loads the warp's activation blocks from the plane-layout vectors at shared
+// offset xs (token t at xs + 4 K t).
+template <int T>
+__device__ __forceinline__ void load_xreg(XReg<T>& x, uint32_t xs, int K, int lane, int j, unsigned m) {
+#pragma unroll
+  for (int t = 0; t < T; ++t)
+#pragma unroll
+    for (int b = 0; b < FK_XB; ++b) {
+      const uint32_t o = xs + (uint32_t)(t * K * 4 + lane * 16 + (FK_GANG * b + j) * 512);
+      x.a[t][b] = (m >> b) & 1u ? lds_f4(o) : make_float4(0.f, 0.f, 0.f, 0.f);
+      x.c[t][b] = (m >> b) & 1u ? lds_f4(o + (uint32_t)K * 2u) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// 8 weights at shared offset w times the 8 activations (a, c) into acc.
+template <class WT>
+__device__ __forceinline__ float dot8w(uint32_t w, const float4& a, const float4& c, float acc) {
+  float wv[8];
+  lds_w8<WT>(w, wv);
+  float s = fmaf(wv[0], a.x, fmaf(wv[1], a.y, fmaf(wv[2], a.z, wv[3] * a.w)));
+  const float s2 = fmaf(wv[4], c.x, fmaf(wv[5], c.y, fmaf(wv[6], c.z, wv[7] * c.w)));
+  return acc + (s + s2);
+}
+
+// This warp's partial dot products of G consecutive rows (shared offset w,
+// pitch rb) with its activation blocks; warp-reduced, in every lane.
 template <class WT, int T, int G>
-__device__ __forceinline__ void rows_part(uint32_t w, int rb, int K, uint32_t xs, int lane, int j,
+__device__ __forceinline__ void rows_part(uint32_t w, int rb, const XReg<T>& x, unsigned m, int lane, int j,
                                           float (&out)[T][G]) {
-  float a[T][G], b[T][G];
+  float acc[T][G];
 #pragma unroll
   for (int t = 0; t < T; ++t)
 #pragma unroll
-    for (int r = 0; r < G; ++r) a[t][r] = b[t][r] = 0.f;
+    for (int r = 0; r < G; ++r) acc[t][r] = 0.f;
   const uint32_t wl = w + (uint32_t)(lane * 8 * (int)sizeof(WT));
-  const uint32_t xa = xs + (uint32_t)lane * 16u, xb = xa + (uint32_t)K * 2u;
-  const int nfull = K >> 8, K4 = K * 4;
-#pragma unroll 2
-  for (int i = j; i < nfull; i += FK_GANG)
-    rows_block<WT, T, G>(wl + (uint32_t)(i * 256 * (int)sizeof(WT)), rb, xa + (uint32_t)(i * 512),
-                         xb + (uint32_t)(i * 512), K4, a, b);
-  if ((K & 255) && (nfull % FK_GANG) == j && lane * 8 < (K & 255))
-    rows_block<WT, T, G>(wl + (uint32_t)(nfull * 256 * (int)sizeof(WT)), rb, xa + (uint32_t)(nfull * 512),
-                         xb + (uint32_t)(nfull * 512), K4, a, b);
+#pragma unroll
+  for (int b = 0; b < FK_XB; ++b) {
+    if ((m >> b) & 1u) {
+      const uint32_t wb = wl + (uint32_t)((FK_GANG * b + j) * 256 * (int)sizeof(WT));
+#pragma unroll
+      for (int r = 0; r < G; ++r)
+#pragma unroll
+        for (int t = 0; t < T; ++t) acc[t][r] = dot8w<WT>(wb + (uint32_t)(r * rb), x.a[t][b], x.c[t][b], acc[t][r]);
+    }
+  }
 #pragma unroll
   for (int t = 0; t < T; ++t)
 #pragma unroll
-    for (int r = 0; r < G; ++r) out[t][r] = warp_sum(a[t][r] + b[t][r]);
+    for (int r = 0; r < G; ++r) out[t][r] = warp_sum(acc[t][r]);
 }
 
 // Rows [r, r + G) of a chunk: each warp posts its partial sums to its half of
 // the exchange buffer (index r T + t).
 template <class WT, int T, int G>
-__device__ __forceinline__ void rows_group(uint32_t w, int r, int rb, int K, uint32_t xs, const Stream& s, float* xb) {
+__device__ __forceinline__ void rows_group(uint32_t w, int r, int rb, const XReg<T>& x, unsigned m, const Stream& s,
+                                           float* xb) {
   float o[T][G];
-  rows_part<WT, T, G>(w + (uint32_t)(r * rb), rb, K, xs, s.lane, s.j, o);
+  rows_part<WT, T, G>(w + (uint32_t)(r * rb), rb, x, m, s.lane, s.j, o);
   if (s.lane == 0) {
 #pragma unroll
     for (int g = 0; g < G; ++g)
@@ -561,15 +593,15 @@ __device__ __forceinline__ void rows_group(uint32_t w, int r, int rb, int K, uin
 // All R rows of a chunk (R T <= FK_XCH); after the gang barrier the first
 // warp's lane 0 passes each completed sum to epi(r, t, v).
 template <class WT, int T, class Epi>
-__device__ __forceinline__ void chunk_rows(uint32_t w, int R, int K, int rb, uint32_t xs, const Stream& s, float* xb,
-                                           Epi& epi) {
+__device__ __forceinline__ void chunk_rows(uint32_t w, int R, int rb, const XReg<T>& x, unsigned m, const Stream& s,
+                                           float* xb, Epi& epi) {
   constexpr int G = FK_GROUP;
   int r = 0;
-  for (; r + G <= R; r += G) rows_group<WT, T, G>(w, r, rb, K, xs, s, xb);
+  for (; r + G <= R; r += G) rows_group<WT, T, G>(w, r, rb, x, m, s, xb);
   if (R - r == 2)
-    rows_group<WT, T, 2>(w, r, rb, K, xs, s, xb);
+    rows_group<WT, T, 2>(w, r, rb, x, m, s, xb);
   else if (R - r == 1)
-    rows_group<WT, T, 1>(w, r, rb, K, xs, s, xb);
+    rows_group<WT, T, 1>(w, r, rb, x, m, s, xb);
   gang_sync(s);
   if (s.j == 0 && s.lane == 0)
     for (int i = 0; i < R; ++i)
@@ -577,31 +609,37 @@ __device__ __forceinline__ void chunk_rows(uint32_t w, int R, int K, int rb, uin
       for (int t = 0; t < T; ++t) epi(i, t, xb[i * T + t] + xb[FK_XCH + i * T + t]);
 }
 
-// Rows [r0, r1) of a row-major [*, K] matrix streamed from the ring (the
-// chunks the producer cut them into), against the T plane-layout vectors at
-// xs; epi(row, t, value) once per row and token.  Advances c.n past the rows'
-// chunks.
-template <class WT, class Epi>
-__device__ __forceinline__ void stream_rows(Cons& c, int r0, int r1, int K, int T, const float* xs, Epi epi) {
+template <class WT, int T, class Epi>
+__device__ __forceinline__ void stream_rows_t(Cons c, int r0, int r1, int K, uint32_t xs, Epi& epi) {
   Stream s = stream_begin(c);
   const int rb = K * (int)sizeof(WT);
   const int rpc = rows_per_chunk(rb);
-  const uint32_t n0 = c.n;
+  const uint32_t n0 = cst().n;
   const uint32_t nch = r1 > r0 ? (uint32_t)((r1 - r0 + rpc - 1) / rpc) : 0u;
-  const uint32_t x = soff(xs);
+  const unsigned m = xblocks(K, s.lane, s.j);
+  XReg<T> x;
+  load_xreg<T>(x, xs, K, s.lane, s.j, m);
   for (uint32_t n = first_chunk(n0, s.gang); n < n0 + nch; n += FK_NGANG) {
     const uint32_t buf = chunk_wait(s, n);
     const int base = r0 + (int)(n - n0) * rpc, R = min(rpc, r1 - base);
     auto e = [&](int r, int t, float v) { epi(base + r, t, v); };
-    float* xb = xch_buf(s, n);
-    if (T > 1)
-      chunk_rows<WT, 2>(buf, R, K, rb, x, s, xb, e);
-    else
-      chunk_rows<WT, 1>(buf, R, K, rb, x, s, xb, e);
+    chunk_rows<WT, T>(buf, R, rb, x, m, s, xch_buf(s, n), e);
     chunk_release(s, n);
   }
-  c.aborted = s.aborted;
-  c.n = n0 + nch;
+  warp_set(cst().aborted, s.aborted ? 1 : 0);
+  warp_set(cst().n, n0 + nch);
+}
+
+// Rows [r0, r1) of a row-major [*, K] matrix streamed from the ring (the
+// chunks the producer cut them into), against the T plane-layout vectors at
+// xs; epi(row, t, value) once per row and token.  Advances cst().n past the rows'
+// chunks.
+template <class WT, class Epi>
+__device__ __forceinline__ void stream_rows(Cons c, int r0, int r1, int K, int T, const float* xs, Epi epi) {
+  if (T > 1)
+    stream_rows_t<WT, 2>(c, r0, r1, K, soff(xs), epi);
+  else
+    stream_rows_t<WT, 1>(c, r0, r1, K, soff(xs), epi);
 }
 
 // ------------------------------------------------------- residual helpers
@@ -617,85 +655,114 @@ __device__ __forceinline__ float* xbuf(const FKParams& p, int idx, int t) {
 }
 __device__ __forceinline__ int xnext(int i, int k) { return (i + k) % 3; }
 
+// Gains g[i .. i+3] (weight dtype) as floats.
+template <class WT>
+__device__ __forceinline__ float4 gain4(const WT* g, int i);
+template <>
+__device__ __forceinline__ float4 gain4<bf16>(const bf16* g, int i) {
+  const uint2 u = *reinterpret_cast<const uint2*>(g + i);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                     __uint_as_float(u.y & 0xffff0000u));
+}
+template <>
+__device__ __forceinline__ float4 gain4<float>(const float* g, int i) {
+  return *reinterpret_cast<const float4*>(g + i);
+}
+
+// The CTA's slice [lo, hi) of a D-vector (32-bit arithmetic: D * ncta < 2^31).
+__device__ __forceinline__ void cta_slice(int D, int& lo, int& hi) {
+  const int nc = fk_prm()->ncta, cta = ccta();
+  lo = D * cta / nc;
+  hi = D * (cta + 1) / nc;
+}
+
 // Builds xs[t] = RMSNorm(x_t) * g (plane layout) for t < T, where x_t is
 // xs[t] itself (from_xs, raw plane layout) or buffer X_src of token t0 + t.
-// All loads of a thread are issued together.  With fold_a >= 0 the CTA's slice
-// of each raw x_t is written to X_fold_a and X_fold_b.  If out is given, the
-// CTA's slice of the normed x_0 goes there.
+// Thread e handles plane float4 e + 256 u of the T tokens; all of a thread's
+// loads are issued together.  With fold_a >= 0 the CTA's slice of each raw
+// x_t is written to X_fold_a and X_fold_b.  If out is given, the CTA's slice
+// of the normed x_0 goes there.  g points into shared memory (4-element
+// aligned groups).
 template <class WT>
-__device__ __noinline__ void load_norm(Cons& c, bool from_xs, int src, int t0, int T, int D, const WT* g,
-                                       int fold_a, int fold_b, float* out) {
-  const FKParams& p = *c.p;
-  float* xs = c.sm->u.g.xs;
+__device__ __forceinline__ void load_norm(Cons c, bool from_xs, int src, int t0, int T, int D, const WT* g,
+                                          int fold_a, int fold_b, float* out) {
+  const FKParams& p = *fk_prm();
+  float* xs = fk_sm()->u.g.xs;
   constexpr int PER = FK_TMAX * FK_DMAX / 4 / FK_CONSUMERS;  // float4 per thread, at most 4
-  const int nq = D / 4;                                       // float4 per token
+  const int nq = D >> 2, tot = T * nq, tid = ctid();
+  const float* xg = xbuf(p, src, t0);
+  const int dmax = p.dmax;
   float4 xv[PER];
-  float gv[PER][4];
-  float ss[FK_TMAX] = {0.f, 0.f};
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
-    const int e = c.tid + FK_CONSUMERS * u;
-    if (e < T * nq) {
-      const int t = e >= nq ? 1 : 0, pq = e - t * nq, i = plane_first(pq, D);
-      xv[u] = from_xs ? reinterpret_cast<const float4*>(xs + t * D)[pq] : ldcg4(xbuf(p, src, t0 + t) + i);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) gv[u][q] = to_f(g[i + q]);
+    const int e = tid + FK_CONSUMERS * u;
+    if (e < tot) {
+      const int t = e >= nq ? 1 : 0, pq = e - t * nq;
+      xv[u] = from_xs ? reinterpret_cast<const float4*>(xs + t * D)[pq]
+                      : ldcg4(xg + t * dmax + plane_first(pq, D));
+    } else {
+      xv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
+  float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
-    const int e = c.tid + FK_CONSUMERS * u;
-    if (e < T * nq) {
-      const int t = e >= nq ? 1 : 0;
-      const float v = xv[u].x * xv[u].x + xv[u].y * xv[u].y + xv[u].z * xv[u].z + xv[u].w * xv[u].w;
-      if (t == 0) ss[0] += v; else ss[1] += v;
-    }
+    const int e = tid + FK_CONSUMERS * u;
+    const float v = xv[u].x * xv[u].x + xv[u].y * xv[u].y + xv[u].z * xv[u].z + xv[u].w * xv[u].w;
+    if (e >= nq) ss1 += v; else ss0 += v;
+  }
+  ss0 = warp_sum(ss0);
+  ss1 = warp_sum(ss1);
+  if (clane() == 0) {
+    fk_sm()->red[0][cwarp()] = ss0;
+    fk_sm()->red[1][cwarp()] = ss1;
   }
   if (fold_a >= 0) {
     int lo, hi;
-    split(D, p.ncta, c.cta, lo, hi);
+    cta_slice(D, lo, hi);
+    float* fa = xbuf(p, fold_a, 0);
+    float* fb = xbuf(p, fold_b, 0);
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
-      const int e = c.tid + FK_CONSUMERS * u;
-      if (e < T * nq) {
+      const int e = tid + FK_CONSUMERS * u;
+      if (e < tot) {
         const int t = e >= nq ? 1 : 0, i = plane_first(e - t * nq, D);
-        const float vals[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+        if (i + 3 >= lo && i < hi) {
+          const float vals[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (i + q >= lo && i + q < hi) {
-            xbuf(p, fold_a, t)[i + q] = vals[q];
-            xbuf(p, fold_b, t)[i + q] = vals[q];
-          }
+          for (int q = 0; q < 4; ++q)
+            if (i + q >= lo && i + q < hi) {
+              fa[t * dmax + i + q] = vals[q];
+              fb[t * dmax + i + q] = vals[q];
+            }
+        }
       }
     }
   }
-#pragma unroll
-  for (int t = 0; t < FK_TMAX; ++t) {
-    const float v = warp_sum(ss[t]);
-    if (c.lane == 0) c.sm->red[t][c.warp] = v;
-  }
   consumer_sync();
-  float inv[FK_TMAX];
+  float inv0, inv1;
+  {
+    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-  for (int t = 0; t < FK_TMAX; ++t) {
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < FK_CONSUMER_WARPS; ++w) tot += c.sm->red[t][w];
-    inv[t] = 1.0f / sqrtf(tot / (float)D + p.eps);
+    for (int w = 0; w < FK_CONSUMER_WARPS; ++w) {
+      a0 += fk_sm()->red[0][w];
+      a1 += fk_sm()->red[1][w];
+    }
+    inv0 = 1.0f / sqrtf(a0 / (float)D + p.eps);
+    inv1 = 1.0f / sqrtf(a1 / (float)D + p.eps);
   }
   int lo = 0, hi = 0;
-  if (out) split(D, p.ncta, c.cta, lo, hi);
+  if (out) cta_slice(D, lo, hi);
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
-    const int e = c.tid + FK_CONSUMERS * u;
-    if (e < T * nq) {
-      const int t = e >= nq ? 1 : 0, pq = e - t * nq;
-      const float iv = t == 0 ? inv[0] : inv[1];
-      float4 y = make_float4(xv[u].x * iv * gv[u][0], xv[u].y * iv * gv[u][1], xv[u].z * iv * gv[u][2],
-                             xv[u].w * iv * gv[u][3]);
+    const int e = tid + FK_CONSUMERS * u;
+    if (e < tot) {
+      const int t = e >= nq ? 1 : 0, pq = e - t * nq, i = plane_first(pq, D);
+      const float iv = t == 0 ? inv0 : inv1;
+      const float4 gv = gain4<WT>(g, i);
+      const float4 y = make_float4(xv[u].x * iv * gv.x, xv[u].y * iv * gv.y, xv[u].z * iv * gv.z, xv[u].w * iv * gv.w);
       reinterpret_cast<float4*>(xs + t * D)[pq] = y;
-      if (out && t == 0) {
-        const int i = plane_first(pq, D);
+      if (out && t == 0 && i + 3 >= lo && i < hi) {
         const float vals[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q)
@@ -757,57 +824,57 @@ constexpr int TALKER_ROPE_ROW = 16;
 // Draws code j of the frame (0: semantic from the pending Talker logits; 1..15:
 // acoustic from the last CodePredictor head) in every CTA, identically.
 // Returns the code fed forward (the forced code under teacher forcing).
-__device__ __noinline__ int draw_code(Cons& c, int j) {
-  const FKParams& p = *c.p;
+__device__ __noinline__ int draw_code(Cons c, int j) {
+  const FKParams& p = *fk_prm();
   const bool sem = j == 0;
   const int V = sem ? p.Vt : p.Vc;
   const float* src = sem ? p.pending_logits + (size_t)p.sid * p.Vt : p.cp_logits;
-  if (p.dump && c.cta == 0) {
+  if (p.dump && ccta() == 0) {
     const int off = sem ? 0 : p.Vt + (j - 1) * p.Vc;
-    for (int i = c.tid; i < V; i += FK_CONSUMERS) p.dump[off + i] = __ldcg(src + i);
+    for (int i = ctid(); i < V; i += FK_CONSUMERS) p.dump[off + i] = __ldcg(src + i);
   }
-  int code = fast_sample<ConsGroup>(c.sm->u.smp, src, V, sem ? p.sp.do_sample : p.sp.sub_do_sample,
+  int code = fast_sample<ConsGroup>(fk_sm()->u.smp, src, V, sem ? p.sp.do_sample : p.sp.sub_do_sample,
                                     sem ? p.sp.top_k : p.sp.sub_top_k, sem ? p.sp.top_p : p.sp.sub_top_p,
                                     sem ? p.sp.temperature : p.sp.sub_temperature,
                                     sem ? p.sp.repetition_penalty : 1.0f,
-                                    sem ? p.history + (size_t)p.sid * p.Vt : nullptr, c.sm->uni[j]);
+                                    sem ? p.history + (size_t)p.sid * p.Vt : nullptr, fk_sm()->uni[j]);
   code = min(max(code, 0), V - 1);
   int fed = code;
   if (p.forced) {
-    fed = c.sm->forced[j];
+    fed = fk_sm()->forced[j];
     if (fed < 0 || fed >= V) {
-      if (c.cta == 0 && c.tid == 0) atomicCAS(p.err, 0, Q3TTS_ERR_ARG);
+      if (ccta() == 0 && ctid() == 0) atomicCAS(p.err, 0, Q3TTS_ERR_ARG);
       fed = code;
     }
   }
-  if (c.cta == 0 && c.tid == 0) p.codes[j] = code;
+  if (ccta() == 0 && ctid() == 0) p.codes[j] = code;
   return fed;
 }
 
 // Gains of the current layer inside its side slot.
 template <class WT>
-__device__ __forceinline__ const WT* side_cur(const Cons& c) {
-  return reinterpret_cast<const WT*>(c.sm->side[c.layer & 1]);
+__device__ __forceinline__ const WT* side_cur(Cons c) {
+  return reinterpret_cast<const WT*>(fk_sm()->side[cst().layer & 1]);
 }
 template <class WT>
-__device__ __forceinline__ const WT* side_gq(const Cons& c, int D) { return side_cur<WT>(c) + 2 * D; }
+__device__ __forceinline__ const WT* side_gq(Cons c, int D) { return side_cur<WT>(c) + 2 * D; }
 template <class WT>
-__device__ __forceinline__ const WT* side_gk(const Cons& c, int D) { return side_cur<WT>(c) + 2 * D + c.p->hd; }
+__device__ __forceinline__ const WT* side_gk(Cons c, int D) { return side_cur<WT>(c) + 2 * D + fk_prm()->hd; }
 
 // ---------------------------------------------------------------- phases
 
 // Phase A: layer input X_in (or tokens already in xs), fold into X_in+1 and
 // X_in+2, RMSNorm, QKV rows out.
 template <class WT>
-__device__ __noinline__ void phase_qkv(Cons& c, int D, int T, int in, bool from_xs) {
-  const FKParams& p = *c.p;
+__device__ __forceinline__ void phase_qkv(Cons c, int D, int T, int in, bool from_xs) {
+  const FKParams& p = *fk_prm();
   const WT* side = side_begin<WT>(c);
   load_norm<WT>(c, from_xs, in, 0, T, D, side, xnext(in, 1), xnext(in, 2), nullptr);
   int lo, hi;
-  split(p.qkv_rows, p.ncta, c.cta, lo, hi);
+  split(p.qkv_rows, p.ncta, ccta(), lo, hi);
   float* qkv = p.qkv;
   const int qr = p.qkv_rows;
-  stream_rows<WT>(c, lo, hi, D, T, c.sm->u.g.xs, [=](int row, int t, float v) { qkv[t * qr + row] = v; });
+  stream_rows<WT>(c, lo, hi, D, T, fk_sm()->u.g.xs, [=](int row, int t, float v) { qkv[t * qr + row] = v; });
   grid_sync(c);
 }
 
@@ -827,8 +894,8 @@ __device__ __forceinline__ void oproj_tiles(const FKParams& p, int D, int cta, i
 // both X_a and X_b.  The two warps of a gang take alternate hd blocks of a
 // tile and meet in the exchange buffer.
 template <class WT>
-__device__ void oproj_cols(Cons& c, int D, int T, int xa, int xb, int t0, int t1, int h_first) {
-  const FKParams& p = *c.p;
+__device__ void oproj_cols(Cons c, int D, int T, int xa, int xb, int t0, int t1, int h_first) {
+  const FKParams& p = *fk_prm();
   Stream s = stream_begin(c);
   const int hd = p.hd, nt = oproj_nt(D), nkb = hd >> 3, dmax = p.dmax;
   const int tb = 32 * hd * (int)sizeof(WT);
@@ -838,7 +905,7 @@ __device__ void oproj_cols(Cons& c, int D, int T, int xa, int xb, int t0, int t1
   FKSmem* sm = fk_sm();
   const uint32_t os0 = soff(sm->os[0][0]);
   constexpr uint32_t OS_HEAD = FK_TMAX * FK_HDMAX * 4, OS_TOK = FK_HDMAX * 4;
-  const uint32_t n0 = c.n;
+  const uint32_t n0 = cst().n;
   const uint32_t nch = t1 > t0 ? (uint32_t)((t1 - t0 + tpc - 1) / tpc) : 0u;
   for (uint32_t n = first_chunk(n0, s.gang); n < n0 + nch; n += FK_NGANG) {
     const uint32_t buf = chunk_wait(s, n);
@@ -877,8 +944,8 @@ __device__ void oproj_cols(Cons& c, int D, int T, int xa, int xb, int t0, int t1
     }
     chunk_release(s, n);
   }
-  c.aborted = s.aborted;
-  c.n = n0 + nch;
+  warp_set(cst().aborted, s.aborted ? 1 : 0);
+  warp_set(cst().n, n0 + nch);
 }
 
 // Stores a warp's head vector (lane holds l + 32 j) into plane layout.
@@ -892,25 +959,25 @@ __device__ __forceinline__ void store_head_plane(float* dst, int hd, const float
 // softmax sums are combined across warps.  The CTA owning column 0 of the
 // first q head of a kv group appends that group's current k, v to the cache.
 template <class WT>
-__device__ __noinline__ void phase_cp_attn(Cons& c, int layer, int T, int pos0, int xa, int xb) {
-  const FKParams& p = *c.p;
+__device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0, int xa, int xb) {
+  const FKParams& p = *fk_prm();
   const int D = p.Dc, hd = p.hd, Hq = p.Hq, Hkv = p.Hkv, rep = Hq / Hkv, J = hd / 32;
   const int nt = oproj_nt(D);
   int v0, v1;  // the CTA's o_proj tiles
-  oproj_tiles(p, D, c.cta, v0, v1);
+  oproj_tiles(p, D, ccta(), v0, v1);
   const int h_first = v0 / nt, h_last = (v1 - 1) / nt;
   const int nh = v1 > v0 ? h_last - h_first + 1 : 0;
   const int npair = nh * T;
   const int g_first = h_first / rep;
   const int ng = nh ? h_last / rep - g_first + 1 : 0;  // kv groups touched (<= 2)
-  AttnScratch& as = c.sm->u.att;
+  AttnScratch& as = fk_sm()->u.att;
   const float scale = 1.0f / sqrtf((float)hd);
   const int S = pos0 + T;  // positions 0..S-1 exist after this pass
   // 1) this warp's positions (warp, warp + 8): k, v of every touched kv group
   float kk[2][2][4], vv[2][2][4];
 #pragma unroll
   for (int np = 0; np < 2; ++np) {
-    const int sp = c.warp + FK_CONSUMER_WARPS * np;
+    const int sp = cwarp() + FK_CONSUMER_WARPS * np;
 #pragma unroll
     for (int gi = 0; gi < 2; ++gi) {
       const int g = g_first + gi;
@@ -926,39 +993,39 @@ __device__ __noinline__ void phase_cp_attn(Cons& c, int layer, int T, int pos0, 
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          kk[np][gi][j] = j < J ? __ldcg(kc + c.lane + 32 * j) : 0.f;
-          vv[np][gi][j] = j < J ? __ldcg(vc + c.lane + 32 * j) : 0.f;
+          kk[np][gi][j] = j < J ? __ldcg(kc + clane() + 32 * j) : 0.f;
+          vv[np][gi][j] = j < J ? __ldcg(vc + clane() + 32 * j) : 0.f;
         }
       }
     }
   }
   // 2) q of each (head, token) pair, normalised and rotated
-  if (c.warp < npair) {
-    const int h = h_first + c.warp / T, t = c.warp % T;
+  if (cwarp() < npair) {
+    const int h = h_first + cwarp() / T, t = cwarp() % T;
     float q[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) q[j] = j < J ? __ldcg(p.qkv + (size_t)t * p.qkv_rows + h * hd + c.lane + 32 * j) : 0.f;
-    norm_rope_head(p, c.sm, q, side_gq<WT>(c, D), cp_rope_row(pos0 + t), c.lane);
+    for (int j = 0; j < 4; ++j) q[j] = j < J ? __ldcg(p.qkv + (size_t)t * p.qkv_rows + h * hd + clane() + 32 * j) : 0.f;
+    norm_rope_head(p, fk_sm(), q, side_gq<WT>(c, D), cp_rope_row(pos0 + t), clane());
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      if (j < J) as.q[c.warp][c.lane + 32 * j] = q[j];
+      if (j < J) as.q[cwarp()][clane() + 32 * j] = q[j];
   }
   // 3) current-position keys: normalise, rotate, append (designated CTA)
 #pragma unroll
   for (int np = 0; np < 2; ++np) {
-    const int sp = c.warp + FK_CONSUMER_WARPS * np;
+    const int sp = cwarp() + FK_CONSUMER_WARPS * np;
 #pragma unroll
     for (int gi = 0; gi < 2; ++gi) {
       if (sp < S && sp >= pos0 && gi < ng) {
         const int g = g_first + gi;
-        norm_rope_head(p, c.sm, kk[np][gi], side_gk<WT>(c, D), cp_rope_row(sp), c.lane);
+        norm_rope_head(p, fk_sm(), kk[np][gi], side_gk<WT>(c, D), cp_rope_row(sp), clane());
         const int first = g * rep * nt;  // first o_proj tile of the group's first q head
         if (first >= v0 && first < v1) {
           float* kc = (float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 0, g);
           float* vc = (float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 1, g);
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            if (j < J) { kc[c.lane + 32 * j] = kk[np][gi][j]; vc[c.lane + 32 * j] = vv[np][gi][j]; }
+            if (j < J) { kc[clane() + 32 * j] = kk[np][gi][j]; vc[clane() + 32 * j] = vv[np][gi][j]; }
         }
       }
     }
@@ -970,7 +1037,7 @@ __device__ __noinline__ void phase_cp_attn(Cons& c, int layer, int T, int pos0, 
     float m = -INFINITY, l = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int np = 0; np < 2; ++np) {
-      const int sp = c.warp + FK_CONSUMER_WARPS * np;
+      const int sp = cwarp() + FK_CONSUMER_WARPS * np;
       if (sp <= pos0 + t) {  // causal (and sp < S)
 #pragma unroll
         for (int gi = 0; gi < 2; ++gi) {
@@ -978,7 +1045,7 @@ __device__ __noinline__ void phase_cp_attn(Cons& c, int layer, int T, int pos0, 
             float d = 0.f;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              if (j < J) d = fmaf(as.q[pr][c.lane + 32 * j], kk[np][gi][j], d);
+              if (j < J) d = fmaf(as.q[pr][clane() + 32 * j], kk[np][gi][j], d);
             d = warp_sum(d) * scale;
             const float mn = fmaxf(m, d), corr = __expf(m - mn), e = __expf(d - mn);
             l = l * corr + e;
@@ -989,14 +1056,14 @@ __device__ __noinline__ void phase_cp_attn(Cons& c, int layer, int T, int pos0, 
         }
       }
     }
-    if (c.lane == 0) { as.m[c.warp][pr] = m; as.l[c.warp][pr] = l; }
+    if (clane() == 0) { as.m[cwarp()][pr] = m; as.l[cwarp()][pr] = l; }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      if (j < J) as.o[c.warp][pr][c.lane + 32 * j] = o[j];
+      if (j < J) as.o[cwarp()][pr][clane() + 32 * j] = o[j];
   }
   consumer_sync();
   // 5) combine the warps: thread (pair, d)
-  for (int e = c.tid; e < npair * hd; e += FK_CONSUMERS) {
+  for (int e = ctid(); e < npair * hd; e += FK_CONSUMERS) {
     const int pr = e / hd, d = e % hd;
     float M = -INFINITY;
 #pragma unroll
@@ -1008,7 +1075,7 @@ __device__ __noinline__ void phase_cp_attn(Cons& c, int layer, int T, int pos0, 
       Ls += as.l[w][pr] * f;
       Os += as.o[w][pr][d] * f;
     }
-    put_plane(c.sm->os[pr / T][pr % T], hd, d, Os / Ls);
+    put_plane(fk_sm()->os[pr / T][pr % T], hd, d, Os / Ls);
   }
   consumer_sync();
   oproj_cols<WT>(c, D, T, xa, xb, v0, v1, h_first);
@@ -1019,25 +1086,25 @@ __device__ __noinline__ void phase_cp_attn(Cons& c, int layer, int T, int pos0, 
 // chunk); the q heads of the group share the K/V reads.  The item holding the
 // current position appends its k, v to the cache.
 template <class WT, class KT>
-__device__ __noinline__ void phase_talker_attn(Cons& c, int layer) {
-  const FKParams& p = *c.p;
+__device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
+  const FKParams& p = *fk_prm();
   const int hd = p.hd, Hq = p.Hq, Hkv = p.Hkv, rep = Hq / Hkv, J = hd / 32;
   const int cpg = p.ncta / Hkv;
-  const int g = c.cta / cpg, ch = c.cta % cpg;
+  const int g = ccta() / cpg, ch = ccta() % cpg;
   const int pos = p.pos, S = pos + 1;
-  AttnScratch& as = c.sm->u.att;
+  AttnScratch& as = fk_sm()->u.att;
   const float scale = 1.0f / sqrtf((float)hd);
   if (g < Hkv) {
     const int cs = (S + cpg - 1) / cpg, s0 = ch * cs, s1 = min(S, s0 + cs);
-    if (c.warp < rep) {
-      const int h = g * rep + c.warp;
+    if (cwarp() < rep) {
+      const int h = g * rep + cwarp();
       float q[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) q[j] = j < J ? __ldcg(p.qkv + h * hd + c.lane + 32 * j) : 0.f;
-      norm_rope_head(p, c.sm, q, side_gq<WT>(c, p.Dt), TALKER_ROPE_ROW, c.lane);
+      for (int j = 0; j < 4; ++j) q[j] = j < J ? __ldcg(p.qkv + h * hd + clane() + 32 * j) : 0.f;
+      norm_rope_head(p, fk_sm(), q, side_gq<WT>(c, p.Dt), TALKER_ROPE_ROW, clane());
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        if (j < J) as.q[c.warp][c.lane + 32 * j] = q[j];
+        if (j < J) as.q[cwarp()][clane() + 32 * j] = q[j];
     }
     consumer_sync();
     float m[FK_REPMAX], l[FK_REPMAX], o[FK_REPMAX][4];
@@ -1048,7 +1115,7 @@ __device__ __noinline__ void phase_talker_attn(Cons& c, int layer) {
       for (int j = 0; j < 4; ++j) o[r][j] = 0.f;
     }
     constexpr int BATCH = 4;
-    for (int sb = s0 + c.warp; sb < s1; sb += BATCH * FK_CONSUMER_WARPS) {
+    for (int sb = s0 + cwarp(); sb < s1; sb += BATCH * FK_CONSUMER_WARPS) {
       float k[BATCH][4], v[BATCH][4];
 #pragma unroll
       for (int b = 0; b < BATCH; ++b) {
@@ -1058,14 +1125,14 @@ __device__ __noinline__ void phase_talker_attn(Cons& c, int layer) {
           const KT* vc = (const KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, sp, 1, g);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            k[b][j] = j < J ? to_f(kc[c.lane + 32 * j]) : 0.f;
-            v[b][j] = j < J ? to_f(vc[c.lane + 32 * j]) : 0.f;
+            k[b][j] = j < J ? to_f(kc[clane() + 32 * j]) : 0.f;
+            v[b][j] = j < J ? to_f(vc[clane() + 32 * j]) : 0.f;
           }
         } else {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            k[b][j] = (sp == pos && j < J) ? __ldcg(p.qkv + (Hq + g) * hd + c.lane + 32 * j) : 0.f;
-            v[b][j] = (sp == pos && j < J) ? __ldcg(p.qkv + (Hq + Hkv + g) * hd + c.lane + 32 * j) : 0.f;
+            k[b][j] = (sp == pos && j < J) ? __ldcg(p.qkv + (Hq + g) * hd + clane() + 32 * j) : 0.f;
+            v[b][j] = (sp == pos && j < J) ? __ldcg(p.qkv + (Hq + Hkv + g) * hd + clane() + 32 * j) : 0.f;
           }
         }
       }
@@ -1074,12 +1141,12 @@ __device__ __noinline__ void phase_talker_attn(Cons& c, int layer) {
         const int sp = sb + b * FK_CONSUMER_WARPS;
         if (sp < s1) {
           if (sp == pos) {
-            norm_rope_head(p, c.sm, k[b], side_gk<WT>(c, p.Dt), TALKER_ROPE_ROW, c.lane);
+            norm_rope_head(p, fk_sm(), k[b], side_gk<WT>(c, p.Dt), TALKER_ROPE_ROW, clane());
             KT* kc = (KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, pos, 0, g);
             KT* vc = (KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, pos, 1, g);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              if (j < J) { kc[c.lane + 32 * j] = from_f<KT>(k[b][j]); vc[c.lane + 32 * j] = from_f<KT>(v[b][j]); }
+              if (j < J) { kc[clane() + 32 * j] = from_f<KT>(k[b][j]); vc[clane() + 32 * j] = from_f<KT>(v[b][j]); }
           }
 #pragma unroll
           for (int r = 0; r < FK_REPMAX; ++r) {
@@ -1087,7 +1154,7 @@ __device__ __noinline__ void phase_talker_attn(Cons& c, int layer) {
               float d = 0.f;
 #pragma unroll
               for (int j = 0; j < 4; ++j)
-                if (j < J) d = fmaf(as.q[r][c.lane + 32 * j], k[b][j], d);
+                if (j < J) d = fmaf(as.q[r][clane() + 32 * j], k[b][j], d);
               d = warp_sum(d) * scale;
               const float mn = fmaxf(m[r], d), corr = __expf(m[r] - mn), e = __expf(d - mn);
               l[r] = l[r] * corr + e;
@@ -1102,14 +1169,14 @@ __device__ __noinline__ void phase_talker_attn(Cons& c, int layer) {
 #pragma unroll
     for (int r = 0; r < FK_REPMAX; ++r) {
       if (r < rep) {
-        if (c.lane == 0) { as.m[c.warp][r] = m[r]; as.l[c.warp][r] = l[r]; }
+        if (clane() == 0) { as.m[cwarp()][r] = m[r]; as.l[cwarp()][r] = l[r]; }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if (j < J) as.o[c.warp][r][c.lane + 32 * j] = o[r][j];
+          if (j < J) as.o[cwarp()][r][clane() + 32 * j] = o[r][j];
       }
     }
     consumer_sync();
-    for (int e = c.tid; e < rep * hd; e += FK_CONSUMERS) {
+    for (int e = ctid(); e < rep * hd; e += FK_CONSUMERS) {
       const int r = e / hd, d = e % hd;
       float M = -INFINITY;
 #pragma unroll
@@ -1134,15 +1201,15 @@ __device__ __noinline__ void phase_talker_attn(Cons& c, int layer) {
 // Talker phase B2: combine the partials of the CTA's heads (all partial loads
 // of a thread issued together), then o_proj.
 template <class WT>
-__device__ __noinline__ void phase_talker_oproj(Cons& c, int xa, int xb) {
-  const FKParams& p = *c.p;
+__device__ __forceinline__ void phase_talker_oproj(Cons c, int xa, int xb) {
+  const FKParams& p = *fk_prm();
   const int D = p.Dt, hd = p.hd, cpg = p.ncta / p.Hkv, nt = oproj_nt(D);
   int v0, v1;  // the CTA's o_proj tiles
-  oproj_tiles(p, D, c.cta, v0, v1);
+  oproj_tiles(p, D, ccta(), v0, v1);
   const int h_first = v0 / nt, h_last = (v1 - 1) / nt;
   const int nh = v1 > v0 ? h_last - h_first + 1 : 0;
   constexpr int CMAX = 20;  // chunks per kv group handled in one batch of loads
-  for (int e = c.tid; e < nh * hd; e += FK_CONSUMERS) {
+  for (int e = ctid(); e < nh * hd; e += FK_CONSUMERS) {
     const int hh = e / hd, d = e % hd, h = h_first + hh;
     const float* base = p.part + (size_t)h * cpg * (hd + 2);
     float M = -INFINITY, Ls = 0.f, Os = 0.f;
@@ -1170,72 +1237,50 @@ __device__ __noinline__ void phase_talker_oproj(Cons& c, int xa, int xb) {
       }
       M = Mn;
     }
-    put_plane(c.sm->os[hh][0], hd, d, Os / Ls);
+    put_plane(fk_sm()->os[hh][0], hd, d, Os / Ls);
   }
   consumer_sync();
   oproj_cols<WT>(c, D, 1, xa, xb, v0, v1, h_first);
   grid_sync(c);
 }
 
-// One 256-wide block of an FFN unit's gate and up rows (at g, g + rb) against
-// T tokens.
-template <class WT, int T>
-__device__ __forceinline__ void gu_block(uint32_t g, uint32_t rb, uint32_t xa, uint32_t xb, int D4, float (&ga)[T],
-                                         float (&gb)[T], float (&ua)[T], float (&ub)[T]) {
-  float g8[8], u8[8];
-  lds_w8<WT>(g, g8);
-  lds_w8<WT>(g + rb, u8);
-#pragma unroll
-  for (int t = 0; t < T; ++t) {
-    const float4 va = lds_f4(xa + (uint32_t)(t * D4)), vb = lds_f4(xb + (uint32_t)(t * D4));
-    ga[t] = fmaf(g8[0], va.x, ga[t]); ga[t] = fmaf(g8[1], va.y, ga[t]);
-    ga[t] = fmaf(g8[2], va.z, ga[t]); ga[t] = fmaf(g8[3], va.w, ga[t]);
-    gb[t] = fmaf(g8[4], vb.x, gb[t]); gb[t] = fmaf(g8[5], vb.y, gb[t]);
-    gb[t] = fmaf(g8[6], vb.z, gb[t]); gb[t] = fmaf(g8[7], vb.w, gb[t]);
-    ua[t] = fmaf(u8[0], va.x, ua[t]); ua[t] = fmaf(u8[1], va.y, ua[t]);
-    ua[t] = fmaf(u8[2], va.z, ua[t]); ua[t] = fmaf(u8[3], va.w, ua[t]);
-    ub[t] = fmaf(u8[4], vb.x, ub[t]); ub[t] = fmaf(u8[5], vb.y, ub[t]);
-    ub[t] = fmaf(u8[6], vb.z, ub[t]); ub[t] = fmaf(u8[7], vb.w, ub[t]);
-  }
-}
-
 // One FFN unit f at shared offset u (gate row, up row, down column; D weights
-// each), shared by the two warps of a gang: each takes alternate 256-wide
-// blocks of the gate/up dot products, the partial sums meet in the exchange
-// buffer slot xu (2 T floats per warp), both form a_t = silu(gate_f . x_t) *
+// each), shared by the two warps of a gang: each takes its activation blocks
+// of the gate/up dot products, the partial sums meet in the exchange buffer
+// slot xu (2 T floats per warp), both form a_t = silu(gate_f . x_t) *
 // (up_f . x_t), and each adds a_t W_down[:, f] into the columns of its own
-// blocks: lane l, block i = 2 ii + j holds columns 8 l + 256 i + q as
-// y[t (4 / T) + ii][q].
+// blocks: lane l, block i = 2 b + j holds columns 8 l + 256 i + q as
+// y[t (4 / T) + b][q].
 template <class WT, int T>
-__device__ __forceinline__ void ffn_unit(uint32_t u, int D, uint32_t xs, const Stream& s, float* xu,
+__device__ __forceinline__ void ffn_unit(uint32_t u, int D, const XReg<T>& x, unsigned m, const Stream& s, float* xu,
                                          float (&y)[4][8]) {
-  constexpr int IM2 = 4 / T;  // blocks per token and warp (D <= 256 IM2 FK_GANG)
+  constexpr int NB = FK_XB / T;  // blocks per token and warp (D <= 256 NB FK_GANG)
   const uint32_t rb = (uint32_t)D * (uint32_t)sizeof(WT);
   const uint32_t wl = u + (uint32_t)(s.lane * 8 * (int)sizeof(WT));
-  const uint32_t xa = xs + (uint32_t)s.lane * 16u, xb = xa + (uint32_t)D * 2u;
-  const int nfull = D >> 8, D4 = D * 4;
-  const bool tail = (D & 255) && (nfull % FK_GANG) == s.j && s.lane * 8 < (D & 255);
-  float ga[T], gb[T], ua[T], ub[T];
+  float g[T], v[T];
 #pragma unroll
-  for (int t = 0; t < T; ++t) ga[t] = gb[t] = ua[t] = ub[t] = 0.f;
-#pragma unroll 2
-  for (int i = s.j; i < nfull; i += FK_GANG)
-    gu_block<WT, T>(wl + (uint32_t)(i * 256 * (int)sizeof(WT)), rb, xa + (uint32_t)(i * 512), xb + (uint32_t)(i * 512),
-                    D4, ga, gb, ua, ub);
-  if (tail)
-    gu_block<WT, T>(wl + (uint32_t)(nfull * 256 * (int)sizeof(WT)), rb, xa + (uint32_t)(nfull * 512),
-                    xb + (uint32_t)(nfull * 512), D4, ga, gb, ua, ub);
-  float pg[T], pu[T];
+  for (int t = 0; t < T; ++t) g[t] = v[t] = 0.f;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    if ((m >> b) & 1u) {
+      const uint32_t wb = wl + (uint32_t)((FK_GANG * b + s.j) * 256 * (int)sizeof(WT));
+#pragma unroll
+      for (int t = 0; t < T; ++t) {
+        g[t] = dot8w<WT>(wb, x.a[t][b], x.c[t][b], g[t]);
+        v[t] = dot8w<WT>(wb + rb, x.a[t][b], x.c[t][b], v[t]);
+      }
+    }
+  }
 #pragma unroll
   for (int t = 0; t < T; ++t) {
-    pg[t] = warp_sum(ga[t] + gb[t]);
-    pu[t] = warp_sum(ua[t] + ub[t]);
+    g[t] = warp_sum(g[t]);
+    v[t] = warp_sum(v[t]);
   }
   if (s.lane == 0) {
 #pragma unroll
     for (int t = 0; t < T; ++t) {
-      xu[s.j * FK_XCH + 2 * t] = pg[t];
-      xu[s.j * FK_XCH + 2 * t + 1] = pu[t];
+      xu[s.j * FK_XCH + 2 * t] = g[t];
+      xu[s.j * FK_XCH + 2 * t + 1] = v[t];
     }
   }
   gang_sync(s);
@@ -1244,17 +1289,15 @@ __device__ __forceinline__ void ffn_unit(uint32_t u, int D, uint32_t xs, const S
   for (int t = 0; t < T; ++t)
     act[t] = silu(xu[2 * t] + xu[FK_XCH + 2 * t]) * (xu[2 * t + 1] + xu[FK_XCH + 2 * t + 1]);
   const uint32_t wd = wl + 2u * rb;
-  const bool dtail = (D & 255) && s.lane * 8 < (D & 255);
 #pragma unroll
-  for (int ii = 0; ii < IM2; ++ii) {
-    const int i = ii * FK_GANG + s.j;
-    if (i < nfull || (i == nfull && dtail)) {
+  for (int b = 0; b < NB; ++b) {
+    if ((m >> b) & 1u) {
       float d8[8];
-      lds_w8<WT>(wd + (uint32_t)(i * 256 * (int)sizeof(WT)), d8);
+      lds_w8<WT>(wd + (uint32_t)((FK_GANG * b + s.j) * 256 * (int)sizeof(WT)), d8);
 #pragma unroll
       for (int t = 0; t < T; ++t)
 #pragma unroll
-        for (int q = 0; q < 8; ++q) y[t * IM2 + ii][q] = fmaf(act[t], d8[q], y[t * IM2 + ii][q]);
+        for (int q = 0; q < 8; ++q) y[t * NB + b][q] = fmaf(act[t], d8[q], y[t * NB + b][q]);
     }
   }
 }
@@ -1262,13 +1305,15 @@ __device__ __forceinline__ void ffn_unit(uint32_t u, int D, uint32_t xs, const S
 // The gang's share of the CTA's FFN units [f0, f1) (chunks n0 .. n0 + nch),
 // its down-projection sums added into yred (layout at phase_ffn).
 template <class WT, int T>
-__device__ __noinline__ void ffn_stream(Cons& c, int D, int f0, int f1, uint32_t n0, uint32_t nch) {
-  constexpr int IM = 8 / T, IM2 = 4 / T;
+__device__ __forceinline__ void ffn_stream(Cons c, int D, int f0, int f1, uint32_t n0, uint32_t nch) {
+  constexpr int IM = 8 / T, NB = FK_XB / T;
   Stream s = stream_begin(c);
   const int ub = 3 * D * (int)sizeof(WT);
   const int upc = rows_per_chunk(ub);
   FKSmem* sm = fk_sm();
-  const uint32_t xs = soff(sm->u.g.xs);
+  const unsigned m = xblocks(D, s.lane, s.j);
+  XReg<T> x;
+  load_xreg<T>(x, soff(sm->u.g.xs), D, s.lane, s.j, m);
   float y[4][8];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -1279,23 +1324,22 @@ __device__ __noinline__ void ffn_stream(Cons& c, int D, int f0, int f1, uint32_t
     const uint32_t buf = chunk_wait(s, n);
     float* xbf = xch_buf(s, n);
     const int nu = min(upc, f1 - (f0 + (int)(n - n0) * upc));
-    for (int jj = 0; jj < nu; ++jj) ffn_unit<WT, T>(buf + (uint32_t)(jj * ub), D, xs, s, xbf + 4 * jj, y);
+    for (int jj = 0; jj < nu; ++jj) ffn_unit<WT, T>(buf + (uint32_t)(jj * ub), D, x, m, s, xbf + 4 * jj, y);
     gang_sync(s);  // both warps are done with the chunk
     chunk_release(s, n);
     any = true;
   }
-  c.aborted = s.aborted;
+  warp_set(cst().aborted, s.aborted ? 1 : 0);
   if (any) {
     float* yred = sm->u.g.yred;
-    const int k0 = s.lane * 8;
 #pragma unroll
     for (int t = 0; t < T; ++t)
 #pragma unroll
-      for (int ii = 0; ii < IM2; ++ii) {
-        const int i = ii * FK_GANG + s.j;
-        if (k0 + 256 * i < D) {
+      for (int b = 0; b < NB; ++b) {
+        if ((m >> b) & 1u) {
+          const int i = FK_GANG * b + s.j;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) atomicAdd(&yred[((t * IM + i) * 8 + q) * 32 + s.lane], y[t * IM2 + ii][q]);
+          for (int q = 0; q < 8; ++q) atomicAdd(&yred[((t * IM + i) * 8 + q) * 32 + s.lane], y[t * NB + b][q]);
         }
       }
   }
@@ -1309,25 +1353,25 @@ __device__ __noinline__ void ffn_stream(Cons& c, int D, int f0, int f1, uint32_t
 // is column 8 lane + 256 i + q of token t -- so the warps' shared-memory adds
 // are bank-conflict free.
 template <class WT>
-__device__ __noinline__ void phase_ffn(Cons& c, int D, int F, int T, int xa, int xb) {
-  const FKParams& p = *c.p;
-  float* yred = c.sm->u.g.yred;
-  for (int e = c.tid; e < 32 * FK_YCOLS; e += FK_CONSUMERS) yred[e] = 0.f;  // before load_norm's barriers
+__device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int xa, int xb) {
+  const FKParams& p = *fk_prm();
+  float* yred = fk_sm()->u.g.yred;
+  for (int e = ctid(); e < 32 * FK_YCOLS; e += FK_CONSUMERS) yred[e] = 0.f;  // before load_norm's barriers
   load_norm<WT>(c, false, xa, 0, T, D, side_cur<WT>(c) + D, -1, -1, nullptr);
   side_end(c);
   int f0, f1;
-  split(F, p.ncta, c.cta, f0, f1);
+  split(F, p.ncta, ccta(), f0, f1);
   const int upc = rows_per_chunk(3 * D * (int)sizeof(WT));
-  const uint32_t n0 = c.n;
+  const uint32_t n0 = cst().n;
   const uint32_t nch = f1 > f0 ? (uint32_t)((f1 - f0 + upc - 1) / upc) : 0u;
   if (T > 1)
     ffn_stream<WT, 2>(c, D, f0, f1, n0, nch);
   else
     ffn_stream<WT, 1>(c, D, f0, f1, n0, nch);
-  c.n = n0 + nch;
+  warp_set(cst().n, n0 + nch);
   consumer_sync();
   const int IM = 8 / T, nq = D / 4;
-  for (int e = c.tid; e < T * nq; e += FK_CONSUMERS) {
+  for (int e = ctid(); e < T * nq; e += FK_CONSUMERS) {
     const int t = e / nq, col = (e % nq) * 4;
     const int i = col >> 8, ln = (col & 255) >> 3, q = col & 7;
     const float* src = yred + ((t * IM + i) * 8 + q) * 32 + ln;
@@ -1339,139 +1383,160 @@ __device__ __noinline__ void phase_ffn(Cons& c, int D, int F, int T, int xa, int
 // The CodePredictor input token(s) of pass j into xs (plane layout, D_t wide):
 // pass 0: [h_T, E_t[c0]]; pass j >= 1: E_cp[j-1][c_j].
 template <class WT>
-__device__ __noinline__ void cp_tokens(Cons& c, int j, int fed) {
-  const FKParams& p = *c.p;
+__device__ __forceinline__ void cp_tokens(Cons c, int j, int fed) {
+  const FKParams& p = *fk_prm();
   const int Dt = p.Dt;
-  float* xs = c.sm->u.g.xs;
+  float* xs = fk_sm()->u.g.xs;
   if (j == 0) {
     const WT* e = (const WT*)p.e_codec + (size_t)fed * Dt;
-    for (int i = c.tid; i < Dt; i += FK_CONSUMERS) {
+    for (int i = ctid(); i < Dt; i += FK_CONSUMERS) {
       put_plane(xs, Dt, i, __ldcg(p.pending_h + (size_t)p.sid * Dt + i));
       put_plane(xs + Dt, Dt, i, to_f(e[i]));
     }
   } else {
     const WT* e = (const WT*)p.cp_embeds + ((size_t)(j - 1) * p.Vc + fed) * Dt;
-    for (int i = c.tid; i < Dt; i += FK_CONSUMERS) put_plane(xs, Dt, i, to_f(e[i]));
+    for (int i = ctid(); i < Dt; i += FK_CONSUMERS) put_plane(xs, Dt, i, to_f(e[i]));
   }
   consumer_sync();
 }
 
 // The CTA's slice of the running embedding sum of the frame's codes.
 template <class WT>
-__device__ __noinline__ void xsum_add(Cons& c, int j, int fed) {
-  const FKParams& p = *c.p;
+__device__ __forceinline__ void xsum_add(Cons c, int j, int fed) {
+  const FKParams& p = *fk_prm();
   int lo, hi;
-  split(p.Dt, p.ncta, c.cta, lo, hi);
+  split(p.Dt, p.ncta, ccta(), lo, hi);
   const WT* e = j == 0 ? (const WT*)p.e_codec + (size_t)fed * p.Dt
                        : (const WT*)p.cp_embeds + ((size_t)(j - 1) * p.Vc + fed) * p.Dt;
-  for (int i = lo + c.tid; i < hi; i += FK_CONSUMERS)
+  for (int i = lo + ctid(); i < hi; i += FK_CONSUMERS)
     p.xsum[i] = j == 0 ? to_f(e[i]) : p.xsum[i] + to_f(e[i]);
 }
 
+// Start of CodePredictor pass j: draw code j, add its embedding to the
+// running sum, stage the pass's input token(s) and, when D_t != D_c, project
+// them (z = W_p u into X_0, one more phase).
+template <class WT>
+__device__ __forceinline__ void pass_begin(Cons c, int j) {
+  ConsState& L = cst();
+  const int fed = draw_code(c, j);
+  if (j == 0) warp_set(L.fed0, fed);
+  xsum_add<WT>(c, j, fed);
+  cp_tokens<WT>(c, j, fed);
+  warp_set(L.in, 0);
+  warp_set(L.from_xs, 1);
+  if (fk_prm()->has_proj) {
+    const FKParams& q = *fk_prm();
+    int lo, hi;
+    split(q.Dc, q.ncta, ccta(), lo, hi);
+    float* X0 = xbuf(q, 0, 0);
+    const int dmax = q.dmax;
+    stream_rows<WT>(c, lo, hi, q.Dt, j == 0 ? 2 : 1, fk_sm()->u.g.xs,
+                    [=](int row, int t, float v) { X0[t * dmax + row] = v; });
+    grid_sync(c);
+    warp_set(L.from_xs, 0);
+  }
+}
+
+// Start of the Talker step: draw the last acoustic code; the Talker input is
+// the sum of the frame's 16 code embeddings.
+template <class WT>
+__device__ __forceinline__ void talker_begin(Cons c) {
+  const int fed15 = draw_code(c, Q3TTS_N_CODEBOOKS - 1);
+  const FKParams& q = *fk_prm();
+  const WT* e = (const WT*)q.cp_embeds + ((size_t)(Q3TTS_N_CODEBOOKS - 2) * q.Vc + fed15) * q.Dt;
+  float* xs = fk_sm()->u.g.xs;
+  for (int i = ctid(); i < q.Dt; i += FK_CONSUMERS) put_plane(xs, q.Dt, i, __ldcg(q.xsum + i) + to_f(e[i]));
+  consumer_sync();
+  ConsState& L = cst();
+  warp_set(L.in, 0);
+  warp_set(L.from_xs, 1);
+}
+
+// Final norm of token t of the stack output and the CTA's head rows (streamed
+// from the ring): a CodePredictor head (logits to cp_logits, then a grid
+// barrier before the draw) or the Talker codec head (pending hidden slice and
+// pending logits).
+template <class WT>
+__device__ __forceinline__ void head_phase(Cons c, bool talker, int t) {
+  const FKParams& q = *fk_prm();
+  const int D = talker ? q.Dt : q.Dc, V = talker ? q.Vt : q.Vc;
+  const WT* g = reinterpret_cast<const WT*>(fk_sm()->fin) + (talker ? q.Dc : 0);
+  load_norm<WT>(c, false, cst().in, t, 1, D, g, -1, -1, talker ? q.pending_h + (size_t)q.sid * q.Dt : nullptr);
+  int lo, hi;
+  split(V, q.ncta, ccta(), lo, hi);
+  float* out = talker ? q.pending_logits + (size_t)q.sid * q.Vt : q.cp_logits;
+  stream_rows<WT>(c, lo, hi, D, 1, fk_sm()->u.g.xs, [=](int row, int, float v) { out[row] = v; });
+  if (!talker) grid_sync(c);
+}
+
+// The consumer warps' schedule for one frame: 15 CodePredictor passes of L_c
+// layers, then the Talker's L_t layers, as one loop over layer steps so that
+// every phase function has a single call site and is inlined.  Loop state
+// lives in the warp's shared-memory record (cst()).
 template <class WT, class KT>
-__device__ void consumer(const FKParams& p, FKSmem* sm) {
+__device__ void consumer() {
   Cons c;
-  c.p = &p;
-  c.sm = sm;
-  c.cta = blockIdx.x;
-  c.tid = threadIdx.x - FK_PRODUCER_THREADS;
-  c.warp = c.tid >> 5;
-  c.lane = c.tid & 31;
-  c.n = 0;
-  c.phase = 0;
-  c.layer = 0;
-  c.aborted = false;
-  if (c.tid < Q3TTS_N_CODEBOOKS) {
-    sm->uni[c.tid] = p.uniforms[c.tid];
-    sm->forced[c.tid] = p.forced ? p.forced[c.tid] : 0;
-  }
   {
+    const FKParams& p = *fk_prm();
+    FKSmem* sm = fk_sm();
+    cst().n = 0;
+    cst().phase = 0;
+    cst().layer = 0;
+    cst().aborted = false;
+    if (ctid() < Q3TTS_N_CODEBOOKS) {
+      sm->uni[ctid()] = p.uniforms[ctid()];
+      sm->forced[ctid()] = p.forced ? p.forced[ctid()] : 0;
+    }
     WT* fin = reinterpret_cast<WT*>(sm->fin);
-    for (int i = c.tid; i < p.Dc; i += FK_CONSUMERS) fin[i] = ((const WT*)p.cp_gfinal)[i];
-    for (int i = c.tid; i < p.Dt; i += FK_CONSUMERS) fin[p.Dc + i] = ((const WT*)p.t_gfinal)[i];
-  }
-  if (c.cta == 0 && c.tid == 0 && p.newpage >= 0)
-    const_cast<int*>(p.tkv.page_table)[p.sid * p.tkv.pages_per_stream + p.pos / p.tkv.page_size] = p.newpage;
-  {
+    for (int i = ctid(); i < p.Dc; i += FK_CONSUMERS) fin[i] = ((const WT*)p.cp_gfinal)[i];
+    for (int i = ctid(); i < p.Dt; i += FK_CONSUMERS) fin[p.Dc + i] = ((const WT*)p.t_gfinal)[i];
+    if (ccta() == 0 && ctid() == 0 && p.newpage >= 0)
+      const_cast<int*>(p.tkv.page_table)[p.sid * p.tkv.pages_per_stream + p.pos / p.tkv.page_size] = p.newpage;
     // rope rows: CodePredictor positions 0..15 and the Talker position
     const int half = p.hd / 2;
-    for (int e = c.tid; e < 17 * half; e += FK_CONSUMERS) {
+    for (int e = ctid(); e < 17 * half; e += FK_CONSUMERS) {
       const int r = e / half, i = e % half, pos = r < 16 ? r : p.pos;
       sm->rope_c[r][i] = p.rope_cos[(size_t)pos * half + i];
       sm->rope_s[r][i] = p.rope_sin[(size_t)pos * half + i];
     }
   }
   consumer_sync();
-  int fed0 = 0;
-  for (int j = 0; j < Q3TTS_N_CODEBOOKS - 1; ++j) {
-    const int T = j == 0 ? 2 : 1, pos0 = j == 0 ? 0 : j + 1;
-    const int fed = draw_code(c, j);
-    if (j == 0) fed0 = fed;
-    xsum_add<WT>(c, j, fed);
-    cp_tokens<WT>(c, j, fed);
-    int in = 0;  // the layer input buffer
-    bool from_xs = true;
-    if (p.has_proj) {
-      // z = W_p u into X_0 (rows of the CTA)
-      int lo, hi;
-      split(p.Dc, p.ncta, c.cta, lo, hi);
-      float* X0 = xbuf(p, 0, 0);
-      const int dmax = p.dmax;
-      stream_rows<WT>(c, lo, hi, p.Dt, T, sm->u.g.xs, [=](int row, int t, float v) { X0[t * dmax + row] = v; });
-      grid_sync(c);
-      from_xs = false;
+  ConsState& L = cst();
+  for (warp_set(L.k, 0); L.k < (Q3TTS_N_CODEBOOKS - 1) * fk_prm()->Lc + fk_prm()->Lt; warp_set(L.k, L.k + 1)) {
+    const int Lc = fk_prm()->Lc, ncp = (Q3TTS_N_CODEBOOKS - 1) * Lc;
+    const bool cp = L.k < ncp;
+    const int j = cp ? L.k / Lc : Q3TTS_N_CODEBOOKS - 1, l = cp ? L.k % Lc : L.k - ncp;
+    if (l == 0) {
+      if (cp)
+        pass_begin<WT>(c, j);
+      else
+        talker_begin<WT>(c);
     }
-    for (int l = 0; l < p.Lc; ++l) {
-      phase_qkv<WT>(c, p.Dc, T, in, from_xs);
-      from_xs = false;
-      phase_cp_attn<WT>(c, l, T, pos0, xnext(in, 1), xnext(in, 2));
-      phase_ffn<WT>(c, p.Dc, p.Fc, T, xnext(in, 1), xnext(in, 2));
-      in = xnext(in, 2);
+    const int T = (cp && j == 0) ? 2 : 1;
+    const int D = cp ? fk_prm()->Dc : fk_prm()->Dt;
+    phase_qkv<WT>(c, D, T, L.in, L.from_xs != 0);
+    warp_set(L.from_xs, 0);
+    if (cp) {
+      phase_cp_attn<WT>(c, l, T, j == 0 ? 0 : j + 1, xnext(L.in, 1), xnext(L.in, 2));
+    } else {
+      phase_talker_attn<WT, KT>(c, l);
+      phase_talker_oproj<WT>(c, xnext(L.in, 1), xnext(L.in, 2));
     }
-    // final norm of the last token, head j
-    load_norm<WT>(c, false, in, T - 1, 1, p.Dc, reinterpret_cast<const WT*>(sm->fin), -1, -1, nullptr);
-    {
-      int lo, hi;
-      split(p.Vc, p.ncta, c.cta, lo, hi);
-      float* lg = p.cp_logits;
-      stream_rows<WT>(c, lo, hi, p.Dc, 1, sm->u.g.xs, [=](int row, int, float v) { lg[row] = v; });
-    }
-    grid_sync(c);
+    phase_ffn<WT>(c, D, cp ? fk_prm()->Fc : fk_prm()->Ft, T, xnext(L.in, 1), xnext(L.in, 2));
+    warp_set(L.in, xnext(L.in, 2));
+    if (cp && l == Lc - 1) head_phase<WT>(c, false, T - 1);
   }
-  // ---- Talker: input = embedding sum of the 16 codes
+  head_phase<WT>(c, true, 0);
   {
-    const int fed15 = draw_code(c, Q3TTS_N_CODEBOOKS - 1);
-    const WT* e = (const WT*)p.cp_embeds + ((size_t)(Q3TTS_N_CODEBOOKS - 2) * p.Vc + fed15) * p.Dt;
-    float* xs = sm->u.g.xs;
-    for (int i = c.tid; i < p.Dt; i += FK_CONSUMERS) put_plane(xs, p.Dt, i, __ldcg(p.xsum + i) + to_f(e[i]));
+    const FKParams& q = *fk_prm();
+    if (ccta() == 0 && ctid() == 0) q.history[(size_t)q.sid * q.Vt + L.fed0] = 1;
     consumer_sync();
-  }
-  int in = 0;
-  bool from_xs = true;
-  for (int l = 0; l < p.Lt; ++l) {
-    phase_qkv<WT>(c, p.Dt, 1, in, from_xs);
-    from_xs = false;
-    phase_talker_attn<WT, KT>(c, l);
-    phase_talker_oproj<WT>(c, xnext(in, 1), xnext(in, 2));
-    phase_ffn<WT>(c, p.Dt, p.Ft, 1, xnext(in, 1), xnext(in, 2));
-    in = xnext(in, 2);
-  }
-  // final norm -> pending hidden (CTA slice) and codec head rows -> pending logits
-  load_norm<WT>(c, false, in, 0, 1, p.Dt, reinterpret_cast<const WT*>(sm->fin) + p.Dc, -1, -1,
-                p.pending_h + (size_t)p.sid * p.Dt);
-  {
-    int lo, hi;
-    split(p.Vt, p.ncta, c.cta, lo, hi);
-    float* out = p.pending_logits + (size_t)p.sid * p.Vt;
-    stream_rows<WT>(c, lo, hi, p.Dt, 1, sm->u.g.xs, [=](int row, int, float v) { out[row] = v; });
-  }
-  if (c.cta == 0 && c.tid == 0) p.history[(size_t)p.sid * p.Vt + fed0] = 1;
-  consumer_sync();
-  if (c.tid == 0) {
-    __threadfence();
-    if (atomicAdd(p.done, 1u) == (unsigned)p.ncta - 1) {
-      *p.bar = 0u;
-      *p.done = 0u;
+    if (ctid() == 0) {
+      __threadfence();
+      if (atomicAdd(q.done, 1u) == (unsigned)q.ncta - 1) {
+        *q.bar = 0u;
+        *q.done = 0u;
+      }
     }
   }
 }
@@ -1622,7 +1687,7 @@ __global__ void __launch_bounds__(FK_THREADS, 1) frame_kernel(const __grid_const
     }
     return;
   }
-  consumer<WT, KT>(sm->prm, sm);
+  consumer<WT, KT>();
 }
 
 // ------------------------------------------------------------- host side
