@@ -499,20 +499,17 @@ __device__ __forceinline__ void fma8(uint32_t w, const float4& xa, const float4&
   b = fmaf(wv[4], xb.x, b); b = fmaf(wv[5], xb.y, b); b = fmaf(wv[6], xb.z, b); b = fmaf(wv[7], xb.w, b);
 }
 
-// The activations a warp multiplies, held in registers for a whole streaming
-// loop: warp j of a gang owns the 256-wide blocks i = j, j + 2, j + 4, j + 6
-// of the reduction (K <= 2048; the block holding the ragged tail K % 256
-// included), lane l elements 8 l + 256 i .. + 7 of token t in a[t][b] (first
-// four) and c[t][b] (last four).  Lanes past a ragged tail hold zeros and are
-// masked out of the weight loads.
-constexpr int FK_XB = 4;  // blocks per warp
-template <int T>
+// The activations a warp multiplies for one token: warp j of a gang owns the
+// 256-wide blocks i = j, j + 2, j + 4, j + 6 of the reduction (K <= 2048, the
+// block holding the ragged tail K % 256 included); lane l holds elements
+// 8 l + 256 i .. + 7 of block slot b (i = 2 b + j) as a[b] (first four) and
+// c[b] (last four).  Lanes past a ragged tail hold zeros and are masked out.
+constexpr int FK_XB = 4;  // block slots per warp
 struct XReg {
-  float4 a[T][FK_XB], c[T][FK_XB];
+  float4 a[FK_XB], c[FK_XB];
 };
 
-// Which of the warp's blocks exist for a reduction of length K: bit b set if
-// block 2 b + j has weights for this lane.
+// Which of the warp's block slots have weights for this lane (bit b).
 __device__ __forceinline__ unsigned xblocks(int K, int lane, int j) {
   const int nfull = K >> 8;
   unsigned m = 0;
@@ -524,18 +521,14 @@ __device__ __forceinline__ unsigned xblocks(int K, int lane, int j) {
   return m;
 }
 
-// Loads the warp's activation blocks from the plane-layout vectors at shared
-// offset xs (token t at xs + 4 K t).
-template <int T>
-__device__ __forceinline__ void load_xreg(XReg<T>& x, uint32_t xs, int K, int lane, int j, unsigned m) {
+// Loads the warp's blocks of the plane-layout vector at shared offset xt.
+__device__ __forceinline__ void load_xreg(XReg& x, uint32_t xt, int K, int lane, int j, unsigned m) {
 #pragma unroll
-  for (int t = 0; t < T; ++t)
-#pragma unroll
-    for (int b = 0; b < FK_XB; ++b) {
-      const uint32_t o = xs + (uint32_t)(t * K * 4 + lane * 16 + (FK_GANG * b + j) * 512);
-      x.a[t][b] = (m >> b) & 1u ? lds_f4(o) : make_float4(0.f, 0.f, 0.f, 0.f);
-      x.c[t][b] = (m >> b) & 1u ? lds_f4(o + (uint32_t)K * 2u) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+  for (int b = 0; b < FK_XB; ++b) {
+    const uint32_t o = xt + (uint32_t)(lane * 16 + (FK_GANG * b + j) * 512);
+    x.a[b] = (m >> b) & 1u ? lds_f4(o) : make_float4(0.f, 0.f, 0.f, 0.f);
+    x.c[b] = (m >> b) & 1u ? lds_f4(o + (uint32_t)K * 2u) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 }
 
 // 8 weights at shared offset w times the 8 activations (a, c) into acc.
@@ -548,98 +541,73 @@ __device__ __forceinline__ float dot8w(uint32_t w, const float4& a, const float4
   return acc + (s + s2);
 }
 
-// This warp's partial dot products of G consecutive rows (shared offset w,
-// pitch rb) with its activation blocks; warp-reduced, in every lane.
-template <class WT, int T, int G>
-__device__ __forceinline__ void rows_part(uint32_t w, int rb, const XReg<T>& x, unsigned m, int lane, int j,
-                                          float (&out)[T][G]) {
-  float acc[T][G];
+// This warp's partial dot products of the FK_GROUP rows at shared offsets
+// w + ro[r] with its activation blocks; warp-reduced, in every lane.
+template <class WT>
+__device__ __forceinline__ void rows_part(uint32_t w, const uint32_t (&ro)[FK_GROUP], const XReg& x, unsigned m,
+                                          int lane, int j, float (&out)[FK_GROUP]) {
+  float acc[FK_GROUP];
 #pragma unroll
-  for (int t = 0; t < T; ++t)
-#pragma unroll
-    for (int r = 0; r < G; ++r) acc[t][r] = 0.f;
+  for (int r = 0; r < FK_GROUP; ++r) acc[r] = 0.f;
   const uint32_t wl = w + (uint32_t)(lane * 8 * (int)sizeof(WT));
 #pragma unroll
   for (int b = 0; b < FK_XB; ++b) {
     if ((m >> b) & 1u) {
       const uint32_t wb = wl + (uint32_t)((FK_GANG * b + j) * 256 * (int)sizeof(WT));
 #pragma unroll
-      for (int r = 0; r < G; ++r)
-#pragma unroll
-        for (int t = 0; t < T; ++t) acc[t][r] = dot8w<WT>(wb + (uint32_t)(r * rb), x.a[t][b], x.c[t][b], acc[t][r]);
+      for (int r = 0; r < FK_GROUP; ++r) acc[r] = dot8w<WT>(wb + ro[r], x.a[b], x.c[b], acc[r]);
     }
   }
 #pragma unroll
-  for (int t = 0; t < T; ++t)
-#pragma unroll
-    for (int r = 0; r < G; ++r) out[t][r] = warp_sum(acc[t][r]);
+  for (int r = 0; r < FK_GROUP; ++r) out[r] = warp_sum(acc[r]);
 }
 
-// Rows [r, r + G) of a chunk: each warp posts its partial sums to its half of
-// the exchange buffer (index r T + t).
-template <class WT, int T, int G>
-__device__ __forceinline__ void rows_group(uint32_t w, int r, int rb, const XReg<T>& x, unsigned m, const Stream& s,
-                                           float* xb) {
-  float o[T][G];
-  rows_part<WT, T, G>(w + (uint32_t)(r * rb), rb, x, m, s.lane, s.j, o);
-  if (s.lane == 0) {
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int t = 0; t < T; ++t) xb[s.j * FK_XCH + (r + g) * T + t] = o[t][g];
-  }
-}
-
-// All R rows of a chunk (R T <= FK_XCH); after the gang barrier the first
-// warp's lane 0 passes each completed sum to epi(r, t, v).
-template <class WT, int T, class Epi>
-__device__ __forceinline__ void chunk_rows(uint32_t w, int R, int rb, const XReg<T>& x, unsigned m, const Stream& s,
-                                           float* xb, Epi& epi) {
-  constexpr int G = FK_GROUP;
-  int r = 0;
-  for (; r + G <= R; r += G) rows_group<WT, T, G>(w, r, rb, x, m, s, xb);
-  if (R - r == 2)
-    rows_group<WT, T, 2>(w, r, rb, x, m, s, xb);
-  else if (R - r == 1)
-    rows_group<WT, T, 1>(w, r, rb, x, m, s, xb);
-  gang_sync(s);
-  if (s.j == 0 && s.lane == 0)
-    for (int i = 0; i < R; ++i)
-#pragma unroll
-      for (int t = 0; t < T; ++t) epi(i, t, xb[i * T + t] + xb[FK_XCH + i * T + t]);
-}
-
-template <class WT, int T, class Epi>
-__device__ __forceinline__ void stream_rows_t(Cons c, int r0, int r1, int K, uint32_t xs, Epi& epi) {
+// Rows [r0, r1) of a row-major [*, K] matrix streamed from the ring (the
+// chunks the producer cut them into) against T plane-layout vectors at shared
+// offset xs (token t at xs + 4 K t): out[t * ts + row] = row . x_t.  Rows go
+// FK_GROUP at a time (a short last group repeats its last row and drops the
+// copies); the two warps of a gang post their halves to the exchange buffer
+// and the first warp's lane 0 stores the sums.  Advances the ring position
+// past the rows' chunks.
+template <class WT>
+__device__ __forceinline__ void stream_rows(Cons c, int r0, int r1, int K, int T, uint32_t xs, float* out, int ts) {
   Stream s = stream_begin(c);
   const int rb = K * (int)sizeof(WT);
   const int rpc = rows_per_chunk(rb);
   const uint32_t n0 = cst().n;
   const uint32_t nch = r1 > r0 ? (uint32_t)((r1 - r0 + rpc - 1) / rpc) : 0u;
   const unsigned m = xblocks(K, s.lane, s.j);
-  XReg<T> x;
-  load_xreg<T>(x, xs, K, s.lane, s.j, m);
   for (uint32_t n = first_chunk(n0, s.gang); n < n0 + nch; n += FK_NGANG) {
     const uint32_t buf = chunk_wait(s, n);
     const int base = r0 + (int)(n - n0) * rpc, R = min(rpc, r1 - base);
-    auto e = [&](int r, int t, float v) { epi(base + r, t, v); };
-    chunk_rows<WT, T>(buf, R, rb, x, m, s, xch_buf(s, n), e);
+    float* xb = xch_buf(s, n);
+    for (int t = 0; t < T; ++t) {
+      XReg x;
+      load_xreg(x, xs + (uint32_t)(t * K * 4), K, s.lane, s.j, m);
+      for (int r = 0; r < R; r += FK_GROUP) {
+        const int cnt = min(FK_GROUP, R - r);  // rows past R repeat row R - 1
+        uint32_t ro[FK_GROUP];
+#pragma unroll
+        for (int g = 0; g < FK_GROUP; ++g) ro[g] = (uint32_t)(min(g, cnt - 1) * rb);
+        float o[FK_GROUP];
+        rows_part<WT>(buf + (uint32_t)(r * rb), ro, x, m, s.lane, s.j, o);
+        if (s.lane == 0) {
+#pragma unroll
+          for (int g = 0; g < FK_GROUP; ++g)
+            if (g < cnt) xb[s.j * FK_XCH + (r + g) * T + t] = o[g];
+        }
+      }
+    }
+    gang_sync(s);
+    if (s.j == 0 && s.lane == 0)
+      for (int i = 0; i < R * T; ++i) {
+        const int row = i / T, t = i - row * T;
+        out[t * ts + base + row] = xb[i] + xb[FK_XCH + i];
+      }
     chunk_release(s, n);
   }
   warp_set(cst().aborted, s.aborted ? 1 : 0);
   warp_set(cst().n, n0 + nch);
-}
-
-// Rows [r0, r1) of a row-major [*, K] matrix streamed from the ring (the
-// chunks the producer cut them into), against the T plane-layout vectors at
-// xs; epi(row, t, value) once per row and token.  Advances cst().n past the rows'
-// chunks.
-template <class WT, class Epi>
-__device__ __forceinline__ void stream_rows(Cons c, int r0, int r1, int K, int T, const float* xs, Epi epi) {
-  if (T > 1)
-    stream_rows_t<WT, 2>(c, r0, r1, K, soff(xs), epi);
-  else
-    stream_rows_t<WT, 1>(c, r0, r1, K, soff(xs), epi);
 }
 
 // ------------------------------------------------------- residual helpers
@@ -862,21 +830,6 @@ template <class WT>
 __device__ __forceinline__ const WT* side_gk(Cons c, int D) { return side_cur<WT>(c) + 2 * D + fk_prm()->hd; }
 
 // ---------------------------------------------------------------- phases
-
-// Phase A: layer input X_in (or tokens already in xs), fold into X_in+1 and
-// X_in+2, RMSNorm, QKV rows out.
-template <class WT>
-__device__ __forceinline__ void phase_qkv(Cons c, int D, int T, int in, bool from_xs) {
-  const FKParams& p = *fk_prm();
-  const WT* side = side_begin<WT>(c);
-  load_norm<WT>(c, from_xs, in, 0, T, D, side, xnext(in, 1), xnext(in, 2), nullptr);
-  int lo, hi;
-  split(p.qkv_rows, p.ncta, ccta(), lo, hi);
-  float* qkv = p.qkv;
-  const int qr = p.qkv_rows;
-  stream_rows<WT>(c, lo, hi, D, T, fk_sm()->u.g.xs, [=](int row, int t, float v) { qkv[t * qr + row] = v; });
-  grid_sync(c);
-}
 
 // o_proj is cut into tiles of 32 output columns of one head.  A tile is
 // stored lane-interleaved, [hd/8][32][8]: lane l's 8 weights of hd block kb
@@ -1245,86 +1198,90 @@ __device__ __forceinline__ void phase_talker_oproj(Cons c, int xa, int xb) {
 }
 
 // One FFN unit f at shared offset u (gate row, up row, down column; D weights
-// each), shared by the two warps of a gang: each takes its activation blocks
-// of the gate/up dot products, the partial sums meet in the exchange buffer
-// slot xu (2 T floats per warp), both form a_t = silu(gate_f . x_t) *
-// (up_f . x_t), and each adds a_t W_down[:, f] into the columns of its own
-// blocks: lane l, block i = 2 b + j holds columns 8 l + 256 i + q as
-// y[t (4 / T) + b][q].
-template <class WT, int T>
-__device__ __forceinline__ void ffn_unit(uint32_t u, int D, const XReg<T>& x, unsigned m, const Stream& s, float* xu,
-                                         float (&y)[4][8]) {
-  constexpr int NB = FK_XB / T;  // blocks per token and warp (D <= 256 NB FK_GANG)
+// each) for T tokens, shared by the two warps of a gang: each takes its
+// activation blocks of the gate/up dot products, the partial sums meet in the
+// exchange buffer slot xu (4 floats per warp), both form a_t =
+// silu(gate_f . x_t) * (up_f . x_t), and each adds a_t W_down[:, f] into the
+// columns of its own blocks.  Down sums: slot q = t nb + b (nb block slots
+// per token, T nb <= 4) holds columns 8 lane + 256 (2 b + j) + k of token t
+// as y[q][k].
+template <class WT>
+__device__ __forceinline__ void ffn_unit(uint32_t u, int D, int T, int nb, uint32_t xs, unsigned m, const Stream& s,
+                                         float* xu, float (&y)[4][8]) {
   const uint32_t rb = (uint32_t)D * (uint32_t)sizeof(WT);
   const uint32_t wl = u + (uint32_t)(s.lane * 8 * (int)sizeof(WT));
-  float g[T], v[T];
+  float g0 = 0.f, u0 = 0.f, g1 = 0.f, u1 = 0.f;
+  for (int t = 0; t < T; ++t) {
+    XReg x;
+    load_xreg(x, xs + (uint32_t)(t * D * 4), D, s.lane, s.j, m);
+    float g = 0.f, v = 0.f;
 #pragma unroll
-  for (int t = 0; t < T; ++t) g[t] = v[t] = 0.f;
-#pragma unroll
-  for (int b = 0; b < NB; ++b) {
-    if ((m >> b) & 1u) {
-      const uint32_t wb = wl + (uint32_t)((FK_GANG * b + s.j) * 256 * (int)sizeof(WT));
-#pragma unroll
-      for (int t = 0; t < T; ++t) {
-        g[t] = dot8w<WT>(wb, x.a[t][b], x.c[t][b], g[t]);
-        v[t] = dot8w<WT>(wb + rb, x.a[t][b], x.c[t][b], v[t]);
+    for (int b = 0; b < FK_XB; ++b) {
+      if ((m >> b) & 1u) {
+        const uint32_t wb = wl + (uint32_t)((FK_GANG * b + s.j) * 256 * (int)sizeof(WT));
+        g = dot8w<WT>(wb, x.a[b], x.c[b], g);
+        v = dot8w<WT>(wb + rb, x.a[b], x.c[b], v);
       }
     }
-  }
-#pragma unroll
-  for (int t = 0; t < T; ++t) {
-    g[t] = warp_sum(g[t]);
-    v[t] = warp_sum(v[t]);
-  }
-  if (s.lane == 0) {
-#pragma unroll
-    for (int t = 0; t < T; ++t) {
-      xu[s.j * FK_XCH + 2 * t] = g[t];
-      xu[s.j * FK_XCH + 2 * t + 1] = v[t];
+    if (t == 0) {
+      g0 = g;
+      u0 = v;
+    } else {
+      g1 = g;
+      u1 = v;
     }
   }
+  g0 = warp_sum(g0);
+  u0 = warp_sum(u0);
+  if (T > 1) {
+    g1 = warp_sum(g1);
+    u1 = warp_sum(u1);
+  }
+  if (s.lane == 0) {
+    xu[s.j * FK_XCH] = g0;
+    xu[s.j * FK_XCH + 1] = u0;
+    xu[s.j * FK_XCH + 2] = g1;
+    xu[s.j * FK_XCH + 3] = u1;
+  }
   gang_sync(s);
-  float act[T];
-#pragma unroll
-  for (int t = 0; t < T; ++t)
-    act[t] = silu(xu[2 * t] + xu[FK_XCH + 2 * t]) * (xu[2 * t + 1] + xu[FK_XCH + 2 * t + 1]);
+  const float a0 = silu(xu[0] + xu[FK_XCH]) * (xu[1] + xu[FK_XCH + 1]);
+  const float a1 = T > 1 ? silu(xu[2] + xu[FK_XCH + 2]) * (xu[3] + xu[FK_XCH + 3]) : 0.f;
   const uint32_t wd = wl + 2u * rb;
 #pragma unroll
-  for (int b = 0; b < NB; ++b) {
-    if ((m >> b) & 1u) {
+  for (int q = 0; q < 4; ++q) {
+    const int t = q >= nb ? 1 : 0, b = q - t * nb;
+    if (t < T && ((m >> b) & 1u)) {
       float d8[8];
       lds_w8<WT>(wd + (uint32_t)((FK_GANG * b + s.j) * 256 * (int)sizeof(WT)), d8);
+      const float a = t ? a1 : a0;
 #pragma unroll
-      for (int t = 0; t < T; ++t)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) y[t * NB + b][q] = fmaf(act[t], d8[q], y[t * NB + b][q]);
+      for (int k = 0; k < 8; ++k) y[q][k] = fmaf(a, d8[k], y[q][k]);
     }
   }
 }
 
 // The gang's share of the CTA's FFN units [f0, f1) (chunks n0 .. n0 + nch),
 // its down-projection sums added into yred (layout at phase_ffn).
-template <class WT, int T>
-__device__ __forceinline__ void ffn_stream(Cons c, int D, int f0, int f1, uint32_t n0, uint32_t nch) {
-  constexpr int IM = 8 / T, NB = FK_XB / T;
+template <class WT>
+__device__ __forceinline__ void ffn_stream(Cons c, int D, int T, int f0, int f1, uint32_t n0, uint32_t nch) {
   Stream s = stream_begin(c);
   const int ub = 3 * D * (int)sizeof(WT);
   const int upc = rows_per_chunk(ub);
   FKSmem* sm = fk_sm();
+  const uint32_t xs = soff(sm->u.g.xs);
   const unsigned m = xblocks(D, s.lane, s.j);
-  XReg<T> x;
-  load_xreg<T>(x, soff(sm->u.g.xs), D, s.lane, s.j, m);
+  const int nb = ((D + 255) >> 8) > FK_GANG * 2 ? FK_XB : FK_XB / 2;  // block slots per token
   float y[4][8];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int q = 0; q < 8; ++q) y[i][q] = 0.f;
+    for (int k = 0; k < 8; ++k) y[i][k] = 0.f;
   bool any = false;
   for (uint32_t n = first_chunk(n0, s.gang); n < n0 + nch; n += FK_NGANG) {
     const uint32_t buf = chunk_wait(s, n);
     float* xbf = xch_buf(s, n);
     const int nu = min(upc, f1 - (f0 + (int)(n - n0) * upc));
-    for (int jj = 0; jj < nu; ++jj) ffn_unit<WT, T>(buf + (uint32_t)(jj * ub), D, x, m, s, xbf + 4 * jj, y);
+    for (int jj = 0; jj < nu; ++jj) ffn_unit<WT>(buf + (uint32_t)(jj * ub), D, T, nb, xs, m, s, xbf + 4 * jj, y);
     gang_sync(s);  // both warps are done with the chunk
     chunk_release(s, n);
     any = true;
@@ -1332,16 +1289,16 @@ __device__ __forceinline__ void ffn_stream(Cons c, int D, int f0, int f1, uint32
   warp_set(cst().aborted, s.aborted ? 1 : 0);
   if (any) {
     float* yred = sm->u.g.yred;
+    const int IM = 8 / T;
 #pragma unroll
-    for (int t = 0; t < T; ++t)
+    for (int q = 0; q < 4; ++q) {
+      const int t = q >= nb ? 1 : 0, b = q - t * nb;
+      if (t < T && ((m >> b) & 1u)) {
+        const int i = FK_GANG * b + s.j;
 #pragma unroll
-      for (int b = 0; b < NB; ++b) {
-        if ((m >> b) & 1u) {
-          const int i = FK_GANG * b + s.j;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) atomicAdd(&yred[((t * IM + i) * 8 + q) * 32 + s.lane], y[t * NB + b][q]);
-        }
+        for (int k = 0; k < 8; ++k) atomicAdd(&yred[((t * IM + i) * 8 + k) * 32 + s.lane], y[q][k]);
       }
+    }
   }
 }
 
@@ -1364,10 +1321,7 @@ __device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int xa, i
   const int upc = rows_per_chunk(3 * D * (int)sizeof(WT));
   const uint32_t n0 = cst().n;
   const uint32_t nch = f1 > f0 ? (uint32_t)((f1 - f0 + upc - 1) / upc) : 0u;
-  if (T > 1)
-    ffn_stream<WT, 2>(c, D, f0, f1, n0, nch);
-  else
-    ffn_stream<WT, 1>(c, D, f0, f1, n0, nch);
+  ffn_stream<WT>(c, D, T, f0, f1, n0, nch);
   warp_set(cst().n, n0 + nch);
   consumer_sync();
   const int IM = 8 / T, nq = D / 4;
@@ -1412,67 +1366,141 @@ __device__ __forceinline__ void xsum_add(Cons c, int j, int fed) {
     p.xsum[i] = j == 0 ? to_f(e[i]) : p.xsum[i] + to_f(e[i]);
 }
 
-// Start of CodePredictor pass j: draw code j, add its embedding to the
-// running sum, stage the pass's input token(s) and, when D_t != D_c, project
-// them (z = W_p u into X_0, one more phase).
+// The frame's schedule as a sequence of steps.  Per CodePredictor pass j
+// (0..14): DRAW (code j; embedding sum; input tokens), PROJ (when D_t != D_c),
+// L_c x (QKV, CP_ATTN, FFN), CP_HEAD.  Then DRAW (code 15; Talker input),
+// L_t x (QKV, T_ATTN, T_OPROJ, FFN), T_HEAD.  Every step kind has one call
+// site in the loop below, so each phase's code exists once.
+enum StepKind { S_DRAW, S_PROJ, S_QKV, S_CP_ATTN, S_FFN, S_CP_HEAD, S_T_ATTN, S_T_OPROJ, S_T_HEAD };
+
+struct Step {
+  int kind, j, l;  // j: CodePredictor pass (15: Talker), l: layer
+};
+
+__device__ __forceinline__ int steps_per_pass(const FKParams& p) { return 2 + (p.has_proj ? 1 : 0) + 3 * p.Lc; }
+
+__device__ __forceinline__ int frame_steps(const FKParams& p) {
+  return (Q3TTS_N_CODEBOOKS - 1) * steps_per_pass(p) + 2 + 4 * p.Lt;
+}
+
+__device__ __forceinline__ Step decode_step(const FKParams& p, int k) {
+  Step st;
+  const int pp = steps_per_pass(p), ncp = (Q3TTS_N_CODEBOOKS - 1) * pp, hp = p.has_proj ? 1 : 0;
+  st.l = 0;
+  if (k < ncp) {
+    st.j = k / pp;
+    const int r = k - st.j * pp;
+    if (r == 0) {
+      st.kind = S_DRAW;
+    } else if (r <= hp) {
+      st.kind = S_PROJ;
+    } else if (r == pp - 1) {
+      st.kind = S_CP_HEAD;
+    } else {
+      const int q = r - 1 - hp;
+      st.l = q / 3;
+      st.kind = q % 3 == 0 ? S_QKV : (q % 3 == 1 ? S_CP_ATTN : S_FFN);
+    }
+  } else {
+    st.j = Q3TTS_N_CODEBOOKS - 1;
+    const int r = k - ncp;
+    if (r == 0) {
+      st.kind = S_DRAW;
+    } else if (r == 1 + 4 * p.Lt) {
+      st.kind = S_T_HEAD;
+    } else {
+      const int q = r - 1;
+      st.l = q / 4;
+      const int w = q % 4;
+      st.kind = w == 0 ? S_QKV : (w == 1 ? S_T_ATTN : (w == 2 ? S_T_OPROJ : S_FFN));
+    }
+  }
+  return st;
+}
+
+// DRAW step: draw code j; code 0..14 starts CodePredictor pass j (running
+// embedding sum, input tokens), code 15 starts the Talker step (its input is
+// the sum of the frame's 16 code embeddings).
 template <class WT>
-__device__ __forceinline__ void pass_begin(Cons c, int j) {
+__device__ __forceinline__ void draw_step(Cons c, int j) {
   ConsState& L = cst();
   const int fed = draw_code(c, j);
   if (j == 0) warp_set(L.fed0, fed);
-  xsum_add<WT>(c, j, fed);
-  cp_tokens<WT>(c, j, fed);
-  warp_set(L.in, 0);
-  warp_set(L.from_xs, 1);
-  if (fk_prm()->has_proj) {
+  if (j < Q3TTS_N_CODEBOOKS - 1) {
+    xsum_add<WT>(c, j, fed);
+    cp_tokens<WT>(c, j, fed);
+  } else {
     const FKParams& q = *fk_prm();
-    int lo, hi;
-    split(q.Dc, q.ncta, ccta(), lo, hi);
-    float* X0 = xbuf(q, 0, 0);
-    const int dmax = q.dmax;
-    stream_rows<WT>(c, lo, hi, q.Dt, j == 0 ? 2 : 1, fk_sm()->u.g.xs,
-                    [=](int row, int t, float v) { X0[t * dmax + row] = v; });
-    grid_sync(c);
-    warp_set(L.from_xs, 0);
+    const WT* e = (const WT*)q.cp_embeds + ((size_t)(Q3TTS_N_CODEBOOKS - 2) * q.Vc + fed) * q.Dt;
+    float* xs = fk_sm()->u.g.xs;
+    for (int i = ctid(); i < q.Dt; i += FK_CONSUMERS) put_plane(xs, q.Dt, i, __ldcg(q.xsum + i) + to_f(e[i]));
+    consumer_sync();
   }
-}
-
-// Start of the Talker step: draw the last acoustic code; the Talker input is
-// the sum of the frame's 16 code embeddings.
-template <class WT>
-__device__ __forceinline__ void talker_begin(Cons c) {
-  const int fed15 = draw_code(c, Q3TTS_N_CODEBOOKS - 1);
-  const FKParams& q = *fk_prm();
-  const WT* e = (const WT*)q.cp_embeds + ((size_t)(Q3TTS_N_CODEBOOKS - 2) * q.Vc + fed15) * q.Dt;
-  float* xs = fk_sm()->u.g.xs;
-  for (int i = ctid(); i < q.Dt; i += FK_CONSUMERS) put_plane(xs, q.Dt, i, __ldcg(q.xsum + i) + to_f(e[i]));
-  consumer_sync();
-  ConsState& L = cst();
   warp_set(L.in, 0);
   warp_set(L.from_xs, 1);
 }
 
-// Final norm of token t of the stack output and the CTA's head rows (streamed
-// from the ring): a CodePredictor head (logits to cp_logits, then a grid
-// barrier before the draw) or the Talker codec head (pending hidden slice and
-// pending logits).
+// Row-GEMV steps (QKV, PROJ, the heads): stage the input -- RMSNorm of the
+// layer input (QKV, folding it into the next two residual buffers), of the
+// stack output (heads), or the raw tokens already in xs (PROJ) -- then the
+// CTA's rows, then (all but the last step of the frame) a grid barrier.
 template <class WT>
-__device__ __forceinline__ void head_phase(Cons c, bool talker, int t) {
-  const FKParams& q = *fk_prm();
-  const int D = talker ? q.Dt : q.Dc, V = talker ? q.Vt : q.Vc;
-  const WT* g = reinterpret_cast<const WT*>(fk_sm()->fin) + (talker ? q.Dc : 0);
-  load_norm<WT>(c, false, cst().in, t, 1, D, g, -1, -1, talker ? q.pending_h + (size_t)q.sid * q.Dt : nullptr);
+__device__ __forceinline__ void rows_step(Cons c, const Step& st) {
+  ConsState& L = cst();
+  const FKParams& p = *fk_prm();
+  const bool cp = st.j < Q3TTS_N_CODEBOOKS - 1;
+  const int Tp = cp && st.j == 0 ? 2 : 1;  // tokens of the pass
+  int K, T, nrows, ts;
+  float* out;
+  if (st.kind == S_QKV) {
+    K = cp ? p.Dc : p.Dt;
+    T = Tp;
+    nrows = p.qkv_rows;
+    out = p.qkv;
+    ts = p.qkv_rows;
+  } else if (st.kind == S_PROJ) {
+    K = p.Dt;
+    T = Tp;
+    nrows = p.Dc;
+    out = xbuf(p, 0, 0);
+    ts = p.dmax;
+  } else if (st.kind == S_CP_HEAD) {
+    K = p.Dc;
+    T = 1;
+    nrows = p.Vc;
+    out = p.cp_logits;
+    ts = 0;
+  } else {
+    K = p.Dt;
+    T = 1;
+    nrows = p.Vt;
+    out = p.pending_logits + (size_t)p.sid * p.Vt;
+    ts = 0;
+  }
+  if (st.kind != S_PROJ) {
+    const WT* g;
+    int fa = -1, fb = -1, t0 = 0;
+    float* hout = nullptr;
+    if (st.kind == S_QKV) {
+      g = side_begin<WT>(c);
+      fa = xnext(L.in, 1);
+      fb = xnext(L.in, 2);
+    } else {
+      g = reinterpret_cast<const WT*>(fk_sm()->fin) + (cp ? 0 : p.Dc);
+      t0 = Tp - 1;
+      if (!cp) hout = p.pending_h + (size_t)p.sid * p.Dt;
+    }
+    load_norm<WT>(c, st.kind == S_QKV && L.from_xs, L.in, t0, T, K, g, fa, fb, hout);
+  }
   int lo, hi;
-  split(V, q.ncta, ccta(), lo, hi);
-  float* out = talker ? q.pending_logits + (size_t)q.sid * q.Vt : q.cp_logits;
-  stream_rows<WT>(c, lo, hi, D, 1, fk_sm()->u.g.xs, [=](int row, int, float v) { out[row] = v; });
-  if (!talker) grid_sync(c);
+  split(nrows, p.ncta, ccta(), lo, hi);
+  stream_rows<WT>(c, lo, hi, K, T, soff(fk_sm()->u.g.xs), out, ts);
+  if (st.kind != S_T_HEAD) grid_sync(c);
+  warp_set(L.from_xs, 0);
 }
 
-// The consumer warps' schedule for one frame: 15 CodePredictor passes of L_c
-// layers, then the Talker's L_t layers, as one loop over layer steps so that
-// every phase function has a single call site and is inlined.  Loop state
-// lives in the warp's shared-memory record (cst()).
+// The consumer warps' schedule for one frame (steps above).  Loop state lives
+// in the warp's shared-memory record (cst()).
 template <class WT, class KT>
 __device__ void consumer() {
   Cons c;
@@ -1502,31 +1530,33 @@ __device__ void consumer() {
   }
   consumer_sync();
   ConsState& L = cst();
-  for (warp_set(L.k, 0); L.k < (Q3TTS_N_CODEBOOKS - 1) * fk_prm()->Lc + fk_prm()->Lt; warp_set(L.k, L.k + 1)) {
-    const int Lc = fk_prm()->Lc, ncp = (Q3TTS_N_CODEBOOKS - 1) * Lc;
-    const bool cp = L.k < ncp;
-    const int j = cp ? L.k / Lc : Q3TTS_N_CODEBOOKS - 1, l = cp ? L.k % Lc : L.k - ncp;
-    if (l == 0) {
-      if (cp)
-        pass_begin<WT>(c, j);
-      else
-        talker_begin<WT>(c);
+  for (warp_set(L.k, 0); L.k < frame_steps(*fk_prm()); warp_set(L.k, L.k + 1)) {
+    const Step st = decode_step(*fk_prm(), L.k);
+    const bool cp = st.j < Q3TTS_N_CODEBOOKS - 1;
+    const int T = cp && st.j == 0 ? 2 : 1;
+    switch (st.kind) {
+      case S_DRAW:
+        draw_step<WT>(c, st.j);
+        break;
+      case S_CP_ATTN:
+        phase_cp_attn<WT>(c, st.l, T, st.j == 0 ? 0 : st.j + 1, xnext(L.in, 1), xnext(L.in, 2));
+        break;
+      case S_T_ATTN:
+        phase_talker_attn<WT, KT>(c, st.l);
+        break;
+      case S_T_OPROJ:
+        phase_talker_oproj<WT>(c, xnext(L.in, 1), xnext(L.in, 2));
+        break;
+      case S_FFN:
+        phase_ffn<WT>(c, cp ? fk_prm()->Dc : fk_prm()->Dt, cp ? fk_prm()->Fc : fk_prm()->Ft, T, xnext(L.in, 1),
+                      xnext(L.in, 2));
+        warp_set(L.in, xnext(L.in, 2));
+        break;
+      default:
+        rows_step<WT>(c, st);
+        break;
     }
-    const int T = (cp && j == 0) ? 2 : 1;
-    const int D = cp ? fk_prm()->Dc : fk_prm()->Dt;
-    phase_qkv<WT>(c, D, T, L.in, L.from_xs != 0);
-    warp_set(L.from_xs, 0);
-    if (cp) {
-      phase_cp_attn<WT>(c, l, T, j == 0 ? 0 : j + 1, xnext(L.in, 1), xnext(L.in, 2));
-    } else {
-      phase_talker_attn<WT, KT>(c, l);
-      phase_talker_oproj<WT>(c, xnext(L.in, 1), xnext(L.in, 2));
-    }
-    phase_ffn<WT>(c, D, cp ? fk_prm()->Fc : fk_prm()->Ft, T, xnext(L.in, 1), xnext(L.in, 2));
-    warp_set(L.in, xnext(L.in, 2));
-    if (cp && l == Lc - 1) head_phase<WT>(c, false, T - 1);
   }
-  head_phase<WT>(c, true, 0);
   {
     const FKParams& q = *fk_prm();
     if (ccta() == 0 && ctid() == 0) q.history[(size_t)q.sid * q.Vt + L.fed0] = 1;
