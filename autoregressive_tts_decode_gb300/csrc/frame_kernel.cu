@@ -61,7 +61,7 @@ constexpr int FK_NSTAGE = 11;
 constexpr int FK_TMAX = 2;     // tokens per pass (CodePredictor pass 0 carries two)
 constexpr int FK_DMAX = 2048;  // widest hidden state staged in shared memory
 constexpr int FK_HDMAX = 128;
-constexpr int FK_REPMAX = 4;   // q heads per kv head
+constexpr int FK_REPMAX = 2;   // q heads per kv head
 constexpr int FK_MAXCTA = 256;
 constexpr int FK_PAIRS = 4;    // (head, token) pairs of one CTA in a CodePredictor attention
 constexpr long long FK_WAIT_CYCLES = 4000000000ll;  // ~2 s at GB300 clocks
@@ -267,6 +267,7 @@ struct AttnScratch {
   float l[FK_CONSUMER_WARPS][FK_PAIRS];
   float o[FK_CONSUMER_WARPS][FK_PAIRS][FK_HDMAX];
   float q[FK_PAIRS][FK_HDMAX];
+  float kcur[FK_PAIRS][FK_HDMAX];  // current-position keys (token, kv group), normalised and rotated
 };
 static_assert(FK_PAIRS >= FK_REPMAX, "talker attention keeps one partial per q head of a group");
 
@@ -843,14 +844,17 @@ __device__ __forceinline__ void oproj_tiles(const FKParams& p, int D, int cta, i
 }
 
 // The CTA's o_proj tiles against the attention outputs of its (<= 2) heads
-// (os, plane layout; h_first is the first head); each column's sum goes into
-// both X_a and X_b.  The two warps of a gang take alternate hd blocks of a
-// tile and meet in the exchange buffer.
+// (os, plane layout), for T tokens; each column's sum goes into both X_a and
+// X_b.  The two warps of a gang take alternate hd blocks of a tile and meet in
+// the exchange buffer.  Closes the attention phase with a grid barrier.
 template <class WT>
-__device__ void oproj_cols(Cons c, int D, int T, int xa, int xb, int t0, int t1, int h_first) {
+__device__ __forceinline__ void oproj_step(Cons c, int D, int T, int xa, int xb) {
   const FKParams& p = *fk_prm();
   Stream s = stream_begin(c);
   const int hd = p.hd, nt = oproj_nt(D), nkb = hd >> 3, dmax = p.dmax;
+  int t0, t1;
+  oproj_tiles(p, D, ccta(), t0, t1);
+  const int h_first = t0 / nt;
   const int tb = 32 * hd * (int)sizeof(WT);
   const int tpc = rows_per_chunk(tb);
   float* XA = xbuf(p, xa, 0);
@@ -866,25 +870,16 @@ __device__ void oproj_cols(Cons c, int D, int T, int xa, int xb, int t0, int t1,
     const int tf = t0 + (int)(n - n0) * tpc, ntl = min(tpc, t1 - tf);
     for (int jt = 0; jt < ntl; ++jt) {
       const int ti = tf + jt, h = ti / nt, col = (ti - h * nt) * 32 + s.lane;
-      const uint32_t xo = os0 + (uint32_t)(h - h_first) * OS_HEAD;
       const uint32_t w = buf + (uint32_t)(jt * tb + s.lane * 8 * (int)sizeof(WT));
-      float a[FK_TMAX] = {0.f, 0.f}, b[FK_TMAX] = {0.f, 0.f};
-      if (T > 1) {
+      for (int t = 0; t < T; ++t) {
+        const uint32_t xo = os0 + (uint32_t)(h - h_first) * OS_HEAD + (uint32_t)t * OS_TOK;
+        float a = 0.f, b = 0.f;
 #pragma unroll 2
-        for (int kb = s.j; kb < nkb; kb += FK_GANG) {
-          const uint32_t wk = w + (uint32_t)(kb * 256 * (int)sizeof(WT));
-          fma8<WT>(wk, lds_f4(xo + (uint32_t)(kb * 16)), lds_f4(xo + (uint32_t)(2 * hd + kb * 16)), a[0], b[0]);
-          fma8<WT>(wk, lds_f4(xo + OS_TOK + (uint32_t)(kb * 16)), lds_f4(xo + OS_TOK + (uint32_t)(2 * hd + kb * 16)),
-                   a[1], b[1]);
-        }
-      } else {
-#pragma unroll 4
         for (int kb = s.j; kb < nkb; kb += FK_GANG)
           fma8<WT>(w + (uint32_t)(kb * 256 * (int)sizeof(WT)), lds_f4(xo + (uint32_t)(kb * 16)),
-                   lds_f4(xo + (uint32_t)(2 * hd + kb * 16)), a[0], b[0]);
+                   lds_f4(xo + (uint32_t)(2 * hd + kb * 16)), a, b);
+        xbf[s.j * FK_XCH + t * 32 + s.lane] = a + b;
       }
-      xbf[s.j * FK_XCH + s.lane] = a[0] + b[0];
-      if (T > 1) xbf[s.j * FK_XCH + 32 + s.lane] = a[1] + b[1];
       gang_sync(s);
       if (s.j == 0 && col < D) {
         for (int t = 0; t < T; ++t) {
@@ -899,6 +894,7 @@ __device__ void oproj_cols(Cons c, int D, int T, int xa, int xb, int t0, int t1,
   }
   warp_set(cst().aborted, s.aborted ? 1 : 0);
   warp_set(cst().n, n0 + nch);
+  grid_sync(c);
 }
 
 // Stores a warp's head vector (lane holds l + 32 j) into plane layout.
@@ -926,7 +922,42 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
   AttnScratch& as = fk_sm()->u.att;
   const float scale = 1.0f / sqrtf((float)hd);
   const int S = pos0 + T;  // positions 0..S-1 exist after this pass
-  // 1) this warp's positions (warp, warp + 8): k, v of every touched kv group
+  // 1) q of each (head, token) pair, normalised and rotated (warps < npair);
+  //    the pass's current-position keys, one (token, kv group) per warp from
+  //    warp 4 on, normalised, rotated and kept in shared memory -- the CTA
+  //    owning the first o_proj tile of the group appends k and v to the cache
+  {
+    const int w = cwarp();
+    const bool isq = w < npair, isk = w >= FK_CONSUMER_WARPS - FK_PAIRS && w - (FK_CONSUMER_WARPS - FK_PAIRS) < T * ng;
+    if (isq || isk) {
+      const int it = w - (FK_CONSUMER_WARPS - FK_PAIRS);
+      const int t = isq ? w % T : it / ng, gi = isq ? 0 : it % ng;
+      const int h = h_first + w / T, g = g_first + gi;
+      const float* src = p.qkv + (size_t)t * p.qkv_rows + (isq ? h * hd : (Hq + g) * hd);
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = j < J ? __ldcg(src + clane() + 32 * j) : 0.f;
+      norm_rope_head(p, fk_sm(), v, isq ? side_gq<WT>(c, D) : side_gk<WT>(c, D), cp_rope_row(pos0 + t), clane());
+      float* dst = isq ? as.q[w] : as.kcur[it];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j < J) dst[clane() + 32 * j] = v[j];
+      if (isk && g * rep * nt >= v0 && g * rep * nt < v1) {
+        const float* vs = p.qkv + (size_t)t * p.qkv_rows + (Hq + Hkv + g) * hd;
+        float* kc = (float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, pos0 + t, 0, g);
+        float* vc = (float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, pos0 + t, 1, g);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < J) {
+            kc[clane() + 32 * j] = v[j];
+            vc[clane() + 32 * j] = __ldcg(vs + clane() + 32 * j);
+          }
+      }
+    }
+  }
+  consumer_sync();
+  // 2) this warp's positions (warp, warp + 8): k, v of every touched kv group
+  //    (earlier positions from the cache, current ones: k from step 1, v raw)
   float kk[2][2][4], vv[2][2][4];
 #pragma unroll
   for (int np = 0; np < 2; ++np) {
@@ -935,56 +966,21 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
     for (int gi = 0; gi < 2; ++gi) {
       const int g = g_first + gi;
       if (sp < S && gi < ng) {
-        const float* kc;
-        const float* vc;
-        if (sp < pos0) {
-          kc = (const float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 0, g);
-          vc = (const float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 1, g);
-        } else {
-          kc = p.qkv + (size_t)(sp - pos0) * p.qkv_rows + (Hq + g) * hd;
-          vc = p.qkv + (size_t)(sp - pos0) * p.qkv_rows + (Hq + Hkv + g) * hd;
-        }
+        const bool cur = sp >= pos0;
+        const float* kc = cur ? (const float*)p.ckv.pool
+                              : (const float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 0, g);
+        const float* vc = cur ? p.qkv + (size_t)(sp - pos0) * p.qkv_rows + (Hq + Hkv + g) * hd
+                              : (const float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 1, g);
+        const float* ks = as.kcur[cur ? (sp - pos0) * ng + gi : 0];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          kk[np][gi][j] = j < J ? __ldcg(kc + clane() + 32 * j) : 0.f;
+          kk[np][gi][j] = j < J ? (cur ? ks[clane() + 32 * j] : __ldcg(kc + clane() + 32 * j)) : 0.f;
           vv[np][gi][j] = j < J ? __ldcg(vc + clane() + 32 * j) : 0.f;
         }
       }
     }
   }
-  // 2) q of each (head, token) pair, normalised and rotated
-  if (cwarp() < npair) {
-    const int h = h_first + cwarp() / T, t = cwarp() % T;
-    float q[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) q[j] = j < J ? __ldcg(p.qkv + (size_t)t * p.qkv_rows + h * hd + clane() + 32 * j) : 0.f;
-    norm_rope_head(p, fk_sm(), q, side_gq<WT>(c, D), cp_rope_row(pos0 + t), clane());
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (j < J) as.q[cwarp()][clane() + 32 * j] = q[j];
-  }
-  // 3) current-position keys: normalise, rotate, append (designated CTA)
-#pragma unroll
-  for (int np = 0; np < 2; ++np) {
-    const int sp = cwarp() + FK_CONSUMER_WARPS * np;
-#pragma unroll
-    for (int gi = 0; gi < 2; ++gi) {
-      if (sp < S && sp >= pos0 && gi < ng) {
-        const int g = g_first + gi;
-        norm_rope_head(p, fk_sm(), kk[np][gi], side_gk<WT>(c, D), cp_rope_row(sp), clane());
-        const int first = g * rep * nt;  // first o_proj tile of the group's first q head
-        if (first >= v0 && first < v1) {
-          float* kc = (float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 0, g);
-          float* vc = (float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 1, g);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (j < J) { kc[clane() + 32 * j] = kk[np][gi][j]; vc[clane() + 32 * j] = vv[np][gi][j]; }
-        }
-      }
-    }
-  }
-  consumer_sync();
-  // 4) per-warp partial softmax over its positions, for every pair
+  // 3) per-warp partial softmax over its positions, for every pair
   for (int pr = 0; pr < npair; ++pr) {
     const int h = h_first + pr / T, t = pr % T, gsel = h / rep - g_first;
     float m = -INFINITY, l = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1015,7 +1011,7 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
       if (j < J) as.o[cwarp()][pr][clane() + 32 * j] = o[j];
   }
   consumer_sync();
-  // 5) combine the warps: thread (pair, d)
+  // 4) combine the warps: thread (pair, d)
   for (int e = ctid(); e < npair * hd; e += FK_CONSUMERS) {
     const int pr = e / hd, d = e % hd;
     float M = -INFINITY;
@@ -1031,8 +1027,7 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
     put_plane(fk_sm()->os[pr / T][pr % T], hd, d, Os / Ls);
   }
   consumer_sync();
-  oproj_cols<WT>(c, D, T, xa, xb, v0, v1, h_first);
-  grid_sync(c);
+  oproj_step<WT>(c, D, T, xa, xb);
 }
 
 // Talker phase B1: attention partials.  Work item = (kv group g, position
@@ -1049,25 +1044,42 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
   const float scale = 1.0f / sqrtf((float)hd);
   if (g < Hkv) {
     const int cs = (S + cpg - 1) / cpg, s0 = ch * cs, s1 = min(S, s0 + cs);
-    if (cwarp() < rep) {
-      const int h = g * rep + cwarp();
-      float q[4];
+    // q of the group's heads (warps < rep); the current key (warp rep, in
+    // the item holding the current position), normalised, rotated, kept in
+    // shared memory and appended to the cache with its v
+    const bool isk = cwarp() == rep && pos >= s0 && pos < s1;
+    if (cwarp() < rep || isk) {
+      const float* src = p.qkv + (isk ? (Hq + g) * hd : (g * rep + cwarp()) * hd);
+      float v[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) q[j] = j < J ? __ldcg(p.qkv + h * hd + clane() + 32 * j) : 0.f;
-      norm_rope_head(p, fk_sm(), q, side_gq<WT>(c, p.Dt), TALKER_ROPE_ROW, clane());
+      for (int j = 0; j < 4; ++j) v[j] = j < J ? __ldcg(src + clane() + 32 * j) : 0.f;
+      norm_rope_head(p, fk_sm(), v, isk ? side_gk<WT>(c, p.Dt) : side_gq<WT>(c, p.Dt), TALKER_ROPE_ROW, clane());
+      float* dst = isk ? as.kcur[0] : as.q[cwarp()];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        if (j < J) as.q[cwarp()][clane() + 32 * j] = q[j];
+        if (j < J) dst[clane() + 32 * j] = v[j];
+      if (isk) {
+        KT* kc = (KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, pos, 0, g);
+        KT* vc = (KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, pos, 1, g);
+        const float* vs = p.qkv + (Hq + Hkv + g) * hd;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < J) {
+            kc[clane() + 32 * j] = from_f<KT>(v[j]);
+            vc[clane() + 32 * j] = from_f<KT>(__ldcg(vs + clane() + 32 * j));
+          }
+      }
     }
     consumer_sync();
     float m[FK_REPMAX], l[FK_REPMAX], o[FK_REPMAX][4];
 #pragma unroll
     for (int r = 0; r < FK_REPMAX; ++r) {
-      m[r] = -INFINITY; l[r] = 0.f;
+      m[r] = -INFINITY;
+      l[r] = 0.f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) o[r][j] = 0.f;
     }
-    constexpr int BATCH = 4;
+    constexpr int BATCH = 2;
     for (int sb = s0 + cwarp(); sb < s1; sb += BATCH * FK_CONSUMER_WARPS) {
       float k[BATCH][4], v[BATCH][4];
 #pragma unroll
@@ -1082,10 +1094,11 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
             v[b][j] = j < J ? to_f(vc[clane() + 32 * j]) : 0.f;
           }
         } else {
+          const float* vs = p.qkv + (Hq + Hkv + g) * hd;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            k[b][j] = (sp == pos && j < J) ? __ldcg(p.qkv + (Hq + g) * hd + clane() + 32 * j) : 0.f;
-            v[b][j] = (sp == pos && j < J) ? __ldcg(p.qkv + (Hq + Hkv + g) * hd + clane() + 32 * j) : 0.f;
+            k[b][j] = (sp == pos && j < J) ? as.kcur[0][clane() + 32 * j] : 0.f;
+            v[b][j] = (sp == pos && j < J) ? __ldcg(vs + clane() + 32 * j) : 0.f;
           }
         }
       }
@@ -1093,14 +1106,6 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
       for (int b = 0; b < BATCH; ++b) {
         const int sp = sb + b * FK_CONSUMER_WARPS;
         if (sp < s1) {
-          if (sp == pos) {
-            norm_rope_head(p, fk_sm(), k[b], side_gk<WT>(c, p.Dt), TALKER_ROPE_ROW, clane());
-            KT* kc = (KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, pos, 0, g);
-            KT* vc = (KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, pos, 1, g);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (j < J) { kc[clane() + 32 * j] = from_f<KT>(k[b][j]); vc[clane() + 32 * j] = from_f<KT>(v[b][j]); }
-          }
 #pragma unroll
           for (int r = 0; r < FK_REPMAX; ++r) {
             if (r < rep) {
@@ -1122,7 +1127,10 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
 #pragma unroll
     for (int r = 0; r < FK_REPMAX; ++r) {
       if (r < rep) {
-        if (clane() == 0) { as.m[cwarp()][r] = m[r]; as.l[cwarp()][r] = l[r]; }
+        if (clane() == 0) {
+          as.m[cwarp()][r] = m[r];
+          as.l[cwarp()][r] = l[r];
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           if (j < J) as.o[cwarp()][r][clane() + 32 * j] = o[r][j];
@@ -1145,7 +1153,10 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
       }
       float* dst = p.part + ((size_t)(g * rep + r) * cpg + ch) * (hd + 2);
       dst[2 + d] = Os;
-      if (d == 0) { dst[0] = M; dst[1] = Ls; }
+      if (d == 0) {
+        dst[0] = M;
+        dst[1] = Ls;
+      }
     }
   }
   grid_sync(c);
@@ -1193,8 +1204,7 @@ __device__ __forceinline__ void phase_talker_oproj(Cons c, int xa, int xb) {
     put_plane(fk_sm()->os[hh][0], hd, d, Os / Ls);
   }
   consumer_sync();
-  oproj_cols<WT>(c, D, 1, xa, xb, v0, v1, h_first);
-  grid_sync(c);
+  oproj_step<WT>(c, D, 1, xa, xb);
 }
 
 // One FFN unit f at shared offset u (gate row, up row, down column; D weights
@@ -1368,8 +1378,8 @@ __device__ __forceinline__ void xsum_add(Cons c, int j, int fed) {
 
 // The frame's schedule as a sequence of steps.  Per CodePredictor pass j
 // (0..14): DRAW (code j; embedding sum; input tokens), PROJ (when D_t != D_c),
-// L_c x (QKV, CP_ATTN, FFN), CP_HEAD.  Then DRAW (code 15; Talker input),
-// L_t x (QKV, T_ATTN, T_OPROJ, FFN), T_HEAD.  Every step kind has one call
+// L_c x (QKV, CP_ATTN (+ o_proj), FFN), CP_HEAD.  Then DRAW (code 15; Talker
+// input), L_t x (QKV, T_ATTN, T_OPROJ (combine + o_proj), FFN), T_HEAD.  Every step kind has one call
 // site in the loop below, so each phase's code exists once.
 enum StepKind { S_DRAW, S_PROJ, S_QKV, S_CP_ATTN, S_FFN, S_CP_HEAD, S_T_ATTN, S_T_OPROJ, S_T_HEAD };
 
@@ -1397,9 +1407,9 @@ __device__ __forceinline__ Step decode_step(const FKParams& p, int k) {
     } else if (r == pp - 1) {
       st.kind = S_CP_HEAD;
     } else {
-      const int q = r - 1 - hp;
+      const int q = r - 1 - hp, w = q % 3;
       st.l = q / 3;
-      st.kind = q % 3 == 0 ? S_QKV : (q % 3 == 1 ? S_CP_ATTN : S_FFN);
+      st.kind = w == 0 ? S_QKV : (w == 1 ? S_CP_ATTN : S_FFN);
     }
   } else {
     st.j = Q3TTS_N_CODEBOOKS - 1;
@@ -1409,9 +1419,8 @@ __device__ __forceinline__ Step decode_step(const FKParams& p, int k) {
     } else if (r == 1 + 4 * p.Lt) {
       st.kind = S_T_HEAD;
     } else {
-      const int q = r - 1;
+      const int q = r - 1, w = q % 4;
       st.l = q / 4;
-      const int w = q % 4;
       st.kind = w == 0 ? S_QKV : (w == 1 ? S_T_ATTN : (w == 2 ? S_T_OPROJ : S_FFN));
     }
   }

@@ -121,18 +121,20 @@ def test_static_scratch_rejections_leave_state(q3):
 
 def test_static_scratch_too_small_is_rejected(q3):
     """A shape the persistent kernel accepts whose scratch exceeds the static
-    array: one KV head shared by four query heads of width 128 at Talker width
-    2048 needs 4 * n_sm * 130 floats of attention partials alone.  The call
-    returns Q3TTS_ERR_SCRATCH before anything is launched (configuration checks
-    come before the stream's state)."""
+    array: 32 query heads over 16 KV heads of width 128 at Talker width 2048
+    (QKV rows, attention partials) with a 4096-entry CodePredictor vocabulary.
+    The call returns Q3TTS_ERR_SCRATCH before anything is launched
+    (configuration checks come before the stream's state)."""
     import torch
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
     shape = dataclasses.replace(synth.WORKLOADS["tiny"].shape, talker_layers=1, cp_layers=1,
                                 talker_hidden=2048, cp_hidden=1024, talker_ffn=256, cp_ffn=256,
-                                n_q_heads=4, n_kv_heads=1, head_dim=128, codec_vocab=256,
-                                cp_vocab=256, weight_dtype=synth.DTYPE_BF16)
+                                n_q_heads=32, n_kv_heads=16, head_dim=128, codec_vocab=256,
+                                cp_vocab=4096, weight_dtype=synth.DTYPE_BF16)
     ncta = min(n_sm, 256)
-    need = 256 + 3 * (4 * 2 * 2 * 2048) + 4 * 2 * 768 + 4 * 4 * ncta * 130 + 4 * 256 + 4 * 2048
+    cpg = max(1, ncta // 16)
+    need = (256 + 3 * (4 * 2 * 2 * 2048) + 4 * 2 * (64 * 128) + 4 * 32 * cpg * 130 + 4 * 4096
+            + 4 * 2048)
     if need <= q3.STATIC_SCRATCH_BYTES:
         pytest.skip(f"{n_sm} SMs: this shape's scratch fits the static array")
     _, Wd = pu.gpu_weights(shape, gen_device="cuda")
