@@ -38,7 +38,7 @@ class _Cfg(C.Structure):
     _fields_ = [(n, C.c_int) for n in (
         "talker_layers", "talker_hidden", "talker_ffn", "cp_layers", "cp_hidden", "cp_ffn",
         "n_q_heads", "n_kv_heads", "head_dim", "codec_vocab", "cp_vocab", "n_codebooks",
-        "kv_cap", "weight_dtype", "n_streams", "qk_norm")] + [
+        "kv_cap", "weight_dtype", "n_streams", "qk_norm", "kv_bf16")] + [
         ("rms_eps", C.c_double), ("rope_theta", C.c_double)]
 
 
@@ -163,7 +163,11 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
 class Oracle:
     """The oracle model over CPU weight tensors (fp32 or bf16 torch tensors)."""
 
-    def __init__(self, shape, weights: Dict[str, "object"], n_streams: int, kv_cap: int):
+    def __init__(self, shape, weights: Dict[str, "object"], n_streams: int, kv_cap: int,
+                 kv_bf16: bool = False):
+        """kv_bf16: the Talker KV cache holds bf16 values (each cached k, v is
+        rounded to fp32 and then to the nearest bf16), as in the serving
+        configuration whose cache is bf16."""
         L = lib()
         self.shape = shape
         self.n_streams = n_streams
@@ -194,7 +198,7 @@ class Oracle:
         self._c = _Cfg(s.talker_layers, s.talker_hidden, s.talker_ffn, s.cp_layers, s.cp_hidden,
                        s.cp_ffn, s.n_q_heads, s.n_kv_heads, s.head_dim, s.codec_vocab, s.cp_vocab,
                        s.n_codebooks, kv_cap, s.weight_dtype, n_streams, s.qk_norm,
-                       float(s.rms_eps), float(s.rope_theta))
+                       1 if kv_bf16 else 0, float(s.rms_eps), float(s.rope_theta))
         self._h = L.q3o_create(C.byref(self._c), C.byref(self._w))
 
     def __del__(self):

@@ -53,6 +53,7 @@ typedef struct {
   int n_q_heads, n_kv_heads, head_dim;
   int codec_vocab, cp_vocab, n_codebooks;
   int kv_cap, weight_dtype, n_streams, qk_norm;
+  int kv_bf16; /* Talker cache stored in bf16 (the serving configuration) */
   double rms_eps, rope_theta;
 } q3o_config;
 
@@ -82,7 +83,19 @@ typedef struct {
 typedef struct {
   double* k; /* [layers][cap][Hkv][hd] */
   double* v;
+  int bf16; /* entries hold bf16 values */
 } kvbuf;
+
+/* The bf16 value of x as a cache written from fp32 activations holds it: x
+ * rounded to fp32, then to the nearest bf16 (ties to even). */
+static double round_bf16(double x) {
+  float f = (float)x;
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7f800000u) != 0x7f800000u) u = (u + 0x7fffu + ((u >> 16) & 1u)) & 0xffff0000u;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
 
 typedef struct {
   kvbuf talker_kv;
@@ -222,8 +235,12 @@ static void stack_forward(const q3o_model* m, const stack_desc* sd, double* x, i
         double* vg = row + (Hq + Hkv + g) * hd;
         if (c->qk_norm) rmsnorm_w(kg, hd, w[L_GK], dt, c->rms_eps, kg);
         rope(kg, hd, pos, c->rope_theta);
-        memcpy(Kc + ((size_t)pos * Hkv + g) * hd, kg, sizeof(double) * hd);
-        memcpy(Vc + ((size_t)pos * Hkv + g) * hd, vg, sizeof(double) * hd);
+        double* kc = Kc + ((size_t)pos * Hkv + g) * hd;
+        double* vc = Vc + ((size_t)pos * Hkv + g) * hd;
+        for (int i = 0; i < hd; ++i) {
+          kc[i] = sd->kv->bf16 ? round_bf16(kg[i]) : kg[i];
+          vc[i] = sd->kv->bf16 ? round_bf16(vg[i]) : vg[i];
+        }
       }
     }
     /* causal: token t sees positions 0..pos0+t, itself included */
@@ -429,6 +446,7 @@ void* q3o_create(const q3o_config* cfg, const q3o_weights* w) {
   size_t kv = (size_t)c->talker_layers * c->kv_cap * c->n_kv_heads * c->head_dim;
   m->st = (stream_state*)calloc((size_t)c->n_streams, sizeof(stream_state));
   for (int s = 0; s < c->n_streams; ++s) {
+    m->st[s].talker_kv.bf16 = c->kv_bf16;
     m->st[s].talker_kv.k = (double*)calloc(kv, sizeof(double));
     m->st[s].talker_kv.v = (double*)calloc(kv, sizeof(double));
     m->st[s].pending_h = (double*)calloc((size_t)c->talker_hidden, sizeof(double));

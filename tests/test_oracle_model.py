@@ -265,17 +265,20 @@ def _rotate_half(x, pos, theta):
                            b * c[:, None, :] + a * s[:, None, :]], axis=-1)
 
 
-def test_attention_block_with_qk_norm_and_causal_mask(oracle_mod):
+@pytest.mark.parametrize("kv_bf16", [False, True])
+def test_attention_block_with_qk_norm_and_causal_mask(oracle_mod, kv_bf16):
     """One Talker layer with W_down = 0 and non-unit q/k norm gains over a
     3-token prompt, rebuilt from library calls: rms_norm -> per-head rms_norm *
-    gain -> rotation -> causal scaled_dot_product_attention -> W_o."""
+    gain -> rotation -> causal scaled_dot_product_attention -> W_o.  With a bf16
+    cache (the serving configuration) the cached k, v enter the attention as
+    torch's own fp32 -> bf16 round-to-nearest-even conversion of them."""
     s = dataclasses.replace(TINY.shape, talker_layers=1)
     W = _tiny_weights(w_down=("talker",))
     W = {k: v for k, v in W.items() if not k.startswith("talker.1.")}
     gen = torch.Generator().manual_seed(99)
     W["talker.0.g_q_norm"] = 1.0 + 0.5 * torch.randn(s.head_dim, generator=gen)
     W["talker.0.g_k_norm"] = 1.0 + 0.5 * torch.randn(s.head_dim, generator=gen)
-    o = oracle_mod.Oracle(s, W, 1, TINY.kv_cap)
+    o = oracle_mod.Oracle(s, W, 1, TINY.kv_cap, kv_bf16=kv_bf16)
     T, Hq, Hkv, hd = 3, s.n_q_heads, s.n_kv_heads, s.head_dim
     e = synth.make_prompts(s, [T])[0].to(torch.float64)
     x = o.talker_stack(0, e.numpy(), 0)
@@ -288,6 +291,9 @@ def test_attention_block_with_qk_norm_and_causal_mask(oracle_mod):
     k = F.rms_norm(k, (hd,), W["talker.0.g_k_norm"].double(), eps=1e-6)
     q = torch.tensor(_rotate_half(q.numpy(), np.arange(T), s.rope_theta))
     k = torch.tensor(_rotate_half(k.numpy(), np.arange(T), s.rope_theta))
+    if kv_bf16:
+        k = k.float().to(torch.bfloat16).double()
+        v = v.float().to(torch.bfloat16).double()
     att = F.scaled_dot_product_attention(q.permute(1, 0, 2)[None], k.permute(1, 0, 2)[None],
                                          v.permute(1, 0, 2)[None], is_causal=True,
                                          enable_gqa=True)[0].permute(1, 0, 2).reshape(T, Hq * hd)
