@@ -1,0 +1,87 @@
+"""GPU parity of the many-stream configurations at their full model shapes:
+several streams with ragged contexts decode frames together through the
+layered step (tensor-core projections, grouped-query attention over the paged
+cache, per-stream sampling).
+
+Checks, per configuration:
+  * the stream with the shortest context against the oracle under teacher
+    forcing (the serving configuration with the oracle's bf16 cache, as its
+    cache is bf16): logits within 3e-2, argmax agreement >= 99.5%, and the
+    drawn codes equal the float sampling rule applied to the GPU's own logits;
+  * two streams decoded alone (one active stream, the same layered step) give
+    the same codes and, up to float reassociation, the same logits as inside
+    the batch -- a stream's result does not depend on the batch around it.
+"""
+import contextlib
+import os
+
+import numpy as np
+import pytest
+
+from autoregressive_tts_decode_gb300 import synth
+from tests import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 3e-2
+FRAMES = 2
+
+CASES = {
+    # name: (workload, context lengths inside the workload's range, oracle cache in bf16)
+    "serving128": ("serving128", [264, 300, 777, 1100, 1530, 2047], True),
+    "batched16": ("batched16", [40, 87, 150, 248], False),
+}
+
+
+@pytest.fixture(scope="module")
+def q3():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from autoregressive_tts_decode_gb300 import build, q3tts
+    build.build()
+    return q3tts
+
+
+@contextlib.contextmanager
+def _layered_only():
+    old = os.environ.get("Q3TTS_FRAME_KERNEL")
+    os.environ["Q3TTS_FRAME_KERNEL"] = "0"
+    try:
+        yield
+    finally:
+        if old is None:
+            del os.environ["Q3TTS_FRAME_KERNEL"]
+        else:
+            os.environ["Q3TTS_FRAME_KERNEL"] = old
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_many_streams_full_shapes(q3, oracle_mod, case):
+    import torch
+    name, lens, kv_bf16 = CASES[case]
+    wl = synth.WORKLOADS[name]
+    s = wl.shape
+    W, Wd = pu.gpu_weights(s, gen_device="cuda")
+    prompts = synth.make_prompts(s, lens)
+    ids = list(range(len(lens)))
+    u = synth.uniforms(ids, FRAMES)
+    eng = q3.Engine(s, Wd, max_streams=len(lens), kv_cap=wl.kv_cap, page_size=wl.page_size)
+    codes, logits = pu.run_gpu(eng, ids, prompts, wl.sampling, FRAMES, uniforms=u)
+    eng.close()
+    # the same streams alone, on the same layered step
+    for k in (0, len(lens) - 1):
+        with _layered_only():
+            one = q3.Engine(s, Wd, max_streams=1, kv_cap=wl.kv_cap, page_size=wl.page_size)
+        c1, l1 = pu.run_gpu(one, [0], [prompts[k]], wl.sampling, FRAMES, uniforms=u[k:k + 1])
+        one.close()
+        assert np.array_equal(c1[0], codes[k]), (k, c1[0], codes[k])
+        assert float(np.max(np.abs(l1[0] - logits[k]))) < 2e-3
+    del Wd
+    torch.cuda.empty_cache()
+    # the shortest context against the oracle
+    orc = oracle_mod.Oracle(s, W, 1, wl.kv_cap, kv_bf16=kv_bf16)
+    oc, ol = pu.run_oracle(orc, 0, prompts[0].numpy(), wl.sampling, FRAMES, forced=codes[0], uniforms=u[0])
+    err, agree = pu.logits_report(logits[0], ol, s)
+    assert err < TOL_BF16, err
+    assert agree >= 0.995, agree
+    assert pu.sampler_replay(oracle_mod, s, wl.sampling, codes[0], logits[0], codes[0], u[0]) == 0
