@@ -38,6 +38,39 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+# Sources of the persistent frame kernel: a recorded DRAM-traffic figure holds
+# only for the exact sources it was captured from.
+KERNEL_SOURCES = ("autoregressive_tts_decode_gb300/csrc/frame_kernel.cu",
+                  "autoregressive_tts_decode_gb300/csrc/sampler.cuh",
+                  "autoregressive_tts_decode_gb300/csrc/common.cuh",
+                  "autoregressive_tts_decode_gb300/csrc/engine.cuh", "include/q3tts.h")
+
+
+def kernel_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def captured_traffic(workload):
+    """DRAM bytes (read + write) per frame-kernel launch from the ncu capture
+    summarised in profiles/frame_kernel_<workload>.md (its `traffic` marker),
+    or None if that capture was of other kernel sources or is missing."""
+    p = os.path.join(ROOT, "profiles", "frame_kernel_%s.md" % workload.replace(".", "p"))
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        for line in f:
+            if line.startswith("<!-- traffic "):
+                d = json.loads(line[len("<!-- traffic "):].rsplit("-->", 1)[0])
+                if d.get("sources_sha") == kernel_source_sha() and d.get("workload") == workload:
+                    return float(d["dram_bytes_per_launch"])
+    return None
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -345,7 +378,8 @@ def main():
                                     if launches == args.steps else
                                     "frame step (all launches of one frame)"),
                          "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
-                         "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                         "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": captured_traffic(wl.name) if launches == args.steps else None,
                          "algorithmic_bytes_per_step": bytes_per_step,
                          "step_ms_median": statistics.median(step_ms),
                          "step_ms_p90": sorted(step_ms)[int(0.9 * (len(step_ms) - 1))]},
