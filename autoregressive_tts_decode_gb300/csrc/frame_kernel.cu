@@ -280,6 +280,8 @@ struct ConsState {
   int k, in, from_xs, fed0;  // the frame schedule's loop state
 };
 
+constexpr int FK_MAXPAGES = 256;  // Talker pages per stream kept in shared memory
+
 struct FKSmem {
   alignas(128) unsigned char ring[FK_NSTAGE][FK_STAGE];
   // Launch parameters and per-layer pointer tables live in shared memory: a
@@ -304,6 +306,8 @@ struct FKSmem {
   alignas(16) unsigned char fin[2 * FK_DMAX * 4];  // final-norm gains: CodePredictor then Talker
   float uni[Q3TTS_N_CODEBOOKS];
   int forced[Q3TTS_N_CODEBOOKS];
+  int tpage[FK_MAXPAGES];  // the stream's Talker page table (when it has at most FK_MAXPAGES pages)
+  int cpage;               // the stream's CodePredictor page
   alignas(8) uint64_t full[FK_NSTAGE];
   alignas(8) uint64_t empty[FK_NSTAGE];
   alignas(8) uint64_t side_full[2];
@@ -326,6 +330,25 @@ struct Cons {};
 
 __device__ __forceinline__ FKSmem* fk_sm() { return reinterpret_cast<FKSmem*>(fk_smem_raw); }
 __device__ __forceinline__ const FKParams* fk_prm() { return &fk_sm()->prm; }
+
+// Offsets of the stream's K/V rows in the paged caches.  The page ids come
+// from the copies of the stream's page tables staged in shared memory at the
+// start of the frame: read from global memory, they would put a second
+// dependent memory round trip in front of every cache access.
+__device__ __forceinline__ size_t kv_row(const KVDesc& d, int page, int layer, int pos, int kv, int head) {
+  return ((((size_t)layer * d.n_pages + page) * 2 + kv) * d.Hkv + head) * d.page_size * d.hd +
+         (size_t)(pos % d.page_size) * d.hd;
+}
+__device__ __forceinline__ size_t tkv_offset(const FKParams& p, int layer, int pos, int kv, int head) {
+  const KVDesc& d = p.tkv;
+  const int pi = pos / d.page_size;
+  const int page = d.pages_per_stream <= FK_MAXPAGES ? fk_sm()->tpage[pi]
+                                                     : __ldcg(d.page_table + p.sid * d.pages_per_stream + pi);
+  return kv_row(d, page, layer, pos, kv, head);
+}
+__device__ __forceinline__ size_t ckv_offset(const FKParams& p, int layer, int pos, int kv, int head) {
+  return kv_row(p.ckv, fk_sm()->cpage, layer, pos, kv, head);
+}
 __device__ __forceinline__ int ctid() { return (int)threadIdx.x - FK_PRODUCER_THREADS; }
 __device__ __forceinline__ int cwarp() { return ctid() >> 5; }
 __device__ __forceinline__ int clane() { return (int)threadIdx.x & 31; }
@@ -922,6 +945,29 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
   AttnScratch& as = fk_sm()->u.att;
   const float scale = 1.0f / sqrtf((float)hd);
   const int S = pos0 + T;  // positions 0..S-1 exist after this pass
+  // 0) this warp's positions (warp, warp + 8): v of every touched kv group
+  //    and k of the cached positions, loaded first -- none of it depends on
+  //    step 1, so the loads are in flight while it runs
+  float kk[2][2][4], vv[2][2][4];
+#pragma unroll
+  for (int np = 0; np < 2; ++np) {
+    const int sp = cwarp() + FK_CONSUMER_WARPS * np;
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi) {
+      const int g = g_first + gi;
+      if (sp < S && gi < ng) {
+        const bool cur = sp >= pos0;
+        const float* kc = (const float*)p.ckv.pool + ckv_offset(p, layer, cur ? 0 : sp, 0, g);
+        const float* vc = cur ? p.qkv + (size_t)(sp - pos0) * p.qkv_rows + (Hq + Hkv + g) * hd
+                              : (const float*)p.ckv.pool + ckv_offset(p, layer, sp, 1, g);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          kk[np][gi][j] = (j < J && !cur) ? __ldcg(kc + clane() + 32 * j) : 0.f;
+          vv[np][gi][j] = j < J ? __ldcg(vc + clane() + 32 * j) : 0.f;
+        }
+      }
+    }
+  }
   // 1) q of each (head, token) pair, normalised and rotated (warps < npair);
   //    the pass's current-position keys, one (token, kv group) per warp from
   //    warp 4 on, normalised, rotated and kept in shared memory -- the CTA
@@ -944,8 +990,8 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
         if (j < J) dst[clane() + 32 * j] = v[j];
       if (isk && g * rep * nt >= v0 && g * rep * nt < v1) {
         const float* vs = p.qkv + (size_t)t * p.qkv_rows + (Hq + Hkv + g) * hd;
-        float* kc = (float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, pos0 + t, 0, g);
-        float* vc = (float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, pos0 + t, 1, g);
+        float* kc = (float*)p.ckv.pool + ckv_offset(p, layer, pos0 + t, 0, g);
+        float* vc = (float*)p.ckv.pool + ckv_offset(p, layer, pos0 + t, 1, g);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           if (j < J) {
@@ -956,27 +1002,17 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
     }
   }
   consumer_sync();
-  // 2) this warp's positions (warp, warp + 8): k, v of every touched kv group
-  //    (earlier positions from the cache, current ones: k from step 1, v raw)
-  float kk[2][2][4], vv[2][2][4];
+  // 2) the current positions' keys, from step 1
 #pragma unroll
   for (int np = 0; np < 2; ++np) {
     const int sp = cwarp() + FK_CONSUMER_WARPS * np;
 #pragma unroll
     for (int gi = 0; gi < 2; ++gi) {
-      const int g = g_first + gi;
-      if (sp < S && gi < ng) {
-        const bool cur = sp >= pos0;
-        const float* kc = cur ? (const float*)p.ckv.pool
-                              : (const float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 0, g);
-        const float* vc = cur ? p.qkv + (size_t)(sp - pos0) * p.qkv_rows + (Hq + Hkv + g) * hd
-                              : (const float*)p.ckv.pool + kv_offset(p.ckv, layer, p.sid, sp, 1, g);
-        const float* ks = as.kcur[cur ? (sp - pos0) * ng + gi : 0];
+      if (sp < S && gi < ng && sp >= pos0) {
+        const float* ks = as.kcur[(sp - pos0) * ng + gi];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          kk[np][gi][j] = j < J ? (cur ? ks[clane() + 32 * j] : __ldcg(kc + clane() + 32 * j)) : 0.f;
-          vv[np][gi][j] = j < J ? __ldcg(vc + clane() + 32 * j) : 0.f;
-        }
+        for (int j = 0; j < 4; ++j)
+          if (j < J) kk[np][gi][j] = ks[clane() + 32 * j];
       }
     }
   }
@@ -1033,6 +1069,34 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
 // Talker phase B1: attention partials.  Work item = (kv group g, position
 // chunk); the q heads of the group share the K/V reads.  The item holding the
 // current position appends its k, v to the cache.
+// K and v rows of Talker positions sb and sb + 8 of kv group g (cached
+// positions from the cache; the current position: v from the QKV rows and a
+// zero key, which the caller replaces; beyond it: zeros).
+template <class KT>
+__device__ __forceinline__ void talker_kv_rows(const FKParams& p, int layer, int g, int pos, int sb, int J,
+                                               float (&k)[2][4], float (&v)[2][4]) {
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const int sp = sb + b * FK_CONSUMER_WARPS;
+    if (sp < pos) {
+      const KT* kc = (const KT*)p.tkv.pool + tkv_offset(p, layer, sp, 0, g);
+      const KT* vc = (const KT*)p.tkv.pool + tkv_offset(p, layer, sp, 1, g);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        k[b][j] = j < J ? to_f(kc[clane() + 32 * j]) : 0.f;
+        v[b][j] = j < J ? to_f(vc[clane() + 32 * j]) : 0.f;
+      }
+    } else {
+      const float* vs = p.qkv + (p.Hq + p.Hkv + g) * p.hd;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        k[b][j] = 0.f;
+        v[b][j] = (sp == pos && j < J) ? __ldcg(vs + clane() + 32 * j) : 0.f;
+      }
+    }
+  }
+}
+
 template <class WT, class KT>
 __device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
   const FKParams& p = *fk_prm();
@@ -1044,6 +1108,11 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
   const float scale = 1.0f / sqrtf((float)hd);
   if (g < Hkv) {
     const int cs = (S + cpg - 1) / cpg, s0 = ch * cs, s1 = min(S, s0 + cs);
+    constexpr int BATCH = 2;
+    float k[BATCH][4], v[BATCH][4];
+    // the warp's first K/V rows are loaded before step 1 (they do not depend
+    // on it), so the loads are in flight while it runs
+    talker_kv_rows<KT>(p, layer, g, pos, s0 + cwarp(), J, k, v);
     // q of the group's heads (warps < rep); the current key (warp rep, in
     // the item holding the current position), normalised, rotated, kept in
     // shared memory and appended to the cache with its v
@@ -1059,8 +1128,8 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
       for (int j = 0; j < 4; ++j)
         if (j < J) dst[clane() + 32 * j] = v[j];
       if (isk) {
-        KT* kc = (KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, pos, 0, g);
-        KT* vc = (KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, pos, 1, g);
+        KT* kc = (KT*)p.tkv.pool + tkv_offset(p, layer, pos, 0, g);
+        KT* vc = (KT*)p.tkv.pool + tkv_offset(p, layer, pos, 1, g);
         const float* vs = p.qkv + (Hq + Hkv + g) * hd;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -1079,29 +1148,15 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) o[r][j] = 0.f;
     }
-    constexpr int BATCH = 2;
     for (int sb = s0 + cwarp(); sb < s1; sb += BATCH * FK_CONSUMER_WARPS) {
-      float k[BATCH][4], v[BATCH][4];
+      if (sb != s0 + cwarp()) talker_kv_rows<KT>(p, layer, g, pos, sb, J, k, v);
 #pragma unroll
-      for (int b = 0; b < BATCH; ++b) {
-        const int sp = sb + b * FK_CONSUMER_WARPS;
-        if (sp < pos) {
-          const KT* kc = (const KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, sp, 0, g);
-          const KT* vc = (const KT*)p.tkv.pool + kv_offset(p.tkv, layer, p.sid, sp, 1, g);
+      for (int b = 0; b < BATCH; ++b)  // the current key comes from step 1
+        if (sb + b * FK_CONSUMER_WARPS == pos) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            k[b][j] = j < J ? to_f(kc[clane() + 32 * j]) : 0.f;
-            v[b][j] = j < J ? to_f(vc[clane() + 32 * j]) : 0.f;
-          }
-        } else {
-          const float* vs = p.qkv + (Hq + Hkv + g) * hd;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            k[b][j] = (sp == pos && j < J) ? as.kcur[0][clane() + 32 * j] : 0.f;
-            v[b][j] = (sp == pos && j < J) ? __ldcg(vs + clane() + 32 * j) : 0.f;
-          }
+          for (int j = 0; j < 4; ++j)
+            if (j < J) k[b][j] = as.kcur[0][clane() + 32 * j];
         }
-      }
 #pragma unroll
       for (int b = 0; b < BATCH; ++b) {
         const int sp = sb + b * FK_CONSUMER_WARPS;
@@ -1529,6 +1584,14 @@ __device__ void consumer() {
     for (int i = ctid(); i < p.Dt; i += FK_CONSUMERS) fin[p.Dc + i] = ((const WT*)p.t_gfinal)[i];
     if (ccta() == 0 && ctid() == 0 && p.newpage >= 0)
       const_cast<int*>(p.tkv.page_table)[p.sid * p.tkv.pages_per_stream + p.pos / p.tkv.page_size] = p.newpage;
+    // the stream's page tables (the page entered this frame from the launch
+    // parameters: CTA 0's store above need not be visible yet)
+    const int tp = p.tkv.pages_per_stream;
+    if (tp <= FK_MAXPAGES)
+      for (int i = ctid(); i < tp; i += FK_CONSUMERS)
+        sm->tpage[i] = (p.newpage >= 0 && i == p.pos / p.tkv.page_size) ? p.newpage
+                                                                         : p.tkv.page_table[p.sid * tp + i];
+    if (ctid() == 0) sm->cpage = p.ckv.page_table[p.sid * p.ckv.pages_per_stream];
     // rope rows: CodePredictor positions 0..15 and the Talker position
     const int half = p.hd / 2;
     for (int e = ctid(); e < 17 * half; e += FK_CONSUMERS) {

@@ -300,23 +300,36 @@ namespace q3 {
 
 // ---------------------------------------------------------------------------
 // Register-resident variant of the same rule for greedy or 1 <= k <= 64, run
-// by a group of 256 threads (8 warps).  Warp w owns indices [w*V8, (w+1)*V8),
-// 16 per lane, as 64-bit keys (order-preserving value key, inverted index):
-// each warp sorts its 512 keys with a shuffle bitonic network and keeps its
-// top 64; warp 0 sorts the 8 x 64 survivors and draws from the first k.
-// Keys are distinct (they carry the index), so the order is exactly
-// (value desc, index asc).  Same float operations as group_sample.
+// by a group of 256 threads (8 warps).  Thread t keeps logits
+// [t per, (t + 1) per) in registers as 64-bit keys (order-preserving value
+// key, inverted index: distinct, so the order (value desc, index asc) is the
+// plain descending key order).  The k largest keys are found without a
+// serial search in the common case:
+//   1. a lower bound theta on the k-th largest key: every lane's largest key,
+//      sorted per warp; the k-th largest of the warps' 8 largest lane maxima
+//      (a subset of the keys, so at least k keys are >= theta);
+//   2. the keys >= theta are gathered (typically little more than k) and
+//      ranked by counting, which places the k largest in order.
+// If more than FAST_CAP keys pass the bound (many equal logits), the k-th
+// largest key is found by bisection over its 32 value bits instead.  The draw
+// is the float rule of group_sample on the ordered candidates.
 constexpr int FAST_NT = 256;
 constexpr int FAST_VPT = SAMPLER_VMAX / FAST_NT;  // 16 logits per thread at most
+constexpr int FAST_NW = FAST_NT / 32;
+constexpr int FAST_TOP = 8;                        // lane maxima per warp entering theta
+constexpr int FAST_CAP = 256;                      // candidates ranked directly
 
 struct FastSamplerSmem {
-  unsigned long long cand[SAMPLER_KSMALL];
+  unsigned long long cand[FAST_CAP];
+  unsigned long long top[FAST_NW * FAST_TOP];
   unsigned long long sorted[SAMPLER_KSMALL];
   float w[SAMPLER_KSMALL];
-  int wc[2][FAST_NT / 32];
-  int wscan[FAST_NT / 32];
-  unsigned long long wbest[FAST_NT / 32];
-  int n_gt, pick;
+  float run[SAMPLER_KSMALL];
+  int wc[2][FAST_NW];
+  int wscan[FAST_NW];
+  unsigned long long wbest[FAST_NW];
+  unsigned long long theta;
+  int n_cand, n_gt, pick;
 };
 
 __device__ __forceinline__ float key_value(unsigned long long k) {
@@ -338,17 +351,60 @@ __device__ __forceinline__ int group_count(FastSamplerSmem& sm, int v, int slot)
   if (lane == 0) sm.wc[slot][warp] = v;
   G::sync();
   int tot = 0;
-  for (int w = 0; w < FAST_NT / 32; ++w) tot += sm.wc[slot][w];
+  for (int w = 0; w < FAST_NW; ++w) tot += sm.wc[slot][w];
   return tot;
 }
 
-// Compact variant of the same rule for greedy or 1 <= k <= 64, run by a group
-// of 256 threads: thread t keeps logits [16t, 16t + 16) in registers; the k-th
-// largest order-preserving key is found by bisection over its 32 bits (one
-// group count per bit), ties at that key go to the lowest indices (threads own
-// contiguous index ranges, so an exclusive count over threads orders them),
-// the k candidates are placed by rank, and thread 0 draws.  Loops stay rolled
-// to keep the code small.  Same float operations as group_sample.
+// Fallback selection: the k-th largest value key t by bisection over its 32
+// bits (one group count per bit); keys above t and the lowest-index ties at t
+// fill sm.cand[0..k), which are then ranked into sm.sorted.
+template <class G>
+__device__ __forceinline__ void fast_select_bisect(FastSamplerSmem& sm, const uint32_t (&key)[FAST_VPT], int i0, int K) {
+  const int tid = G::tid(), lane = tid & 31, warp = tid >> 5;
+  uint32_t t = 0u;
+  for (int b = 31; b >= 0; --b) {
+    const uint32_t c = t | (1u << b);
+    int cnt = 0;
+#pragma unroll
+    for (int r = 0; r < FAST_VPT; ++r) cnt += key[r] >= c ? 1 : 0;
+    if (group_count<G>(sm, cnt, b & 1) >= K) t = c;
+  }
+  int n_gt = 0, n_eq = 0;
+#pragma unroll
+  for (int r = 0; r < FAST_VPT; ++r) {
+    n_gt += key[r] > t ? 1 : 0;
+    n_eq += (key[r] == t && key[r] != 0u) ? 1 : 0;
+  }
+  // ties before this thread's (lower indices): warp scan + warp totals
+  int incl = n_eq;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) sm.wscan[warp] = incl;
+  if (tid == 0) sm.n_gt = 0;
+  const int above = group_count<G>(sm, n_gt, 1);  // keys above t (fewer than K)
+  int before = incl - n_eq;
+  for (int w = 0; w < warp; ++w) before += sm.wscan[w];
+#pragma unroll
+  for (int r = 0; r < FAST_VPT; ++r) {
+    const unsigned long long k = ((unsigned long long)key[r] << 32) | (0xffffffffu - (uint32_t)(i0 + r));
+    if (key[r] > t) {
+      sm.cand[atomicAdd(&sm.n_gt, 1)] = k;
+    } else if (key[r] == t && key[r] != 0u) {
+      if (above + before < K) sm.cand[above + before] = k;
+      ++before;
+    }
+  }
+  G::sync();
+  if (tid < K) {
+    const unsigned long long my = sm.cand[tid];
+    int rank = 0;
+    for (int j = 0; j < K; ++j) rank += sm.cand[j] > my ? 1 : 0;
+    sm.sorted[rank] = my;
+  }
+}
+
 template <class G>
 __device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits, int V, int do_sample,
                                         int top_k, float top_p, float temperature, float rep,
@@ -386,7 +442,7 @@ __device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits
     if (lane == 0) sm.wbest[warp] = best;
     G::sync();
     unsigned long long b = 0ull;
-    for (int w = 0; w < FAST_NT / 32; ++w) b = sm.wbest[w] > b ? sm.wbest[w] : b;
+    for (int w = 0; w < FAST_NW; ++w) b = sm.wbest[w] > b ? sm.wbest[w] : b;
     G::sync();
     return key_index(b);
   }
@@ -398,77 +454,91 @@ __device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits
     key[r] = (r < per && i < V) ? fkey(__fdiv_rn(v[r], temperature)) : 0u;
   }
   const int K = (top_k <= 0 || top_k >= V) ? V : top_k;  // caller: K <= SAMPLER_KSMALL
-  // bisection: the largest t with count(key >= t) >= K is the K-th largest key
-  uint32_t t = 0u;
-  for (int b = 31; b >= 0; --b) {
-    const uint32_t cand = t | (1u << b);
-    int cnt = 0;
-#pragma unroll
-    for (int r = 0; r < FAST_VPT; ++r) cnt += key[r] >= cand ? 1 : 0;
-    if (group_count<G>(sm, cnt, b & 1) >= K) t = cand;
-  }
-  int n_gt = 0, n_eq = 0;
+  // 1) theta: the lane's largest key, sorted descending across the warp
+  //    (bitonic network); lanes 0..7 post the warp's 8 largest
+  unsigned long long lm = 0ull;
 #pragma unroll
   for (int r = 0; r < FAST_VPT; ++r) {
-    n_gt += key[r] > t ? 1 : 0;
-    n_eq += (key[r] == t && key[r] != 0u) ? 1 : 0;
+    const unsigned long long k = key[r] ? ((unsigned long long)key[r] << 32) | (0xffffffffu - (uint32_t)(i0 + r))
+                                        : 0ull;
+    lm = k > lm ? k : lm;
   }
-  // ties before this thread's (lower indices): warp scan + warp totals
-  int incl = n_eq;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int x = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += x;
-  }
-  if (lane == 31) sm.wscan[warp] = incl;
-  if (tid == 0) sm.n_gt = 0;
-  const int above = group_count<G>(sm, n_gt, 1);  // keys above t (fewer than K)
-  int before = incl - n_eq;
-  for (int w = 0; w < warp; ++w) before += sm.wscan[w];
-  // keys above t take any of the first `above` slots; ties take slot
-  // above + (rank among ties) while that is below K
 #pragma unroll
-  for (int r = 0; r < FAST_VPT; ++r) {
-    const int i = i0 + r;
-    if (key[r] > t) {
-      sm.cand[atomicAdd(&sm.n_gt, 1)] = ((unsigned long long)key[r] << 32) | (0xffffffffu - (uint32_t)i);
-    } else if (key[r] == t && key[r] != 0u) {
-      if (above + before < K)
-        sm.cand[above + before] = ((unsigned long long)key[r] << 32) | (0xffffffffu - (uint32_t)i);
-      ++before;
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, lm, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+      lm = keep_max ? (o > lm ? o : lm) : (o < lm ? o : lm);
+    }
+  }
+  if (lane < FAST_TOP) sm.top[warp * FAST_TOP + lane] = lm;
+  if (tid == 0) {
+    sm.theta = 0ull;  // fewer than K real keys posted: every real key is a candidate
+    sm.n_cand = 0;
+  }
+  G::sync();
+  if (warp == 0) {
+    // the K-th largest posted key (posted real keys are distinct; zeros are padding)
+#pragma unroll
+    for (int h = 0; h < FAST_NW * FAST_TOP / 32; ++h) {
+      const unsigned long long my = sm.top[lane + 32 * h];
+      int rank = 0;
+#pragma unroll 8
+      for (int j = 0; j < FAST_NW * FAST_TOP; ++j) rank += sm.top[j] > my ? 1 : 0;
+      if (my != 0ull && rank == K - 1) sm.theta = my;
     }
   }
   G::sync();
-  if (tid < K) {
+  // 2) gather the keys >= theta
+  const unsigned long long theta = sm.theta;
+#pragma unroll
+  for (int r = 0; r < FAST_VPT; ++r) {
+    const unsigned long long k = ((unsigned long long)key[r] << 32) | (0xffffffffu - (uint32_t)(i0 + r));
+    if (key[r] != 0u && k >= theta) {
+      const int slot = atomicAdd(&sm.n_cand, 1);
+      if (slot < FAST_CAP) sm.cand[slot] = k;
+    }
+  }
+  G::sync();
+  const int C = sm.n_cand;
+  if (C > FAST_CAP) {
+    G::sync();  // every thread has read n_cand before the fallback reuses the buffers
+    fast_select_bisect<G>(sm, key, i0, K);
+  } else if (tid < C) {
     const unsigned long long my = sm.cand[tid];
     int rank = 0;
-    for (int j = 0; j < K; ++j) rank += sm.cand[j] > my ? 1 : 0;
-    sm.sorted[rank] = my;
+    for (int j = 0; j < C; ++j) rank += sm.cand[j] > my ? 1 : 0;
+    if (rank < K) sm.sorted[rank] = my;
   }
   G::sync();
   if (tid < K) sm.w[tid] = exp_cw(__fsub_rn(key_value(sm.sorted[tid]), key_value(sm.sorted[0])));
   G::sync();
-  if (tid == 0) {
-    int kept = K;
-    if (top_p < 1.0f) {
-      float z = 0.0f;
-      for (int i = 0; i < K; ++i) z = __fadd_rn(z, sm.w[i]);
-      const float tp = __fmul_rn(top_p, z);
+  if (warp == 0) {
+    // running sums in order (one thread: the float rule's summation order)
+    if (lane == 0) {
       float run = 0.0f;
       for (int i = 0; i < K; ++i) {
         run = __fadd_rn(run, sm.w[i]);
-        if (run >= tp) { kept = i + 1; break; }
+        sm.run[i] = run;
       }
     }
-    float z = 0.0f;
-    for (int i = 0; i < kept; ++i) z = __fadd_rn(z, sm.w[i]);
-    const float th = __fmul_rn(u, z);
-    float run = 0.0f;
-    int sel = kept - 1;
-    for (int i = 0; i < kept; ++i) {
-      run = __fadd_rn(run, sm.w[i]);
-      if (run > th) { sel = i; break; }
+    __syncwarp();
+    const float r0 = lane < K ? sm.run[lane] : 0.f, r1 = lane + 32 < K ? sm.run[lane + 32] : 0.f;
+    int kept = K;
+    if (top_p < 1.0f) {
+      // the first i with run_i >= top_p * z (z = run_{K-1}) closes the nucleus
+      const float tp = __fmul_rn(top_p, sm.run[K - 1]);
+      const unsigned b0 = __ballot_sync(0xffffffffu, lane < K && r0 >= tp);
+      const unsigned b1 = __ballot_sync(0xffffffffu, lane + 32 < K && r1 >= tp);
+      kept = b0 ? __ffs(b0) : (b1 ? 32 + __ffs(b1) : K);
     }
-    sm.pick = key_index(sm.sorted[sel]);
+    // the first i < kept with run_i > u * run_{kept-1}, else the last kept
+    const float th = __fmul_rn(u, sm.run[kept - 1]);
+    const unsigned c0 = __ballot_sync(0xffffffffu, lane < kept && r0 > th);
+    const unsigned c1 = __ballot_sync(0xffffffffu, lane + 32 < kept && r1 > th);
+    const int selk = c0 ? __ffs(c0) - 1 : (c1 ? 31 + __ffs(c1) : kept - 1);
+    if (lane == 0) sm.pick = key_index(sm.sorted[selk]);
   }
   G::sync();
   const int pick = sm.pick;
