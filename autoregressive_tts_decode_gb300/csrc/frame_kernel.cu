@@ -215,9 +215,13 @@ __device__ __forceinline__ int ld_volatile(const int* p) { return *(const volati
 
 __device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
 
+// Part i of n items cut into `parts` near-equal parts.  32-bit unsigned
+// arithmetic: n * parts stays far below 2^32 for every split made here (rows,
+// FFN units, tiles, vector elements; parts = CTAs <= 256), and a 64-bit
+// division would be a long software routine on the critical path of a phase.
 __device__ __forceinline__ void split(int n, int parts, int i, int& lo, int& hi) {
-  lo = (int)((long long)n * i / parts);
-  hi = (int)((long long)n * (i + 1) / parts);
+  lo = (int)((unsigned)n * (unsigned)i / (unsigned)parts);
+  hi = (int)((unsigned)n * (unsigned)(i + 1) / (unsigned)parts);
 }
 
 __device__ __forceinline__ int rows_per_chunk(int row_bytes) {
@@ -277,7 +281,7 @@ static_assert(FK_PAIRS >= FK_REPMAX, "talker attention keeps one partial per q h
 struct ConsState {
   uint32_t n, phase, layer;
   int aborted;
-  int k, in, from_xs, fed0;  // the frame schedule's loop state
+  int j, k, in, from_xs, fed0;  // the frame schedule's loop state: pass j, its step k
 };
 
 constexpr int FK_MAXPAGES = 256;  // Talker pages per stream kept in shared memory
@@ -335,19 +339,32 @@ __device__ __forceinline__ const FKParams* fk_prm() { return &fk_sm()->prm; }
 // from the copies of the stream's page tables staged in shared memory at the
 // start of the frame: read from global memory, they would put a second
 // dependent memory round trip in front of every cache access.
-__device__ __forceinline__ size_t kv_row(const KVDesc& d, int page, int layer, int pos, int kv, int head) {
-  return ((((size_t)layer * d.n_pages + page) * 2 + kv) * d.Hkv + head) * d.page_size * d.hd +
-         (size_t)(pos % d.page_size) * d.hd;
+__device__ __forceinline__ size_t kv_row(const KVDesc& d, int page, int layer, int slot, int kv, int head) {
+  return ((((size_t)layer * d.n_pages + page) * 2 + kv) * d.Hkv + head) * d.page_size * d.hd + (size_t)slot * d.hd;
+}
+// Page and slot of a position (pages of a power-of-two size by shift and mask).
+__device__ __forceinline__ void page_slot(const KVDesc& d, int pos, int& pi, int& slot) {
+  const int ps = d.page_size;
+  if ((ps & (ps - 1)) == 0) {
+    pi = pos >> (__ffs(ps) - 1);
+    slot = pos & (ps - 1);
+  } else {
+    pi = pos / ps;
+    slot = pos - pi * ps;
+  }
 }
 __device__ __forceinline__ size_t tkv_offset(const FKParams& p, int layer, int pos, int kv, int head) {
   const KVDesc& d = p.tkv;
-  const int pi = pos / d.page_size;
+  int pi, slot;
+  page_slot(d, pos, pi, slot);
   const int page = d.pages_per_stream <= FK_MAXPAGES ? fk_sm()->tpage[pi]
                                                      : __ldcg(d.page_table + p.sid * d.pages_per_stream + pi);
-  return kv_row(d, page, layer, pos, kv, head);
+  return kv_row(d, page, layer, slot, kv, head);
 }
 __device__ __forceinline__ size_t ckv_offset(const FKParams& p, int layer, int pos, int kv, int head) {
-  return kv_row(p.ckv, fk_sm()->cpage, layer, pos, kv, head);
+  int pi, slot;
+  page_slot(p.ckv, pos, pi, slot);
+  return kv_row(p.ckv, fk_sm()->cpage, layer, slot, kv, head);
 }
 __device__ __forceinline__ int ctid() { return (int)threadIdx.x - FK_PRODUCER_THREADS; }
 __device__ __forceinline__ int cwarp() { return ctid() >> 5; }
@@ -624,10 +641,8 @@ __device__ __forceinline__ void stream_rows(Cons c, int r0, int r1, int K, int T
     }
     gang_sync(s);
     if (s.j == 0 && s.lane == 0)
-      for (int i = 0; i < R * T; ++i) {
-        const int row = i / T, t = i - row * T;
-        out[t * ts + base + row] = xb[i] + xb[FK_XCH + i];
-      }
+      for (int row = 0, i = 0; row < R; ++row)
+        for (int t = 0; t < T; ++t, ++i) out[t * ts + base + row] = xb[i] + xb[FK_XCH + i];
     chunk_release(s, n);
   }
   warp_set(cst().aborted, s.aborted ? 1 : 0);
@@ -1391,7 +1406,7 @@ __device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int xa, i
   consumer_sync();
   const int IM = 8 / T, nq = D / 4;
   for (int e = ctid(); e < T * nq; e += FK_CONSUMERS) {
-    const int t = e / nq, col = (e % nq) * 4;
+    const int t = e >= nq ? 1 : 0, col = (e - t * nq) * 4;  // T <= 2
     const int i = col >> 8, ln = (col & 255) >> 3, q = col & 7;
     const float* src = yred + ((t * IM + i) * 8 + q) * 32 + ln;
     atomicAdd(reinterpret_cast<float4*>(xbuf(p, xb, t) + col), make_float4(src[0], src[32], src[64], src[96]));
@@ -1444,22 +1459,24 @@ struct Step {
 
 __device__ __forceinline__ int steps_per_pass(const FKParams& p) { return 2 + (p.has_proj ? 1 : 0) + 3 * p.Lc; }
 
-__device__ __forceinline__ int frame_steps(const FKParams& p) {
-  return (Q3TTS_N_CODEBOOKS - 1) * steps_per_pass(p) + 2 + 4 * p.Lt;
+// Steps of pass j (j < 15: CodePredictor pass j; 15: the Talker step).
+__device__ __forceinline__ int pass_steps(const FKParams& p, int j) {
+  return j < Q3TTS_N_CODEBOOKS - 1 ? steps_per_pass(p) : 2 + 4 * p.Lt;
 }
 
-__device__ __forceinline__ Step decode_step(const FKParams& p, int k) {
+// Step r of pass j.  The schedule position is kept as (pass, step) so that
+// decoding it needs no division by a runtime value.
+__device__ __forceinline__ Step decode_step(const FKParams& p, int j, int r) {
   Step st;
-  const int pp = steps_per_pass(p), ncp = (Q3TTS_N_CODEBOOKS - 1) * pp, hp = p.has_proj ? 1 : 0;
+  st.j = j;
   st.l = 0;
-  if (k < ncp) {
-    st.j = k / pp;
-    const int r = k - st.j * pp;
+  if (j < Q3TTS_N_CODEBOOKS - 1) {
+    const int hp = p.has_proj ? 1 : 0;
     if (r == 0) {
       st.kind = S_DRAW;
     } else if (r <= hp) {
       st.kind = S_PROJ;
-    } else if (r == pp - 1) {
+    } else if (r == steps_per_pass(p) - 1) {
       st.kind = S_CP_HEAD;
     } else {
       const int q = r - 1 - hp, w = q % 3;
@@ -1467,19 +1484,28 @@ __device__ __forceinline__ Step decode_step(const FKParams& p, int k) {
       st.kind = w == 0 ? S_QKV : (w == 1 ? S_CP_ATTN : S_FFN);
     }
   } else {
-    st.j = Q3TTS_N_CODEBOOKS - 1;
-    const int r = k - ncp;
     if (r == 0) {
       st.kind = S_DRAW;
     } else if (r == 1 + 4 * p.Lt) {
       st.kind = S_T_HEAD;
     } else {
-      const int q = r - 1, w = q % 4;
-      st.l = q / 4;
+      const int q = r - 1, w = q & 3;
+      st.l = q >> 2;
       st.kind = w == 0 ? S_QKV : (w == 1 ? S_T_ATTN : (w == 2 ? S_T_OPROJ : S_FFN));
     }
   }
   return st;
+}
+
+// Moves the warp's schedule position to the next step.
+__device__ __forceinline__ void next_step(ConsState& L) {
+  __syncwarp();
+  const int j = L.j, k = L.k + 1;
+  const bool wrap = k >= pass_steps(*fk_prm(), j);
+  __syncwarp();
+  L.k = wrap ? 0 : k;
+  L.j = wrap ? j + 1 : j;
+  __syncwarp();
 }
 
 // DRAW step: draw code j; code 0..14 starts CodePredictor pass j (running
@@ -1602,8 +1628,10 @@ __device__ void consumer() {
   }
   consumer_sync();
   ConsState& L = cst();
-  for (warp_set(L.k, 0); L.k < frame_steps(*fk_prm()); warp_set(L.k, L.k + 1)) {
-    const Step st = decode_step(*fk_prm(), L.k);
+  warp_set(L.j, 0);
+  warp_set(L.k, 0);
+  for (; L.j < Q3TTS_N_CODEBOOKS; next_step(L)) {
+    const Step st = decode_step(*fk_prm(), L.j, L.k);
     const bool cp = st.j < Q3TTS_N_CODEBOOKS - 1;
     const int T = cp && st.j == 0 ? 2 : 1;
     switch (st.kind) {
