@@ -101,7 +101,6 @@ struct FKParams {
   float* qkv;          // [FK_TMAX][qkv_rows]
   float* part;         // [Hq][cpg][hd + 2]
   float* cp_logits;    // [Vc]
-  float* xsum;         // [Dt]
   unsigned* bar;
   unsigned* done;
   int* err;
@@ -121,7 +120,7 @@ struct FKState {
   char* sideC;
   LayerDev* tl;
   LayerDev* cl;
-  float *R, *dA, *dF, *qkv, *part, *cp_logits, *xsum;
+  float *R, *dA, *dF, *qkv, *part, *cp_logits;
   unsigned *bar, *done;
   int* abort_flag;
   int ncta, dmax;
@@ -293,7 +292,9 @@ struct FKSmem {
   // memory round trip, which the short phases cannot afford.
   FKParams prm;
   LayerDev lay[FK_MAXLAYERS];  // Talker layers, then CodePredictor layers
-  union {
+  // Arrays read or written with 16-byte vector accesses are 16-byte aligned
+  // whatever the size of the fields before them.
+  union alignas(16) {
     struct {
       float xs[FK_TMAX * FK_DMAX];      // normed activations of the current GEMV (plane layout)
       float yred[32 * FK_YCOLS];        // FFN output of the CTA, lane-transposed (see phase_ffn)
@@ -301,15 +302,16 @@ struct FKSmem {
     FastSamplerSmem smp;
     AttnScratch att;
   } u;
-  float os[2][FK_TMAX][FK_HDMAX];  // attention outputs of the CTA's (<= 2) heads, plane layout
-  float red[FK_TMAX][FK_CONSUMER_WARPS];
-  float xch[FK_NGANG][2][FK_GANG * FK_XCH];  // a gang's partial sums per warp (double-buffered by chunk)
-  float rope_c[17][FK_HDMAX / 2];  // rows 0..15: CodePredictor positions; 16: the Talker position
-  float rope_s[17][FK_HDMAX / 2];
+  alignas(16) float os[2][FK_TMAX][FK_HDMAX];  // attention outputs of the CTA's (<= 2) heads, plane layout
+  alignas(16) float red[FK_TMAX][FK_CONSUMER_WARPS];
+  alignas(16) float xch[FK_NGANG][2][FK_GANG * FK_XCH];  // a gang's partial sums per warp (double-buffered by chunk)
+  alignas(16) float rope_c[17][FK_HDMAX / 2];  // rows 0..15: CodePredictor positions; 16: the Talker position
+  alignas(16) float rope_s[17][FK_HDMAX / 2];
   alignas(128) unsigned char side[2][FK_SIDE_BYTES];
   alignas(16) unsigned char fin[2 * FK_DMAX * 4];  // final-norm gains: CodePredictor then Talker
   float uni[Q3TTS_N_CODEBOOKS];
   int forced[Q3TTS_N_CODEBOOKS];
+  int fedc[Q3TTS_N_CODEBOOKS];  // the frame's codes fed forward so far
   int tpage[FK_MAXPAGES];  // the stream's Talker page table (when it has at most FK_MAXPAGES pages)
   int cpage;               // the stream's CodePredictor page
   alignas(8) uint64_t full[FK_NSTAGE];
@@ -320,6 +322,9 @@ struct FKSmem {
   ConsState cs[FK_CONSUMER_WARPS];
 };
 static_assert(sizeof(FKSmem) <= 227 * 1024, "persistent kernel shared memory");
+static_assert(offsetof(FKSmem, u) % 16 == 0 && offsetof(FKSmem, os) % 16 == 0 && offsetof(FKSmem, xch) % 16 == 0 &&
+                  offsetof(FKSmem, fin) % 16 == 0 && offsetof(FKSmem, side) % 16 == 0,
+              "vector-accessed shared-memory arrays are 16-byte aligned");
 
 // ---------------------------------------------------------------- context
 
@@ -1416,34 +1421,85 @@ __device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int xa, i
 
 // The CodePredictor input token(s) of pass j into xs (plane layout, D_t wide):
 // pass 0: [h_T, E_t[c0]]; pass j >= 1: E_cp[j-1][c_j].
+// Eight consecutive weights from global memory as floats (16-byte aligned).
+template <class WT>
+__device__ __forceinline__ void ld8(const WT* src, float (&f)[8]);
+template <>
+__device__ __forceinline__ void ld8<bf16>(const bf16* src, float (&f)[8]) {
+  const uint4 u = __ldcg(reinterpret_cast<const uint4*>(src));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    f[2 * k] = __uint_as_float(w[k] << 16);
+    f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+  }
+}
+template <>
+__device__ __forceinline__ void ld8<float>(const float* src, float (&f)[8]) {
+  const float4 a = __ldcg(reinterpret_cast<const float4*>(src)), b = __ldcg(reinterpret_cast<const float4*>(src) + 1);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+// Elements 8 b .. 8 b + 7 of a plane-layout vector of width D (D % 8 == 0).
+__device__ __forceinline__ void put_plane8(float* xs_t, int D, int b, const float (&f)[8]) {
+  *reinterpret_cast<float4*>(xs_t + 4 * b) = make_float4(f[0], f[1], f[2], f[3]);
+  *reinterpret_cast<float4*>(xs_t + (D >> 1) + 4 * b) = make_float4(f[4], f[5], f[6], f[7]);
+}
+
+// Row `code` of embedding table j of the frame: j = 0 the Talker codec table,
+// j >= 1 the CodePredictor table of codebook j (width D_t).
+template <class WT>
+__device__ __forceinline__ const WT* code_row(const FKParams& p, int j, int code) {
+  return j == 0 ? (const WT*)p.e_codec + (size_t)code * p.Dt
+                : (const WT*)p.cp_embeds + ((size_t)(j - 1) * p.Vc + code) * p.Dt;
+}
+
+// The CodePredictor input token(s) of pass j into xs (plane layout, D_t wide):
+// pass 0: [h_T, E_t[c0]]; pass j >= 1: E_cp[j-1][c_j].
 template <class WT>
 __device__ __forceinline__ void cp_tokens(Cons c, int j, int fed) {
   const FKParams& p = *fk_prm();
   const int Dt = p.Dt;
   float* xs = fk_sm()->u.g.xs;
-  if (j == 0) {
-    const WT* e = (const WT*)p.e_codec + (size_t)fed * Dt;
-    for (int i = ctid(); i < Dt; i += FK_CONSUMERS) {
-      put_plane(xs, Dt, i, __ldcg(p.pending_h + (size_t)p.sid * Dt + i));
-      put_plane(xs + Dt, Dt, i, to_f(e[i]));
+  const WT* e = code_row<WT>(p, j, fed);
+  for (int b = ctid(); b < (Dt >> 3); b += FK_CONSUMERS) {
+    float f[8];
+    ld8<WT>(e + 8 * b, f);
+    put_plane8(j == 0 ? xs + Dt : xs, Dt, b, f);
+    if (j == 0) {
+      ld8<float>(p.pending_h + (size_t)p.sid * Dt + 8 * b, f);
+      put_plane8(xs, Dt, b, f);
     }
-  } else {
-    const WT* e = (const WT*)p.cp_embeds + ((size_t)(j - 1) * p.Vc + fed) * Dt;
-    for (int i = ctid(); i < Dt; i += FK_CONSUMERS) put_plane(xs, Dt, i, to_f(e[i]));
   }
   consumer_sync();
 }
 
-// The CTA's slice of the running embedding sum of the frame's codes.
+// The Talker input of the next position: the fp32 sum of the frame's 16 code
+// embeddings, E_t[c0] + E_cp[0][c1] + ... + E_cp[14][c15], added in that
+// order, into xs (plane layout).  Every CTA forms the whole vector from the
+// codes it drew (the row reads are independent of one another).  Rows are
+// read 8 weights at a time: the kernel is only set up for D_t % 8 == 0 and
+// 16-byte aligned embedding tables.
 template <class WT>
-__device__ __forceinline__ void xsum_add(Cons c, int j, int fed) {
+__device__ __forceinline__ void talker_input(Cons c, int fed15) {
   const FKParams& p = *fk_prm();
-  int lo, hi;
-  split(p.Dt, p.ncta, ccta(), lo, hi);
-  const WT* e = j == 0 ? (const WT*)p.e_codec + (size_t)fed * p.Dt
-                       : (const WT*)p.cp_embeds + ((size_t)(j - 1) * p.Vc + fed) * p.Dt;
-  for (int i = lo + ctid(); i < hi; i += FK_CONSUMERS)
-    p.xsum[i] = j == 0 ? to_f(e[i]) : p.xsum[i] + to_f(e[i]);
+  const int Dt = p.Dt;
+  float* xs = fk_sm()->u.g.xs;
+  const int* fedc = fk_sm()->fedc;
+  for (int b = ctid(); b < (Dt >> 3); b += FK_CONSUMERS) {
+    float s[8];
+    ld8<WT>(code_row<WT>(p, 0, fedc[0]) + 8 * b, s);
+#pragma unroll 5
+    for (int j = 1; j < Q3TTS_N_CODEBOOKS; ++j) {
+      float f[8];
+      ld8<WT>(code_row<WT>(p, j, j < Q3TTS_N_CODEBOOKS - 1 ? fedc[j] : fed15) + 8 * b, f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s[k] += f[k];
+    }
+    put_plane8(xs, Dt, b, s);
+  }
+  consumer_sync();
 }
 
 // The frame's schedule as a sequence of steps.  Per CodePredictor pass j
@@ -1516,16 +1572,11 @@ __device__ __forceinline__ void draw_step(Cons c, int j) {
   ConsState& L = cst();
   const int fed = draw_code(c, j);
   if (j == 0) warp_set(L.fed0, fed);
-  if (j < Q3TTS_N_CODEBOOKS - 1) {
-    xsum_add<WT>(c, j, fed);
+  if (ctid() == 0) fk_sm()->fedc[j] = fed;  // read in later steps, after barriers
+  if (j < Q3TTS_N_CODEBOOKS - 1)
     cp_tokens<WT>(c, j, fed);
-  } else {
-    const FKParams& q = *fk_prm();
-    const WT* e = (const WT*)q.cp_embeds + ((size_t)(Q3TTS_N_CODEBOOKS - 2) * q.Vc + fed) * q.Dt;
-    float* xs = fk_sm()->u.g.xs;
-    for (int i = ctid(); i < q.Dt; i += FK_CONSUMERS) put_plane(xs, q.Dt, i, __ldcg(q.xsum + i) + to_f(e[i]));
-    consumer_sync();
-  }
+  else
+    talker_input<WT>(c, fed);
   warp_set(L.in, 0);
   warp_set(L.from_xs, 1);
 }
@@ -1886,14 +1937,13 @@ static size_t fk_layout(const q3tts_config& c, int ncta, FKState* st, char* base
   char* qkv = take(sizeof(float) * FK_TMAX * qkv_rows);
   char* part = take(sizeof(float) * (size_t)Hq * cpg * (hd + 2));
   char* lg = take(sizeof(float) * c.cp_vocab);
-  char* xsum = take(sizeof(float) * c.talker_hidden);
   char* sync = take(sizeof(unsigned) * 4);
   if (st) {
     st->base = base;
     st->tl = (LayerDev*)tl;
     st->cl = (LayerDev*)cl;
     st->R = (float*)R; st->dA = (float*)dA; st->dF = (float*)dF;
-    st->qkv = (float*)qkv; st->part = (float*)part; st->cp_logits = (float*)lg; st->xsum = (float*)xsum;
+    st->qkv = (float*)qkv; st->part = (float*)part; st->cp_logits = (float*)lg;
     st->bar = (unsigned*)sync;
     st->done = st->bar + 1;
     st->abort_flag = (int*)(st->bar + 2);
@@ -1927,7 +1977,8 @@ int frame_kernel_create(q3tts_handle* h) {
   if (c.talker_hidden > FK_DMAX || c.cp_hidden > FK_DMAX || c.head_dim > FK_HDMAX ||
       c.talker_layers + c.cp_layers > FK_MAXLAYERS ||
       c.n_q_heads / c.n_kv_heads > FK_REPMAX || c.codec_vocab > SAMPLER_VMAX ||
-      c.cp_vocab > SAMPLER_VMAX || (c.talker_hidden % 4) || (c.cp_hidden % 4))
+      c.cp_vocab > SAMPLER_VMAX || (c.talker_hidden % 8) || (c.cp_hidden % 4) ||
+      ((uintptr_t)h->w.talker_e_codec & 15) || ((uintptr_t)h->w.cp_embeds & 15))
     return Q3TTS_OK;
   const int ncta = std::min(h->n_sm, FK_MAXCTA);
   // every CTA's o_proj tile range must touch at most two heads (32-column
@@ -2050,7 +2101,7 @@ static void frame_params(FKParams& p, const q3tts_handle* h, int sid, int pos, i
   p.pending_h = h->pending_h; p.pending_logits = h->pending_logits; p.history = h->history;
   p.tkv = talker_kv(h); p.ckv = cp_kv(h); p.rope_cos = h->rope_cos; p.rope_sin = h->rope_sin;
   p.R = st->R; p.dA = st->dA; p.dF = st->dF; p.qkv = st->qkv; p.part = st->part;
-  p.cp_logits = st->cp_logits; p.xsum = st->xsum;
+  p.cp_logits = st->cp_logits;
   p.bar = st->bar; p.done = st->done; p.err = h->d_err; p.abort_flag = st->abort_flag;
   p.sid = sid; p.pos = pos; p.newpage = newpage; p.sp = sp;
   p.uniforms = uniforms; p.codes = codes; p.forced = forced; p.dump = logits;
@@ -2082,8 +2133,8 @@ int frame_kernel_recover(q3tts_handle* h) {
 // ------------------------------------------- frame step with static scratch
 //
 // q3tts_step_frame_static runs the same kernel with its per-frame scratch (the
-// three residual vectors, QKV rows, attention partials, CodePredictor logits,
-// the running embedding sum and the grid-barrier words) in this file-scope
+// three residual vectors, QKV rows, attention partials, CodePredictor logits
+// and the grid-barrier words) in this file-scope
 // device array instead of the caller's workspace, so a frame needs no memory
 // from the caller beyond what q3tts_create was given, and the call itself
 // makes no device or host allocation.  Layout: the barrier words (bar, done,
@@ -2115,10 +2166,9 @@ static size_t fk_static_layout(const q3tts_config& c, int ncta, char* base, FKPa
   float* qkv = take(sizeof(float) * FK_TMAX * qkv_rows);
   float* part = take(sizeof(float) * (size_t)c.n_q_heads * cpg * (c.head_dim + 2));
   float* lg = take(sizeof(float) * c.cp_vocab);
-  float* xsum = take(sizeof(float) * c.talker_hidden);
   if (p) {
     p->R = R; p->dA = dA; p->dF = dF; p->qkv = qkv; p->part = part;
-    p->cp_logits = lg; p->xsum = xsum;
+    p->cp_logits = lg;
     p->bar = (unsigned*)base;
     p->done = p->bar + 1;
     p->abort_flag = (int*)(p->bar + 2);

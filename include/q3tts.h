@@ -169,7 +169,7 @@ int q3tts_step_frame(q3tts_handle* h, const q3tts_sampling* params, const int32_
 
 /* One frame of one stream, like q3tts_step_frame with n_active = 1, but with
  * the frame's scratch (residual vectors, QKV rows, attention partials,
- * CodePredictor logits, embedding sum, grid-barrier words) in a static device
+ * CodePredictor logits, grid-barrier words) in a static device
  * array of Q3TTS_STATIC_SCRATCH_BYTES bytes compiled into the library instead
  * of the handle's workspace.  The method's description has no counterpart to
  * this call.  It exists for callers that must not allocate while decoding: a

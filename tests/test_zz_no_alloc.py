@@ -133,8 +133,7 @@ def test_static_scratch_too_small_is_rejected(q3):
                                 cp_vocab=4096, weight_dtype=synth.DTYPE_BF16)
     ncta = min(n_sm, 256)
     cpg = max(1, ncta // 16)
-    need = (256 + 3 * (4 * 2 * 2 * 2048) + 4 * 2 * (64 * 128) + 4 * 32 * cpg * 130 + 4 * 4096
-            + 4 * 2048)
+    need = 256 + 3 * (4 * 2 * 2 * 2048) + 4 * 2 * (64 * 128) + 4 * 32 * cpg * 130 + 4 * 4096
     if need <= q3.STATIC_SCRATCH_BYTES:
         pytest.skip(f"{n_sm} SMs: this shape's scratch fits the static array")
     _, Wd = pu.gpu_weights(shape, gen_device="cuda")
