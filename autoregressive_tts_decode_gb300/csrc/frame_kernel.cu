@@ -500,28 +500,34 @@ __device__ __forceinline__ float* xch_buf(const Stream& s, uint32_t n) {
   return fk_sm()->xch[s.gang][(n / FK_NGANG) & 1];
 }
 
+// The slow path of chunk_wait (out of line: it keeps the streaming loops'
+// code short): waits for the mbarrier phase at shared offset bar with a bound;
+// returns whether the warp gave up (timeout or abort flag), after recording
+// the timeout.
+__device__ __noinline__ bool chunk_wait_slow(uint32_t bar, unsigned par) {
+  const long long t0 = clock64();
+  unsigned it = 0;
+  bool ab = false;
+  uint64_t* b = reinterpret_cast<uint64_t*>(fk_smem_raw + bar);
+  while (!mbar_try_wait(b, par)) {
+    if ((++it & 255u) == 0 && (ld_volatile(fk_prm()->abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
+      ab = true;
+      break;
+    }
+  }
+  ab = __any_sync(0xffffffffu, ab);  // one decision per warp
+  if (ab && clane() == 0) raise_abort(*fk_prm(), Q3TTS_ERR_TIMEOUT);
+  return ab;
+}
+
 // Waits (bounded) for ring chunk n; returns its shared-memory offset.
 __device__ __forceinline__ uint32_t chunk_wait(Stream& s, uint32_t n) {
   FKSmem* sm = fk_sm();
   const uint32_t slot = n % FK_NSTAGE;
   if (!s.aborted) {
     const unsigned par = (n / FK_NSTAGE) & 1u;
-    if (!__all_sync(0xffffffffu, mbar_try_wait(&sm->full[slot], par))) {
-      const long long t0 = clock64();
-      unsigned it = 0;
-      bool ab = false;
-      while (!mbar_try_wait(&sm->full[slot], par)) {
-        if ((++it & 255u) == 0 && (ld_volatile(s.abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
-          ab = true;
-          break;
-        }
-      }
-      s.aborted = __any_sync(0xffffffffu, ab);  // one decision per warp
-      if (s.aborted && s.lane == 0) {
-        atomicCAS(s.err, 0, Q3TTS_ERR_TIMEOUT);
-        atomicExch(const_cast<int*>(s.abort_flag), 1);
-      }
-    }
+    if (!__all_sync(0xffffffffu, mbar_try_wait(&sm->full[slot], par)))
+      s.aborted = chunk_wait_slow(soff(&sm->full[slot]), par);
   }
   return soff(sm->ring[slot]);
 }

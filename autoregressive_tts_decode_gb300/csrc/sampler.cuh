@@ -299,20 +299,7 @@ __device__ inline int block_sample(SamplerSmem& sm, int V, int do_sample, int to
 namespace q3 {
 
 // ---------------------------------------------------------------------------
-// Register-resident variant of the same rule for greedy or 1 <= k <= 64, run
-// by a group of 256 threads (8 warps).  Thread t keeps logits
-// [t per, (t + 1) per) in registers as 64-bit keys (order-preserving value
-// key, inverted index: distinct, so the order (value desc, index asc) is the
-// plain descending key order).  The k largest keys are found without a
-// serial search in the common case:
-//   1. a lower bound theta on the k-th largest key: every lane's largest key,
-//      sorted per warp; the k-th largest of the warps' 8 largest lane maxima
-//      (a subset of the keys, so at least k keys are >= theta);
-//   2. the keys >= theta are gathered (typically little more than k) and
-//      ranked by counting, which places the k largest in order.
-// If more than FAST_CAP keys pass the bound (many equal logits), the k-th
-// largest key is found by bisection over its 32 value bits instead.  The draw
-// is the float rule of group_sample on the ordered candidates.
+// Register-resident sampler of the frame kernel (fast_sample, at the end).
 constexpr int FAST_NT = 256;
 constexpr int FAST_VPT = SAMPLER_VMAX / FAST_NT;  // 16 logits per thread at most
 constexpr int FAST_NW = FAST_NT / 32;
@@ -325,6 +312,7 @@ struct FastSamplerSmem {
   unsigned long long sorted[SAMPLER_KSMALL];
   float w[SAMPLER_KSMALL];
   float run[SAMPLER_KSMALL];
+  uint32_t keys[SAMPLER_VMAX];  // the fallback selection's copy of the value keys
   int wc[2][FAST_NW];
   int wscan[FAST_NW];
   unsigned long long wbest[FAST_NW];
@@ -355,25 +343,73 @@ __device__ __forceinline__ int group_count(FastSamplerSmem& sm, int v, int slot)
   return tot;
 }
 
-// Fallback selection: the k-th largest value key t by bisection over its 32
-// bits (one group count per bit); keys above t and the lowest-index ties at t
-// fill sm.cand[0..k), which are then ranked into sm.sorted.
-template <class G>
-__device__ __forceinline__ void fast_select_bisect(FastSamplerSmem& sm, const uint32_t (&key)[FAST_VPT], int i0, int K) {
+// The logits of thread t, [t per, (t + 1) per), with the repetition penalty
+// applied (history != nullptr and rep != 1); entries past V are 0.
+template <int VPT>
+__device__ __forceinline__ void fast_load(float (&v)[VPT], const float* logits, int V, int i0, int per,
+                                          float rep, const uint8_t* history) {
+#pragma unroll
+  for (int r = 0; r < VPT; ++r) {
+    const int i = i0 + r;
+    v[r] = (r < per && i < V) ? __ldcg(logits + i) : 0.f;
+  }
+  if (history != nullptr && rep != 1.0f) {
+#pragma unroll
+    for (int r = 0; r < VPT; ++r) {
+      const int i = i0 + r;
+      if (r < per && i < V && history[i]) v[r] = v[r] > 0.0f ? __fdiv_rn(v[r], rep) : __fmul_rn(v[r], rep);
+    }
+  }
+}
+
+// Greedy: the argmax (lowest index on ties) of the penalised logits.
+template <class G, int VPT>
+__device__ __noinline__ int fast_argmax(FastSamplerSmem& sm, const float* logits, int V, float rep,
+                                        const uint8_t* history) {
   const int tid = G::tid(), lane = tid & 31, warp = tid >> 5;
+  const int per = (V + FAST_NT - 1) / FAST_NT, i0 = tid * per;
+  float v[VPT];
+  fast_load<VPT>(v, logits, V, i0, per, rep, history);
+  unsigned long long best = 0ull;
+#pragma unroll
+  for (int r = 0; r < VPT; ++r) {
+    const int i = i0 + r;
+    if (r < per && i < V) {
+      const unsigned long long k = skey(v[r], i);
+      best = k > best ? k : best;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long t = __shfl_xor_sync(0xffffffffu, best, o);
+    best = t > best ? t : best;
+  }
+  if (lane == 0) sm.wbest[warp] = best;
+  G::sync();
+  unsigned long long b = 0ull;
+  for (int w = 0; w < FAST_NW; ++w) b = sm.wbest[w] > b ? sm.wbest[w] : b;
+  G::sync();
+  return key_index(b);
+}
+
+// Fallback selection from the value keys in sm.keys[0..V): the K-th largest
+// key t by bisection over its 32 bits (one group count per bit); keys above t
+// and the lowest-index ties at t fill sm.cand[0..K), which are then ranked
+// into sm.sorted.  Loops stay rolled: this path is rare and kept small.
+template <class G>
+__device__ __noinline__ void fast_select_bisect(FastSamplerSmem& sm, int V, int K) {
+  const int tid = G::tid(), lane = tid & 31, warp = tid >> 5;
+  const int per = (V + FAST_NT - 1) / FAST_NT, i0 = tid * per, i1 = min(V, i0 + per);
   uint32_t t = 0u;
   for (int b = 31; b >= 0; --b) {
     const uint32_t c = t | (1u << b);
     int cnt = 0;
-#pragma unroll
-    for (int r = 0; r < FAST_VPT; ++r) cnt += key[r] >= c ? 1 : 0;
+    for (int i = i0; i < i1; ++i) cnt += sm.keys[i] >= c ? 1 : 0;
     if (group_count<G>(sm, cnt, b & 1) >= K) t = c;
   }
   int n_gt = 0, n_eq = 0;
-#pragma unroll
-  for (int r = 0; r < FAST_VPT; ++r) {
-    n_gt += key[r] > t ? 1 : 0;
-    n_eq += (key[r] == t && key[r] != 0u) ? 1 : 0;
+  for (int i = i0; i < i1; ++i) {
+    n_gt += sm.keys[i] > t ? 1 : 0;
+    n_eq += sm.keys[i] == t ? 1 : 0;
   }
   // ties before this thread's (lower indices): warp scan + warp totals
   int incl = n_eq;
@@ -386,12 +422,12 @@ __device__ __forceinline__ void fast_select_bisect(FastSamplerSmem& sm, const ui
   const int above = group_count<G>(sm, n_gt, 1);  // keys above t (fewer than K)
   int before = incl - n_eq;
   for (int w = 0; w < warp; ++w) before += sm.wscan[w];
-#pragma unroll
-  for (int r = 0; r < FAST_VPT; ++r) {
-    const unsigned long long k = ((unsigned long long)key[r] << 32) | (0xffffffffu - (uint32_t)(i0 + r));
-    if (key[r] > t) {
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = sm.keys[i];
+    const unsigned long long k = ((unsigned long long)key << 32) | (0xffffffffu - (uint32_t)i);
+    if (key > t) {
       sm.cand[atomicAdd(&sm.n_gt, 1)] = k;
-    } else if (key[r] == t && key[r] != 0u) {
+    } else if (key == t) {
       if (above + before < K) sm.cand[above + before] = k;
       ++before;
     }
@@ -405,50 +441,27 @@ __device__ __forceinline__ void fast_select_bisect(FastSamplerSmem& sm, const ui
   }
 }
 
-template <class G>
-__device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits, int V, int do_sample,
-                                        int top_k, float top_p, float temperature, float rep,
-                                        const uint8_t* history, float u) {
+// Sampling with top-k (1 <= k <= 64), thread t holding logits
+// [t per, (t + 1) per) in registers (per <= VPT) as 64-bit keys.  The k
+// largest keys are found without a serial search in the common case:
+//   1. a lower bound theta on the k-th largest key: every lane's largest key,
+//      sorted per warp; the k-th largest of the warps' 8 largest lane maxima
+//      (a subset of the keys, so at least k keys are >= theta);
+//   2. the keys >= theta are gathered (typically little more than k) and
+//      ranked by counting, which places the k largest in order.
+// If more than FAST_CAP keys pass the bound (many equal logits), the k-th
+// largest key is found by bisection instead (fast_select_bisect).  The draw is
+// the float rule of group_sample on the ordered candidates.
+template <class G, int VPT>
+__device__ __noinline__ int fast_topk(FastSamplerSmem& sm, const float* logits, int V, int top_k, float top_p,
+                                      float temperature, float rep, const uint8_t* history, float u) {
   const int tid = G::tid(), lane = tid & 31, warp = tid >> 5;
-  const int per = (V + FAST_NT - 1) / FAST_NT;
-  const int i0 = tid * per;
-  float v[FAST_VPT];
+  const int per = (V + FAST_NT - 1) / FAST_NT, i0 = tid * per;
+  float v[VPT];
+  fast_load<VPT>(v, logits, V, i0, per, rep, history);
+  uint32_t key[VPT];
 #pragma unroll
-  for (int r = 0; r < FAST_VPT; ++r) {
-    const int i = i0 + r;
-    v[r] = (r < per && i < V) ? __ldcg(logits + i) : 0.f;
-  }
-  if (history != nullptr && rep != 1.0f) {
-#pragma unroll
-    for (int r = 0; r < FAST_VPT; ++r) {
-      const int i = i0 + r;
-      if (r < per && i < V && history[i]) v[r] = v[r] > 0.0f ? __fdiv_rn(v[r], rep) : __fmul_rn(v[r], rep);
-    }
-  }
-  if (!do_sample) {
-    unsigned long long best = 0ull;
-#pragma unroll
-    for (int r = 0; r < FAST_VPT; ++r) {
-      const int i = i0 + r;
-      if (r < per && i < V) {
-        const unsigned long long k = skey(v[r], i);
-        best = k > best ? k : best;
-      }
-    }
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long t = __shfl_xor_sync(0xffffffffu, best, o);
-      best = t > best ? t : best;
-    }
-    if (lane == 0) sm.wbest[warp] = best;
-    G::sync();
-    unsigned long long b = 0ull;
-    for (int w = 0; w < FAST_NW; ++w) b = sm.wbest[w] > b ? sm.wbest[w] : b;
-    G::sync();
-    return key_index(b);
-  }
-  uint32_t key[FAST_VPT];
-#pragma unroll
-  for (int r = 0; r < FAST_VPT; ++r) {
+  for (int r = 0; r < VPT; ++r) {
     const int i = i0 + r;
     // 0 is below the key of every float, so padding never counts
     key[r] = (r < per && i < V) ? fkey(__fdiv_rn(v[r], temperature)) : 0u;
@@ -458,7 +471,7 @@ __device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits
   //    (bitonic network); lanes 0..7 post the warp's 8 largest
   unsigned long long lm = 0ull;
 #pragma unroll
-  for (int r = 0; r < FAST_VPT; ++r) {
+  for (int r = 0; r < VPT; ++r) {
     const unsigned long long k = key[r] ? ((unsigned long long)key[r] << 32) | (0xffffffffu - (uint32_t)(i0 + r))
                                         : 0ull;
     lm = k > lm ? k : lm;
@@ -493,7 +506,7 @@ __device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits
   // 2) gather the keys >= theta
   const unsigned long long theta = sm.theta;
 #pragma unroll
-  for (int r = 0; r < FAST_VPT; ++r) {
+  for (int r = 0; r < VPT; ++r) {
     const unsigned long long k = ((unsigned long long)key[r] << 32) | (0xffffffffu - (uint32_t)(i0 + r));
     if (key[r] != 0u && k >= theta) {
       const int slot = atomicAdd(&sm.n_cand, 1);
@@ -503,8 +516,11 @@ __device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits
   G::sync();
   const int C = sm.n_cand;
   if (C > FAST_CAP) {
-    G::sync();  // every thread has read n_cand before the fallback reuses the buffers
-    fast_select_bisect<G>(sm, key, i0, K);
+#pragma unroll
+    for (int r = 0; r < VPT; ++r)
+      if (r < per && i0 + r < V) sm.keys[i0 + r] = key[r];
+    G::sync();  // every thread has read n_cand and posted its keys
+    fast_select_bisect<G>(sm, V, K);
   } else if (tid < C) {
     const unsigned long long my = sm.cand[tid];
     int rank = 0;
@@ -544,6 +560,21 @@ __device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits
   const int pick = sm.pick;
   G::sync();
   return pick;
+}
+
+// Register-resident variant of the same rule for greedy or 1 <= k <= 64, run
+// by a group of 256 threads (8 warps) on at most SAMPLER_VMAX logits.  Each
+// case is its own function, specialised on the logits per thread (8 covers
+// V <= 2048), so a draw runs through compact code.
+template <class G>
+__device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits, int V, int do_sample,
+                                        int top_k, float top_p, float temperature, float rep,
+                                        const uint8_t* history, float u) {
+  const bool small = V <= 8 * FAST_NT;
+  if (!do_sample)
+    return small ? fast_argmax<G, 8>(sm, logits, V, rep, history) : fast_argmax<G, FAST_VPT>(sm, logits, V, rep, history);
+  return small ? fast_topk<G, 8>(sm, logits, V, top_k, top_p, temperature, rep, history, u)
+               : fast_topk<G, FAST_VPT>(sm, logits, V, top_k, top_p, temperature, rep, history, u);
 }
 
 }  // namespace q3
