@@ -117,6 +117,10 @@ size_t carve(const q3tts_config& c, void* base, q3tts_handle* h) {
   float* cpx = cv.take<float>((size_t)2 * d.S * d.Dc);
   float* logits = cv.take<float>((size_t)d.S * V);
   int* err = cv.take<int>(64);
+  q3::StepDesc* desc = cv.take<q3::StepDesc>(1);
+  float* g_uni = cv.take<float>((size_t)d.S * Q3TTS_N_CODEBOOKS);
+  int32_t* g_forced = cv.take<int32_t>((size_t)d.S * Q3TTS_N_CODEBOOKS);
+  int32_t* g_codes = cv.take<int32_t>((size_t)d.S * Q3TTS_N_CODEBOOKS);
   if (h) {
     h->rope_cos = rope_cos; h->rope_sin = rope_sin; h->kv_pool = kv_pool;
     h->page_table = page_table; h->cp_kv = cpkv; h->cp_page_table = cp_pt;
@@ -125,6 +129,7 @@ size_t carve(const q3tts_config& c, void* base, q3tts_handle* h) {
     h->d_tok_stream = tok_s; h->d_tok_pos = tok_p;
     h->x = x; h->hb = hb; h->qkv = qkv; h->att = att; h->gu = gu; h->act = act;
     h->uin = uin; h->cpx = cpx; h->logits = logits; h->d_err = err;
+    h->d_desc = desc; h->g_uni = g_uni; h->g_forced = g_forced; h->g_codes = g_codes;
   }
   cv.off = (cv.off + 255) & ~(size_t)255;
   return cv.off;
@@ -200,6 +205,8 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
   carve(c, workspace, h);
   const char* env = getenv("Q3TTS_FRAME_KERNEL");
   h->frame_kernel_off = env && env[0] == '0';
+  const char* genv = getenv("Q3TTS_GRAPH");
+  h->graph_off = genv && genv[0] == '0';
 
   // RoPE tables: angle pos * theta^(-2i/hd), computed in double, stored as float.
   const int half = d.hd / 2;
@@ -395,6 +402,7 @@ uint64_t q3tts_kernel_launches(const q3tts_handle* h) { return h ? h->launches :
 void q3tts_destroy(q3tts_handle* h) {
   if (!h) return;
   q3::frame_kernel_destroy(h);
+  q3::step_graph_destroy(h);
   delete h;
 }
 

@@ -52,6 +52,12 @@ struct q3tts_handle {
   int* d_tok_pos;         // [m_max]
   float *x, *hb, *qkv, *att, *gu, *act, *uin, *cpx, *logits;
   int* d_err;
+  // layered step replayed as a CUDA graph: the step's descriptor and its
+  // per-call inputs/outputs pass through these fixed device buffers
+  q3::StepDesc* d_desc;
+  float* g_uni;      // [max_streams][16]
+  int32_t* g_forced;  // [max_streams][16]
+  int32_t* g_codes;   // [max_streams][16]
 
   // host-side stream bookkeeping
   std::vector<int> len;  // Talker positions held; -1 = no prompt yet
@@ -64,6 +70,14 @@ struct q3tts_handle {
   bool used_static = false;   // q3tts_step_frame_static has run on this handle
   bool static_ready = false;  // per-stream page lists reserved for it
   uint64_t launches = 0;
+  // the captured layered step (valid for g_n active streams, with or without
+  // forced codes); g_launches kernels per replay
+  cudaGraphExec_t gexec = nullptr;
+  int g_n = 0;
+  bool g_forced_on = false;
+  uint64_t g_launches = 0;
+  cudaStream_t cap_stream = nullptr;  // stream the step is captured on
+  bool graph_off = false;             // Q3TTS_GRAPH=0: launch the layered step kernel by kernel
 };
 
 namespace q3 {
@@ -72,6 +86,7 @@ namespace q3 {
 int step_layered(q3tts_handle* h, const StepDesc& d, const float* uniforms, int32_t* codes,
                  const int32_t* forced, float* logits);
 int prefill_layered(q3tts_handle* h, int sid, const float* embeds, int len);
+void step_graph_destroy(q3tts_handle* h);
 
 KVDesc talker_kv(const q3tts_handle* h);
 KVDesc cp_kv(const q3tts_handle* h);

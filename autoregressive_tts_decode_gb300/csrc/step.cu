@@ -40,8 +40,9 @@ KVDesc cp_kv(const q3tts_handle* h) {
 
 // ----------------------------------------------------------- small kernels
 
-__global__ void setup_kernel(StepDesc d, int* sid, int* pos, q3tts_sampling* sp, int* page_table,
-                             int pps, int page_size, int* tok_stream, int* tok_pos) {
+__global__ void setup_kernel(const StepDesc* __restrict__ dd, int* sid, int* pos, q3tts_sampling* sp,
+                             int* page_table, int pps, int page_size, int* tok_stream, int* tok_pos) {
+  const StepDesc& d = *dd;
   for (int b = threadIdx.x; b < d.n; b += blockDim.x) {
     sid[b] = d.sid[b];
     pos[b] = d.pos[b];
@@ -193,16 +194,15 @@ int prefill_layered(q3tts_handle* h, int sid, const float* embeds, int len) {
   return cudaGetLastError() == cudaSuccess ? Q3TTS_OK : Q3TTS_ERR_CUDA;
 }
 
-int step_layered(q3tts_handle* h, const StepDesc& d, const float* uniforms, int32_t* codes,
-                 const int32_t* forced, float* logits) {
+// The layered step's kernels for n active streams, whose descriptor is in
+// h->d_desc; the attention kernels are sized for contexts up to max_ctx.
+static void step_kernels(q3tts_handle* h, int n, int max_ctx, const float* uniforms, int32_t* codes,
+                         const int32_t* forced, float* logits) {
   cudaStream_t s = h->s;
-  const int n = d.n, Dt = h->Dt, Dc = h->Dc, Vt = h->Vt, Vc = h->Vc, wdt = h->c.weight_dtype;
+  const int Dt = h->Dt, Dc = h->Dc, Vt = h->Vt, Vc = h->Vc, wdt = h->c.weight_dtype;
   const int dump_ld = Vt + (Q3TTS_N_CODEBOOKS - 1) * Vc;
   const size_t smem = sizeof(SamplerSmem);
-  int max_ctx = 0;
-  for (int b = 0; b < n; ++b) max_ctx = d.pos[b] + 1 > max_ctx ? d.pos[b] + 1 : max_ctx;
-
-  setup_kernel<<<1, 256, 0, s>>>(d, h->d_sid, h->d_pos, h->d_sp, h->page_table, h->pps,
+  setup_kernel<<<1, 256, 0, s>>>(h->d_desc, h->d_sid, h->d_pos, h->d_sp, h->page_table, h->pps,
                                  h->c.page_size, h->d_tok_stream, h->d_tok_pos);
   sample_kernel<<<n, 256, smem, s>>>(h->pending_logits, Vt, 1, h->d_sid, h->d_sp, h->history,
                                      uniforms, 0, forced, codes, h->d_fed, logits, dump_ld, 0,
@@ -248,6 +248,75 @@ int step_layered(q3tts_handle* h, const StepDesc& d, const float* uniforms, int3
   scatter_pending_kernel<<<n, 256, 0, s>>>(h->d_sid, h->hb, h->logits, Dt, Vt, h->pending_h,
                                            h->pending_logits);
   h->launches += 6;  // setup, semantic sample, embed-sum, final norm, head, scatter
+}
+
+void step_graph_destroy(q3tts_handle* h) {
+  if (h->gexec) cudaGraphExecDestroy(h->gexec);
+  h->gexec = nullptr;
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  h->cap_stream = nullptr;
+}
+
+// Captures the step's kernels for n streams into h->gexec (inputs and
+// outputs in the handle's fixed buffers); false if capture is not possible.
+static bool step_graph_build(q3tts_handle* h, int n, bool with_forced) {
+  if (h->gexec) cudaGraphExecDestroy(h->gexec);
+  h->gexec = nullptr;
+  if (!h->cap_stream && cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    h->cap_stream = nullptr;
+    return false;
+  }
+  cudaStream_t user = h->s;
+  h->s = h->cap_stream;
+  const uint64_t l0 = h->launches;
+  cudaGraph_t g = nullptr;
+  bool ok = cudaStreamBeginCapture(h->s, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+  if (ok) {
+    step_kernels(h, n, h->c.kv_cap_steps, h->g_uni, h->g_codes, with_forced ? h->g_forced : nullptr, nullptr);
+    ok = cudaStreamEndCapture(h->s, &g) == cudaSuccess && g != nullptr;
+  }
+  h->s = user;
+  h->g_launches = h->launches - l0;
+  h->launches = l0;
+  if (ok) ok = cudaGraphInstantiate(&h->gexec, g, 0) == cudaSuccess;
+  if (g) cudaGraphDestroy(g);
+  cudaGetLastError();
+  if (!ok) {  // not capturable here: launch kernel by kernel from now on
+    h->gexec = nullptr;
+    h->graph_off = true;
+    return false;
+  }
+  h->g_n = n;
+  h->g_forced_on = with_forced;
+  return true;
+}
+
+// The layered frame step.  Without a logits dump it is replayed from a CUDA
+// graph captured once per (active streams, forced or not): the descriptor
+// goes to the device ahead of it, the caller's uniforms and forced codes are
+// copied into the handle's buffers and the codes copied out after it.
+int step_layered(q3tts_handle* h, const StepDesc& d, const float* uniforms, int32_t* codes,
+                 const int32_t* forced, float* logits) {
+  cudaStream_t s = h->s;
+  const int n = d.n;
+  // pageable source: the copy is staged before the call returns, so d may change
+  if (cudaMemcpyAsync(h->d_desc, &d, sizeof(StepDesc), cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return Q3TTS_ERR_CUDA;
+  const size_t att_smem = sizeof(float) * (size_t)(h->hd + h->c.kv_cap_steps);  // non-grouped attention
+  const bool graph = !h->graph_off && !logits && ((h->hd <= 128 && h->Hq / h->Hkv <= 4) || att_smem <= 48 * 1024);
+  if (graph && ((h->gexec && h->g_n == n && h->g_forced_on == (forced != nullptr)) ||
+                step_graph_build(h, n, forced != nullptr))) {
+    const size_t nb = sizeof(int32_t) * (size_t)n * Q3TTS_N_CODEBOOKS;
+    cudaMemcpyAsync(h->g_uni, uniforms, nb, cudaMemcpyDeviceToDevice, s);
+    if (forced) cudaMemcpyAsync(h->g_forced, forced, nb, cudaMemcpyDeviceToDevice, s);
+    cudaGraphLaunch(h->gexec, s);
+    cudaMemcpyAsync(codes, h->g_codes, nb, cudaMemcpyDeviceToDevice, s);
+    h->launches += h->g_launches;
+  } else {
+    int max_ctx = 0;
+    for (int b = 0; b < n; ++b) max_ctx = d.pos[b] + 1 > max_ctx ? d.pos[b] + 1 : max_ctx;
+    step_kernels(h, n, max_ctx, uniforms, codes, forced, logits);
+  }
   return cudaGetLastError() == cudaSuccess ? Q3TTS_OK : Q3TTS_ERR_CUDA;
 }
 
