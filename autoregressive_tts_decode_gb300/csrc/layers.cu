@@ -447,13 +447,14 @@ __global__ void __launch_bounds__(128) attention_kernel(const float* __restrict_
   }
 }
 
-// Single-query attention, one CTA per (token, kv head): the q heads of the
-// group share every K/V read.  Four warps take interleaved positions with an
-// online softmax each (lane l holds elements l + 32 j of a head vector), and
-// combine through shared memory.  The stream's page-table row is staged in
-// shared memory once.  hd <= 128, at most 4 q heads per kv head.
+// Single-query attention, one CTA per (token, kv head), for launches with many
+// CTAs (many tokens): the q heads of the group share every K/V read.  Four
+// warps take interleaved positions with an online softmax each (lane l holds
+// elements l + 32 j of a head vector), and combine through shared memory.  The
+// stream's page-table row is staged in shared memory once.  hd <= 128, at
+// most 4 q heads per kv head.  Few registers, so many CTAs share an SM.
 template <class KT>
-__global__ void __launch_bounds__(128) attention_gqa_kernel(const float* __restrict__ qkv, int ld, TokDesc td,
+__global__ void __launch_bounds__(128) attention_gqa4_kernel(const float* __restrict__ qkv, int ld, TokDesc td,
                                                             KVDesc kv, int layer, int Hq,
                                                             float* __restrict__ out, int ldo) {
   constexpr int NW = 4, RMAX = 4;
@@ -538,16 +539,163 @@ __global__ void __launch_bounds__(128) attention_gqa_kernel(const float* __restr
   }
 }
 
+// Single-query attention, one CTA per (token, kv head), for launches with few
+// CTAs (few tokens): the q heads of the group share every K/V read.  Eight
+// warps take runs of GQA_B consecutive positions (warp w: w B .. w B + B - 1,
+// then + 8 B), issuing the K/V loads of a run together before the
+// online-softmax updates; lane l holds the E = hd / 32 contiguous elements
+// l E .. l E + E - 1 of a head vector (one vector load per row).  The warps
+// combine through shared memory; the stream's page-table row is staged in
+// shared memory once.  hd = 64 or 128, at most 4 q heads per kv head.
+constexpr int GQA_NW = 8, GQA_B = 4, GQA_RMAX = 4;
+
+template <class KT, int E>
+__device__ __forceinline__ void load_row(const KT* p, float (&f)[4]);
+template <>
+__device__ __forceinline__ void load_row<float, 4>(const float* p, float (&f)[4]) {
+  const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
+  f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void load_row<float, 2>(const float* p, float (&f)[4]) {
+  const float2 v = __ldcg(reinterpret_cast<const float2*>(p));
+  f[0] = v.x; f[1] = v.y; f[2] = 0.f; f[3] = 0.f;
+}
+template <>
+__device__ __forceinline__ void load_row<bf16, 4>(const bf16* p, float (&f)[4]) {
+  const uint2 v = __ldcg(reinterpret_cast<const uint2*>(p));
+  f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xffff0000u);
+  f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xffff0000u);
+}
+template <>
+__device__ __forceinline__ void load_row<bf16, 2>(const bf16* p, float (&f)[4]) {
+  const uint32_t v = __ldcg(reinterpret_cast<const unsigned int*>(p));
+  f[0] = __uint_as_float(v << 16); f[1] = __uint_as_float(v & 0xffff0000u); f[2] = 0.f; f[3] = 0.f;
+}
+
+template <class KT, int E>
+__global__ void __launch_bounds__(GQA_NW * 32) attention_gqa8_kernel(const float* __restrict__ qkv, int ld,
+                                                                    TokDesc td, KVDesc kv, int layer, int Hq,
+                                                                    float* __restrict__ out, int ldo) {
+  constexpr int NW = GQA_NW, B = GQA_B, RMAX = GQA_RMAX;
+  extern __shared__ int pt[];  // the stream's page-table row
+  __shared__ float wm[NW][RMAX], wl[NW][RMAX];
+  __shared__ __align__(16) float wo[NW][RMAX][128];
+  const int m = blockIdx.x, g = blockIdx.y, hd = E * 32, rep = Hq / kv.Hkv;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int stream = td.tok_stream[m];
+  const int pos = td.tok_pos ? td.tok_pos[m] : td.pos_const;
+  const int S = pos + 1, npg = (S + kv.page_size - 1) / kv.page_size;
+  for (int i = threadIdx.x; i < npg; i += blockDim.x) pt[i] = kv.page_table[stream * kv.pages_per_stream + i];
+  float q[RMAX][4];
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      q[r][e] = (r < rep && e < E) ? qkv[(size_t)m * ld + (g * rep + r) * hd + lane * E + e] : 0.f;
+  __syncthreads();
+  const float scale = 1.0f / sqrtf((float)hd);
+  const size_t head_stride = (size_t)kv.page_size * hd;
+  float mx[RMAX], l[RMAX], o[RMAX][4];
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r) {
+    mx[r] = -INFINITY;
+    l[r] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[r][e] = 0.f;
+  }
+  for (int t0 = warp * B; t0 < S; t0 += NW * B) {
+    float k[B][4], v[B][4];
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int t = t0 + b;
+      if (t < S) {
+        const int page = pt[t / kv.page_size];
+        const size_t base = ((((size_t)layer * kv.n_pages + page) * 2) * kv.Hkv + g) * head_stride +
+                            (size_t)(t % kv.page_size) * hd + lane * E;
+        const KT* kp = (const KT*)kv.pool + base;
+        load_row<KT, E>(kp, k[b]);
+        load_row<KT, E>(kp + (size_t)kv.Hkv * head_stride, v[b]);  // the V plane of the same page
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      if (t0 + b < S) {
+#pragma unroll
+        for (int r = 0; r < RMAX; ++r) {
+          if (r < rep) {
+            float d = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) d = fmaf(q[r][e], k[b][e], d);
+            d = warp_sum(d) * scale;
+            const float mn = fmaxf(mx[r], d), corr = __expf(mx[r] - mn), ex = __expf(d - mn);
+            l[r] = l[r] * corr + ex;
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[r][e] = o[r][e] * corr + ex * v[b][e];
+            mx[r] = mn;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < RMAX; ++r) {
+    if (r < rep) {
+      if (lane == 0) {
+        wm[warp][r] = mx[r];
+        wl[warp][r] = l[r];
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) wo[warp][r][lane * E + e] = o[r][e];
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < rep * hd; e += blockDim.x) {
+    const int r = e / hd, i = e % hd;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, wm[w][r]);
+    float Ls = 0.f, Os = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float f = wm[w][r] == -INFINITY ? 0.f : __expf(wm[w][r] - M);
+      Ls += wl[w][r] * f;
+      Os += wo[w][r][i] * f;
+    }
+    out[(size_t)m * ldo + (g * rep + r) * hd + i] = Os / Ls;
+  }
+}
+
 void launch_attention(int kdt, const float* qkv, int ld, int M, TokDesc td, KVDesc kv, int layer,
                       int Hq, float* out, int ldo, int max_ctx, cudaStream_t s) {
   if (M <= 0) return;
+  static int n_sm = 0;  // the current device's SM count (one device per process)
+  if (!n_sm) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n_sm = 1;
+  }
+  const size_t pts = sizeof(int) * (size_t)((max_ctx + kv.page_size - 1) / kv.page_size + 1);
+  const bool bf = kdt == Q3TTS_BF16;
+  if ((kv.hd == 128 || kv.hd == 64) && Hq / kv.Hkv <= GQA_RMAX && M * kv.Hkv < 2 * n_sm) {
+    // few CTAs: eight warps per CTA, several K/V rows in flight per warp
+    dim3 grid(M, kv.Hkv);
+    const int nt = GQA_NW * 32;
+    if (bf) {
+      if (kv.hd == 128) attention_gqa8_kernel<bf16, 4><<<grid, nt, pts, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
+      else attention_gqa8_kernel<bf16, 2><<<grid, nt, pts, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
+    } else {
+      if (kv.hd == 128) attention_gqa8_kernel<float, 4><<<grid, nt, pts, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
+      else attention_gqa8_kernel<float, 2><<<grid, nt, pts, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
+    }
+    return;
+  }
   if (kv.hd <= 128 && Hq / kv.Hkv <= 4) {
     dim3 grid(M, kv.Hkv);
-    const size_t smem = sizeof(int) * (size_t)((max_ctx + kv.page_size - 1) / kv.page_size + 1);
-    if (kdt == Q3TTS_BF16)
-      attention_gqa_kernel<bf16><<<grid, 128, smem, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
+    if (bf)
+      attention_gqa4_kernel<bf16><<<grid, 128, pts, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
     else
-      attention_gqa_kernel<float><<<grid, 128, smem, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
+      attention_gqa4_kernel<float><<<grid, 128, pts, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
     return;
   }
   dim3 grid(M, Hq);

@@ -303,7 +303,7 @@ int step_layered(q3tts_handle* h, const StepDesc& d, const float* uniforms, int3
   if (cudaMemcpyAsync(h->d_desc, &d, sizeof(StepDesc), cudaMemcpyHostToDevice, s) != cudaSuccess)
     return Q3TTS_ERR_CUDA;
   const size_t att_smem = sizeof(float) * (size_t)(h->hd + h->c.kv_cap_steps);  // non-grouped attention
-  const bool graph = !h->graph_off && !logits && ((h->hd <= 128 && h->Hq / h->Hkv <= 4) || att_smem <= 48 * 1024);
+  const bool graph = !h->graph_off && !logits && (((h->hd == 128 || h->hd == 64) && h->Hq / h->Hkv <= 4) || att_smem <= 48 * 1024);
   if (graph && ((h->gexec && h->g_n == n && h->g_forced_on == (forced != nullptr)) ||
                 step_graph_build(h, n, forced != nullptr))) {
     const size_t nb = sizeof(int32_t) * (size_t)n * Q3TTS_N_CODEBOOKS;
