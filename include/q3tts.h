@@ -162,7 +162,14 @@ int q3tts_prefill(q3tts_handle* h, int stream_id, const float* embeds_dev, int l
  *                    logits behind each draw (pending Talker logits, then the
  *                    15 CodePredictor heads).
  * Each stream advances by one Talker position.  Q3TTS_ERR_STATE if a stream
- * has no prompt, Q3TTS_ERR_CAPACITY if its cache is full. */
+ * has no prompt, Q3TTS_ERR_CAPACITY if its cache is full.
+ * Execution: one stream whose configuration and sampling settings the
+ * persistent frame kernel covers runs as one launch of that kernel; otherwise
+ * the frame runs layer by layer, and without a logits dump that sequence is
+ * captured into a CUDA graph on the first call for a given n_active (and
+ * forced_dev NULL or not) and replayed on later calls, the inputs and codes
+ * passing through buffers in the workspace.  Q3TTS_FRAME_KERNEL=0 and
+ * Q3TTS_GRAPH=0 in the environment at q3tts_create turn either off. */
 int q3tts_step_frame(q3tts_handle* h, const q3tts_sampling* params, const int32_t* stream_ids,
                      int n_active, const float* uniforms_dev, int32_t* codes_dev,
                      const int32_t* forced_dev, float* logits_dev);
