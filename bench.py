@@ -39,19 +39,35 @@ def dist_env():
 
 
 # Sources of the persistent frame kernel: a recorded DRAM-traffic figure holds
-# only for the exact sources it was captured from.
+# only for the code it was captured from.
 KERNEL_SOURCES = ("autoregressive_tts_decode_gb300/csrc/frame_kernel.cu",
                   "autoregressive_tts_decode_gb300/csrc/sampler.cuh",
                   "autoregressive_tts_decode_gb300/csrc/common.cuh",
                   "autoregressive_tts_decode_gb300/csrc/engine.cuh", "include/q3tts.h")
 
 
-def kernel_source_sha():
+def _code_only(text):
+    """C/C++ source without comments and blank lines: edits to comments do not
+    change what is compiled (these sources hold no string literal with a
+    comment marker)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
+def kernel_source_sha(texts=None):
+    """Hash of the frame kernel's code (comments excluded); `texts` overrides
+    the files' contents (same order as KERNEL_SOURCES)."""
     import hashlib
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+    for i, f in enumerate(KERNEL_SOURCES):
+        if texts is None:
+            with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+                t = fh.read()
+        else:
+            t = texts[i]
+        h.update(_code_only(t).encode("utf-8"))
     return h.hexdigest()[:16]
 
 
