@@ -38,6 +38,24 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def slowest(seconds, world, device):
+    """The largest of the ranks' timed-region lengths (every rank gets it): the
+    whole job's time, since the replicas run side by side.  One rank: itself."""
+    if world <= 1:
+        return float(seconds)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(seconds)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(frames_per_rank, world, seconds):
+    """Whole-job throughput: the frames all ranks decoded over the slowest
+    rank's time."""
+    return frames_per_rank * world / seconds
+
+
 # Sources of the persistent frame kernel: a recorded DRAM-traffic figure holds
 # only for the code it was captured from.
 KERNEL_SOURCES = ("autoregressive_tts_decode_gb300/csrc/frame_kernel.cu",
@@ -304,12 +322,9 @@ def main():
     launches = eng.kernel_launches() - launches0
     elapsed = t_start.elapsed_time(t_end) / 1e3
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    if world > 1:
-        t = torch.tensor([elapsed], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = slowest(elapsed, world, "cuda")
     frames = args.steps * B * world
-    value = frames / elapsed
+    value = job_rate(args.steps * B, world, elapsed)
 
     # algorithmic bytes of the timed steps (weights once per use, KV per stream)
     byts = 0
@@ -358,11 +373,9 @@ def main():
             torch.cuda.current_stream().synchronize()
         dt = time.perf_counter() - t0
         eng.sync()
-        if world > 1:
-            t = torch.tensor([dt], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dt = float(t.item())
-        e2e = {"value": frames / dt, "unit": UNIT, "h2d_bytes_per_step": 16 * 4 * B,
+        dt = slowest(dt, world, "cuda")
+        e2e = {"value": job_rate(args.steps * B, world, dt), "unit": UNIT,
+               "h2d_bytes_per_step": 16 * 4 * B,
                "d2h_bytes_per_step": 16 * 4 * B}
 
     cpu = None
