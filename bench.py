@@ -323,7 +323,6 @@ def main():
     elapsed = t_start.elapsed_time(t_end) / 1e3
     step_ms = [a.elapsed_time(b) for a, b in ev]
     elapsed = slowest(elapsed, world, "cuda")
-    frames = args.steps * B * world
     value = job_rate(args.steps * B, world, elapsed)
 
     # algorithmic bytes of the timed steps (weights once per use, KV per stream)
