@@ -14,33 +14,36 @@
 // Design (GB300, one CTA per SM, cooperative launch):
 //  * A producer warp walks the frame's weight schedule for its CTA -- the
 //    same row slices the consumers will need, in frame order -- and streams
-//    them through a 6-deep ring of 16 KB stages in shared memory with 1-D
-//    bulk TMA copies (cp.async.bulk + mbarrier transaction counts).  Weights do not
-//    depend on activations, so the stream runs ahead across the grid
-//    barriers that separate dependent phases and HBM stays busy.
-//  * Eight consumer warps run the phases: fused RMSNorm + GEMV on the staged
-//    rows; attention; a fused SwiGLU FFN that multiplies each CTA's gate/up
-//    rows and the matching rows of the transposed down projection and adds
-//    its partial result into the residual with float4 atomics (split-K over
-//    the FFN width, no extra phase); o_proj as a split over (head, output
-//    column) with the same atomic accumulation.  Draws are made redundantly
-//    by every CTA from the full logit vector, so a sampled code needs no
-//    extra barrier.
-//  * Residual bookkeeping: a layer's input is R + dA + dF (two alternating
-//    buffer sets); phase A folds it into the other set's R and zeroes that
-//    set's deltas, which phase B (attention) and phase C (FFN) accumulate.
+//    them through an 11-deep ring of 12 KB chunks in shared memory with 1-D
+//    bulk copies (cp.async.bulk + mbarrier transaction counts, L2
+//    evict-first).  Weights do not depend on activations, so the stream runs
+//    ahead across the grid barriers that separate dependent phases.
+//  * Eight consumer warps form four gangs of two; ring chunk n belongs to
+//    gang n % 4, whose warps split each row's reduction between them and meet
+//    once per chunk (a 64-thread named barrier and a small exchange buffer):
+//    no block-wide barrier sits inside a streaming loop.  Phases: RMSNorm
+//    staged once per phase, then row GEMVs (QKV, projection, heads);
+//    attention; a fused SwiGLU FFN over "units" (gate row, up row and down
+//    column of one intermediate channel, contiguous) whose partial outputs
+//    are added into the residual with float4 atomics (split-K over the FFN
+//    width, no extra phase); o_proj over 32-column tiles of one head with
+//    the same atomic accumulation.  Draws are made redundantly by every CTA
+//    from the full logit vector (sampler.cuh, fast_sample), so a sampled code
+//    needs no barrier.
+//  * Residual bookkeeping: three rotating buffers; a layer folds its input
+//    into the next two, so every phase reads one complete vector.
 //  * Phases per layer: CodePredictor 3 (QKV | attention + o_proj | FFN) --
 //    its context is at most 16 positions, so every CTA recomputes the one or
 //    two heads it needs; Talker 4 (QKV | attention partials over position
 //    chunks | combine + o_proj | FFN).
-//  * Latency is the constraint of the short CodePredictor phases: every
-//    thread issues all of a step's global loads before using them (residual
-//    gathers, K/V rows, partial sums), draws are register-resident (per-warp
-//    radix histograms, a shuffle sort of the <= 64 candidates), and the grid
-//    barrier is a release-add / acquire-load counter.
-//  * Every wait (ring slots, grid barrier) is bounded; on expiry the kernel
-//    records Q3TTS_ERR_TIMEOUT, raises an abort flag, stops waiting, lets
-//    in-flight copies land and returns.
+//  * The frame is a list of steps decoded from a (pass, step) position, each
+//    step kind with one call site; the consumers' loop state and launch
+//    parameters live in shared memory (local memory is costly beside a
+//    shared-memory carve-out this large).
+//  * The grid barrier is a release-add / acquire-load counter polled by one
+//    thread per CTA.  Every wait (ring slots, side slots, grid barrier) is
+//    bounded; on expiry the kernel records Q3TTS_ERR_TIMEOUT, raises an abort
+//    flag, stops waiting, lets in-flight copies land and returns.
 #include <algorithm>
 #include <atomic>
 #include <mutex>
@@ -1570,9 +1573,9 @@ __device__ __forceinline__ void next_step(ConsState& L) {
   __syncwarp();
 }
 
-// DRAW step: draw code j; code 0..14 starts CodePredictor pass j (running
-// embedding sum, input tokens), code 15 starts the Talker step (its input is
-// the sum of the frame's 16 code embeddings).
+// DRAW step: draw code j; code 0..14 starts CodePredictor pass j (its input
+// tokens), code 15 starts the Talker step (its input is the sum of the frame's
+// 16 code embeddings).
 template <class WT>
 __device__ __forceinline__ void draw_step(Cons c, int j) {
   ConsState& L = cst();
