@@ -14,9 +14,12 @@
 //   6. top_p < 1: keep the shortest prefix whose running float sum >= top_p * Z
 //   7. Z = running float sum of kept w, t = u * Z, pick the first id whose
 //      running sum > t, else the last kept id.
-// Selection (step 4) uses a radix select on order-preserving keys when k is
-// small (ties at the k-th value resolved by lowest index) and a bitonic sort of
-// all ids otherwise.
+// Selection (step 4), in the block sampler of the layered step (group_sample):
+// a radix select on order-preserving keys when k is small (ties at the k-th
+// value resolved by lowest index) and a bitonic sort of all ids otherwise.  In
+// the persistent frame kernel (fast_sample, at the end): a lower bound on the
+// k-th largest key from the lanes' maxima, the keys above it gathered and
+// ranked by counting.  Both give the same ordered candidates, so the same draw.
 #pragma once
 
 #include "common.cuh"
