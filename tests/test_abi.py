@@ -88,3 +88,11 @@ def test_binding_refuses_missing_library(tmp_path):
             q3tts.load(str(tmp_path / "nope.so"))
         finally:
             q3tts._lib = q3tts._lib_saved
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    """No CPU fallback: without the built library the binding raises instead of
+    running anything."""
+    monkeypatch.setattr(q3tts, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        q3tts.load(str(tmp_path / "libq3tts.so"))
