@@ -32,10 +32,27 @@ def _deps():
     return max(os.path.getmtime(f) for f in files)
 
 
+def _up_to_date() -> bool:
+    return os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps()
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps():
+    """Compiles and links the library unless it is newer than every source.
+    Processes building at once (one per rank) take turns on a file lock, so
+    none links objects another is still writing."""
+    import fcntl
+
+    if not force and _up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, "build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and _up_to_date():
+            return LIB
+        return _build(verbose)
+
+
+def _build(verbose: bool) -> str:
     srcs = sources()
     objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
 
