@@ -22,15 +22,20 @@ LAYER_KEYS = ("w_qkv", "w_o", "w_gateup", "w_down",
               "g_attn_norm", "g_ffn_norm", "g_q_norm", "g_k_norm")
 
 
-def build_cmd():
+def build_cmd(out=None):
     # -ffp-contract=off: the sampler's float steps must not be fused.
     return ["gcc", "-O3", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
-            SRC, "-o", LIB, "-lm"]
+            SRC, "-o", out or LIB, "-lm"]
 
 
 def build(force: bool = False) -> str:
+    """Compiles the oracle library unless it is newer than its source; the
+    result replaces the old file in one step (a process loading it meanwhile
+    sees the old or the new library, never a partial one)."""
     if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < os.path.getmtime(SRC):
-        subprocess.run(build_cmd(), check=True)
+        tmp = "%s.%d.tmp" % (LIB, os.getpid())
+        subprocess.run(build_cmd(tmp), check=True)
+        os.replace(tmp, LIB)
     return LIB
 
 
