@@ -80,8 +80,8 @@ def test_attention_matches_sdpa(oracle_mod, Hq, Hkv, S):
         assert np.allclose(o, np.repeat(V[0], Hq // Hkv, axis=0), atol=1e-12)
 
 
-def _tiny_weights(**zero):
-    W = synth.make_weights(TINY.shape)
+def _tiny_weights(dtype=synth.DTYPE_F32, **zero):
+    W = synth.make_weights(dataclasses.replace(TINY.shape, weight_dtype=dtype))
     for name in list(W):
         for key, layers in zero.items():
             if name.endswith("." + key) and name.split(".")[0] in layers:
@@ -108,11 +108,13 @@ def test_identity_stack_gives_head_of_normed_input(oracle_mod):
     assert np.allclose(lg, f64(W["talker.w_head"]) @ hn, rtol=1e-9, atol=1e-12)
 
 
-def test_single_position_attention_block(oracle_mod):
+@pytest.mark.parametrize("dtype", [synth.DTYPE_F32, synth.DTYPE_BF16])
+def test_single_position_attention_block(oracle_mod, dtype):
     """Prompt of length 1 and W_down = 0: attention over one position returns v,
-    so x = e + W_o v with v = W_v RMSNorm(e) (the v rows of W_qkv)."""
-    s = dataclasses.replace(TINY.shape, talker_layers=1)
-    W = _tiny_weights(w_down=("talker",))
+    so x = e + W_o v with v = W_v RMSNorm(e) (the v rows of W_qkv).  With bf16
+    weights the expected value widens them through torch, not the oracle."""
+    s = dataclasses.replace(TINY.shape, talker_layers=1, weight_dtype=dtype)
+    W = _tiny_weights(dtype, w_down=("talker",))
     W = {k: v for k, v in W.items() if not k.startswith("talker.1.")}
     o = oracle_mod.Oracle(s, W, 1, TINY.kv_cap)
     e = synth.make_prompts(s, [1])[0].numpy().astype(np.float64)
@@ -125,10 +127,11 @@ def test_single_position_attention_block(oracle_mod):
     assert np.allclose(x, want, rtol=1e-9, atol=1e-12)
 
 
-def test_ffn_block_is_swiglu(oracle_mod):
+@pytest.mark.parametrize("dtype", [synth.DTYPE_F32, synth.DTYPE_BF16])
+def test_ffn_block_is_swiglu(oracle_mod, dtype):
     """W_o = 0 leaves the FFN: x = e + W_down(silu(W_gate n) * W_up n), n = RMSNorm(e)."""
-    s = dataclasses.replace(TINY.shape, talker_layers=1)
-    W = _tiny_weights(w_o=("talker",))
+    s = dataclasses.replace(TINY.shape, talker_layers=1, weight_dtype=dtype)
+    W = _tiny_weights(dtype, w_o=("talker",))
     W = {k: v for k, v in W.items() if not k.startswith("talker.1.")}
     o = oracle_mod.Oracle(s, W, 1, TINY.kv_cap)
     e = synth.make_prompts(s, [3])[0].to(torch.float64)
@@ -147,13 +150,17 @@ def _embed_sum(W, codes):
     return x
 
 
+@pytest.mark.parametrize("dtype", [synth.DTYPE_F32, synth.DTYPE_BF16])
 @pytest.mark.parametrize("proj", [False, True])
-def test_frame_wiring_with_identity_stacks(oracle_mod, proj):
+def test_frame_wiring_with_identity_stacks(oracle_mod, proj, dtype):
     """Both stacks reduced to the identity (W_o = W_down = 0): each CodePredictor
     logit vector is head_j . RMSNorm(P u_j) with u_0 = E_t[c0] (pass 0's last token)
     and u_j = E_cp[j-1][c_j]; the next pending logits are the codec head of the
-    normed embedding sum of the frame's 16 codes."""
-    shape = TINY.shape
+    normed embedding sum of the frame's 16 codes.  For bf16 storage the
+    expected values come from torch's own bf16 -> fp64 conversion of the same
+    tensors, so a wrong shift or half-word order in the oracle's widening of
+    bf16 weights fails here."""
+    shape = dataclasses.replace(TINY.shape, weight_dtype=dtype)
     if proj:
         shape = dataclasses.replace(shape, cp_hidden=128, cp_ffn=384)
     W = synth.make_weights(shape)
@@ -299,3 +306,72 @@ def test_attention_block_with_qk_norm_and_causal_mask(oracle_mod, kv_bf16):
                                          enable_gqa=True)[0].permute(1, 0, 2).reshape(T, Hq * hd)
     want = e + F.linear(att, W["talker.0.w_o"].double())
     assert np.allclose(x, want.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def _penalty_case():
+    """Identity stacks (W_o = W_down = 0 everywhere) and a hand-made codec head
+    whose rows A and B carry a near tie: rows = s * u1 and 0.98 s * u1 + 3 s * u2
+    for two orthonormal directions.  u1 is the direction of the embedding sum
+    of a fixed forced frame (semantic code A, first acoustic code B), so after
+    that frame the pending logits are l_A > l_B > 0 with l_B / l_A = 0.98; a
+    prompt ending in u2 gives the pending logits l_B = 3 s |h| and l_A = 0, so
+    the first frame draws B greedily.  All other rows are 0."""
+    shape = TINY.shape
+    W = synth.make_weights(shape)
+    for name in list(W):
+        if name.endswith(".w_o") or name.endswith(".w_down"):
+            W[name] = torch.zeros_like(W[name])
+    D, Vt = shape.talker_hidden, shape.codec_vocab
+    A, B = 1234, 77
+    rng = np.random.default_rng(5)
+    forced = np.concatenate([[A, B], rng.integers(0, shape.cp_vocab, 14)]).astype(np.int32)
+    x1 = _embed_sum(W, forced)
+    u1 = x1 / np.linalg.norm(x1)
+    r = rng.normal(size=D)
+    u2 = r - (r @ u1) * u1
+    u2 /= np.linalg.norm(u2)
+    head = np.zeros((Vt, D))
+    s = 0.05
+    head[A] = s * u1
+    head[B] = 0.98 * s * u1 + 3.0 * s * u2
+    W["talker.w_head"] = torch.tensor(head, dtype=torch.float32)
+    return shape, W, A, B, forced, u1, u2
+
+
+def test_repetition_penalty_history_is_the_fed_semantic_code(oracle_mod):
+    """Repetition penalty bookkeeping ("qwen3-tts-hip" README, "Library Usage",
+    GenerateOptions::repetition_penalty; the usual divide-positive rule):
+      * the history holds the semantic code fed forward (the forced one under
+        teacher forcing), not the drawn one -- frame 1 draws B but feeds A;
+      * it changes the next frame's pick: with rho = 1.5 the near tie A > B of
+        frame 2 flips to B, with rho = 1 it stays A;
+      * acoustic codes never enter it -- frame 1 feeds B as its first acoustic
+        code, and a penalised B would turn the flip back to A;
+      * prefill restarts it, and another stream's history is its own."""
+    shape, W, A, B, forced, u1, u2 = _penalty_case()
+    pen = dataclasses.replace(synth.GREEDY, repetition_penalty=1.5)
+    u = synth.uniforms([0], 2)[0]
+    prompt = np.zeros((3, shape.talker_hidden), np.float32)
+    prompt[-1] = u2
+    for rho, want2 in ((1.0, A), (1.5, B)):
+        sp = dataclasses.replace(synth.GREEDY, repetition_penalty=rho)
+        o = oracle_mod.Oracle(shape, W, 1, TINY.kv_cap)
+        o.prefill(0, prompt)
+        c1, _ = o.step_frame(0, sp, u[0], forced=forced)
+        assert c1[0] == B  # drawn B, fed A
+        _, l2 = o.pending(0)
+        assert l2[A] > l2[B] > l2[A] / 1.5 > 0
+        c2, _ = o.step_frame(0, sp, u[1])
+        assert c2[0] == want2, (rho, c2[0])
+    # a prompt ending in u1 gives the near tie A > B at once
+    tie_prompt = np.zeros((2, shape.talker_hidden), np.float32)
+    tie_prompt[-1] = u1
+    o = oracle_mod.Oracle(shape, W, 2, TINY.kv_cap)
+    o.prefill(0, prompt)
+    o.step_frame(0, pen, u[0], forced=forced)  # history of stream 0: {A}
+    o.prefill(1, tie_prompt)                    # stream 1 never fed A
+    c, _ = o.step_frame(1, pen, u[0])
+    assert c[0] == A
+    o.prefill(0, tie_prompt)                    # stream 0 restarts: history cleared
+    c, _ = o.step_frame(0, pen, u[0])
+    assert c[0] == A
