@@ -43,6 +43,9 @@ struct Carver {
 
 bool pos_int(int v) { return v > 0; }
 
+// A non-null pointer that is not 16-byte aligned (NULL passes: optional tensors).
+bool misaligned16(const void* p) { return ((uintptr_t)p & 15u) != 0; }
+
 int check_config(const q3tts_config* c) {
   if (!c) return Q3TTS_ERR_ARG;
   if (!pos_int(c->talker_layers) || !pos_int(c->talker_hidden) || !pos_int(c->talker_ffn) ||
@@ -173,11 +176,20 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
       !w->cp_heads || !w->cp_embeds)
     return Q3TTS_ERR_ARG;
   if ((c.talker_hidden != c.cp_hidden) != (w->cp_w_proj != nullptr)) return Q3TTS_ERR_ARG;
+  // every weight and gain is read with 16-byte vector loads or bulk copies
+  if (misaligned16(w->talker_g_final) || misaligned16(w->talker_w_head) ||
+      misaligned16(w->talker_e_codec) || misaligned16(w->cp_g_final) ||
+      misaligned16(w->cp_heads) || misaligned16(w->cp_embeds) || misaligned16(w->cp_w_proj))
+    return Q3TTS_ERR_ARG;
   for (int l = 0; l < c.talker_layers + c.cp_layers; ++l) {
     const q3tts_layer_weights& L =
         l < c.talker_layers ? w->talker_layers[l] : w->cp_layers[l - c.talker_layers];
     if (!L.w_qkv || !L.w_o || !L.w_gateup || !L.w_down || !L.g_attn_norm || !L.g_ffn_norm ||
         (c.qk_norm && (!L.g_q_norm || !L.g_k_norm)))
+      return Q3TTS_ERR_ARG;
+    if (misaligned16(L.w_qkv) || misaligned16(L.w_o) || misaligned16(L.w_gateup) ||
+        misaligned16(L.w_down) || misaligned16(L.g_attn_norm) || misaligned16(L.g_ffn_norm) ||
+        misaligned16(L.g_q_norm) || misaligned16(L.g_k_norm))
       return Q3TTS_ERR_ARG;
   }
   if (workspace_bytes < q3tts_workspace_size(cfg)) return Q3TTS_ERR_ARG;
@@ -293,18 +305,17 @@ int q3tts_step_frame(q3tts_handle* h, const q3tts_sampling* params, const int32_
     if (h->len[s] / h->c.page_size >= (int)h->pages[s].size()) ++pages_needed;
   }
   if (pages_needed > (int)h->free_pages.size()) return Q3TTS_ERR_CAPACITY;
+  // pages are picked from the top of the free list here and taken off it only
+  // once the frame is launched, so a failed launch leaves every list as it was
+  int taken = 0;
   for (int b = 0; b < n_active; ++b) {
     int s = stream_ids[b];
     d.sid[b] = s;
     d.pos[b] = h->len[s];
     d.sp[b] = params[b];
     d.newpage[b] = -1;
-    if (h->len[s] / h->c.page_size >= (int)h->pages[s].size()) {
-      int p = h->free_pages.back();
-      h->free_pages.pop_back();
-      h->pages[s].push_back(p);
-      d.newpage[b] = p;
-    }
+    if (h->len[s] / h->c.page_size >= (int)h->pages[s].size())
+      d.newpage[b] = h->free_pages[h->free_pages.size() - 1 - taken++];
   }
   int rc;
   if (q3::frame_kernel_supports(h, n_active, d.sp))
@@ -312,7 +323,11 @@ int q3tts_step_frame(q3tts_handle* h, const q3tts_sampling* params, const int32_
   else
     rc = q3::step_layered(h, d, uniforms_dev, codes_dev, forced_dev, logits_dev);
   if (rc != Q3TTS_OK) return rc;
-  for (int b = 0; b < n_active; ++b) h->len[stream_ids[b]] += 1;
+  for (int b = 0; b < n_active; ++b) {
+    if (d.newpage[b] >= 0) h->pages[stream_ids[b]].push_back(d.newpage[b]);
+    h->len[stream_ids[b]] += 1;
+  }
+  h->free_pages.resize(h->free_pages.size() - taken);
   return Q3TTS_OK;
 }
 

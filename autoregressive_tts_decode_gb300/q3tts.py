@@ -126,6 +126,18 @@ def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+def _need(t, name: str, dtype, numel: int, what: str):
+    """Raises Q3TTSError(ERR_ARG) unless t is a contiguous CUDA tensor of the
+    given dtype with at least numel elements (checked before the C call, so a
+    wrong buffer is an error instead of an out-of-bounds device write)."""
+    import torch
+    ok = (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous() and t.dtype == dtype
+          and t.numel() >= numel)
+    if not ok:
+        raise Q3TTSError(ERR_ARG, f"{what}: {name} must be a contiguous CUDA {dtype} tensor "
+                                  f"of at least {numel} elements")
+
+
 class Engine:
     """One libq3tts handle over device weights (dict of CUDA tensors named as in
     ``synth.weight_specs``) and a workspace allocated here through torch."""
@@ -178,8 +190,11 @@ class Engine:
             pass
 
     def prefill(self, stream_id: int, embeds) -> None:
-        if not embeds.is_cuda or embeds.dtype.itemsize != 4 or not embeds.is_contiguous():
-            raise ValueError("embeds must be a contiguous CUDA float32 tensor")
+        import torch
+        if embeds.dim() != 2 or embeds.shape[1] != self.shape.talker_hidden:
+            raise Q3TTSError(ERR_ARG, "q3tts_prefill: embeds must be [len, talker_hidden]")
+        _need(embeds, "embeds", torch.float32, embeds.shape[0] * self.shape.talker_hidden,
+              "q3tts_prefill")
         _check(load().q3tts_prefill(self.h, stream_id, embeds.data_ptr(), embeds.shape[0]),
                "q3tts_prefill")
 
@@ -189,6 +204,7 @@ class Engine:
         forced: None or CUDA int32 [n, 16]; logits: None or CUDA fp32
         [n, V_t + 15 V_c].  `sampling` is one Sampling-like object or a list."""
         n = len(stream_ids)
+        self._check_frame_buffers(n, uniforms, codes, forced, logits, "q3tts_step_frame")
         if not isinstance(sampling, (list, tuple)):
             sampling = [sampling] * n
         sp = (Sampling * n)(*[sampling_struct(x) for x in sampling])
@@ -200,11 +216,22 @@ class Engine:
                           logits=None) -> None:
         """One frame of one stream through q3tts_step_frame_static (scratch in the
         library's static device array); tensors as for step_frame with n = 1."""
+        self._check_frame_buffers(1, uniforms, codes, forced, logits, "q3tts_step_frame_static")
         sp = sampling_struct(sampling)
         _check(load().q3tts_step_frame_static(self.h, C.byref(sp), int(stream_id),
                                               uniforms.data_ptr(), codes.data_ptr(),
                                               _ptr(forced), _ptr(logits)),
                "q3tts_step_frame_static")
+
+    def _check_frame_buffers(self, n, uniforms, codes, forced, logits, what):
+        import torch
+        _need(uniforms, "uniforms", torch.float32, n * N_CODEBOOKS, what)
+        _need(codes, "codes", torch.int32, n * N_CODEBOOKS, what)
+        if forced is not None:
+            _need(forced, "forced", torch.int32, n * N_CODEBOOKS, what)
+        if logits is not None:
+            s = self.shape
+            _need(logits, "logits", torch.float32, n * (s.codec_vocab + 15 * s.cp_vocab), what)
 
     def read_pending(self, stream_id: int):
         import torch

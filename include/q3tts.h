@@ -80,6 +80,10 @@ typedef struct q3tts_config {
 } q3tts_config;
 
 /* One decoder layer; device pointers, row-major [out, in], weight_dtype.
+ * Every weight and gain pointer (here and in q3tts_weights) must be 16-byte
+ * aligned: the kernels read them with 16-byte vector loads and bulk copies.
+ * q3tts_create returns Q3TTS_ERR_ARG for a pointer that is not, before it
+ * launches or copies anything.
  *   w_qkv    [(Hq + 2 Hkv) hd, D]   q rows, then k rows, then v rows
  *   w_o      [D, Hq hd]
  *   w_gateup [2 F, D]                gate rows, then up rows
@@ -143,7 +147,12 @@ size_t q3tts_workspace_size(const q3tts_config* cfg);
 int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspace,
                  size_t workspace_bytes, void* cuda_stream, q3tts_handle** out);
 
-/* Restarts stream stream_id with a prompt: embeds_dev is a device fp32
+/* Counterpart of the engine's prompt-conditioned start of a stream
+ * ("qwen3-tts-hip" README, "Library Usage": a model loaded with
+ * load_with_max_frames / EngineOptions::max_cache_steps, then
+ * start_stream over the prompt), with random prompt vectors standing in for
+ * the text conditioning.
+ * Restarts stream stream_id with a prompt: embeds_dev is a device fp32
  * [len, D_t] array of Talker input vectors for positions 0..len-1.  Writes
  * their KV and leaves the final-normed hidden and codec logits of position
  * len-1 as the stream's pending state, from which the next frame's semantic
@@ -219,14 +228,20 @@ int q3tts_step_frame_static(q3tts_handle* h, const q3tts_sampling* params, int s
 int q3tts_read_pending(q3tts_handle* h, int stream_id, float* hidden_dev, float* logits_dev);
 
 /* Forgets a stream (-1 = all): length, semantic history, pending state; its
- * KV pages return to the pool. */
+ * KV pages return to the pool -- the end of a persistent stream of the
+ * "qwen3-tts-hip" README ("Library Usage"), whose KV capacity is fixed by
+ * max_cache_steps. */
 int q3tts_reset(q3tts_handle* h, int stream_id);
 
 /* Talker positions held by a stream (0 after reset), or a negative error. */
 int q3tts_stream_length(q3tts_handle* h, int stream_id);
 
 /* Waits for the handle's stream and reports any error recorded by a kernel
- * (Q3TTS_ERR_TIMEOUT for a device-side wait that gave up), or a CUDA error. */
+ * (Q3TTS_ERR_TIMEOUT for a device-side wait that gave up), or a CUDA error --
+ * the status-code counterpart of the Result every engine call of the
+ * "qwen3-tts-hip" README ("Library Usage") returns.  After a kernel error it
+ * clears the error word and the frame kernels' barrier words, so the next
+ * frame runs normally. */
 int q3tts_sync_status(q3tts_handle* h);
 
 /* Number of kernel launches this handle has issued since q3tts_create (a

@@ -96,3 +96,56 @@ def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(q3tts, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         q3tts.load(str(tmp_path / "libq3tts.so"))
+
+
+def _fake_weights(shape, base=1 << 40):
+    """Weights struct of distinct, 256-byte aligned fake addresses (never
+    dereferenced: the calls below must stop at their argument checks)."""
+    addr = [base]
+
+    def nxt():
+        addr[0] += 1 << 20
+        return addr[0]
+    tl = (q3tts.LayerWeights * shape.talker_layers)()
+    for i in range(shape.talker_layers):
+        tl[i] = q3tts.LayerWeights(*[nxt() for _ in q3tts.LAYER_KEYS])
+    cl = (q3tts.LayerWeights * shape.cp_layers)()
+    for i in range(shape.cp_layers):
+        cl[i] = q3tts.LayerWeights(*[nxt() for _ in q3tts.LAYER_KEYS])
+    w = q3tts.Weights(tl, nxt(), nxt(), nxt(), cl, nxt(), nxt(), nxt(),
+                      nxt() if shape.has_proj else None)
+    return w, tl, cl
+
+
+def test_create_rejects_unaligned_weight_pointers(lib):
+    """Every weight and gain pointer must be 16-byte aligned (the kernels read
+    them with 16-byte vector loads and bulk copies): an 8-byte offset in any one
+    of them is Q3TTS_ERR_ARG, returned before anything touches the device."""
+    import torch
+    from autoregressive_tts_decode_gb300 import synth
+    L = q3tts.load(build.LIB)
+    shape = synth.SHAPE_17B
+    cfg = q3tts.make_config(shape, 1, 512)
+    ws = ctypes.c_void_p(1 << 41)
+    top = ["talker_g_final", "talker_w_head", "talker_e_codec", "cp_g_final", "cp_heads",
+           "cp_embeds", "cp_w_proj"]
+    cases = [(None, f) for f in top] + [("talker", k) for k in q3tts.LAYER_KEYS] + \
+            [("cp", k) for k in q3tts.LAYER_KEYS]
+    for where, field in cases:
+        w, tl, cl = _fake_weights(shape)
+        if where is None:
+            setattr(w, field, getattr(w, field) + 8)
+        else:
+            arr = tl if where == "talker" else cl
+            setattr(arr[len(arr) - 1], field, getattr(arr[len(arr) - 1], field) + 8)
+        h = ctypes.c_void_p()
+        rc = L.q3tts_create(ctypes.byref(cfg), ctypes.byref(w), ws, 1 << 60, None, ctypes.byref(h))
+        assert rc == q3tts.ERR_ARG, (where, field, rc)
+        assert not h.value
+    if not torch.cuda.is_available():
+        # the aligned set passes the argument checks and stops at the first
+        # CUDA call, which fails here for want of a device
+        w, tl, cl = _fake_weights(shape)
+        h = ctypes.c_void_p()
+        rc = L.q3tts_create(ctypes.byref(cfg), ctypes.byref(w), ws, 1 << 60, None, ctypes.byref(h))
+        assert rc == q3tts.ERR_CUDA
