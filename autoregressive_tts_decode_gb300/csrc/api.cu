@@ -24,6 +24,7 @@ int frame_kernel_static_check(const q3tts_handle* h, const q3tts_sampling& sp);
 int frame_kernel_step_static(q3tts_handle* h, int sid, int pos, int newpage, const q3tts_sampling& sp,
                              const float* uniforms, int32_t* codes, const int32_t* forced, float* logits);
 int frame_kernel_recover_static(q3tts_handle* h);
+int frame_kernel_debug_fail(q3tts_handle* h, int barrier, int wait_us);
 }  // namespace q3
 
 namespace {
@@ -413,6 +414,11 @@ int q3tts_sync_status(q3tts_handle* h) {
 }
 
 uint64_t q3tts_kernel_launches(const q3tts_handle* h) { return h ? h->launches : 0; }
+
+int q3tts_debug_fail_barrier(q3tts_handle* h, int barrier, int wait_us) {
+  if (!h || barrier < 0 || wait_us < 1 || wait_us > 2000000) return Q3TTS_ERR_ARG;
+  return q3::frame_kernel_debug_fail(h, barrier, wait_us);
+}
 
 void q3tts_destroy(q3tts_handle* h) {
   if (!h) return;

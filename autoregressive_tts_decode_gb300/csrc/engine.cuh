@@ -68,6 +68,9 @@ struct q3tts_handle {
   char* fk_base;           // workspace region of the persistent frame kernel
   bool frame_kernel_off;   // Q3TTS_FRAME_KERNEL=0: always use the layered step
   bool used_static = false;   // q3tts_step_frame_static has run on this handle
+  // failure-path test (q3tts_debug_fail_barrier), armed for one persistent launch
+  int dbg_fail_bar = -1;
+  long long dbg_wait_cycles = 0;
   bool static_ready = false;  // per-stream page lists reserved for it
   uint64_t launches = 0;
   // the captured layered step (valid for g_n active streams, with or without

@@ -67,7 +67,7 @@ constexpr int FK_HDMAX = 128;
 constexpr int FK_REPMAX = 2;   // q heads per kv head
 constexpr int FK_MAXCTA = 256;
 constexpr int FK_PAIRS = 4;    // (head, token) pairs of one CTA in a CodePredictor attention
-constexpr long long FK_WAIT_CYCLES = 4000000000ll;  // ~2 s at GB300 clocks
+constexpr long long FK_WAIT_CYCLES = 4000000000ll;  // ~2 s at GB300 clocks: the default wait bound
 // Per-layer "side block" (norm gains g_attn | g_ffn | g_q | g_k, weight dtype),
 // copied into a double-buffered shared-memory slot one layer ahead.
 constexpr int FK_SIDE_BYTES = (2 * FK_DMAX + 2 * FK_HDMAX) * 4;
@@ -108,6 +108,8 @@ struct FKParams {
   unsigned* done;
   int* err;
   int* abort_flag;
+  long long wait_cycles;  // bound of every wait on another thread or CTA (clock64 cycles)
+  int fail_bar;           // grid barrier whose arrival CTA 0 skips (-1: none; failure-path test)
   // this call
   int sid, pos, newpage;
   q3tts_sampling sp;
@@ -408,7 +410,7 @@ __device__ __forceinline__ void wait_bar(Cons c, uint64_t* bar, unsigned par) {
   unsigned it = 0;
   bool ab = false;
   while (!mbar_try_wait(bar, par)) {
-    if ((++it & 255u) == 0 && (ld_volatile(fk_prm()->abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
+    if ((++it & 255u) == 0 && (ld_volatile(fk_prm()->abort_flag) || clock64() - t0 > fk_prm()->wait_cycles)) {
       ab = true;
       break;
     }
@@ -440,7 +442,9 @@ __device__ void grid_sync(Cons c) {
   consumer_sync();
   if (ctid() == 0) {
     const FKParams& p = *fk_prm();
-    red_release_add(p.bar, 1u);
+    // the failure-path test leaves one arrival out, so every CTA's wait below
+    // runs out of its bound
+    if (!(ccta() == 0 && cst().phase == (unsigned)p.fail_bar)) red_release_add(p.bar, 1u);
     cst().phase++;
     const unsigned target = cst().phase * (unsigned)p.ncta;
     int fail = cst().aborted ? 1 : 0;
@@ -448,7 +452,7 @@ __device__ void grid_sync(Cons c) {
       long long t0 = clock64();
       unsigned it = 0;
       while (ld_acquire(p.bar) < target) {
-        if ((++it & 63u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
+        if ((++it & 63u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > p.wait_cycles)) {
           raise_abort(p, Q3TTS_ERR_TIMEOUT);
           fail = 1;
           break;
@@ -513,7 +517,7 @@ __device__ __noinline__ bool chunk_wait_slow(uint32_t bar, unsigned par) {
   bool ab = false;
   uint64_t* b = reinterpret_cast<uint64_t*>(fk_smem_raw + bar);
   while (!mbar_try_wait(b, par)) {
-    if ((++it & 255u) == 0 && (ld_volatile(fk_prm()->abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
+    if ((++it & 255u) == 0 && (ld_volatile(fk_prm()->abort_flag) || clock64() - t0 > fk_prm()->wait_cycles)) {
       ab = true;
       break;
     }
@@ -1756,7 +1760,7 @@ struct Producer {
       // the ring is full most of the time: wait suspended so this warp does
       // not take issue slots from the consumer warps of its scheduler
       while (!mbar_try_wait_sleep(&sm->empty[s], par, 2000)) {
-        if ((++it & 15u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
+        if ((++it & 15u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > p.wait_cycles)) {
           raise_abort(p, Q3TTS_ERR_TIMEOUT);
           stop = true;
           return;
@@ -1785,6 +1789,7 @@ struct Producer {
 
   int nlayers = 0;  // layers in the frame (15 CodePredictor passes, then the Talker)
   int layer_i = 0;  // next layer whose weights are streamed
+  int side_last[2] = {-1, -1};  // last layer whose side block was copied into each slot
 
   __device__ const LayerDev& layer_at(int k) const {
     const int ncp = (Q3TTS_N_CODEBOOKS - 1) * p.Lc;
@@ -1800,7 +1805,7 @@ struct Producer {
       long long t0 = clock64();
       unsigned it = 0;
       while (!mbar_try_wait_sleep(&sm->side_empty[slot], par, 2000)) {
-        if ((++it & 15u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > FK_WAIT_CYCLES)) {
+        if ((++it & 15u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > p.wait_cycles)) {
           raise_abort(p, Q3TTS_ERR_TIMEOUT);
           stop = true;
           return;
@@ -1812,6 +1817,7 @@ struct Producer {
     const unsigned bytes = (unsigned)((2 * D + 2 * p.hd) * (int)sizeof(WT));
     mbar_expect_tx(&sm->side_full[slot], bytes);
     bulk_g2s(sm->side[slot], layer_at(k).side, bytes, &sm->side_full[slot], pol);
+    side_last[slot] = k;
   }
 
   __device__ void layer(const LayerDev& L, int D, int F) {
@@ -1836,11 +1842,15 @@ struct Producer {
     }
     for (int l = 0; l < p.Lt; ++l) layer(sm->lay[l], p.Dt, p.Ft);
     split_rows(p.t_head, p.Vt, p.Dt * esz);
-    // copies still in flight must land before the CTA may exit
-    for (int k = nlayers - 2; k < nlayers; ++k) {
+    // copies still in flight must land before the CTA may exit: the last
+    // side block copied into each slot (after an abort the producer stops
+    // early, so these need not be the frame's last two layers) and the last
+    // FK_NSTAGE ring chunks
+    for (int slot = 0; slot < 2; ++slot) {
+      const int k = side_last[slot];
       if (k < 0) continue;
       long long t0 = clock64();
-      while (!mbar_try_wait(&sm->side_full[k & 1], (k >> 1) & 1u))
+      while (!mbar_try_wait(&sm->side_full[slot], (k >> 1) & 1u))
         if (clock64() - t0 > FK_WAIT_CYCLES) break;
     }
     const uint32_t first = n > (uint32_t)FK_NSTAGE ? n - FK_NSTAGE : 0;
@@ -2112,6 +2122,8 @@ static void frame_params(FKParams& p, const q3tts_handle* h, int sid, int pos, i
   p.R = st->R; p.dA = st->dA; p.dF = st->dF; p.qkv = st->qkv; p.part = st->part;
   p.cp_logits = st->cp_logits;
   p.bar = st->bar; p.done = st->done; p.err = h->d_err; p.abort_flag = st->abort_flag;
+  p.wait_cycles = h->dbg_wait_cycles > 0 ? h->dbg_wait_cycles : FK_WAIT_CYCLES;
+  p.fail_bar = h->dbg_fail_bar;
   p.sid = sid; p.pos = pos; p.newpage = newpage; p.sp = sp;
   p.uniforms = uniforms; p.codes = codes; p.forced = forced; p.dump = logits;
 }
@@ -2121,6 +2133,8 @@ static int frame_launch(q3tts_handle* h, FKParams& p) {
   cudaError_t e = cudaLaunchCooperativeKernel(pick_kernel(h->c.weight_dtype, h->c.kv_dtype),
                                               dim3(h->fk->ncta), dim3(FK_THREADS), args, h->fk->smem, h->s);
   h->launches += 1;
+  h->dbg_fail_bar = -1;  // an armed failure-path test covers one launch
+  h->dbg_wait_cycles = 0;
   return e == cudaSuccess ? Q3TTS_OK : Q3TTS_ERR_CUDA;
 }
 
@@ -2129,6 +2143,14 @@ int frame_kernel_step(q3tts_handle* h, const StepDesc& d, const float* uniforms,
   FKParams p;
   frame_params(p, h, d.sid[0], d.pos[0], d.newpage[0], d.sp[0], uniforms, codes, forced, logits);
   return frame_launch(h, p);
+}
+
+// Arms the failure-path test for the handle's next persistent launch.
+int frame_kernel_debug_fail(q3tts_handle* h, int barrier, int wait_us) {
+  if (!h->fk || !h->fk->ok) return Q3TTS_ERR_UNSUPPORTED;
+  h->dbg_fail_bar = barrier;
+  h->dbg_wait_cycles = (long long)wait_us * 2070;  // clock64 ticks at the highest SM clock
+  return Q3TTS_OK;
 }
 
 // After a device-side error: clear the barrier counters and the abort flag.

@@ -60,7 +60,7 @@ class Sampling(C.Structure):
 EXPORTS = ("q3tts_workspace_size", "q3tts_create", "q3tts_prefill", "q3tts_step_frame",
            "q3tts_read_pending", "q3tts_reset", "q3tts_stream_length", "q3tts_sync_status",
            "q3tts_kernel_launches", "q3tts_destroy", "q3tts_strerror",
-           "q3tts_step_frame_static")
+           "q3tts_step_frame_static", "q3tts_debug_fail_barrier")
 
 _lib = None
 
@@ -89,6 +89,7 @@ def load(path: str = LIB_PATH):
     L.q3tts_destroy.argtypes = [vp]
     L.q3tts_kernel_launches.restype = C.c_uint64
     L.q3tts_kernel_launches.argtypes = [vp]
+    L.q3tts_debug_fail_barrier.argtypes = [vp, C.c_int, C.c_int]
     L.q3tts_strerror.restype = C.c_char_p
     L.q3tts_strerror.argtypes = [C.c_int]
     _lib = L
@@ -252,6 +253,12 @@ class Engine:
 
     def kernel_launches(self) -> int:
         return int(load().q3tts_kernel_launches(self.h))
+
+    def debug_fail_barrier(self, barrier: int, wait_us: int) -> None:
+        """Arms the next persistent frame to leave out CTA 0's arrival at grid
+        barrier `barrier` with every wait bounded to wait_us (failure-path test)."""
+        _check(load().q3tts_debug_fail_barrier(self.h, int(barrier), int(wait_us)),
+               "q3tts_debug_fail_barrier")
 
     def sync(self) -> None:
         _check(load().q3tts_sync_status(self.h), "q3tts_sync_status")

@@ -248,6 +248,23 @@ int q3tts_sync_status(q3tts_handle* h);
  * diagnostic for launch-overhead accounting). */
 uint64_t q3tts_kernel_launches(const q3tts_handle* h);
 
+/* Test hook for the failure path (no counterpart in the method's
+ * description): arms the handle's next persistent-kernel frame
+ * (q3tts_step_frame with one stream, or q3tts_step_frame_static) so that CTA 0
+ * leaves out its arrival at grid barrier `barrier` (0-based, in frame order)
+ * and every device-side wait of that frame gives up after about wait_us
+ * microseconds.  No GPU fault, trap or endless wait is involved: the other
+ * CTAs' bounded waits run out, the kernel records Q3TTS_ERR_TIMEOUT, raises
+ * its abort flag, lets its in-flight copies land and returns.
+ * q3tts_sync_status then returns Q3TTS_ERR_TIMEOUT and clears the error and
+ * barrier words; the decoded stream's state is undefined (prefill it again),
+ * every other stream and the handle stay usable.  A barrier index past the
+ * frame's last barrier arms nothing that fires, and the frame runs normally.
+ * The arming covers exactly one launch.  Q3TTS_ERR_ARG for barrier < 0 or
+ * wait_us outside 1..2,000,000; Q3TTS_ERR_UNSUPPORTED if this handle has no
+ * persistent frame kernel. */
+int q3tts_debug_fail_barrier(q3tts_handle* h, int barrier, int wait_us);
+
 void q3tts_destroy(q3tts_handle* h);
 
 const char* q3tts_strerror(int code);
