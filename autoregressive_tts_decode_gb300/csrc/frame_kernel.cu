@@ -58,9 +58,11 @@ namespace q3 {
 constexpr int FK_CONSUMER_WARPS = 8;
 constexpr int FK_CONSUMERS = FK_CONSUMER_WARPS * 32;
 constexpr int FK_PRODUCER_THREADS = 32;  // one warp; one thread issues the copies
-constexpr int FK_THREADS = FK_PRODUCER_THREADS + FK_CONSUMERS;
-constexpr int FK_STAGE = 12288;  // one ring chunk: 3 rows of 2048 bf16, one 2048-wide FFN unit
-constexpr int FK_NSTAGE = 11;
+constexpr int FK_PREFETCH_THREADS = 32;  // one warp; one thread issues L2 prefetches
+constexpr int FK_THREADS = FK_PRODUCER_THREADS + FK_CONSUMERS + FK_PREFETCH_THREADS;
+constexpr int FK_STAGE = 8192;  // one ring chunk: 2 rows of 2048 bf16, one o_proj tile of 32 x 128 bf16
+constexpr int FK_NSTAGE = 20;
+constexpr int FK_PF_AHEAD = 40;  // chunks the L2 prefetch runs ahead of the ring's copies
 constexpr int FK_TMAX = 2;     // tokens per pass (CodePredictor pass 0 carries two)
 constexpr int FK_DMAX = 2048;  // widest hidden state staged in shared memory
 constexpr int FK_HDMAX = 128;
@@ -70,13 +72,14 @@ constexpr int FK_PAIRS = 4;    // (head, token) pairs of one CTA in a CodePredic
 constexpr long long FK_WAIT_CYCLES = 4000000000ll;  // ~2 s at GB300 clocks: the default wait bound
 // Per-layer "side block" (norm gains g_attn | g_ffn | g_q | g_k, weight dtype),
 // copied into a double-buffered shared-memory slot one layer ahead.
-constexpr int FK_SIDE_BYTES = (2 * FK_DMAX + 2 * FK_HDMAX) * 4;
+// Largest over the configurations the kernel takes (bf16 at D = 2048, fp32 at
+// D <= 1024); checked at create.
+constexpr int FK_SIDE_BYTES = 9216;
+constexpr int FK_FIN_BYTES = 8192;  // final-norm gains of both stacks
 constexpr int FK_MAXLAYERS = 64;  // Talker + CodePredictor layers held in shared memory
-constexpr int FK_GROUP = 3;       // rows one warp keeps in registers in a row GEMV
-constexpr int FK_YCOLS = 64;      // FFN output columns of one lane over a gang (2048 / 32)
-constexpr int FK_GANG = 2;        // warps that stream one ring chunk together
-constexpr int FK_NGANG = FK_CONSUMER_WARPS / FK_GANG;
-constexpr int FK_XCH = 64;        // floats one gang exchanges per chunk (rows x tokens, or a tile's columns)
+constexpr int FK_RMAX = 8;        // rows of one ring chunk a warp keeps in flight
+constexpr int FK_KC = 4;          // copies of each residual buffer the split-K sums are spread over
+constexpr int FK_UMAX = 64;       // FFN units of one CTA
 
 static_assert(FAST_NT == FK_CONSUMERS, "the register sampler runs on the consumer warps");
 
@@ -84,7 +87,8 @@ struct LayerDev {
   const void* side;   // [g_attn D | g_ffn D | g_q hd | g_k hd], weight dtype, contiguous
   const void* w_qkv;
   const void* w_oT;   // o_proj tiles [Hq][ceil(D/32)][hd/8][32][8] (see oproj_tiles)
-  const void* w_ffn;  // [F][3][D]: FFN unit f = gate row f, up row f, column f of W_down
+  const void* w_gu;   // [2F][D]: gate rows, then up rows (the caller's tensor)
+  const void* w_dT;   // [F][D]: W_down transposed, row f = column f of W_down
 };
 
 struct FKParams {
@@ -100,7 +104,8 @@ struct FKParams {
   KVDesc tkv, ckv;
   const float* rope_cos;
   const float* rope_sin;
-  float *R, *dA, *dF;  // [2][FK_TMAX][dmax] each
+  float *R, *dA, *dF;  // [FK_KC][xstride] each: copies of [tokens][D]
+  int xstride;
   float* qkv;          // [FK_TMAX][qkv_rows]
   float* part;         // [Hq][cpg][hd + 2]
   float* cp_logits;    // [Vc]
@@ -159,6 +164,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* b) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive_n(uint64_t* b, unsigned n) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(n) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, unsigned parity) {
   unsigned ok;
   asm volatile(
@@ -201,6 +210,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
       : "memory");
 }
 
+// Moves bytes at src (16-byte aligned, a multiple of 16) towards L2 ahead of
+// their copy into shared memory.
+__device__ __forceinline__ void prefetch_l2(const void* src, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(FK_CONSUMERS) : "memory");
 }
@@ -229,8 +244,8 @@ __device__ __forceinline__ void split(int n, int parts, int i, int& lo, int& hi)
 }
 
 __device__ __forceinline__ int rows_per_chunk(int row_bytes) {
-  int r = FK_STAGE / row_bytes;
-  return r < 1 ? 1 : r;
+  const int r = FK_STAGE / row_bytes;
+  return r < 1 ? 1 : (r > FK_RMAX ? FK_RMAX : r);
 }
 
 // Activations staged for a GEMV use a "plane" layout so that lane reads of 8
@@ -301,19 +316,18 @@ struct FKSmem {
   // whatever the size of the fields before them.
   union alignas(16) {
     struct {
-      float xs[FK_TMAX * FK_DMAX];      // normed activations of the current GEMV (plane layout)
-      float yred[32 * FK_YCOLS];        // FFN output of the CTA, lane-transposed (see phase_ffn)
+      float xs[FK_TMAX * FK_DMAX];      // staged activations of the current GEMV (plane layout)
     } g;
     FastSamplerSmem smp;
     AttnScratch att;
   } u;
   alignas(16) float os[2][FK_TMAX][FK_HDMAX];  // attention outputs of the CTA's (<= 2) heads, plane layout
   alignas(16) float red[FK_TMAX][FK_CONSUMER_WARPS];
-  alignas(16) float xch[FK_NGANG][2][FK_GANG * FK_XCH];  // a gang's partial sums per warp (double-buffered by chunk)
+  alignas(16) float act[FK_TMAX][FK_UMAX];  // the CTA's FFN activations silu(gate) * up
   alignas(16) float rope_c[17][FK_HDMAX / 2];  // rows 0..15: CodePredictor positions; 16: the Talker position
   alignas(16) float rope_s[17][FK_HDMAX / 2];
   alignas(128) unsigned char side[2][FK_SIDE_BYTES];
-  alignas(16) unsigned char fin[2 * FK_DMAX * 4];  // final-norm gains: CodePredictor then Talker
+  alignas(16) unsigned char fin[FK_FIN_BYTES];  // final-norm gains: CodePredictor then Talker
   float uni[Q3TTS_N_CODEBOOKS];
   int forced[Q3TTS_N_CODEBOOKS];
   int fedc[Q3TTS_N_CODEBOOKS];  // the frame's codes fed forward so far
@@ -324,10 +338,14 @@ struct FKSmem {
   alignas(8) uint64_t side_full[2];
   alignas(8) uint64_t side_empty[2];
   int flag;
+  uint32_t pf_gate;  // chunks the ring's producer has issued (read by the prefetch warp)
   ConsState cs[FK_CONSUMER_WARPS];
+#ifdef Q3TTS_TRACE
+  int trace_n;
+#endif
 };
 static_assert(sizeof(FKSmem) <= 227 * 1024, "persistent kernel shared memory");
-static_assert(offsetof(FKSmem, u) % 16 == 0 && offsetof(FKSmem, os) % 16 == 0 && offsetof(FKSmem, xch) % 16 == 0 &&
+static_assert(offsetof(FKSmem, u) % 16 == 0 && offsetof(FKSmem, os) % 16 == 0 && offsetof(FKSmem, act) % 16 == 0 &&
                   offsetof(FKSmem, fin) % 16 == 0 && offsetof(FKSmem, side) % 16 == 0,
               "vector-accessed shared-memory arrays are 16-byte aligned");
 
@@ -398,6 +416,30 @@ struct ConsGroup {
   __device__ static void sync() { consumer_sync(); }
 };
 
+// Phase timestamps for profiling builds (compiled only with -DQ3TTS_TRACE):
+// consumer thread 0 of each CTA appends {globaltimer, clock64, tag, aux} to
+// the CTA's row of fk_trace_buf.  Without the define FK_MARK is empty.
+#ifdef Q3TTS_TRACE
+constexpr int FK_TRACE_EV = 8192;
+__device__ uint4 fk_trace_buf[FK_MAXCTA * FK_TRACE_EV];
+__device__ __forceinline__ void fk_mark(int tag, int aux) {
+  if (ctid() != 0) return;
+  int& n = fk_sm()->trace_n;
+  if (n >= FK_TRACE_EV) return;
+  unsigned long long g;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g));
+  const unsigned long long c = clock64();
+  fk_trace_buf[blockIdx.x * FK_TRACE_EV + n] =
+      make_uint4((unsigned)g, (unsigned)(g >> 32), (unsigned)c, ((unsigned)tag << 16) | ((unsigned)aux & 0xffffu));
+  n++;
+}
+#define FK_MARK(tag, aux) fk_mark(tag, aux)
+#else
+#define FK_MARK(tag, aux) ((void)0)
+#endif
+enum { TR_STEP = 1, TR_NORM = 2, TR_ARRIVE = 3, TR_PASS = 4, TR_WAIT0 = 5, TR_WAIT1 = 6, TR_END = 7,
+       TR_CW0 = 8, TR_CW1 = 9, TR_REL = 10, TR_SUB = 11 };
+
 __device__ __forceinline__ void raise_abort(const FKParams& p, int code) {
   atomicCAS(p.err, 0, code);
   atomicExch(p.abort_flag, 1);
@@ -440,6 +482,7 @@ __device__ __forceinline__ void side_end(Cons c) {
 // launch resets it).
 __device__ void grid_sync(Cons c) {
   consumer_sync();
+  FK_MARK(TR_ARRIVE, 0);
   if (ctid() == 0) {
     const FKParams& p = *fk_prm();
     // the failure-path test leaves one arrival out, so every CTA's wait below
@@ -462,49 +505,38 @@ __device__ void grid_sync(Cons c) {
     fk_sm()->flag = fail;
   }
   consumer_sync();
+  FK_MARK(TR_PASS, 0);
   if (fk_sm()->flag) warp_set(cst().aborted, 1);
 }
 
 // ------------------------------------------------------------ streaming
 //
-// Ring chunk n belongs to gang n % 4 -- a pair of consumer warps that stream
-// it together, each taking every other 256-wide block of the reduction (or
-// every other hd block of an o_proj tile), meeting once per chunk through a
-// named barrier of the pair and a small exchange buffer.  No block-wide
-// synchronisation happens inside a streaming loop.  A streaming loop keeps
-// what it touches per chunk in registers (the Stream state, hoisted pointers).
+// A ring chunk is consumed in one of two ways.  A private chunk (rows of a
+// GEMV, an o_proj tile, the gate and up rows of a few FFN units) belongs to
+// warp n % 8, which computes whole dot products over it alone: no exchange
+// between warps and no barrier inside a streaming loop.  A shared chunk (rows
+// of the transposed down projection) is read by every warp, each for its own
+// output columns.  A slot's "empty" barrier expects FK_CONSUMER_WARPS
+// arrivals: the owner of a private chunk arrives with that count, every warp
+// once for a shared chunk.  A streaming loop keeps what it touches per chunk
+// in registers.
 
 struct Stream {
-  int lane, gang, j;  // j: the warp's place in its gang
+  int lane, warp;
   bool aborted;
-  const int* abort_flag;
-  int* err;
 };
 
 __device__ __forceinline__ Stream stream_begin(Cons c) {
   Stream s;
   s.lane = clane();
-  s.gang = cwarp() / FK_GANG;
-  s.j = cwarp() % FK_GANG;
+  s.warp = cwarp();
   s.aborted = cst().aborted;
-  s.abort_flag = fk_prm()->abort_flag;
-  s.err = fk_prm()->err;
   return s;
 }
 
-// The gang's named barrier (ids 2..5; 0 is __syncthreads, 1 the consumers').
-__device__ __forceinline__ void gang_sync(const Stream& s) {
-  asm volatile("bar.sync %0, %1;" ::"r"(2 + s.gang), "n"(FK_GANG * 32) : "memory");
-}
-
-// The gang's first chunk at or after n0.
-__device__ __forceinline__ uint32_t first_chunk(uint32_t n0, int gang) {
-  return n0 + (uint32_t)((gang - (int)(n0 % FK_NGANG) + FK_NGANG) % FK_NGANG);
-}
-
-// Exchange buffer of chunk n for the gang (alternates between two).
-__device__ __forceinline__ float* xch_buf(const Stream& s, uint32_t n) {
-  return fk_sm()->xch[s.gang][(n / FK_NGANG) & 1];
+// The warp's first private chunk at or after n0.
+__device__ __forceinline__ uint32_t first_chunk(uint32_t n0, int warp) {
+  return n0 + (uint32_t)((warp - (int)(n0 % FK_CONSUMER_WARPS) + FK_CONSUMER_WARPS) % FK_CONSUMER_WARPS);
 }
 
 // The slow path of chunk_wait (out of line: it keeps the streaming loops'
@@ -533,19 +565,26 @@ __device__ __forceinline__ uint32_t chunk_wait(Stream& s, uint32_t n) {
   const uint32_t slot = n % FK_NSTAGE;
   if (!s.aborted) {
     const unsigned par = (n / FK_NSTAGE) & 1u;
-    if (!__all_sync(0xffffffffu, mbar_try_wait(&sm->full[slot], par)))
+    if (!__all_sync(0xffffffffu, mbar_try_wait(&sm->full[slot], par))) {
+      FK_MARK(TR_WAIT0, (int)n);
       s.aborted = chunk_wait_slow(soff(&sm->full[slot]), par);
+      FK_MARK(TR_WAIT1, (int)n);
+    }
   }
   return soff(sm->ring[slot]);
 }
 
-// Hands ring chunk n back to the producer: one arrival, from the gang's first
-// warp after the gang's last barrier of the chunk (so both warps are done with
-// it).  After an abort a consumer has stopped waiting for data, so it must not
-// free slots either: the producer then blocks, sees the abort flag and lets
-// its in-flight copies land before the CTA can exit.
-__device__ __forceinline__ void chunk_release(const Stream& s, uint32_t n) {
-  if (s.j == 0 && s.lane == 0 && !s.aborted) mbar_arrive(&fk_sm()->empty[n % FK_NSTAGE]);
+// Hands ring chunk n back to the producer once the whole warp is done with it.
+// After an abort a consumer has stopped waiting for data, so it must not free
+// slots either: the producer then blocks, sees the abort flag and lets its
+// in-flight copies land before the CTA can exit.
+__device__ __forceinline__ void release_private(const Stream& s, uint32_t n) {
+  __syncwarp();
+  if (s.lane == 0 && !s.aborted) mbar_arrive_n(&fk_sm()->empty[n % FK_NSTAGE], FK_CONSUMER_WARPS);
+}
+__device__ __forceinline__ void release_shared(const Stream& s, uint32_t n) {
+  __syncwarp();
+  if (s.lane == 0 && !s.aborted) mbar_arrive_n(&fk_sm()->empty[n % FK_NSTAGE], 1u);
 }
 
 // 8 weights at shared offset w times 8 activations (plane halves xa, xb) into
@@ -558,125 +597,138 @@ __device__ __forceinline__ void fma8(uint32_t w, const float4& xa, const float4&
   b = fmaf(wv[4], xb.x, b); b = fmaf(wv[5], xb.y, b); b = fmaf(wv[6], xb.z, b); b = fmaf(wv[7], xb.w, b);
 }
 
-// The activations a warp multiplies for one token: warp j of a gang owns the
-// 256-wide blocks i = j, j + 2, j + 4, j + 6 of the reduction (K <= 2048, the
-// block holding the ragged tail K % 256 included); lane l holds elements
-// 8 l + 256 i .. + 7 of block slot b (i = 2 b + j) as a[b] (first four) and
-// c[b] (last four).  Lanes past a ragged tail hold zeros and are masked out.
-constexpr int FK_XB = 4;  // block slots per warp
-struct XReg {
-  float4 a[FK_XB], c[FK_XB];
-};
-
-// Which of the warp's block slots have weights for this lane (bit b).
-__device__ __forceinline__ unsigned xblocks(int K, int lane, int j) {
-  const int nfull = K >> 8;
-  unsigned m = 0;
-#pragma unroll
-  for (int b = 0; b < FK_XB; ++b) {
-    const int i = FK_GANG * b + j;
-    if (i < nfull || (i == nfull && lane * 8 < (K & 255))) m |= 1u << b;
-  }
-  return m;
-}
-
-// Loads the warp's blocks of the plane-layout vector at shared offset xt.
-__device__ __forceinline__ void load_xreg(XReg& x, uint32_t xt, int K, int lane, int j, unsigned m) {
-#pragma unroll
-  for (int b = 0; b < FK_XB; ++b) {
-    const uint32_t o = xt + (uint32_t)(lane * 16 + (FK_GANG * b + j) * 512);
-    x.a[b] = (m >> b) & 1u ? lds_f4(o) : make_float4(0.f, 0.f, 0.f, 0.f);
-    x.c[b] = (m >> b) & 1u ? lds_f4(o + (uint32_t)K * 2u) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-}
-
-// 8 weights at shared offset w times the 8 activations (a, c) into acc.
-template <class WT>
-__device__ __forceinline__ float dot8w(uint32_t w, const float4& a, const float4& c, float acc) {
-  float wv[8];
-  lds_w8<WT>(w, wv);
-  float s = fmaf(wv[0], a.x, fmaf(wv[1], a.y, fmaf(wv[2], a.z, wv[3] * a.w)));
-  const float s2 = fmaf(wv[4], c.x, fmaf(wv[5], c.y, fmaf(wv[6], c.z, wv[7] * c.w)));
+// acc + w . (a, c): two short chains of four, then one add.
+__device__ __forceinline__ float dot8(const float (&w)[8], const float4& a, const float4& c, float acc) {
+  const float s = fmaf(w[0], a.x, fmaf(w[1], a.y, fmaf(w[2], a.z, w[3] * a.w)));
+  const float s2 = fmaf(w[4], c.x, fmaf(w[5], c.y, fmaf(w[6], c.z, w[7] * c.w)));
   return acc + (s + s2);
 }
 
-// This warp's partial dot products of the FK_GROUP rows at shared offsets
-// w + ro[r] with its activation blocks; warp-reduced, in every lane.
-template <class WT>
-__device__ __forceinline__ void rows_part(uint32_t w, const uint32_t (&ro)[FK_GROUP], const XReg& x, unsigned m,
-                                          int lane, int j, float (&out)[FK_GROUP]) {
-  float acc[FK_GROUP];
+// Dot products of NR rows of a chunk at shared offset w (row i at w + ro[i];
+// K elements each) with the T staged vectors at shared offset xs (plane
+// layout, token t at xs + 4 K t): acc[i][t], the full sums in every lane.
+// Lane l takes elements 256 b + 8 l .. + 7 of each 256-wide block b (lanes past
+// a ragged last block take none); a block's activations are loaded once for
+// all rows, and the NR T sums are reduced together so that their shuffle
+// chains overlap.  NR and T are compile-time: a guard on a runtime row count
+// inside an unrolled loop would issue the skipped rows' instructions anyway.
+template <class WT, int T, int NR>
+__device__ __forceinline__ void dots(uint32_t w, const uint32_t (&ro)[NR], int K, uint32_t xs, int lane,
+                                     float (&acc)[NR][T]) {
 #pragma unroll
-  for (int r = 0; r < FK_GROUP; ++r) acc[r] = 0.f;
+  for (int r = 0; r < NR; ++r)
+#pragma unroll
+    for (int t = 0; t < T; ++t) acc[r][t] = 0.f;
   const uint32_t wl = w + (uint32_t)(lane * 8 * (int)sizeof(WT));
+  const uint32_t xl = xs + (uint32_t)(lane * 16);
+  const int nb = (K >> 8) + (lane * 8 < (K & 255) ? 1 : 0);  // blocks with elements of this lane
+  for (int b = 0; b < nb; ++b) {
+    float4 xa[T], xc[T];
 #pragma unroll
-  for (int b = 0; b < FK_XB; ++b) {
-    if ((m >> b) & 1u) {
-      const uint32_t wb = wl + (uint32_t)((FK_GANG * b + j) * 256 * (int)sizeof(WT));
+    for (int t = 0; t < T; ++t) {
+      const uint32_t o = xl + (uint32_t)(b * 512 + t * K * 4);
+      xa[t] = lds_f4(o);
+      xc[t] = lds_f4(o + (uint32_t)K * 2u);
+    }
+    const uint32_t wb = wl + (uint32_t)(b * 256 * (int)sizeof(WT));
 #pragma unroll
-      for (int r = 0; r < FK_GROUP; ++r) acc[r] = dot8w<WT>(wb + ro[r], x.a[b], x.c[b], acc[r]);
+    for (int r = 0; r < NR; ++r) {
+      float wv[8];
+      lds_w8<WT>(wb + ro[r], wv);
+#pragma unroll
+      for (int t = 0; t < T; ++t) acc[r][t] = dot8(wv, xa[t], xc[t], acc[r][t]);
     }
   }
 #pragma unroll
-  for (int r = 0; r < FK_GROUP; ++r) out[r] = warp_sum(acc[r]);
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+      for (int t = 0; t < T; ++t) acc[r][t] += __shfl_xor_sync(0xffffffffu, acc[r][t], o);
+}
+
+// Rows base + r0 .. base + r0 + NR - 1 of a chunk (row stride rb) against T
+// tokens, stored as out[t * ts + row] = inv_t (row . x_t) by lane r T + t (the
+// stores go out together); with zero_stride > 0 the same element of the
+// residual copies 1 .. FK_KC - 1 is cleared too.
+template <class WT, int T, int NR>
+__device__ __forceinline__ void rows_group(uint32_t buf, int rb, int r0, int K, uint32_t xs, int lane, float* out,
+                                           int ts, int base, const float (&inv)[T], int zero_stride) {
+  uint32_t ro[NR];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) ro[r] = (uint32_t)((r0 + r) * rb);
+  float acc[NR][T];
+  dots<WT, T, NR>(buf, ro, K, xs, lane, acc);
+#pragma unroll
+  for (int r = 0; r < NR; ++r)
+#pragma unroll
+    for (int t = 0; t < T; ++t)
+      if (lane == r * T + t) {
+        float* o = out + t * ts + base + r0 + r;
+        *o = acc[r][t] * inv[t];
+        if (zero_stride)
+#pragma unroll
+          for (int k = 1; k < FK_KC; ++k) o[k * zero_stride] = 0.f;
+      }
 }
 
 // Rows [r0, r1) of a row-major [*, K] matrix streamed from the ring (the
-// chunks the producer cut them into) against T plane-layout vectors at shared
-// offset xs (token t at xs + 4 K t): out[t * ts + row] = row . x_t.  Rows go
-// FK_GROUP at a time (a short last group repeats its last row and drops the
-// copies); the two warps of a gang post their halves to the exchange buffer
-// and the first warp's lane 0 stores the sums.  Advances the ring position
-// past the rows' chunks.
-template <class WT>
-__device__ __forceinline__ void stream_rows(Cons c, int r0, int r1, int K, int T, uint32_t xs, float* out, int ts) {
+// private chunks the producer cut them into) against T staged vectors at
+// shared offset xs: out[t * ts + row] = inv_t (row . x_t).  With zero_stride >
+// 0, out is copy 0 of a residual buffer and the same element of its other
+// FK_KC - 1 copies (zero_stride floats apart) is cleared.  A chunk's rows go
+// in groups of 4, then 2, then 1.  Advances the ring position past the rows'
+// chunks.
+template <class WT, int T>
+__device__ __forceinline__ void stream_rows_t(Cons c, int r0, int r1, int K, uint32_t xs, float* out, int ts,
+                                              const float (&inv)[T], int zero_stride) {
   Stream s = stream_begin(c);
   const int rb = K * (int)sizeof(WT);
   const int rpc = rows_per_chunk(rb);
   const uint32_t n0 = cst().n;
   const uint32_t nch = r1 > r0 ? (uint32_t)((r1 - r0 + rpc - 1) / rpc) : 0u;
-  const unsigned m = xblocks(K, s.lane, s.j);
-  for (uint32_t n = first_chunk(n0, s.gang); n < n0 + nch; n += FK_NGANG) {
+  for (uint32_t n = first_chunk(n0, s.warp); n < n0 + nch; n += FK_CONSUMER_WARPS) {
     const uint32_t buf = chunk_wait(s, n);
     const int base = r0 + (int)(n - n0) * rpc, R = min(rpc, r1 - base);
-    float* xb = xch_buf(s, n);
-    for (int t = 0; t < T; ++t) {
-      XReg x;
-      load_xreg(x, xs + (uint32_t)(t * K * 4), K, s.lane, s.j, m);
-      for (int r = 0; r < R; r += FK_GROUP) {
-        const int cnt = min(FK_GROUP, R - r);  // rows past R repeat row R - 1
-        uint32_t ro[FK_GROUP];
-#pragma unroll
-        for (int g = 0; g < FK_GROUP; ++g) ro[g] = (uint32_t)(min(g, cnt - 1) * rb);
-        float o[FK_GROUP];
-        rows_part<WT>(buf + (uint32_t)(r * rb), ro, x, m, s.lane, s.j, o);
-        if (s.lane == 0) {
-#pragma unroll
-          for (int g = 0; g < FK_GROUP; ++g)
-            if (g < cnt) xb[s.j * FK_XCH + (r + g) * T + t] = o[g];
-        }
-      }
+    int r = 0;
+    for (; r + 4 <= R; r += 4) rows_group<WT, T, 4>(buf, rb, r, K, xs, s.lane, out, ts, base, inv, zero_stride);
+    if (r + 2 <= R) {
+      rows_group<WT, T, 2>(buf, rb, r, K, xs, s.lane, out, ts, base, inv, zero_stride);
+      r += 2;
     }
-    gang_sync(s);
-    if (s.j == 0 && s.lane == 0)
-      for (int row = 0, i = 0; row < R; ++row)
-        for (int t = 0; t < T; ++t, ++i) out[t * ts + base + row] = xb[i] + xb[FK_XCH + i];
-    chunk_release(s, n);
+    if (r < R) rows_group<WT, T, 1>(buf, rb, r, K, xs, s.lane, out, ts, base, inv, zero_stride);
+    release_private(s, n);
   }
   warp_set(cst().aborted, s.aborted ? 1 : 0);
   warp_set(cst().n, n0 + nch);
 }
 
+template <class WT>
+__device__ __forceinline__ void stream_rows(Cons c, int r0, int r1, int K, int T, uint32_t xs, float* out, int ts,
+                                            float inv0, float inv1, int zero_stride) {
+  if (T == 1) {
+    const float inv[1] = {inv0};
+    stream_rows_t<WT, 1>(c, r0, r1, K, xs, out, ts, inv, zero_stride);
+  } else {
+    const float inv[2] = {inv0, inv1};
+    stream_rows_t<WT, 2>(c, r0, r1, K, xs, out, ts, inv, zero_stride);
+  }
+}
+
 // ------------------------------------------------------- residual helpers
 
-// Residual stream: three rotating buffers X0..X2 ([FK_TMAX][dmax] each).  A
-// layer whose input sits in X_i folds it (each CTA its slice) into both
-// X_{i+1} and X_{i+2}; attention output is added into both, the FFN output
-// into X_{i+2}, which is the next layer's input.  So every phase reads one
-// complete vector: phase A reads X_i, phase C reads X_{i+1}.
-__device__ __forceinline__ float* xbuf(const FKParams& p, int idx, int t) {
+// Residual stream: three rotating buffers X0..X2, each FK_KC copies of
+// [tokens][D] (D the width of the stack running; copy stride p.xstride
+// floats).  A buffer's value is the sum of its copies: the split-K partial
+// sums of all CTAs are added into copy (CTA % FK_KC), so that fewer CTAs add
+// into any one cache line.  A layer whose input sits in X_i folds it (each
+// CTA its slice) into copy 0 of X_{i+1} and X_{i+2} and clears their other
+// copies there; attention output is added into both, the FFN output into
+// X_{i+2}, which is the next layer's input.  So every phase reads one complete
+// vector: phase A reads X_i, phase C reads X_{i+1}.
+__device__ __forceinline__ float* xbuf(const FKParams& p, int idx, int copy) {
   float* base = idx == 0 ? p.R : (idx == 1 ? p.dA : p.dF);
-  return base + (size_t)t * p.dmax;
+  return base + (size_t)copy * p.xstride;
 }
 __device__ __forceinline__ int xnext(int i, int k) { return (i + k) % 3; }
 
@@ -701,32 +753,59 @@ __device__ __forceinline__ void cta_slice(int D, int& lo, int& hi) {
   hi = D * (cta + 1) / nc;
 }
 
-// Builds xs[t] = RMSNorm(x_t) * g (plane layout) for t < T, where x_t is
-// xs[t] itself (from_xs, raw plane layout) or buffer X_src of token t0 + t.
-// Thread e handles plane float4 e + 256 u of the T tokens; all of a thread's
-// loads are issued together.  With fold_a >= 0 the CTA's slice of each raw
-// x_t is written to X_fold_a and X_fold_b.  If out is given, the CTA's slice
-// of the normed x_0 goes there.  g points into shared memory (4-element
-// aligned groups).
+// 1 / rms of staged token t (width D), from load_norm's partial sums.
+__device__ __forceinline__ float norm_inv(int t, int D) {
+  const float* r = fk_sm()->red[t];
+  float a = 0.f;
+#pragma unroll
+  for (int w = 0; w < FK_CONSUMER_WARPS; ++w) a += r[w];
+  return 1.0f / sqrtf(a / (float)D + fk_prm()->eps);
+}
+
+// Stages y_t = g * x_t in xs (plane layout) for t < T, where x_t is xs[t]
+// itself (from_xs, raw plane layout) or token t0 + t of buffer X_src (the sum
+// of its copies), and leaves x_t's partial sums of squares in red[t][warp]:
+// RMSNorm(x_t) * g = y_t / rms_t, and the GEMVs that follow scale their sums
+// by 1 / rms_t (norm_inv) instead of normalising first, so staging takes one
+// block-wide barrier.  Thread e handles plane float4 e + 256 u of the T
+// tokens, all of its loads issued together.  With fold_a >= 0 the CTA's slice
+// of each raw x_t goes to copy 0 of X_fold_a and X_fold_b, whose other copies
+// of the slice are cleared.  If out is given, the CTA's slice of the normed
+// x_0 goes there.  g points into shared memory (4-element aligned groups).
 template <class WT>
 __device__ __forceinline__ void load_norm(Cons c, bool from_xs, int src, int t0, int T, int D, const WT* g,
                                           int fold_a, int fold_b, float* out) {
   const FKParams& p = *fk_prm();
   float* xs = fk_sm()->u.g.xs;
-  constexpr int PER = FK_TMAX * FK_DMAX / 4 / FK_CONSUMERS;  // float4 per thread, at most 4
+  constexpr int PER = FK_DMAX / 4 / FK_CONSUMERS;  // float4 per thread: T D <= FK_DMAX (checked at create)
   const int nq = D >> 2, tot = T * nq, tid = ctid();
-  const float* xg = xbuf(p, src, t0);
-  const int dmax = p.dmax;
   float4 xv[PER];
+  if (from_xs) {
 #pragma unroll
-  for (int u = 0; u < PER; ++u) {
-    const int e = tid + FK_CONSUMERS * u;
-    if (e < tot) {
-      const int t = e >= nq ? 1 : 0, pq = e - t * nq;
-      xv[u] = from_xs ? reinterpret_cast<const float4*>(xs + t * D)[pq]
-                      : ldcg4(xg + t * dmax + plane_first(pq, D));
-    } else {
-      xv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < PER; ++u) {
+      const int e = tid + FK_CONSUMERS * u;
+      xv[u] = e < tot ? reinterpret_cast<const float4*>(xs)[e] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  } else {
+    const float* xg = xbuf(p, src, 0) + t0 * D;
+    const int xst = p.xstride;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int e = tid + FK_CONSUMERS * u;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < tot) {
+        const int t = e >= nq ? 1 : 0;
+        const float* q = xg + t * D + plane_first(e - t * nq, D);
+        float4 cv[FK_KC];
+#pragma unroll
+        for (int k = 0; k < FK_KC; ++k) cv[k] = ldcg4(q + k * xst);
+        v = cv[0];
+#pragma unroll
+        for (int k = 1; k < FK_KC; ++k) {
+          v.x += cv[k].x; v.y += cv[k].y; v.z += cv[k].z; v.w += cv[k].w;
+        }
+      }
+      xv[u] = v;
     }
   }
   float ss0 = 0.f, ss1 = 0.f;
@@ -738,13 +817,15 @@ __device__ __forceinline__ void load_norm(Cons c, bool from_xs, int src, int t0,
   }
   ss0 = warp_sum(ss0);
   ss1 = warp_sum(ss1);
+  FK_MARK(TR_SUB, 2);
   if (clane() == 0) {
     fk_sm()->red[0][cwarp()] = ss0;
     fk_sm()->red[1][cwarp()] = ss1;
   }
+  int lo, hi;
+  cta_slice(D, lo, hi);
   if (fold_a >= 0) {
-    int lo, hi;
-    cta_slice(D, lo, hi);
+    const int xst = p.xstride;
     float* fa = xbuf(p, fold_a, 0);
     float* fb = xbuf(p, fold_b, 0);
 #pragma unroll
@@ -757,45 +838,48 @@ __device__ __forceinline__ void load_norm(Cons c, bool from_xs, int src, int t0,
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             if (i + q >= lo && i + q < hi) {
-              fa[t * dmax + i + q] = vals[q];
-              fb[t * dmax + i + q] = vals[q];
+              const int o = t * D + i + q;
+              fa[o] = vals[q];
+              fb[o] = vals[q];
+#pragma unroll
+              for (int k = 1; k < FK_KC; ++k) {
+                fa[o + k * xst] = 0.f;
+                fb[o + k * xst] = 0.f;
+              }
             }
         }
       }
     }
   }
-  consumer_sync();
-  float inv0, inv1;
-  {
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (int w = 0; w < FK_CONSUMER_WARPS; ++w) {
-      a0 += fk_sm()->red[0][w];
-      a1 += fk_sm()->red[1][w];
-    }
-    inv0 = 1.0f / sqrtf(a0 / (float)D + p.eps);
-    inv1 = 1.0f / sqrtf(a1 / (float)D + p.eps);
-  }
-  int lo = 0, hi = 0;
-  if (out) cta_slice(D, lo, hi);
+  float4 y[PER];
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
     const int e = tid + FK_CONSUMERS * u;
     if (e < tot) {
-      const int t = e >= nq ? 1 : 0, pq = e - t * nq, i = plane_first(pq, D);
-      const float iv = t == 0 ? inv0 : inv1;
-      const float4 gv = gain4<WT>(g, i);
-      const float4 y = make_float4(xv[u].x * iv * gv.x, xv[u].y * iv * gv.y, xv[u].z * iv * gv.z, xv[u].w * iv * gv.w);
-      reinterpret_cast<float4*>(xs + t * D)[pq] = y;
-      if (out && t == 0 && i + 3 >= lo && i < hi) {
-        const float vals[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (i + q >= lo && i + q < hi) out[i + q] = vals[q];
-      }
+      const int t = e >= nq ? 1 : 0;
+      const float4 gv = gain4<WT>(g, plane_first(e - t * nq, D));
+      y[u] = make_float4(xv[u].x * gv.x, xv[u].y * gv.y, xv[u].z * gv.z, xv[u].w * gv.w);
+      reinterpret_cast<float4*>(xs)[e] = y[u];
     }
   }
   consumer_sync();
+  if (out) {
+    const float iv = norm_inv(0, D);
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int e = tid + FK_CONSUMERS * u;
+      if (e < nq) {
+        const int i = plane_first(e, D);
+        if (i + 3 >= lo && i < hi) {
+          const float vals[4] = {y[u].x, y[u].y, y[u].z, y[u].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (i + q >= lo && i + q < hi) out[i + q] = vals[q] * iv;
+        }
+      }
+    }
+  }
+  FK_MARK(TR_NORM, 0);
 }
 
 // Writes a raw vector (natural order, D floats at src) into xs token t (plane layout).
@@ -863,6 +947,7 @@ __device__ __noinline__ int draw_code(Cons c, int j) {
                                     sem ? p.sp.temperature : p.sp.sub_temperature,
                                     sem ? p.sp.repetition_penalty : 1.0f,
                                     sem ? p.history + (size_t)p.sid * p.Vt : nullptr, fk_sm()->uni[j]);
+  FK_MARK(TR_SUB, 7);
   code = min(max(code, 0), V - 1);
   int fed = code;
   if (p.forced) {
@@ -899,54 +984,52 @@ __device__ __forceinline__ void oproj_tiles(const FKParams& p, int D, int cta, i
   split(p.Hq * oproj_nt(D), p.ncta, cta, t0, t1);
 }
 
-// The CTA's o_proj tiles against the attention outputs of its (<= 2) heads
-// (os, plane layout), for T tokens; each column's sum goes into both X_a and
-// X_b.  The two warps of a gang take alternate hd blocks of a tile and meet in
-// the exchange buffer.  Closes the attention phase with a grid barrier.
+// The CTA's o_proj tiles, one per ring chunk and private to a warp, against
+// the attention outputs of the CTA's (<= 2) heads (os, plane layout) for T
+// tokens; lane l owns column 32 j + l of its tile, and each column's sum goes
+// into copy CTA % FK_KC of both X_a and X_b.  Closes the attention phase with
+// a grid barrier.
 template <class WT>
 __device__ __forceinline__ void oproj_step(Cons c, int D, int T, int xa, int xb) {
   const FKParams& p = *fk_prm();
   Stream s = stream_begin(c);
-  const int hd = p.hd, nt = oproj_nt(D), nkb = hd >> 3, dmax = p.dmax;
+  const int hd = p.hd, nt = oproj_nt(D), nkb = hd >> 3;
   int t0, t1;
   oproj_tiles(p, D, ccta(), t0, t1);
   const int h_first = t0 / nt;
-  const int tb = 32 * hd * (int)sizeof(WT);
-  const int tpc = rows_per_chunk(tb);
-  float* XA = xbuf(p, xa, 0);
-  float* XB = xbuf(p, xb, 0);
-  FKSmem* sm = fk_sm();
-  const uint32_t os0 = soff(sm->os[0][0]);
+  const int cpy = ccta() % FK_KC;
+  float* XA = xbuf(p, xa, cpy);
+  float* XB = xbuf(p, xb, cpy);
+  const uint32_t os0 = soff(fk_sm()->os[0][0]);
   constexpr uint32_t OS_HEAD = FK_TMAX * FK_HDMAX * 4, OS_TOK = FK_HDMAX * 4;
   const uint32_t n0 = cst().n;
-  const uint32_t nch = t1 > t0 ? (uint32_t)((t1 - t0 + tpc - 1) / tpc) : 0u;
-  for (uint32_t n = first_chunk(n0, s.gang); n < n0 + nch; n += FK_NGANG) {
+  const uint32_t nch = t1 > t0 ? (uint32_t)(t1 - t0) : 0u;
+  for (uint32_t n = first_chunk(n0, s.warp); n < n0 + nch; n += FK_CONSUMER_WARPS) {
     const uint32_t buf = chunk_wait(s, n);
-    float* xbf = xch_buf(s, n);
-    const int tf = t0 + (int)(n - n0) * tpc, ntl = min(tpc, t1 - tf);
-    for (int jt = 0; jt < ntl; ++jt) {
-      const int ti = tf + jt, h = ti / nt, col = (ti - h * nt) * 32 + s.lane;
-      const uint32_t w = buf + (uint32_t)(jt * tb + s.lane * 8 * (int)sizeof(WT));
-      for (int t = 0; t < T; ++t) {
+    const int ti = t0 + (int)(n - n0), h = ti / nt, col = (ti - h * nt) * 32 + s.lane;
+    const uint32_t w = buf + (uint32_t)(s.lane * 8 * (int)sizeof(WT));
+    float a[FK_TMAX];
+#pragma unroll
+    for (int t = 0; t < FK_TMAX; ++t) {
+      a[t] = 0.f;
+      if (t < T) {
         const uint32_t xo = os0 + (uint32_t)(h - h_first) * OS_HEAD + (uint32_t)t * OS_TOK;
-        float a = 0.f, b = 0.f;
-#pragma unroll 2
-        for (int kb = s.j; kb < nkb; kb += FK_GANG)
+        float u = 0.f, v = 0.f;
+#pragma unroll 4
+        for (int kb = 0; kb < nkb; ++kb)
           fma8<WT>(w + (uint32_t)(kb * 256 * (int)sizeof(WT)), lds_f4(xo + (uint32_t)(kb * 16)),
-                   lds_f4(xo + (uint32_t)(2 * hd + kb * 16)), a, b);
-        xbf[s.j * FK_XCH + t * 32 + s.lane] = a + b;
+                   lds_f4(xo + (uint32_t)(2 * hd + kb * 16)), u, v);
+        a[t] = u + v;
       }
-      gang_sync(s);
-      if (s.j == 0 && col < D) {
-        for (int t = 0; t < T; ++t) {
-          const float v = xbf[t * 32 + s.lane] + xbf[FK_XCH + t * 32 + s.lane];
-          atomicAdd(XA + t * dmax + col, v);
-          atomicAdd(XB + t * dmax + col, v);
-        }
-      }
-      gang_sync(s);  // the buffer is rewritten by the next tile
     }
-    chunk_release(s, n);
+    release_private(s, n);
+    if (col < D)
+#pragma unroll
+      for (int t = 0; t < FK_TMAX; ++t)
+        if (t < T) {
+          atomicAdd(XA + t * D + col, a[t]);
+          atomicAdd(XB + t * D + col, a[t]);
+        }
   }
   warp_set(cst().aborted, s.aborted ? 1 : 0);
   warp_set(cst().n, n0 + nch);
@@ -1034,7 +1117,9 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
       }
     }
   }
+  FK_MARK(TR_SUB, 3);
   consumer_sync();
+  FK_MARK(TR_SUB, 4);
   // 2) the current positions' keys, from step 1
 #pragma unroll
   for (int np = 0; np < 2; ++np) {
@@ -1079,6 +1164,7 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
     for (int j = 0; j < 4; ++j)
       if (j < J) as.o[cwarp()][pr][clane() + 32 * j] = o[j];
   }
+  FK_MARK(TR_SUB, 5);
   consumer_sync();
   // 4) combine the warps: thread (pair, d)
   for (int e = ctid(); e < npair * hd; e += FK_CONSUMERS) {
@@ -1096,6 +1182,7 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
     put_plane(fk_sm()->os[pr / T][pr % T], hd, d, Os / Ls);
   }
   consumer_sync();
+  FK_MARK(TR_SUB, 6);
   oproj_step<WT>(c, D, T, xa, xb);
 }
 
@@ -1295,140 +1382,129 @@ __device__ __forceinline__ void phase_talker_oproj(Cons c, int xa, int xb) {
   oproj_step<WT>(c, D, 1, xa, xb);
 }
 
-// One FFN unit f at shared offset u (gate row, up row, down column; D weights
-// each) for T tokens, shared by the two warps of a gang: each takes its
-// activation blocks of the gate/up dot products, the partial sums meet in the
-// exchange buffer slot xu (4 floats per warp), both form a_t =
-// silu(gate_f . x_t) * (up_f . x_t), and each adds a_t W_down[:, f] into the
-// columns of its own blocks.  Down sums: slot q = t nb + b (nb block slots
-// per token, T nb <= 4) holds columns 8 lane + 256 (2 b + j) + k of token t
-// as y[q][k].
-template <class WT>
-__device__ __forceinline__ void ffn_unit(uint32_t u, int D, int T, int nb, uint32_t xs, unsigned m, const Stream& s,
-                                         float* xu, float (&y)[4][8]) {
-  const uint32_t rb = (uint32_t)D * (uint32_t)sizeof(WT);
-  const uint32_t wl = u + (uint32_t)(s.lane * 8 * (int)sizeof(WT));
-  float g0 = 0.f, u0 = 0.f, g1 = 0.f, u1 = 0.f;
-  for (int t = 0; t < T; ++t) {
-    XReg x;
-    load_xreg(x, xs + (uint32_t)(t * D * 4), D, s.lane, s.j, m);
-    float g = 0.f, v = 0.f;
+// Units u0 .. u0 + G - 1 of a chunk that holds the gate rows of U units and
+// then their up rows: a_{f,t} = silu(gate_f . y_t / rms_t) * (up_f . y_t /
+// rms_t) into act[t][a0 + u] (lane u T + t writes one).
+template <class WT, int T, int G>
+__device__ __forceinline__ void ffn_units(uint32_t buf, int rb, int U, int u0, int D, uint32_t xs, int lane,
+                                          const float (&inv)[T], float (*act)[FK_UMAX], int a0) {
+  uint32_t ro[2 * G];
 #pragma unroll
-    for (int b = 0; b < FK_XB; ++b) {
-      if ((m >> b) & 1u) {
-        const uint32_t wb = wl + (uint32_t)((FK_GANG * b + s.j) * 256 * (int)sizeof(WT));
-        g = dot8w<WT>(wb, x.a[b], x.c[b], g);
-        v = dot8w<WT>(wb + rb, x.a[b], x.c[b], v);
-      }
-    }
-    if (t == 0) {
-      g0 = g;
-      u0 = v;
-    } else {
-      g1 = g;
-      u1 = v;
-    }
+  for (int g = 0; g < G; ++g) {
+    ro[2 * g] = (uint32_t)((u0 + g) * rb);
+    ro[2 * g + 1] = (uint32_t)((U + u0 + g) * rb);
   }
-  g0 = warp_sum(g0);
-  u0 = warp_sum(u0);
-  if (T > 1) {
-    g1 = warp_sum(g1);
-    u1 = warp_sum(u1);
-  }
-  if (s.lane == 0) {
-    xu[s.j * FK_XCH] = g0;
-    xu[s.j * FK_XCH + 1] = u0;
-    xu[s.j * FK_XCH + 2] = g1;
-    xu[s.j * FK_XCH + 3] = u1;
-  }
-  gang_sync(s);
-  const float a0 = silu(xu[0] + xu[FK_XCH]) * (xu[1] + xu[FK_XCH + 1]);
-  const float a1 = T > 1 ? silu(xu[2] + xu[FK_XCH + 2]) * (xu[3] + xu[FK_XCH + 3]) : 0.f;
-  const uint32_t wd = wl + 2u * rb;
+  float acc[2 * G][T];
+  dots<WT, T, 2 * G>(buf, ro, D, xs, lane, acc);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int t = q >= nb ? 1 : 0, b = q - t * nb;
-    if (t < T && ((m >> b) & 1u)) {
-      float d8[8];
-      lds_w8<WT>(wd + (uint32_t)((FK_GANG * b + s.j) * 256 * (int)sizeof(WT)), d8);
-      const float a = t ? a1 : a0;
+  for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int k = 0; k < 8; ++k) y[q][k] = fmaf(a, d8[k], y[q][k]);
-    }
-  }
+    for (int t = 0; t < T; ++t)
+      if (lane == g * T + t) act[t][a0 + u0 + g] = silu(acc[2 * g][t] * inv[t]) * (acc[2 * g + 1][t] * inv[t]);
 }
 
-// The gang's share of the CTA's FFN units [f0, f1) (chunks n0 .. n0 + nch),
-// its down-projection sums added into yred (layout at phase_ffn).
-template <class WT>
-__device__ __forceinline__ void ffn_stream(Cons c, int D, int T, int f0, int f1, uint32_t n0, uint32_t nch) {
-  Stream s = stream_begin(c);
-  const int ub = 3 * D * (int)sizeof(WT);
-  const int upc = rows_per_chunk(ub);
-  FKSmem* sm = fk_sm();
-  const uint32_t xs = soff(sm->u.g.xs);
-  const unsigned m = xblocks(D, s.lane, s.j);
-  const int nb = ((D + 255) >> 8) > FK_GANG * 2 ? FK_XB : FK_XB / 2;  // block slots per token
-  float y[4][8];
+// The down projection of the CTA's FFN units [f0, f1): shared chunks of
+// W_down^T rows from ring position n0; lane l of warp w owns output columns
+// 8 (32 w + l) .. + 7, accumulates a_{f,t} W_down[:, f] over the units in
+// registers and adds the CTA's partial sums into copy CTA % FK_KC of X_b
+// with float4 atomics.
+template <class WT, int T>
+__device__ __forceinline__ void ffn_down(Stream& s, int D, int f0, int f1, uint32_t n0, int xb) {
+  const FKParams& p = *fk_prm();
+  const float(*act)[FK_UMAX] = fk_sm()->act;
+  const int rb = D * (int)sizeof(WT);
+  const int rpc = rows_per_chunk(rb);
+  const uint32_t nd = f1 > f0 ? (uint32_t)((f1 - f0 + rpc - 1) / rpc) : 0u;
+  const int col = (s.warp * 32 + s.lane) * 8;  // the lane's first output column
+  const bool active = col < D;
+  float y[T][8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int t = 0; t < T; ++t)
 #pragma unroll
-    for (int k = 0; k < 8; ++k) y[i][k] = 0.f;
-  bool any = false;
-  for (uint32_t n = first_chunk(n0, s.gang); n < n0 + nch; n += FK_NGANG) {
+    for (int k = 0; k < 8; ++k) y[t][k] = 0.f;
+  for (uint32_t n = n0; n < n0 + nd; ++n) {
     const uint32_t buf = chunk_wait(s, n);
-    float* xbf = xch_buf(s, n);
-    const int nu = min(upc, f1 - (f0 + (int)(n - n0) * upc));
-    for (int jj = 0; jj < nu; ++jj) ffn_unit<WT>(buf + (uint32_t)(jj * ub), D, T, nb, xs, m, s, xbf + 4 * jj, y);
-    gang_sync(s);  // both warps are done with the chunk
-    chunk_release(s, n);
-    any = true;
+    const int fb = f0 + (int)(n - n0) * rpc, R = min(rpc, f1 - fb);
+    if (active) {
+      const uint32_t w = buf + (uint32_t)(col * (int)sizeof(WT));
+      for (int r = 0; r < R; ++r) {
+        float d8[8];
+        lds_w8<WT>(w + (uint32_t)(r * rb), d8);
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+          const float a = act[t][fb - f0 + r];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) y[t][k] = fmaf(a, d8[k], y[t][k]);
+        }
+      }
+    }
+    release_shared(s, n);
   }
   warp_set(cst().aborted, s.aborted ? 1 : 0);
-  if (any) {
-    float* yred = sm->u.g.yred;
-    const int IM = 8 / T;
+  warp_set(cst().n, n0 + nd);
+  if (active && nd) {
+    float* X = xbuf(p, xb, ccta() % FK_KC);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int t = q >= nb ? 1 : 0, b = q - t * nb;
-      if (t < T && ((m >> b) & 1u)) {
-        const int i = FK_GANG * b + s.j;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) atomicAdd(&yred[((t * IM + i) * 8 + k) * 32 + s.lane], y[q][k]);
-      }
+    for (int t = 0; t < T; ++t) {
+      atomicAdd(reinterpret_cast<float4*>(X + t * D + col), make_float4(y[t][0], y[t][1], y[t][2], y[t][3]));
+      atomicAdd(reinterpret_cast<float4*>(X + t * D + col + 4), make_float4(y[t][4], y[t][5], y[t][6], y[t][7]));
     }
   }
 }
 
-// Phase C: y = X_a (input + attention), RMSNorm, then the CTA's FFN units
-// (split-K over the FFN width), each warp accumulating its units' down
-// projection in registers; the warps' sums meet in shared memory and the
-// CTA's partial D-vector is added into X_b with float4 atomics.  yred holds
-// the sums lane-transposed -- element ((t IM + i) 8 + q) 32 + lane, IM = 8 / T,
-// is column 8 lane + 256 i + q of token t -- so the warps' shared-memory adds
-// are bank-conflict free.
+// FFN units of the CTA whose gate and up rows share one ring chunk.
+__device__ __forceinline__ int units_per_chunk(int row_bytes) {
+  const int u = FK_STAGE / (2 * row_bytes);
+  return u < 1 ? 1 : (u > FK_RMAX / 2 ? FK_RMAX / 2 : u);
+}
+
+// Phase C: y = X_a (input + attention) staged for RMSNorm, then the CTA's FFN
+// units [f0, f1) (split-K over the FFN width) in two streams.  First the gate
+// and up rows: a private chunk holds the gate rows of U units and then their
+// up rows, and its warp forms a_{f,t} = silu(gate_f . y_t / rms_t) *
+// (up_f . y_t / rms_t) into act.  After one block-wide barrier, the rows of the
+// transposed down projection W_down^T[f] (shared chunks): lane l of warp w
+// owns output columns 8 (32 w + l) .. + 7 and adds a_{f,t} W_down[:, f] over
+// the CTA's units in registers.  The CTA's partial D-vector goes into copy
+// CTA % FK_KC of X_b with float4 atomics.
 template <class WT>
 __device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int xa, int xb) {
   const FKParams& p = *fk_prm();
-  float* yred = fk_sm()->u.g.yred;
-  for (int e = ctid(); e < 32 * FK_YCOLS; e += FK_CONSUMERS) yred[e] = 0.f;  // before load_norm's barriers
   load_norm<WT>(c, false, xa, 0, T, D, side_cur<WT>(c) + D, -1, -1, nullptr);
   side_end(c);
+  const float inv0 = norm_inv(0, D), inv1 = T > 1 ? norm_inv(1, D) : 0.f;
   int f0, f1;
   split(F, p.ncta, ccta(), f0, f1);
-  const int upc = rows_per_chunk(3 * D * (int)sizeof(WT));
-  const uint32_t n0 = cst().n;
+  const int rb = D * (int)sizeof(WT);
+  const int upc = units_per_chunk(rb);
+  FKSmem* sm = fk_sm();
+  const uint32_t xs = soff(sm->u.g.xs);
+  Stream s = stream_begin(c);
+  uint32_t n0 = cst().n;
   const uint32_t nch = f1 > f0 ? (uint32_t)((f1 - f0 + upc - 1) / upc) : 0u;
-  ffn_stream<WT>(c, D, T, f0, f1, n0, nch);
-  warp_set(cst().n, n0 + nch);
-  consumer_sync();
-  const int IM = 8 / T, nq = D / 4;
-  for (int e = ctid(); e < T * nq; e += FK_CONSUMERS) {
-    const int t = e >= nq ? 1 : 0, col = (e - t * nq) * 4;  // T <= 2
-    const int i = col >> 8, ln = (col & 255) >> 3, q = col & 7;
-    const float* src = yred + ((t * IM + i) * 8 + q) * 32 + ln;
-    atomicAdd(reinterpret_cast<float4*>(xbuf(p, xb, t) + col), make_float4(src[0], src[32], src[64], src[96]));
+  for (uint32_t n = first_chunk(n0, s.warp); n < n0 + nch; n += FK_CONSUMER_WARPS) {
+    const uint32_t buf = chunk_wait(s, n);
+    const int fb = f0 + (int)(n - n0) * upc, U = min(upc, f1 - fb);
+    // the chunk holds the gate rows of units fb .. fb + U - 1, then their up rows
+    int u = 0;
+    if (T == 1) {
+      const float inv[1] = {inv0};
+      for (; u + 2 <= U; u += 2) ffn_units<WT, 1, 2>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0);
+      if (u < U) ffn_units<WT, 1, 1>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0);
+    } else {
+      const float inv[2] = {inv0, inv1};
+      for (; u + 2 <= U; u += 2) ffn_units<WT, 2, 2>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0);
+      if (u < U) ffn_units<WT, 2, 1>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0);
+    }
+    release_private(s, n);
   }
+  warp_set(cst().n, n0 + nch);
+  n0 += nch;
+  consumer_sync();  // act complete
+  if (T == 1)
+    ffn_down<WT, 1>(s, D, f0, f1, n0, xb);
+  else
+    ffn_down<WT, 2>(s, D, f0, f1, n0, xb);
   grid_sync(c);
 }
 
@@ -1617,7 +1693,7 @@ __device__ __forceinline__ void rows_step(Cons c, const Step& st) {
     T = Tp;
     nrows = p.Dc;
     out = xbuf(p, 0, 0);
-    ts = p.dmax;
+    ts = p.Dc;
   } else if (st.kind == S_CP_HEAD) {
     K = p.Dc;
     T = 1;
@@ -1631,12 +1707,14 @@ __device__ __forceinline__ void rows_step(Cons c, const Step& st) {
     out = p.pending_logits + (size_t)p.sid * p.Vt;
     ts = 0;
   }
+  float inv0 = 1.f, inv1 = 1.f;  // the projection's input is not normed
   if (st.kind != S_PROJ) {
     const WT* g;
     int fa = -1, fb = -1, t0 = 0;
     float* hout = nullptr;
     if (st.kind == S_QKV) {
       g = side_begin<WT>(c);
+      FK_MARK(TR_SUB, 1);
       fa = xnext(L.in, 1);
       fb = xnext(L.in, 2);
     } else {
@@ -1645,10 +1723,12 @@ __device__ __forceinline__ void rows_step(Cons c, const Step& st) {
       if (!cp) hout = p.pending_h + (size_t)p.sid * p.Dt;
     }
     load_norm<WT>(c, st.kind == S_QKV && L.from_xs, L.in, t0, T, K, g, fa, fb, hout);
+    inv0 = norm_inv(0, K);
+    inv1 = T > 1 ? norm_inv(1, K) : 0.f;
   }
   int lo, hi;
   split(nrows, p.ncta, ccta(), lo, hi);
-  stream_rows<WT>(c, lo, hi, K, T, soff(fk_sm()->u.g.xs), out, ts);
+  stream_rows<WT>(c, lo, hi, K, T, soff(fk_sm()->u.g.xs), out, ts, inv0, inv1, st.kind == S_PROJ ? p.xstride : 0);
   if (st.kind != S_T_HEAD) grid_sync(c);
   warp_set(L.from_xs, 0);
 }
@@ -1691,11 +1771,16 @@ __device__ void consumer() {
     }
   }
   consumer_sync();
+#ifdef Q3TTS_TRACE
+  if (ctid() == 0) fk_sm()->trace_n = 0;
+#endif
+  FK_MARK(TR_STEP, 15);
   ConsState& L = cst();
   warp_set(L.j, 0);
   warp_set(L.k, 0);
   for (; L.j < Q3TTS_N_CODEBOOKS; next_step(L)) {
     const Step st = decode_step(*fk_prm(), L.j, L.k);
+    FK_MARK(TR_STEP, st.kind | (st.j << 4) | (st.l << 9));
     const bool cp = st.j < Q3TTS_N_CODEBOOKS - 1;
     const int T = cp && st.j == 0 ? 2 : 1;
     switch (st.kind) {
@@ -1724,6 +1809,7 @@ __device__ void consumer() {
   {
     const FKParams& q = *fk_prm();
     if (ccta() == 0 && ctid() == 0) q.history[(size_t)q.sid * q.Vt + L.fed0] = 1;
+    FK_MARK(TR_END, 0);
     consumer_sync();
     if (ctid() == 0) {
       __threadfence();
@@ -1737,7 +1823,13 @@ __device__ void consumer() {
 
 // ---------------------------------------------------------------- producer
 
-template <class WT>
+// The frame's weight schedule for one CTA, walked twice: by the ring's
+// producer (PF false: bulk copies into the ring, side blocks into their
+// slots) and by the prefetch warp (PF true: the same chunks as L2 prefetches,
+// at most FK_PF_AHEAD chunks ahead of the producer), so that HBM keeps
+// streaming while the consumers sit in barriers, attention and draws, and the
+// ring's copies hit L2.
+template <class WT, bool PF>
 struct Producer {
   const FKParams& p;
   FKSmem* sm;
@@ -1750,26 +1842,60 @@ struct Producer {
     pol = l2_evict_first_policy();
   }
 
-  __device__ void issue(const void* src, unsigned bytes) {
-    if (stop) return;
-    const int s = n % FK_NSTAGE;
-    if (n >= (uint32_t)FK_NSTAGE) {
-      const unsigned par = ((n / FK_NSTAGE) - 1) & 1u;
-      long long t0 = clock64();
-      unsigned it = 0;
-      // the ring is full most of the time: wait suspended so this warp does
-      // not take issue slots from the consumer warps of its scheduler
-      while (!mbar_try_wait_sleep(&sm->empty[s], par, 2000)) {
-        if ((++it & 15u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > p.wait_cycles)) {
-          raise_abort(p, Q3TTS_ERR_TIMEOUT);
-          stop = true;
-          return;
-        }
+  // Waits (bounded) until slot s may be refilled with chunk n; false after an
+  // abort or a timeout (the producer then stops issuing).
+  __device__ bool wait_empty(int s) {
+    const unsigned par = ((n / FK_NSTAGE) - 1) & 1u;
+    long long t0 = clock64();
+    unsigned it = 0;
+    // the ring is full most of the time: wait suspended so this warp does
+    // not take issue slots from the consumer warps of its scheduler
+    while (!mbar_try_wait_sleep(&sm->empty[s], par, 2000)) {
+      if ((++it & 15u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > p.wait_cycles)) {
+        raise_abort(p, Q3TTS_ERR_TIMEOUT);
+        stop = true;
+        return false;
       }
     }
+    return true;
+  }
+
+  // Prefetch mode: waits (bounded) until chunk n is at most FK_PF_AHEAD
+  // chunks ahead of the producer; false to stop (an abort, or a producer that
+  // no longer advances -- it reports the timeout itself).
+  __device__ bool pf_gate_wait() {
+    const volatile uint32_t* gate = &sm->pf_gate;
+    long long t0 = clock64();
+    unsigned it = 0;
+    while (n >= *gate + (uint32_t)FK_PF_AHEAD) {
+      __nanosleep(256);
+      if ((++it & 15u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > p.wait_cycles)) {
+        stop = true;
+        return false;
+      }
+    }
+    return true;
+  }
+
+  __device__ void publish() {
+    if (!PF) *(volatile uint32_t*)&sm->pf_gate = n;
+  }
+
+  __device__ void issue(const void* src, unsigned bytes) {
+    if (stop) return;
+    if (PF) {
+      if (pf_gate_wait()) {
+        prefetch_l2(src, bytes);
+        n++;
+      }
+      return;
+    }
+    const int s = n % FK_NSTAGE;
+    if (n >= (uint32_t)FK_NSTAGE && !wait_empty(s)) return;
     mbar_expect_tx(&sm->full[s], bytes);
     bulk_g2s(sm->ring[s], src, bytes, &sm->full[s], pol);
     n++;
+    publish();
   }
 
   __device__ void rows(const void* base, int r0, int r1, int row_bytes) {
@@ -1784,8 +1910,39 @@ struct Producer {
     rows(base, lo, hi, row_bytes);
   }
 
-  // The CTA's FFN units (gate row, up row, down column: 3 D weights each).
-  __device__ void ffn(const LayerDev& L, int D, int F) { split_rows(L.w_ffn, F, 3 * D * (int)sizeof(WT)); }
+  // One chunk from two sources (the gate rows and the up rows of a few FFN units).
+  __device__ void issue2(const void* a, const void* b, unsigned bytes) {
+    if (stop) return;
+    if (PF) {
+      if (pf_gate_wait()) {
+        prefetch_l2(a, bytes);
+        prefetch_l2(b, bytes);
+        n++;
+      }
+      return;
+    }
+    const int s = n % FK_NSTAGE;
+    if (n >= (uint32_t)FK_NSTAGE && !wait_empty(s)) return;
+    mbar_expect_tx(&sm->full[s], 2 * bytes);
+    bulk_g2s(sm->ring[s], a, bytes, &sm->full[s], pol);
+    bulk_g2s(sm->ring[s] + bytes, b, bytes, &sm->full[s], pol);
+    n++;
+    publish();
+  }
+
+  // The CTA's FFN units [f0, f1): chunks of the gate rows then the up rows of
+  // a few units, then the rows of W_down^T.
+  __device__ void ffn(const LayerDev& L, int D, int F) {
+    int f0, f1;
+    split(F, p.ncta, cta, f0, f1);
+    const int rb = D * (int)sizeof(WT), upc = units_per_chunk(rb);
+    const char* gu = (const char*)L.w_gu;
+    for (int f = f0; f < f1; f += upc) {
+      const int U = min(upc, f1 - f);
+      issue2(gu + (size_t)f * rb, gu + (size_t)(F + f) * rb, (unsigned)(U * rb));
+    }
+    rows(L.w_dT, f0, f1, rb);
+  }
 
   int nlayers = 0;  // layers in the frame (15 CodePredictor passes, then the Talker)
   int layer_i = 0;  // next layer whose weights are streamed
@@ -1798,7 +1955,7 @@ struct Producer {
 
   // Side block of layer k into slot k & 1 (after the consumers freed it).
   __device__ void side(int k) {
-    if (stop || k >= nlayers) return;
+    if (PF || stop || k >= nlayers) return;
     const int slot = k & 1;
     if (k >= 2) {
       const unsigned par = ((k >> 1) - 1) & 1u;
@@ -1822,19 +1979,20 @@ struct Producer {
 
   __device__ void layer(const LayerDev& L, int D, int F) {
     const int esz = (int)sizeof(WT);
-    // the next layer's gains go out one layer ahead
-    if (layer_i >= 1) side(layer_i + 1);
-    layer_i++;
     split_rows(L.w_qkv, p.qkv_rows, D * esz);
     split_rows(L.w_oT, p.Hq * oproj_nt(D), 32 * p.hd * esz);
     ffn(L, D, F);
+    // the next layer's gains go out once this layer's weights are queued: their
+    // slot was freed when the consumers began the previous layer's FFN, which
+    // lies at least a ring's depth behind this point
+    layer_i++;
+    side(layer_i);
   }
 
   __device__ void run() {
     const int esz = (int)sizeof(WT);
     nlayers = (Q3TTS_N_CODEBOOKS - 1) * p.Lc + p.Lt;
     side(0);
-    side(1);
     for (int j = 0; j < Q3TTS_N_CODEBOOKS - 1; ++j) {
       if (p.has_proj) split_rows(p.cp_proj, p.Dc, p.Dt * esz);
       for (int l = 0; l < p.Lc; ++l) layer(sm->lay[p.Lt + l], p.Dc, p.Fc);
@@ -1842,10 +2000,14 @@ struct Producer {
     }
     for (int l = 0; l < p.Lt; ++l) layer(sm->lay[l], p.Dt, p.Ft);
     split_rows(p.t_head, p.Vt, p.Dt * esz);
-    // copies still in flight must land before the CTA may exit: the last
-    // side block copied into each slot (after an abort the producer stops
-    // early, so these need not be the frame's last two layers) and the last
-    // FK_NSTAGE ring chunks
+    if (!PF) drain();  // prefetches leave nothing in flight that the CTA owns
+  }
+
+  // Copies still in flight must land before the CTA may exit: the last side
+  // block copied into each slot (after an abort the producer stops early, so
+  // these need not be the frame's last two layers) and the last FK_NSTAGE
+  // ring chunks.
+  __device__ void drain() {
     for (int slot = 0; slot < 2; ++slot) {
       const int k = side_last[slot];
       if (k < 0) continue;
@@ -1869,9 +2031,10 @@ __global__ void __launch_bounds__(FK_THREADS, 1) frame_kernel(const __grid_const
   for (int i = threadIdx.x; i < p.Lt + p.Lc; i += blockDim.x)
     sm->lay[i] = i < p.Lt ? p.tl[i] : p.cl[i - p.Lt];
   if (threadIdx.x == 0) {
+    sm->pf_gate = 0;
     for (int s = 0; s < FK_NSTAGE; ++s) {
       mbar_init(&sm->full[s], 1);
-      mbar_init(&sm->empty[s], 1);  // the one warp that streams the chunk
+      mbar_init(&sm->empty[s], FK_CONSUMER_WARPS);  // see release_private / release_shared
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm->side_full[s], 1);
@@ -1882,8 +2045,15 @@ __global__ void __launch_bounds__(FK_THREADS, 1) frame_kernel(const __grid_const
   __syncthreads();
   if (threadIdx.x < FK_PRODUCER_THREADS) {
     if (threadIdx.x == 0) {
-      Producer<WT> pr(sm->prm, sm, blockIdx.x);
+      Producer<WT, false> pr(sm->prm, sm, blockIdx.x);
       pr.run();
+    }
+    return;
+  }
+  if (threadIdx.x >= FK_PRODUCER_THREADS + FK_CONSUMERS) {
+    if (threadIdx.x == FK_PRODUCER_THREADS + FK_CONSUMERS) {
+      Producer<WT, true> pf(sm->prm, sm, blockIdx.x);
+      pf.run();
     }
     return;
   }
@@ -1930,12 +2100,21 @@ __global__ void transpose_kernel(const T* __restrict__ in, T* __restrict__ out, 
 
 static size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Floats between the copies of a residual buffer: the widest [tokens][D]
+// either stack stages (the Talker's one token, or the CodePredictor's two),
+// rounded to 256 bytes.
+static int fk_xstride(const q3tts_config& c) {
+  const int w = std::max(c.talker_hidden, FK_TMAX * c.cp_hidden);
+  return (w + 63) & ~63;
+}
+
 static size_t fk_layout(const q3tts_config& c, int ncta, FKState* st, char* base) {
   const int esz = c.weight_dtype == Q3TTS_F32 ? 4 : 2;
   const int Hq = c.n_q_heads, hd = c.head_dim, Hkv = c.n_kv_heads;
   const int dmax = std::max(c.talker_hidden, c.cp_hidden);
   const int qkv_rows = (Hq + 2 * Hkv) * hd;
   const int cpg = std::max(1, ncta / Hkv);
+  const size_t xst = (size_t)fk_xstride(c);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     size_t o = off;
@@ -1944,15 +2123,16 @@ static size_t fk_layout(const q3tts_config& c, int ncta, FKState* st, char* base
   };
   const size_t oT_t = (size_t)Hq * hd * 32 * ((c.talker_hidden + 31) / 32);
   const size_t oT_c = (size_t)Hq * hd * 32 * ((c.cp_hidden + 31) / 32);
-  char* reT = take((size_t)c.talker_layers * (oT_t + 3 * (size_t)c.talker_ffn * c.talker_hidden) * esz);
-  char* reC = take((size_t)c.cp_layers * (oT_c + 3 * (size_t)c.cp_ffn * c.cp_hidden) * esz);
+  // re-laid-out weights per layer: o_proj tiles, W_down^T
+  char* reT = take((size_t)c.talker_layers * (oT_t + (size_t)c.talker_ffn * c.talker_hidden) * esz);
+  char* reC = take((size_t)c.cp_layers * (oT_c + (size_t)c.cp_ffn * c.cp_hidden) * esz);
   char* sideT = take((size_t)c.talker_layers * (2 * c.talker_hidden + 2 * hd) * esz);
   char* sideC = take((size_t)c.cp_layers * (2 * c.cp_hidden + 2 * hd) * esz);
   char* tl = take(sizeof(LayerDev) * c.talker_layers);
   char* cl = take(sizeof(LayerDev) * c.cp_layers);
-  char* R = take(sizeof(float) * 2 * FK_TMAX * dmax);
-  char* dA = take(sizeof(float) * 2 * FK_TMAX * dmax);
-  char* dF = take(sizeof(float) * 2 * FK_TMAX * dmax);
+  char* R = take(sizeof(float) * FK_KC * xst);
+  char* dA = take(sizeof(float) * FK_KC * xst);
+  char* dF = take(sizeof(float) * FK_KC * xst);
   char* qkv = take(sizeof(float) * FK_TMAX * qkv_rows);
   char* part = take(sizeof(float) * (size_t)Hq * cpg * (hd + 2));
   char* lg = take(sizeof(float) * c.cp_vocab);
@@ -1996,7 +2176,8 @@ int frame_kernel_create(q3tts_handle* h) {
   if (c.talker_hidden > FK_DMAX || c.cp_hidden > FK_DMAX || c.head_dim > FK_HDMAX ||
       c.talker_layers + c.cp_layers > FK_MAXLAYERS ||
       c.n_q_heads / c.n_kv_heads > FK_REPMAX || c.codec_vocab > SAMPLER_VMAX ||
-      c.cp_vocab > SAMPLER_VMAX || (c.talker_hidden % 8) || (c.cp_hidden % 4) ||
+      c.cp_vocab > SAMPLER_VMAX || (c.codec_vocab % 4) || (c.cp_vocab % 4) || (c.talker_hidden % 8) ||
+      (c.cp_hidden % 8) ||
       ((uintptr_t)h->w.talker_e_codec & 15) || ((uintptr_t)h->w.cp_embeds & 15))
     return Q3TTS_OK;
   const int ncta = std::min(h->n_sm, FK_MAXCTA);
@@ -2008,13 +2189,19 @@ int frame_kernel_create(q3tts_handle* h) {
     return (c.n_q_heads * nt + ncta - 1) / ncta <= nt;
   };
   if (ncta < c.n_kv_heads || !tiles_ok(c.talker_hidden) || !tiles_ok(c.cp_hidden)) return Q3TTS_OK;
-  // a ring chunk holds at least one row and one FFN unit (3 D weights); the
-  // two-token CodePredictor pass keeps 2 x (D_c / 32) FFN sums per lane
+  // a ring chunk holds the gate and up rows of one FFN unit (2 D weights) and
+  // one o_proj tile (32 hd weights); a CTA's FFN activations fit act
   const int esz_w = c.weight_dtype == Q3TTS_F32 ? 4 : 2;
-  if (3 * std::max(c.talker_hidden, c.cp_hidden) * esz_w > FK_STAGE || 2 * c.cp_hidden > 32 * FK_YCOLS)
+  if (2 * std::max(c.talker_hidden, c.cp_hidden) * esz_w > FK_STAGE || 32 * c.head_dim * esz_w > FK_STAGE)
     return Q3TTS_OK;
-  // a gang exchanges at most FK_XCH partial sums per chunk (rows x 2 tokens)
-  if (2 * (FK_STAGE / (std::min(c.talker_hidden, c.cp_hidden) * esz_w)) > FK_XCH) return Q3TTS_OK;
+  if ((std::max(c.talker_ffn, c.cp_ffn) + ncta - 1) / ncta > FK_UMAX) return Q3TTS_OK;
+  // RMSNorm staging holds at most FK_DMAX values: the CodePredictor's first
+  // pass stages two tokens
+  if (FK_TMAX * c.cp_hidden > FK_DMAX) return Q3TTS_OK;
+  // per-layer gains and both final norms fit their shared-memory slots
+  if ((2 * std::max(c.talker_hidden, c.cp_hidden) + 2 * c.head_dim) * esz_w > FK_SIDE_BYTES ||
+      (c.talker_hidden + c.cp_hidden) * esz_w > FK_FIN_BYTES)
+    return Q3TTS_OK;
   st->smem = sizeof(FKSmem);
   void* k = pick_kernel(c.weight_dtype, c.kv_dtype);
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)st->smem) != cudaSuccess) {
@@ -2047,25 +2234,21 @@ int frame_kernel_create(q3tts_handle* h) {
       return false;
     d.side = side;
     d.w_qkv = w.w_qkv;
+    d.w_gu = w.w_gateup;
     char* oT = re;
     re += (size_t)Hq * hd * 32 * ((D + 31) / 32) * esz;
-    char* ffn = re;
-    re += 3 * (size_t)F * D * esz;
+    char* dT = re;
+    re += (size_t)F * D * esz;
     d.w_oT = oT;
-    d.w_ffn = ffn;
-    // FFN unit f = [gate row f | up row f | column f of W_down]
-    const size_t rb = (size_t)D * esz;
-    if (cudaMemcpy2DAsync(ffn, 3 * rb, w.w_gateup, rb, rb, F, cudaMemcpyDeviceToDevice, h->s) != cudaSuccess ||
-        cudaMemcpy2DAsync(ffn + rb, 3 * rb, (const char*)w.w_gateup + (size_t)F * rb, rb, rb, F,
-                          cudaMemcpyDeviceToDevice, h->s) != cudaSuccess)
-      return false;
+    d.w_dT = dT;
+    // W_down^T [F][D]: dT[f][d] = W_down[d][f]
     dim3 tb(32, 8), tg((F + 31) / 32 < 1024 ? (F + 31) / 32 : 1024, (D + 31) / 32 < 1024 ? (D + 31) / 32 : 1024);
     if (esz == 2) {
       repack_oT_kernel<bf16><<<1024, 256, 0, h->s>>>((const bf16*)w.w_o, (bf16*)oT, D, Hq, hd);
-      transpose_kernel<bf16><<<tg, tb, 0, h->s>>>((const bf16*)w.w_down, (bf16*)(ffn + 2 * rb), D, F, 3 * (size_t)D);
+      transpose_kernel<bf16><<<tg, tb, 0, h->s>>>((const bf16*)w.w_down, (bf16*)dT, D, F, (size_t)D);
     } else {
       repack_oT_kernel<float><<<1024, 256, 0, h->s>>>((const float*)w.w_o, (float*)oT, D, Hq, hd);
-      transpose_kernel<float><<<tg, tb, 0, h->s>>>((const float*)w.w_down, (float*)(ffn + 2 * rb), D, F, 3 * (size_t)D);
+      transpose_kernel<float><<<tg, tb, 0, h->s>>>((const float*)w.w_down, (float*)dT, D, F, (size_t)D);
     }
     return cudaGetLastError() == cudaSuccess;
   };
@@ -2113,6 +2296,7 @@ static void frame_params(FKParams& p, const q3tts_handle* h, int sid, int pos, i
   p.Hq = c.n_q_heads; p.Hkv = c.n_kv_heads; p.hd = c.head_dim; p.Vt = c.codec_vocab; p.Vc = c.cp_vocab;
   p.Lt = c.talker_layers; p.Lc = c.cp_layers; p.qkv_rows = h->qkv_rows;
   p.has_proj = h->w.cp_w_proj != nullptr; p.qk_norm = c.qk_norm; p.dmax = st->dmax; p.eps = c.rms_eps;
+  p.xstride = fk_xstride(c);
   p.tl = st->tl; p.cl = st->cl;
   p.t_head = h->w.talker_w_head; p.e_codec = h->w.talker_e_codec; p.cp_heads = h->w.cp_heads;
   p.cp_embeds = h->w.cp_embeds; p.cp_proj = h->w.cp_w_proj; p.t_gfinal = h->w.talker_g_final;
@@ -2144,6 +2328,13 @@ int frame_kernel_step(q3tts_handle* h, const StepDesc& d, const float* uniforms,
   frame_params(p, h, d.sid[0], d.pos[0], d.newpage[0], d.sp[0], uniforms, codes, forced, logits);
   return frame_launch(h, p);
 }
+
+#ifdef Q3TTS_TRACE
+// Profiling builds: copies the timestamp buffer to host memory.
+extern "C" int q3tts_trace_fetch(void* host, size_t bytes) {
+  return cudaMemcpyFromSymbol(host, fk_trace_buf, bytes) == cudaSuccess ? 0 : -3;
+}
+#endif
 
 // Arms the failure-path test for the handle's next persistent launch.
 int frame_kernel_debug_fail(q3tts_handle* h, int barrier, int wait_us) {
@@ -2182,7 +2373,7 @@ static std::atomic<unsigned char*> g_static_addr[FK_MAX_DEVICES];
 // Places the scratch vectors of config c behind the barrier words at base
 // (size only when base is null); returns the bytes used.
 static size_t fk_static_layout(const q3tts_config& c, int ncta, char* base, FKParams* p) {
-  const int dmax = std::max(c.talker_hidden, c.cp_hidden);
+  const size_t xst = (size_t)fk_xstride(c);
   const int qkv_rows = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
   const int cpg = std::max(1, ncta / c.n_kv_heads);
   size_t off = 256;  // barrier words
@@ -2191,9 +2382,9 @@ static size_t fk_static_layout(const q3tts_config& c, int ncta, char* base, FKPa
     off = al256(off + bytes);
     return (float*)(base ? base + o : nullptr);
   };
-  float* R = take(sizeof(float) * 2 * FK_TMAX * dmax);
-  float* dA = take(sizeof(float) * 2 * FK_TMAX * dmax);
-  float* dF = take(sizeof(float) * 2 * FK_TMAX * dmax);
+  float* R = take(sizeof(float) * FK_KC * xst);
+  float* dA = take(sizeof(float) * FK_KC * xst);
+  float* dF = take(sizeof(float) * FK_KC * xst);
   float* qkv = take(sizeof(float) * FK_TMAX * qkv_rows);
   float* part = take(sizeof(float) * (size_t)c.n_q_heads * cpg * (c.head_dim + 2));
   float* lg = take(sizeof(float) * c.cp_vocab);

@@ -304,7 +304,8 @@ namespace q3 {
 // ---------------------------------------------------------------------------
 // Register-resident sampler of the frame kernel (fast_sample, at the end).
 constexpr int FAST_NT = 256;
-constexpr int FAST_VPT = SAMPLER_VMAX / FAST_NT;  // 16 logits per thread at most
+constexpr int FAST_V4 = SAMPLER_VMAX / 4 / FAST_NT;  // float4 of logits per thread
+constexpr int FAST_VPT = 4 * FAST_V4;              // 16 logits per thread at most
 constexpr int FAST_NW = FAST_NT / 32;
 constexpr int FAST_TOP = 8;                        // lane maxima per warp entering theta
 constexpr int FAST_CAP = 256;                      // candidates ranked directly
@@ -318,7 +319,6 @@ struct FastSamplerSmem {
   uint32_t keys[SAMPLER_VMAX];  // the fallback selection's copy of the value keys
   int wc[2][FAST_NW];
   int wscan[FAST_NW];
-  unsigned long long wbest[FAST_NW];
   unsigned long long theta;
   int n_cand, n_gt, pick;
 };
@@ -344,54 +344,6 @@ __device__ __forceinline__ int group_count(FastSamplerSmem& sm, int v, int slot)
   int tot = 0;
   for (int w = 0; w < FAST_NW; ++w) tot += sm.wc[slot][w];
   return tot;
-}
-
-// The logits of thread t, [t per, (t + 1) per), with the repetition penalty
-// applied (history != nullptr and rep != 1); entries past V are 0.
-template <int VPT>
-__device__ __forceinline__ void fast_load(float (&v)[VPT], const float* logits, int V, int i0, int per,
-                                          float rep, const uint8_t* history) {
-#pragma unroll
-  for (int r = 0; r < VPT; ++r) {
-    const int i = i0 + r;
-    v[r] = (r < per && i < V) ? __ldcg(logits + i) : 0.f;
-  }
-  if (history != nullptr && rep != 1.0f) {
-#pragma unroll
-    for (int r = 0; r < VPT; ++r) {
-      const int i = i0 + r;
-      if (r < per && i < V && history[i]) v[r] = v[r] > 0.0f ? __fdiv_rn(v[r], rep) : __fmul_rn(v[r], rep);
-    }
-  }
-}
-
-// Greedy: the argmax (lowest index on ties) of the penalised logits.
-template <class G, int VPT>
-__device__ __noinline__ int fast_argmax(FastSamplerSmem& sm, const float* logits, int V, float rep,
-                                        const uint8_t* history) {
-  const int tid = G::tid(), lane = tid & 31, warp = tid >> 5;
-  const int per = (V + FAST_NT - 1) / FAST_NT, i0 = tid * per;
-  float v[VPT];
-  fast_load<VPT>(v, logits, V, i0, per, rep, history);
-  unsigned long long best = 0ull;
-#pragma unroll
-  for (int r = 0; r < VPT; ++r) {
-    const int i = i0 + r;
-    if (r < per && i < V) {
-      const unsigned long long k = skey(v[r], i);
-      best = k > best ? k : best;
-    }
-  }
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long t = __shfl_xor_sync(0xffffffffu, best, o);
-    best = t > best ? t : best;
-  }
-  if (lane == 0) sm.wbest[warp] = best;
-  G::sync();
-  unsigned long long b = 0ull;
-  for (int w = 0; w < FAST_NW; ++w) b = sm.wbest[w] > b ? sm.wbest[w] : b;
-  G::sync();
-  return key_index(b);
 }
 
 // Fallback selection from the value keys in sm.keys[0..V): the K-th largest
@@ -444,9 +396,14 @@ __device__ __noinline__ void fast_select_bisect(FastSamplerSmem& sm, int V, int 
   }
 }
 
-// Sampling with top-k (1 <= k <= 64), thread t holding logits
-// [t per, (t + 1) per) in registers (per <= VPT) as 64-bit keys.  The k
-// largest keys are found without a serial search in the common case:
+// The draw of the frame kernel: greedy, or sampling with 1 <= top_k <= 64,
+// run by a group of 256 threads (8 warps) on V <= SAMPLER_VMAX logits (V a
+// multiple of 4, logits 16-byte and history 4-byte aligned): thread t reads
+// float4 q of the logits at elements 4 (t + 256 q) (a warp's loads are
+// contiguous) and keeps their 32-bit value keys in shared memory; candidates
+// are 64-bit keys (value key, inverted index).  Greedy is the same rule with k = 1 and T = 1 (dividing by 1 is
+// exact): the largest penalised logit, lowest index on ties.  The k largest
+// keys are found without a serial search in the common case:
 //   1. a lower bound theta on the k-th largest key: every lane's largest key,
 //      sorted per warp; the k-th largest of the warps' 8 largest lane maxima
 //      (a subset of the keys, so at least k keys are >= theta);
@@ -455,30 +412,39 @@ __device__ __noinline__ void fast_select_bisect(FastSamplerSmem& sm, int V, int 
 // If more than FAST_CAP keys pass the bound (many equal logits), the k-th
 // largest key is found by bisection instead (fast_select_bisect).  The draw is
 // the float rule of group_sample on the ordered candidates.
-template <class G, int VPT>
-__device__ __noinline__ int fast_topk(FastSamplerSmem& sm, const float* logits, int V, int top_k, float top_p,
-                                      float temperature, float rep, const uint8_t* history, float u) {
+template <class G>
+__device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits, int V, int do_sample,
+                                        int top_k, float top_p, float temperature, float rep,
+                                        const uint8_t* history, float u) {
   const int tid = G::tid(), lane = tid & 31, warp = tid >> 5;
-  const int per = (V + FAST_NT - 1) / FAST_NT, i0 = tid * per;
-  float v[VPT];
-  fast_load<VPT>(v, logits, V, i0, per, rep, history);
-  uint32_t key[VPT];
-#pragma unroll
-  for (int r = 0; r < VPT; ++r) {
-    const int i = i0 + r;
-    // 0 is below the key of every float, so padding never counts
-    key[r] = (r < per && i < V) ? fkey(__fdiv_rn(v[r], temperature)) : 0u;
-  }
-  const int K = (top_k <= 0 || top_k >= V) ? V : top_k;  // caller: K <= SAMPLER_KSMALL
-  // 1) theta: the lane's largest key, sorted descending across the warp
-  //    (bitonic network); lanes 0..7 post the warp's 8 largest
+  const int K = !do_sample ? 1 : ((top_k <= 0 || top_k >= V) ? V : top_k);  // caller: K <= SAMPLER_KSMALL
+  const float T = do_sample ? temperature : 1.0f;
+  const float P = do_sample ? top_p : 1.0f;
+  const bool pen = history != nullptr && rep != 1.0f;
+  // value keys of the thread's logits (float4 q: elements 4 (tid + FAST_NT q)
+  // .. + 3) into sm.keys, the lane's largest (key, index) kept: rolled loops,
+  // so the float divisions of the rule appear once in the code
   unsigned long long lm = 0ull;
-#pragma unroll
-  for (int r = 0; r < VPT; ++r) {
-    const unsigned long long k = key[r] ? ((unsigned long long)key[r] << 32) | (0xffffffffu - (uint32_t)(i0 + r))
-                                        : 0ull;
-    lm = k > lm ? k : lm;
+#pragma unroll 1
+  for (int q = 0; q < FAST_V4; ++q) {
+    const int e = 4 * (tid + FAST_NT * q);
+    if (e >= V) break;
+    float4 v = __ldcg(reinterpret_cast<const float4*>(logits + e));
+    uint32_t hb = pen ? *reinterpret_cast<const uint32_t*>(history + e) : 0u;
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+      float l = v.x;
+      if (hb & 0xffu) l = l > 0.0f ? __fdiv_rn(l, rep) : __fmul_rn(l, rep);
+      const uint32_t kv = fkey(__fdiv_rn(l, T));
+      sm.keys[e + k] = kv;
+      const unsigned long long kk = ((unsigned long long)kv << 32) | (0xffffffffu - (uint32_t)(e + k));
+      lm = kk > lm ? kk : lm;
+      v = make_float4(v.y, v.z, v.w, 0.f);
+      hb >>= 8;
+    }
   }
+  // 1) theta: the lanes' largest keys sorted descending across the warp
+  //    (bitonic network); lanes 0..7 post the warp's 8 largest
 #pragma unroll
   for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
@@ -496,7 +462,6 @@ __device__ __noinline__ int fast_topk(FastSamplerSmem& sm, const float* logits, 
   G::sync();
   if (warp == 0) {
     // the K-th largest posted key (posted real keys are distinct; zeros are padding)
-#pragma unroll
     for (int h = 0; h < FAST_NW * FAST_TOP / 32; ++h) {
       const unsigned long long my = sm.top[lane + 32 * h];
       int rank = 0;
@@ -506,24 +471,27 @@ __device__ __noinline__ int fast_topk(FastSamplerSmem& sm, const float* logits, 
     }
   }
   G::sync();
-  // 2) gather the keys >= theta
+  // 2) gather the keys >= theta (a thread reads back its own keys)
   const unsigned long long theta = sm.theta;
+#pragma unroll 1
+  for (int q = 0; q < FAST_V4; ++q) {
+    const int e = 4 * (tid + FAST_NT * q);
+    if (e >= V) break;
+    const uint4 kv = *reinterpret_cast<const uint4*>(&sm.keys[e]);
+    const uint32_t ks[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-  for (int r = 0; r < VPT; ++r) {
-    const unsigned long long k = ((unsigned long long)key[r] << 32) | (0xffffffffu - (uint32_t)(i0 + r));
-    if (key[r] != 0u && k >= theta) {
-      const int slot = atomicAdd(&sm.n_cand, 1);
-      if (slot < FAST_CAP) sm.cand[slot] = k;
+    for (int k = 0; k < 4; ++k) {
+      const unsigned long long kk = ((unsigned long long)ks[k] << 32) | (0xffffffffu - (uint32_t)(e + k));
+      if (kk >= theta) {
+        const int slot = atomicAdd(&sm.n_cand, 1);
+        if (slot < FAST_CAP) sm.cand[slot] = kk;
+      }
     }
   }
   G::sync();
   const int C = sm.n_cand;
   if (C > FAST_CAP) {
-#pragma unroll
-    for (int r = 0; r < VPT; ++r)
-      if (r < per && i0 + r < V) sm.keys[i0 + r] = key[r];
-    G::sync();  // every thread has read n_cand and posted its keys
-    fast_select_bisect<G>(sm, V, K);
+    fast_select_bisect<G>(sm, V, K);  // sm.keys holds every key
   } else if (tid < C) {
     const unsigned long long my = sm.cand[tid];
     int rank = 0;
@@ -545,9 +513,9 @@ __device__ __noinline__ int fast_topk(FastSamplerSmem& sm, const float* logits, 
     __syncwarp();
     const float r0 = lane < K ? sm.run[lane] : 0.f, r1 = lane + 32 < K ? sm.run[lane + 32] : 0.f;
     int kept = K;
-    if (top_p < 1.0f) {
+    if (P < 1.0f) {
       // the first i with run_i >= top_p * z (z = run_{K-1}) closes the nucleus
-      const float tp = __fmul_rn(top_p, sm.run[K - 1]);
+      const float tp = __fmul_rn(P, sm.run[K - 1]);
       const unsigned b0 = __ballot_sync(0xffffffffu, lane < K && r0 >= tp);
       const unsigned b1 = __ballot_sync(0xffffffffu, lane + 32 < K && r1 >= tp);
       kept = b0 ? __ffs(b0) : (b1 ? 32 + __ffs(b1) : K);
@@ -563,21 +531,6 @@ __device__ __noinline__ int fast_topk(FastSamplerSmem& sm, const float* logits, 
   const int pick = sm.pick;
   G::sync();
   return pick;
-}
-
-// Register-resident variant of the same rule for greedy or 1 <= k <= 64, run
-// by a group of 256 threads (8 warps) on at most SAMPLER_VMAX logits.  Each
-// case is its own function, specialised on the logits per thread (8 covers
-// V <= 2048), so a draw runs through compact code.
-template <class G>
-__device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits, int V, int do_sample,
-                                        int top_k, float top_p, float temperature, float rep,
-                                        const uint8_t* history, float u) {
-  const bool small = V <= 8 * FAST_NT;
-  if (!do_sample)
-    return small ? fast_argmax<G, 8>(sm, logits, V, rep, history) : fast_argmax<G, FAST_VPT>(sm, logits, V, rep, history);
-  return small ? fast_topk<G, 8>(sm, logits, V, top_k, top_p, temperature, rep, history, u)
-               : fast_topk<G, FAST_VPT>(sm, logits, V, top_k, top_p, temperature, rep, history, u);
 }
 
 }  // namespace q3
