@@ -62,7 +62,7 @@ constexpr int FK_PREFETCH_THREADS = 32;  // one warp; one thread issues L2 prefe
 constexpr int FK_THREADS = FK_PRODUCER_THREADS + FK_CONSUMERS + FK_PREFETCH_THREADS;
 constexpr int FK_STAGE = 8192;  // one ring chunk: 2 rows of 2048 bf16, one o_proj tile of 32 x 128 bf16
 constexpr int FK_NSTAGE = 20;
-constexpr int FK_PF_AHEAD = 40;  // chunks the L2 prefetch runs ahead of the ring's copies
+constexpr int FK_PF_AHEAD = 0;  // default distance (chunks) the L2 prefetch runs ahead of the ring: off (deeper prefetch queues up memory traffic that delays the latency-bound phases)
 constexpr int FK_TMAX = 2;     // tokens per pass (CodePredictor pass 0 carries two)
 constexpr int FK_DMAX = 2048;  // widest hidden state staged in shared memory
 constexpr int FK_HDMAX = 128;
@@ -104,11 +104,20 @@ struct FKParams {
   KVDesc tkv, ckv;
   const float* rope_cos;
   const float* rope_sin;
-  float *R, *dA, *dF;  // [FK_KC][xstride] each: copies of [tokens][D]
+  // residual stream (see xbase), by layer parity: base vectors, attention
+  // deltas, FFN deltas (FK_KC copies); each [tokens][D] within xstride floats
+  float* xb;  // [2][xstride]
+  float* xa;  // [2][xstride]
+  float* xf;  // [2][FK_KC][xstride]
   int xstride;
-  float* qkv;          // [FK_TMAX][qkv_rows]
-  float* part;         // [Hq][cpg][hd + 2]
-  float* cp_logits;    // [Vc]
+  // values handed from one phase to the next without a grid barrier, each
+  // stored with the tag of the step that wrote it (see tag_of)
+  uint64_t* qkv;        // [FK_TMAX][qkv_rows]
+  uint64_t* z;          // [FK_TMAX][Dc]: the CodePredictor input projection
+  uint64_t* part;       // [Hq][cpg][hd + 2]: Talker attention partials
+  uint64_t* cp_logits;  // [Vc]
+  uint32_t seq;         // this launch's sequence number
+  int pf_ahead;         // chunks the L2 prefetch warp may run ahead of the ring (0: off)
   unsigned* bar;
   unsigned* done;
   int* err;
@@ -130,7 +139,10 @@ struct FKState {
   char* sideC;
   LayerDev* tl;
   LayerDev* cl;
-  float *R, *dA, *dF, *qkv, *part, *cp_logits;
+  float *xb, *xa, *xf;
+  uint64_t *qkv, *z, *part, *cp_logits;
+  uint32_t seq;  // launches of this handle with its workspace scratch
+  int pf_ahead;  // L2 prefetch distance in chunks (Q3TTS_PF_AHEAD at create; 0 turns it off)
   unsigned *bar, *done;
   int* abort_flag;
   int ncta, dmax;
@@ -232,6 +244,22 @@ __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
 
 __device__ __forceinline__ int ld_volatile(const int* p) { return *(const volatile int*)p; }
 
+// A value handed between CTAs without a grid barrier travels with a tag in
+// one 64-bit word (value bits | tag << 32), written and read as relaxed
+// gpu-scope accesses: an aligned 64-bit access is single-copy atomic, so a
+// reader that sees the expected tag sees the value stored with it.
+__device__ __forceinline__ uint64_t tag_word(float v, uint32_t tag) {
+  return ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(v);
+}
+__device__ __forceinline__ void st_tagged(uint64_t* p, float v, uint32_t tag) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(tag_word(v, tag)) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_relaxed64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
 
 // Part i of n items cut into `parts` near-equal parts.  32-bit unsigned
@@ -300,7 +328,8 @@ static_assert(FK_PAIRS >= FK_REPMAX, "talker attention keeps one partial per q h
 struct ConsState {
   uint32_t n, phase, layer;
   int aborted;
-  int j, k, in, from_xs, fed0;  // the frame schedule's loop state: pass j, its step k
+  int j, k, s, src, fed0;  // the frame schedule's loop state: pass j, its step k, step s of the frame;
+                           // where the next QKV step finds its input (SRC_*)
 };
 
 constexpr int FK_MAXPAGES = 256;  // Talker pages per stream kept in shared memory
@@ -444,6 +473,51 @@ __device__ __forceinline__ void raise_abort(const FKParams& p, int code) {
   atomicCAS(p.err, 0, code);
   atomicExch(p.abort_flag, 1);
 }
+
+// The tag of frame step s: unique over the launches of a workspace (the host
+// numbers them), so a word left by an earlier step or frame never passes for
+// the current one.
+constexpr int FK_MAXSTEPS = 1024;  // steps of a frame (checked at create)
+__device__ __forceinline__ uint32_t tag_of(int s) { return fk_prm()->seq * (uint32_t)FK_MAXSTEPS + (uint32_t)s; }
+
+// Whether a thread waiting for tagged words should stop: the abort flag, or
+// its bound (wait_cycles since t0) ran out, which it records.
+__device__ __noinline__ bool tag_give_up(long long t0) {
+  if (ld_volatile(fk_prm()->abort_flag)) return true;
+  if (clock64() - t0 > fk_prm()->wait_cycles) {
+    raise_abort(*fk_prm(), Q3TTS_ERR_TIMEOUT);
+    return true;
+  }
+  return false;
+}
+
+// Resolves N words loaded (raw) from base + off[i]: each poll re-loads every
+// word whose tag is not yet `tag`, all together, so the wait ends about one
+// round trip after the last of them is written.  Entries a caller does not
+// need hold a word already tagged `tag`.  After an abort or a timeout the
+// words stay as they are.
+template <int N>
+__device__ __forceinline__ void tag_resolve(uint64_t (&raw)[N], const uint64_t* base, const int (&off)[N],
+                                            uint32_t tag) {
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < N; ++i) ok = ok && (uint32_t)(raw[i] >> 32) == tag;
+  if (ok) return;
+  const long long t0 = clock64();
+  unsigned it = 0;
+  while (true) {
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if ((uint32_t)(raw[i] >> 32) != tag) raw[i] = ld_relaxed64(base + off[i]);
+    ok = true;
+#pragma unroll
+    for (int i = 0; i < N; ++i) ok = ok && (uint32_t)(raw[i] >> 32) == tag;
+    if (ok || ((++it & 15u) == 0 && tag_give_up(t0))) break;
+  }
+}
+
+__device__ __forceinline__ float tag_float(uint64_t w) { return __uint_as_float((uint32_t)w); }
+__device__ __forceinline__ uint64_t tag_filler(uint32_t tag) { return (uint64_t)tag << 32; }
 
 // Bounded wait on an arbitrary mbarrier phase (all lanes of the calling warp).
 __device__ __forceinline__ void wait_bar(Cons c, uint64_t* bar, unsigned par) {
@@ -647,13 +721,21 @@ __device__ __forceinline__ void dots(uint32_t w, const uint32_t (&ro)[NR], int K
       for (int t = 0; t < T; ++t) acc[r][t] += __shfl_xor_sync(0xffffffffu, acc[r][t], o);
 }
 
+// Where a row GEMV puts its outputs: out[t * ts + row] as a plain float, or
+// out64[t * ts + row] as a word tagged `tag` (out64 non-null).
+struct RowsOut {
+  float* out;
+  uint64_t* out64;
+  uint32_t tag;
+  int ts;
+};
+
 // Rows base + r0 .. base + r0 + NR - 1 of a chunk (row stride rb) against T
-// tokens, stored as out[t * ts + row] = inv_t (row . x_t) by lane r T + t (the
-// stores go out together); with zero_stride > 0 the same element of the
-// residual copies 1 .. FK_KC - 1 is cleared too.
+// tokens, inv_t (row . x_t) stored by lane r T + t (the stores go out
+// together).
 template <class WT, int T, int NR>
-__device__ __forceinline__ void rows_group(uint32_t buf, int rb, int r0, int K, uint32_t xs, int lane, float* out,
-                                           int ts, int base, const float (&inv)[T], int zero_stride) {
+__device__ __forceinline__ void rows_group(uint32_t buf, int rb, int r0, int K, uint32_t xs, int lane,
+                                           const RowsOut& o, int base, const float (&inv)[T]) {
   uint32_t ro[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) ro[r] = (uint32_t)((r0 + r) * rb);
@@ -664,24 +746,22 @@ __device__ __forceinline__ void rows_group(uint32_t buf, int rb, int r0, int K, 
 #pragma unroll
     for (int t = 0; t < T; ++t)
       if (lane == r * T + t) {
-        float* o = out + t * ts + base + r0 + r;
-        *o = acc[r][t] * inv[t];
-        if (zero_stride)
-#pragma unroll
-          for (int k = 1; k < FK_KC; ++k) o[k * zero_stride] = 0.f;
+        const int i = t * o.ts + base + r0 + r;
+        if (o.out64)
+          st_tagged(o.out64 + i, acc[r][t] * inv[t], o.tag);
+        else
+          o.out[i] = acc[r][t] * inv[t];
       }
 }
 
 // Rows [r0, r1) of a row-major [*, K] matrix streamed from the ring (the
 // private chunks the producer cut them into) against T staged vectors at
-// shared offset xs: out[t * ts + row] = inv_t (row . x_t).  With zero_stride >
-// 0, out is copy 0 of a residual buffer and the same element of its other
-// FK_KC - 1 copies (zero_stride floats apart) is cleared.  A chunk's rows go
-// in groups of 4, then 2, then 1.  Advances the ring position past the rows'
-// chunks.
+// shared offset xs: output row of token t = inv_t (row . x_t), placed as o
+// says.  A chunk's rows go in groups of 4, then 2, then 1.  Advances the ring
+// position past the rows' chunks.
 template <class WT, int T>
-__device__ __forceinline__ void stream_rows_t(Cons c, int r0, int r1, int K, uint32_t xs, float* out, int ts,
-                                              const float (&inv)[T], int zero_stride) {
+__device__ __forceinline__ void stream_rows_t(Cons c, int r0, int r1, int K, uint32_t xs, const RowsOut& o,
+                                              const float (&inv)[T]) {
   Stream s = stream_begin(c);
   const int rb = K * (int)sizeof(WT);
   const int rpc = rows_per_chunk(rb);
@@ -691,12 +771,12 @@ __device__ __forceinline__ void stream_rows_t(Cons c, int r0, int r1, int K, uin
     const uint32_t buf = chunk_wait(s, n);
     const int base = r0 + (int)(n - n0) * rpc, R = min(rpc, r1 - base);
     int r = 0;
-    for (; r + 4 <= R; r += 4) rows_group<WT, T, 4>(buf, rb, r, K, xs, s.lane, out, ts, base, inv, zero_stride);
+    for (; r + 4 <= R; r += 4) rows_group<WT, T, 4>(buf, rb, r, K, xs, s.lane, o, base, inv);
     if (r + 2 <= R) {
-      rows_group<WT, T, 2>(buf, rb, r, K, xs, s.lane, out, ts, base, inv, zero_stride);
+      rows_group<WT, T, 2>(buf, rb, r, K, xs, s.lane, o, base, inv);
       r += 2;
     }
-    if (r < R) rows_group<WT, T, 1>(buf, rb, r, K, xs, s.lane, out, ts, base, inv, zero_stride);
+    if (r < R) rows_group<WT, T, 1>(buf, rb, r, K, xs, s.lane, o, base, inv);
     release_private(s, n);
   }
   warp_set(cst().aborted, s.aborted ? 1 : 0);
@@ -704,33 +784,40 @@ __device__ __forceinline__ void stream_rows_t(Cons c, int r0, int r1, int K, uin
 }
 
 template <class WT>
-__device__ __forceinline__ void stream_rows(Cons c, int r0, int r1, int K, int T, uint32_t xs, float* out, int ts,
-                                            float inv0, float inv1, int zero_stride) {
+__device__ __forceinline__ void stream_rows(Cons c, int r0, int r1, int K, int T, uint32_t xs, const RowsOut& o,
+                                            float inv0, float inv1) {
   if (T == 1) {
     const float inv[1] = {inv0};
-    stream_rows_t<WT, 1>(c, r0, r1, K, xs, out, ts, inv, zero_stride);
+    stream_rows_t<WT, 1>(c, r0, r1, K, xs, o, inv);
   } else {
     const float inv[2] = {inv0, inv1};
-    stream_rows_t<WT, 2>(c, r0, r1, K, xs, out, ts, inv, zero_stride);
+    stream_rows_t<WT, 2>(c, r0, r1, K, xs, o, inv);
   }
 }
 
 // ------------------------------------------------------- residual helpers
 
-// Residual stream: three rotating buffers X0..X2, each FK_KC copies of
-// [tokens][D] (D the width of the stack running; copy stride p.xstride
-// floats).  A buffer's value is the sum of its copies: the split-K partial
-// sums of all CTAs are added into copy (CTA % FK_KC), so that fewer CTAs add
-// into any one cache line.  A layer whose input sits in X_i folds it (each
-// CTA its slice) into copy 0 of X_{i+1} and X_{i+2} and clears their other
-// copies there; attention output is added into both, the FFN output into
-// X_{i+2}, which is the next layer's input.  So every phase reads one complete
-// vector: phase A reads X_i, phase C reads X_{i+1}.
-__device__ __forceinline__ float* xbuf(const FKParams& p, int idx, int copy) {
-  float* base = idx == 0 ? p.R : (idx == 1 ? p.dA : p.dF);
-  return base + (size_t)copy * p.xstride;
+// Residual stream.  Layer k of the frame (CodePredictor layers of the 15
+// passes, then the Talker's) keeps, by the parity of k, [tokens][D] vectors
+// (D the width of its stack): xbase(k), its input x_k, which the QKV phase
+// writes (each CTA its slice; nobody adds into it); xattn(k), which the o_proj
+// tiles of all CTAs add into; and xffn(k), FK_KC copies which the FFN's
+// split-K sums of CTA c add into (copy c % FK_KC, so fewer CTAs add into one
+// cache line).  So the FFN phase reads x_k + a_k = xbase + xattn, and layer
+// k + 1 (or a head) reads x_{k+1} = xbase + xattn + the sum of the xffn copies.
+// The FFN phase of layer k clears its CTA's slice of xattn(k + 1) and xffn(k +
+// 1) (their last readers -- layer k's QKV phase -- are past the grid barrier
+// that closed layer k's attention); the frame's first layer finds its deltas
+// cleared at the start of the frame.
+__device__ __forceinline__ float* xbase(const FKParams& p, int k) { return p.xb + (size_t)(k & 1) * p.xstride; }
+__device__ __forceinline__ float* xattn(const FKParams& p, int k) { return p.xa + (size_t)(k & 1) * p.xstride; }
+__device__ __forceinline__ float* xffn(const FKParams& p, int k, int copy) {
+  return p.xf + ((size_t)(k & 1) * FK_KC + copy) * p.xstride;
 }
-__device__ __forceinline__ int xnext(int i, int k) { return (i + k) % 3; }
+
+// Where load_norm finds its input: raw tokens in xs, the tagged projection z,
+// or the residual of a layer (x + a + f, or x + a within the FFN phase).
+enum { SRC_XS = 0, SRC_Z = 1, SRC_RES = 2, SRC_RES_A = 3 };
 
 // Gains g[i .. i+3] (weight dtype) as floats.
 template <class WT>
@@ -762,46 +849,71 @@ __device__ __forceinline__ float norm_inv(int t, int D) {
   return 1.0f / sqrtf(a / (float)D + fk_prm()->eps);
 }
 
-// Stages y_t = g * x_t in xs (plane layout) for t < T, where x_t is xs[t]
-// itself (from_xs, raw plane layout) or token t0 + t of buffer X_src (the sum
-// of its copies), and leaves x_t's partial sums of squares in red[t][warp]:
+// Stages y_t = g * x_t in xs (plane layout) for t < T, where x_t comes from
+// src: SRC_XS, xs itself (raw plane layout); SRC_Z, token t of the tagged
+// projection z (tag ztag); SRC_RES / SRC_RES_A, token t0 + t of layer kp's
+// residual.  Leaves x_t's partial sums of squares in red[t][warp]:
 // RMSNorm(x_t) * g = y_t / rms_t, and the GEMVs that follow scale their sums
 // by 1 / rms_t (norm_inv) instead of normalising first, so staging takes one
 // block-wide barrier.  Thread e handles plane float4 e + 256 u of the T
-// tokens, all of its loads issued together.  With fold_a >= 0 the CTA's slice
-// of each raw x_t goes to copy 0 of X_fold_a and X_fold_b, whose other copies
-// of the slice are cleared.  If out is given, the CTA's slice of the normed
-// x_0 goes there.  g points into shared memory (4-element aligned groups).
+// tokens, all of its loads issued together.  With fold >= 0 the CTA's slice of
+// each raw x_t goes to xbase(fold).  If out is given, the CTA's slice of the
+// normed x_0 goes there.  g points into shared memory (4-element aligned
+// groups).
 template <class WT>
-__device__ __forceinline__ void load_norm(Cons c, bool from_xs, int src, int t0, int T, int D, const WT* g,
-                                          int fold_a, int fold_b, float* out) {
+__device__ __forceinline__ void load_norm(Cons c, int src, int kp, uint32_t ztag, int t0, int T, int D, const WT* g,
+                                          int fold, float* out) {
   const FKParams& p = *fk_prm();
   float* xs = fk_sm()->u.g.xs;
   constexpr int PER = FK_DMAX / 4 / FK_CONSUMERS;  // float4 per thread: T D <= FK_DMAX (checked at create)
   const int nq = D >> 2, tot = T * nq, tid = ctid();
   float4 xv[PER];
-  if (from_xs) {
+  if (src == SRC_XS) {
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
       const int e = tid + FK_CONSUMERS * u;
       xv[u] = e < tot ? reinterpret_cast<const float4*>(xs)[e] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+  } else if (src == SRC_Z) {
+    uint64_t raw[PER * 4];
+    int off[PER * 4];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int e = tid + FK_CONSUMERS * u;
+      const int t = e >= nq ? 1 : 0;
+      const int o = e < tot ? t * D + plane_first(e - t * nq, D) : 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        off[4 * u + k] = o + k;
+        raw[4 * u + k] = e < tot ? ld_relaxed64(p.z + o + k) : tag_filler(ztag);
+      }
+    }
+    tag_resolve<PER * 4>(raw, p.z, off, ztag);
+#pragma unroll
+    for (int u = 0; u < PER; ++u)
+      xv[u] = make_float4(tag_float(raw[4 * u]), tag_float(raw[4 * u + 1]), tag_float(raw[4 * u + 2]),
+                          tag_float(raw[4 * u + 3]));
   } else {
-    const float* xg = xbuf(p, src, 0) + t0 * D;
+    const float* xg = xbase(p, kp) + t0 * D;
+    const float* ag = xattn(p, kp) + t0 * D;
+    const float* fg = xffn(p, kp, 0) + t0 * D;
     const int xst = p.xstride;
+    const bool with_f = src == SRC_RES;
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
       const int e = tid + FK_CONSUMERS * u;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       if (e < tot) {
         const int t = e >= nq ? 1 : 0;
-        const float* q = xg + t * D + plane_first(e - t * nq, D);
-        float4 cv[FK_KC];
+        const int o = t * D + plane_first(e - t * nq, D);
+        float4 cv[2 + FK_KC];
+        cv[0] = ldcg4(xg + o);
+        cv[1] = ldcg4(ag + o);
 #pragma unroll
-        for (int k = 0; k < FK_KC; ++k) cv[k] = ldcg4(q + k * xst);
+        for (int k = 0; k < FK_KC; ++k) cv[2 + k] = with_f ? ldcg4(fg + k * xst + o) : make_float4(0.f, 0.f, 0.f, 0.f);
         v = cv[0];
 #pragma unroll
-        for (int k = 1; k < FK_KC; ++k) {
+        for (int k = 1; k < 2 + FK_KC; ++k) {
           v.x += cv[k].x; v.y += cv[k].y; v.z += cv[k].z; v.w += cv[k].w;
         }
       }
@@ -824,10 +936,8 @@ __device__ __forceinline__ void load_norm(Cons c, bool from_xs, int src, int t0,
   }
   int lo, hi;
   cta_slice(D, lo, hi);
-  if (fold_a >= 0) {
-    const int xst = p.xstride;
-    float* fa = xbuf(p, fold_a, 0);
-    float* fb = xbuf(p, fold_b, 0);
+  if (fold >= 0) {
+    float* fb = xbase(p, fold);
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
       const int e = tid + FK_CONSUMERS * u;
@@ -837,16 +947,7 @@ __device__ __forceinline__ void load_norm(Cons c, bool from_xs, int src, int t0,
           const float vals[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            if (i + q >= lo && i + q < hi) {
-              const int o = t * D + i + q;
-              fa[o] = vals[q];
-              fb[o] = vals[q];
-#pragma unroll
-              for (int k = 1; k < FK_KC; ++k) {
-                fa[o + k * xst] = 0.f;
-                fb[o + k * xst] = 0.f;
-              }
-            }
+            if (i + q >= lo && i + q < hi) fb[t * D + i + q] = vals[q];
         }
       }
     }
@@ -931,23 +1032,60 @@ constexpr int TALKER_ROPE_ROW = 16;
 // ------------------------------------------------------------ the sampler
 
 // Draws code j of the frame (0: semantic from the pending Talker logits; 1..15:
-// acoustic from the last CodePredictor head) in every CTA, identically.
-// Returns the code fed forward (the forced code under teacher forcing).
-__device__ __noinline__ int draw_code(Cons c, int j) {
+// acoustic from the last CodePredictor head, whose words carry tag ltag) in
+// every CTA, identically.  The logits are staged in shared memory (the
+// sampler turns them into keys in place).  Returns the code fed forward (the
+// forced code under teacher forcing).
+__device__ __noinline__ int draw_code(Cons c, int j, uint32_t ltag) {
   const FKParams& p = *fk_prm();
   const bool sem = j == 0;
   const int V = sem ? p.Vt : p.Vc;
-  const float* src = sem ? p.pending_logits + (size_t)p.sid * p.Vt : p.cp_logits;
-  if (p.dump && ccta() == 0) {
-    const int off = sem ? 0 : p.Vt + (j - 1) * p.Vc;
-    for (int i = ctid(); i < V; i += FK_CONSUMERS) p.dump[off + i] = __ldcg(src + i);
+  float* lv = reinterpret_cast<float*>(fk_sm()->u.smp.keys);
+  {
+    // float4 q of thread t: elements 4 (t + FK_CONSUMERS q) .. + 3 (V % 4 == 0)
+    const float* pl = p.pending_logits + (size_t)p.sid * p.Vt;
+    float4 v[FAST_V4];
+    if (sem) {
+#pragma unroll
+      for (int q = 0; q < FAST_V4; ++q) {
+        const int e = 4 * (ctid() + FK_CONSUMERS * q);
+        if (e < V) v[q] = ldcg4(pl + e);
+      }
+    } else {
+      uint64_t raw[4 * FAST_V4];
+      int off[4 * FAST_V4];
+#pragma unroll
+      for (int q = 0; q < FAST_V4; ++q) {
+        const int e = 4 * (ctid() + FK_CONSUMERS * q);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          off[4 * q + k] = e < V ? e + k : 0;
+          raw[4 * q + k] = e < V ? ld_relaxed64(p.cp_logits + e + k) : tag_filler(ltag);
+        }
+      }
+      tag_resolve<4 * FAST_V4>(raw, p.cp_logits, off, ltag);
+#pragma unroll
+      for (int q = 0; q < FAST_V4; ++q)
+        v[q] = make_float4(tag_float(raw[4 * q]), tag_float(raw[4 * q + 1]), tag_float(raw[4 * q + 2]),
+                           tag_float(raw[4 * q + 3]));
+    }
+    float* dump = p.dump && ccta() == 0 ? p.dump + (sem ? 0 : p.Vt + (j - 1) * p.Vc) : nullptr;
+#pragma unroll
+    for (int q = 0; q < FAST_V4; ++q) {
+      const int e = 4 * (ctid() + FK_CONSUMERS * q);
+      if (e < V) {
+        *reinterpret_cast<float4*>(lv + e) = v[q];
+        if (dump) *reinterpret_cast<float4*>(dump + e) = v[q];
+      }
+    }
   }
-  int code = fast_sample<ConsGroup>(fk_sm()->u.smp, src, V, sem ? p.sp.do_sample : p.sp.sub_do_sample,
+  consumer_sync();
+  int code = fast_sample<ConsGroup>(fk_sm()->u.smp, lv, V, sem ? p.sp.do_sample : p.sp.sub_do_sample,
                                     sem ? p.sp.top_k : p.sp.sub_top_k, sem ? p.sp.top_p : p.sp.sub_top_p,
                                     sem ? p.sp.temperature : p.sp.sub_temperature,
                                     sem ? p.sp.repetition_penalty : 1.0f,
                                     sem ? p.history + (size_t)p.sid * p.Vt : nullptr, fk_sm()->uni[j]);
-  FK_MARK(TR_SUB, 7);
+  FK_MARK(TR_SUB, 7);  // (draw done)
   code = min(max(code, 0), V - 1);
   int fed = code;
   if (p.forced) {
@@ -986,20 +1124,18 @@ __device__ __forceinline__ void oproj_tiles(const FKParams& p, int D, int cta, i
 
 // The CTA's o_proj tiles, one per ring chunk and private to a warp, against
 // the attention outputs of the CTA's (<= 2) heads (os, plane layout) for T
-// tokens; lane l owns column 32 j + l of its tile, and each column's sum goes
-// into copy CTA % FK_KC of both X_a and X_b.  Closes the attention phase with
-// a grid barrier.
+// tokens; lane l owns column 32 j + l of its tile, and each column's sum is
+// added into xattn(k).  Closes the attention phase of layer k with a grid
+// barrier.
 template <class WT>
-__device__ __forceinline__ void oproj_step(Cons c, int D, int T, int xa, int xb) {
+__device__ __forceinline__ void oproj_step(Cons c, int D, int T, int k) {
   const FKParams& p = *fk_prm();
   Stream s = stream_begin(c);
   const int hd = p.hd, nt = oproj_nt(D), nkb = hd >> 3;
   int t0, t1;
   oproj_tiles(p, D, ccta(), t0, t1);
   const int h_first = t0 / nt;
-  const int cpy = ccta() % FK_KC;
-  float* XA = xbuf(p, xa, cpy);
-  float* XB = xbuf(p, xb, cpy);
+  float* XA = xattn(p, k);
   const uint32_t os0 = soff(fk_sm()->os[0][0]);
   constexpr uint32_t OS_HEAD = FK_TMAX * FK_HDMAX * 4, OS_TOK = FK_HDMAX * 4;
   const uint32_t n0 = cst().n;
@@ -1026,10 +1162,7 @@ __device__ __forceinline__ void oproj_step(Cons c, int D, int T, int xa, int xb)
     if (col < D)
 #pragma unroll
       for (int t = 0; t < FK_TMAX; ++t)
-        if (t < T) {
-          atomicAdd(XA + t * D + col, a[t]);
-          atomicAdd(XB + t * D + col, a[t]);
-        }
+        if (t < T) atomicAdd(XA + t * D + col, a[t]);
   }
   warp_set(cst().aborted, s.aborted ? 1 : 0);
   warp_set(cst().n, n0 + nch);
@@ -1047,7 +1180,7 @@ __device__ __forceinline__ void store_head_plane(float* dst, int hd, const float
 // softmax sums are combined across warps.  The CTA owning column 0 of the
 // first q head of a kv group appends that group's current k, v to the cache.
 template <class WT>
-__device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0, int xa, int xb) {
+__device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0, int k, uint32_t qtag) {
   const FKParams& p = *fk_prm();
   const int D = p.Dc, hd = p.hd, Hq = p.Hq, Hkv = p.Hkv, rep = Hq / Hkv, J = hd / 32;
   const int nt = oproj_nt(D);
@@ -1072,16 +1205,51 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
     for (int gi = 0; gi < 2; ++gi) {
       const int g = g_first + gi;
       if (sp < S && gi < ng) {
-        const bool cur = sp >= pos0;
-        const float* kc = (const float*)p.ckv.pool + ckv_offset(p, layer, cur ? 0 : sp, 0, g);
-        const float* vc = cur ? p.qkv + (size_t)(sp - pos0) * p.qkv_rows + (Hq + Hkv + g) * hd
-                              : (const float*)p.ckv.pool + ckv_offset(p, layer, sp, 1, g);
+        if (sp < pos0) {
+          const float* kc = (const float*)p.ckv.pool + ckv_offset(p, layer, sp, 0, g);
+          const float* vc = (const float*)p.ckv.pool + ckv_offset(p, layer, sp, 1, g);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          kk[np][gi][j] = (j < J && !cur) ? __ldcg(kc + clane() + 32 * j) : 0.f;
-          vv[np][gi][j] = j < J ? __ldcg(vc + clane() + 32 * j) : 0.f;
+          for (int j = 0; j < 4; ++j) {
+            kk[np][gi][j] = j < J ? __ldcg(kc + clane() + 32 * j) : 0.f;
+            vv[np][gi][j] = j < J ? __ldcg(vc + clane() + 32 * j) : 0.f;
+          }
+        } else {  // a position of this pass: its v from the tagged QKV rows, resolved below
+#pragma unroll
+          for (int j = 0; j < 4; ++j) kk[np][gi][j] = vv[np][gi][j] = 0.f;
         }
       }
+    }
+  }
+  // the current positions' v (after the cached rows' loads went out), all
+  // resolved together
+  {
+    uint64_t raw[16];
+    int off[16];
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      const int sp = cwarp() + FK_CONSUMER_WARPS * np;
+#pragma unroll
+      for (int gi = 0; gi < 2; ++gi) {
+        const bool need = sp < S && gi < ng && sp >= pos0;
+        const int o = need ? (sp - pos0) * p.qkv_rows + (Hq + Hkv + g_first + gi) * hd + clane() : 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = (np * 2 + gi) * 4 + j;
+          off[i] = o + 32 * j;
+          raw[i] = (need && j < J) ? ld_relaxed64(p.qkv + o + 32 * j) : tag_filler(qtag);
+        }
+      }
+    }
+    tag_resolve<16>(raw, p.qkv, off, qtag);
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      const int sp = cwarp() + FK_CONSUMER_WARPS * np;
+#pragma unroll
+      for (int gi = 0; gi < 2; ++gi)
+        if (sp < S && gi < ng && sp >= pos0)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (j < J) vv[np][gi][j] = tag_float(raw[(np * 2 + gi) * 4 + j]);
     }
   }
   // 1) q of each (head, token) pair, normalised and rotated (warps < npair);
@@ -1095,24 +1263,35 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
       const int it = w - (FK_CONSUMER_WARPS - FK_PAIRS);
       const int t = isq ? w % T : it / ng, gi = isq ? 0 : it % ng;
       const int h = h_first + w / T, g = g_first + gi;
-      const float* src = p.qkv + (size_t)t * p.qkv_rows + (isq ? h * hd : (Hq + g) * hd);
+      const int so = t * p.qkv_rows + (isq ? h * hd : (Hq + g) * hd) + clane();
+      const int vo = t * p.qkv_rows + (Hq + Hkv + g) * hd + clane();
+      const bool app = isk && g * rep * nt >= v0 && g * rep * nt < v1;  // this CTA appends k, v
+      uint64_t raw[8];  // the q or k row, then (when appending) the v row
+      int off[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        off[j] = so + 32 * j;
+        off[4 + j] = vo + 32 * j;
+        raw[j] = j < J ? ld_relaxed64(p.qkv + so + 32 * j) : tag_filler(qtag);
+        raw[4 + j] = (j < J && app) ? ld_relaxed64(p.qkv + vo + 32 * j) : tag_filler(qtag);
+      }
+      tag_resolve<8>(raw, p.qkv, off, qtag);
       float v[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] = j < J ? __ldcg(src + clane() + 32 * j) : 0.f;
+      for (int j = 0; j < 4; ++j) v[j] = j < J ? tag_float(raw[j]) : 0.f;
       norm_rope_head(p, fk_sm(), v, isq ? side_gq<WT>(c, D) : side_gk<WT>(c, D), cp_rope_row(pos0 + t), clane());
       float* dst = isq ? as.q[w] : as.kcur[it];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         if (j < J) dst[clane() + 32 * j] = v[j];
-      if (isk && g * rep * nt >= v0 && g * rep * nt < v1) {
-        const float* vs = p.qkv + (size_t)t * p.qkv_rows + (Hq + Hkv + g) * hd;
+      if (app) {
         float* kc = (float*)p.ckv.pool + ckv_offset(p, layer, pos0 + t, 0, g);
         float* vc = (float*)p.ckv.pool + ckv_offset(p, layer, pos0 + t, 1, g);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           if (j < J) {
             kc[clane() + 32 * j] = v[j];
-            vc[clane() + 32 * j] = __ldcg(vs + clane() + 32 * j);
+            vc[clane() + 32 * j] = tag_float(raw[4 + j]);
           }
       }
     }
@@ -1183,7 +1362,7 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
   }
   consumer_sync();
   FK_MARK(TR_SUB, 6);
-  oproj_step<WT>(c, D, T, xa, xb);
+  oproj_step<WT>(c, D, T, k);
 }
 
 // Talker phase B1: attention partials.  Work item = (kv group g, position
@@ -1194,7 +1373,7 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
 // zero key, which the caller replaces; beyond it: zeros).
 template <class KT>
 __device__ __forceinline__ void talker_kv_rows(const FKParams& p, int layer, int g, int pos, int sb, int J,
-                                               float (&k)[2][4], float (&v)[2][4]) {
+                                               uint32_t qtag, float (&k)[2][4], float (&v)[2][4]) {
 #pragma unroll
   for (int b = 0; b < 2; ++b) {
     const int sp = sb + b * FK_CONSUMER_WARPS;
@@ -1207,18 +1386,28 @@ __device__ __forceinline__ void talker_kv_rows(const FKParams& p, int layer, int
         v[b][j] = j < J ? to_f(vc[clane() + 32 * j]) : 0.f;
       }
     } else {
-      const float* vs = p.qkv + (p.Hq + p.Hkv + g) * p.hd;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        k[b][j] = 0.f;
-        v[b][j] = (sp == pos && j < J) ? __ldcg(vs + clane() + 32 * j) : 0.f;
+      for (int j = 0; j < 4; ++j) k[b][j] = v[b][j] = 0.f;
+      if (sp == pos) {  // v of the current position: the tagged QKV rows
+        const int vo = (p.Hq + p.Hkv + g) * p.hd + clane();
+        uint64_t raw[4];
+        int off[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          off[j] = vo + 32 * j;
+          raw[j] = j < J ? ld_relaxed64(p.qkv + vo + 32 * j) : tag_filler(qtag);
+        }
+        tag_resolve<4>(raw, p.qkv, off, qtag);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < J) v[b][j] = tag_float(raw[j]);
       }
     }
   }
 }
 
 template <class WT, class KT>
-__device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
+__device__ __forceinline__ void phase_talker_attn(Cons c, int layer, uint32_t qtag, uint32_t ptag) {
   const FKParams& p = *fk_prm();
   const int hd = p.hd, Hq = p.Hq, Hkv = p.Hkv, rep = Hq / Hkv, J = hd / 32;
   const int cpg = p.ncta / Hkv;
@@ -1232,16 +1421,27 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
     float k[BATCH][4], v[BATCH][4];
     // the warp's first K/V rows are loaded before step 1 (they do not depend
     // on it), so the loads are in flight while it runs
-    talker_kv_rows<KT>(p, layer, g, pos, s0 + cwarp(), J, k, v);
+    talker_kv_rows<KT>(p, layer, g, pos, s0 + cwarp(), J, qtag, k, v);
     // q of the group's heads (warps < rep); the current key (warp rep, in
     // the item holding the current position), normalised, rotated, kept in
     // shared memory and appended to the cache with its v
     const bool isk = cwarp() == rep && pos >= s0 && pos < s1;
     if (cwarp() < rep || isk) {
-      const float* src = p.qkv + (isk ? (Hq + g) * hd : (g * rep + cwarp()) * hd);
+      const int so = (isk ? (Hq + g) * hd : (g * rep + cwarp()) * hd) + clane();
+      const int vo = (Hq + Hkv + g) * hd + clane();
+      uint64_t raw[8];  // the q or k row, then (for the key) the v row
+      int off[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        off[j] = so + 32 * j;
+        off[4 + j] = vo + 32 * j;
+        raw[j] = j < J ? ld_relaxed64(p.qkv + so + 32 * j) : tag_filler(qtag);
+        raw[4 + j] = (j < J && isk) ? ld_relaxed64(p.qkv + vo + 32 * j) : tag_filler(qtag);
+      }
+      tag_resolve<8>(raw, p.qkv, off, qtag);
       float v[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] = j < J ? __ldcg(src + clane() + 32 * j) : 0.f;
+      for (int j = 0; j < 4; ++j) v[j] = j < J ? tag_float(raw[j]) : 0.f;
       norm_rope_head(p, fk_sm(), v, isk ? side_gk<WT>(c, p.Dt) : side_gq<WT>(c, p.Dt), TALKER_ROPE_ROW, clane());
       float* dst = isk ? as.kcur[0] : as.q[cwarp()];
 #pragma unroll
@@ -1250,12 +1450,11 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
       if (isk) {
         KT* kc = (KT*)p.tkv.pool + tkv_offset(p, layer, pos, 0, g);
         KT* vc = (KT*)p.tkv.pool + tkv_offset(p, layer, pos, 1, g);
-        const float* vs = p.qkv + (Hq + Hkv + g) * hd;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           if (j < J) {
             kc[clane() + 32 * j] = from_f<KT>(v[j]);
-            vc[clane() + 32 * j] = from_f<KT>(__ldcg(vs + clane() + 32 * j));
+            vc[clane() + 32 * j] = from_f<KT>(tag_float(raw[4 + j]));
           }
       }
     }
@@ -1269,7 +1468,7 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
       for (int j = 0; j < 4; ++j) o[r][j] = 0.f;
     }
     for (int sb = s0 + cwarp(); sb < s1; sb += BATCH * FK_CONSUMER_WARPS) {
-      if (sb != s0 + cwarp()) talker_kv_rows<KT>(p, layer, g, pos, sb, J, k, v);
+      if (sb != s0 + cwarp()) talker_kv_rows<KT>(p, layer, g, pos, sb, J, qtag, k, v);
 #pragma unroll
       for (int b = 0; b < BATCH; ++b)  // the current key comes from step 1
         if (sb + b * FK_CONSUMER_WARPS == pos) {
@@ -1326,41 +1525,53 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer) {
           Os += as.o[w][r][d] * f;
         }
       }
-      float* dst = p.part + ((size_t)(g * rep + r) * cpg + ch) * (hd + 2);
-      dst[2 + d] = Os;
+      uint64_t* dst = p.part + ((size_t)(g * rep + r) * cpg + ch) * (hd + 2);
+      st_tagged(dst + 2 + d, Os, ptag);
       if (d == 0) {
-        dst[0] = M;
-        dst[1] = Ls;
+        st_tagged(dst, M, ptag);
+        st_tagged(dst + 1, Ls, ptag);
       }
     }
   }
-  grid_sync(c);
+  // no grid barrier: the combine reads the partials by their tag
 }
 
 // Talker phase B2: combine the partials of the CTA's heads (all partial loads
 // of a thread issued together), then o_proj.
 template <class WT>
-__device__ __forceinline__ void phase_talker_oproj(Cons c, int xa, int xb) {
+__device__ __forceinline__ void phase_talker_oproj(Cons c, int k, uint32_t ptag) {
   const FKParams& p = *fk_prm();
   const int D = p.Dt, hd = p.hd, cpg = p.ncta / p.Hkv, nt = oproj_nt(D);
   int v0, v1;  // the CTA's o_proj tiles
   oproj_tiles(p, D, ccta(), v0, v1);
   const int h_first = v0 / nt, h_last = (v1 - 1) / nt;
   const int nh = v1 > v0 ? h_last - h_first + 1 : 0;
-  constexpr int CMAX = 20;  // chunks per kv group handled in one batch of loads
+  constexpr int CMAX = 8;  // chunks per kv group handled in one batch of loads
   for (int e = ctid(); e < nh * hd; e += FK_CONSUMERS) {
     const int hh = e / hd, d = e % hd, h = h_first + hh;
-    const float* base = p.part + (size_t)h * cpg * (hd + 2);
+    const uint64_t* base = p.part + (size_t)h * cpg * (hd + 2);
     float M = -INFINITY, Ls = 0.f, Os = 0.f;
     for (int c0 = 0; c0 < cpg; c0 += CMAX) {
       float mm[CMAX], ll[CMAX], oo[CMAX];
+      uint64_t raw[3 * CMAX];  // (m, l, o_d) of chunks c0 .. c0 + CMAX - 1
+      int off[3 * CMAX];
 #pragma unroll
       for (int q = 0; q < CMAX; ++q) {
         const int chn = c0 + q;
-        const float* pr = base + (size_t)(chn < cpg ? chn : 0) * (hd + 2);
-        mm[q] = chn < cpg ? __ldcg(pr) : -INFINITY;
-        ll[q] = chn < cpg ? __ldcg(pr + 1) : 0.f;
-        oo[q] = chn < cpg ? __ldcg(pr + 2 + d) : 0.f;
+        const int o = (chn < cpg ? chn : 0) * (hd + 2);
+        off[3 * q] = o;
+        off[3 * q + 1] = o + 1;
+        off[3 * q + 2] = o + 2 + d;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) raw[3 * q + k] = chn < cpg ? ld_relaxed64(base + off[3 * q + k]) : tag_filler(ptag);
+      }
+      tag_resolve<3 * CMAX>(raw, base, off, ptag);
+#pragma unroll
+      for (int q = 0; q < CMAX; ++q) {
+        const bool in = c0 + q < cpg;
+        mm[q] = in ? tag_float(raw[3 * q]) : -INFINITY;
+        ll[q] = in ? tag_float(raw[3 * q + 1]) : 0.f;
+        oo[q] = in ? tag_float(raw[3 * q + 2]) : 0.f;
       }
       float Mn = M;
 #pragma unroll
@@ -1379,7 +1590,7 @@ __device__ __forceinline__ void phase_talker_oproj(Cons c, int xa, int xb) {
     put_plane(fk_sm()->os[hh][0], hd, d, Os / Ls);
   }
   consumer_sync();
-  oproj_step<WT>(c, D, 1, xa, xb);
+  oproj_step<WT>(c, D, 1, k);
 }
 
 // Units u0 .. u0 + G - 1 of a chunk that holds the gate rows of U units and
@@ -1406,10 +1617,10 @@ __device__ __forceinline__ void ffn_units(uint32_t buf, int rb, int U, int u0, i
 // The down projection of the CTA's FFN units [f0, f1): shared chunks of
 // W_down^T rows from ring position n0; lane l of warp w owns output columns
 // 8 (32 w + l) .. + 7, accumulates a_{f,t} W_down[:, f] over the units in
-// registers and adds the CTA's partial sums into copy CTA % FK_KC of X_b
-// with float4 atomics.
+// registers and adds the CTA's partial sums into copy CTA % FK_KC of
+// xffn(k) with float4 atomics.
 template <class WT, int T>
-__device__ __forceinline__ void ffn_down(Stream& s, int D, int f0, int f1, uint32_t n0, int xb) {
+__device__ __forceinline__ void ffn_down(Stream& s, int D, int f0, int f1, uint32_t n0, int k) {
   const FKParams& p = *fk_prm();
   const float(*act)[FK_UMAX] = fk_sm()->act;
   const int rb = D * (int)sizeof(WT);
@@ -1443,7 +1654,7 @@ __device__ __forceinline__ void ffn_down(Stream& s, int D, int f0, int f1, uint3
   warp_set(cst().aborted, s.aborted ? 1 : 0);
   warp_set(cst().n, n0 + nd);
   if (active && nd) {
-    float* X = xbuf(p, xb, ccta() % FK_KC);
+    float* X = xffn(p, k, ccta() % FK_KC);
 #pragma unroll
     for (int t = 0; t < T; ++t) {
       atomicAdd(reinterpret_cast<float4*>(X + t * D + col), make_float4(y[t][0], y[t][1], y[t][2], y[t][3]));
@@ -1458,7 +1669,7 @@ __device__ __forceinline__ int units_per_chunk(int row_bytes) {
   return u < 1 ? 1 : (u > FK_RMAX / 2 ? FK_RMAX / 2 : u);
 }
 
-// Phase C: y = X_a (input + attention) staged for RMSNorm, then the CTA's FFN
+// Phase C of layer k: x_k + a_k staged for RMSNorm, then the CTA's FFN
 // units [f0, f1) (split-K over the FFN width) in two streams.  First the gate
 // and up rows: a private chunk holds the gate rows of U units and then their
 // up rows, and its warp forms a_{f,t} = silu(gate_f . y_t / rms_t) *
@@ -1466,12 +1677,24 @@ __device__ __forceinline__ int units_per_chunk(int row_bytes) {
 // transposed down projection W_down^T[f] (shared chunks): lane l of warp w
 // owns output columns 8 (32 w + l) .. + 7 and adds a_{f,t} W_down[:, f] over
 // the CTA's units in registers.  The CTA's partial D-vector goes into copy
-// CTA % FK_KC of X_b with float4 atomics.
+// CTA % FK_KC of xffn(k) with float4 atomics.  The CTA also clears its slice
+// of layer k + 1's deltas (see xbase).
 template <class WT>
-__device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int xa, int xb) {
+__device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int k) {
   const FKParams& p = *fk_prm();
-  load_norm<WT>(c, false, xa, 0, T, D, side_cur<WT>(c) + D, -1, -1, nullptr);
+  load_norm<WT>(c, SRC_RES_A, k, 0u, 0, T, D, side_cur<WT>(c) + D, -1, nullptr);
   side_end(c);
+  {
+    int lo, hi;
+    cta_slice(p.xstride, lo, hi);
+    float* a1 = xattn(p, k + 1);
+    float* f1 = xffn(p, k + 1, 0);
+    for (int i = lo + ctid(); i < hi; i += FK_CONSUMERS) {
+      a1[i] = 0.f;
+#pragma unroll
+      for (int q = 0; q < FK_KC; ++q) f1[q * p.xstride + i] = 0.f;
+    }
+  }
   const float inv0 = norm_inv(0, D), inv1 = T > 1 ? norm_inv(1, D) : 0.f;
   int f0, f1;
   split(F, p.ncta, ccta(), f0, f1);
@@ -1502,9 +1725,9 @@ __device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int xa, i
   n0 += nch;
   consumer_sync();  // act complete
   if (T == 1)
-    ffn_down<WT, 1>(s, D, f0, f1, n0, xb);
+    ffn_down<WT, 1>(s, D, f0, f1, n0, k);
   else
-    ffn_down<WT, 2>(s, D, f0, f1, n0, xb);
+    ffn_down<WT, 2>(s, D, f0, f1, n0, k);
   grid_sync(c);
 }
 
@@ -1645,11 +1868,12 @@ __device__ __forceinline__ Step decode_step(const FKParams& p, int j, int r) {
 // Moves the warp's schedule position to the next step.
 __device__ __forceinline__ void next_step(ConsState& L) {
   __syncwarp();
-  const int j = L.j, k = L.k + 1;
+  const int j = L.j, k = L.k + 1, s = L.s + 1;
   const bool wrap = k >= pass_steps(*fk_prm(), j);
   __syncwarp();
   L.k = wrap ? 0 : k;
   L.j = wrap ? j + 1 : j;
+  L.s = s;
   __syncwarp();
 }
 
@@ -1659,15 +1883,14 @@ __device__ __forceinline__ void next_step(ConsState& L) {
 template <class WT>
 __device__ __forceinline__ void draw_step(Cons c, int j) {
   ConsState& L = cst();
-  const int fed = draw_code(c, j);
+  const int fed = draw_code(c, j, tag_of(L.s - 1));
   if (j == 0) warp_set(L.fed0, fed);
   if (ctid() == 0) fk_sm()->fedc[j] = fed;  // read in later steps, after barriers
   if (j < Q3TTS_N_CODEBOOKS - 1)
     cp_tokens<WT>(c, j, fed);
   else
     talker_input<WT>(c, fed);
-  warp_set(L.in, 0);
-  warp_set(L.from_xs, 1);
+  warp_set(L.src, (int)SRC_XS);
 }
 
 // Row-GEMV steps (QKV, PROJ, the heads): stage the input -- RMSNorm of the
@@ -1680,57 +1903,64 @@ __device__ __forceinline__ void rows_step(Cons c, const Step& st) {
   const FKParams& p = *fk_prm();
   const bool cp = st.j < Q3TTS_N_CODEBOOKS - 1;
   const int Tp = cp && st.j == 0 ? 2 : 1;  // tokens of the pass
-  int K, T, nrows, ts;
-  float* out;
+  const uint32_t tag = tag_of(L.s);
+  int K, T, nrows;
+  RowsOut o;
+  o.out = nullptr;
+  o.out64 = nullptr;
+  o.tag = tag;
+  o.ts = 0;
   if (st.kind == S_QKV) {
     K = cp ? p.Dc : p.Dt;
     T = Tp;
     nrows = p.qkv_rows;
-    out = p.qkv;
-    ts = p.qkv_rows;
+    o.out64 = p.qkv;
+    o.ts = p.qkv_rows;
   } else if (st.kind == S_PROJ) {
     K = p.Dt;
     T = Tp;
     nrows = p.Dc;
-    out = xbuf(p, 0, 0);
-    ts = p.Dc;
+    o.out64 = p.z;
+    o.ts = p.Dc;
   } else if (st.kind == S_CP_HEAD) {
     K = p.Dc;
     T = 1;
     nrows = p.Vc;
-    out = p.cp_logits;
-    ts = 0;
+    o.out64 = p.cp_logits;
   } else {
     K = p.Dt;
     T = 1;
     nrows = p.Vt;
-    out = p.pending_logits + (size_t)p.sid * p.Vt;
-    ts = 0;
+    o.out = p.pending_logits + (size_t)p.sid * p.Vt;
   }
   float inv0 = 1.f, inv1 = 1.f;  // the projection's input is not normed
   if (st.kind != S_PROJ) {
     const WT* g;
-    int fa = -1, fb = -1, t0 = 0;
+    int src = SRC_RES, fold = -1, t0 = 0;
+    const int k = (int)L.layer;  // QKV: this layer; heads: the layers done so far
     float* hout = nullptr;
     if (st.kind == S_QKV) {
       g = side_begin<WT>(c);
       FK_MARK(TR_SUB, 1);
-      fa = xnext(L.in, 1);
-      fb = xnext(L.in, 2);
+      src = L.src;  // the raw tokens, the projection, or layer k - 1's residual
+      fold = k;
     } else {
       g = reinterpret_cast<const WT*>(fk_sm()->fin) + (cp ? 0 : p.Dc);
       t0 = Tp - 1;
       if (!cp) hout = p.pending_h + (size_t)p.sid * p.Dt;
     }
-    load_norm<WT>(c, st.kind == S_QKV && L.from_xs, L.in, t0, T, K, g, fa, fb, hout);
+    load_norm<WT>(c, src, k - 1, tag_of(L.s - 1), t0, T, K, g, fold, hout);
     inv0 = norm_inv(0, K);
     inv1 = T > 1 ? norm_inv(1, K) : 0.f;
   }
   int lo, hi;
   split(nrows, p.ncta, ccta(), lo, hi);
-  stream_rows<WT>(c, lo, hi, K, T, soff(fk_sm()->u.g.xs), out, ts, inv0, inv1, st.kind == S_PROJ ? p.xstride : 0);
-  if (st.kind != S_T_HEAD) grid_sync(c);
-  warp_set(L.from_xs, 0);
+  stream_rows<WT>(c, lo, hi, K, T, soff(fk_sm()->u.g.xs), o, inv0, inv1);
+  // no grid barrier after a row GEMV: its readers wait for the outputs' tags
+  // (the Talker head is the frame's last step); the CTA's warps still meet,
+  // since the next step reuses the staging area
+  if (st.kind != S_T_HEAD) consumer_sync();
+  warp_set(L.src, st.kind == S_PROJ ? (int)SRC_Z : (int)SRC_RES);
 }
 
 // The consumer warps' schedule for one frame (steps above).  Loop state lives
@@ -1778,6 +2008,24 @@ __device__ void consumer() {
   ConsState& L = cst();
   warp_set(L.j, 0);
   warp_set(L.k, 0);
+  warp_set(L.s, 0);
+  warp_set(L.src, (int)SRC_XS);
+  {
+    // the frame's first layer finds its deltas cleared (later layers' are
+    // cleared by the FFN phase before them); one grid barrier orders this
+    // before any CTA adds into them
+    const FKParams& p = *fk_prm();
+    int lo, hi;
+    cta_slice(p.xstride, lo, hi);
+    float* a0 = xattn(p, 0);
+    float* f0 = xffn(p, 0, 0);
+    for (int i = lo + ctid(); i < hi; i += FK_CONSUMERS) {
+      a0[i] = 0.f;
+#pragma unroll
+      for (int q = 0; q < FK_KC; ++q) f0[q * p.xstride + i] = 0.f;
+    }
+    grid_sync(c);
+  }
   for (; L.j < Q3TTS_N_CODEBOOKS; next_step(L)) {
     const Step st = decode_step(*fk_prm(), L.j, L.k);
     FK_MARK(TR_STEP, st.kind | (st.j << 4) | (st.l << 9));
@@ -1788,18 +2036,16 @@ __device__ void consumer() {
         draw_step<WT>(c, st.j);
         break;
       case S_CP_ATTN:
-        phase_cp_attn<WT>(c, st.l, T, st.j == 0 ? 0 : st.j + 1, xnext(L.in, 1), xnext(L.in, 2));
+        phase_cp_attn<WT>(c, st.l, T, st.j == 0 ? 0 : st.j + 1, (int)L.layer, tag_of(L.s - 1));
         break;
       case S_T_ATTN:
-        phase_talker_attn<WT, KT>(c, st.l);
+        phase_talker_attn<WT, KT>(c, st.l, tag_of(L.s - 1), tag_of(L.s));
         break;
       case S_T_OPROJ:
-        phase_talker_oproj<WT>(c, xnext(L.in, 1), xnext(L.in, 2));
+        phase_talker_oproj<WT>(c, (int)L.layer, tag_of(L.s - 1));
         break;
       case S_FFN:
-        phase_ffn<WT>(c, cp ? fk_prm()->Dc : fk_prm()->Dt, cp ? fk_prm()->Fc : fk_prm()->Ft, T, xnext(L.in, 1),
-                      xnext(L.in, 2));
-        warp_set(L.in, xnext(L.in, 2));
+        phase_ffn<WT>(c, cp ? fk_prm()->Dc : fk_prm()->Dt, cp ? fk_prm()->Fc : fk_prm()->Ft, T, (int)L.layer);
         break;
       default:
         rows_step<WT>(c, st);
@@ -1867,7 +2113,7 @@ struct Producer {
     const volatile uint32_t* gate = &sm->pf_gate;
     long long t0 = clock64();
     unsigned it = 0;
-    while (n >= *gate + (uint32_t)FK_PF_AHEAD) {
+    while (n >= *gate + (uint32_t)p.pf_ahead) {
       __nanosleep(256);
       if ((++it & 15u) == 0 && (ld_volatile(p.abort_flag) || clock64() - t0 > p.wait_cycles)) {
         stop = true;
@@ -1898,18 +2144,6 @@ struct Producer {
     publish();
   }
 
-  __device__ void rows(const void* base, int r0, int r1, int row_bytes) {
-    const int rpc = rows_per_chunk(row_bytes);
-    for (int r = r0; r < r1; r += rpc)
-      issue((const char*)base + (size_t)r * row_bytes, (unsigned)(min(rpc, r1 - r) * row_bytes));
-  }
-
-  __device__ void split_rows(const void* base, int N, int row_bytes) {
-    int lo, hi;
-    split(N, p.ncta, cta, lo, hi);
-    rows(base, lo, hi, row_bytes);
-  }
-
   // One chunk from two sources (the gate rows and the up rows of a few FFN units).
   __device__ void issue2(const void* a, const void* b, unsigned bytes) {
     if (stop) return;
@@ -1930,22 +2164,7 @@ struct Producer {
     publish();
   }
 
-  // The CTA's FFN units [f0, f1): chunks of the gate rows then the up rows of
-  // a few units, then the rows of W_down^T.
-  __device__ void ffn(const LayerDev& L, int D, int F) {
-    int f0, f1;
-    split(F, p.ncta, cta, f0, f1);
-    const int rb = D * (int)sizeof(WT), upc = units_per_chunk(rb);
-    const char* gu = (const char*)L.w_gu;
-    for (int f = f0; f < f1; f += upc) {
-      const int U = min(upc, f1 - f);
-      issue2(gu + (size_t)f * rb, gu + (size_t)(F + f) * rb, (unsigned)(U * rb));
-    }
-    rows(L.w_dT, f0, f1, rb);
-  }
-
   int nlayers = 0;  // layers in the frame (15 CodePredictor passes, then the Talker)
-  int layer_i = 0;  // next layer whose weights are streamed
   int side_last[2] = {-1, -1};  // last layer whose side block was copied into each slot
 
   __device__ const LayerDev& layer_at(int k) const {
@@ -1977,29 +2196,86 @@ struct Producer {
     side_last[slot] = k;
   }
 
-  __device__ void layer(const LayerDev& L, int D, int F) {
-    const int esz = (int)sizeof(WT);
-    split_rows(L.w_qkv, p.qkv_rows, D * esz);
-    split_rows(L.w_oT, p.Hq * oproj_nt(D), 32 * p.hd * esz);
-    ffn(L, D, F);
-    // the next layer's gains go out once this layer's weights are queued: their
-    // slot was freed when the consumers began the previous layer's FFN, which
-    // lies at least a ring's depth behind this point
-    layer_i++;
-    side(layer_i);
-  }
-
+  // The frame's weight schedule as a list of segments, each one matrix (or
+  // matrix pair) of which the CTA streams its share: per CodePredictor pass
+  // [projection], per layer [QKV rows, o_proj tiles, gate/up units, W_down^T
+  // rows], head j; then the Talker's layers and its head.  One loop with two
+  // copy sites walks it (the producer's code runs beside the consumers' on
+  // every SM, so it is kept small).
   __device__ void run() {
     const int esz = (int)sizeof(WT);
     nlayers = (Q3TTS_N_CODEBOOKS - 1) * p.Lc + p.Lt;
+    const int hp = p.has_proj ? 1 : 0;
+    const int cp_seg = hp + 4 * p.Lc + 1;  // segments of a CodePredictor pass
+    const int nseg = (Q3TTS_N_CODEBOOKS - 1) * cp_seg + 4 * p.Lt + 1;
     side(0);
-    for (int j = 0; j < Q3TTS_N_CODEBOOKS - 1; ++j) {
-      if (p.has_proj) split_rows(p.cp_proj, p.Dc, p.Dt * esz);
-      for (int l = 0; l < p.Lc; ++l) layer(sm->lay[p.Lt + l], p.Dc, p.Fc);
-      split_rows((const char*)p.cp_heads + (size_t)j * p.Vc * p.Dc * esz, p.Vc, p.Dc * esz);
+    int layer = 0;  // layer of the frame the schedule is in
+    for (int sg = 0; sg < nseg && !stop; ++sg) {
+      // decode: pass j (15: the Talker), position q inside it
+      int j = 0, q = sg;
+      if (sg >= (Q3TTS_N_CODEBOOKS - 1) * cp_seg) {
+        j = Q3TTS_N_CODEBOOKS - 1;
+        q = sg - (Q3TTS_N_CODEBOOKS - 1) * cp_seg;
+      } else {
+        j = sg / cp_seg;
+        q = sg - j * cp_seg;
+      }
+      const bool cp = j < Q3TTS_N_CODEBOOKS - 1;
+      const int D = cp ? p.Dc : p.Dt, F = cp ? p.Fc : p.Ft;
+      const int lq = cp ? q - hp : q;  // position within the layers (-1: projection)
+      const char* base;
+      const char* up = nullptr;  // gate/up segment: the up rows
+      int N, rb;
+      bool layer_end = false;
+      if (cp && q < hp) {
+        base = (const char*)p.cp_proj;
+        N = p.Dc;
+        rb = p.Dt * esz;
+      } else if (lq >= 4 * (cp ? p.Lc : p.Lt)) {  // the head
+        base = cp ? (const char*)p.cp_heads + (size_t)j * p.Vc * p.Dc * esz : (const char*)p.t_head;
+        N = cp ? p.Vc : p.Vt;
+        rb = D * esz;
+      } else {
+        const LayerDev& L = layer_at(layer);
+        const int m = lq & 3;
+        if (m == 0) {
+          base = (const char*)L.w_qkv;
+          N = p.qkv_rows;
+          rb = D * esz;
+        } else if (m == 1) {
+          base = (const char*)L.w_oT;
+          N = p.Hq * oproj_nt(D);
+          rb = 32 * p.hd * esz;
+        } else if (m == 2) {
+          base = (const char*)L.w_gu;
+          up = base + (size_t)F * D * esz;
+          N = F;
+          rb = D * esz;
+        } else {
+          base = (const char*)L.w_dT;
+          N = F;
+          rb = D * esz;
+          layer_end = true;
+        }
+      }
+      int lo, hi;
+      split(N, p.ncta, cta, lo, hi);
+      const int per = up ? units_per_chunk(rb) : rows_per_chunk(rb);
+      for (int r = lo; r < hi && !stop; r += per) {
+        const unsigned bytes = (unsigned)(min(per, hi - r) * rb);
+        if (up)
+          issue2(base + (size_t)r * rb, up + (size_t)r * rb, bytes);
+        else
+          issue(base + (size_t)r * rb, bytes);
+      }
+      if (layer_end) {
+        // the next layer's gains go out once this layer's weights are queued:
+        // their slot was freed when the consumers began the previous layer's
+        // FFN, which lies at least a ring's depth behind this point
+        ++layer;
+        side(layer);
+      }
     }
-    for (int l = 0; l < p.Lt; ++l) layer(sm->lay[l], p.Dt, p.Ft);
-    split_rows(p.t_head, p.Vt, p.Dt * esz);
     if (!PF) drain();  // prefetches leave nothing in flight that the CTA owns
   }
 
@@ -2051,7 +2327,7 @@ __global__ void __launch_bounds__(FK_THREADS, 1) frame_kernel(const __grid_const
     return;
   }
   if (threadIdx.x >= FK_PRODUCER_THREADS + FK_CONSUMERS) {
-    if (threadIdx.x == FK_PRODUCER_THREADS + FK_CONSUMERS) {
+    if (threadIdx.x == FK_PRODUCER_THREADS + FK_CONSUMERS && sm->prm.pf_ahead > 0) {
       Producer<WT, true> pf(sm->prm, sm, blockIdx.x);
       pf.run();
     }
@@ -2130,19 +2406,20 @@ static size_t fk_layout(const q3tts_config& c, int ncta, FKState* st, char* base
   char* sideC = take((size_t)c.cp_layers * (2 * c.cp_hidden + 2 * hd) * esz);
   char* tl = take(sizeof(LayerDev) * c.talker_layers);
   char* cl = take(sizeof(LayerDev) * c.cp_layers);
-  char* R = take(sizeof(float) * FK_KC * xst);
-  char* dA = take(sizeof(float) * FK_KC * xst);
-  char* dF = take(sizeof(float) * FK_KC * xst);
-  char* qkv = take(sizeof(float) * FK_TMAX * qkv_rows);
-  char* part = take(sizeof(float) * (size_t)Hq * cpg * (hd + 2));
-  char* lg = take(sizeof(float) * c.cp_vocab);
+  char* xb = take(sizeof(float) * 2 * xst);
+  char* xa = take(sizeof(float) * 2 * xst);
+  char* xf = take(sizeof(float) * 2 * FK_KC * xst);
+  char* qkv = take(sizeof(uint64_t) * FK_TMAX * qkv_rows);
+  char* z = take(sizeof(uint64_t) * FK_TMAX * c.cp_hidden);
+  char* part = take(sizeof(uint64_t) * (size_t)Hq * cpg * (hd + 2));
+  char* lg = take(sizeof(uint64_t) * c.cp_vocab);
   char* sync = take(sizeof(unsigned) * 4);
   if (st) {
     st->base = base;
     st->tl = (LayerDev*)tl;
     st->cl = (LayerDev*)cl;
-    st->R = (float*)R; st->dA = (float*)dA; st->dF = (float*)dF;
-    st->qkv = (float*)qkv; st->part = (float*)part; st->cp_logits = (float*)lg;
+    st->xb = (float*)xb; st->xa = (float*)xa; st->xf = (float*)xf;
+    st->qkv = (uint64_t*)qkv; st->z = (uint64_t*)z; st->part = (uint64_t*)part; st->cp_logits = (uint64_t*)lg;
     st->bar = (unsigned*)sync;
     st->done = st->bar + 1;
     st->abort_flag = (int*)(st->bar + 2);
@@ -2170,6 +2447,11 @@ int frame_kernel_create(q3tts_handle* h) {
   FrameKernelState* st = new (std::nothrow) FrameKernelState();
   if (!st) return Q3TTS_ERR_ARG;
   st->ok = false;
+  st->seq = 0;
+  {
+    const char* e = getenv("Q3TTS_PF_AHEAD");
+    st->pf_ahead = e ? std::max(0, std::min(atoi(e), 1024)) : FK_PF_AHEAD;
+  }
   h->fk = st;
   const q3tts_config& c = h->c;
   // eligibility: shapes the kernel's shared-memory layout covers
@@ -2198,6 +2480,10 @@ int frame_kernel_create(q3tts_handle* h) {
   // RMSNorm staging holds at most FK_DMAX values: the CodePredictor's first
   // pass stages two tokens
   if (FK_TMAX * c.cp_hidden > FK_DMAX) return Q3TTS_OK;
+  // tags number a frame's steps below FK_MAXSTEPS
+  const int steps = (Q3TTS_N_CODEBOOKS - 1) * (2 + (c.talker_hidden != c.cp_hidden ? 1 : 0) + 3 * c.cp_layers) +
+                    2 + 4 * c.talker_layers;
+  if (steps >= FK_MAXSTEPS) return Q3TTS_OK;
   // per-layer gains and both final norms fit their shared-memory slots
   if ((2 * std::max(c.talker_hidden, c.cp_hidden) + 2 * c.head_dim) * esz_w > FK_SIDE_BYTES ||
       (c.talker_hidden + c.cp_hidden) * esz_w > FK_FIN_BYTES)
@@ -2303,11 +2589,12 @@ static void frame_params(FKParams& p, const q3tts_handle* h, int sid, int pos, i
   p.cp_gfinal = h->w.cp_g_final;
   p.pending_h = h->pending_h; p.pending_logits = h->pending_logits; p.history = h->history;
   p.tkv = talker_kv(h); p.ckv = cp_kv(h); p.rope_cos = h->rope_cos; p.rope_sin = h->rope_sin;
-  p.R = st->R; p.dA = st->dA; p.dF = st->dF; p.qkv = st->qkv; p.part = st->part;
-  p.cp_logits = st->cp_logits;
+  p.xb = st->xb; p.xa = st->xa; p.xf = st->xf;
+  p.qkv = st->qkv; p.z = st->z; p.part = st->part; p.cp_logits = st->cp_logits;
   p.bar = st->bar; p.done = st->done; p.err = h->d_err; p.abort_flag = st->abort_flag;
   p.wait_cycles = h->dbg_wait_cycles > 0 ? h->dbg_wait_cycles : FK_WAIT_CYCLES;
   p.fail_bar = h->dbg_fail_bar;
+  p.pf_ahead = st->pf_ahead;
   p.sid = sid; p.pos = pos; p.newpage = newpage; p.sp = sp;
   p.uniforms = uniforms; p.codes = codes; p.forced = forced; p.dump = logits;
 }
@@ -2322,10 +2609,18 @@ static int frame_launch(q3tts_handle* h, FKParams& p) {
   return e == cudaSuccess ? Q3TTS_OK : Q3TTS_ERR_CUDA;
 }
 
+// The next sequence number of a scratch area (its tagged words start at 0,
+// so the numbers start at 1 and skip 0 when they wrap).
+static uint32_t next_seq(uint32_t& s) {
+  s = s + 1 == 0 ? 1 : s + 1;
+  return s;
+}
+
 int frame_kernel_step(q3tts_handle* h, const StepDesc& d, const float* uniforms, int32_t* codes,
                       const int32_t* forced, float* logits) {
   FKParams p;
   frame_params(p, h, d.sid[0], d.pos[0], d.newpage[0], d.sp[0], uniforms, codes, forced, logits);
+  p.seq = next_seq(h->fk->seq);
   return frame_launch(h, p);
 }
 
@@ -2369,6 +2664,9 @@ static __device__ __align__(256) unsigned char fk_static_scratch[Q3TTS_STATIC_SC
 constexpr int FK_MAX_DEVICES = 64;
 static std::mutex g_static_mu;
 static std::atomic<unsigned char*> g_static_addr[FK_MAX_DEVICES];
+// Launches that used each device's static scratch (tags: the array is shared
+// by every handle, so its sequence numbers are too).
+static std::atomic<uint32_t> g_static_seq[FK_MAX_DEVICES];
 
 // Places the scratch vectors of config c behind the barrier words at base
 // (size only when base is null); returns the bytes used.
@@ -2380,17 +2678,18 @@ static size_t fk_static_layout(const q3tts_config& c, int ncta, char* base, FKPa
   auto take = [&](size_t bytes) {
     size_t o = off;
     off = al256(off + bytes);
-    return (float*)(base ? base + o : nullptr);
+    return base ? base + o : nullptr;
   };
-  float* R = take(sizeof(float) * FK_KC * xst);
-  float* dA = take(sizeof(float) * FK_KC * xst);
-  float* dF = take(sizeof(float) * FK_KC * xst);
-  float* qkv = take(sizeof(float) * FK_TMAX * qkv_rows);
-  float* part = take(sizeof(float) * (size_t)c.n_q_heads * cpg * (c.head_dim + 2));
-  float* lg = take(sizeof(float) * c.cp_vocab);
+  char* xb = take(sizeof(float) * 2 * xst);
+  char* xa = take(sizeof(float) * 2 * xst);
+  char* xf = take(sizeof(float) * 2 * FK_KC * xst);
+  char* qkv = take(sizeof(uint64_t) * FK_TMAX * qkv_rows);
+  char* z = take(sizeof(uint64_t) * FK_TMAX * c.cp_hidden);
+  char* part = take(sizeof(uint64_t) * (size_t)c.n_q_heads * cpg * (c.head_dim + 2));
+  char* lg = take(sizeof(uint64_t) * c.cp_vocab);
   if (p) {
-    p->R = R; p->dA = dA; p->dF = dF; p->qkv = qkv; p->part = part;
-    p->cp_logits = lg;
+    p->xb = (float*)xb; p->xa = (float*)xa; p->xf = (float*)xf;
+    p->qkv = (uint64_t*)qkv; p->z = (uint64_t*)z; p->part = (uint64_t*)part; p->cp_logits = (uint64_t*)lg;
     p->bar = (unsigned*)base;
     p->done = p->bar + 1;
     p->abort_flag = (int*)(p->bar + 2);
@@ -2449,6 +2748,9 @@ int frame_kernel_step_static(q3tts_handle* h, int sid, int pos, int newpage, con
   FKParams p;
   frame_params(p, h, sid, pos, newpage, sp, uniforms, codes, forced, logits);
   fk_static_layout(h->c, h->fk->ncta, (char*)base, &p);
+  uint32_t sq = g_static_seq[h->dev].fetch_add(1u, std::memory_order_relaxed) + 1u;
+  if (sq == 0) sq = g_static_seq[h->dev].fetch_add(1u, std::memory_order_relaxed) + 1u;
+  p.seq = sq;
   return frame_launch(h, p);
 }
 

@@ -398,7 +398,9 @@ __device__ __noinline__ void fast_select_bisect(FastSamplerSmem& sm, int V, int 
 
 // The draw of the frame kernel: greedy, or sampling with 1 <= top_k <= 64,
 // run by a group of 256 threads (8 warps) on V <= SAMPLER_VMAX logits (V a
-// multiple of 4, logits 16-byte and history 4-byte aligned): thread t reads
+// multiple of 4, logits 16-byte and history 4-byte aligned; the logits may
+// be sm.keys itself -- they are read before their keys replace them, or any
+// memory the group can read with plain loads): thread t reads
 // float4 q of the logits at elements 4 (t + 256 q) (a warp's loads are
 // contiguous) and keeps their 32-bit value keys in shared memory; candidates
 // are 64-bit keys (value key, inverted index).  Greedy is the same rule with k = 1 and T = 1 (dividing by 1 is
@@ -429,7 +431,7 @@ __device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits
   for (int q = 0; q < FAST_V4; ++q) {
     const int e = 4 * (tid + FAST_NT * q);
     if (e >= V) break;
-    float4 v = __ldcg(reinterpret_cast<const float4*>(logits + e));
+    float4 v = *reinterpret_cast<const float4*>(logits + e);
     uint32_t hb = pen ? *reinterpret_cast<const uint32_t*>(history + e) : 0u;
 #pragma unroll 1
     for (int k = 0; k < 4; ++k) {

@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(HERE, "libq3tts.so")
 OK = 0
 ERR_ARG, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED, ERR_STATE = -1, -2, -3, -4, -5, -6
 ERR_SCRATCH = -7
-STATIC_SCRATCH_BYTES = 327680
+STATIC_SCRATCH_BYTES = 786432
 F32, BF16 = 0, 1
 MAX_STREAMS = 256
 N_CODEBOOKS = 16

@@ -52,9 +52,9 @@ extern "C" {
 #define Q3TTS_MAX_STREAMS 256
 #define Q3TTS_N_CODEBOOKS 16
 
-/* Size of the library's static device scratch array (320 KiB), used only by
+/* Size of the library's static device scratch array (768 KiB), used only by
  * q3tts_step_frame_static. */
-#define Q3TTS_STATIC_SCRATCH_BYTES 327680
+#define Q3TTS_STATIC_SCRATCH_BYTES 786432
 
 /* Model and engine shape.  Dimensions follow the Qwen3-style decoder: RMSNorm
  * (eps rms_eps), per-head q/k RMSNorm when qk_norm != 0, rotate-half RoPE

@@ -121,19 +121,27 @@ def test_static_scratch_rejections_leave_state(q3):
 
 def test_static_scratch_too_small_is_rejected(q3):
     """A shape the persistent kernel accepts whose scratch exceeds the static
-    array: 32 query heads over 16 KV heads of width 128 at Talker width 2048
-    (QKV rows, attention partials) with a 4096-entry CodePredictor vocabulary.
-    The call returns Q3TTS_ERR_SCRATCH before anything is launched
-    (configuration checks come before the stream's state)."""
+    array: 128 query heads over 64 KV heads of width 128 (wide QKV rows and
+    many attention partials) with a 4096-entry CodePredictor vocabulary.  The
+    call returns Q3TTS_ERR_SCRATCH before anything is launched (configuration
+    checks come before the stream's state)."""
     import torch
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
     shape = dataclasses.replace(synth.WORKLOADS["tiny"].shape, talker_layers=1, cp_layers=1,
                                 talker_hidden=2048, cp_hidden=1024, talker_ffn=256, cp_ffn=256,
-                                n_q_heads=32, n_kv_heads=16, head_dim=128, codec_vocab=256,
+                                n_q_heads=128, n_kv_heads=64, head_dim=128, codec_vocab=256,
                                 cp_vocab=4096, weight_dtype=synth.DTYPE_BF16)
     ncta = min(n_sm, 256)
-    cpg = max(1, ncta // 16)
-    need = 256 + 3 * (4 * 2 * 2 * 2048) + 4 * 2 * (64 * 128) + 4 * 32 * cpg * 130 + 4 * 4096
+    cpg = max(1, ncta // 64)
+
+    def al(x):
+        return (x + 255) // 256 * 256
+    xst = max(2048, 2 * 1024)
+    qkv_rows = (128 + 2 * 64) * 128
+    # barrier words, residual base / attention / FFN buffers, then the tagged
+    # words (8 bytes each): QKV rows, projection, attention partials, logits
+    need = 256 + al(4 * 2 * xst) * 2 + al(4 * 2 * 4 * xst) + al(8 * 2 * qkv_rows) + al(8 * 2 * 1024) \
+        + al(8 * 128 * cpg * 130) + al(8 * 4096)
     if need <= q3.STATIC_SCRATCH_BYTES:
         pytest.skip(f"{n_sm} SMs: this shape's scratch fits the static array")
     _, Wd = pu.gpu_weights(shape, gen_device="cuda")
