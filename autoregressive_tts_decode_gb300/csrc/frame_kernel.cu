@@ -696,6 +696,7 @@ __device__ __forceinline__ void dots(uint32_t w, const uint32_t (&ro)[NR], int K
   const uint32_t wl = w + (uint32_t)(lane * 8 * (int)sizeof(WT));
   const uint32_t xl = xs + (uint32_t)(lane * 16);
   const int nb = (K >> 8) + (lane * 8 < (K & 255) ? 1 : 0);  // blocks with elements of this lane
+#pragma unroll 1
   for (int b = 0; b < nb; ++b) {
     float4 xa[T], xc[T];
 #pragma unroll
@@ -861,7 +862,7 @@ __device__ __forceinline__ float norm_inv(int t, int D) {
 // normed x_0 goes there.  g points into shared memory (4-element aligned
 // groups).
 template <class WT>
-__device__ __forceinline__ void load_norm(Cons c, int src, int kp, uint32_t ztag, int t0, int T, int D, const WT* g,
+__device__ __noinline__ void load_norm(Cons c, int src, int kp, uint32_t ztag, int t0, int T, int D, const WT* g,
                                           int fold, float* out) {
   const FKParams& p = *fk_prm();
   float* xs = fk_sm()->u.g.xs;
@@ -1546,48 +1547,55 @@ __device__ __forceinline__ void phase_talker_oproj(Cons c, int k, uint32_t ptag)
   oproj_tiles(p, D, ccta(), v0, v1);
   const int h_first = v0 / nt, h_last = (v1 - 1) / nt;
   const int nh = v1 > v0 ? h_last - h_first + 1 : 0;
-  constexpr int CMAX = 8;  // chunks per kv group handled in one batch of loads
-  for (int e = ctid(); e < nh * hd; e += FK_CONSUMERS) {
-    const int hh = e / hd, d = e % hd, h = h_first + hh;
-    const uint64_t* base = p.part + (size_t)h * cpg * (hd + 2);
-    float M = -INFINITY, Ls = 0.f, Os = 0.f;
-    for (int c0 = 0; c0 < cpg; c0 += CMAX) {
-      float mm[CMAX], ll[CMAX], oo[CMAX];
-      uint64_t raw[3 * CMAX];  // (m, l, o_d) of chunks c0 .. c0 + CMAX - 1
-      int off[3 * CMAX];
-#pragma unroll
-      for (int q = 0; q < CMAX; ++q) {
-        const int chn = c0 + q;
-        const int o = (chn < cpg ? chn : 0) * (hd + 2);
-        off[3 * q] = o;
-        off[3 * q + 1] = o + 1;
-        off[3 * q + 2] = o + 2 + d;
-#pragma unroll
-        for (int k = 0; k < 3; ++k) raw[3 * q + k] = chn < cpg ? ld_relaxed64(base + off[3 * q + k]) : tag_filler(ptag);
-      }
-      tag_resolve<3 * CMAX>(raw, base, off, ptag);
-#pragma unroll
-      for (int q = 0; q < CMAX; ++q) {
-        const bool in = c0 + q < cpg;
-        mm[q] = in ? tag_float(raw[3 * q]) : -INFINITY;
-        ll[q] = in ? tag_float(raw[3 * q + 1]) : 0.f;
-        oo[q] = in ? tag_float(raw[3 * q + 2]) : 0.f;
-      }
-      float Mn = M;
-#pragma unroll
-      for (int q = 0; q < CMAX; ++q) Mn = fmaxf(Mn, mm[q]);
-      const float corr = M == -INFINITY ? 0.f : __expf(M - Mn);
-      Ls *= corr;
-      Os *= corr;
-#pragma unroll
-      for (int q = 0; q < CMAX; ++q) {
-        const float f = mm[q] == -INFINITY ? 0.f : __expf(mm[q] - Mn);
-        Ls += ll[q] * f;
-        Os += oo[q] * f;
-      }
-      M = Mn;
+  // warp-cooperative: thread (hh, d) = ctid() of the CTA's nh heads (whole
+  // warps, as hd is a multiple of 32); lane c of a warp reads chunk c's
+  // (m, l) header and the warp reduces them, then every lane reads its d of
+  // the chunks' partial outputs, weighted by the header weights it gets by
+  // shuffle
+  const int e = ctid();
+  if (e < nh * hd) {
+    const int hh = e / hd, d = e % hd, lane = clane();
+    const uint64_t* base = p.part + (size_t)(h_first + hh) * cpg * (hd + 2);
+    float M = -INFINITY;
+    for (int c0 = 0; c0 < cpg; c0 += 32) {
+      const bool in = c0 + lane < cpg;
+      uint64_t raw[1];
+      const int off[1] = {(in ? c0 + lane : 0) * (hd + 2)};
+      raw[0] = in ? ld_relaxed64(base + off[0]) : tag_filler(ptag);
+      tag_resolve<1>(raw, base, off, ptag);
+      M = fmaxf(M, warp_max(in ? tag_float(raw[0]) : -INFINITY));
     }
-    put_plane(fk_sm()->os[hh][0], hd, d, Os / Ls);
+    float L = 0.f, O = 0.f;
+    for (int c0 = 0; c0 < cpg; c0 += 32) {
+      const bool in = c0 + lane < cpg;
+      uint64_t raw[2];
+      const int o = (in ? c0 + lane : 0) * (hd + 2);
+      const int off[2] = {o, o + 1};
+      raw[0] = in ? ld_relaxed64(base + o) : tag_filler(ptag);
+      raw[1] = in ? ld_relaxed64(base + o + 1) : tag_filler(ptag);
+      tag_resolve<2>(raw, base, off, ptag);
+      const float m = in ? tag_float(raw[0]) : -INFINITY;
+      const float f = m == -INFINITY ? 0.f : __expf(m - M);
+      L += warp_sum(in ? tag_float(raw[1]) * f : 0.f);
+      const int nc = min(32, cpg - c0);
+      for (int cb = 0; cb < nc; cb += 8) {
+        uint64_t ro[8];
+        int oo[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const bool iq = cb + q < nc;
+          oo[q] = (iq ? c0 + cb + q : 0) * (hd + 2) + 2 + d;
+          ro[q] = iq ? ld_relaxed64(base + oo[q]) : tag_filler(ptag);
+        }
+        tag_resolve<8>(ro, base, oo, ptag);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float fq = __shfl_sync(0xffffffffu, f, (cb + q) & 31);
+          if (cb + q < nc) O = fmaf(fq, tag_float(ro[q]), O);
+        }
+      }
+    }
+    put_plane(fk_sm()->os[hh][0], hd, d, O / L);
   }
   consumer_sync();
   oproj_step<WT>(c, D, 1, k);
