@@ -122,15 +122,23 @@ static double wval(const void* w, int dt, size_t i) {
   return (double)f;
 }
 
-/* y[t][r] = sum_k W[r][k] x[t][k]  (W row-major [rows, cols]); a plain matrix product. */
+/* y[t][r] = sum_k W[r][k] x[t][k]  (W row-major [rows, cols]); a plain matrix
+ * product, each row widened once and then used for every token (the sums run
+ * over k in order for each (t, r), whatever the number of tokens). */
 static void linear(const void* W, int dt, int rows, int cols, const double* x, int T, double* y) {
-#pragma omp parallel for schedule(static)
-  for (int r = 0; r < rows; ++r) {
-    for (int t = 0; t < T; ++t) {
-      double acc = 0.0;
-      for (int k = 0; k < cols; ++k) acc += wval(W, dt, (size_t)r * cols + k) * x[(size_t)t * cols + k];
-      y[(size_t)t * rows + r] = acc;
+#pragma omp parallel
+  {
+    double* w = (double*)malloc(sizeof(double) * (size_t)cols);
+#pragma omp for schedule(static)
+    for (int r = 0; r < rows; ++r) {
+      for (int k = 0; k < cols; ++k) w[k] = wval(W, dt, (size_t)r * cols + k);
+      for (int t = 0; t < T; ++t) {
+        double acc = 0.0;
+        for (int k = 0; k < cols; ++k) acc += w[k] * x[(size_t)t * cols + k];
+        y[(size_t)t * rows + r] = acc;
+      }
     }
+    free(w);
   }
 }
 
@@ -243,7 +251,9 @@ static void stack_forward(const q3o_model* m, const stack_desc* sd, double* x, i
         }
       }
     }
-    /* causal: token t sees positions 0..pos0+t, itself included */
+    /* causal: token t sees positions 0..pos0+t, itself included (tokens are
+     * independent here: each reads the cache filled above) */
+#pragma omp parallel for schedule(dynamic, 4)
     for (int t = 0; t < T; ++t)
       attention(qkv + (size_t)t * qkv_rows, Kc, Vc, pos0 + t + 1, Hq, Hkv, hd, o + (size_t)t * Hq * hd);
     linear(w[L_O], dt, D, Hq * hd, o, T, y);
