@@ -11,39 +11,48 @@
 // per frame -- makes this a weight-streaming problem: at batch 1 every weight
 // byte is used by one multiply-add.
 //
-// Design (GB300, one CTA per SM, cooperative launch):
+// Design (GB300, one CTA per SM, cooperative launch, 320 threads):
 //  * A producer warp walks the frame's weight schedule for its CTA -- the
-//    same row slices the consumers will need, in frame order -- and streams
-//    them through an 11-deep ring of 12 KB chunks in shared memory with 1-D
-//    bulk copies (cp.async.bulk + mbarrier transaction counts, L2
-//    evict-first).  Weights do not depend on activations, so the stream runs
-//    ahead across the grid barriers that separate dependent phases.
-//  * Eight consumer warps form four gangs of two; ring chunk n belongs to
-//    gang n % 4, whose warps split each row's reduction between them and meet
-//    once per chunk (a 64-thread named barrier and a small exchange buffer):
-//    no block-wide barrier sits inside a streaming loop.  Phases: RMSNorm
-//    staged once per phase, then row GEMVs (QKV, projection, heads);
-//    attention; a fused SwiGLU FFN over "units" (gate row, up row and down
-//    column of one intermediate channel, contiguous) whose partial outputs
-//    are added into the residual with float4 atomics (split-K over the FFN
-//    width, no extra phase); o_proj over 32-column tiles of one head with
-//    the same atomic accumulation.  Draws are made redundantly by every CTA
-//    from the full logit vector (sampler.cuh, fast_sample), so a sampled code
-//    needs no barrier.
-//  * Residual bookkeeping: three rotating buffers; a layer folds its input
-//    into the next two, so every phase reads one complete vector.
-//  * Phases per layer: CodePredictor 3 (QKV | attention + o_proj | FFN) --
-//    its context is at most 16 positions, so every CTA recomputes the one or
-//    two heads it needs; Talker 4 (QKV | attention partials over position
-//    chunks | combine + o_proj | FFN).
+//    same slices the consumers will need, in frame order -- and streams them
+//    through a 20-deep ring of 8 KB chunks in shared memory with 1-D bulk
+//    copies (cp.async.bulk + mbarrier transaction counts, L2 evict-first).
+//    Weights do not depend on activations, so the stream runs ahead across
+//    phase boundaries.  An optional second warp prefetches further ahead
+//    into L2 (off by default: the extra traffic delays the latency-bound
+//    phases).
+//  * Eight consumer warps.  A private chunk (rows of a GEMV, an o_proj tile,
+//    gate and up rows) belongs to one warp, which computes whole dot
+//    products over it alone; a shared chunk (rows of the transposed down
+//    projection) is read by every warp for its own output columns.  No
+//    block-wide barrier sits inside a streaming loop.
+//  * RMSNorm is lazy: the staged input is g * x (one CTA-wide pass), and
+//    each GEMV output is scaled by the one inverse RMS afterwards.
+//  * The residual stream of layer k is a base vector plus an attention delta
+//    and an FFN delta (FK_KC copies of the latter, so that the split-K
+//    atomics of 152 CTAs spread over more addresses); the next layer's
+//    RMSNorm sums them while staging and folds the sum into its own base.
+//  * FFN in two stages without a grid barrier between them: a CTA computes
+//    silu(gate) * up for its own intermediate channels (rows of the caller's
+//    gate/up tensor), then adds their rank-k contribution to all outputs
+//    through rows of W_down^T (a copy made at create) with float4 atomics.
+//    o_proj works the same way over 32-column tiles of one head.
+//  * Values that one phase hands to the next without a reduction -- QKV
+//    rows, the CodePredictor input projection, Talker attention partials,
+//    CodePredictor logits -- are 64-bit words (value, step tag) written with
+//    relaxed stores; a reader polls the words it needs until their tag is
+//    this step's.  Grid barriers remain only where the next phase reads a
+//    complete atomic sum (after o_proj and after the FFN, plus one at the
+//    frame start): 207 per 1.7B frame.
+//  * Draws are made redundantly by every CTA from the full logit vector
+//    (sampler.cuh, fast_sample), so a sampled code needs no barrier.
 //  * The frame is a list of steps decoded from a (pass, step) position, each
-//    step kind with one call site; the consumers' loop state and launch
-//    parameters live in shared memory (local memory is costly beside a
-//    shared-memory carve-out this large).
+//    step kind with one call site, so every phase's code exists once (the
+//    kernel is sensitive to instruction-cache misses); the consumers' loop
+//    state and launch parameters live in shared memory.
 //  * The grid barrier is a release-add / acquire-load counter polled by one
-//    thread per CTA.  Every wait (ring slots, side slots, grid barrier) is
-//    bounded; on expiry the kernel records Q3TTS_ERR_TIMEOUT, raises an abort
-//    flag, stops waiting, lets in-flight copies land and returns.
+//    thread per CTA.  Every wait (ring slots, side slots, tags, grid barrier)
+//    is bounded; on expiry the kernel records Q3TTS_ERR_TIMEOUT, raises an
+//    abort flag, stops waiting, lets in-flight copies land and returns.
 #include <algorithm>
 #include <atomic>
 #include <mutex>

@@ -58,10 +58,11 @@ def job_rate(frames_per_rank, world, seconds):
 
 # Sources of the persistent frame kernel: a recorded DRAM-traffic figure holds
 # only for the code it was captured from.
+# (The handle's host-side struct in engine.cuh is not among them: its fields
+# do not reach the kernel's device code.)
 KERNEL_SOURCES = ("autoregressive_tts_decode_gb300/csrc/frame_kernel.cu",
                   "autoregressive_tts_decode_gb300/csrc/sampler.cuh",
-                  "autoregressive_tts_decode_gb300/csrc/common.cuh",
-                  "autoregressive_tts_decode_gb300/csrc/engine.cuh", "include/q3tts.h")
+                  "autoregressive_tts_decode_gb300/csrc/common.cuh", "include/q3tts.h")
 
 
 def _code_only(text):
@@ -173,6 +174,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-ttfa", action="store_true", help="skip the prefill / first-frame timing")
     return ap.parse_args()
 
 
@@ -195,16 +197,72 @@ def cpu_baseline(wl, sample_frames=3, prompt_len=16):
     torch.cuda.empty_cache()
     orc = oracle.Oracle(s, Wc, 1, wl.kv_cap)
     orc.prefill(0, synth.make_prompts(s, [prompt_len])[0].numpy())
-    u = synth.uniforms([0], sample_frames + 1)[0]
+    u = synth.uniforms([0], sample_frames + 3)[0]
     orc.step_frame(0, wl.sampling, u[0])  # warm-up
+    cores = oracle.max_threads()
     t0 = time.perf_counter()
     for f in range(sample_frames):
         orc.step_frame(0, wl.sampling, u[f + 1])
     dt = time.perf_counter() - t0
-    return {"value": sample_frames / dt, "unit": UNIT, "cores": oracle.max_threads(),
+    # the same oracle on one core, for two further frames
+    oracle.set_threads(1)
+    t1 = time.perf_counter()
+    for f in range(2):
+        orc.step_frame(0, wl.sampling, u[sample_frames + 1 + f])
+    dt1 = time.perf_counter() - t1
+    oracle.set_threads(cores)
+    return {"value": sample_frames / dt, "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": f"{sample_frames} frames of stream 0 after a {prompt_len}-position prompt "
-                      f"(one warm-up frame discarded), {wl.name} shapes, fp64 oracle"}
+                      f"(one warm-up frame discarded), {wl.name} shapes, fp64 oracle",
+            "one_core": {"value": 2 / dt1, "unit": UNIT, "cores": 1,
+                         "sample": "the next 2 frames of the same stream on one thread"}}
+
+
+def prefill_and_ttfa(eng, stream, prompt, sampling, u_dev, codes, reps=5):
+    """Prefill time of one prompt and the time to the first frame of codes.
+
+    Device-timed: CUDA events on the engine's stream around q3tts_prefill alone,
+    and around prefill + the first frame decode (codes on the device).  End to
+    end: from the host's pinned prompt to the first frame's 16 codes back in
+    pinned host memory (H2D copy, prefill, frame, D2H copy, synchronise).  The
+    codec decoder that turns codes into samples is not part of this library, so
+    first audio here means the first frame of codes.  Median of `reps` runs
+    after one warm-up run."""
+    import torch
+    st = eng.stream
+    host_p = prompt.cpu().pin_memory()
+    dev_p = torch.empty_like(prompt)
+    host_c = torch.zeros((1, 16), dtype=torch.int32).pin_memory()
+    pre, ttfa, e2e = [], [], []
+    for r in range(reps + 1):
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        torch.cuda.synchronize()
+        a.record(st)
+        eng.prefill(stream, prompt)
+        b.record(st)
+        eng.step_frame([stream], sampling, u_dev, codes)
+        c.record(st)
+        eng.sync()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dev_p.copy_(host_p, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        eng.prefill(stream, dev_p)
+        eng.step_frame([stream], sampling, u_dev, codes)
+        host_c.copy_(codes[:1], non_blocking=True)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        if r:
+            pre.append(a.elapsed_time(b))
+            ttfa.append(a.elapsed_time(c))
+            e2e.append(1e3 * dt)
+    L = int(prompt.shape[0])
+    med = statistics.median
+    return {"prompt_len": L, "prefill_ms": med(pre), "prefill_tokens_per_s": 1e3 * L / med(pre),
+            "ttfa_ms": med(ttfa), "ttfa_e2e_ms": med(e2e), "runs": reps,
+            "note": "first audio = first frame of 16 codes (prefill + one frame decode); "
+                    "excluded from frames/s"}
 
 
 def run_reference(args):
@@ -377,6 +435,9 @@ def main():
                "h2d_bytes_per_step": 16 * 4 * B,
                "d2h_bytes_per_step": 16 * 4 * B}
 
+    ttfa = prefill_and_ttfa(eng, 0, prompts[0], wl.sampling, uni_d[0:1, 0].contiguous(),
+                            codes) if rank == 0 and not args.no_ttfa else None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         eng.close()
@@ -411,6 +472,7 @@ def main():
                          "algorithmic_bytes_per_step": bytes_per_step,
                          "step_ms_median": statistics.median(step_ms),
                          "step_ms_p90": sorted(step_ms)[int(0.9 * (len(step_ms) - 1))]},
+            "prefill": ttfa,
             "gpu_launches": launches,
             "clocks": clocks,
             "e2e": e2e,

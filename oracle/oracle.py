@@ -90,6 +90,7 @@ def lib():
         L.q3o_attention.argtypes = [dp, dp, dp, C.c_int, C.c_int, C.c_int, C.c_int, dp]
         L.q3o_talker_stack.argtypes = [C.c_void_p, C.c_int, dp, C.c_int, C.c_int]
         L.q3o_max_threads.restype = C.c_int
+        L.q3o_set_threads.argtypes = [C.c_int]
         L.q3o_cp_full.argtypes = [C.c_void_p, dp, fp]
         _lib = L
     return _lib
@@ -115,6 +116,11 @@ def sampling_struct(sp) -> _Sampling:
 
 def max_threads() -> int:
     return int(lib().q3o_max_threads())
+
+
+def set_threads(n: int) -> None:
+    """Thread count of the oracle's later parallel regions."""
+    lib().q3o_set_threads(int(n))
 
 
 def sample(logits: np.ndarray, do_sample: bool, top_k: int, top_p: float, temperature: float,

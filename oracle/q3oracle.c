@@ -487,6 +487,15 @@ int q3o_max_threads(void) {
 #endif
 }
 
+/* Thread count of later parallel regions (timing on a given number of cores). */
+void q3o_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /* Prompt (N(0,1) hidden vectors used directly as Talker inputs) at positions
  * 0..len-1; the stream restarts.  Returns 0, or -1 if len is out of range. */
 int q3o_prefill(void* h, int stream, const float* embeds, int len) {
