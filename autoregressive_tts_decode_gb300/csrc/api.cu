@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "engine.cuh"
+#include "layers.cuh"
 
 namespace q3 {
 int sampler_setup();
@@ -117,6 +118,9 @@ size_t carve(const q3tts_config& c, void* base, q3tts_handle* h) {
   float* att = cv.take<float>((size_t)d.m_max * d.Hq * d.hd);
   float* gu = cv.take<float>((size_t)d.m_max * 2 * F);
   float* act = cv.take<float>((size_t)d.m_max * F);
+  const int Kx = std::max(std::max(D, F), d.Hq * d.hd);
+  q3::bf16* xh = cv.take<q3::bf16>((size_t)d.m_max * Kx);
+  q3::bf16* xl = cv.take<q3::bf16>((size_t)d.m_max * Kx);
   float* uin = cv.take<float>((size_t)2 * d.S * d.Dt);
   float* cpx = cv.take<float>((size_t)2 * d.S * d.Dc);
   float* logits = cv.take<float>((size_t)d.S * V);
@@ -132,6 +136,7 @@ size_t carve(const q3tts_config& c, void* base, q3tts_handle* h) {
     h->d_sid = sid; h->d_pos = pos; h->d_sp = sp; h->d_fed = fed;
     h->d_tok_stream = tok_s; h->d_tok_pos = tok_p;
     h->x = x; h->hb = hb; h->qkv = qkv; h->att = att; h->gu = gu; h->act = act;
+    h->xh = xh; h->xl = xl;
     h->uin = uin; h->cpx = cpx; h->logits = logits; h->d_err = err;
     h->d_desc = desc; h->g_uni = g_uni; h->g_forced = g_forced; h->g_codes = g_codes;
   }
@@ -220,6 +225,13 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
   h->frame_kernel_off = env && env[0] == '0';
   const char* genv = getenv("Q3TTS_GRAPH");
   h->graph_off = genv && genv[0] == '0';
+  // the tensor-core projections: bf16 weights, every inner dimension a
+  // multiple of 64 (Q3TTS_TC=0: the fp32-FMA kernels instead)
+  const char* tenv = getenv("Q3TTS_TC");
+  h->tc = !(tenv && tenv[0] == '0') && c.weight_dtype == Q3TTS_BF16 &&
+          q3::tc_linear_ok(d.qkv_rows, d.Dt, 1) && q3::tc_linear_ok(d.qkv_rows, d.Dc, 1) &&
+          q3::tc_linear_ok(d.Dt, d.Ft, 1) && q3::tc_linear_ok(d.Dc, d.Fc, 1) &&
+          q3::tc_linear_ok(d.Dt, d.Hq * d.hd, 1);
 
   // RoPE tables: angle pos * theta^(-2i/hd), computed in double, stored as float.
   const int half = d.hd / 2;

@@ -51,6 +51,12 @@ struct q3tts_handle {
   int* d_tok_stream;      // [m_max]
   int* d_tok_pos;         // [m_max]
   float *x, *hb, *qkv, *att, *gu, *act, *uin, *cpx, *logits;
+  // hi/lo bf16 terms of the activations the tensor-core projections read
+  // ([m_max][K] each); tc: bf16 weights whose every inner dimension is a
+  // multiple of 64 take that path (Q3TTS_TC=0 turns it off)
+  q3::bf16 *xh, *xl;
+  bool tc = false;
+  bool tc_failed = false;  // a projection could not be launched
   int* d_err;
   // layered step replayed as a CUDA graph: the step's descriptor and its
   // per-call inputs/outputs pass through these fixed device buffers

@@ -308,6 +308,35 @@ __global__ void rmsnorm_kernel(const float* __restrict__ X, int ldx, int in_mul,
   for (int i = threadIdx.x; i < D; i += blockDim.x) Y[(size_t)m * ldy + i] = x[i] * inv * to_f(g[i]);
 }
 
+__device__ __forceinline__ void store_hilo(bf16* hi, bf16* lo, size_t i, float v) {
+  const bf16 h = __float2bfloat16_rn(v);
+  hi[i] = h;
+  lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
+template <class WT>
+__global__ void rmsnorm_hilo_kernel(const float* __restrict__ X, int ldx, int in_mul, int in_add,
+                                    const WT* __restrict__ g, bf16* __restrict__ hi, bf16* __restrict__ lo,
+                                    int D, float eps) {
+  __shared__ float red[32];
+  const int m = blockIdx.x;
+  const float* x = X + (size_t)(m * in_mul + in_add) * ldx;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+  ss = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(ss / (float)D + eps);
+  for (int i = threadIdx.x; i < D; i += blockDim.x) store_hilo(hi, lo, (size_t)m * D + i, x[i] * inv * to_f(g[i]));
+}
+
+void launch_rmsnorm_hilo(int wdt, const float* X, int ldx, int in_mul, int in_add, const void* g, const HiLo& y,
+                         int M, int D, float eps, cudaStream_t s) {
+  if (M <= 0) return;
+  if (wdt == Q3TTS_BF16)
+    rmsnorm_hilo_kernel<<<M, 256, 0, s>>>(X, ldx, in_mul, in_add, (const bf16*)g, y.hi, y.lo, D, eps);
+  else
+    rmsnorm_hilo_kernel<<<M, 256, 0, s>>>(X, ldx, in_mul, in_add, (const float*)g, y.hi, y.lo, D, eps);
+}
+
 void launch_rmsnorm(int wdt, const float* X, int ldx, int in_mul, int in_add, const void* g,
                     float* Y, int ldy, int M, int D, float eps, cudaStream_t s) {
   if (M <= 0) return;
@@ -722,6 +751,24 @@ void launch_silu_mul(const float* gu, float* a, int M, int F, cudaStream_t s) {
   int blocks = (int)((n + 255) / 256);
   if (blocks > 8192) blocks = 8192;
   silu_mul_kernel<<<blocks, 256, 0, s>>>(gu, a, M, F);
+}
+
+__global__ void silu_mul_hilo_kernel(const float* __restrict__ gu, bf16* __restrict__ hi, bf16* __restrict__ lo,
+                                     int M, int F) {
+  size_t n = (size_t)M * F;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n;
+       e += (size_t)gridDim.x * blockDim.x) {
+    size_t m = e / F, f = e % F;
+    store_hilo(hi, lo, e, silu(gu[m * 2 * F + f]) * gu[m * 2 * F + F + f]);
+  }
+}
+
+void launch_silu_mul_hilo(const float* gu, const HiLo& a, int M, int F, cudaStream_t s) {
+  if (M <= 0) return;
+  size_t n = (size_t)M * F;
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 8192) blocks = 8192;
+  silu_mul_hilo_kernel<<<blocks, 256, 0, s>>>(gu, a.hi, a.lo, M, F);
 }
 
 }  // namespace q3

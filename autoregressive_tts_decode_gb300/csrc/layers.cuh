@@ -43,4 +43,33 @@ void launch_attention(int kdt, const float* qkv, int ld, int M, TokDesc td, KVDe
 // a[m, f] = silu(gu[m, f]) * gu[m, F + f]
 void launch_silu_mul(const float* gu, float* a, int M, int F, cudaStream_t s);
 
+// Activation operand of the tensor-core projections: x = hi + lo, two bf16
+// matrices [rows][K] (row pitch K, the product's inner dimension), hi = bf16(x)
+// and lo = bf16(x - hi).
+struct HiLo {
+  bf16* hi;
+  bf16* lo;
+  int rows;  // rows the buffers hold
+};
+
+// Whether the tensor-core path takes a product of this shape (K % 64 == 0 and
+// the driver's tensor-map encoder is available).
+bool tc_linear_ok(int N, int K, int M);
+
+// Y[m, n] (+)= sum_k (hi[m, k] + lo[m, k]) W[n, k] for bf16 W [N, K] on the
+// tcgen05 tensor cores (tc_gemm.cu); err receives Q3TTS_ERR_TIMEOUT if a
+// bounded device wait runs out.  False if nothing was launched.
+bool tc_linear(const HiLo& x, const void* W, int N, int K, float* Y, int ldy, int M, bool accumulate, int* err,
+               cudaStream_t s);
+
+// x (fp32 [M, K], row pitch ldx) -> its hi/lo terms.
+void launch_split_hilo(const float* X, int ldx, const HiLo& x, int M, int K, cudaStream_t s);
+
+// RMSNorm (as launch_rmsnorm) written as hi/lo terms.
+void launch_rmsnorm_hilo(int wdt, const float* X, int ldx, int in_mul, int in_add, const void* g, const HiLo& y,
+                         int M, int D, float eps, cudaStream_t s);
+
+// silu(gu[m, f]) * gu[m, F + f] written as hi/lo terms.
+void launch_silu_mul_hilo(const float* gu, const HiLo& a, int M, int F, cudaStream_t s);
+
 }  // namespace q3

@@ -148,6 +148,28 @@ __global__ void scatter_pending_kernel(const int* __restrict__ sid, const float*
 
 // ------------------------------------------------------------ stack pass
 
+static HiLo hilo(const q3tts_handle* h) { return HiLo{h->xh, h->xl, h->m_max}; }
+
+// Y (+)= X W^T.  On the tensor-core path X is the hi/lo pair already written
+// by the producing kernel (xf unused); otherwise xf (fp32, row pitch ldx).
+static void proj(q3tts_handle* h, const float* xf, int ldx, const void* W, int N, int K, float* Y, int ldy,
+                 int M, bool acc) {
+  if (h->tc) {
+    if (!tc_linear(hilo(h), W, N, K, Y, ldy, M, acc, h->d_err, h->s)) h->tc_failed = true;
+  } else {
+    launch_linear(h->c.weight_dtype, xf, ldx, W, N, K, Y, ldy, M, acc, h->s);
+  }
+}
+
+// RMSNorm of M rows of X into the next projection's input: hi/lo terms on the
+// tensor-core path, else fp32 in h->hb.
+static void norm_in(q3tts_handle* h, const float* X, int ldx, int in_mul, int in_add, const void* g, int M, int D) {
+  if (h->tc)
+    launch_rmsnorm_hilo(h->c.weight_dtype, X, ldx, in_mul, in_add, g, hilo(h), M, D, h->c.rms_eps, h->s);
+  else
+    launch_rmsnorm(h->c.weight_dtype, X, ldx, in_mul, in_add, g, h->hb, D, M, D, h->c.rms_eps, h->s);
+}
+
 // M tokens through all layers of one decoder stack (residual stream x [M, D]).
 static void stack_pass(q3tts_handle* h, const q3tts_layer_weights* lw, int layers, int D, int F,
                        float* x, int M, TokDesc td, KVDesc kv, int kdt, int max_ctx) {
@@ -155,18 +177,22 @@ static void stack_pass(q3tts_handle* h, const q3tts_layer_weights* lw, int layer
   const int wdt = h->c.weight_dtype, HqD = h->Hq * h->hd;
   for (int l = 0; l < layers; ++l) {
     const q3tts_layer_weights& L = lw[l];
-    launch_rmsnorm(wdt, x, D, 1, 0, L.g_attn_norm, h->hb, D, M, D, h->c.rms_eps, s);
-    launch_linear(wdt, h->hb, D, L.w_qkv, h->qkv_rows, D, h->qkv, h->qkv_rows, M, false, s);
+    norm_in(h, x, D, 1, 0, L.g_attn_norm, M, D);
+    proj(h, h->hb, D, L.w_qkv, h->qkv_rows, D, h->qkv, h->qkv_rows, M, false);
     launch_qk_rope_append(wdt, kdt, h->qkv, h->qkv_rows, M, td, L.g_q_norm, L.g_k_norm,
                           h->c.qk_norm, h->c.rms_eps, h->rope_cos, h->rope_sin, kv, l, h->Hq, s);
     launch_attention(kdt, h->qkv, h->qkv_rows, M, td, kv, l, h->Hq, h->att, HqD, max_ctx, s);
-    launch_linear(wdt, h->att, HqD, L.w_o, D, HqD, x, D, M, true, s);
-    launch_rmsnorm(wdt, x, D, 1, 0, L.g_ffn_norm, h->hb, D, M, D, h->c.rms_eps, s);
-    launch_linear(wdt, h->hb, D, L.w_gateup, 2 * F, D, h->gu, 2 * F, M, false, s);
-    launch_silu_mul(h->gu, h->act, M, F, s);
-    launch_linear(wdt, h->act, F, L.w_down, D, F, x, D, M, true, s);
+    if (h->tc) launch_split_hilo(h->att, HqD, hilo(h), M, HqD, s);
+    proj(h, h->att, HqD, L.w_o, D, HqD, x, D, M, true);
+    norm_in(h, x, D, 1, 0, L.g_ffn_norm, M, D);
+    proj(h, h->hb, D, L.w_gateup, 2 * F, D, h->gu, 2 * F, M, false);
+    if (h->tc)
+      launch_silu_mul_hilo(h->gu, hilo(h), M, F, s);
+    else
+      launch_silu_mul(h->gu, h->act, M, F, s);
+    proj(h, h->act, F, L.w_down, D, F, x, D, M, true);
   }
-  h->launches += 9ull * layers;
+  h->launches += (h->tc ? 10ull : 9ull) * layers;
 }
 
 static size_t wbytes(const q3tts_handle* h) { return (size_t)h->esz; }
@@ -190,6 +216,10 @@ int prefill_layered(q3tts_handle* h, int sid, const float* embeds, int len) {
                     h->Vt, Dt, h->pending_logits + (size_t)sid * h->Vt, h->Vt, 1, false, s);
       h->launches += 2;
     }
+  }
+  if (h->tc_failed) {
+    h->tc_failed = false;
+    return Q3TTS_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? Q3TTS_OK : Q3TTS_ERR_CUDA;
 }
@@ -218,17 +248,20 @@ static void step_kernels(q3tts_handle* h, int n, int max_ctx, const float* unifo
       cp_input_kernel<float><<<M, 256, 0, s>>>(j, n, h->d_sid, h->d_fed, h->pending_h,
                                                (const float*)h->w.talker_e_codec,
                                                (const float*)h->w.cp_embeds, Dt, Vc, h->uin);
-    if (h->w.cp_w_proj)
-      launch_linear(wdt, h->uin, Dt, h->w.cp_w_proj, Dc, Dt, h->cpx, Dc, M, false, s);
-    else
+    if (h->w.cp_w_proj) {
+      if (h->tc) {
+        launch_split_hilo(h->uin, Dt, hilo(h), M, Dt, s);
+        h->launches += 1;
+      }
+      proj(h, h->uin, Dt, h->w.cp_w_proj, Dc, Dt, h->cpx, Dc, M, false);
+    } else
       cudaMemcpyAsync(h->cpx, h->uin, sizeof(float) * (size_t)M * Dc, cudaMemcpyDeviceToDevice, s);
     TokDesc td = j == 0 ? TokDesc{h->d_tok_stream, h->d_tok_pos, 0} : TokDesc{h->d_sid, nullptr, j + 1};
     stack_pass(h, h->cl.data(), h->c.cp_layers, Dc, h->Fc, h->cpx, M, td, cp_kv(h), Q3TTS_F32,
                Q3TTS_N_CODEBOOKS);
-    launch_rmsnorm(wdt, h->cpx, Dc, j == 0 ? 2 : 1, j == 0 ? 1 : 0, h->w.cp_g_final, h->hb, Dc, n,
-                   Dc, h->c.rms_eps, s);
+    norm_in(h, h->cpx, Dc, j == 0 ? 2 : 1, j == 0 ? 1 : 0, h->w.cp_g_final, n, Dc);
     const void* head = (const char*)h->w.cp_heads + (size_t)j * Vc * Dc * es;
-    launch_linear(wdt, h->hb, Dc, head, Vc, Dc, h->logits, Vc, n, false, s);
+    proj(h, h->hb, Dc, head, Vc, Dc, h->logits, Vc, n, false);
     sample_kernel<<<n, 256, smem, s>>>(h->logits, Vc, 0, h->d_sid, h->d_sp, nullptr, uniforms,
                                        j + 1, forced, codes, h->d_fed, logits, dump_ld,
                                        Vt + j * Vc, h->d_err);
@@ -243,8 +276,13 @@ static void step_kernels(q3tts_handle* h, int n, int max_ctx, const float* unifo
   TokDesc td{h->d_sid, h->d_pos, 0};
   stack_pass(h, h->tl.data(), h->c.talker_layers, Dt, h->Ft, h->x, n, td, talker_kv(h),
              h->c.kv_dtype, max_ctx);
+  // the normed hidden is also the stream's pending h_T (fp32)
   launch_rmsnorm(wdt, h->x, Dt, 1, 0, h->w.talker_g_final, h->hb, Dt, n, Dt, h->c.rms_eps, s);
-  launch_linear(wdt, h->hb, Dt, h->w.talker_w_head, Vt, Dt, h->logits, Vt, n, false, s);
+  if (h->tc) {
+    launch_split_hilo(h->hb, Dt, hilo(h), n, Dt, s);
+    h->launches += 1;
+  }
+  proj(h, h->hb, Dt, h->w.talker_w_head, Vt, Dt, h->logits, Vt, n, false);
   scatter_pending_kernel<<<n, 256, 0, s>>>(h->d_sid, h->hb, h->logits, Dt, Vt, h->pending_h,
                                            h->pending_logits);
   h->launches += 6;  // setup, semantic sample, embed-sum, final norm, head, scatter
@@ -316,6 +354,10 @@ int step_layered(q3tts_handle* h, const StepDesc& d, const float* uniforms, int3
     int max_ctx = 0;
     for (int b = 0; b < n; ++b) max_ctx = d.pos[b] + 1 > max_ctx ? d.pos[b] + 1 : max_ctx;
     step_kernels(h, n, max_ctx, uniforms, codes, forced, logits);
+  }
+  if (h->tc_failed) {
+    h->tc_failed = false;
+    return Q3TTS_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? Q3TTS_OK : Q3TTS_ERR_CUDA;
 }
