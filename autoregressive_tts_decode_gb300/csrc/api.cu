@@ -121,6 +121,9 @@ size_t carve(const q3tts_config& c, void* base, q3tts_handle* h) {
   const int Kx = std::max(std::max(D, F), d.Hq * d.hd);
   q3::bf16* xh = cv.take<q3::bf16>((size_t)d.m_max * Kx);
   q3::bf16* xl = cv.take<q3::bf16>((size_t)d.m_max * Kx);
+  const int nsmax = q3::attention_split_spans(c.kv_cap_steps);
+  float* spl_part = cv.take<float>((size_t)d.m_max * d.Hq * nsmax * (d.hd + 2));
+  int* spl_cnt = cv.take<int>((size_t)d.m_max * d.Hkv);
   float* uin = cv.take<float>((size_t)2 * d.S * d.Dt);
   float* cpx = cv.take<float>((size_t)2 * d.S * d.Dc);
   float* logits = cv.take<float>((size_t)d.S * V);
@@ -137,6 +140,7 @@ size_t carve(const q3tts_config& c, void* base, q3tts_handle* h) {
     h->d_tok_stream = tok_s; h->d_tok_pos = tok_p;
     h->x = x; h->hb = hb; h->qkv = qkv; h->att = att; h->gu = gu; h->act = act;
     h->xh = xh; h->xl = xl;
+    h->spl_part = spl_part; h->spl_cnt = spl_cnt; h->spl_nsmax = nsmax;
     h->uin = uin; h->cpx = cpx; h->logits = logits; h->d_err = err;
     h->d_desc = desc; h->g_uni = g_uni; h->g_forced = g_forced; h->g_codes = g_codes;
   }
@@ -249,7 +253,8 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
             cudaMemcpy(h->cp_page_table, cp_pt.data(), cp_pt.size() * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemset(h->page_table, 0, sizeof(int) * (size_t)d.S * d.pps) == cudaSuccess &&
             cudaMemset(h->history, 0, (size_t)d.S * d.Vt) == cudaSuccess &&
-            cudaMemset(h->d_err, 0, sizeof(int) * 64) == cudaSuccess;
+            cudaMemset(h->d_err, 0, sizeof(int) * 64) == cudaSuccess &&
+            cudaMemset(h->spl_cnt, 0, sizeof(int) * (size_t)d.m_max * d.Hkv) == cudaSuccess;
   if (!ok || q3::sampler_setup() != Q3TTS_OK) {
     delete h;
     return Q3TTS_ERR_CUDA;

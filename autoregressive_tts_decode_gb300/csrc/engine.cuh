@@ -57,6 +57,11 @@ struct q3tts_handle {
   q3::bf16 *xh, *xl;
   bool tc = false;
   bool tc_failed = false;  // a projection could not be launched
+  // split-context attention: span results [m_max][Hq][spl_nsmax][hd + 2] and
+  // per-(token, kv head) counters [m_max][Hkv] (zero between launches)
+  float* spl_part;
+  int* spl_cnt;
+  int spl_nsmax;
   int* d_err;
   // layered step replayed as a CUDA graph: the step's descriptor and its
   // per-call inputs/outputs pass through these fixed device buffers

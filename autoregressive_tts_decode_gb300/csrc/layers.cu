@@ -695,6 +695,357 @@ __global__ void __launch_bounds__(GQA_NW * 32) attention_gqa8_kernel(const float
   }
 }
 
+// ------------------------------------------ split-context paged attention
+//
+// Single-query attention for many tokens with long contexts (serving streams,
+// prefill chunks).  All (token, kv head) pairs' cache pages, 16 positions
+// each, form one list -- token by token, kv head by kv head -- and every warp
+// of a fixed grid (one wave; the grid does not depend on the contexts, so a
+// captured graph replays it unchanged) takes an equal run of consecutive
+// pages (at least SPL_MINP), so all warps finish together.  A warp's run
+// covers one or more segments (the pages of one (token, kv head)); per
+// segment it keeps an online softmax in registers and then writes the output
+// (when the run holds the whole segment) or (max, sum, unnormalised output) to
+// part[], where the last of the segment's runs to finish (a counter per
+// (token, kv head)) merges them and resets the counter.
+//
+// Per page the warp loads its K and V rows straight into registers -- lanes 2p
+// and 2p + 1 take position p, the even and the odd 16-byte pieces of its row
+// (each load instruction reads whole 32-byte sectors), and lane l takes
+// elements l hd/32 .. of every V row -- so a whole page is in flight, with no
+// shared-memory staging and no block barrier.  Scores use the group's q
+// vectors from the warp's shared slot (the same address for the 16 lanes of a
+// parity: a broadcast).
+constexpr int SPL_PAGE = 16;   // positions of a cache page this kernel takes
+constexpr int SPL_MINP = 2;    // fewest pages of a warp's run
+constexpr int SPL_RMAX = 4;    // q heads per kv head
+constexpr int SPL_WARPS = 4;   // warps of a CTA
+
+struct SplitArgs {
+  const float* qkv;
+  int ld, M;
+  TokDesc td;
+  KVDesc kv;
+  int layer, Hq;
+  float* out;
+  int ldo;
+  float* part;      // [M][Hq][nsmax][hd + 2]
+  int* cnt;         // [M][Hkv], zero between launches
+  int nsmax;        // runs per (token, kv head) the part buffer holds
+};
+
+// The token whose segments hold list entry idx, from the exclusive prefix
+// pfx[0..M] of the tokens' page counts x Hkv.
+__device__ __forceinline__ int split_token(const int* pfx, int M, int idx) {
+  int lo = 0, hi = M - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pfx[mid] <= idx) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <class KT, int HD, int REP>
+__global__ void __launch_bounds__(SPL_WARPS * 32) attention_split_kernel(SplitArgs a) {
+  constexpr int NCH = HD * (int)sizeof(KT) / 32;   // 16-byte loads per lane: its half of a row
+  constexpr int EPC = 16 / (int)sizeof(KT);        // elements per load
+  constexpr int OPL = HD / 32;                     // output elements per lane
+  constexpr int VW = OPL * (int)sizeof(KT);        // bytes of a lane's slice of a V row
+  extern __shared__ __align__(16) uint8_t spl_smem[];
+  float* qsm = reinterpret_cast<float*>(spl_smem);  // [warps][REP][HD]
+  int* pfx = reinterpret_cast<int*>(qsm + SPL_WARPS * REP * HD);  // [M + 1] page-list prefix
+  int* tpos = pfx + a.M + 1;                                     // [M] token positions
+  int* tstr = tpos + a.M;                                        // [M] token streams
+  const KVDesc& kv = a.kv;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int Hkv = kv.Hkv;
+  const float scale = 1.0f / sqrtf((float)HD);
+  const size_t head_stride = (size_t)SPL_PAGE * HD;
+  // page counts x Hkv per token (all threads), then their exclusive prefix
+  // (warp 0: lane i sums a run of consecutive tokens, a shuffle scan adds the runs)
+  for (int m = threadIdx.x; m < a.M; m += blockDim.x) {
+    const int pos = a.td.tok_pos ? a.td.tok_pos[m] : a.td.pos_const;
+    tpos[m] = pos;
+    tstr[m] = a.td.tok_stream[m];
+    pfx[m + 1] = (pos / SPL_PAGE + 1) * Hkv;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int run = (a.M + 31) / 32, m0 = lane * run, m1 = min(a.M, m0 + run);
+    int sum = 0;
+    for (int m = m0; m < m1; ++m) sum += pfx[m + 1];
+    int inc = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += v;
+    }
+    __syncwarp();
+    int acc = inc - sum;  // pages of the tokens before this run
+    for (int m = m0; m < m1; ++m) {
+      const int n = pfx[m + 1];
+      pfx[m + 1] = acc + n;
+      acc += n;
+    }
+    if (lane == 0) pfx[0] = 0;
+  }
+  __syncthreads();
+  const int total = pfx[a.M];
+  const int nwarps = gridDim.x * SPL_WARPS, wid = blockIdx.x * SPL_WARPS + warp;
+  const int ppw = max(SPL_MINP, (total + nwarps - 1) / nwarps);
+  const int lo = wid * ppw, hi = min(total, lo + ppw);
+  float* qw = qsm + warp * REP * HD;
+  const int p = lane >> 1, half = lane & 1;  // position, parity of the row's 16-byte pieces
+  for (int idx = lo; idx < hi;) {
+    // the segment (m, g) holding idx, and this run's pages j0 .. j1 - 1 of it
+    const int m = split_token(pfx, a.M, idx);
+    const int npg = tpos[m] / SPL_PAGE + 1, S = tpos[m] + 1, stream = tstr[m];
+    const int o = idx - pfx[m], g = o / npg, j0 = o % npg;
+    const int seg0 = pfx[m] + g * npg, seg1 = seg0 + npg;
+    const int j1 = j0 + (min(hi, seg1) - idx);
+    idx += j1 - j0;
+    // the group's q heads (contiguous in the token's qkv row)
+    __syncwarp();
+    {
+      const float4* qg = reinterpret_cast<const float4*>(a.qkv + (size_t)m * a.ld + (size_t)g * REP * HD);
+#pragma unroll
+      for (int e = lane; e < REP * HD / 4; e += 32) reinterpret_cast<float4*>(qw)[e] = __ldg(qg + e);
+    }
+    __syncwarp();
+    float M_[REP], L_[REP], ov[REP][OPL];
+#pragma unroll
+    for (int r = 0; r < REP; ++r) {
+      M_[r] = -INFINITY;
+      L_[r] = 0.f;
+#pragma unroll
+      for (int j = 0; j < OPL; ++j) ov[r][j] = 0.f;
+    }
+    const int* ptab = kv.page_table + (size_t)stream * kv.pages_per_stream;
+    for (int jb = j0; jb < j1; jb += 32) {
+      // page ids of up to 32 pages (lane k: page jb + k), loaded together
+      const int pid = jb + lane < j1 ? ptab[jb + lane] : 0;
+      const int jn = min(32, j1 - jb);
+      for (int jj = 0; jj < jn; ++jj) {
+        const int j = jb + jj;
+        const int page = __shfl_sync(0xffffffffu, pid, jj);
+        const KT* kb = (const KT*)kv.pool + ((((size_t)a.layer * kv.n_pages + page) * 2) * Hkv + g) * head_stride;
+        const uint8_t* kp = reinterpret_cast<const uint8_t*>(kb) + (size_t)p * HD * sizeof(KT) + (size_t)half * 16;
+        const uint8_t* vp = reinterpret_cast<const uint8_t*>(kb + (size_t)Hkv * head_stride) + (size_t)lane * VW;
+        const int nvalid = min(SPL_PAGE, S - j * SPL_PAGE);
+        // the page's loads, all in flight together
+        uint4 kr[NCH];
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) kr[i] = __ldcg(reinterpret_cast<const uint4*>(kp) + 2 * i);
+        uint32_t vr[SPL_PAGE][VW / 4];
+#pragma unroll
+        for (int q = 0; q < SPL_PAGE; ++q) {
+          if (q < nvalid) {  // rows past the context are not read (unwritten words may hold NaN)
+            if constexpr (VW == 8) {
+              const uint2 u = __ldcg(reinterpret_cast<const uint2*>(vp + (size_t)q * HD * sizeof(KT)));
+              vr[q][0] = u.x; vr[q][1] = u.y;
+            } else if constexpr (VW == 4) {
+              vr[q][0] = __ldcg(reinterpret_cast<const unsigned int*>(vp + (size_t)q * HD * sizeof(KT)));
+            } else {
+              const uint4 u = __ldcg(reinterpret_cast<const uint4*>(vp + (size_t)q * HD * sizeof(KT)));
+              vr[q][0] = u.x; vr[q][1] = u.y; vr[q][2] = u.z; vr[q][3] = u.w;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < VW / 4; ++e) vr[q][e] = 0u;
+          }
+        }
+        // scores of position p over this lane's half, both halves added
+        float d[REP];
+#pragma unroll
+        for (int r = 0; r < REP; ++r) d[r] = 0.f;
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+          float kf[EPC];
+          if constexpr (sizeof(KT) == 2) {
+            unpack_bf16x8(kr[i], kf);
+          } else {
+            kf[0] = __uint_as_float(kr[i].x); kf[1] = __uint_as_float(kr[i].y);
+            kf[2] = __uint_as_float(kr[i].z); kf[3] = __uint_as_float(kr[i].w);
+          }
+          const int i0 = (2 * i + half) * EPC;
+#pragma unroll
+          for (int r = 0; r < REP; ++r) {
+#pragma unroll
+            for (int e = 0; e < EPC; e += 4) {
+              const float4 qv = *reinterpret_cast<const float4*>(qw + r * HD + i0 + e);
+              d[r] = fmaf(qv.x, kf[e], d[r]);
+              d[r] = fmaf(qv.y, kf[e + 1], d[r]);
+              d[r] = fmaf(qv.z, kf[e + 2], d[r]);
+              d[r] = fmaf(qv.w, kf[e + 3], d[r]);
+            }
+          }
+        }
+        float w[REP];
+#pragma unroll
+        for (int r = 0; r < REP; ++r) {
+          float sc = (d[r] + __shfl_xor_sync(0xffffffffu, d[r], 1)) * scale;
+          if (p >= nvalid) sc = -INFINITY;
+          float pm = sc;  // over the 16 positions (lanes 2p and 2p + 1 hold the same value)
+#pragma unroll
+          for (int off = 16; off > 1; off >>= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, off));
+          const float Mn = fmaxf(M_[r], pm);  // finite: position 0 of a page exists
+          const float corr = __expf(M_[r] - Mn);
+          const float ex = sc == -INFINITY ? 0.f : __expf(sc - Mn);
+          float ps = ex;
+#pragma unroll
+          for (int off = 16; off > 1; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+          L_[r] = L_[r] * corr + ps;
+          M_[r] = Mn;
+#pragma unroll
+          for (int q = 0; q < OPL; ++q) ov[r][q] *= corr;
+          w[r] = ex;
+        }
+        // weighted values: lane l owns elements l OPL .. l OPL + OPL - 1
+#pragma unroll
+        for (int q = 0; q < SPL_PAGE; ++q) {
+          float vf[OPL];
+          if constexpr (sizeof(KT) == 2) {
+#pragma unroll
+            for (int e = 0; e < OPL / 2; ++e) {
+              vf[2 * e] = __uint_as_float(vr[q][e] << 16);
+              vf[2 * e + 1] = __uint_as_float(vr[q][e] & 0xffff0000u);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < OPL; ++e) vf[e] = __uint_as_float(vr[q][e]);
+          }
+#pragma unroll
+          for (int r = 0; r < REP; ++r) {
+            const float wq = __shfl_sync(0xffffffffu, w[r], 2 * q);
+#pragma unroll
+            for (int e = 0; e < OPL; ++e) ov[r][e] = fmaf(wq, vf[e], ov[r][e]);
+          }
+        }
+      }
+    }
+    // runs covering this segment: warps seg0 / ppw .. (seg1 - 1) / ppw
+    const int first = seg0 / ppw, nparts = (seg1 - 1) / ppw - first + 1;
+    if (nparts == 1) {
+#pragma unroll
+      for (int r = 0; r < REP; ++r) {
+        const float inv = 1.f / L_[r];
+        float* dst = a.out + (size_t)m * a.ldo + (g * REP + r) * HD + lane * OPL;
+#pragma unroll
+        for (int e = 0; e < OPL; ++e) dst[e] = ov[r][e] * inv;
+      }
+      continue;
+    }
+    // this run's (max, sum, unnormalised output) per head, in slot wid - first
+    float* pb0 = a.part + ((size_t)m * a.Hq + g * REP) * a.nsmax * (HD + 2);
+#pragma unroll
+    for (int r = 0; r < REP; ++r) {
+      float* pr = pb0 + ((size_t)r * a.nsmax + (wid - first)) * (HD + 2);
+#pragma unroll
+      for (int e = 0; e < OPL; ++e) pr[lane * OPL + e] = ov[r][e];
+      if (lane == 0) {
+        pr[HD] = M_[r];
+        pr[HD + 1] = L_[r];
+      }
+    }
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = atomicAdd(a.cnt + (size_t)m * Hkv + g, 1) == nparts - 1;
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) continue;
+    // the last run merges all runs of (m, g): lane s reads run s's max and sum
+    // (32 runs per pass), then each lane its OPL outputs
+    __threadfence();
+#pragma unroll
+    for (int r = 0; r < REP; ++r) {
+      const float* pr = pb0 + (size_t)r * a.nsmax * (HD + 2);
+      float mx = -INFINITY;
+      for (int s0 = lane; s0 < nparts; s0 += 32) mx = fmaxf(mx, __ldcg(pr + (size_t)s0 * (HD + 2) + HD));
+#pragma unroll
+      for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      float ls = 0.f;
+      for (int s0 = lane; s0 < nparts; s0 += 32) {
+        const float* q = pr + (size_t)s0 * (HD + 2);
+        ls += __ldcg(q + HD + 1) * __expf(__ldcg(q + HD) - mx);
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+      float acc[OPL];
+#pragma unroll
+      for (int e = 0; e < OPL; ++e) acc[e] = 0.f;
+#pragma unroll 4
+      for (int s0 = 0; s0 < nparts; ++s0) {
+        const float* q = pr + (size_t)s0 * (HD + 2);
+        const float f = __expf(__ldcg(q + HD) - mx);
+#pragma unroll
+        for (int e = 0; e < OPL; ++e) acc[e] = fmaf(__ldcg(q + lane * OPL + e), f, acc[e]);
+      }
+      const float inv = 1.f / ls;
+      float* dst = a.out + (size_t)m * a.ldo + (g * REP + r) * HD + lane * OPL;
+#pragma unroll
+      for (int e = 0; e < OPL; ++e) dst[e] = acc[e] * inv;
+    }
+    if (lane == 0) a.cnt[(size_t)m * Hkv + g] = 0;
+  }
+}
+
+template <class KT, int HD, int REP>
+static size_t split_smem(int M) {
+  return sizeof(float) * SPL_WARPS * REP * HD + sizeof(int) * (3 * (size_t)M + 1);
+}
+
+// Runs per (token, kv head) the split kernel's part buffer must hold for
+// contexts of up to kv_cap positions: a segment of npg pages meets at most
+// npg / SPL_MINP + 2 runs of at least SPL_MINP pages.
+int attention_split_spans(int kv_cap) { return (kv_cap + SPL_PAGE - 1) / SPL_PAGE / SPL_MINP + 2; }
+
+template <class KT, int HD, int REP>
+static bool launch_split_t(const SplitArgs& a, int n_sm, cudaStream_t s) {
+  static int per_sm = 0;  // resident CTAs per SM at the largest shared-memory size
+  if (a.M > 1024) return false;
+  if (!per_sm) {
+    if (cudaFuncSetAttribute(attention_split_kernel<KT, HD, REP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)split_smem<KT, HD, REP>(1024)) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attention_split_kernel<KT, HD, REP>, SPL_WARPS * 32,
+                                                      split_smem<KT, HD, REP>(1024)) != cudaSuccess ||
+        per_sm < 1) {
+      cudaGetLastError();
+      per_sm = 0;
+      return false;
+    }
+  }
+  // a persistent grid of one wave: every CTA stays resident and walks items
+  attention_split_kernel<KT, HD, REP><<<n_sm * per_sm, SPL_WARPS * 32, split_smem<KT, HD, REP>(a.M), s>>>(a);
+  return true;
+}
+
+template <class KT, int HD>
+static bool launch_split_rep(const SplitArgs& a, int rep, int n_sm, cudaStream_t s) {
+  switch (rep) {
+    case 1: return launch_split_t<KT, HD, 1>(a, n_sm, s);
+    case 2: return launch_split_t<KT, HD, 2>(a, n_sm, s);
+    case 4: return launch_split_t<KT, HD, 4>(a, n_sm, s);
+    default: return false;
+  }
+}
+
+bool launch_attention_split(int kdt, const float* qkv, int ld, int M, TokDesc td, KVDesc kv, int layer, int Hq,
+                            float* out, int ldo, float* part, int* cnt, int nsmax, cudaStream_t s) {
+  if (M <= 0) return true;
+  if (kv.page_size != SPL_PAGE || Hq / kv.Hkv > SPL_RMAX || (kv.hd != 64 && kv.hd != 128)) return false;
+  static int n_sm = 0;
+  if (!n_sm) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n_sm = 1;
+  }
+  SplitArgs a{qkv, ld, M, td, kv, layer, Hq, out, ldo, part, cnt, nsmax};
+  const int rep = Hq / kv.Hkv;
+  if (kdt == Q3TTS_BF16)
+    return kv.hd == 128 ? launch_split_rep<bf16, 128>(a, rep, n_sm, s) : launch_split_rep<bf16, 64>(a, rep, n_sm, s);
+  return kv.hd == 128 ? launch_split_rep<float, 128>(a, rep, n_sm, s) : launch_split_rep<float, 64>(a, rep, n_sm, s);
+}
+
 void launch_attention(int kdt, const float* qkv, int ld, int M, TokDesc td, KVDesc kv, int layer,
                       int Hq, float* out, int ldo, int max_ctx, cudaStream_t s) {
   if (M <= 0) return;

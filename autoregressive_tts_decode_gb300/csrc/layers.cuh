@@ -40,6 +40,16 @@ void launch_qk_rope_append(int wdt, int kdt, float* qkv, int ld, int M, TokDesc 
 void launch_attention(int kdt, const float* qkv, int ld, int M, TokDesc td, KVDesc kv, int layer,
                       int Hq, float* out, int ldo, int max_ctx, cudaStream_t s);
 
+// The same attention with all tokens' cache pages spread evenly over the
+// GPU's warps (pages of 16 positions, hd 64 or 128, 1, 2 or 4 q heads per kv
+// head; false if the shape is not one it takes).  part holds
+// [M][Hq][nsmax][hd + 2] floats of partial results (nsmax =
+// attention_split_spans(kv_cap)), cnt [M][Hkv] ints that must be zero before
+// the first launch (every launch leaves them zero).
+bool launch_attention_split(int kdt, const float* qkv, int ld, int M, TokDesc td, KVDesc kv, int layer, int Hq,
+                            float* out, int ldo, float* part, int* cnt, int nsmax, cudaStream_t s);
+int attention_split_spans(int kv_cap);
+
 // a[m, f] = silu(gu[m, f]) * gu[m, F + f]
 void launch_silu_mul(const float* gu, float* a, int M, int F, cudaStream_t s);
 

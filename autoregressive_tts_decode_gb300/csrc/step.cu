@@ -181,7 +181,10 @@ static void stack_pass(q3tts_handle* h, const q3tts_layer_weights* lw, int layer
     proj(h, h->hb, D, L.w_qkv, h->qkv_rows, D, h->qkv, h->qkv_rows, M, false);
     launch_qk_rope_append(wdt, kdt, h->qkv, h->qkv_rows, M, td, L.g_q_norm, L.g_k_norm,
                           h->c.qk_norm, h->c.rms_eps, h->rope_cos, h->rope_sin, kv, l, h->Hq, s);
-    launch_attention(kdt, h->qkv, h->qkv_rows, M, td, kv, l, h->Hq, h->att, HqD, max_ctx, s);
+    // contexts longer than one span: spread over the GPU by span
+    if (max_ctx <= 64 || !launch_attention_split(kdt, h->qkv, h->qkv_rows, M, td, kv, l, h->Hq, h->att, HqD,
+                                                 h->spl_part, h->spl_cnt, h->spl_nsmax, s))
+      launch_attention(kdt, h->qkv, h->qkv_rows, M, td, kv, l, h->Hq, h->att, HqD, max_ctx, s);
     if (h->tc) launch_split_hilo(h->att, HqD, hilo(h), M, HqD, s);
     proj(h, h->att, HqD, L.w_o, D, HqD, x, D, M, true);
     norm_in(h, x, D, 1, 0, L.g_ffn_norm, M, D);

@@ -270,3 +270,28 @@ def test_persistent_kernel_matches_layered_step(q3, oracle_mod, shape_name):
     for fk in (True, False):
         codes, logits, _ = out[fk]
         assert pu.sampler_replay(oracle_mod, shape, sp, codes[0], logits[0], out[True][0][0], u[0]) == 0
+
+
+@pytest.mark.parametrize("kv", ["f32", "bf16"])
+def test_long_contexts_split_attention(q3, oracle_mod, tiny_weights, kv):
+    """Streams whose contexts span several 64-position spans: the layered step and a
+    chunked prefill take the split-context attention (tiny shapes: head_dim 64, two
+    q heads per kv head), with an fp32 cache and with a bf16 cache (the oracle then
+    rounds k and v to bf16 as they enter its cache)."""
+    W, Wd = tiny_weights
+    shape = TINY.shape if kv == "f32" else dataclasses.replace(TINY.shape, kv_dtype=synth.DTYPE_BF16)
+    tol = TOL_F32 if kv == "f32" else 1e-3
+    sp = synth.QWEN_DEFAULT_SAMPLING
+    lens = [70, 300, 129]  # 2, 5 and 3 spans; the prefill runs in chunks of 128
+    ids = [0, 1, 2]
+    prompts = synth.make_prompts(shape, lens)
+    u = synth.uniforms(ids, 4)
+    eng = q3.Engine(shape, Wd, max_streams=3, kv_cap=512, prefill_chunk=128)
+    codes, logits = pu.run_gpu(eng, ids, prompts, sp, 4, uniforms=u)
+    eng.close()
+    for b, sid in enumerate(ids):
+        orc = oracle_mod.Oracle(shape, W, 1, 512, kv_bf16=(kv == "bf16"))
+        oc, ol = pu.run_oracle(orc, 0, prompts[b].numpy(), sp, 4, forced=codes[b], uniforms=u[b])
+        err, agree = pu.logits_report(logits[b], ol, shape)
+        assert err < tol and agree == 1.0, (lens[b], err, agree)
+        assert pu.sampler_replay(oracle_mod, shape, sp, codes[b], logits[b], codes[b], u[b]) == 0
