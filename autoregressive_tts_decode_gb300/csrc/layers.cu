@@ -90,184 +90,10 @@ __global__ void __launch_bounds__(256) gemm_kernel(const float* __restrict__ X, 
     }
 }
 
-// ------------------------------------------------ tensor-core skinny GEMM
-//
-// Y[m, n] (+)= sum_k X[m, k] W[n, k] for bf16 W with K % 64 == 0 and up to
-// 128 tokens per launch, on the tensor cores (mma.sync m16n8k16, fp32
-// accumulators).  The weight rows are the MMA's M side (16 per warp, 128 per
-// CTA) and the tokens its N side, so a few tokens still fill the MMA.  The fp32
-// activations enter as two bf16 terms, x = hi + lo with hi = bf16(x) and
-// lo = bf16(x - hi), each multiplied by the same weights: the product keeps
-// about 16 mantissa bits of x, close to an fp32 dot product.  K is split
-// across CTAs (blockIdx.y) so that every SM streams weights; partial sums meet
-// in Y through fp32 atomics (Y is cleared first unless accumulating).
-constexpr int MM_ROWS = 128;  // weight rows per CTA
-constexpr int MM_KC = 64;     // k per shared-memory stage
-constexpr int MM_MT = 128;    // tokens per launch
-constexpr int MM_LD = MM_KC + 8;  // padded smem row (bf16): ldmatrix rows fall in distinct banks
-constexpr int MM_STAGE = (MM_ROWS + 2 * MM_MT) * MM_LD;  // bf16 per stage: weights, x hi, x lo
-constexpr size_t MM_SMEM = (size_t)2 * MM_STAGE * sizeof(bf16);  // two stages
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// 16-byte asynchronous global -> shared copy; src_bytes 0 fills zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// Stage k-chunk kc into stage buffer sb: weight rows by asynchronous copies,
-// activations through registers (converted to bf16 hi and lo terms).
-__device__ __forceinline__ void mm_stage(bf16* smem, uint32_t sbase, int sb, const float* X, int ldx, const bf16* W,
-                                         int N, int K, int M, int n0, int kc, int nt) {
-  const int tid = threadIdx.x, k0 = kc * MM_KC;
-  bf16* st = smem + sb * MM_STAGE;
-  const uint32_t sw = sbase + (uint32_t)(sb * MM_STAGE * 2);
-  for (int e = tid; e < MM_ROWS * (MM_KC / 8); e += 256) {
-    const int r = e >> 3, c8 = (e & 7) * 8;
-    const int row = n0 + r < N ? n0 + r : N - 1;
-    cp_async16(sw + (uint32_t)((r * MM_LD + c8) * 2), W + (size_t)row * K + k0 + c8, n0 + r < N ? 16 : 0);
-  }
-  cp_async_commit();
-  bf16* Xh = st + MM_ROWS * MM_LD;
-  bf16* Xl = Xh + MM_MT * MM_LD;
-  for (int e = tid; e < nt * 8 * (MM_KC / 4); e += 256) {
-    const int m = e / (MM_KC / 4), c4 = (e % (MM_KC / 4)) * 4;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m < M) x = *reinterpret_cast<const float4*>(X + (size_t)m * ldx + k0 + c4);
-    const float xs[4] = {x.x, x.y, x.z, x.w};
-    bf16 hi[4], lo[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      hi[q] = __float2bfloat16_rn(xs[q]);
-      lo[q] = __float2bfloat16_rn(xs[q] - __bfloat162float(hi[q]));
-    }
-    *reinterpret_cast<uint2*>(Xh + m * MM_LD + c4) = *reinterpret_cast<const uint2*>(hi);
-    *reinterpret_cast<uint2*>(Xl + m * MM_LD + c4) = *reinterpret_cast<const uint2*>(lo);
-  }
-}
-
-__global__ void __launch_bounds__(256) gemm_mma_kernel(const float* __restrict__ X, int ldx,
-                                                       const bf16* __restrict__ W, int N, int K,
-                                                       float* __restrict__ Y, int ldy, int M, int kc_per) {
-  extern __shared__ __align__(16) bf16 mm_smem[];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * MM_ROWS;
-  const int kc0 = blockIdx.y * kc_per, kc1 = min(K / MM_KC, kc0 + kc_per);
-  const int nt = (M + 7) >> 3;  // token tiles of 8
-  float acc[MM_MT / 8][4];
-#pragma unroll
-  for (int j = 0; j < MM_MT / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(mm_smem);
-  if (kc0 < kc1) mm_stage(mm_smem, sbase, 0, X, ldx, W, N, K, M, n0, kc0, nt);
-  for (int kc = kc0; kc < kc1; ++kc) {
-    const int sb = (kc - kc0) & 1;
-    // the next chunk's copies go out before this chunk is multiplied
-    if (kc + 1 < kc1) {
-      mm_stage(mm_smem, sbase, sb ^ 1, X, ldx, W, N, K, M, n0, kc + 1, nt);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const uint32_t ws = sbase + (uint32_t)(sb * MM_STAGE * 2);
-    const uint32_t xh = ws + (uint32_t)(MM_ROWS * MM_LD * 2), xl = xh + (uint32_t)(MM_MT * MM_LD * 2);
-#pragma unroll
-    for (int ks = 0; ks < MM_KC / 16; ++ks) {
-      // A: the warp's 16 weight rows x 16 k (x4: rows 0-7 / 8-15, k 0-7 / 8-15)
-      uint32_t a0, a1, a2, a3;
-      {
-        const int r = warp * 16 + (lane & 15), c = ks * 16 + (lane >> 4) * 8;
-        ldsm_x4(ws + (uint32_t)((r * MM_LD + c) * 2), a0, a1, a2, a3);
-      }
-#pragma unroll
-      for (int j = 0; j < MM_MT / 8; ++j) {
-        if (j < nt) {
-          // B: 8 tokens x 16 k of each term (x2: k 0-7 / 8-15)
-          const int m = j * 8 + (lane & 7), c = ks * 16 + ((lane >> 3) & 1) * 8;
-          const uint32_t off = (uint32_t)((m * MM_LD + c) * 2);
-          uint32_t b0, b1, l0, l1;
-          ldsm_x2(xh + off, b0, b1);
-          ldsm_x2(xl + off, l0, l1);
-          mma_bf16(acc[j], a0, a1, a2, a3, b0, b1);
-          mma_bf16(acc[j], a0, a1, a2, a3, l0, l1);
-        }
-      }
-    }
-    __syncthreads();  // the stage is refilled two chunks later
-  }
-  // C fragment: rows (lane / 4, + 8) of the warp's 16, tokens 8 j + 2 (lane % 4) + {0, 1}
-  const int r0 = n0 + warp * 16 + (lane >> 2);
-#pragma unroll
-  for (int j = 0; j < MM_MT / 8; ++j) {
-    if (j < nt) {
-      const int m = j * 8 + (lane & 3) * 2;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int row = r0 + (q >> 1) * 8, tok = m + (q & 1);
-        if (row < N && tok < M && kc1 > kc0) atomicAdd(Y + (size_t)tok * ldy + row, acc[j][q]);
-      }
-    }
-  }
-}
-
-static int mm_ready = 0;
-
-// The tensor-core path for bf16 weights (see gemm_mma_kernel); false if this
-// shape is not one it takes.
-static bool linear_mma(const float* X, int ldx, const bf16* W, int N, int K, float* Y, int ldy, int M, bool acc,
-                       cudaStream_t s) {
-  if (M < 2 || K % MM_KC != 0 || (ldx & 3) || (((uintptr_t)X) & 15)) return false;
-  if (!mm_ready) {
-    if (cudaFuncSetAttribute(gemm_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MM_SMEM) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return false;
-    }
-    mm_ready = 1;
-  }
-  int dev = 0, nsm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  const int nrb = (N + MM_ROWS - 1) / MM_ROWS, nkc = K / MM_KC;
-  int splits = (2 * nsm + nrb - 1) / nrb;  // about two CTAs per SM
-  if (splits > nkc) splits = nkc;
-  if (splits < 1) splits = 1;
-  const int kc_per = (nkc + splits - 1) / splits;
-  splits = (nkc + kc_per - 1) / kc_per;
-  for (int m0 = 0; m0 < M; m0 += MM_MT) {
-    const int mm = M - m0 < MM_MT ? M - m0 : MM_MT;
-    float* y = Y + (size_t)m0 * ldy;
-    if (!acc && cudaMemset2DAsync(y, (size_t)ldy * sizeof(float), 0, (size_t)N * sizeof(float), mm, s) != cudaSuccess)
-      return false;
-    gemm_mma_kernel<<<dim3(nrb, splits), 256, MM_SMEM, s>>>(X + (size_t)m0 * ldx, ldx, W, N, K, y, ldy, mm, kc_per);
-  }
-  return true;
-}
-
 template <class WT>
 static void linear_t(const float* X, int ldx, const WT* W, int N, int K, float* Y, int ldy, int M,
                      bool acc, cudaStream_t s) {
   if (M <= 0 || N <= 0) return;
-  if constexpr (sizeof(WT) == 2) {
-    if (linear_mma(X, ldx, W, N, K, Y, ldy, M, acc, s)) return;
-  }
   if (M <= 16) {
     int blocks = (N + 7) / 8;
     if (blocks > 4096) blocks = 4096;
