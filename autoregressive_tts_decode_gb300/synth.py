@@ -61,6 +61,11 @@ class Sampling:
     sub_top_k: int = 50
     sub_top_p: float = 1.0
     sub_temperature: float = 0.9
+    # stop conditions: the semantic code that ends a stream (< 0: none), and
+    # the first special semantic code (codes >= it, other than eos_token, are
+    # never drawn; <= 0: none)
+    eos_token: int = -1
+    special_from: int = 0
 
 
 GREEDY = Sampling()

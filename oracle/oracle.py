@@ -58,7 +58,7 @@ class _Sampling(C.Structure):
     _fields_ = [("do_sample", C.c_int), ("top_k", C.c_int), ("top_p", C.c_float),
                 ("temperature", C.c_float), ("repetition_penalty", C.c_float),
                 ("sub_do_sample", C.c_int), ("sub_top_k", C.c_int), ("sub_top_p", C.c_float),
-                ("sub_temperature", C.c_float)]
+                ("sub_temperature", C.c_float), ("eos_token", C.c_int), ("special_from", C.c_int)]
 
 
 _lib = None
@@ -80,9 +80,9 @@ def lib():
         L.q3o_length.argtypes = [C.c_void_p, C.c_int]
         L.q3o_step_frame.argtypes = [C.c_void_p, C.c_int, C.POINTER(_Sampling), fp, ip, ip, fp]
         L.q3o_sample.argtypes = [fp, C.c_int, C.c_int, C.c_int, C.c_float, C.c_float, C.c_float,
-                                 C.c_char_p, C.c_float]
+                                 C.c_char_p, C.c_float, C.c_int, C.c_int]
         L.q3o_sample_f64.argtypes = [fp, C.c_int, C.c_int, C.c_int, C.c_double, C.c_double,
-                                     C.c_double, C.c_char_p, C.c_double, dp]
+                                     C.c_double, C.c_char_p, C.c_double, dp, C.c_int, C.c_int]
         L.q3o_expf.restype = C.c_float
         L.q3o_expf.argtypes = [C.c_float]
         L.q3o_rmsnorm.argtypes = [dp, C.c_int, fp, C.c_double, dp]
@@ -111,7 +111,8 @@ def _iptr(a: np.ndarray):
 def sampling_struct(sp) -> _Sampling:
     return _Sampling(int(sp.do_sample), int(sp.top_k), float(sp.top_p), float(sp.temperature),
                      float(sp.repetition_penalty), int(sp.sub_do_sample), int(sp.sub_top_k),
-                     float(sp.sub_top_p), float(sp.sub_temperature))
+                     float(sp.sub_top_p), float(sp.sub_temperature),
+                     int(getattr(sp, "eos_token", -1)), int(getattr(sp, "special_from", 0)))
 
 
 def max_threads() -> int:
@@ -124,20 +125,26 @@ def set_threads(n: int) -> None:
 
 
 def sample(logits: np.ndarray, do_sample: bool, top_k: int, top_p: float, temperature: float,
-           rep_penalty: float = 1.0, history: Optional[np.ndarray] = None, u: float = 0.0) -> int:
+           rep_penalty: float = 1.0, history: Optional[np.ndarray] = None, u: float = 0.0,
+           special_from: int = 0, eos_token: int = -1) -> int:
+    """The float rule; ids >= special_from (when > 0) other than eos_token are
+    never drawn."""
     lg = np.ascontiguousarray(logits, dtype=np.float32)
     hist = None if history is None else np.ascontiguousarray(history, dtype=np.uint8).tobytes()
     return int(lib().q3o_sample(_fptr(lg), lg.size, int(do_sample), int(top_k), float(top_p),
-                                float(temperature), float(rep_penalty), hist, float(u)))
+                                float(temperature), float(rep_penalty), hist, float(u),
+                                int(special_from), int(eos_token)))
 
 
-def sample_f64(logits, do_sample, top_k, top_p, temperature, rep_penalty=1.0, history=None, u=0.0):
+def sample_f64(logits, do_sample, top_k, top_p, temperature, rep_penalty=1.0, history=None, u=0.0,
+               special_from=0, eos_token=-1):
     """Returns (pick, margin): margin = distance of u*Z to the nearest CDF boundary / Z."""
     lg = np.ascontiguousarray(logits, dtype=np.float32)
     hist = None if history is None else np.ascontiguousarray(history, dtype=np.uint8).tobytes()
     mg = C.c_double(0.0)
     pick = lib().q3o_sample_f64(_fptr(lg), lg.size, int(do_sample), int(top_k), float(top_p),
-                                float(temperature), float(rep_penalty), hist, float(u), C.byref(mg))
+                                float(temperature), float(rep_penalty), hist, float(u), C.byref(mg),
+                                int(special_from), int(eos_token))
     return int(pick), float(mg.value)
 
 
@@ -235,7 +242,10 @@ class Oracle:
 
     def step_frame(self, stream: int, sampling, u: Sequence[float], forced=None,
                    want_logits: bool = False):
-        """Returns (codes int32[16], logits float32[V_t + 15 V_c] or None)."""
+        """Returns (codes int32[16], logits float32[V_t + 15 V_c] or None).  With
+        sampling.eos_token >= 0, a frame whose fed semantic code is that code
+        ends the stream (codes 1..15 are -1); every later frame of the stream
+        yields sixteen -1 until the stream is prefilled again."""
         s = self.shape
         uu = np.ascontiguousarray(np.asarray(u, dtype=np.float32).reshape(16))
         codes = np.zeros(16, dtype=np.int32)

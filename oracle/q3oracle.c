@@ -78,6 +78,8 @@ typedef struct {
   float top_p, temperature, repetition_penalty;
   int sub_do_sample, sub_top_k;
   float sub_top_p, sub_temperature;
+  int eos_token;     /* semantic code that ends the stream; < 0: none */
+  int special_from;  /* semantic codes >= this, except eos_token, are never drawn; <= 0: none */
 } q3o_sampling;
 
 typedef struct {
@@ -103,6 +105,7 @@ typedef struct {
   double* pending_h;       /* [D_t] final-normed hidden of the last position */
   double* pending_logits;  /* [V_t] */
   unsigned char* history;  /* [V_t] semantic codes emitted so far */
+  int finished;            /* the stream fed its end-of-stream code */
 } stream_state;
 
 typedef struct {
@@ -302,40 +305,51 @@ static int cand_cmp(const void* a, const void* b) {
   return (x->i > y->i) - (x->i < y->i);
 }
 
+/* Whether id may be drawn: ids >= special_from (when special_from > 0) are
+ * special codes, of which only eos_token may be drawn. */
+static int allowed_id(int id, int special_from, int eos_token) {
+  return special_from <= 0 || id < special_from || id == eos_token;
+}
+
 /* The token rule, in float, in this order ("qwen3-tts-hip" README, "Library
- * Usage": repetition_penalty, temperature, top_k, top_p, do_sample):
+ * Usage": repetition_penalty, temperature, top_k, top_p, do_sample; the
+ * candidate set first drops the special codes that may not be drawn):
+ *  0. candidates: the ids allowed_id() admits (V_eff of them);
  *  1. repetition penalty rho != 1: for each id in the history,
  *     l = l > 0 ? l / rho : l * rho;
  *  2. greedy (do_sample == 0): the largest l, lowest index on ties;
  *  3. l = l / T for every id;
  *  4. order ids by (l descending, index ascending); keep the first k
- *     (k <= 0 or k >= V keeps all);
+ *     (k <= 0 or k >= V_eff keeps all V_eff);
  *  5. m = first kept l; w_i = q3o_expf(l_i - m) in that order;
  *  6. top-p < 1: Z = w_0 + w_1 + ... (left to right, float); keep the shortest
  *     prefix whose running sum reaches top_p * Z (>=);
  *  7. Z = running float sum of the kept w; t = u * Z; the pick is the first
  *     kept id whose running sum is > t, else the last kept id. */
 int q3o_sample(const float* logits, int V, int do_sample, int top_k, float top_p, float temperature,
-               float rep_penalty, const unsigned char* history, float u) {
+               float rep_penalty, const unsigned char* history, float u, int special_from, int eos_token) {
   float* l = (float*)malloc(sizeof(float) * (size_t)V);
   memcpy(l, logits, sizeof(float) * (size_t)V);
   if (history && rep_penalty != 1.0f)
     for (int i = 0; i < V; ++i)
       if (history[i]) l[i] = l[i] > 0.0f ? l[i] / rep_penalty : l[i] * rep_penalty;
   if (!do_sample) {
-    int best = 0;
-    for (int i = 1; i < V; ++i)
-      if (l[i] > l[best]) best = i;
+    int best = -1;
+    for (int i = 0; i < V; ++i)
+      if (allowed_id(i, special_from, eos_token) && (best < 0 || l[i] > l[best])) best = i;
     free(l);
     return best;
   }
   cand* cs = (cand*)malloc(sizeof(cand) * (size_t)V);
+  int Ve = 0;
   for (int i = 0; i < V; ++i) {
-    cs[i].v = l[i] / temperature;
-    cs[i].i = i;
+    if (!allowed_id(i, special_from, eos_token)) continue;
+    cs[Ve].v = l[i] / temperature;
+    cs[Ve].i = i;
+    ++Ve;
   }
-  qsort(cs, (size_t)V, sizeof(cand), cand_cmp);
-  int K = (top_k <= 0 || top_k >= V) ? V : top_k;
+  qsort(cs, (size_t)Ve, sizeof(cand), cand_cmp);
+  int K = (top_k <= 0 || top_k >= Ve) ? Ve : top_k;
   float m = cs[0].v;
   float* w = (float*)malloc(sizeof(float) * (size_t)K);
   for (int i = 0; i < K; ++i) w[i] = q3o_expf(cs[i].v - m);
@@ -375,24 +389,30 @@ static int candd_cmp(const void* a, const void* b) {
  * receives |running_sum - u*Z| / Z at the nearest boundary. */
 int q3o_sample_f64(const float* logits, int V, int do_sample, int top_k, double top_p,
                    double temperature, double rep_penalty, const unsigned char* history, double u,
-                   double* margin) {
+                   double* margin, int special_from, int eos_token) {
   double* l = (double*)malloc(sizeof(double) * (size_t)V);
   for (int i = 0; i < V; ++i) l[i] = logits[i];
   if (history && rep_penalty != 1.0)
     for (int i = 0; i < V; ++i)
       if (history[i]) l[i] = l[i] > 0.0 ? l[i] / rep_penalty : l[i] * rep_penalty;
   if (!do_sample) {
-    int best = 0;
-    for (int i = 1; i < V; ++i)
-      if (l[i] > l[best]) best = i;
+    int best = -1;
+    for (int i = 0; i < V; ++i)
+      if (allowed_id(i, special_from, eos_token) && (best < 0 || l[i] > l[best])) best = i;
     if (margin) *margin = INFINITY;
     free(l);
     return best;
   }
   candd* cs = (candd*)malloc(sizeof(candd) * (size_t)V);
-  for (int i = 0; i < V; ++i) { cs[i].v = l[i] / temperature; cs[i].i = i; }
-  qsort(cs, (size_t)V, sizeof(candd), candd_cmp);
-  int K = (top_k <= 0 || top_k >= V) ? V : top_k;
+  int Ve = 0;
+  for (int i = 0; i < V; ++i) {
+    if (!allowed_id(i, special_from, eos_token)) continue;
+    cs[Ve].v = l[i] / temperature;
+    cs[Ve].i = i;
+    ++Ve;
+  }
+  qsort(cs, (size_t)Ve, sizeof(candd), candd_cmp);
+  int K = (top_k <= 0 || top_k >= Ve) ? Ve : top_k;
   double* w = (double*)malloc(sizeof(double) * (size_t)K);
   for (int i = 0; i < K; ++i) w[i] = exp(cs[i].v - cs[0].v);
   if (top_p < 1.0) {
@@ -504,6 +524,7 @@ int q3o_prefill(void* h, int stream, const float* embeds, int len) {
   if (stream < 0 || stream >= c->n_streams || len < 1 || len >= c->kv_cap) return -1;
   stream_state* st = &m->st[stream];
   memset(st->history, 0, (size_t)c->codec_vocab);
+  st->finished = 0;
   int D = c->talker_hidden;
   double* x = (double*)malloc(sizeof(double) * (size_t)len * D);
   for (size_t i = 0; i < (size_t)len * D; ++i) x[i] = embeds[i];
@@ -574,11 +595,25 @@ int q3o_step_frame(void* h, int stream, const q3o_sampling* sp, const float* u, 
   float* lf = (float*)malloc(sizeof(float) * (size_t)(Vt > Vc ? Vt : Vc));
   double* ld = (double*)malloc(sizeof(double) * (size_t)Vc);
 
+  /* a finished stream yields no codes and keeps its state */
+  if (st->finished) {
+    for (int j = 0; j < c->n_codebooks; ++j) codes_out[j] = -1;
+    free(lf); free(ld);
+    return 0;
+  }
   for (int i = 0; i < Vt; ++i) lf[i] = (float)st->pending_logits[i];
   if (logits_out) memcpy(logits_out, lf, sizeof(float) * (size_t)Vt);
   codes_out[0] = q3o_sample(lf, Vt, sp->do_sample, sp->top_k, sp->top_p, sp->temperature,
-                            sp->repetition_penalty, st->history, u[0]);
+                            sp->repetition_penalty, st->history, u[0], sp->special_from, sp->eos_token);
   fed[0] = forced ? forced[0] : codes_out[0];
+  /* the end-of-stream code ends the stream with this frame: no acoustic
+   * codes, no Talker step */
+  if (sp->eos_token >= 0 && fed[0] == sp->eos_token) {
+    st->finished = 1;
+    for (int j = 1; j < c->n_codebooks; ++j) codes_out[j] = -1;
+    free(lf); free(ld);
+    return 0;
+  }
   st->history[fed[0]] = 1;
 
   /* CodePredictor: the cache restarts every frame */
@@ -596,7 +631,7 @@ int q3o_step_frame(void* h, int stream, const q3o_sampling* sp, const float* u, 
     for (int i = 0; i < Vc; ++i) lf[i] = (float)ld[i];
     if (logits_out) memcpy(logits_out + Vt + (size_t)j * Vc, lf, sizeof(float) * (size_t)Vc);
     codes_out[j + 1] = q3o_sample(lf, Vc, sp->sub_do_sample, sp->sub_top_k, sp->sub_top_p,
-                                  sp->sub_temperature, 1.0f, NULL, u[j + 1]);
+                                  sp->sub_temperature, 1.0f, NULL, u[j + 1], 0, -1);
     fed[j + 1] = forced ? forced[j + 1] : codes_out[j + 1];
   }
 

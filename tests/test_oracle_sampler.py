@@ -144,3 +144,81 @@ def test_float_rule_matches_double_rule_away_from_boundaries(oracle_mod):
         else:
             n += 1
     assert n >= 295
+
+
+# --- special codes and the end-of-stream code (stop conditions) -------------
+# Reading adopted: codes >= special_from are special; of them only eos_token may
+# be drawn.  The candidate set is the allowed codes, so the draw is the same
+# rule over the allowed codes alone.
+
+def test_masked_measure_v8(oracle_mod):
+    """V = 8, special_from = 5, eos_token = 6: the measure of u mapped to token
+    i is softmax over the allowed codes {0..4, 6} (zero for 5 and 7), checked on
+    a 2^-14 grid of u, with top-k disabled (0) and with k >= the allowed count."""
+    rng = np.random.default_rng(11)
+    allowed = np.array([1, 1, 1, 1, 1, 0, 1, 0], dtype=bool)
+    for trial in range(3):
+        lg = rng.normal(scale=2.0, size=8).astype(np.float32)
+        lg[7] = lg.max() + 3.0  # a special code that would otherwise dominate
+        T = [1.0, 0.7, 1.6][trial]
+        z = np.where(allowed, lg.astype(np.float64) / T, -np.inf)
+        p = np.exp(z - z.max())
+        p /= p.sum()
+        n = 1 << 14
+        for k_top in (0, 6, 8):
+            counts = np.zeros(8)
+            for k in range(n):
+                counts[oracle_mod.sample(lg, True, k_top, 1.0, T, u=k / n, special_from=5, eos_token=6)] += 1
+            assert counts[5] == 0 and counts[7] == 0
+            assert np.allclose(counts / n, p, atol=2.0 / n + 1e-6), (k_top, counts / n, p)
+        # u just below 1 still picks an allowed code (the fallback is the last allowed kept)
+        assert allowed[oracle_mod.sample(lg, True, 0, 1.0, T, u=1.0 - 2 ** -24, special_from=5, eos_token=6)]
+
+
+def test_masked_greedy_and_eos_allowed(oracle_mod):
+    lg = np.array([0.1, 0.5, 0.2, 3.0, 2.0, 1.0], dtype=np.float32)
+    # codes 3.. are special: 3 and 5 are masked, 4 is the end-of-stream code
+    assert oracle_mod.sample(lg, False, 0, 1.0, 1.0, special_from=3, eos_token=4) == 4
+    assert oracle_mod.sample(lg, False, 0, 1.0, 1.0, special_from=3, eos_token=-1) == 1
+    assert oracle_mod.sample(lg, False, 0, 1.0, 1.0) == 3  # no masking
+    # top-k 1 over the allowed codes is their argmax
+    assert oracle_mod.sample(lg, True, 1, 1.0, 1.0, u=0.99, special_from=3, eos_token=4) == 4
+
+
+def test_end_of_stream_frames(oracle_mod):
+    """A frame whose fed semantic code is eos_token yields [c0, -1 x 15] and ends
+    the stream; later frames yield sixteen -1 and leave the stream's state as it
+    was; a prefill restarts it."""
+    import dataclasses
+    from autoregressive_tts_decode_gb300 import synth
+    shape = synth.WORKLOADS["tiny"].shape
+    W = synth.make_weights(shape)
+    p = synth.make_prompts(shape, [8])[0].numpy()
+    u = synth.uniforms([0], 4)[0]
+    eos = 777
+    sp = dataclasses.replace(synth.GREEDY, eos_token=eos, special_from=0)
+    orc = oracle_mod.Oracle(shape, W, 1, 64)
+    orc.prefill(0, p)
+    c0, _ = orc.step_frame(0, sp, u[0])
+    assert (c0 >= 0).all()
+    forced = c0.copy()
+    forced[0] = eos
+    h_before, l_before = orc.pending(0)
+    n_before = orc.length(0)
+    c1, _ = orc.step_frame(0, sp, u[1], forced=forced)
+    assert (c1[1:] == -1).all() and c1[0] >= 0
+    c2, _ = orc.step_frame(0, sp, u[2])
+    assert (c2 == -1).all()
+    h_after, l_after = orc.pending(0)
+    assert orc.length(0) == n_before
+    assert np.array_equal(h_before, h_after) and np.array_equal(l_before, l_after)
+    # a prefill restarts the stream: the same first frame as before
+    orc.prefill(0, p)
+    c3, _ = orc.step_frame(0, sp, u[0])
+    assert np.array_equal(c3, c0)
+    # without an end-of-stream code the forced code is an ordinary semantic code
+    orc2 = oracle_mod.Oracle(shape, W, 1, 64)
+    orc2.prefill(0, p)
+    orc2.step_frame(0, synth.GREEDY, u[0])
+    c4, _ = orc2.step_frame(0, synth.GREEDY, u[1], forced=forced)
+    assert (c4 >= 0).all()
