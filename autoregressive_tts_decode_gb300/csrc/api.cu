@@ -106,6 +106,7 @@ size_t carve(const q3tts_config& c, void* base, q3tts_handle* h) {
   float* pend_h = cv.take<float>((size_t)d.S * d.Dt);
   float* pend_l = cv.take<float>((size_t)d.S * d.Vt);
   uint8_t* hist = cv.take<uint8_t>((size_t)d.S * d.Vt);
+  uint8_t* fin = cv.take<uint8_t>((size_t)d.S);
   int* sid = cv.take<int>(d.S);
   int* pos = cv.take<int>(d.S);
   q3tts_sampling* sp = cv.take<q3tts_sampling>(d.S);
@@ -135,7 +136,7 @@ size_t carve(const q3tts_config& c, void* base, q3tts_handle* h) {
   if (h) {
     h->rope_cos = rope_cos; h->rope_sin = rope_sin; h->kv_pool = kv_pool;
     h->page_table = page_table; h->cp_kv = cpkv; h->cp_page_table = cp_pt;
-    h->pending_h = pend_h; h->pending_logits = pend_l; h->history = hist;
+    h->pending_h = pend_h; h->pending_logits = pend_l; h->history = hist; h->finished = fin;
     h->d_sid = sid; h->d_pos = pos; h->d_sp = sp; h->d_fed = fed;
     h->d_tok_stream = tok_s; h->d_tok_pos = tok_p;
     h->x = x; h->hb = hb; h->qkv = qkv; h->att = att; h->gu = gu; h->act = act;
@@ -153,12 +154,27 @@ void free_stream_pages(q3tts_handle* h, int sid) {
   h->pages[sid].clear();
 }
 
-bool check_sampling(const q3tts_sampling& p) {
+bool check_sampling(const q3tts_sampling& p, int Vt) {
   if (p.do_sample && !(p.temperature > 0.f)) return false;
   if (p.sub_do_sample && !(p.sub_temperature > 0.f)) return false;
   if (!(p.top_p > 0.f) || !(p.sub_top_p > 0.f)) return false;
   if (!(p.repetition_penalty > 0.f)) return false;
+  if (p.eos_token >= Vt || p.special_from > Vt) return false;
   return true;
+}
+
+// The controls as the kernels take them: with special codes masked, a
+// disabled semantic top-k (<= 0 or >= the allowed count) keeps exactly the
+// allowed codes, which the masked logits' order puts first.
+q3tts_sampling device_sampling(const q3tts_sampling& p, int Vt) {
+  q3tts_sampling d = p;
+  if (p.special_from > 0 && p.special_from < Vt) {
+    const int allowed = p.special_from + (p.eos_token >= p.special_from ? 1 : 0);
+    if (d.top_k <= 0 || d.top_k >= allowed) d.top_k = allowed;
+  } else {
+    d.special_from = 0;
+  }
+  return d;
 }
 
 }  // namespace
@@ -253,6 +269,7 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
             cudaMemcpy(h->cp_page_table, cp_pt.data(), cp_pt.size() * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
             cudaMemset(h->page_table, 0, sizeof(int) * (size_t)d.S * d.pps) == cudaSuccess &&
             cudaMemset(h->history, 0, (size_t)d.S * d.Vt) == cudaSuccess &&
+            cudaMemset(h->finished, 0, (size_t)d.S) == cudaSuccess &&
             cudaMemset(h->d_err, 0, sizeof(int) * 64) == cudaSuccess &&
             cudaMemset(h->spl_cnt, 0, sizeof(int) * (size_t)d.m_max * d.Hkv) == cudaSuccess;
   if (!ok || q3::sampler_setup() != Q3TTS_OK) {
@@ -297,7 +314,8 @@ int q3tts_prefill(q3tts_handle* h, int sid, const float* embeds_dev, int len) {
   // pageable source: staged before the call returns, so `row` may go away
   if (cudaMemcpyAsync(h->page_table + (size_t)sid * h->pps, row.data(), sizeof(int) * need,
                       cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemsetAsync(h->history + (size_t)sid * h->Vt, 0, h->Vt, s) != cudaSuccess)
+      cudaMemsetAsync(h->history + (size_t)sid * h->Vt, 0, h->Vt, s) != cudaSuccess ||
+      cudaMemsetAsync(h->finished + sid, 0, 1, s) != cudaSuccess)
     return Q3TTS_ERR_CUDA;
   int rc = q3::prefill_layered(h, sid, embeds_dev, len);
   h->len[sid] = rc == Q3TTS_OK ? len : -1;
@@ -317,7 +335,7 @@ int q3tts_step_frame(q3tts_handle* h, const q3tts_sampling* params, const int32_
     int s = stream_ids[b];
     if (s < 0 || s >= h->c.max_streams || seen[s]) return Q3TTS_ERR_ARG;
     seen[s] = 1;
-    if (!check_sampling(params[b])) return Q3TTS_ERR_ARG;
+    if (!check_sampling(params[b], h->Vt)) return Q3TTS_ERR_ARG;
     if (h->len[s] < 1) return Q3TTS_ERR_STATE;
     if (h->len[s] >= h->c.kv_cap_steps) return Q3TTS_ERR_CAPACITY;
     if (h->len[s] / h->c.page_size >= (int)h->pages[s].size()) ++pages_needed;
@@ -330,7 +348,7 @@ int q3tts_step_frame(q3tts_handle* h, const q3tts_sampling* params, const int32_
     int s = stream_ids[b];
     d.sid[b] = s;
     d.pos[b] = h->len[s];
-    d.sp[b] = params[b];
+    d.sp[b] = device_sampling(params[b], h->Vt);
     d.newpage[b] = -1;
     if (h->len[s] / h->c.page_size >= (int)h->pages[s].size())
       d.newpage[b] = h->free_pages[h->free_pages.size() - 1 - taken++];
@@ -359,8 +377,9 @@ int q3tts_step_frame_static(q3tts_handle* h, const q3tts_sampling* params, int s
                             const int32_t* forced_dev, float* logits_dev) {
   if (!h || !params || !uniforms_dev || !codes_dev) return Q3TTS_ERR_ARG;
   const int s = stream_id;
-  if (s < 0 || s >= h->c.max_streams || !check_sampling(*params)) return Q3TTS_ERR_ARG;
-  int rc = q3::frame_kernel_static_check(h, *params);
+  if (s < 0 || s >= h->c.max_streams || !check_sampling(*params, h->Vt)) return Q3TTS_ERR_ARG;
+  const q3tts_sampling sp = device_sampling(*params, h->Vt);
+  int rc = q3::frame_kernel_static_check(h, sp);
   if (rc != Q3TTS_OK) return rc;
   if (h->len[s] < 1) return Q3TTS_ERR_STATE;
   if (h->len[s] >= h->c.kv_cap_steps) return Q3TTS_ERR_CAPACITY;
@@ -371,7 +390,7 @@ int q3tts_step_frame_static(q3tts_handle* h, const q3tts_sampling* params, int s
   const bool grow = h->len[s] / h->c.page_size >= (int)h->pages[s].size();
   if (grow && h->free_pages.empty()) return Q3TTS_ERR_CAPACITY;
   const int newpage = grow ? h->free_pages.back() : -1;
-  rc = q3::frame_kernel_step_static(h, s, h->len[s], newpage, *params, uniforms_dev, codes_dev,
+  rc = q3::frame_kernel_step_static(h, s, h->len[s], newpage, sp, uniforms_dev, codes_dev,
                                     forced_dev, logits_dev);
   if (rc != Q3TTS_OK) return rc;
   if (grow) {
@@ -404,8 +423,19 @@ int q3tts_reset(q3tts_handle* h, int sid) {
     h->len[s] = -1;
   }
   size_t n = (size_t)(hi - lo) * h->Vt;
-  if (cudaMemsetAsync(h->history + (size_t)lo * h->Vt, 0, n, h->s) != cudaSuccess)
+  if (cudaMemsetAsync(h->history + (size_t)lo * h->Vt, 0, n, h->s) != cudaSuccess ||
+      cudaMemsetAsync(h->finished + lo, 0, (size_t)(hi - lo), h->s) != cudaSuccess)
     return Q3TTS_ERR_CUDA;
+  return Q3TTS_OK;
+}
+
+int q3tts_stream_finished(q3tts_handle* h, int sid, int* finished) {
+  if (!h || !finished || sid < 0 || sid >= h->c.max_streams) return Q3TTS_ERR_ARG;
+  uint8_t f = 0;
+  if (cudaMemcpyAsync(&f, h->finished + sid, 1, cudaMemcpyDeviceToHost, h->s) != cudaSuccess ||
+      cudaStreamSynchronize(h->s) != cudaSuccess)
+    return Q3TTS_ERR_CUDA;
+  *finished = f ? 1 : 0;
   return Q3TTS_OK;
 }
 

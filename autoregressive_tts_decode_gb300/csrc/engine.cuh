@@ -44,6 +44,7 @@ struct q3tts_handle {
   float* pending_h;       // [max_streams][D_t]
   float* pending_logits;  // [max_streams][V_t]
   uint8_t* history;       // [max_streams][V_t]
+  uint8_t* finished;      // [max_streams]: the stream fed its end-of-stream code
   int* d_sid;             // [max_streams]
   int* d_pos;
   q3tts_sampling* d_sp;

@@ -110,6 +110,7 @@ struct FKParams {
   float* pending_h;
   float* pending_logits;
   uint8_t* history;
+  uint8_t* finished;  // per stream: its end-of-stream code was fed
   KVDesc tkv, ckv;
   const float* rope_cos;
   const float* rope_sin;
@@ -369,6 +370,7 @@ struct FKSmem {
   float uni[Q3TTS_N_CODEBOOKS];
   int forced[Q3TTS_N_CODEBOOKS];
   int fedc[Q3TTS_N_CODEBOOKS];  // the frame's codes fed forward so far
+  int fin_state;                 // CTA 0: 0 running, 1 ended by this frame, 2 ended before
   int tpage[FK_MAXPAGES];  // the stream's Talker page table (when it has at most FK_MAXPAGES pages)
   int cpage;               // the stream's CodePredictor page
   alignas(8) uint64_t full[FK_NSTAGE];
@@ -1080,12 +1082,21 @@ __device__ __noinline__ int draw_code(Cons c, int j, uint32_t ltag) {
                            tag_float(raw[4 * q + 3]));
     }
     float* dump = p.dump && ccta() == 0 ? p.dump + (sem ? 0 : p.Vt + (j - 1) * p.Vc) : nullptr;
+    // special semantic codes other than the end-of-stream code are never
+    // drawn (the dump keeps the raw logits)
+    const int sf = sem ? p.sp.special_from : 0;
 #pragma unroll
     for (int q = 0; q < FAST_V4; ++q) {
       const int e = 4 * (ctid() + FK_CONSUMERS * q);
       if (e < V) {
-        *reinterpret_cast<float4*>(lv + e) = v[q];
         if (dump) *reinterpret_cast<float4*>(dump + e) = v[q];
+        if (sf > 0) {
+          float* f = reinterpret_cast<float*>(&v[q]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (e + k >= sf && e + k != p.sp.eos_token) f[k] = -INFINITY;
+        }
+        *reinterpret_cast<float4*>(lv + e) = v[q];
       }
     }
   }
@@ -1105,7 +1116,21 @@ __device__ __noinline__ int draw_code(Cons c, int j, uint32_t ltag) {
       fed = code;
     }
   }
-  if (ccta() == 0 && ctid() == 0) p.codes[j] = code;
+  // codes out (CTA 0, thread 0 alone): a finished stream writes -1; the frame
+  // that feeds the end-of-stream code keeps its semantic code and ends the
+  // stream.  The frame itself is computed either way.
+  if (ccta() == 0 && ctid() == 0) {
+    FKSmem* sm = fk_sm();
+    if (sem) {
+      const bool before = p.finished[p.sid] != 0;
+      const bool eos = p.sp.eos_token >= 0 && fed == p.sp.eos_token;
+      sm->fin_state = before ? 2 : (eos ? 1 : 0);
+      if (eos && !before) p.finished[p.sid] = 1;
+      p.codes[0] = before ? -1 : code;
+    } else {
+      p.codes[j] = sm->fin_state ? -1 : code;
+    }
+  }
   return fed;
 }
 
@@ -2605,6 +2630,7 @@ static void frame_params(FKParams& p, const q3tts_handle* h, int sid, int pos, i
   p.cp_embeds = h->w.cp_embeds; p.cp_proj = h->w.cp_w_proj; p.t_gfinal = h->w.talker_g_final;
   p.cp_gfinal = h->w.cp_g_final;
   p.pending_h = h->pending_h; p.pending_logits = h->pending_logits; p.history = h->history;
+  p.finished = h->finished;
   p.tkv = talker_kv(h); p.ckv = cp_kv(h); p.rope_cos = h->rope_cos; p.rope_sin = h->rope_sin;
   p.xb = st->xb; p.xa = st->xa; p.xf = st->xf;
   p.qkv = st->qkv; p.z = st->z; p.part = st->part; p.cp_logits = st->cp_logits;

@@ -66,22 +66,30 @@ __global__ void fill_tokens_kernel(int* tok_stream, int* tok_pos, int T, int sid
 // One block per active stream.  semantic != 0: the Talker's pending logits of
 // the stream, its repetition history and the semantic controls; otherwise row
 // b of `logits` with the sub-talker controls.
+// Codes out follow the stop conditions: a stream whose end-of-stream code was
+// fed writes -1; the frame that feeds it keeps its semantic code, marks the
+// stream finished, and writes -1 for its acoustic codes (the frame itself is
+// computed either way).  Special semantic codes other than the end-of-stream
+// code are masked before the draw (the dump keeps the raw logits).
 __global__ void __launch_bounds__(256) sample_kernel(
     const float* __restrict__ logits, int V, int semantic, const int* __restrict__ sid,
-    const q3tts_sampling* __restrict__ sp, uint8_t* history, const float* __restrict__ uniforms,
-    int cb, const int32_t* __restrict__ forced, int32_t* __restrict__ codes, int* __restrict__ fed,
-    float* __restrict__ dump, int dump_ld, int dump_off, int* err) {
+    const q3tts_sampling* __restrict__ sp, uint8_t* history, uint8_t* finished,
+    const float* __restrict__ uniforms, int cb, const int32_t* __restrict__ forced,
+    int32_t* __restrict__ codes, int* __restrict__ fed, float* __restrict__ dump, int dump_ld, int dump_off,
+    int* err) {
   extern __shared__ __align__(16) unsigned char smraw[];
   SamplerSmem& sm = *reinterpret_cast<SamplerSmem*>(smraw);
   const int b = blockIdx.x, s = sid[b];
+  const q3tts_sampling p = sp[b];
   const float* row = semantic ? logits + (size_t)s * V : logits + (size_t)b * V;
+  const int sf = semantic ? p.special_from : 0;
   for (int i = threadIdx.x; i < V; i += blockDim.x) {
     float v = row[i];
-    sm.val[i] = v;
     if (dump) dump[(size_t)b * dump_ld + dump_off + i] = v;
+    if (sf > 0 && i >= sf && i != p.eos_token) v = -INFINITY;
+    sm.val[i] = v;
   }
   __syncthreads();
-  const q3tts_sampling p = sp[b];
   const uint8_t* hist = semantic ? history + (size_t)s * V : nullptr;
   int code = semantic
                  ? block_sample(sm, V, p.do_sample, p.top_k, p.top_p, p.temperature,
@@ -90,14 +98,20 @@ __global__ void __launch_bounds__(256) sample_kernel(
                                 p.sub_temperature, 1.0f, nullptr, uniforms[b * 16 + cb]);
   code = min(max(code, 0), V - 1);
   if (threadIdx.x == 0) {
-    codes[b * 16 + cb] = code;
     int f = forced ? forced[b * 16 + cb] : code;
     if (f < 0 || f >= V) {
       atomicExch(err, Q3TTS_ERR_ARG);
       f = code;
     }
     fed[b * 16 + cb] = f;
-    if (semantic) history[(size_t)s * V + f] = 1;
+    if (semantic) {
+      const bool before = finished[s] != 0;
+      if (!before && p.eos_token >= 0 && f == p.eos_token) finished[s] = 1;
+      codes[b * 16 + cb] = before ? -1 : code;
+      history[(size_t)s * V + f] = 1;
+    } else {
+      codes[b * 16 + cb] = finished[s] ? -1 : code;
+    }
   }
 }
 
@@ -237,7 +251,7 @@ static void step_kernels(q3tts_handle* h, int n, int max_ctx, const float* unifo
   const size_t smem = sizeof(SamplerSmem);
   setup_kernel<<<1, 256, 0, s>>>(h->d_desc, h->d_sid, h->d_pos, h->d_sp, h->page_table, h->pps,
                                  h->c.page_size, h->d_tok_stream, h->d_tok_pos);
-  sample_kernel<<<n, 256, smem, s>>>(h->pending_logits, Vt, 1, h->d_sid, h->d_sp, h->history,
+  sample_kernel<<<n, 256, smem, s>>>(h->pending_logits, Vt, 1, h->d_sid, h->d_sp, h->history, h->finished,
                                      uniforms, 0, forced, codes, h->d_fed, logits, dump_ld, 0,
                                      h->d_err);
   const size_t es = wbytes(h);
@@ -265,7 +279,7 @@ static void step_kernels(q3tts_handle* h, int n, int max_ctx, const float* unifo
     norm_in(h, h->cpx, Dc, j == 0 ? 2 : 1, j == 0 ? 1 : 0, h->w.cp_g_final, n, Dc);
     const void* head = (const char*)h->w.cp_heads + (size_t)j * Vc * Dc * es;
     proj(h, h->hb, Dc, head, Vc, Dc, h->logits, Vc, n, false);
-    sample_kernel<<<n, 256, smem, s>>>(h->logits, Vc, 0, h->d_sid, h->d_sp, nullptr, uniforms,
+    sample_kernel<<<n, 256, smem, s>>>(h->logits, Vc, 0, h->d_sid, h->d_sp, nullptr, h->finished, uniforms,
                                        j + 1, forced, codes, h->d_fed, logits, dump_ld,
                                        Vt + j * Vc, h->d_err);
     h->launches += 4 + (h->w.cp_w_proj ? 1 : 0);

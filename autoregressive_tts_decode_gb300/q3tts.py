@@ -54,13 +54,13 @@ class Sampling(C.Structure):
     _fields_ = [("do_sample", C.c_int), ("top_k", C.c_int), ("top_p", C.c_float),
                 ("temperature", C.c_float), ("repetition_penalty", C.c_float),
                 ("sub_do_sample", C.c_int), ("sub_top_k", C.c_int), ("sub_top_p", C.c_float),
-                ("sub_temperature", C.c_float)]
+                ("sub_temperature", C.c_float), ("eos_token", C.c_int), ("special_from", C.c_int)]
 
 
 EXPORTS = ("q3tts_workspace_size", "q3tts_create", "q3tts_prefill", "q3tts_step_frame",
            "q3tts_read_pending", "q3tts_reset", "q3tts_stream_length", "q3tts_sync_status",
            "q3tts_kernel_launches", "q3tts_destroy", "q3tts_strerror",
-           "q3tts_step_frame_static", "q3tts_debug_fail_barrier")
+           "q3tts_step_frame_static", "q3tts_debug_fail_barrier", "q3tts_stream_finished")
 
 _lib = None
 
@@ -90,6 +90,7 @@ def load(path: str = LIB_PATH):
     L.q3tts_kernel_launches.restype = C.c_uint64
     L.q3tts_kernel_launches.argtypes = [vp]
     L.q3tts_debug_fail_barrier.argtypes = [vp, C.c_int, C.c_int]
+    L.q3tts_stream_finished.argtypes = [vp, C.c_int, C.POINTER(C.c_int)]
     L.q3tts_strerror.restype = C.c_char_p
     L.q3tts_strerror.argtypes = [C.c_int]
     _lib = L
@@ -120,7 +121,8 @@ def make_config(shape, max_streams: int, kv_cap: int, page_size: int = 16, kv_pa
 def sampling_struct(sp) -> Sampling:
     return Sampling(int(sp.do_sample), int(sp.top_k), float(sp.top_p), float(sp.temperature),
                     float(sp.repetition_penalty), int(sp.sub_do_sample), int(sp.sub_top_k),
-                    float(sp.sub_top_p), float(sp.sub_temperature))
+                    float(sp.sub_top_p), float(sp.sub_temperature),
+                    int(getattr(sp, "eos_token", -1)), int(getattr(sp, "special_from", 0)))
 
 
 def _ptr(t) -> Optional[int]:
@@ -250,6 +252,13 @@ class Engine:
         if rc < 0:
             raise Q3TTSError(rc, "q3tts_stream_length")
         return rc
+
+    def finished(self, stream_id: int) -> bool:
+        """Whether the stream fed its end-of-stream code since its last prefill
+        (waits for the engine's stream)."""
+        f = C.c_int(0)
+        _check(load().q3tts_stream_finished(self.h, stream_id, C.byref(f)), "q3tts_stream_finished")
+        return bool(f.value)
 
     def kernel_launches(self) -> int:
         return int(load().q3tts_kernel_launches(self.h))

@@ -132,9 +132,24 @@ typedef struct q3tts_sampling {
   float top_p, temperature, repetition_penalty;
   int sub_do_sample, sub_top_k;
   float sub_top_p, sub_temperature;
+  /* Stop conditions (the README lists end-of-stream handling as open parity
+   * work; this is the plainest reading).  eos_token >= 0: a frame whose fed
+   * semantic code equals it ends the stream -- its codes are [c0, -1 x 15] --
+   * and every later frame of the stream writes sixteen -1 (it is still
+   * computed; the stream's state is undefined until q3tts_prefill or
+   * q3tts_reset).  special_from > 0: semantic codes >= special_from other than
+   * eos_token are never drawn (the draw runs over the allowed codes; a
+   * disabled top-k keeps all of them).  eos_token < 0 and special_from <= 0:
+   * no stop condition, every code may be drawn. */
+  int eos_token, special_from;
 } q3tts_sampling;
 
 typedef struct q3tts_handle q3tts_handle;
+
+/* *finished receives 1 if `stream` has fed its end-of-stream code since its
+ * last prefill or reset, else 0.  Waits for the handle's stream (the flag is
+ * written on the device).  Q3TTS_ERR_ARG for a bad stream id. */
+int q3tts_stream_finished(q3tts_handle* h, int stream, int* finished);
 
 /* Bytes of workspace q3tts_create needs for cfg (0 if cfg is invalid). */
 size_t q3tts_workspace_size(const q3tts_config* cfg);

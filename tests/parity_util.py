@@ -69,11 +69,12 @@ def sampler_replay(oracle_mod, shape, sampling, codes, logits, fed, uniforms):
     Vt, Vc = shape.codec_vocab, shape.cp_vocab
     hist = np.zeros(Vt, dtype=np.uint8)
     bad = 0
+    sf, eos = getattr(sampling, "special_from", 0), getattr(sampling, "eos_token", -1)
     for f in range(codes.shape[0]):
         lg = logits[f]
         c0 = oracle_mod.sample(lg[:Vt], sampling.do_sample, sampling.top_k, sampling.top_p,
                                sampling.temperature, sampling.repetition_penalty, hist,
-                               float(uniforms[f, 0]))
+                               float(uniforms[f, 0]), special_from=sf, eos_token=eos)
         bad += int(c0 != codes[f, 0])
         hist[fed[f, 0]] = 1
         for j in range(15):
