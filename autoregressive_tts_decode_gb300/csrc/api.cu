@@ -272,7 +272,11 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
             cudaMemset(h->finished, 0, (size_t)d.S) == cudaSuccess &&
             cudaMemset(h->d_err, 0, sizeof(int) * 64) == cudaSuccess &&
             cudaMemset(h->spl_cnt, 0, sizeof(int) * (size_t)d.m_max * d.Hkv) == cudaSuccess;
+  for (cudaEvent_t& e : h->chunk_ev)
+    ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
   if (!ok || q3::sampler_setup() != Q3TTS_OK) {
+    for (cudaEvent_t& e : h->chunk_ev)
+      if (e) cudaEventDestroy(e);
     delete h;
     return Q3TTS_ERR_CUDA;
   }
@@ -282,11 +286,13 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
   for (int p = d.n_pages - 1; p >= 0; --p) h->free_pages.push_back(p);
   rc = q3::frame_kernel_create(h);
   if (rc != Q3TTS_OK) {
+    for (cudaEvent_t& e : h->chunk_ev) cudaEventDestroy(e);
     delete h;
     return rc;
   }
   if (cudaDeviceSynchronize() != cudaSuccess) {
     q3::frame_kernel_destroy(h);
+    for (cudaEvent_t& e : h->chunk_ev) cudaEventDestroy(e);
     delete h;
     return Q3TTS_ERR_CUDA;
   }
@@ -365,6 +371,42 @@ int q3tts_step_frame(q3tts_handle* h, const q3tts_sampling* params, const int32_
   }
   h->free_pages.resize(h->free_pages.size() - taken);
   return Q3TTS_OK;
+}
+
+int q3tts_step_frames(q3tts_handle* h, const q3tts_sampling* params, const int32_t* stream_ids,
+                      int n_active, int n_frames, const float* uniforms_dev, int32_t* codes_dev,
+                      int32_t* codes_host, const int32_t* forced_dev) {
+  if (!h || !params || !stream_ids || !uniforms_dev || !codes_dev) return Q3TTS_ERR_ARG;
+  if (n_frames < 1 || n_frames > Q3TTS_MAX_CHUNK || n_active < 1 || n_active > h->c.max_streams)
+    return Q3TTS_ERR_ARG;
+  h->chunk_n = 0;
+  const size_t per = (size_t)n_active * Q3TTS_N_CODEBOOKS;
+  for (int f = 0; f < n_frames; ++f) {
+    const int rc = q3tts_step_frame(h, params, stream_ids, n_active, uniforms_dev + f * per, codes_dev + f * per,
+                                    forced_dev ? forced_dev + f * per : nullptr, nullptr);
+    if (rc != Q3TTS_OK) return rc;
+    if (codes_host && cudaMemcpyAsync(codes_host + f * per, codes_dev + f * per, per * sizeof(int32_t),
+                                      cudaMemcpyDeviceToHost, h->s) != cudaSuccess)
+      return Q3TTS_ERR_CUDA;
+    if (cudaEventRecord(h->chunk_ev[f], h->s) != cudaSuccess) return Q3TTS_ERR_CUDA;
+    h->chunk_n = f + 1;
+  }
+  return Q3TTS_OK;
+}
+
+int q3tts_frames_ready(q3tts_handle* h) {
+  if (!h) return Q3TTS_ERR_ARG;
+  int n = 0;
+  while (n < h->chunk_n) {
+    const cudaError_t e = cudaEventQuery(h->chunk_ev[n]);
+    if (e == cudaErrorNotReady) {
+      cudaGetLastError();
+      break;
+    }
+    if (e != cudaSuccess) return Q3TTS_ERR_CUDA;
+    ++n;
+  }
+  return n;
 }
 
 // Batch-1 frame with the persistent kernel's per-frame scratch in a static
@@ -469,6 +511,8 @@ int q3tts_debug_fail_barrier(q3tts_handle* h, int barrier, int wait_us) {
 
 void q3tts_destroy(q3tts_handle* h) {
   if (!h) return;
+  for (cudaEvent_t& e : h->chunk_ev)
+    if (e) cudaEventDestroy(e);
   q3::frame_kernel_destroy(h);
   q3::step_graph_destroy(h);
   delete h;

@@ -85,6 +85,10 @@ struct q3tts_handle {
   long long dbg_wait_cycles = 0;
   bool static_ready = false;  // per-stream page lists reserved for it
   uint64_t launches = 0;
+  // streaming chunks (q3tts_step_frames): one event per frame, recorded after
+  // the frame's codes are copied out
+  cudaEvent_t chunk_ev[Q3TTS_MAX_CHUNK] = {};
+  int chunk_n = 0;
   // the captured layered step (valid for g_n active streams, with or without
   // forced codes); g_launches kernels per replay
   cudaGraphExec_t gexec = nullptr;

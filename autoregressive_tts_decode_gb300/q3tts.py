@@ -60,7 +60,9 @@ class Sampling(C.Structure):
 EXPORTS = ("q3tts_workspace_size", "q3tts_create", "q3tts_prefill", "q3tts_step_frame",
            "q3tts_read_pending", "q3tts_reset", "q3tts_stream_length", "q3tts_sync_status",
            "q3tts_kernel_launches", "q3tts_destroy", "q3tts_strerror",
-           "q3tts_step_frame_static", "q3tts_debug_fail_barrier", "q3tts_stream_finished")
+           "q3tts_step_frame_static", "q3tts_debug_fail_barrier", "q3tts_stream_finished",
+           "q3tts_step_frames", "q3tts_frames_ready")
+MAX_CHUNK = 64
 
 _lib = None
 
@@ -91,6 +93,9 @@ def load(path: str = LIB_PATH):
     L.q3tts_kernel_launches.argtypes = [vp]
     L.q3tts_debug_fail_barrier.argtypes = [vp, C.c_int, C.c_int]
     L.q3tts_stream_finished.argtypes = [vp, C.c_int, C.POINTER(C.c_int)]
+    L.q3tts_step_frames.argtypes = [vp, C.POINTER(Sampling), C.POINTER(C.c_int32), C.c_int, C.c_int, vp, vp,
+                                    vp, vp]
+    L.q3tts_frames_ready.argtypes = [vp]
     L.q3tts_strerror.restype = C.c_char_p
     L.q3tts_strerror.argtypes = [C.c_int]
     _lib = L
@@ -225,6 +230,73 @@ class Engine:
                                               uniforms.data_ptr(), codes.data_ptr(),
                                               _ptr(forced), _ptr(logits)),
                "q3tts_step_frame_static")
+
+    def step_frames(self, stream_ids: Sequence[int], sampling, uniforms, codes, codes_host=None,
+                    forced=None) -> None:
+        """q3tts_step_frames: F = uniforms.shape[0] frames (<= MAX_CHUNK) enqueued back
+        to back.  uniforms: CUDA fp32 [F, n, 16]; codes: CUDA int32 [F, n, 16]
+        (written); codes_host: None or a pinned CPU int32 [F, n, 16] tensor (written
+        asynchronously, frame by frame); forced: None or CUDA int32 [F, n, 16]."""
+        import torch
+        n = len(stream_ids)
+        F = int(uniforms.shape[0])
+        what = "q3tts_step_frames"
+        _need(uniforms, "uniforms", torch.float32, F * n * N_CODEBOOKS, what)
+        _need(codes, "codes", torch.int32, F * n * N_CODEBOOKS, what)
+        if forced is not None:
+            _need(forced, "forced", torch.int32, F * n * N_CODEBOOKS, what)
+        hp = None
+        if codes_host is not None:
+            ok = (isinstance(codes_host, torch.Tensor) and not codes_host.is_cuda and codes_host.is_contiguous()
+                  and codes_host.dtype == torch.int32 and codes_host.numel() >= F * n * N_CODEBOOKS)
+            if not ok:
+                raise Q3TTSError(ERR_ARG, f"{what}: codes_host must be a contiguous CPU int32 tensor")
+            hp = codes_host.data_ptr()
+        if not isinstance(sampling, (list, tuple)):
+            sampling = [sampling] * n
+        sp = (Sampling * n)(*[sampling_struct(x) for x in sampling])
+        ids = (C.c_int32 * n)(*[int(i) for i in stream_ids])
+        _check(load().q3tts_step_frames(self.h, sp, ids, n, F, uniforms.data_ptr(), codes.data_ptr(), hp,
+                                        _ptr(forced)), what)
+
+    def frames_ready(self) -> int:
+        """Frames of the latest step_frames chunk whose codes have landed (non-blocking)."""
+        r = load().q3tts_frames_ready(self.h)
+        if r < 0:
+            _check(r, "q3tts_frames_ready")
+        return r
+
+    def stream_codes(self, stream_ids: Sequence[int], sampling, uniforms, chunk: int):
+        """Frame-incremental decode of the given streams, chunk frames at a time
+        (the counterpart of a streaming session's next_audio_chunk): yields numpy
+        int32 arrays [frames, n, 16] of codes in order.  uniforms: CUDA fp32
+        [total_frames, n, 16].  Double-buffered: chunk k + 1 is enqueued before
+        the host waits for chunk k, so the GPU never idles on the host."""
+        import numpy as np
+        import torch
+        n = len(stream_ids)
+        total = int(uniforms.shape[0])
+        chunk = max(1, min(int(chunk), MAX_CHUNK))
+        dev = [torch.zeros((chunk, n, N_CODEBOOKS), dtype=torch.int32, device="cuda") for _ in range(2)]
+        host = [torch.zeros((chunk, n, N_CODEBOOKS), dtype=torch.int32).pin_memory() for _ in range(2)]
+        done = [torch.cuda.Event(), torch.cuda.Event()]
+        spans = [(f0, min(total, f0 + chunk)) for f0 in range(0, total, chunk)]
+
+        def submit(k):
+            f0, f1 = spans[k]
+            b = k & 1
+            self.step_frames(stream_ids, sampling, uniforms[f0:f1].contiguous(), dev[b][:f1 - f0],
+                             codes_host=host[b][:f1 - f0])
+            done[b].record(self.stream)
+
+        if spans:
+            submit(0)
+        for k in range(len(spans)):
+            if k + 1 < len(spans):
+                submit(k + 1)
+            done[k & 1].synchronize()
+            f0, f1 = spans[k]
+            yield np.array(host[k & 1][:f1 - f0].numpy(), copy=True)
 
     def _check_frame_buffers(self, n, uniforms, codes, forced, logits, what):
         import torch

@@ -265,6 +265,31 @@ def prefill_and_ttfa(eng, stream, prompt, sampling, u_dev, codes, reps=5):
                     "excluded from frames/s"}
 
 
+def streaming_chunks(eng, stream, prompt, sampling, uni_dev, frames=64, chunks=(1, 8, 32)):
+    """Frame-incremental decode through q3tts_step_frames (double-buffered, codes to
+    pinned host memory): per chunk size, the host time from a finished prefill
+    to the first chunk's codes on the host, and frames/s over `frames` frames."""
+    import torch
+    out = {}
+    u = uni_dev[:frames].unsqueeze(1).contiguous()  # [frames, 1, 16]
+    for ch in chunks:
+        eng.prefill(stream, prompt)
+        eng.sync()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        first = None
+        n = 0
+        for c in eng.stream_codes([stream], sampling, u, ch):
+            if first is None:
+                first = time.perf_counter() - t0
+            n += c.shape[0]
+        dt = time.perf_counter() - t0
+        out[str(ch)] = {"first_chunk_ms": 1e3 * first, "frames_per_s": n / dt}
+    return {"frames": frames, "chunks": out,
+            "note": "host-timed: prefill done -> codes in pinned host memory; chunk k+1 is "
+                    "enqueued before the host waits for chunk k"}
+
+
 def run_reference(args):
     """The reference arm: the CPU oracle on this workload, bounded per step."""
     rank, world, _ = dist_env()
@@ -437,6 +462,8 @@ def main():
 
     ttfa = prefill_and_ttfa(eng, 0, prompts[0], wl.sampling, uni_d[0:1, 0].contiguous(),
                             codes) if rank == 0 and not args.no_ttfa else None
+    streaming = (streaming_chunks(eng, 0, prompts[0], wl.sampling, uni_d[0])
+                 if rank == 0 and not args.no_ttfa and wl.kv_cap - lens[0] > 64 else None)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -473,6 +500,7 @@ def main():
                          "step_ms_median": statistics.median(step_ms),
                          "step_ms_p90": sorted(step_ms)[int(0.9 * (len(step_ms) - 1))]},
             "prefill": ttfa,
+            "streaming": streaming,
             "gpu_launches": launches,
             "clocks": clocks,
             "e2e": e2e,

@@ -51,6 +51,7 @@ extern "C" {
 
 #define Q3TTS_MAX_STREAMS 256
 #define Q3TTS_N_CODEBOOKS 16
+#define Q3TTS_MAX_CHUNK 64  /* frames one q3tts_step_frames call enqueues at most */
 
 /* Size of the library's static device scratch array (768 KiB), used only by
  * q3tts_step_frame_static. */
@@ -197,6 +198,35 @@ int q3tts_prefill(q3tts_handle* h, int stream_id, const float* embeds_dev, int l
 int q3tts_step_frame(q3tts_handle* h, const q3tts_sampling* params, const int32_t* stream_ids,
                      int n_active, const float* uniforms_dev, int32_t* codes_dev,
                      const int32_t* forced_dev, float* logits_dev);
+
+/* Frame-incremental streaming, the counterpart of the engine's streaming
+ * session ("qwen3-tts-hip" README, "Library Usage": start_stream, then
+ * next_audio_chunk until the stream ends): enqueues n_frames (1 ..
+ * Q3TTS_MAX_CHUNK) frames for the n_active streams back to back on the
+ * handle's stream, with no host synchronisation between them, and copies each
+ * frame's codes to host memory as soon as that frame is done.  The call
+ * returns once the frames are enqueued; q3tts_frames_ready tells how many of
+ * them have landed, so a caller double-buffers: enqueue chunk k + 1, then
+ * consume chunk k.  Larger chunks cost fewer host round trips; smaller ones
+ * deliver the first codes sooner.
+ *   uniforms_dev  device fp32 [n_frames][n_active][16]
+ *   codes_dev     device int32 [n_frames][n_active][16]
+ *   codes_host    NULL, or host int32 [n_frames][n_active][16] (pinned memory
+ *                 keeps the copies asynchronous); caller-owned, not read or
+ *                 written by the host side of the library after the call
+ *   forced_dev    NULL, or device int32 [n_frames][n_active][16] (teacher
+ *                 forcing, as in q3tts_step_frame)
+ * Frame f runs exactly as q3tts_step_frame would with the f-th slices.  A
+ * frame that cannot be enqueued (e.g. Q3TTS_ERR_CAPACITY) stops the call with
+ * that code; the frames before it stay enqueued and count as this chunk. */
+int q3tts_step_frames(q3tts_handle* h, const q3tts_sampling* params, const int32_t* stream_ids,
+                      int n_active, int n_frames, const float* uniforms_dev, int32_t* codes_dev,
+                      int32_t* codes_host, const int32_t* forced_dev);
+
+/* Frames of the latest q3tts_step_frames chunk whose codes have reached the
+ * host buffer (codes_dev when no host buffer was given), counted in order;
+ * does not block.  A negative value is an error code. */
+int q3tts_frames_ready(q3tts_handle* h);
 
 /* One frame of one stream, like q3tts_step_frame with n_active = 1, but with
  * the frame's scratch (residual vectors, QKV rows, attention partials,
