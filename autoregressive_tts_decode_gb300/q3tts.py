@@ -17,12 +17,13 @@ OK = 0
 ERR_ARG, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED, ERR_STATE = -1, -2, -3, -4, -5, -6
 ERR_SCRATCH = -7
 STATIC_SCRATCH_BYTES = 786432
-F32, BF16 = 0, 1
+F32, BF16, FP8 = 0, 1, 2
 MAX_STREAMS = 256
 N_CODEBOOKS = 16
 
 LAYER_KEYS = ("w_qkv", "w_o", "w_gateup", "w_down",
               "g_attn_norm", "g_ffn_norm", "g_q_norm", "g_k_norm")
+LAYER_SCALES = ("s_qkv", "s_o", "s_gateup", "s_down")  # FP8 matrices' per-row scales
 
 
 class Q3TTSError(RuntimeError):
@@ -40,14 +41,15 @@ class Config(C.Structure):
 
 
 class LayerWeights(C.Structure):
-    _fields_ = [(k, C.c_void_p) for k in LAYER_KEYS]
+    _fields_ = [(k, C.c_void_p) for k in LAYER_KEYS + LAYER_SCALES]
 
 
 class Weights(C.Structure):
     _fields_ = [("talker_layers", C.POINTER(LayerWeights)), ("talker_g_final", C.c_void_p),
                 ("talker_w_head", C.c_void_p), ("talker_e_codec", C.c_void_p),
                 ("cp_layers", C.POINTER(LayerWeights)), ("cp_g_final", C.c_void_p),
-                ("cp_heads", C.c_void_p), ("cp_embeds", C.c_void_p), ("cp_w_proj", C.c_void_p)]
+                ("cp_heads", C.c_void_p), ("cp_embeds", C.c_void_p), ("cp_w_proj", C.c_void_p),
+                ("s_head", C.c_void_p), ("s_cp_heads", C.c_void_p), ("s_cp_proj", C.c_void_p)]
 
 
 class Sampling(C.Structure):
@@ -161,19 +163,23 @@ class Engine:
         for k, t in weights.items():
             if not t.is_cuda or not t.is_contiguous():
                 raise ValueError(f"weight {k} must be a contiguous CUDA tensor")
+        def layer(prefix):
+            return LayerWeights(*[_ptr(weights.get(f"{prefix}.{k}")) for k in LAYER_KEYS + LAYER_SCALES])
+
         tl = (LayerWeights * shape.talker_layers)()
         for i in range(shape.talker_layers):
-            tl[i] = LayerWeights(*[weights[f"talker.{i}.{k}"].data_ptr() for k in LAYER_KEYS])
+            tl[i] = layer(f"talker.{i}")
         cl = (LayerWeights * shape.cp_layers)()
         for i in range(shape.cp_layers):
-            cl[i] = LayerWeights(*[weights[f"cp.{i}.{k}"].data_ptr() for k in LAYER_KEYS])
+            cl[i] = layer(f"cp.{i}")
         proj = weights.get("cp.w_proj")
         self._tl, self._cl = tl, cl
         self.wstruct = Weights(tl, weights["talker.g_final"].data_ptr(),
                                weights["talker.w_head"].data_ptr(),
                                weights["talker.e_codec"].data_ptr(), cl,
                                weights["cp.g_final"].data_ptr(), weights["cp.heads"].data_ptr(),
-                               weights["cp.embeds"].data_ptr(), _ptr(proj))
+                               weights["cp.embeds"].data_ptr(), _ptr(proj), _ptr(weights.get("talker.s_head")),
+                               _ptr(weights.get("cp.s_heads")), _ptr(weights.get("cp.s_proj")))
         n = L.q3tts_workspace_size(C.byref(self.cfg))
         if n == 0:
             raise Q3TTSError(ERR_ARG, "q3tts_workspace_size")

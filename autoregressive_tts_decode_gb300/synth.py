@@ -41,6 +41,8 @@ FRAMES_PER_SECOND = SAMPLE_RATE / SAMPLES_PER_FRAME  # 12.5: real time
 
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
+DTYPE_FP8 = 2  # matrices as FP8 E4M3 codes with per-row fp32 scales; gains, embeddings bf16
+FP8_MAX = 448.0  # largest finite E4M3 value
 
 
 @dataclass(frozen=True)
@@ -87,7 +89,7 @@ class ModelShape:
     head_dim: int
     codec_vocab: int      # V_t, Talker codec vocabulary
     cp_vocab: int         # V_c, CodePredictor vocabulary per codebook
-    weight_dtype: int     # DTYPE_F32 or DTYPE_BF16
+    weight_dtype: int     # DTYPE_F32, DTYPE_BF16 or DTYPE_FP8
     kv_dtype: int
     rms_eps: float = 1e-6
     rope_theta: float = 1e6
@@ -139,6 +141,7 @@ SHAPE_17B = ModelShape(talker_layers=28, talker_hidden=2048, talker_ffn=6144, cp
                        codec_vocab=3072, cp_vocab=2048, weight_dtype=DTYPE_BF16,
                        kv_dtype=DTYPE_F32)
 SHAPE_17B_KV16 = dataclasses.replace(SHAPE_17B, kv_dtype=DTYPE_BF16)
+SHAPE_17B_FP8 = dataclasses.replace(SHAPE_17B, weight_dtype=DTYPE_FP8)
 
 WORKLOADS: Dict[str, Workload] = {
     "tiny": Workload("tiny", TINY_SHAPE, streams=1, frames=8, kv_cap=64, page_size=16,
@@ -152,6 +155,10 @@ WORKLOADS: Dict[str, Workload] = {
                           prompt_len_range=(32, 256)),
     "serving128": Workload("serving128", SHAPE_17B_KV16, streams=128, frames=64, kv_cap=2112,
                            page_size=16, sampling=GREEDY, prompt_len_range=(256, 2048)),
+    # the 1.7B workload with 8-bit weight streaming (not one of the benchmark's
+    # headline configurations: its own tolerance contract, see the tests)
+    "1.7b-fp8": Workload("1.7b-fp8", SHAPE_17B_FP8, streams=1, frames=240, kv_cap=512, page_size=16,
+                         sampling=QWEN_DEFAULT_SAMPLING, prompt_len=128),
 }
 
 
@@ -173,6 +180,10 @@ def with_shape(w: Workload, **kw) -> Workload:
 # --------------------------------------------------------------------------
 LAYER_KEYS = ("w_qkv", "w_o", "w_gateup", "w_down",
               "g_attn_norm", "g_ffn_norm", "g_q_norm", "g_k_norm")
+# per-output-row scales of the FP8 matrices (FP8 weights only)
+LAYER_SCALE_KEYS = ("s_qkv", "s_o", "s_gateup", "s_down")
+SCALE_OF = {"w_qkv": "s_qkv", "w_o": "s_o", "w_gateup": "s_gateup", "w_down": "s_down",
+            "w_head": "s_head", "heads": "s_heads", "w_proj": "s_proj"}
 
 
 def layer_shapes(s: ModelShape, hidden: int, ffn: int):
@@ -213,9 +224,16 @@ def make_weights(s: ModelShape, seed: int = SEED_WEIGHTS, device="cpu", std: flo
     torch generator seeded once and walked in ``weight_specs`` order, then rounded
     to the storage dtype (bf16 round-to-nearest-even); norm gains are 1.0.
 
+    FP8 weights: the same fp32 draws; each matrix row r (the last dimension is
+    the row) gets the scale s_r = max|w_r| / 448 (fp32) and the codes
+    float8_e4m3fn(w / s_r) (torch's round-to-nearest-even), stored as uint8
+    bytes under the matrix's name, the scales under its scale name (SCALE_OF);
+    embedding tables and gains are bf16.
+
     The values depend on (seed, device type) only.
     """
     import torch
+    fp8 = s.weight_dtype == DTYPE_FP8
     dt = torch.float32 if s.weight_dtype == DTYPE_F32 else torch.bfloat16
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
@@ -223,9 +241,16 @@ def make_weights(s: ModelShape, seed: int = SEED_WEIGHTS, device="cpu", std: flo
     for name, shp, kind in weight_specs(s):
         if kind == "gain":
             out[name] = torch.ones(shp, dtype=dt, device=device)
+            continue
+        t = torch.empty(shp, dtype=torch.float32, device=device)
+        t.normal_(0.0, std, generator=gen)
+        short = name.rsplit(".", 1)[1]
+        if fp8 and short in SCALE_OF:
+            sc = (t.abs().amax(dim=-1) / FP8_MAX).to(torch.float32)
+            q = (t / sc.unsqueeze(-1)).to(torch.float8_e4m3fn)
+            out[name] = q.view(torch.uint8).contiguous()
+            out[name.rsplit(".", 1)[0] + "." + SCALE_OF[short]] = sc.contiguous()
         else:
-            t = torch.empty(shp, dtype=torch.float32, device=device)
-            t.normal_(0.0, std, generator=gen)
             out[name] = t.to(dt)
     return out
 

@@ -48,6 +48,13 @@ extern "C" {
 
 #define Q3TTS_F32 0
 #define Q3TTS_BF16 1
+/* Weight streaming in 8 bits: every matrix (w_qkv, w_o, w_gateup, w_down,
+ * talker_w_head, cp_heads, cp_w_proj) holds FP8 E4M3 codes (1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits, subnormals, no infinities; codes
+ * 0x7f and 0xff are NaN), one byte per element, with one fp32 scale per output
+ * row (the element is code value x scale); norm gains and embedding tables
+ * stay bf16.  Weight dtype only. */
+#define Q3TTS_FP8 2
 
 #define Q3TTS_MAX_STREAMS 256
 #define Q3TTS_N_CODEBOOKS 16
@@ -74,13 +81,17 @@ typedef struct q3tts_config {
   int cp_vocab;    /* V_c: vocabulary of each acoustic codebook */
   int n_codebooks; /* must be 16 */
   int max_streams, kv_cap_steps, page_size, kv_pages, prefill_chunk;
-  int weight_dtype; /* Q3TTS_F32 or Q3TTS_BF16: every weight tensor */
+  int weight_dtype; /* Q3TTS_F32 or Q3TTS_BF16: every weight tensor; Q3TTS_FP8: the
+                       matrices (gains and embeddings bf16) */
   int kv_dtype;     /* Talker KV cache: Q3TTS_F32 or Q3TTS_BF16 */
   int qk_norm;
   float rms_eps, rope_theta;
 } q3tts_config;
 
 /* One decoder layer; device pointers, row-major [out, in], weight_dtype.
+ * With Q3TTS_FP8 the s_* arrays hold each matrix's per-output-row scales
+ * (fp32, one per row: s_qkv [(Hq + 2 Hkv) hd], s_o [D], s_gateup [2 F],
+ * s_down [D]) and the gains are bf16; otherwise the s_* pointers are unused.
  * Every weight and gain pointer (here and in q3tts_weights) must be 16-byte
  * aligned: the kernels read them with 16-byte vector loads and bulk copies.
  * q3tts_create returns Q3TTS_ERR_ARG for a pointer that is not, before it
@@ -99,6 +110,10 @@ typedef struct q3tts_layer_weights {
   const void* g_ffn_norm;
   const void* g_q_norm;
   const void* g_k_norm;
+  const float* s_qkv;
+  const float* s_o;
+  const float* s_gateup;
+  const float* s_down;
 } q3tts_layer_weights;
 
 /* All weights.  talker_layers / cp_layers are HOST arrays of per-layer device
@@ -106,7 +121,9 @@ typedef struct q3tts_layer_weights {
  *   talker_g_final [D_t], talker_w_head [V_t, D_t], talker_e_codec [V_t, D_t]
  *   cp_g_final [D_c], cp_heads [15, V_c, D_c], cp_embeds [15, V_c, D_t]
  *   cp_w_proj [D_c, D_t]: the CodePredictor input projection, required when
- *   D_t != D_c and NULL otherwise. */
+ *   D_t != D_c and NULL otherwise.
+ * With Q3TTS_FP8: s_head [V_t], s_cp_heads [15 V_c], s_cp_proj [D_c] (NULL
+ * when cp_w_proj is) are the scales of the FP8 heads and projection. */
 typedef struct q3tts_weights {
   const q3tts_layer_weights* talker_layers;
   const void* talker_g_final;
@@ -117,6 +134,9 @@ typedef struct q3tts_weights {
   const void* cp_heads;
   const void* cp_embeds;
   const void* cp_w_proj;
+  const float* s_head;
+  const float* s_cp_heads;
+  const float* s_cp_proj;
 } q3tts_weights;
 
 /* Sampling controls of one stream ("qwen3-tts-hip" README, "Library Usage",

@@ -51,7 +51,12 @@ class _Weights(C.Structure):
     _fields_ = [("talker_layers", C.POINTER(C.c_void_p)), ("talker_g_final", C.c_void_p),
                 ("talker_w_head", C.c_void_p), ("talker_e_codec", C.c_void_p),
                 ("cp_layers", C.POINTER(C.c_void_p)), ("cp_g_final", C.c_void_p),
-                ("cp_heads", C.c_void_p), ("cp_embeds", C.c_void_p), ("cp_w_proj", C.c_void_p)]
+                ("cp_heads", C.c_void_p), ("cp_embeds", C.c_void_p), ("cp_w_proj", C.c_void_p),
+                ("s_head", C.c_void_p), ("s_cp_heads", C.c_void_p), ("s_cp_proj", C.c_void_p)]
+
+# per-layer pointers: the LAYER_KEYS tensors, then the FP8 matrices' scales
+LAYER_SCALES = ("s_qkv", "s_o", "s_gateup", "s_down")
+NPTR = len(LAYER_KEYS) + len(LAYER_SCALES)
 
 
 class _Sampling(C.Structure):
@@ -83,6 +88,8 @@ def lib():
                                  C.c_char_p, C.c_float, C.c_int, C.c_int]
         L.q3o_sample_f64.argtypes = [fp, C.c_int, C.c_int, C.c_int, C.c_double, C.c_double,
                                      C.c_double, C.c_char_p, C.c_double, dp, C.c_int, C.c_int]
+        L.q3o_fp8_value.restype = C.c_double
+        L.q3o_fp8_value.argtypes = [C.c_uint]
         L.q3o_expf.restype = C.c_float
         L.q3o_expf.argtypes = [C.c_float]
         L.q3o_rmsnorm.argtypes = [dp, C.c_int, fp, C.c_double, dp]
@@ -148,6 +155,11 @@ def sample_f64(logits, do_sample, top_k, top_p, temperature, rep_penalty=1.0, hi
     return int(pick), float(mg.value)
 
 
+def fp8_value(code: int) -> float:
+    """The value of an FP8 E4M3 code (the oracle's decoder)."""
+    return float(lib().q3o_fp8_value(int(code)))
+
+
 def expf(x: float) -> float:
     return float(lib().q3o_expf(float(x)))
 
@@ -199,19 +211,22 @@ class Oracle:
             t = self._keep.get(name)
             return None if t is None else C.c_void_p(t.data_ptr())
 
-        tl = (C.c_void_p * (shape.talker_layers * 8))()
-        for li in range(shape.talker_layers):
-            for j, k in enumerate(LAYER_KEYS):
-                tl[li * 8 + j] = self._keep[f"talker.{li}.{k}"].data_ptr()
-        cl = (C.c_void_p * (shape.cp_layers * 8))()
-        for li in range(shape.cp_layers):
-            for j, k in enumerate(LAYER_KEYS):
-                cl[li * 8 + j] = self._keep[f"cp.{li}.{k}"].data_ptr()
+        def layer_ptrs(prefix, n):
+            arr = (C.c_void_p * (n * NPTR))()
+            for li in range(n):
+                for j, k in enumerate(LAYER_KEYS + LAYER_SCALES):
+                    t = self._keep.get(f"{prefix}.{li}.{k}")
+                    arr[li * NPTR + j] = None if t is None else t.data_ptr()
+            return arr
+
+        tl = layer_ptrs("talker", shape.talker_layers)
+        cl = layer_ptrs("cp", shape.cp_layers)
         self._tl, self._cl = tl, cl
         self._w = _Weights(C.cast(tl, C.POINTER(C.c_void_p)), p("talker.g_final"),
                            p("talker.w_head"), p("talker.e_codec"),
                            C.cast(cl, C.POINTER(C.c_void_p)), p("cp.g_final"), p("cp.heads"),
-                           p("cp.embeds"), p("cp.w_proj"))
+                           p("cp.embeds"), p("cp.w_proj"), p("talker.s_head"), p("cp.s_heads"),
+                           p("cp.s_proj"))
         s = shape
         self._c = _Cfg(s.talker_layers, s.talker_hidden, s.talker_ffn, s.cp_layers, s.cp_hidden,
                        s.cp_ffn, s.n_q_heads, s.n_kv_heads, s.head_dim, s.codec_vocab, s.cp_vocab,

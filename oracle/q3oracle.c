@@ -58,8 +58,13 @@ typedef struct {
 } q3o_config;
 
 /* Per-layer pointer order: w_qkv, w_o, w_gateup, w_down,
- * g_attn_norm, g_ffn_norm, g_q_norm, g_k_norm. */
-enum { L_QKV = 0, L_O, L_GU, L_DOWN, L_GATTN, L_GFFN, L_GQ, L_GK, L_NPTR };
+ * g_attn_norm, g_ffn_norm, g_q_norm, g_k_norm, then the per-row scales of the
+ * four matrices (FP8 weights; NULL otherwise). */
+enum { L_QKV = 0, L_O, L_GU, L_DOWN, L_GATTN, L_GFFN, L_GQ, L_GK, L_SQKV, L_SO, L_SGU, L_SDOWN, L_NPTR };
+
+/* weight_dtype: 0 fp32, 1 bf16, 2 FP8 E4M3 matrices with per-row fp32 scales
+ * (gains and embedding tables then bf16). */
+#define Q3O_FP8 2
 
 typedef struct {
   const void* const* talker_layers; /* [talker_layers * L_NPTR] */
@@ -71,6 +76,9 @@ typedef struct {
   const void* cp_heads;             /* [15, V_c, D_c] */
   const void* cp_embeds;            /* [15, V_c, D_t] */
   const void* cp_w_proj;            /* [D_c, D_t] or NULL */
+  const float* s_head;              /* FP8: scales of talker_w_head [V_t] */
+  const float* s_cp_heads;          /* FP8: [15, V_c] */
+  const float* s_cp_proj;           /* FP8: [D_c] or NULL */
 } q3o_weights;
 
 typedef struct {
@@ -117,24 +125,50 @@ typedef struct {
 
 /* ---------------------------------------------------------------- helpers */
 
+/* The value of an FP8 E4M3 code: sign bit, 4 exponent bits (bias 7), 3
+ * mantissa bits; exponent field 0 is subnormal (m/8 * 2^-6); the all-ones code
+ * (exponent 15, mantissa 7) is NaN; there are no infinities, so the largest
+ * finite value is 1.75 * 2^8 = 448. */
+double q3o_fp8_value(unsigned code) {
+  const int sgn = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sgn ? -v : v;
+}
+
+/* Element i of a weight tensor of dtype dt (an FP8 code's value, unscaled). */
 static double wval(const void* w, int dt, size_t i) {
   if (dt == 0) return (double)((const float*)w)[i];
+  if (dt == Q3O_FP8) return q3o_fp8_value(((const uint8_t*)w)[i]);
   uint32_t bits = (uint32_t)((const uint16_t*)w)[i] << 16;
   float f;
   memcpy(&f, &bits, sizeof f);
   return (double)f;
 }
 
-/* y[t][r] = sum_k W[r][k] x[t][k]  (W row-major [rows, cols]); a plain matrix
- * product, each row widened once and then used for every token (the sums run
- * over k in order for each (t, r), whatever the number of tokens). */
-static void linear(const void* W, int dt, int rows, int cols, const double* x, int T, double* y) {
+/* dtype of the gains and embedding tables of a model whose matrices are dt */
+static int gain_dt(int dt) { return dt == Q3O_FP8 ? 1 : dt; }
+
+/* bytes of one matrix element */
+static size_t mat_esz(int dt) { return dt == 0 ? 4 : (dt == Q3O_FP8 ? 1 : 2); }
+
+/* y[t][r] = sum_k W[r][k] x[t][k]  (W row-major [rows, cols]; FP8 rows are
+ * their codes' values times the row's scale sc[r]); a plain matrix product,
+ * each row widened once and then used for every token (the sums run over k in
+ * order for each (t, r), whatever the number of tokens). */
+static void linear(const void* W, int dt, const float* sc, int rows, int cols, const double* x, int T,
+                   double* y) {
 #pragma omp parallel
   {
     double* w = (double*)malloc(sizeof(double) * (size_t)cols);
 #pragma omp for schedule(static)
     for (int r = 0; r < rows; ++r) {
-      for (int k = 0; k < cols; ++k) w[k] = wval(W, dt, (size_t)r * cols + k);
+      const double srow = dt == Q3O_FP8 ? (double)sc[r] : 1.0;
+      for (int k = 0; k < cols; ++k) w[k] = wval(W, dt, (size_t)r * cols + k) * srow;
       for (int t = 0; t < T; ++t) {
         double acc = 0.0;
         for (int k = 0; k < cols; ++k) acc += w[k] * x[(size_t)t * cols + k];
@@ -219,7 +253,7 @@ typedef struct {
 static void stack_forward(const q3o_model* m, const stack_desc* sd, double* x, int T, int pos0) {
   const q3o_config* c = &m->c;
   int D = sd->hidden, F = sd->ffn, Hq = c->n_q_heads, Hkv = c->n_kv_heads, hd = c->head_dim;
-  int dt = c->weight_dtype;
+  int dt = c->weight_dtype, gdt = gain_dt(dt);
   int qkv_rows = (Hq + 2 * Hkv) * hd;
   double* n = (double*)malloc(sizeof(double) * (size_t)T * D);
   double* qkv = (double*)malloc(sizeof(double) * (size_t)T * qkv_rows);
@@ -231,20 +265,20 @@ static void stack_forward(const q3o_model* m, const stack_desc* sd, double* x, i
     const void* const* w = sd->lw + (size_t)l * L_NPTR;
     double* Kc = sd->kv->k + l * layer_stride;
     double* Vc = sd->kv->v + l * layer_stride;
-    for (int t = 0; t < T; ++t) rmsnorm_w(x + (size_t)t * D, D, w[L_GATTN], dt, c->rms_eps, n + (size_t)t * D);
-    linear(w[L_QKV], dt, qkv_rows, D, n, T, qkv);
+    for (int t = 0; t < T; ++t) rmsnorm_w(x + (size_t)t * D, D, w[L_GATTN], gdt, c->rms_eps, n + (size_t)t * D);
+    linear(w[L_QKV], dt, (const float*)w[L_SQKV], qkv_rows, D, n, T, qkv);
     for (int t = 0; t < T; ++t) {
       double* row = qkv + (size_t)t * qkv_rows;
       int pos = pos0 + t;
       for (int h = 0; h < Hq; ++h) {
         double* qh = row + h * hd;
-        if (c->qk_norm) rmsnorm_w(qh, hd, w[L_GQ], dt, c->rms_eps, qh);
+        if (c->qk_norm) rmsnorm_w(qh, hd, w[L_GQ], gdt, c->rms_eps, qh);
         rope(qh, hd, pos, c->rope_theta);
       }
       for (int g = 0; g < Hkv; ++g) {
         double* kg = row + (Hq + g) * hd;
         double* vg = row + (Hq + Hkv + g) * hd;
-        if (c->qk_norm) rmsnorm_w(kg, hd, w[L_GK], dt, c->rms_eps, kg);
+        if (c->qk_norm) rmsnorm_w(kg, hd, w[L_GK], gdt, c->rms_eps, kg);
         rope(kg, hd, pos, c->rope_theta);
         double* kc = Kc + ((size_t)pos * Hkv + g) * hd;
         double* vc = Vc + ((size_t)pos * Hkv + g) * hd;
@@ -259,14 +293,14 @@ static void stack_forward(const q3o_model* m, const stack_desc* sd, double* x, i
 #pragma omp parallel for schedule(dynamic, 4)
     for (int t = 0; t < T; ++t)
       attention(qkv + (size_t)t * qkv_rows, Kc, Vc, pos0 + t + 1, Hq, Hkv, hd, o + (size_t)t * Hq * hd);
-    linear(w[L_O], dt, D, Hq * hd, o, T, y);
+    linear(w[L_O], dt, (const float*)w[L_SO], D, Hq * hd, o, T, y);
     for (size_t i = 0; i < (size_t)T * D; ++i) x[i] += y[i];
-    for (int t = 0; t < T; ++t) rmsnorm_w(x + (size_t)t * D, D, w[L_GFFN], dt, c->rms_eps, n + (size_t)t * D);
-    linear(w[L_GU], dt, 2 * F, D, n, T, y);
+    for (int t = 0; t < T; ++t) rmsnorm_w(x + (size_t)t * D, D, w[L_GFFN], gdt, c->rms_eps, n + (size_t)t * D);
+    linear(w[L_GU], dt, (const float*)w[L_SGU], 2 * F, D, n, T, y);
     for (int t = 0; t < T; ++t)
       for (int f = 0; f < F; ++f)
         a[(size_t)t * F + f] = silu(y[(size_t)t * 2 * F + f]) * y[(size_t)t * 2 * F + F + f];
-    linear(w[L_DOWN], dt, D, F, a, T, y);
+    linear(w[L_DOWN], dt, (const float*)w[L_SDOWN], D, F, a, T, y);
     for (size_t i = 0; i < (size_t)T * D; ++i) x[i] += y[i];
   }
   free(n); free(qkv); free(o); free(y); free(a);
@@ -463,8 +497,8 @@ static void cp_stack(q3o_model* m, stack_desc* sd) {
  * state from which the next frame's semantic token is drawn. */
 static void talker_pending(q3o_model* m, stream_state* st, const double* x_last) {
   const q3o_config* c = &m->c;
-  rmsnorm_w(x_last, c->talker_hidden, m->w.talker_g_final, c->weight_dtype, c->rms_eps, st->pending_h);
-  linear(m->w.talker_w_head, c->weight_dtype, c->codec_vocab, c->talker_hidden, st->pending_h, 1,
+  rmsnorm_w(x_last, c->talker_hidden, m->w.talker_g_final, gain_dt(c->weight_dtype), c->rms_eps, st->pending_h);
+  linear(m->w.talker_w_head, c->weight_dtype, m->w.s_head, c->codec_vocab, c->talker_hidden, st->pending_h, 1,
          st->pending_logits);
 }
 
@@ -555,22 +589,23 @@ static void cp_pass(q3o_model* m, const double* u, int T, int pos0, int head, do
   int Dt = c->talker_hidden, Dc = c->cp_hidden, dt = c->weight_dtype;
   double* z = (double*)malloc(sizeof(double) * (size_t)T * Dc);
   if (c->talker_hidden != c->cp_hidden)
-    linear(m->w.cp_w_proj, dt, Dc, Dt, u, T, z);
+    linear(m->w.cp_w_proj, dt, m->w.s_cp_proj, Dc, Dt, u, T, z);
   else
     memcpy(z, u, sizeof(double) * (size_t)T * Dc);
   stack_desc sd;
   cp_stack(m, &sd);
   stack_forward(m, &sd, z, T, pos0);
   double* hn = (double*)malloc(sizeof(double) * (size_t)Dc);
-  rmsnorm_w(z + (size_t)(T - 1) * Dc, Dc, m->w.cp_g_final, dt, c->rms_eps, hn);
-  const void* W = (const char*)m->w.cp_heads + (size_t)head * c->cp_vocab * Dc * (dt == 0 ? 4 : 2);
-  linear(W, dt, c->cp_vocab, Dc, hn, 1, logits);
+  rmsnorm_w(z + (size_t)(T - 1) * Dc, Dc, m->w.cp_g_final, gain_dt(dt), c->rms_eps, hn);
+  const void* W = (const char*)m->w.cp_heads + (size_t)head * c->cp_vocab * Dc * mat_esz(dt);
+  linear(W, dt, m->w.s_cp_heads ? m->w.s_cp_heads + (size_t)head * c->cp_vocab : NULL, c->cp_vocab, Dc, hn, 1,
+         logits);
   free(hn); free(z);
 }
 
 static void embed_row(const q3o_model* m, const void* table, size_t row, double* out) {
   int Dt = m->c.talker_hidden;
-  for (int i = 0; i < Dt; ++i) out[i] = wval(table, m->c.weight_dtype, row * Dt + i);
+  for (int i = 0; i < Dt; ++i) out[i] = wval(table, gain_dt(m->c.weight_dtype), row * Dt + i);
 }
 
 /* One acoustic frame of one stream ([R9700] "Running Qwen3-TTS"):
@@ -589,8 +624,8 @@ int q3o_step_frame(void* h, int stream, const q3o_sampling* sp, const float* u, 
   const q3o_config* c = &m->c;
   stream_state* st = &m->st[stream];
   if (st->len >= c->kv_cap) return -1;
-  int Dt = c->talker_hidden, Vt = c->codec_vocab, Vc = c->cp_vocab, dt = c->weight_dtype;
-  size_t esz = dt == 0 ? 4 : 2;
+  int Dt = c->talker_hidden, Vt = c->codec_vocab, Vc = c->cp_vocab, dt = gain_dt(c->weight_dtype);
+  size_t esz = dt == 0 ? 4 : 2; /* embedding tables */
   int fed[Q3O_NCB];
   float* lf = (float*)malloc(sizeof(float) * (size_t)(Vt > Vc ? Vt : Vc));
   double* ld = (double*)malloc(sizeof(double) * (size_t)Vc);
@@ -686,7 +721,7 @@ void q3o_cp_full(void* h, const double* tokens, float* logits) {
   int dt = c->weight_dtype;
   double* z = (double*)malloc(sizeof(double) * (size_t)T * Dc);
   if (Dt != Dc)
-    linear(m->w.cp_w_proj, dt, Dc, Dt, tokens, T, z);
+    linear(m->w.cp_w_proj, dt, m->w.s_cp_proj, Dc, Dt, tokens, T, z);
   else
     memcpy(z, tokens, sizeof(double) * (size_t)T * Dc);
   stack_desc sd;
@@ -695,9 +730,9 @@ void q3o_cp_full(void* h, const double* tokens, float* logits) {
   double* hn = (double*)malloc(sizeof(double) * (size_t)Dc);
   double* ld = (double*)malloc(sizeof(double) * (size_t)Vc);
   for (int j = 0; j < T - 1; ++j) {
-    rmsnorm_w(z + (size_t)(j + 1) * Dc, Dc, m->w.cp_g_final, dt, c->rms_eps, hn);
-    const void* W = (const char*)m->w.cp_heads + (size_t)j * Vc * Dc * (dt == 0 ? 4 : 2);
-    linear(W, dt, Vc, Dc, hn, 1, ld);
+    rmsnorm_w(z + (size_t)(j + 1) * Dc, Dc, m->w.cp_g_final, gain_dt(dt), c->rms_eps, hn);
+    const void* W = (const char*)m->w.cp_heads + (size_t)j * Vc * Dc * mat_esz(dt);
+    linear(W, dt, m->w.s_cp_heads ? m->w.s_cp_heads + (size_t)j * Vc : NULL, Vc, Dc, hn, 1, ld);
     for (int i = 0; i < Vc; ++i) logits[(size_t)j * Vc + i] = (float)ld[i];
   }
   free(ld); free(hn); free(z);

@@ -89,6 +89,19 @@ def _tiny_weights(dtype=synth.DTYPE_F32, **zero):
     return W
 
 
+def mat(W, name, j=None):
+    """A weight matrix as torch float64 through torch's own conversions: FP8
+    codes (uint8 storage) through float8_e4m3fn -> float64 times the row scales
+    (synth.SCALE_OF); bf16 / fp32 directly.  j picks one head of a stacked
+    tensor."""
+    t = W[name] if j is None else W[name][j]
+    if t.dtype == torch.uint8:
+        sname = name.rsplit(".", 1)[0] + "." + synth.SCALE_OF[name.rsplit(".", 1)[1]]
+        sc = W[sname] if j is None else W[sname][j]
+        return t.view(torch.float8_e4m3fn).to(torch.float64) * sc.to(torch.float64).unsqueeze(-1)
+    return t.to(torch.float64)
+
+
 def _rms(x, g, eps=1e-6):
     return F.rms_norm(torch.tensor(x, dtype=torch.float64), (x.shape[-1],),
                       torch.tensor(g, dtype=torch.float64), eps=eps).numpy()
@@ -108,7 +121,7 @@ def test_identity_stack_gives_head_of_normed_input(oracle_mod):
     assert np.allclose(lg, f64(W["talker.w_head"]) @ hn, rtol=1e-9, atol=1e-12)
 
 
-@pytest.mark.parametrize("dtype", [synth.DTYPE_F32, synth.DTYPE_BF16])
+@pytest.mark.parametrize("dtype", [synth.DTYPE_F32, synth.DTYPE_BF16, synth.DTYPE_FP8])
 def test_single_position_attention_block(oracle_mod, dtype):
     """Prompt of length 1 and W_down = 0: attention over one position returns v,
     so x = e + W_o v with v = W_v RMSNorm(e) (the v rows of W_qkv).  With bf16
@@ -120,14 +133,14 @@ def test_single_position_attention_block(oracle_mod, dtype):
     e = synth.make_prompts(s, [1])[0].numpy().astype(np.float64)
     x = o.talker_stack(0, e, 0)[0]
     n = _rms(e[0], f64(W["talker.0.g_attn_norm"]))
-    vrows = f64(W["talker.0.w_qkv"])[(s.n_q_heads + s.n_kv_heads) * s.head_dim:]
+    vrows = mat(W, "talker.0.w_qkv").numpy()[(s.n_q_heads + s.n_kv_heads) * s.head_dim:]
     v = (vrows @ n).reshape(s.n_kv_heads, s.head_dim)
     o_heads = np.repeat(v, s.n_q_heads // s.n_kv_heads, axis=0).reshape(-1)
-    want = e[0] + f64(W["talker.0.w_o"]) @ o_heads
+    want = e[0] + mat(W, "talker.0.w_o").numpy() @ o_heads
     assert np.allclose(x, want, rtol=1e-9, atol=1e-12)
 
 
-@pytest.mark.parametrize("dtype", [synth.DTYPE_F32, synth.DTYPE_BF16])
+@pytest.mark.parametrize("dtype", [synth.DTYPE_F32, synth.DTYPE_BF16, synth.DTYPE_FP8])
 def test_ffn_block_is_swiglu(oracle_mod, dtype):
     """W_o = 0 leaves the FFN: x = e + W_down(silu(W_gate n) * W_up n), n = RMSNorm(e)."""
     s = dataclasses.replace(TINY.shape, talker_layers=1, weight_dtype=dtype)
@@ -137,9 +150,9 @@ def test_ffn_block_is_swiglu(oracle_mod, dtype):
     e = synth.make_prompts(s, [3])[0].to(torch.float64)
     x = o.talker_stack(0, e.numpy(), 0)
     n = F.rms_norm(e, (s.talker_hidden,), W["talker.0.g_ffn_norm"].double(), eps=1e-6)
-    gu = F.linear(n, W["talker.0.w_gateup"].double())
+    gu = F.linear(n, mat(W, "talker.0.w_gateup"))
     a = F.silu(gu[:, :s.talker_ffn]) * gu[:, s.talker_ffn:]
-    want = e + F.linear(a, W["talker.0.w_down"].double())
+    want = e + F.linear(a, mat(W, "talker.0.w_down"))
     assert np.allclose(x, want.numpy(), rtol=1e-9, atol=1e-12)
 
 
@@ -150,7 +163,7 @@ def _embed_sum(W, codes):
     return x
 
 
-@pytest.mark.parametrize("dtype", [synth.DTYPE_F32, synth.DTYPE_BF16])
+@pytest.mark.parametrize("dtype", [synth.DTYPE_F32, synth.DTYPE_BF16, synth.DTYPE_FP8])
 @pytest.mark.parametrize("proj", [False, True])
 def test_frame_wiring_with_identity_stacks(oracle_mod, proj, dtype):
     """Both stacks reduced to the identity (W_o = W_down = 0): each CodePredictor
@@ -179,14 +192,14 @@ def test_frame_wiring_with_identity_stacks(oracle_mod, proj, dtype):
     for j in range(15):
         u_j = (f64(W["talker.e_codec"])[codes[0]] if j == 0
                else f64(W["cp.embeds"][j - 1])[codes[j]])
-        z = f64(W["cp.w_proj"]) @ u_j if proj else u_j
-        want = f64(W["cp.heads"][j]) @ _rms(z, f64(W["cp.g_final"]))
+        z = mat(W, "cp.w_proj").numpy() @ u_j if proj else u_j
+        want = mat(W, "cp.heads", j).numpy() @ _rms(z, f64(W["cp.g_final"]))
         got = lg[Vt + j * Vc: Vt + (j + 1) * Vc]
         assert np.allclose(got, want, rtol=1e-5, atol=1e-6), j
         assert codes[j + 1] == int(np.argmax(got))
     _, l1 = o.pending(0)
     x = _embed_sum(W, codes)
-    want = f64(W["talker.w_head"]) @ _rms(x, f64(W["talker.g_final"]))
+    want = mat(W, "talker.w_head").numpy() @ _rms(x, f64(W["talker.g_final"]))
     assert np.allclose(l1, want, rtol=1e-9, atol=1e-12)
 
 
@@ -375,3 +388,16 @@ def test_repetition_penalty_history_is_the_fed_semantic_code(oracle_mod):
     o.prefill(0, tie_prompt)                    # stream 0 restarts: history cleared
     c, _ = o.step_frame(0, pen, u[0])
     assert c[0] == A
+
+
+def test_fp8_decoder_all_codes(oracle_mod):
+    """The oracle's E4M3 decoder on all 256 codes equals torch's float8_e4m3fn
+    conversion (NaN exactly at 0x7f and 0xff; 448 the largest value)."""
+    codes = torch.arange(256, dtype=torch.uint8)
+    want = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle_mod.fp8_value(c) for c in range(256)])
+    nan = np.isnan(want)
+    assert list(np.nonzero(nan)[0]) == [0x7f, 0xff]
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert got[0x7e] == 448.0 and got[0x01] == 2.0 ** -9
