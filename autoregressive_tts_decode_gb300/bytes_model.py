@@ -15,11 +15,27 @@ from __future__ import annotations
 
 from dataclasses import dataclass
 
-from .synth import DTYPE_F32, ModelShape, N_CODEBOOKS
+from .synth import DTYPE_F32, DTYPE_FP8, ModelShape, N_CODEBOOKS
 
 
 def esize(dtype: int) -> int:
+    """Bytes of a gain or embedding element (bf16 beside FP8 matrices)."""
     return 4 if dtype == DTYPE_F32 else 2
+
+
+def mat_bytes(s: ModelShape, rows: int, cols: int) -> int:
+    """A [rows, cols] weight matrix: FP8 codes plus one fp32 scale per row, else
+    rows * cols elements of the weight dtype."""
+    if s.weight_dtype == DTYPE_FP8:
+        return rows * cols + 4 * rows
+    return rows * cols * esize(s.weight_dtype)
+
+
+def layer_bytes(s: ModelShape, hidden: int, ffn: int) -> int:
+    """One decoder layer: QKV, o_proj, gate/up, down, and its four gains."""
+    return (mat_bytes(s, s.qkv_rows, hidden) + mat_bytes(s, hidden, s.n_q_heads * s.head_dim)
+            + mat_bytes(s, 2 * ffn, hidden) + mat_bytes(s, hidden, ffn)
+            + (2 * hidden + 2 * s.head_dim) * esize(s.weight_dtype))
 
 
 def layer_weight_elems(s: ModelShape, hidden: int, ffn: int) -> int:
@@ -45,12 +61,12 @@ def frame_bytes(s: ModelShape, talker_pos: int) -> FrameBytes:
     """Bytes for one frame of one stream whose Talker step writes position talker_pos."""
     e = esize(s.weight_dtype)
     kv_e = esize(s.kv_dtype)
-    tw = (s.talker_layers * layer_weight_elems(s, s.talker_hidden, s.talker_ffn)
-          + s.talker_hidden + s.codec_vocab * s.talker_hidden) * e
-    cw = (s.cp_layers * layer_weight_elems(s, s.cp_hidden, s.cp_ffn) + s.cp_hidden
-          + s.cp_vocab * s.cp_hidden) * e
+    tw = (s.talker_layers * layer_bytes(s, s.talker_hidden, s.talker_ffn) + s.talker_hidden * e
+          + mat_bytes(s, s.codec_vocab, s.talker_hidden))
+    cw = (s.cp_layers * layer_bytes(s, s.cp_hidden, s.cp_ffn) + s.cp_hidden * e
+          + mat_bytes(s, s.cp_vocab, s.cp_hidden))
     if s.has_proj:
-        cw += s.cp_hidden * s.talker_hidden * e
+        cw += mat_bytes(s, s.cp_hidden, s.talker_hidden)
     # next Talker input: 16 rows; CodePredictor inputs: E_t[c0] in pass 0 and
     # E_cp[j-1][c_j] in passes 1..14.
     emb = (N_CODEBOOKS + (N_CODEBOOKS - 1)) * s.talker_hidden * e

@@ -57,7 +57,8 @@ int check_config(const q3tts_config* c) {
       !pos_int(c->kv_cap_steps) || !pos_int(c->page_size))
     return Q3TTS_ERR_ARG;
   if (c->n_codebooks != Q3TTS_N_CODEBOOKS) return Q3TTS_ERR_UNSUPPORTED;
-  if (c->weight_dtype != Q3TTS_F32 && c->weight_dtype != Q3TTS_BF16) return Q3TTS_ERR_ARG;
+  if (c->weight_dtype != Q3TTS_F32 && c->weight_dtype != Q3TTS_BF16 && c->weight_dtype != Q3TTS_FP8)
+    return Q3TTS_ERR_ARG;
   if (c->kv_dtype != Q3TTS_F32 && c->kv_dtype != Q3TTS_BF16) return Q3TTS_ERR_ARG;
   if (c->n_q_heads % c->n_kv_heads) return Q3TTS_ERR_ARG;
   if (c->head_dim != 64 && c->head_dim != 128) return Q3TTS_ERR_UNSUPPORTED;
@@ -87,7 +88,7 @@ Dims dims_of(const q3tts_config& c) {
   d.n_pages = c.kv_pages > 0 ? c.kv_pages : d.pps * d.S;
   d.chunk = c.prefill_chunk > 0 ? c.prefill_chunk : 256;
   d.m_max = std::max(d.chunk, 2 * d.S);
-  d.esz = c.weight_dtype == Q3TTS_F32 ? 4 : 2;
+  d.esz = c.weight_dtype == Q3TTS_F32 ? 4 : (c.weight_dtype == Q3TTS_FP8 ? 1 : 2);  // matrix elements
   d.kvesz = c.kv_dtype == Q3TTS_F32 ? 4 : 2;
   return d;
 }
@@ -217,7 +218,11 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
         misaligned16(L.w_down) || misaligned16(L.g_attn_norm) || misaligned16(L.g_ffn_norm) ||
         misaligned16(L.g_q_norm) || misaligned16(L.g_k_norm))
       return Q3TTS_ERR_ARG;
+    // FP8 matrices come with their row scales
+    if (c.weight_dtype == Q3TTS_FP8 && (!L.s_qkv || !L.s_o || !L.s_gateup || !L.s_down)) return Q3TTS_ERR_ARG;
   }
+  if (c.weight_dtype == Q3TTS_FP8 && (!w->s_head || !w->s_cp_heads || (w->cp_w_proj && !w->s_cp_proj)))
+    return Q3TTS_ERR_ARG;
   if (workspace_bytes < q3tts_workspace_size(cfg)) return Q3TTS_ERR_ARG;
 
   q3tts_handle* h = new (std::nothrow) q3tts_handle();

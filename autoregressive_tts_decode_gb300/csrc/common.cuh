@@ -2,12 +2,44 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace q3 {
 
 typedef __nv_bfloat16 bf16;
+
+// One FP8 E4M3 weight: the byte is its code (Q3TTS_FP8 weights).
+struct fp8e4 {
+  uint8_t v;
+};
+
+// Four E4M3 codes (the bytes of w, lowest first) as floats: each pair goes
+// through the hardware's exact E4M3 -> f16 conversion, then to float.
+__device__ __forceinline__ void fp8x4_to_f32(uint32_t w, float* f) {
+  uint32_t lo, hi;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"(static_cast<unsigned short>(w & 0xffffu)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"(static_cast<unsigned short>(w >> 16)));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
+
+// The storage type of the norm gains and embedding tables of a model whose
+// matrices are WT (bf16 beside FP8 matrices), and whether WT is FP8.
+template <class WT>
+struct GainOf {
+  using T = WT;
+};
+template <>
+struct GainOf<fp8e4> {
+  using T = bf16;
+};
+template <class WT>
+constexpr bool kFp8 = false;
+template <>
+constexpr bool kFp8<fp8e4> = true;
 
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(bf16 v) { return __bfloat162float(v); }
@@ -47,6 +79,17 @@ __device__ __forceinline__ void load_w8(const float* p, float* w) {
   w[2] = __uint_as_float(a.z); w[3] = __uint_as_float(a.w);
   w[4] = __uint_as_float(b.x); w[5] = __uint_as_float(b.y);
   w[6] = __uint_as_float(b.z); w[7] = __uint_as_float(b.w);
+}
+
+__device__ __forceinline__ void load_w8(const fp8e4* p, float* w) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+  fp8x4_to_f32(u.x, w);
+  fp8x4_to_f32(u.y, w + 4);
+}
+__device__ __forceinline__ float to_f(fp8e4 v) {
+  float f[4];
+  fp8x4_to_f32(v.v, f);
+  return f[0];
 }
 
 __device__ __forceinline__ void load_f8(const float* p, float* x) {

@@ -98,6 +98,12 @@ struct LayerDev {
   const void* w_oT;   // o_proj tiles [Hq][ceil(D/32)][hd/8][32][8] (see oproj_tiles)
   const void* w_gu;   // [2F][D]: gate rows, then up rows (the caller's tensor)
   const void* w_dT;   // [F][D]: W_down transposed, row f = column f of W_down
+  // FP8 matrices: per-output-row scales (W_qkv rows, W_o rows = output
+  // columns of o_proj, gate rows then up rows, W_down rows = output columns)
+  const float* s_qkv;
+  const float* s_o;
+  const float* s_gu;
+  const float* s_d;
 };
 
 struct FKParams {
@@ -107,6 +113,7 @@ struct FKParams {
   const LayerDev* tl;
   const LayerDev* cl;
   const void *t_head, *e_codec, *cp_heads, *cp_embeds, *cp_proj, *t_gfinal, *cp_gfinal;
+  const float *s_head, *s_cp_heads, *s_cp_proj;  // FP8: the heads' and projection's row scales
   float* pending_h;
   float* pending_logits;
   uint8_t* history;
@@ -321,6 +328,12 @@ template <>
 __device__ __forceinline__ void lds_w8<float>(uint32_t off, float* w) {
   const float4 a = lds_f4(off), b = lds_f4(off + 16);
   w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void lds_w8<fp8e4>(uint32_t off, float* w) {
+  const uint2 u = *reinterpret_cast<const uint2*>(fk_smem_raw + off);
+  fp8x4_to_f32(u.x, w);
+  fp8x4_to_f32(u.y, w + 4);
 }
 
 struct AttnScratch {
@@ -740,6 +753,7 @@ struct RowsOut {
   uint64_t* out64;
   uint32_t tag;
   int ts;
+  const float* sc;  // FP8: the matrix's row scales
 };
 
 // Rows base + r0 .. base + r0 + NR - 1 of a chunk (row stride rb) against T
@@ -759,10 +773,12 @@ __device__ __forceinline__ void rows_group(uint32_t buf, int rb, int r0, int K, 
     for (int t = 0; t < T; ++t)
       if (lane == r * T + t) {
         const int i = t * o.ts + base + r0 + r;
+        float v = acc[r][t] * inv[t];
+        if constexpr (kFp8<WT>) v *= __ldg(o.sc + base + r0 + r);
         if (o.out64)
-          st_tagged(o.out64 + i, acc[r][t] * inv[t], o.tag);
+          st_tagged(o.out64 + i, v, o.tag);
         else
-          o.out[i] = acc[r][t] * inv[t];
+          o.out[i] = v;
       }
 }
 
@@ -1163,7 +1179,7 @@ __device__ __forceinline__ void oproj_tiles(const FKParams& p, int D, int cta, i
 // added into xattn(k).  Closes the attention phase of layer k with a grid
 // barrier.
 template <class WT>
-__device__ __forceinline__ void oproj_step(Cons c, int D, int T, int k) {
+__device__ __forceinline__ void oproj_step(Cons c, int D, int T, int k, const float* so) {
   const FKParams& p = *fk_prm();
   Stream s = stream_begin(c);
   const int hd = p.hd, nt = oproj_nt(D), nkb = hd >> 3;
@@ -1194,10 +1210,16 @@ __device__ __forceinline__ void oproj_step(Cons c, int D, int T, int k) {
       }
     }
     release_private(s, n);
-    if (col < D)
+    if (col < D) {
+      if constexpr (kFp8<WT>) {  // W_o row (output column) scale
+        const float sc = __ldg(so + col);
+#pragma unroll
+        for (int t = 0; t < FK_TMAX; ++t) a[t] *= sc;
+      }
 #pragma unroll
       for (int t = 0; t < FK_TMAX; ++t)
         if (t < T) atomicAdd(XA + t * D + col, a[t]);
+    }
   }
   warp_set(cst().aborted, s.aborted ? 1 : 0);
   warp_set(cst().n, n0 + nch);
@@ -1314,7 +1336,8 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
       float v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[j] = j < J ? tag_float(raw[j]) : 0.f;
-      norm_rope_head(p, fk_sm(), v, isq ? side_gq<WT>(c, D) : side_gk<WT>(c, D), cp_rope_row(pos0 + t), clane());
+      norm_rope_head(p, fk_sm(), v, isq ? side_gq<typename GainOf<WT>::T>(c, D) : side_gk<typename GainOf<WT>::T>(c, D),
+                     cp_rope_row(pos0 + t), clane());
       float* dst = isq ? as.q[w] : as.kcur[it];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
@@ -1397,7 +1420,7 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
   }
   consumer_sync();
   FK_MARK(TR_SUB, 6);
-  oproj_step<WT>(c, D, T, k);
+  oproj_step<WT>(c, D, T, k, p.cl[layer].s_o);
 }
 
 // Talker phase B1: attention partials.  Work item = (kv group g, position
@@ -1477,7 +1500,8 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer, uint32_t qt
       float v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[j] = j < J ? tag_float(raw[j]) : 0.f;
-      norm_rope_head(p, fk_sm(), v, isk ? side_gk<WT>(c, p.Dt) : side_gq<WT>(c, p.Dt), TALKER_ROPE_ROW, clane());
+      norm_rope_head(p, fk_sm(), v, isk ? side_gk<typename GainOf<WT>::T>(c, p.Dt) : side_gq<typename GainOf<WT>::T>(c, p.Dt),
+                     TALKER_ROPE_ROW, clane());
       float* dst = isk ? as.kcur[0] : as.q[cwarp()];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
@@ -1574,7 +1598,7 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer, uint32_t qt
 // Talker phase B2: combine the partials of the CTA's heads (all partial loads
 // of a thread issued together), then o_proj.
 template <class WT>
-__device__ __forceinline__ void phase_talker_oproj(Cons c, int k, uint32_t ptag) {
+__device__ __forceinline__ void phase_talker_oproj(Cons c, int k, uint32_t ptag, int l) {
   const FKParams& p = *fk_prm();
   const int D = p.Dt, hd = p.hd, cpg = p.ncta / p.Hkv, nt = oproj_nt(D);
   int v0, v1;  // the CTA's o_proj tiles
@@ -1632,7 +1656,7 @@ __device__ __forceinline__ void phase_talker_oproj(Cons c, int k, uint32_t ptag)
     put_plane(fk_sm()->os[hh][0], hd, d, O / L);
   }
   consumer_sync();
-  oproj_step<WT>(c, D, 1, k);
+  oproj_step<WT>(c, D, 1, k, p.tl[l].s_o);
 }
 
 // Units u0 .. u0 + G - 1 of a chunk that holds the gate rows of U units and
@@ -1640,7 +1664,8 @@ __device__ __forceinline__ void phase_talker_oproj(Cons c, int k, uint32_t ptag)
 // rms_t) into act[t][a0 + u] (lane u T + t writes one).
 template <class WT, int T, int G>
 __device__ __forceinline__ void ffn_units(uint32_t buf, int rb, int U, int u0, int D, uint32_t xs, int lane,
-                                          const float (&inv)[T], float (*act)[FK_UMAX], int a0) {
+                                          const float (&inv)[T], float (*act)[FK_UMAX], int a0, const float* sgu,
+                                          int F, int f0) {
   uint32_t ro[2 * G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -1653,7 +1678,14 @@ __device__ __forceinline__ void ffn_units(uint32_t buf, int rb, int U, int u0, i
   for (int g = 0; g < G; ++g)
 #pragma unroll
     for (int t = 0; t < T; ++t)
-      if (lane == g * T + t) act[t][a0 + u0 + g] = silu(acc[2 * g][t] * inv[t]) * (acc[2 * g + 1][t] * inv[t]);
+      if (lane == g * T + t) {
+        float gs = 1.f, us = 1.f;
+        if constexpr (kFp8<WT>) {  // gate row f and up row F + f of W_gateup
+          gs = __ldg(sgu + f0 + a0 + u0 + g);
+          us = __ldg(sgu + F + f0 + a0 + u0 + g);
+        }
+        act[t][a0 + u0 + g] = silu(acc[2 * g][t] * inv[t] * gs) * (acc[2 * g + 1][t] * inv[t] * us);
+      }
 }
 
 // The down projection of the CTA's FFN units [f0, f1): shared chunks of
@@ -1662,7 +1694,7 @@ __device__ __forceinline__ void ffn_units(uint32_t buf, int rb, int U, int u0, i
 // registers and adds the CTA's partial sums into copy CTA % FK_KC of
 // xffn(k) with float4 atomics.
 template <class WT, int T>
-__device__ __forceinline__ void ffn_down(Stream& s, int D, int f0, int f1, uint32_t n0, int k) {
+__device__ __forceinline__ void ffn_down(Stream& s, int D, int f0, int f1, uint32_t n0, int k, const float* sd) {
   const FKParams& p = *fk_prm();
   const float(*act)[FK_UMAX] = fk_sm()->act;
   const int rb = D * (int)sizeof(WT);
@@ -1696,6 +1728,14 @@ __device__ __forceinline__ void ffn_down(Stream& s, int D, int f0, int f1, uint3
   warp_set(cst().aborted, s.aborted ? 1 : 0);
   warp_set(cst().n, n0 + nd);
   if (active && nd) {
+    if constexpr (kFp8<WT>) {  // W_down row (output column) scales
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float sc = __ldg(sd + col + q);
+#pragma unroll
+        for (int t = 0; t < T; ++t) y[t][q] *= sc;
+      }
+    }
     float* X = xffn(p, k, ccta() % FK_KC);
 #pragma unroll
     for (int t = 0; t < T; ++t) {
@@ -1722,9 +1762,10 @@ __device__ __forceinline__ int units_per_chunk(int row_bytes) {
 // CTA % FK_KC of xffn(k) with float4 atomics.  The CTA also clears its slice
 // of layer k + 1's deltas (see xbase).
 template <class WT>
-__device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int k) {
+__device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int k, const LayerDev* lw) {
+  using GT = typename GainOf<WT>::T;
   const FKParams& p = *fk_prm();
-  load_norm<WT>(c, SRC_RES_A, k, 0u, 0, T, D, side_cur<WT>(c) + D, -1, nullptr);
+  load_norm<GT>(c, SRC_RES_A, k, 0u, 0, T, D, side_cur<GT>(c) + D, -1, nullptr);
   side_end(c);
   {
     int lo, hi;
@@ -1754,12 +1795,12 @@ __device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int k) {
     int u = 0;
     if (T == 1) {
       const float inv[1] = {inv0};
-      for (; u + 2 <= U; u += 2) ffn_units<WT, 1, 2>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0);
-      if (u < U) ffn_units<WT, 1, 1>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0);
+      for (; u + 2 <= U; u += 2) ffn_units<WT, 1, 2>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0, lw->s_gu, F, f0);
+      if (u < U) ffn_units<WT, 1, 1>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0, lw->s_gu, F, f0);
     } else {
       const float inv[2] = {inv0, inv1};
-      for (; u + 2 <= U; u += 2) ffn_units<WT, 2, 2>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0);
-      if (u < U) ffn_units<WT, 2, 1>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0);
+      for (; u + 2 <= U; u += 2) ffn_units<WT, 2, 2>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0, lw->s_gu, F, f0);
+      if (u < U) ffn_units<WT, 2, 1>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0, lw->s_gu, F, f0);
     }
     release_private(s, n);
   }
@@ -1767,9 +1808,9 @@ __device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int k) {
   n0 += nch;
   consumer_sync();  // act complete
   if (T == 1)
-    ffn_down<WT, 1>(s, D, f0, f1, n0, k);
+    ffn_down<WT, 1>(s, D, f0, f1, n0, k, lw->s_d);
   else
-    ffn_down<WT, 2>(s, D, f0, f1, n0, k);
+    ffn_down<WT, 2>(s, D, f0, f1, n0, k, lw->s_d);
   grid_sync(c);
 }
 
@@ -1816,10 +1857,11 @@ __device__ __forceinline__ void cp_tokens(Cons c, int j, int fed) {
   const FKParams& p = *fk_prm();
   const int Dt = p.Dt;
   float* xs = fk_sm()->u.g.xs;
-  const WT* e = code_row<WT>(p, j, fed);
+  using GT = typename GainOf<WT>::T;
+  const GT* e = code_row<GT>(p, j, fed);
   for (int b = ctid(); b < (Dt >> 3); b += FK_CONSUMERS) {
     float f[8];
-    ld8<WT>(e + 8 * b, f);
+    ld8<GT>(e + 8 * b, f);
     put_plane8(j == 0 ? xs + Dt : xs, Dt, b, f);
     if (j == 0) {
       ld8<float>(p.pending_h + (size_t)p.sid * Dt + 8 * b, f);
@@ -1837,17 +1879,18 @@ __device__ __forceinline__ void cp_tokens(Cons c, int j, int fed) {
 // 16-byte aligned embedding tables.
 template <class WT>
 __device__ __forceinline__ void talker_input(Cons c, int fed15) {
+  using GT = typename GainOf<WT>::T;
   const FKParams& p = *fk_prm();
   const int Dt = p.Dt;
   float* xs = fk_sm()->u.g.xs;
   const int* fedc = fk_sm()->fedc;
   for (int b = ctid(); b < (Dt >> 3); b += FK_CONSUMERS) {
     float s[8];
-    ld8<WT>(code_row<WT>(p, 0, fedc[0]) + 8 * b, s);
+    ld8<GT>(code_row<GT>(p, 0, fedc[0]) + 8 * b, s);
 #pragma unroll 5
     for (int j = 1; j < Q3TTS_N_CODEBOOKS; ++j) {
       float f[8];
-      ld8<WT>(code_row<WT>(p, j, j < Q3TTS_N_CODEBOOKS - 1 ? fedc[j] : fed15) + 8 * b, f);
+      ld8<GT>(code_row<GT>(p, j, j < Q3TTS_N_CODEBOOKS - 1 ? fedc[j] : fed15) + 8 * b, f);
 #pragma unroll
       for (int k = 0; k < 8; ++k) s[k] += f[k];
     }
@@ -1952,46 +1995,52 @@ __device__ __forceinline__ void rows_step(Cons c, const Step& st) {
   o.out64 = nullptr;
   o.tag = tag;
   o.ts = 0;
+  o.sc = nullptr;
   if (st.kind == S_QKV) {
     K = cp ? p.Dc : p.Dt;
     T = Tp;
     nrows = p.qkv_rows;
     o.out64 = p.qkv;
     o.ts = p.qkv_rows;
+    if constexpr (kFp8<WT>) o.sc = (cp ? p.cl : p.tl)[st.l].s_qkv;
   } else if (st.kind == S_PROJ) {
     K = p.Dt;
     T = Tp;
     nrows = p.Dc;
     o.out64 = p.z;
     o.ts = p.Dc;
+    o.sc = p.s_cp_proj;
   } else if (st.kind == S_CP_HEAD) {
     K = p.Dc;
     T = 1;
     nrows = p.Vc;
     o.out64 = p.cp_logits;
+    if constexpr (kFp8<WT>) o.sc = p.s_cp_heads + (size_t)st.j * p.Vc;
   } else {
     K = p.Dt;
     T = 1;
     nrows = p.Vt;
     o.out = p.pending_logits + (size_t)p.sid * p.Vt;
+    o.sc = p.s_head;
   }
   float inv0 = 1.f, inv1 = 1.f;  // the projection's input is not normed
   if (st.kind != S_PROJ) {
-    const WT* g;
+    using GT = typename GainOf<WT>::T;
+    const GT* g;
     int src = SRC_RES, fold = -1, t0 = 0;
     const int k = (int)L.layer;  // QKV: this layer; heads: the layers done so far
     float* hout = nullptr;
     if (st.kind == S_QKV) {
-      g = side_begin<WT>(c);
+      g = side_begin<GT>(c);
       FK_MARK(TR_SUB, 1);
       src = L.src;  // the raw tokens, the projection, or layer k - 1's residual
       fold = k;
     } else {
-      g = reinterpret_cast<const WT*>(fk_sm()->fin) + (cp ? 0 : p.Dc);
+      g = reinterpret_cast<const GT*>(fk_sm()->fin) + (cp ? 0 : p.Dc);
       t0 = Tp - 1;
       if (!cp) hout = p.pending_h + (size_t)p.sid * p.Dt;
     }
-    load_norm<WT>(c, src, k - 1, tag_of(L.s - 1), t0, T, K, g, fold, hout);
+    load_norm<GT>(c, src, k - 1, tag_of(L.s - 1), t0, T, K, g, fold, hout);
     inv0 = norm_inv(0, K);
     inv1 = T > 1 ? norm_inv(1, K) : 0.f;
   }
@@ -2021,9 +2070,10 @@ __device__ void consumer() {
       sm->uni[ctid()] = p.uniforms[ctid()];
       sm->forced[ctid()] = p.forced ? p.forced[ctid()] : 0;
     }
-    WT* fin = reinterpret_cast<WT*>(sm->fin);
-    for (int i = ctid(); i < p.Dc; i += FK_CONSUMERS) fin[i] = ((const WT*)p.cp_gfinal)[i];
-    for (int i = ctid(); i < p.Dt; i += FK_CONSUMERS) fin[p.Dc + i] = ((const WT*)p.t_gfinal)[i];
+    using GT = typename GainOf<WT>::T;
+    GT* fin = reinterpret_cast<GT*>(sm->fin);
+    for (int i = ctid(); i < p.Dc; i += FK_CONSUMERS) fin[i] = ((const GT*)p.cp_gfinal)[i];
+    for (int i = ctid(); i < p.Dt; i += FK_CONSUMERS) fin[p.Dc + i] = ((const GT*)p.t_gfinal)[i];
     if (ccta() == 0 && ctid() == 0 && p.newpage >= 0)
       const_cast<int*>(p.tkv.page_table)[p.sid * p.tkv.pages_per_stream + p.pos / p.tkv.page_size] = p.newpage;
     // the stream's page tables (the page entered this frame from the launch
@@ -2084,10 +2134,11 @@ __device__ void consumer() {
         phase_talker_attn<WT, KT>(c, st.l, tag_of(L.s - 1), tag_of(L.s));
         break;
       case S_T_OPROJ:
-        phase_talker_oproj<WT>(c, (int)L.layer, tag_of(L.s - 1));
+        phase_talker_oproj<WT>(c, (int)L.layer, tag_of(L.s - 1), st.l);
         break;
       case S_FFN:
-        phase_ffn<WT>(c, cp ? fk_prm()->Dc : fk_prm()->Dt, cp ? fk_prm()->Fc : fk_prm()->Ft, T, (int)L.layer);
+        phase_ffn<WT>(c, cp ? fk_prm()->Dc : fk_prm()->Dt, cp ? fk_prm()->Fc : fk_prm()->Ft, T, (int)L.layer,
+                      (cp ? fk_prm()->cl : fk_prm()->tl) + st.l);
         break;
       default:
         rows_step<WT>(c, st);
@@ -2232,7 +2283,7 @@ struct Producer {
     }
     const int ncp = (Q3TTS_N_CODEBOOKS - 1) * p.Lc;
     const int D = k < ncp ? p.Dc : p.Dt;
-    const unsigned bytes = (unsigned)((2 * D + 2 * p.hd) * (int)sizeof(WT));
+    const unsigned bytes = (unsigned)((2 * D + 2 * p.hd) * (int)sizeof(typename GainOf<WT>::T));
     mbar_expect_tx(&sm->side_full[slot], bytes);
     bulk_g2s(sm->side[slot], layer_at(k).side, bytes, &sm->side_full[slot], pol);
     side_last[slot] = k;
@@ -2268,7 +2319,7 @@ struct Producer {
       const char* base;
       const char* up = nullptr;  // gate/up segment: the up rows
       int N, rb;
-      bool layer_end = false;
+      bool layer_end = false, one = false;  // one: one row (o_proj tile) per chunk
       if (cp && q < hp) {
         base = (const char*)p.cp_proj;
         N = p.Dc;
@@ -2288,6 +2339,7 @@ struct Producer {
           base = (const char*)L.w_oT;
           N = p.Hq * oproj_nt(D);
           rb = 32 * p.hd * esz;
+          one = true;  // the consumers take one tile per chunk, however small
         } else if (m == 2) {
           base = (const char*)L.w_gu;
           up = base + (size_t)F * D * esz;
@@ -2302,7 +2354,7 @@ struct Producer {
       }
       int lo, hi;
       split(N, p.ncta, cta, lo, hi);
-      const int per = up ? units_per_chunk(rb) : rows_per_chunk(rb);
+      const int per = one ? 1 : (up ? units_per_chunk(rb) : rows_per_chunk(rb));
       for (int r = lo; r < hi && !stop; r += per) {
         const unsigned bytes = (unsigned)(min(per, hi - r) * rb);
         if (up)
@@ -2426,8 +2478,12 @@ static int fk_xstride(const q3tts_config& c) {
   return (w + 63) & ~63;
 }
 
+// Bytes of one matrix element and of one gain / embedding element.
+static int mat_esz(int wdt) { return wdt == Q3TTS_F32 ? 4 : (wdt == Q3TTS_FP8 ? 1 : 2); }
+static int gain_esz(int wdt) { return wdt == Q3TTS_F32 ? 4 : 2; }
+
 static size_t fk_layout(const q3tts_config& c, int ncta, FKState* st, char* base) {
-  const int esz = c.weight_dtype == Q3TTS_F32 ? 4 : 2;
+  const int esz = mat_esz(c.weight_dtype), gsz = gain_esz(c.weight_dtype);
   const int Hq = c.n_q_heads, hd = c.head_dim, Hkv = c.n_kv_heads;
   const int dmax = std::max(c.talker_hidden, c.cp_hidden);
   const int qkv_rows = (Hq + 2 * Hkv) * hd;
@@ -2444,8 +2500,8 @@ static size_t fk_layout(const q3tts_config& c, int ncta, FKState* st, char* base
   // re-laid-out weights per layer: o_proj tiles, W_down^T
   char* reT = take((size_t)c.talker_layers * (oT_t + (size_t)c.talker_ffn * c.talker_hidden) * esz);
   char* reC = take((size_t)c.cp_layers * (oT_c + (size_t)c.cp_ffn * c.cp_hidden) * esz);
-  char* sideT = take((size_t)c.talker_layers * (2 * c.talker_hidden + 2 * hd) * esz);
-  char* sideC = take((size_t)c.cp_layers * (2 * c.cp_hidden + 2 * hd) * esz);
+  char* sideT = take((size_t)c.talker_layers * (2 * c.talker_hidden + 2 * hd) * gsz);
+  char* sideC = take((size_t)c.cp_layers * (2 * c.cp_hidden + 2 * hd) * gsz);
   char* tl = take(sizeof(LayerDev) * c.talker_layers);
   char* cl = take(sizeof(LayerDev) * c.cp_layers);
   char* xb = take(sizeof(float) * 2 * xst);
@@ -2481,6 +2537,7 @@ static void* kernel_ptr() {
 }
 
 static void* pick_kernel(int wdt, int kdt) {
+  if (wdt == Q3TTS_FP8) return kdt == Q3TTS_BF16 ? kernel_ptr<fp8e4, bf16>() : kernel_ptr<fp8e4, float>();
   if (wdt == Q3TTS_BF16) return kdt == Q3TTS_BF16 ? kernel_ptr<bf16, bf16>() : kernel_ptr<bf16, float>();
   return kdt == Q3TTS_BF16 ? kernel_ptr<float, bf16>() : kernel_ptr<float, float>();
 }
@@ -2515,7 +2572,7 @@ int frame_kernel_create(q3tts_handle* h) {
   if (ncta < c.n_kv_heads || !tiles_ok(c.talker_hidden) || !tiles_ok(c.cp_hidden)) return Q3TTS_OK;
   // a ring chunk holds the gate and up rows of one FFN unit (2 D weights) and
   // one o_proj tile (32 hd weights); a CTA's FFN activations fit act
-  const int esz_w = c.weight_dtype == Q3TTS_F32 ? 4 : 2;
+  const int esz_w = mat_esz(c.weight_dtype), esz_g = gain_esz(c.weight_dtype);
   if (2 * std::max(c.talker_hidden, c.cp_hidden) * esz_w > FK_STAGE || 32 * c.head_dim * esz_w > FK_STAGE)
     return Q3TTS_OK;
   if ((std::max(c.talker_ffn, c.cp_ffn) + ncta - 1) / ncta > FK_UMAX) return Q3TTS_OK;
@@ -2527,8 +2584,8 @@ int frame_kernel_create(q3tts_handle* h) {
                     2 + 4 * c.talker_layers;
   if (steps >= FK_MAXSTEPS) return Q3TTS_OK;
   // per-layer gains and both final norms fit their shared-memory slots
-  if ((2 * std::max(c.talker_hidden, c.cp_hidden) + 2 * c.head_dim) * esz_w > FK_SIDE_BYTES ||
-      (c.talker_hidden + c.cp_hidden) * esz_w > FK_FIN_BYTES)
+  if ((2 * std::max(c.talker_hidden, c.cp_hidden) + 2 * c.head_dim) * esz_g > FK_SIDE_BYTES ||
+      (c.talker_hidden + c.cp_hidden) * esz_g > FK_FIN_BYTES)
     return Q3TTS_OK;
   st->smem = sizeof(FKSmem);
   void* k = pick_kernel(c.weight_dtype, c.kv_dtype);
@@ -2549,12 +2606,12 @@ int frame_kernel_create(q3tts_handle* h) {
   char* base = (char*)h->fk_base;  // workspace tail reserved by frame_kernel_workspace
   fk_layout(c, ncta, st, base);
   // re-laid-out weights
-  const int esz = c.weight_dtype == Q3TTS_F32 ? 4 : 2;
+  const int esz = esz_w, gsz = esz_g;
   const int Hq = c.n_q_heads, hd = c.head_dim;
   std::vector<LayerDev> tl(c.talker_layers), cl(c.cp_layers);
   char* re = base;
   auto fill = [&](const q3tts_layer_weights& w, LayerDev& d, int D, int F, char* side) -> bool {
-    const size_t gd = (size_t)D * esz, gh = (size_t)hd * esz;
+    const size_t gd = (size_t)D * gsz, gh = (size_t)hd * gsz;
     if (cudaMemcpyAsync(side, w.g_attn_norm, gd, cudaMemcpyDeviceToDevice, h->s) != cudaSuccess ||
         cudaMemcpyAsync(side + gd, w.g_ffn_norm, gd, cudaMemcpyDeviceToDevice, h->s) != cudaSuccess ||
         (w.g_q_norm && cudaMemcpyAsync(side + 2 * gd, w.g_q_norm, gh, cudaMemcpyDeviceToDevice, h->s) != cudaSuccess) ||
@@ -2563,6 +2620,10 @@ int frame_kernel_create(q3tts_handle* h) {
     d.side = side;
     d.w_qkv = w.w_qkv;
     d.w_gu = w.w_gateup;
+    d.s_qkv = w.s_qkv;
+    d.s_o = w.s_o;
+    d.s_gu = w.s_gateup;
+    d.s_d = w.s_down;
     char* oT = re;
     re += (size_t)Hq * hd * 32 * ((D + 31) / 32) * esz;
     char* dT = re;
@@ -2571,7 +2632,10 @@ int frame_kernel_create(q3tts_handle* h) {
     d.w_dT = dT;
     // W_down^T [F][D]: dT[f][d] = W_down[d][f]
     dim3 tb(32, 8), tg((F + 31) / 32 < 1024 ? (F + 31) / 32 : 1024, (D + 31) / 32 < 1024 ? (D + 31) / 32 : 1024);
-    if (esz == 2) {
+    if (esz == 1) {
+      repack_oT_kernel<uint8_t><<<1024, 256, 0, h->s>>>((const uint8_t*)w.w_o, (uint8_t*)oT, D, Hq, hd);
+      transpose_kernel<uint8_t><<<tg, tb, 0, h->s>>>((const uint8_t*)w.w_down, (uint8_t*)dT, D, F, (size_t)D);
+    } else if (esz == 2) {
       repack_oT_kernel<bf16><<<1024, 256, 0, h->s>>>((const bf16*)w.w_o, (bf16*)oT, D, Hq, hd);
       transpose_kernel<bf16><<<tg, tb, 0, h->s>>>((const bf16*)w.w_down, (bf16*)dT, D, F, (size_t)D);
     } else {
@@ -2582,10 +2646,10 @@ int frame_kernel_create(q3tts_handle* h) {
   };
   for (int l = 0; l < c.talker_layers; ++l)
     if (!fill(h->tl[l], tl[l], c.talker_hidden, c.talker_ffn,
-              st->sideT + (size_t)l * (2 * c.talker_hidden + 2 * hd) * esz))
+              st->sideT + (size_t)l * (2 * c.talker_hidden + 2 * hd) * gsz))
       return Q3TTS_ERR_CUDA;
   for (int l = 0; l < c.cp_layers; ++l)
-    if (!fill(h->cl[l], cl[l], c.cp_hidden, c.cp_ffn, st->sideC + (size_t)l * (2 * c.cp_hidden + 2 * hd) * esz))
+    if (!fill(h->cl[l], cl[l], c.cp_hidden, c.cp_ffn, st->sideC + (size_t)l * (2 * c.cp_hidden + 2 * hd) * gsz))
       return Q3TTS_ERR_CUDA;
   if (cudaMemcpyAsync(st->tl, tl.data(), sizeof(LayerDev) * tl.size(), cudaMemcpyHostToDevice, h->s) != cudaSuccess ||
       cudaMemcpyAsync(st->cl, cl.data(), sizeof(LayerDev) * cl.size(), cudaMemcpyHostToDevice, h->s) != cudaSuccess ||
@@ -2629,6 +2693,7 @@ static void frame_params(FKParams& p, const q3tts_handle* h, int sid, int pos, i
   p.t_head = h->w.talker_w_head; p.e_codec = h->w.talker_e_codec; p.cp_heads = h->w.cp_heads;
   p.cp_embeds = h->w.cp_embeds; p.cp_proj = h->w.cp_w_proj; p.t_gfinal = h->w.talker_g_final;
   p.cp_gfinal = h->w.cp_g_final;
+  p.s_head = h->w.s_head; p.s_cp_heads = h->w.s_cp_heads; p.s_cp_proj = h->w.s_cp_proj;
   p.pending_h = h->pending_h; p.pending_logits = h->pending_logits; p.history = h->history;
   p.finished = h->finished;
   p.tkv = talker_kv(h); p.ckv = cp_kv(h); p.rope_cos = h->rope_cos; p.rope_sin = h->rope_sin;

@@ -11,7 +11,7 @@ template <class WT, int MT>
 __global__ void __launch_bounds__(256) gemv_kernel(const float* __restrict__ X, int ldx,
                                                    const WT* __restrict__ W, int N, int K,
                                                    float* __restrict__ Y, int ldy, int M,
-                                                   int accumulate) {
+                                                   int accumulate, const float* __restrict__ sc) {
   const int lane = threadIdx.x & 31;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(256) gemv_kernel(const float* __restrict__ X, 
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         float v = warp_sum(acc[t]);
+        if (sc) v *= sc[n];  // FP8 rows: the row scale
         if (lane == 0 && m0 + t < M) {
           float* y = Y + (size_t)(m0 + t) * ldy + n;
           *y = accumulate ? *y + v : v;
@@ -51,7 +52,7 @@ template <class WT>
 __global__ void __launch_bounds__(256) gemm_kernel(const float* __restrict__ X, int ldx,
                                                    const WT* __restrict__ W, int N, int K,
                                                    float* __restrict__ Y, int ldy, int M,
-                                                   int accumulate) {
+                                                   int accumulate, const float* __restrict__ sc) {
   __shared__ float As[16][64 + 4];
   __shared__ float Bs[16][64 + 4];
   const int tid = threadIdx.x;
@@ -85,38 +86,41 @@ __global__ void __launch_bounds__(256) gemm_kernel(const float* __restrict__ X, 
       int gm = m0 + tm + i, gn = n0 + tn + j;
       if (gm < M && gn < N) {
         float* y = Y + (size_t)gm * ldy + gn;
-        *y = accumulate ? *y + acc[i][j] : acc[i][j];
+        const float v = sc ? acc[i][j] * sc[gn] : acc[i][j];  // FP8 rows: the row scale
+        *y = accumulate ? *y + v : v;
       }
     }
 }
 
 template <class WT>
 static void linear_t(const float* X, int ldx, const WT* W, int N, int K, float* Y, int ldy, int M,
-                     bool acc, cudaStream_t s) {
+                     bool acc, const float* sc, cudaStream_t s) {
   if (M <= 0 || N <= 0) return;
   if (M <= 16) {
     int blocks = (N + 7) / 8;
     if (blocks > 4096) blocks = 4096;
     if (M <= 1)
-      gemv_kernel<WT, 1><<<blocks, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc);
+      gemv_kernel<WT, 1><<<blocks, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc, sc);
     else if (M <= 2)
-      gemv_kernel<WT, 2><<<blocks, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc);
+      gemv_kernel<WT, 2><<<blocks, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc, sc);
     else if (M <= 4)
-      gemv_kernel<WT, 4><<<blocks, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc);
+      gemv_kernel<WT, 4><<<blocks, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc, sc);
     else
-      gemv_kernel<WT, 8><<<blocks, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc);
+      gemv_kernel<WT, 8><<<blocks, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc, sc);
   } else {
     dim3 grid((N + 63) / 64, (M + 63) / 64);
-    gemm_kernel<WT><<<grid, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc);
+    gemm_kernel<WT><<<grid, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc, sc);
   }
 }
 
 void launch_linear(int wdt, const float* X, int ldx, const void* W, int N, int K, float* Y, int ldy,
-                   int M, bool accumulate, cudaStream_t s) {
-  if (wdt == Q3TTS_BF16)
-    linear_t(X, ldx, (const bf16*)W, N, K, Y, ldy, M, accumulate, s);
+                   int M, bool accumulate, cudaStream_t s, const float* scale) {
+  if (wdt == Q3TTS_FP8)
+    linear_t(X, ldx, (const fp8e4*)W, N, K, Y, ldy, M, accumulate, scale, s);
+  else if (wdt == Q3TTS_BF16)
+    linear_t(X, ldx, (const bf16*)W, N, K, Y, ldy, M, accumulate, nullptr, s);
   else
-    linear_t(X, ldx, (const float*)W, N, K, Y, ldy, M, accumulate, s);
+    linear_t(X, ldx, (const float*)W, N, K, Y, ldy, M, accumulate, nullptr, s);
 }
 
 // --------------------------------------------------------------- rmsnorm

@@ -22,9 +22,10 @@ struct TokDesc {
   int pos_const;
 };
 
-// Y[m, n] (+)= sum_k X[m, k] W[n, k] for m < M, n < N.
+// Y[m, n] (+)= sum_k X[m, k] W[n, k] for m < M, n < N (FP8 W: times the row
+// scale scale[n]).
 void launch_linear(int wdt, const float* X, int ldx, const void* W, int N, int K, float* Y, int ldy,
-                   int M, bool accumulate, cudaStream_t s);
+                   int M, bool accumulate, cudaStream_t s, const float* scale = nullptr);
 
 // Y[m] = X[in_row(m)] / rms * g, in_row(m) = m * in_mul + in_add.
 void launch_rmsnorm(int wdt, const float* X, int ldx, int in_mul, int in_add, const void* g,

@@ -167,47 +167,52 @@ static HiLo hilo(const q3tts_handle* h) { return HiLo{h->xh, h->xl, h->m_max}; }
 // Y (+)= X W^T.  On the tensor-core path X is the hi/lo pair already written
 // by the producing kernel (xf unused); otherwise xf (fp32, row pitch ldx).
 static void proj(q3tts_handle* h, const float* xf, int ldx, const void* W, int N, int K, float* Y, int ldy,
-                 int M, bool acc) {
+                 int M, bool acc, const float* scale = nullptr) {
   if (h->tc) {
     if (!tc_linear(hilo(h), W, N, K, Y, ldy, M, acc, h->d_err, h->s)) h->tc_failed = true;
   } else {
-    launch_linear(h->c.weight_dtype, xf, ldx, W, N, K, Y, ldy, M, acc, h->s);
+    launch_linear(h->c.weight_dtype, xf, ldx, W, N, K, Y, ldy, M, acc, h->s, scale);
   }
+}
+
+// dtype of the norm gains and embedding tables (bf16 beside FP8 matrices)
+static int gain_dt(const q3tts_handle* h) {
+  return h->c.weight_dtype == Q3TTS_FP8 ? Q3TTS_BF16 : h->c.weight_dtype;
 }
 
 // RMSNorm of M rows of X into the next projection's input: hi/lo terms on the
 // tensor-core path, else fp32 in h->hb.
 static void norm_in(q3tts_handle* h, const float* X, int ldx, int in_mul, int in_add, const void* g, int M, int D) {
   if (h->tc)
-    launch_rmsnorm_hilo(h->c.weight_dtype, X, ldx, in_mul, in_add, g, hilo(h), M, D, h->c.rms_eps, h->s);
+    launch_rmsnorm_hilo(gain_dt(h), X, ldx, in_mul, in_add, g, hilo(h), M, D, h->c.rms_eps, h->s);
   else
-    launch_rmsnorm(h->c.weight_dtype, X, ldx, in_mul, in_add, g, h->hb, D, M, D, h->c.rms_eps, h->s);
+    launch_rmsnorm(gain_dt(h), X, ldx, in_mul, in_add, g, h->hb, D, M, D, h->c.rms_eps, h->s);
 }
 
 // M tokens through all layers of one decoder stack (residual stream x [M, D]).
 static void stack_pass(q3tts_handle* h, const q3tts_layer_weights* lw, int layers, int D, int F,
                        float* x, int M, TokDesc td, KVDesc kv, int kdt, int max_ctx) {
   cudaStream_t s = h->s;
-  const int wdt = h->c.weight_dtype, HqD = h->Hq * h->hd;
+  const int gdt = gain_dt(h), HqD = h->Hq * h->hd;
   for (int l = 0; l < layers; ++l) {
     const q3tts_layer_weights& L = lw[l];
     norm_in(h, x, D, 1, 0, L.g_attn_norm, M, D);
-    proj(h, h->hb, D, L.w_qkv, h->qkv_rows, D, h->qkv, h->qkv_rows, M, false);
-    launch_qk_rope_append(wdt, kdt, h->qkv, h->qkv_rows, M, td, L.g_q_norm, L.g_k_norm,
+    proj(h, h->hb, D, L.w_qkv, h->qkv_rows, D, h->qkv, h->qkv_rows, M, false, L.s_qkv);
+    launch_qk_rope_append(gdt, kdt, h->qkv, h->qkv_rows, M, td, L.g_q_norm, L.g_k_norm,
                           h->c.qk_norm, h->c.rms_eps, h->rope_cos, h->rope_sin, kv, l, h->Hq, s);
     // contexts longer than one span: spread over the GPU by span
     if (max_ctx <= 64 || !launch_attention_split(kdt, h->qkv, h->qkv_rows, M, td, kv, l, h->Hq, h->att, HqD,
                                                  h->spl_part, h->spl_cnt, h->spl_nsmax, s))
       launch_attention(kdt, h->qkv, h->qkv_rows, M, td, kv, l, h->Hq, h->att, HqD, max_ctx, s);
     if (h->tc) launch_split_hilo(h->att, HqD, hilo(h), M, HqD, s);
-    proj(h, h->att, HqD, L.w_o, D, HqD, x, D, M, true);
+    proj(h, h->att, HqD, L.w_o, D, HqD, x, D, M, true, L.s_o);
     norm_in(h, x, D, 1, 0, L.g_ffn_norm, M, D);
-    proj(h, h->hb, D, L.w_gateup, 2 * F, D, h->gu, 2 * F, M, false);
+    proj(h, h->hb, D, L.w_gateup, 2 * F, D, h->gu, 2 * F, M, false, L.s_gateup);
     if (h->tc)
       launch_silu_mul_hilo(h->gu, hilo(h), M, F, s);
     else
       launch_silu_mul(h->gu, h->act, M, F, s);
-    proj(h, h->act, F, L.w_down, D, F, x, D, M, true);
+    proj(h, h->act, F, L.w_down, D, F, x, D, M, true, L.s_down);
   }
   h->launches += (h->tc ? 10ull : 9ull) * layers;
 }
@@ -227,10 +232,10 @@ int prefill_layered(q3tts_handle* h, int sid, const float* embeds, int len) {
     stack_pass(h, h->tl.data(), h->c.talker_layers, Dt, h->Ft, h->x, T, td, talker_kv(h),
                h->c.kv_dtype, c0 + T);
     if (c0 + T == len) {
-      launch_rmsnorm(h->c.weight_dtype, h->x, Dt, 1, T - 1, h->w.talker_g_final,
+      launch_rmsnorm(gain_dt(h), h->x, Dt, 1, T - 1, h->w.talker_g_final,
                      h->pending_h + (size_t)sid * Dt, Dt, 1, Dt, h->c.rms_eps, s);
       launch_linear(h->c.weight_dtype, h->pending_h + (size_t)sid * Dt, Dt, h->w.talker_w_head,
-                    h->Vt, Dt, h->pending_logits + (size_t)sid * h->Vt, h->Vt, 1, false, s);
+                    h->Vt, Dt, h->pending_logits + (size_t)sid * h->Vt, h->Vt, 1, false, s, h->w.s_head);
       h->launches += 2;
     }
   }
@@ -246,7 +251,7 @@ int prefill_layered(q3tts_handle* h, int sid, const float* embeds, int len) {
 static void step_kernels(q3tts_handle* h, int n, int max_ctx, const float* uniforms, int32_t* codes,
                          const int32_t* forced, float* logits) {
   cudaStream_t s = h->s;
-  const int Dt = h->Dt, Dc = h->Dc, Vt = h->Vt, Vc = h->Vc, wdt = h->c.weight_dtype;
+  const int Dt = h->Dt, Dc = h->Dc, Vt = h->Vt, Vc = h->Vc, gdt = gain_dt(h);
   const int dump_ld = Vt + (Q3TTS_N_CODEBOOKS - 1) * Vc;
   const size_t smem = sizeof(SamplerSmem);
   setup_kernel<<<1, 256, 0, s>>>(h->d_desc, h->d_sid, h->d_pos, h->d_sp, h->page_table, h->pps,
@@ -257,7 +262,7 @@ static void step_kernels(q3tts_handle* h, int n, int max_ctx, const float* unifo
   const size_t es = wbytes(h);
   for (int j = 0; j < Q3TTS_N_CODEBOOKS - 1; ++j) {
     const int M = j == 0 ? 2 * n : n;
-    if (wdt == Q3TTS_BF16)
+    if (gdt == Q3TTS_BF16)
       cp_input_kernel<bf16><<<M, 256, 0, s>>>(j, n, h->d_sid, h->d_fed, h->pending_h,
                                               (const bf16*)h->w.talker_e_codec,
                                               (const bf16*)h->w.cp_embeds, Dt, Vc, h->uin);
@@ -270,7 +275,7 @@ static void step_kernels(q3tts_handle* h, int n, int max_ctx, const float* unifo
         launch_split_hilo(h->uin, Dt, hilo(h), M, Dt, s);
         h->launches += 1;
       }
-      proj(h, h->uin, Dt, h->w.cp_w_proj, Dc, Dt, h->cpx, Dc, M, false);
+      proj(h, h->uin, Dt, h->w.cp_w_proj, Dc, Dt, h->cpx, Dc, M, false, h->w.s_cp_proj);
     } else
       cudaMemcpyAsync(h->cpx, h->uin, sizeof(float) * (size_t)M * Dc, cudaMemcpyDeviceToDevice, s);
     TokDesc td = j == 0 ? TokDesc{h->d_tok_stream, h->d_tok_pos, 0} : TokDesc{h->d_sid, nullptr, j + 1};
@@ -278,13 +283,14 @@ static void step_kernels(q3tts_handle* h, int n, int max_ctx, const float* unifo
                Q3TTS_N_CODEBOOKS);
     norm_in(h, h->cpx, Dc, j == 0 ? 2 : 1, j == 0 ? 1 : 0, h->w.cp_g_final, n, Dc);
     const void* head = (const char*)h->w.cp_heads + (size_t)j * Vc * Dc * es;
-    proj(h, h->hb, Dc, head, Vc, Dc, h->logits, Vc, n, false);
+    proj(h, h->hb, Dc, head, Vc, Dc, h->logits, Vc, n, false,
+         h->w.s_cp_heads ? h->w.s_cp_heads + (size_t)j * Vc : nullptr);
     sample_kernel<<<n, 256, smem, s>>>(h->logits, Vc, 0, h->d_sid, h->d_sp, nullptr, h->finished, uniforms,
                                        j + 1, forced, codes, h->d_fed, logits, dump_ld,
                                        Vt + j * Vc, h->d_err);
     h->launches += 4 + (h->w.cp_w_proj ? 1 : 0);
   }
-  if (wdt == Q3TTS_BF16)
+  if (gdt == Q3TTS_BF16)
     embed_sum_kernel<bf16><<<dim3((Dt + 255) / 256, n), 256, 0, s>>>(
         h->d_fed, (const bf16*)h->w.talker_e_codec, (const bf16*)h->w.cp_embeds, Dt, Vc, h->x);
   else
@@ -294,12 +300,12 @@ static void step_kernels(q3tts_handle* h, int n, int max_ctx, const float* unifo
   stack_pass(h, h->tl.data(), h->c.talker_layers, Dt, h->Ft, h->x, n, td, talker_kv(h),
              h->c.kv_dtype, max_ctx);
   // the normed hidden is also the stream's pending h_T (fp32)
-  launch_rmsnorm(wdt, h->x, Dt, 1, 0, h->w.talker_g_final, h->hb, Dt, n, Dt, h->c.rms_eps, s);
+  launch_rmsnorm(gdt, h->x, Dt, 1, 0, h->w.talker_g_final, h->hb, Dt, n, Dt, h->c.rms_eps, s);
   if (h->tc) {
     launch_split_hilo(h->hb, Dt, hilo(h), n, Dt, s);
     h->launches += 1;
   }
-  proj(h, h->hb, Dt, h->w.talker_w_head, Vt, Dt, h->logits, Vt, n, false);
+  proj(h, h->hb, Dt, h->w.talker_w_head, Vt, Dt, h->logits, Vt, n, false, h->w.s_head);
   scatter_pending_kernel<<<n, 256, 0, s>>>(h->d_sid, h->hb, h->logits, Dt, Vt, h->pending_h,
                                            h->pending_logits);
   h->launches += 6;  // setup, semantic sample, embed-sum, final norm, head, scatter

@@ -478,7 +478,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if s.weight_dtype == synth.DTYPE_BF16 else "f32",
+            "dtype": {synth.DTYPE_BF16: "bf16", synth.DTYPE_FP8: "fp8-e4m3 weights"}.get(s.weight_dtype, "f32"),
             "data": "synthetic (random N(0,0.02) weights of the named shapes, N(0,1) prompts, "
                     "seeded uniforms)",
             "rtf": synth.FRAMES_PER_SECOND / (value / world),
