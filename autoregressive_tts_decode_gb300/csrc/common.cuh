@@ -26,6 +26,34 @@ __device__ __forceinline__ void fp8x4_to_f32(uint32_t w, float* f) {
   f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
 }
 
+// Programmatic dependent launch.  A kernel started by launch_pdl may begin
+// while its predecessor on the stream is still running: pdl_wait() blocks
+// until that grid has completed and its memory is visible (a no-op for a
+// kernel launched without the attribute), pdl_trigger() lets the next
+// kernel's CTAs be scheduled (they then wait in their own pdl_wait()).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Whether launch_pdl sets the attribute (Q3TTS_PDL=0 in the environment: plain
+// stream order, for comparison).
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // The storage type of the norm gains and embedding tables of a model whose
 // matrices are WT (bf16 beside FP8 matrices), and whether WT is FP8.
 template <class WT>

@@ -1,7 +1,17 @@
 // layers.cu -- one-kernel-per-operation decoder building blocks (see layers.cuh).
+#include <stdlib.h>
+
 #include "layers.cuh"
 
 namespace q3 {
+
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = getenv("Q3TTS_PDL");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
 
 // ---------------------------------------------------------------- linear
 // Skinny case (few tokens): one warp per output row, eight weights per lane per
@@ -12,6 +22,8 @@ __global__ void __launch_bounds__(256) gemv_kernel(const float* __restrict__ X, 
                                                    const WT* __restrict__ W, int N, int K,
                                                    float* __restrict__ Y, int ldy, int M,
                                                    int accumulate, const float* __restrict__ sc) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -53,6 +65,8 @@ __global__ void __launch_bounds__(256) gemm_kernel(const float* __restrict__ X, 
                                                    const WT* __restrict__ W, int N, int K,
                                                    float* __restrict__ Y, int ldy, int M,
                                                    int accumulate, const float* __restrict__ sc) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   __shared__ float As[16][64 + 4];
   __shared__ float Bs[16][64 + 4];
   const int tid = threadIdx.x;
@@ -100,16 +114,16 @@ static void linear_t(const float* X, int ldx, const WT* W, int N, int K, float* 
     int blocks = (N + 7) / 8;
     if (blocks > 4096) blocks = 4096;
     if (M <= 1)
-      gemv_kernel<WT, 1><<<blocks, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc, sc);
+      launch_pdl(gemv_kernel<WT, 1>, dim3(blocks), dim3(256), 0, s, X, ldx, W, N, K, Y, ldy, M, acc, sc);
     else if (M <= 2)
-      gemv_kernel<WT, 2><<<blocks, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc, sc);
+      launch_pdl(gemv_kernel<WT, 2>, dim3(blocks), dim3(256), 0, s, X, ldx, W, N, K, Y, ldy, M, acc, sc);
     else if (M <= 4)
-      gemv_kernel<WT, 4><<<blocks, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc, sc);
+      launch_pdl(gemv_kernel<WT, 4>, dim3(blocks), dim3(256), 0, s, X, ldx, W, N, K, Y, ldy, M, acc, sc);
     else
-      gemv_kernel<WT, 8><<<blocks, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc, sc);
+      launch_pdl(gemv_kernel<WT, 8>, dim3(blocks), dim3(256), 0, s, X, ldx, W, N, K, Y, ldy, M, acc, sc);
   } else {
     dim3 grid((N + 63) / 64, (M + 63) / 64);
-    gemm_kernel<WT><<<grid, 256, 0, s>>>(X, ldx, W, N, K, Y, ldy, M, acc, sc);
+    launch_pdl(gemm_kernel<WT>, dim3(grid), dim3(256), 0, s, X, ldx, W, N, K, Y, ldy, M, acc, sc);
   }
 }
 
@@ -128,6 +142,8 @@ template <class WT>
 __global__ void rmsnorm_kernel(const float* __restrict__ X, int ldx, int in_mul, int in_add,
                                const WT* __restrict__ g, float* __restrict__ Y, int ldy, int D,
                                float eps) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   __shared__ float red[32];
   const int m = blockIdx.x;
   const float* x = X + (size_t)(m * in_mul + in_add) * ldx;
@@ -148,6 +164,8 @@ template <class WT>
 __global__ void rmsnorm_hilo_kernel(const float* __restrict__ X, int ldx, int in_mul, int in_add,
                                     const WT* __restrict__ g, bf16* __restrict__ hi, bf16* __restrict__ lo,
                                     int D, float eps) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   __shared__ float red[32];
   const int m = blockIdx.x;
   const float* x = X + (size_t)(m * in_mul + in_add) * ldx;
@@ -162,18 +180,18 @@ void launch_rmsnorm_hilo(int wdt, const float* X, int ldx, int in_mul, int in_ad
                          int M, int D, float eps, cudaStream_t s) {
   if (M <= 0) return;
   if (wdt == Q3TTS_BF16)
-    rmsnorm_hilo_kernel<<<M, 256, 0, s>>>(X, ldx, in_mul, in_add, (const bf16*)g, y.hi, y.lo, D, eps);
+    launch_pdl(rmsnorm_hilo_kernel<bf16>, dim3(M), dim3(256), 0, s, X, ldx, in_mul, in_add, (const bf16*)g, y.hi, y.lo, D, eps);
   else
-    rmsnorm_hilo_kernel<<<M, 256, 0, s>>>(X, ldx, in_mul, in_add, (const float*)g, y.hi, y.lo, D, eps);
+    launch_pdl(rmsnorm_hilo_kernel<float>, dim3(M), dim3(256), 0, s, X, ldx, in_mul, in_add, (const float*)g, y.hi, y.lo, D, eps);
 }
 
 void launch_rmsnorm(int wdt, const float* X, int ldx, int in_mul, int in_add, const void* g,
                     float* Y, int ldy, int M, int D, float eps, cudaStream_t s) {
   if (M <= 0) return;
   if (wdt == Q3TTS_BF16)
-    rmsnorm_kernel<<<M, 256, 0, s>>>(X, ldx, in_mul, in_add, (const bf16*)g, Y, ldy, D, eps);
+    launch_pdl(rmsnorm_kernel<bf16>, dim3(M), dim3(256), 0, s, X, ldx, in_mul, in_add, (const bf16*)g, Y, ldy, D, eps);
   else
-    rmsnorm_kernel<<<M, 256, 0, s>>>(X, ldx, in_mul, in_add, (const float*)g, Y, ldy, D, eps);
+    launch_pdl(rmsnorm_kernel<float>, dim3(M), dim3(256), 0, s, X, ldx, in_mul, in_add, (const float*)g, Y, ldy, D, eps);
 }
 
 // ------------------------------------------------ q/k norm + RoPE + append
@@ -184,6 +202,8 @@ __global__ void qk_rope_append_kernel(float* __restrict__ qkv, int ld, TokDesc t
                                       const WT* __restrict__ gq, const WT* __restrict__ gk,
                                       int qk_norm, float eps, const float* __restrict__ rc,
                                       const float* __restrict__ rs, KVDesc kv, int layer, int Hq) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   constexpr int J = HD / 32, P = J / 2, HALF = HD / 2;
   const int m = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nw = blockDim.x >> 5;
@@ -234,10 +254,10 @@ static void qk_rope_t(float* qkv, int ld, int M, TokDesc td, const void* gq, con
                       int qk_norm, float eps, const float* rc, const float* rs, KVDesc kv, int layer,
                       int Hq, cudaStream_t s) {
   if (kv.hd == 128)
-    qk_rope_append_kernel<WT, KT, 128><<<M, 256, 0, s>>>(qkv, ld, td, (const WT*)gq, (const WT*)gk,
+    launch_pdl(qk_rope_append_kernel<WT, KT, 128>, dim3(M), dim3(256), 0, s, qkv, ld, td, (const WT*)gq, (const WT*)gk,
                                                          qk_norm, eps, rc, rs, kv, layer, Hq);
   else
-    qk_rope_append_kernel<WT, KT, 64><<<M, 256, 0, s>>>(qkv, ld, td, (const WT*)gq, (const WT*)gk,
+    launch_pdl(qk_rope_append_kernel<WT, KT, 64>, dim3(M), dim3(256), 0, s, qkv, ld, td, (const WT*)gq, (const WT*)gk,
                                                         qk_norm, eps, rc, rs, kv, layer, Hq);
 }
 
@@ -265,6 +285,8 @@ template <class KT>
 __global__ void __launch_bounds__(128) attention_kernel(const float* __restrict__ qkv, int ld,
                                                         TokDesc td, KVDesc kv, int layer, int Hq,
                                                         float* __restrict__ out, int ldo) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   extern __shared__ float sm[];
   __shared__ float red[32];
   const int m = blockIdx.x, h = blockIdx.y, hd = kv.hd;
@@ -316,6 +338,8 @@ template <class KT>
 __global__ void __launch_bounds__(128) attention_gqa4_kernel(const float* __restrict__ qkv, int ld, TokDesc td,
                                                             KVDesc kv, int layer, int Hq,
                                                             float* __restrict__ out, int ldo) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   constexpr int NW = 4, RMAX = 4;
   extern __shared__ int pt[];  // the stream's page-table row
   __shared__ float qs[RMAX][128];
@@ -436,6 +460,8 @@ template <class KT, int E>
 __global__ void __launch_bounds__(GQA_NW * 32) attention_gqa8_kernel(const float* __restrict__ qkv, int ld,
                                                                     TokDesc td, KVDesc kv, int layer, int Hq,
                                                                     float* __restrict__ out, int ldo) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   constexpr int NW = GQA_NW, B = GQA_B, RMAX = GQA_RMAX;
   extern __shared__ int pt[];  // the stream's page-table row
   __shared__ float wm[NW][RMAX], wl[NW][RMAX];
@@ -577,6 +603,7 @@ __device__ __forceinline__ int split_token(const int* pfx, int M, int idx) {
 
 template <class KT, int HD, int REP>
 __global__ void __launch_bounds__(SPL_WARPS * 32) attention_split_kernel(SplitArgs a) {
+  pdl_wait();  // inputs come from the previous kernel (the next one is let in at the end)
   constexpr int NCH = HD * (int)sizeof(KT) / 32;   // 16-byte loads per lane: its half of a row
   constexpr int EPC = 16 / (int)sizeof(KT);        // elements per load
   constexpr int OPL = HD / 32;                     // output elements per lane
@@ -817,6 +844,7 @@ __global__ void __launch_bounds__(SPL_WARPS * 32) attention_split_kernel(SplitAr
     }
     if (lane == 0) a.cnt[(size_t)m * Hkv + g] = 0;
   }
+  pdl_trigger();
 }
 
 template <class KT, int HD, int REP>
@@ -845,6 +873,9 @@ static bool launch_split_t(const SplitArgs& a, int n_sm, cudaStream_t s) {
     }
   }
   // a persistent grid of one wave: every CTA stays resident and walks items
+  // a plain launch: the grid is one wave of resident CTAs with fixed page
+  // runs, so it must not start beside the previous kernel's CTAs (a CTA that
+  // did not fit would run its whole run a wave late)
   attention_split_kernel<KT, HD, REP><<<n_sm * per_sm, SPL_WARPS * 32, split_smem<KT, HD, REP>(a.M), s>>>(a);
   return true;
 }
@@ -892,32 +923,34 @@ void launch_attention(int kdt, const float* qkv, int ld, int M, TokDesc td, KVDe
     dim3 grid(M, kv.Hkv);
     const int nt = GQA_NW * 32;
     if (bf) {
-      if (kv.hd == 128) attention_gqa8_kernel<bf16, 4><<<grid, nt, pts, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
-      else attention_gqa8_kernel<bf16, 2><<<grid, nt, pts, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
+      if (kv.hd == 128) launch_pdl(attention_gqa8_kernel<bf16, 4>, dim3(grid), dim3(nt), pts, s, qkv, ld, td, kv, layer, Hq, out, ldo);
+      else launch_pdl(attention_gqa8_kernel<bf16, 2>, dim3(grid), dim3(nt), pts, s, qkv, ld, td, kv, layer, Hq, out, ldo);
     } else {
-      if (kv.hd == 128) attention_gqa8_kernel<float, 4><<<grid, nt, pts, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
-      else attention_gqa8_kernel<float, 2><<<grid, nt, pts, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
+      if (kv.hd == 128) launch_pdl(attention_gqa8_kernel<float, 4>, dim3(grid), dim3(nt), pts, s, qkv, ld, td, kv, layer, Hq, out, ldo);
+      else launch_pdl(attention_gqa8_kernel<float, 2>, dim3(grid), dim3(nt), pts, s, qkv, ld, td, kv, layer, Hq, out, ldo);
     }
     return;
   }
   if (kv.hd <= 128 && Hq / kv.Hkv <= 4) {
     dim3 grid(M, kv.Hkv);
     if (bf)
-      attention_gqa4_kernel<bf16><<<grid, 128, pts, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
+      launch_pdl(attention_gqa4_kernel<bf16>, dim3(grid), dim3(128), pts, s, qkv, ld, td, kv, layer, Hq, out, ldo);
     else
-      attention_gqa4_kernel<float><<<grid, 128, pts, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
+      launch_pdl(attention_gqa4_kernel<float>, dim3(grid), dim3(128), pts, s, qkv, ld, td, kv, layer, Hq, out, ldo);
     return;
   }
   dim3 grid(M, Hq);
   size_t smem = sizeof(float) * (size_t)(kv.hd + max_ctx);
   if (kdt == Q3TTS_BF16)
-    attention_kernel<bf16><<<grid, 128, smem, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
+    launch_pdl(attention_kernel<bf16>, dim3(grid), dim3(128), smem, s, qkv, ld, td, kv, layer, Hq, out, ldo);
   else
-    attention_kernel<float><<<grid, 128, smem, s>>>(qkv, ld, td, kv, layer, Hq, out, ldo);
+    launch_pdl(attention_kernel<float>, dim3(grid), dim3(128), smem, s, qkv, ld, td, kv, layer, Hq, out, ldo);
 }
 
 // ---------------------------------------------------------------- SwiGLU
 __global__ void silu_mul_kernel(const float* __restrict__ gu, float* __restrict__ a, int M, int F) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   size_t n = (size_t)M * F;
   for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n;
        e += (size_t)gridDim.x * blockDim.x) {
@@ -931,11 +964,13 @@ void launch_silu_mul(const float* gu, float* a, int M, int F, cudaStream_t s) {
   size_t n = (size_t)M * F;
   int blocks = (int)((n + 255) / 256);
   if (blocks > 8192) blocks = 8192;
-  silu_mul_kernel<<<blocks, 256, 0, s>>>(gu, a, M, F);
+  launch_pdl(silu_mul_kernel, dim3(blocks), dim3(256), 0, s, gu, a, M, F);
 }
 
 __global__ void silu_mul_hilo_kernel(const float* __restrict__ gu, bf16* __restrict__ hi, bf16* __restrict__ lo,
                                      int M, int F) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   size_t n = (size_t)M * F;
   for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n;
        e += (size_t)gridDim.x * blockDim.x) {
@@ -949,7 +984,7 @@ void launch_silu_mul_hilo(const float* gu, const HiLo& a, int M, int F, cudaStre
   size_t n = (size_t)M * F;
   int blocks = (int)((n + 255) / 256);
   if (blocks > 8192) blocks = 8192;
-  silu_mul_hilo_kernel<<<blocks, 256, 0, s>>>(gu, a.hi, a.lo, M, F);
+  launch_pdl(silu_mul_hilo_kernel, dim3(blocks), dim3(256), 0, s, gu, a.hi, a.lo, M, F);
 }
 
 }  // namespace q3

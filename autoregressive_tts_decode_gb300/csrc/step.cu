@@ -42,6 +42,8 @@ KVDesc cp_kv(const q3tts_handle* h) {
 
 __global__ void setup_kernel(const StepDesc* __restrict__ dd, int* sid, int* pos, q3tts_sampling* sp,
                              int* page_table, int pps, int page_size, int* tok_stream, int* tok_pos) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   const StepDesc& d = *dd;
   for (int b = threadIdx.x; b < d.n; b += blockDim.x) {
     sid[b] = d.sid[b];
@@ -57,6 +59,8 @@ __global__ void setup_kernel(const StepDesc* __restrict__ dd, int* sid, int* pos
 }
 
 __global__ void fill_tokens_kernel(int* tok_stream, int* tok_pos, int T, int sid, int pos0) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   for (int m = blockIdx.x * blockDim.x + threadIdx.x; m < T; m += gridDim.x * blockDim.x) {
     tok_stream[m] = sid;
     tok_pos[m] = pos0 + m;
@@ -77,6 +81,8 @@ __global__ void __launch_bounds__(256) sample_kernel(
     const float* __restrict__ uniforms, int cb, const int32_t* __restrict__ forced,
     int32_t* __restrict__ codes, int* __restrict__ fed, float* __restrict__ dump, int dump_ld, int dump_off,
     int* err) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   extern __shared__ __align__(16) unsigned char smraw[];
   SamplerSmem& sm = *reinterpret_cast<SamplerSmem*>(smraw);
   const int b = blockIdx.x, s = sid[b];
@@ -120,6 +126,8 @@ __global__ void cp_input_kernel(int j, int n, const int* __restrict__ sid,
                                 const int* __restrict__ fed, const float* __restrict__ pending_h,
                                 const WT* __restrict__ e_codec, const WT* __restrict__ cp_embeds,
                                 int Dt, int Vc, float* __restrict__ uin) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   const int r = blockIdx.x;  // output row
   const float* srcf = nullptr;
   const WT* srcw = nullptr;
@@ -140,6 +148,8 @@ template <class WT>
 __global__ void embed_sum_kernel(const int* __restrict__ fed, const WT* __restrict__ e_codec,
                                  const WT* __restrict__ cp_embeds, int Dt, int Vc,
                                  float* __restrict__ x) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   const int b = blockIdx.y;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= Dt) return;
@@ -153,6 +163,8 @@ __global__ void scatter_pending_kernel(const int* __restrict__ sid, const float*
                                        const float* __restrict__ lg, int Dt, int Vt,
                                        float* __restrict__ pending_h,
                                        float* __restrict__ pending_logits) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   const int b = blockIdx.x, s = sid[b];
   for (int i = threadIdx.x; i < Dt; i += blockDim.x)
     pending_h[(size_t)s * Dt + i] = hn[(size_t)b * Dt + i];
@@ -226,7 +238,7 @@ int prefill_layered(q3tts_handle* h, int sid, const float* embeds, int len) {
     int T = len - c0 < h->chunk ? len - c0 : h->chunk;
     cudaMemcpyAsync(h->x, embeds + (size_t)c0 * Dt, sizeof(float) * (size_t)T * Dt,
                     cudaMemcpyDeviceToDevice, s);
-    fill_tokens_kernel<<<(T + 255) / 256, 256, 0, s>>>(h->d_tok_stream, h->d_tok_pos, T, sid, c0);
+    launch_pdl(fill_tokens_kernel, dim3((T + 255) / 256), dim3(256), 0, s, h->d_tok_stream, h->d_tok_pos, T, sid, c0);
     h->launches += 1;
     TokDesc td{h->d_tok_stream, h->d_tok_pos, 0};
     stack_pass(h, h->tl.data(), h->c.talker_layers, Dt, h->Ft, h->x, T, td, talker_kv(h),
@@ -254,20 +266,20 @@ static void step_kernels(q3tts_handle* h, int n, int max_ctx, const float* unifo
   const int Dt = h->Dt, Dc = h->Dc, Vt = h->Vt, Vc = h->Vc, gdt = gain_dt(h);
   const int dump_ld = Vt + (Q3TTS_N_CODEBOOKS - 1) * Vc;
   const size_t smem = sizeof(SamplerSmem);
-  setup_kernel<<<1, 256, 0, s>>>(h->d_desc, h->d_sid, h->d_pos, h->d_sp, h->page_table, h->pps,
+  launch_pdl(setup_kernel, dim3(1), dim3(256), 0, s, h->d_desc, h->d_sid, h->d_pos, h->d_sp, h->page_table, h->pps,
                                  h->c.page_size, h->d_tok_stream, h->d_tok_pos);
-  sample_kernel<<<n, 256, smem, s>>>(h->pending_logits, Vt, 1, h->d_sid, h->d_sp, h->history, h->finished,
+  launch_pdl(sample_kernel, dim3(n), dim3(256), smem, s, h->pending_logits, Vt, 1, h->d_sid, h->d_sp, h->history, h->finished,
                                      uniforms, 0, forced, codes, h->d_fed, logits, dump_ld, 0,
                                      h->d_err);
   const size_t es = wbytes(h);
   for (int j = 0; j < Q3TTS_N_CODEBOOKS - 1; ++j) {
     const int M = j == 0 ? 2 * n : n;
     if (gdt == Q3TTS_BF16)
-      cp_input_kernel<bf16><<<M, 256, 0, s>>>(j, n, h->d_sid, h->d_fed, h->pending_h,
+      launch_pdl(cp_input_kernel<bf16>, dim3(M), dim3(256), 0, s, j, n, h->d_sid, h->d_fed, h->pending_h,
                                               (const bf16*)h->w.talker_e_codec,
                                               (const bf16*)h->w.cp_embeds, Dt, Vc, h->uin);
     else
-      cp_input_kernel<float><<<M, 256, 0, s>>>(j, n, h->d_sid, h->d_fed, h->pending_h,
+      launch_pdl(cp_input_kernel<float>, dim3(M), dim3(256), 0, s, j, n, h->d_sid, h->d_fed, h->pending_h,
                                                (const float*)h->w.talker_e_codec,
                                                (const float*)h->w.cp_embeds, Dt, Vc, h->uin);
     if (h->w.cp_w_proj) {
@@ -285,16 +297,16 @@ static void step_kernels(q3tts_handle* h, int n, int max_ctx, const float* unifo
     const void* head = (const char*)h->w.cp_heads + (size_t)j * Vc * Dc * es;
     proj(h, h->hb, Dc, head, Vc, Dc, h->logits, Vc, n, false,
          h->w.s_cp_heads ? h->w.s_cp_heads + (size_t)j * Vc : nullptr);
-    sample_kernel<<<n, 256, smem, s>>>(h->logits, Vc, 0, h->d_sid, h->d_sp, nullptr, h->finished, uniforms,
+    launch_pdl(sample_kernel, dim3(n), dim3(256), smem, s, h->logits, Vc, 0, h->d_sid, h->d_sp, nullptr, h->finished, uniforms,
                                        j + 1, forced, codes, h->d_fed, logits, dump_ld,
                                        Vt + j * Vc, h->d_err);
     h->launches += 4 + (h->w.cp_w_proj ? 1 : 0);
   }
   if (gdt == Q3TTS_BF16)
-    embed_sum_kernel<bf16><<<dim3((Dt + 255) / 256, n), 256, 0, s>>>(
+    launch_pdl(embed_sum_kernel<bf16>, dim3(dim3((Dt + 255) / 256, n)), dim3(256), 0, s, 
         h->d_fed, (const bf16*)h->w.talker_e_codec, (const bf16*)h->w.cp_embeds, Dt, Vc, h->x);
   else
-    embed_sum_kernel<float><<<dim3((Dt + 255) / 256, n), 256, 0, s>>>(
+    launch_pdl(embed_sum_kernel<float>, dim3(dim3((Dt + 255) / 256, n)), dim3(256), 0, s, 
         h->d_fed, (const float*)h->w.talker_e_codec, (const float*)h->w.cp_embeds, Dt, Vc, h->x);
   TokDesc td{h->d_sid, h->d_pos, 0};
   stack_pass(h, h->tl.data(), h->c.talker_layers, Dt, h->Ft, h->x, n, td, talker_kv(h),
@@ -306,7 +318,7 @@ static void step_kernels(q3tts_handle* h, int n, int max_ctx, const float* unifo
     h->launches += 1;
   }
   proj(h, h->hb, Dt, h->w.talker_w_head, Vt, Dt, h->logits, Vt, n, false, h->w.s_head);
-  scatter_pending_kernel<<<n, 256, 0, s>>>(h->d_sid, h->hb, h->logits, Dt, Vt, h->pending_h,
+  launch_pdl(scatter_pending_kernel, dim3(n), dim3(256), 0, s, h->d_sid, h->hb, h->logits, Dt, Vt, h->pending_h,
                                            h->pending_logits);
   h->launches += 6;  // setup, semantic sample, embed-sum, final norm, head, scatter
 }

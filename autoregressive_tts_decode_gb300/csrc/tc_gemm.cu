@@ -206,6 +206,8 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the set-up above overlaps the previous kernel; its outputs are read below
+  pdl_wait();
 
   if (threadIdx.x == 0) {
     // producer
@@ -255,7 +257,9 @@ __global__ void __launch_bounds__(128, 1)
   }
   __syncwarp();
 
-  // epilogue: warp w holds weight rows n0 + 32 w + lane, all NT token columns
+  // epilogue: warp w holds weight rows n0 + 32 w + lane, all NT token columns;
+  // the next kernel may start its set-up meanwhile
+  pdl_trigger();
   bool ok = tc_wait(done, 0u, abort_w, a.err);
   ok = __all_sync(0xffffffffu, ok) && !*abort_w;
   tc_fence_after();
@@ -373,13 +377,15 @@ bool launch_nt(const CUtensorMap& wm, const HiLo& x, int N, int K, float* Y, int
   if (splits > 1 && !acc &&
       cudaMemset2DAsync(Y, (size_t)ldy * sizeof(float), 0, (size_t)N * sizeof(float), M, s) != cudaSuccess)
     return false;
-  tc_gemm_kernel<NT><<<dim3(nrb, splits, ntt), 128, C::SMEM, s>>>(wm, hm, lm, args);
+  launch_pdl(tc_gemm_kernel<NT>, dim3(nrb, splits, ntt), dim3(128), C::SMEM, s, wm, hm, lm, args);
   return cudaPeekAtLastError() == cudaSuccess;
 }
 
 // X = hi + lo, hi = bf16(x), lo = bf16(x - hi)
 __global__ void split_hilo_kernel(const float* __restrict__ X, int ldx, bf16* __restrict__ hi,
                                   bf16* __restrict__ lo, int M, int K) {
+  pdl_wait();  // inputs come from the previous kernel
+  pdl_trigger();
   const int m = blockIdx.y;
   for (int k = (blockIdx.x * blockDim.x + threadIdx.x) * 4; k < K; k += gridDim.x * blockDim.x * 4) {
     const float4 v = *reinterpret_cast<const float4*>(X + (size_t)m * ldx + k);
@@ -438,7 +444,7 @@ bool tc_linear(const HiLo& x, const void* W, int N, int K, float* Y, int ldy, in
 void launch_split_hilo(const float* X, int ldx, const HiLo& x, int M, int K, cudaStream_t s) {
   if (M <= 0) return;
   int bx = (K / 4 + 255) / 256;
-  split_hilo_kernel<<<dim3(bx, M), 256, 0, s>>>(X, ldx, x.hi, x.lo, M, K);
+  launch_pdl(split_hilo_kernel, dim3(dim3(bx, M)), dim3(256), 0, s, X, ldx, x.hi, x.lo, M, K);
 }
 
 }  // namespace q3
