@@ -86,7 +86,9 @@ Dims dims_of(const q3tts_config& c) {
   d.pps = (c.kv_cap_steps + c.page_size - 1) / c.page_size;
   d.S = c.max_streams;
   d.n_pages = c.kv_pages > 0 ? c.kv_pages : d.pps * d.S;
-  d.chunk = c.prefill_chunk > 0 ? c.prefill_chunk : 256;
+  // default prefill chunk: up to 1024 positions (long prompts read the
+  // weights fewer times and give the attention more query tiles per launch)
+  d.chunk = c.prefill_chunk > 0 ? c.prefill_chunk : std::min(std::max(c.kv_cap_steps, 16), 1024);
   d.m_max = std::max(d.chunk, 2 * d.S);
   d.esz = c.weight_dtype == Q3TTS_F32 ? 4 : (c.weight_dtype == Q3TTS_FP8 ? 1 : 2);  // matrix elements
   d.kvesz = c.kv_dtype == Q3TTS_F32 ? 4 : 2;

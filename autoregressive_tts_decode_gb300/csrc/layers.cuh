@@ -51,6 +51,15 @@ bool launch_attention_split(int kdt, const float* qkv, int ld, int M, TokDesc td
                             float* out, int ldo, float* part, int* cnt, int nsmax, cudaStream_t s);
 int attention_split_spans(int kv_cap);
 
+// Causal attention of a prefill chunk on the tensor cores (fa_prefill.cu):
+// tokens t < T of one stream at positions pos0 + t, whose k and v are already
+// in the cache; bf16 cache, hd 128, two q heads per kv head, pages of 16.
+// err receives Q3TTS_ERR_TIMEOUT if a bounded wait runs out.  False if the
+// shape is not one it takes (nothing launched).
+bool fa_prefill_ok(const KVDesc& kv, int kdt, int Hq);
+bool launch_fa_prefill(const float* qkv, int ld, int T, int stream, int pos0, KVDesc kv, int kdt, int layer, int Hq,
+                       float* out, int ldo, int* err, cudaStream_t s);
+
 // a[m, f] = silu(gu[m, f]) * gu[m, F + f]
 void launch_silu_mul(const float* gu, float* a, int M, int F, cudaStream_t s);
 

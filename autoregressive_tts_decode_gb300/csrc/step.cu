@@ -202,8 +202,11 @@ static void norm_in(q3tts_handle* h, const float* X, int ldx, int in_mul, int in
 }
 
 // M tokens through all layers of one decoder stack (residual stream x [M, D]).
+// pf_sid >= 0: the tokens are a prefill chunk of stream pf_sid at positions
+// pf_pos0 .. pf_pos0 + M - 1.
 static void stack_pass(q3tts_handle* h, const q3tts_layer_weights* lw, int layers, int D, int F,
-                       float* x, int M, TokDesc td, KVDesc kv, int kdt, int max_ctx) {
+                       float* x, int M, TokDesc td, KVDesc kv, int kdt, int max_ctx, int pf_sid = -1,
+                       int pf_pos0 = 0) {
   cudaStream_t s = h->s;
   const int gdt = gain_dt(h), HqD = h->Hq * h->hd;
   for (int l = 0; l < layers; ++l) {
@@ -212,9 +215,12 @@ static void stack_pass(q3tts_handle* h, const q3tts_layer_weights* lw, int layer
     proj(h, h->hb, D, L.w_qkv, h->qkv_rows, D, h->qkv, h->qkv_rows, M, false, L.s_qkv);
     launch_qk_rope_append(gdt, kdt, h->qkv, h->qkv_rows, M, td, L.g_q_norm, L.g_k_norm,
                           h->c.qk_norm, h->c.rms_eps, h->rope_cos, h->rope_sin, kv, l, h->Hq, s);
-    // contexts longer than one span: spread over the GPU by span
-    if (max_ctx <= 64 || !launch_attention_split(kdt, h->qkv, h->qkv_rows, M, td, kv, l, h->Hq, h->att, HqD,
-                                                 h->spl_part, h->spl_cnt, h->spl_nsmax, s))
+    // a prefill chunk: query tiles on the tensor cores; contexts longer than
+    // one span: spread over the GPU by span
+    const bool fa = pf_sid >= 0 && launch_fa_prefill(h->qkv, h->qkv_rows, M, pf_sid, pf_pos0, kv, kdt, l, h->Hq,
+                                                      h->att, HqD, h->d_err, s);
+    if (!fa && (max_ctx <= 64 || !launch_attention_split(kdt, h->qkv, h->qkv_rows, M, td, kv, l, h->Hq, h->att,
+                                                         HqD, h->spl_part, h->spl_cnt, h->spl_nsmax, s)))
       launch_attention(kdt, h->qkv, h->qkv_rows, M, td, kv, l, h->Hq, h->att, HqD, max_ctx, s);
     if (h->tc) launch_split_hilo(h->att, HqD, hilo(h), M, HqD, s);
     proj(h, h->att, HqD, L.w_o, D, HqD, x, D, M, true, L.s_o);
@@ -242,7 +248,7 @@ int prefill_layered(q3tts_handle* h, int sid, const float* embeds, int len) {
     h->launches += 1;
     TokDesc td{h->d_tok_stream, h->d_tok_pos, 0};
     stack_pass(h, h->tl.data(), h->c.talker_layers, Dt, h->Ft, h->x, T, td, talker_kv(h),
-               h->c.kv_dtype, c0 + T);
+               h->c.kv_dtype, c0 + T, sid, c0);
     if (c0 + T == len) {
       launch_rmsnorm(gain_dt(h), h->x, Dt, 1, T - 1, h->w.talker_g_final,
                      h->pending_h + (size_t)sid * Dt, Dt, 1, Dt, h->c.rms_eps, s);

@@ -350,17 +350,22 @@ bool launch_nt(const CUtensorMap& wm, const HiLo& x, int N, int K, float* Y, int
   // CTAs resident per SM at this stage count (TMEM holds 512 columns)
   const int per_sm = (int)std::min<size_t>(228 * 1024 / (C::SMEM + 1024), 512 / C::TMEM_COLS);
   const int slots = std::max(1, per_sm) * n_sm;
-  // K split: the fewest splits that minimise (waves of CTAs) x (k blocks per
-  // CTA), the critical path when every k block costs about the same
+  // K split, only when the output tiles alone leave SMs idle: the fewest
+  // splits that minimise (waves of CTAs) x (k blocks per CTA + c), c standing
+  // for a CTA's fixed costs in k blocks (set-up, pipeline fill, and the
+  // read-back and atomic adds of its 128 x NT outputs, repeated per split)
   int splits = 1;
-  long best = -1;
-  for (int sp = 1; sp <= nkb; ++sp) {
-    const int per = (nkb + sp - 1) / sp;
-    const long ctas = (long)nrb * ntt * ((nkb + per - 1) / per);
-    const long cost = ((ctas + slots - 1) / slots) * per;
-    if (best < 0 || cost < best) {
-      best = cost;
-      splits = sp;
+  if ((long)nrb * ntt < slots) {
+    constexpr int c = 2 + NT / 32;
+    long best = -1;
+    for (int sp = 1; sp <= nkb; ++sp) {
+      const int per = (nkb + sp - 1) / sp;
+      const long ctas = (long)nrb * ntt * ((nkb + per - 1) / per);
+      const long cost = ((ctas + slots - 1) / slots) * (per + c);
+      if (best < 0 || cost < best) {
+        best = cost;
+        splits = sp;
+      }
     }
   }
   const int kb_per = (nkb + splits - 1) / splits;

@@ -72,7 +72,7 @@ extern "C" {
  * (max_cache_steps); the KV cache is paged in pages of page_size positions
  * drawn from a pool of kv_pages pages shared by all streams (0 = enough for
  * max_streams full streams).  prefill_chunk bounds the positions one prefill
- * launch processes (0 = 256). */
+ * launch processes (0 = min(kv_cap_steps, 1024)). */
 typedef struct q3tts_config {
   int talker_layers, talker_hidden, talker_ffn;
   int cp_layers, cp_hidden, cp_ffn;

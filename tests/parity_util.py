@@ -85,14 +85,20 @@ def sampler_replay(oracle_mod, shape, sampling, codes, logits, fed, uniforms):
     return bad
 
 
-def logits_report(gpu_logits, ora_logits, shape):
-    """(max abs error, argmax agreement over all 16 draws per frame)."""
+def logits_report(gpu_logits, ora_logits, shape, tie=3e-2):
+    """(max abs error, argmax agreement over all 16 draws per frame).  A draw
+    whose two argmaxes differ counts as agreeing when the oracle's logits at
+    them are within 2 * tie of each other: each logit may be off by the
+    tolerance, so a gap that small does not fix the argmax (a near-tie, where
+    float reassociation from run to run may pick either)."""
     Vt, Vc = shape.codec_vocab, shape.cp_vocab
     err = float(np.max(np.abs(gpu_logits - ora_logits)))
     agree, total = 0, 0
     for f in range(gpu_logits.shape[0]):
         segs = [(0, Vt)] + [(Vt + j * Vc, Vt + (j + 1) * Vc) for j in range(15)]
         for a, b in segs:
-            agree += int(np.argmax(gpu_logits[f, a:b]) == np.argmax(ora_logits[f, a:b]))
+            g, o = int(np.argmax(gpu_logits[f, a:b])), int(np.argmax(ora_logits[f, a:b]))
+            near_tie = abs(float(ora_logits[f, a + g]) - float(ora_logits[f, a + o])) <= 2 * tie
+            agree += int(g == o or near_tie)
             total += 1
     return err, agree / total

@@ -295,3 +295,34 @@ def test_long_contexts_split_attention(q3, oracle_mod, tiny_weights, kv):
         err, agree = pu.logits_report(logits[b], ol, shape)
         assert err < tol and agree == 1.0, (lens[b], err, agree)
         assert pu.sampler_replay(oracle_mod, shape, sp, codes[b], logits[b], codes[b], u[b]) == 0
+
+
+def test_prefill_tensor_core_attention_17b_bf16_cache(q3, oracle_mod):
+    """Chunked prefill at the 1.7B shapes with a bf16 cache: the causal attention
+    of each chunk runs as 64-token query tiles on the tensor cores.  A 300-position
+    prompt in chunks of 128 (later chunks start past position 0, the last query
+    tile is ragged) against the oracle with the bf16 cache: pending hidden and
+    logits after the prompt, and two teacher-forced frames."""
+    import torch
+    wl = synth.WORKLOADS["1.7b"]
+    s = synth.SHAPE_17B_KV16
+    W, Wd = pu.gpu_weights(s, gen_device="cuda")
+    p = synth.make_prompts(s, [300])[0]
+    eng = q3.Engine(s, Wd, max_streams=1, kv_cap=512, prefill_chunk=128)
+    eng.prefill(0, p.cuda())
+    hp, lp = eng.read_pending(0)
+    hp, lp = hp.cpu().numpy(), lp.cpu().numpy()
+    u = synth.uniforms([0], 2)
+    codes, logits = pu.run_gpu(eng, [0], [p], wl.sampling, 2, uniforms=u)
+    eng.close()
+    del Wd
+    torch.cuda.empty_cache()
+    orc = oracle_mod.Oracle(s, W, 1, 512, kv_bf16=True)
+    orc.prefill(0, p.numpy())
+    oh, ol0 = orc.pending(0)
+    assert np.max(np.abs(lp - ol0)) < TOL_BF16, np.max(np.abs(lp - ol0))
+    assert np.max(np.abs(hp - oh)) < 0.05, np.max(np.abs(hp - oh))
+    oc, ol = pu.run_oracle(orc, 0, p.numpy(), wl.sampling, 2, forced=codes[0], uniforms=u[0])
+    err, agree = pu.logits_report(logits[0], ol, s)
+    assert err < TOL_BF16, err
+    assert agree >= 0.995, agree
