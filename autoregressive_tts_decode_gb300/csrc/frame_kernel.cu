@@ -208,6 +208,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, unsigned parity) {
   return ok != 0;
 }
 
+#ifdef Q3TTS_TRACE
+// Whether the phase has completed, without suspending the thread.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* b, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+#endif
+
 // As mbar_try_wait, but the thread may be suspended up to about `ns`
 // nanoseconds while the phase is incomplete (woken early when it completes),
 // so a waiting thread issues few instructions.
@@ -342,6 +356,7 @@ struct AttnScratch {
   float o[FK_CONSUMER_WARPS][FK_PAIRS][FK_HDMAX];
   float q[FK_PAIRS][FK_HDMAX];
   float kcur[FK_PAIRS][FK_HDMAX];  // current-position keys (token, kv group), normalised and rotated
+  float vcur[FK_PAIRS][FK_HDMAX];  // current-position values (token, kv group)
 };
 static_assert(FK_PAIRS >= FK_REPMAX, "talker attention keeps one partial per q head of a group");
 
@@ -395,6 +410,7 @@ struct FKSmem {
   ConsState cs[FK_CONSUMER_WARPS];
 #ifdef Q3TTS_TRACE
   int trace_n;
+  long long trace_wait;  // clock64 cycles consumer thread 0 spent in ring waits this step
 #endif
 };
 static_assert(sizeof(FKSmem) <= 227 * 1024, "persistent kernel shared memory");
@@ -423,16 +439,12 @@ __device__ __forceinline__ const FKParams* fk_prm() { return &fk_sm()->prm; }
 __device__ __forceinline__ size_t kv_row(const KVDesc& d, int page, int layer, int slot, int kv, int head) {
   return ((((size_t)layer * d.n_pages + page) * 2 + kv) * d.Hkv + head) * d.page_size * d.hd + (size_t)slot * d.hd;
 }
-// Page and slot of a position (pages of a power-of-two size by shift and mask).
+// Page and slot of a position (the persistent kernel takes power-of-two page
+// sizes only, so a shift and a mask, with no division code in the kernel).
 __device__ __forceinline__ void page_slot(const KVDesc& d, int pos, int& pi, int& slot) {
   const int ps = d.page_size;
-  if ((ps & (ps - 1)) == 0) {
-    pi = pos >> (__ffs(ps) - 1);
-    slot = pos & (ps - 1);
-  } else {
-    pi = pos / ps;
-    slot = pos - pi * ps;
-  }
+  pi = pos >> (__ffs(ps) - 1);
+  slot = pos & (ps - 1);
 }
 __device__ __forceinline__ size_t tkv_offset(const FKParams& p, int layer, int pos, int kv, int head) {
   const KVDesc& d = p.tkv;
@@ -442,10 +454,11 @@ __device__ __forceinline__ size_t tkv_offset(const FKParams& p, int layer, int p
                                                      : __ldcg(d.page_table + p.sid * d.pages_per_stream + pi);
   return kv_row(d, page, layer, slot, kv, head);
 }
-__device__ __forceinline__ size_t ckv_offset(const FKParams& p, int layer, int pos, int kv, int head) {
-  int pi, slot;
-  page_slot(p.ckv, pos, pi, slot);
-  return kv_row(p.ckv, fk_sm()->cpage, layer, slot, kv, head);
+// The CodePredictor cache holds a stream's 16 positions in one page: the k
+// (kv = 0) or v row of position pos of kv group `head` is pos * hd past the
+// row of position 0.
+__device__ __forceinline__ size_t ckv_base(const FKParams& p, int layer, int kv, int head) {
+  return kv_row(p.ckv, fk_sm()->cpage, layer, 0, kv, head);
 }
 __device__ __forceinline__ int ctid() { return (int)threadIdx.x - FK_PRODUCER_THREADS; }
 __device__ __forceinline__ int cwarp() { return ctid() >> 5; }
@@ -663,11 +676,16 @@ __device__ __forceinline__ uint32_t chunk_wait(Stream& s, uint32_t n) {
   const uint32_t slot = n % FK_NSTAGE;
   if (!s.aborted) {
     const unsigned par = (n / FK_NSTAGE) & 1u;
-    if (!__all_sync(0xffffffffu, mbar_try_wait(&sm->full[slot], par))) {
-      FK_MARK(TR_WAIT0, (int)n);
+#ifdef Q3TTS_TRACE
+    // profiling builds test without suspending, so that the wait is seen
+    const long long tw = clock64();
+    if (!__all_sync(0xffffffffu, mbar_test_wait(&sm->full[slot], par)))
       s.aborted = chunk_wait_slow(soff(&sm->full[slot]), par);
-      FK_MARK(TR_WAIT1, (int)n);
-    }
+    if (ctid() == 0) sm->trace_wait += clock64() - tw;
+#else
+    if (!__all_sync(0xffffffffu, mbar_try_wait(&sm->full[slot], par)))
+      s.aborted = chunk_wait_slow(soff(&sm->full[slot]), par);
+#endif
   }
   return soff(sm->ring[slot]);
 }
@@ -758,10 +776,12 @@ struct RowsOut {
 
 // Rows base + r0 .. base + r0 + NR - 1 of a chunk (row stride rb) against T
 // tokens, inv_t (row . x_t) stored by lane r T + t (the stores go out
-// together).
+// together) for the nv (<= NR) rows that exist.  The others are computed on
+// whatever their shared-memory bytes hold (still inside the CTA's shared
+// memory) and not stored: one row-group shape serves every chunk.
 template <class WT, int T, int NR>
 __device__ __forceinline__ void rows_group(uint32_t buf, int rb, int r0, int K, uint32_t xs, int lane,
-                                           const RowsOut& o, int base, const float (&inv)[T]) {
+                                           const RowsOut& o, int base, const float (&inv)[T], int nv) {
   uint32_t ro[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) ro[r] = (uint32_t)((r0 + r) * rb);
@@ -771,7 +791,7 @@ __device__ __forceinline__ void rows_group(uint32_t buf, int rb, int r0, int K, 
   for (int r = 0; r < NR; ++r)
 #pragma unroll
     for (int t = 0; t < T; ++t)
-      if (lane == r * T + t) {
+      if (lane == r * T + t && r < nv) {
         const int i = t * o.ts + base + r0 + r;
         float v = acc[r][t] * inv[t];
         if constexpr (kFp8<WT>) v *= __ldg(o.sc + base + r0 + r);
@@ -785,8 +805,8 @@ __device__ __forceinline__ void rows_group(uint32_t buf, int rb, int r0, int K, 
 // Rows [r0, r1) of a row-major [*, K] matrix streamed from the ring (the
 // private chunks the producer cut them into) against T staged vectors at
 // shared offset xs: output row of token t = inv_t (row . x_t), placed as o
-// says.  A chunk's rows go in groups of 4, then 2, then 1.  Advances the ring
-// position past the rows' chunks.
+// says.  A chunk's rows go in pairs (a ragged last row alone).  Advances the
+// ring position past the rows' chunks.
 template <class WT, int T>
 __device__ __forceinline__ void stream_rows_t(Cons c, int r0, int r1, int K, uint32_t xs, const RowsOut& o,
                                               const float (&inv)[T]) {
@@ -798,13 +818,8 @@ __device__ __forceinline__ void stream_rows_t(Cons c, int r0, int r1, int K, uin
   for (uint32_t n = first_chunk(n0, s.warp); n < n0 + nch; n += FK_CONSUMER_WARPS) {
     const uint32_t buf = chunk_wait(s, n);
     const int base = r0 + (int)(n - n0) * rpc, R = min(rpc, r1 - base);
-    int r = 0;
-    for (; r + 4 <= R; r += 4) rows_group<WT, T, 4>(buf, rb, r, K, xs, s.lane, o, base, inv);
-    if (r + 2 <= R) {
-      rows_group<WT, T, 2>(buf, rb, r, K, xs, s.lane, o, base, inv);
-      r += 2;
-    }
-    if (r < R) rows_group<WT, T, 1>(buf, rb, r, K, xs, s.lane, o, base, inv);
+#pragma unroll 1
+    for (int r = 0; r < R; r += 2) rows_group<WT, T, 2>(buf, rb, r, K, xs, s.lane, o, base, inv, R - r);
     release_private(s, n);
   }
   warp_set(cst().aborted, s.aborted ? 1 : 0);
@@ -1195,31 +1210,19 @@ __device__ __forceinline__ void oproj_step(Cons c, int D, int T, int k, const fl
     const uint32_t buf = chunk_wait(s, n);
     const int ti = t0 + (int)(n - n0), h = ti / nt, col = (ti - h * nt) * 32 + s.lane;
     const uint32_t w = buf + (uint32_t)(s.lane * 8 * (int)sizeof(WT));
-    float a[FK_TMAX];
-#pragma unroll
-    for (int t = 0; t < FK_TMAX; ++t) {
-      a[t] = 0.f;
-      if (t < T) {
-        const uint32_t xo = os0 + (uint32_t)(h - h_first) * OS_HEAD + (uint32_t)t * OS_TOK;
-        float u = 0.f, v = 0.f;
+    float sc = 1.f;
+    if constexpr (kFp8<WT>) sc = col < D ? __ldg(so + col) : 0.f;  // W_o row (output column) scale
+#pragma unroll 1
+    for (int t = 0; t < T; ++t) {
+      const uint32_t xo = os0 + (uint32_t)(h - h_first) * OS_HEAD + (uint32_t)t * OS_TOK;
+      float u = 0.f, v = 0.f;
 #pragma unroll 4
-        for (int kb = 0; kb < nkb; ++kb)
-          fma8<WT>(w + (uint32_t)(kb * 256 * (int)sizeof(WT)), lds_f4(xo + (uint32_t)(kb * 16)),
-                   lds_f4(xo + (uint32_t)(2 * hd + kb * 16)), u, v);
-        a[t] = u + v;
-      }
+      for (int kb = 0; kb < nkb; ++kb)
+        fma8<WT>(w + (uint32_t)(kb * 256 * (int)sizeof(WT)), lds_f4(xo + (uint32_t)(kb * 16)),
+                 lds_f4(xo + (uint32_t)(2 * hd + kb * 16)), u, v);
+      if (col < D) atomicAdd(XA + t * D + col, (u + v) * sc);
     }
     release_private(s, n);
-    if (col < D) {
-      if constexpr (kFp8<WT>) {  // W_o row (output column) scale
-        const float sc = __ldg(so + col);
-#pragma unroll
-        for (int t = 0; t < FK_TMAX; ++t) a[t] *= sc;
-      }
-#pragma unroll
-      for (int t = 0; t < FK_TMAX; ++t)
-        if (t < T) atomicAdd(XA + t * D + col, a[t]);
-    }
   }
   warp_set(cst().aborted, s.aborted ? 1 : 0);
   warp_set(cst().n, n0 + nch);
@@ -1233,9 +1236,13 @@ __device__ __forceinline__ void store_head_plane(float* dst, int hd, const float
 
 // CodePredictor phase B: attention of the CTA's one or two heads for each of
 // the pass's tokens over positions 0..pos0+t (at most 16), then o_proj.
-// Positions are spread over the warps (K/V loads issued up front), partial
-// softmax sums are combined across warps.  The CTA owning column 0 of the
-// first q head of a kv group appends that group's current k, v to the cache.
+// Warp w takes positions w and w + 8: their cached K/V rows are loaded first,
+// into registers, so that the loads are in flight while the q and current k
+// rows are resolved; per-warp partial softmax sums are combined across warps.
+// The CTA owning column 0 of the first q head of a kv group appends that
+// group's current k, v to the cache.  The loops over pairs and positions are
+// not unrolled: this phase runs once per layer and pass, and its code has to
+// stay in the instruction cache with the rest of the pass.
 template <class WT>
 __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0, int k, uint32_t qtag) {
   const FKParams& p = *fk_prm();
@@ -1250,106 +1257,71 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
   const int ng = nh ? h_last / rep - g_first + 1 : 0;  // kv groups touched (<= 2)
   AttnScratch& as = fk_sm()->u.att;
   const float scale = 1.0f / sqrtf((float)hd);
-  const int S = pos0 + T;  // positions 0..S-1 exist after this pass
-  // 0) this warp's positions (warp, warp + 8): v of every touched kv group
-  //    and k of the cached positions, loaded first -- none of it depends on
-  //    step 1, so the loads are in flight while it runs
+  const int w = cwarp(), lane = clane();
+  const float* ckb = (const float*)p.ckv.pool + ckv_base(p, layer, 0, g_first);  // group g_first, k, position 0
+  const int gstride = p.ckv.page_size * hd, vstride = Hkv * gstride;  // next kv group; k -> v
+  // 0) cached k, v rows of positions w, w + 8 (< pos0) of the touched groups
   float kk[2][2][4], vv[2][2][4];
 #pragma unroll
   for (int np = 0; np < 2; ++np) {
-    const int sp = cwarp() + FK_CONSUMER_WARPS * np;
+    const int sp = w + FK_CONSUMER_WARPS * np;
 #pragma unroll
     for (int gi = 0; gi < 2; ++gi) {
-      const int g = g_first + gi;
-      if (sp < S && gi < ng) {
-        if (sp < pos0) {
-          const float* kc = (const float*)p.ckv.pool + ckv_offset(p, layer, sp, 0, g);
-          const float* vc = (const float*)p.ckv.pool + ckv_offset(p, layer, sp, 1, g);
+      const bool cached = sp < pos0 && gi < ng;
+      const float* kc = ckb + (cached ? gi * gstride + sp * hd : 0);
+      const float* vc = kc + vstride;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            kk[np][gi][j] = j < J ? __ldcg(kc + clane() + 32 * j) : 0.f;
-            vv[np][gi][j] = j < J ? __ldcg(vc + clane() + 32 * j) : 0.f;
-          }
-        } else {  // a position of this pass: its v from the tagged QKV rows, resolved below
-#pragma unroll
-          for (int j = 0; j < 4; ++j) kk[np][gi][j] = vv[np][gi][j] = 0.f;
-        }
+      for (int j = 0; j < 4; ++j) {
+        kk[np][gi][j] = cached && j < J ? __ldcg(kc + lane + 32 * j) : 0.f;
+        vv[np][gi][j] = cached && j < J ? __ldcg(vc + lane + 32 * j) : 0.f;
       }
-    }
-  }
-  // the current positions' v (after the cached rows' loads went out), all
-  // resolved together
-  {
-    uint64_t raw[16];
-    int off[16];
-#pragma unroll
-    for (int np = 0; np < 2; ++np) {
-      const int sp = cwarp() + FK_CONSUMER_WARPS * np;
-#pragma unroll
-      for (int gi = 0; gi < 2; ++gi) {
-        const bool need = sp < S && gi < ng && sp >= pos0;
-        const int o = need ? (sp - pos0) * p.qkv_rows + (Hq + Hkv + g_first + gi) * hd + clane() : 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = (np * 2 + gi) * 4 + j;
-          off[i] = o + 32 * j;
-          raw[i] = (need && j < J) ? ld_relaxed64(p.qkv + o + 32 * j) : tag_filler(qtag);
-        }
-      }
-    }
-    tag_resolve<16>(raw, p.qkv, off, qtag);
-#pragma unroll
-    for (int np = 0; np < 2; ++np) {
-      const int sp = cwarp() + FK_CONSUMER_WARPS * np;
-#pragma unroll
-      for (int gi = 0; gi < 2; ++gi)
-        if (sp < S && gi < ng && sp >= pos0)
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (j < J) vv[np][gi][j] = tag_float(raw[(np * 2 + gi) * 4 + j]);
     }
   }
   // 1) q of each (head, token) pair, normalised and rotated (warps < npair);
-  //    the pass's current-position keys, one (token, kv group) per warp from
-  //    warp 4 on, normalised, rotated and kept in shared memory -- the CTA
-  //    owning the first o_proj tile of the group appends k and v to the cache
+  //    the k and v of the pass's positions, one (token, kv group) per warp
+  //    from warp 4 on, k normalised and rotated; both kept in shared memory.
+  //    The CTA owning the first o_proj tile of the group appends k and v.
   {
-    const int w = cwarp();
     const bool isq = w < npair, isk = w >= FK_CONSUMER_WARPS - FK_PAIRS && w - (FK_CONSUMER_WARPS - FK_PAIRS) < T * ng;
     if (isq || isk) {
       const int it = w - (FK_CONSUMER_WARPS - FK_PAIRS);
       const int t = isq ? w % T : it / ng, gi = isq ? 0 : it % ng;
       const int h = h_first + w / T, g = g_first + gi;
-      const int so = t * p.qkv_rows + (isq ? h * hd : (Hq + g) * hd) + clane();
-      const int vo = t * p.qkv_rows + (Hq + Hkv + g) * hd + clane();
+      const int so = t * p.qkv_rows + (isq ? h * hd : (Hq + g) * hd) + lane;
+      const int vo = t * p.qkv_rows + (Hq + Hkv + g) * hd + lane;
       const bool app = isk && g * rep * nt >= v0 && g * rep * nt < v1;  // this CTA appends k, v
-      uint64_t raw[8];  // the q or k row, then (when appending) the v row
+      uint64_t raw[8];  // the q or k row, then (for a k job) the v row
       int off[8];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         off[j] = so + 32 * j;
         off[4 + j] = vo + 32 * j;
         raw[j] = j < J ? ld_relaxed64(p.qkv + so + 32 * j) : tag_filler(qtag);
-        raw[4 + j] = (j < J && app) ? ld_relaxed64(p.qkv + vo + 32 * j) : tag_filler(qtag);
+        raw[4 + j] = (j < J && isk) ? ld_relaxed64(p.qkv + vo + 32 * j) : tag_filler(qtag);
       }
       tag_resolve<8>(raw, p.qkv, off, qtag);
       float v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[j] = j < J ? tag_float(raw[j]) : 0.f;
       norm_rope_head(p, fk_sm(), v, isq ? side_gq<typename GainOf<WT>::T>(c, D) : side_gk<typename GainOf<WT>::T>(c, D),
-                     cp_rope_row(pos0 + t), clane());
+                     cp_rope_row(pos0 + t), lane);
       float* dst = isq ? as.q[w] : as.kcur[it];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        if (j < J) dst[clane() + 32 * j] = v[j];
+        if (j < J) dst[lane + 32 * j] = v[j];
+      if (isk) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (j < J) as.vcur[it][lane + 32 * j] = tag_float(raw[4 + j]);
+      }
       if (app) {
-        float* kc = (float*)p.ckv.pool + ckv_offset(p, layer, pos0 + t, 0, g);
-        float* vc = (float*)p.ckv.pool + ckv_offset(p, layer, pos0 + t, 1, g);
+        float* kc = const_cast<float*>(ckb) + gi * gstride + (pos0 + t) * hd;
+        float* vc = kc + vstride;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           if (j < J) {
-            kc[clane() + 32 * j] = v[j];
-            vc[clane() + 32 * j] = tag_float(raw[4 + j]);
+            kc[lane + 32 * j] = v[j];
+            vc[lane + 32 * j] = tag_float(raw[4 + j]);
           }
       }
     }
@@ -1357,64 +1329,60 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
   FK_MARK(TR_SUB, 3);
   consumer_sync();
   FK_MARK(TR_SUB, 4);
-  // 2) the current positions' keys, from step 1
-#pragma unroll
-  for (int np = 0; np < 2; ++np) {
-    const int sp = cwarp() + FK_CONSUMER_WARPS * np;
-#pragma unroll
-    for (int gi = 0; gi < 2; ++gi) {
-      if (sp < S && gi < ng && sp >= pos0) {
-        const float* ks = as.kcur[(sp - pos0) * ng + gi];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (j < J) kk[np][gi][j] = ks[clane() + 32 * j];
-      }
-    }
-  }
-  // 3) per-warp partial softmax over its positions, for every pair
+  // 2) per-warp partial softmax over its positions, for every pair
+#pragma unroll 1
   for (int pr = 0; pr < npair; ++pr) {
     const int h = h_first + pr / T, t = pr % T, gsel = h / rep - g_first;
     float m = -INFINITY, l = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+#pragma unroll 1
     for (int np = 0; np < 2; ++np) {
-      const int sp = cwarp() + FK_CONSUMER_WARPS * np;
-      if (sp <= pos0 + t) {  // causal (and sp < S)
+      const int sp = w + FK_CONSUMER_WARPS * np;
+      if (sp > pos0 + t) break;  // causal (and sp < S)
+      float kr[4], vr[4];
+      if (sp < pos0) {
 #pragma unroll
-        for (int gi = 0; gi < 2; ++gi) {
-          if (gi == gsel) {
-            float d = 0.f;
+        for (int j = 0; j < 4; ++j) {
+          kr[j] = np ? (gsel ? kk[1][1][j] : kk[1][0][j]) : (gsel ? kk[0][1][j] : kk[0][0][j]);
+          vr[j] = np ? (gsel ? vv[1][1][j] : vv[1][0][j]) : (gsel ? vv[0][1][j] : vv[0][0][j]);
+        }
+      } else {
+        const int ci = (sp - pos0) * ng + gsel;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (j < J) d = fmaf(as.q[pr][clane() + 32 * j], kk[np][gi][j], d);
-            d = warp_sum(d) * scale;
-            const float mn = fmaxf(m, d), corr = __expf(m - mn), e = __expf(d - mn);
-            l = l * corr + e;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) o[j] = o[j] * corr + e * vv[np][gi][j];
-            m = mn;
-          }
+        for (int j = 0; j < 4; ++j) {
+          kr[j] = j < J ? as.kcur[ci][lane + 32 * j] : 0.f;
+          vr[j] = j < J ? as.vcur[ci][lane + 32 * j] : 0.f;
         }
       }
+      float d = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j < J) d = fmaf(as.q[pr][lane + 32 * j], kr[j], d);
+      d = warp_sum(d) * scale;
+      const float mn = fmaxf(m, d), corr = __expf(m - mn), e = __expf(d - mn);
+      l = l * corr + e;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[j] = o[j] * corr + e * vr[j];
+      m = mn;
     }
-    if (clane() == 0) { as.m[cwarp()][pr] = m; as.l[cwarp()][pr] = l; }
+    if (lane == 0) { as.m[w][pr] = m; as.l[w][pr] = l; }
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      if (j < J) as.o[cwarp()][pr][clane() + 32 * j] = o[j];
+      if (j < J) as.o[w][pr][lane + 32 * j] = o[j];
   }
   FK_MARK(TR_SUB, 5);
   consumer_sync();
-  // 4) combine the warps: thread (pair, d)
+  // 3) combine the warps: thread (pair, d)
   for (int e = ctid(); e < npair * hd; e += FK_CONSUMERS) {
     const int pr = e / hd, d = e % hd;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < FK_CONSUMER_WARPS; ++w) M = fmaxf(M, as.m[w][pr]);
+    for (int q = 0; q < FK_CONSUMER_WARPS; ++q) M = fmaxf(M, as.m[q][pr]);
     float Ls = 0.f, Os = 0.f;
 #pragma unroll
-    for (int w = 0; w < FK_CONSUMER_WARPS; ++w) {
-      const float f = as.m[w][pr] == -INFINITY ? 0.f : __expf(as.m[w][pr] - M);
-      Ls += as.l[w][pr] * f;
-      Os += as.o[w][pr][d] * f;
+    for (int q = 0; q < FK_CONSUMER_WARPS; ++q) {
+      const float f = as.m[q][pr] == -INFINITY ? 0.f : __expf(as.m[q][pr] - M);
+      Ls += as.l[q][pr] * f;
+      Os += as.o[q][pr][d] * f;
     }
     put_plane(fk_sm()->os[pr / T][pr % T], hd, d, Os / Ls);
   }
@@ -1665,7 +1633,7 @@ __device__ __forceinline__ void phase_talker_oproj(Cons c, int k, uint32_t ptag,
 template <class WT, int T, int G>
 __device__ __forceinline__ void ffn_units(uint32_t buf, int rb, int U, int u0, int D, uint32_t xs, int lane,
                                           const float (&inv)[T], float (*act)[FK_UMAX], int a0, const float* sgu,
-                                          int F, int f0) {
+                                          int F, int f0, int nv) {
   uint32_t ro[2 * G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -1678,7 +1646,7 @@ __device__ __forceinline__ void ffn_units(uint32_t buf, int rb, int U, int u0, i
   for (int g = 0; g < G; ++g)
 #pragma unroll
     for (int t = 0; t < T; ++t)
-      if (lane == g * T + t) {
+      if (lane == g * T + t && g < nv) {  // units past nv: computed on other bytes of shared memory, not kept
         float gs = 1.f, us = 1.f;
         if constexpr (kFp8<WT>) {  // gate row f and up row F + f of W_gateup
           gs = __ldg(sgu + f0 + a0 + u0 + g);
@@ -1792,15 +1760,18 @@ __device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int k, co
     const uint32_t buf = chunk_wait(s, n);
     const int fb = f0 + (int)(n - n0) * upc, U = min(upc, f1 - fb);
     // the chunk holds the gate rows of units fb .. fb + U - 1, then their up rows
+    // two units (their gate and up rows) at a time, an odd last unit alone
     int u = 0;
     if (T == 1) {
       const float inv[1] = {inv0};
-      for (; u + 2 <= U; u += 2) ffn_units<WT, 1, 2>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0, lw->s_gu, F, f0);
-      if (u < U) ffn_units<WT, 1, 1>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0, lw->s_gu, F, f0);
+#pragma unroll 1
+      for (; u + 2 <= U; u += 2) ffn_units<WT, 1, 2>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0, lw->s_gu, F, f0, 2);
+      if (u < U) ffn_units<WT, 1, 1>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0, lw->s_gu, F, f0, 1);
     } else {
       const float inv[2] = {inv0, inv1};
-      for (; u + 2 <= U; u += 2) ffn_units<WT, 2, 2>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0, lw->s_gu, F, f0);
-      if (u < U) ffn_units<WT, 2, 1>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0, lw->s_gu, F, f0);
+#pragma unroll 1
+      for (; u + 2 <= U; u += 2) ffn_units<WT, 2, 2>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0, lw->s_gu, F, f0, 2);
+      if (u < U) ffn_units<WT, 2, 1>(buf, rb, U, u, D, xs, s.lane, inv, sm->act, fb - f0, lw->s_gu, F, f0, 1);
     }
     release_private(s, n);
   }
@@ -2047,10 +2018,12 @@ __device__ __forceinline__ void rows_step(Cons c, const Step& st) {
   int lo, hi;
   split(nrows, p.ncta, ccta(), lo, hi);
   stream_rows<WT>(c, lo, hi, K, T, soff(fk_sm()->u.g.xs), o, inv0, inv1);
+  FK_MARK(TR_SUB, 8);
   // no grid barrier after a row GEMV: its readers wait for the outputs' tags
   // (the Talker head is the frame's last step); the CTA's warps still meet,
   // since the next step reuses the staging area
   if (st.kind != S_T_HEAD) consumer_sync();
+  FK_MARK(TR_SUB, 9);
   warp_set(L.src, st.kind == S_PROJ ? (int)SRC_Z : (int)SRC_RES);
 }
 
@@ -2075,13 +2048,13 @@ __device__ void consumer() {
     for (int i = ctid(); i < p.Dc; i += FK_CONSUMERS) fin[i] = ((const GT*)p.cp_gfinal)[i];
     for (int i = ctid(); i < p.Dt; i += FK_CONSUMERS) fin[p.Dc + i] = ((const GT*)p.t_gfinal)[i];
     if (ccta() == 0 && ctid() == 0 && p.newpage >= 0)
-      const_cast<int*>(p.tkv.page_table)[p.sid * p.tkv.pages_per_stream + p.pos / p.tkv.page_size] = p.newpage;
+      const_cast<int*>(p.tkv.page_table)[p.sid * p.tkv.pages_per_stream + (p.pos >> (__ffs(p.tkv.page_size) - 1))] = p.newpage;
     // the stream's page tables (the page entered this frame from the launch
     // parameters: CTA 0's store above need not be visible yet)
     const int tp = p.tkv.pages_per_stream;
     if (tp <= FK_MAXPAGES)
       for (int i = ctid(); i < tp; i += FK_CONSUMERS)
-        sm->tpage[i] = (p.newpage >= 0 && i == p.pos / p.tkv.page_size) ? p.newpage
+        sm->tpage[i] = (p.newpage >= 0 && i == (p.pos >> (__ffs(p.tkv.page_size) - 1))) ? p.newpage
                                                                          : p.tkv.page_table[p.sid * tp + i];
     if (ctid() == 0) sm->cpage = p.ckv.page_table[p.sid * p.ckv.pages_per_stream];
     // rope rows: CodePredictor positions 0..15 and the Talker position
@@ -2094,7 +2067,10 @@ __device__ void consumer() {
   }
   consumer_sync();
 #ifdef Q3TTS_TRACE
-  if (ctid() == 0) fk_sm()->trace_n = 0;
+  if (ctid() == 0) {
+    fk_sm()->trace_n = 0;
+    fk_sm()->trace_wait = 0;
+  }
 #endif
   FK_MARK(TR_STEP, 15);
   ConsState& L = cst();
@@ -2120,6 +2096,13 @@ __device__ void consumer() {
   }
   for (; L.j < Q3TTS_N_CODEBOOKS; next_step(L)) {
     const Step st = decode_step(*fk_prm(), L.j, L.k);
+#ifdef Q3TTS_TRACE
+    if (ctid() == 0) {  // the previous step's ring-wait cycles, in units of 16
+      const long long w = fk_sm()->trace_wait >> 4;
+      fk_mark(TR_CW0, (int)(w > 0xffff ? 0xffff : w));
+      fk_sm()->trace_wait = 0;
+    }
+#endif
     FK_MARK(TR_STEP, st.kind | (st.j << 4) | (st.l << 9));
     const bool cp = st.j < Q3TTS_N_CODEBOOKS - 1;
     const int T = cp && st.j == 0 ? 2 : 1;
@@ -2579,6 +2562,8 @@ int frame_kernel_create(q3tts_handle* h) {
   // RMSNorm staging holds at most FK_DMAX values: the CodePredictor's first
   // pass stages two tokens
   if (FK_TMAX * c.cp_hidden > FK_DMAX) return Q3TTS_OK;
+  // cache pages of a power-of-two size (positions split by shift and mask)
+  if (c.page_size & (c.page_size - 1)) return Q3TTS_OK;
   // tags number a frame's steps below FK_MAXSTEPS
   const int steps = (Q3TTS_N_CODEBOOKS - 1) * (2 + (c.talker_hidden != c.cp_hidden ? 1 : 0) + 3 * c.cp_layers) +
                     2 + 4 * c.talker_layers;
