@@ -57,6 +57,7 @@
 #include <atomic>
 #include <mutex>
 #include <new>
+#include <type_traits>
 #include <vector>
 
 #include "engine.cuh"
@@ -282,8 +283,11 @@ __device__ __forceinline__ int ld_volatile(const int* p) { return *(const volati
 __device__ __forceinline__ uint64_t tag_word(float v, uint32_t tag) {
   return ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(v);
 }
+// (No compiler memory clobber on the store: nothing is ordered against it but
+// through the tag itself, and a clobber would keep the compiler from issuing
+// the next rows' shared-memory loads ahead of it.)
 __device__ __forceinline__ void st_tagged(uint64_t* p, float v, uint32_t tag) {
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(tag_word(v, tag)) : "memory");
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(tag_word(v, tag)));
 }
 __device__ __forceinline__ uint64_t ld_relaxed64(const uint64_t* p) {
   uint64_t v;
@@ -410,7 +414,7 @@ struct FKSmem {
   ConsState cs[FK_CONSUMER_WARPS];
 #ifdef Q3TTS_TRACE
   int trace_n;
-  long long trace_wait;  // clock64 cycles consumer thread 0 spent in ring waits this step
+  long long trace_wait[FK_CONSUMER_WARPS];  // clock64 cycles each consumer warp spent in ring waits this step
 #endif
 };
 static_assert(sizeof(FKSmem) <= 227 * 1024, "persistent kernel shared memory");
@@ -681,7 +685,7 @@ __device__ __forceinline__ uint32_t chunk_wait(Stream& s, uint32_t n) {
     const long long tw = clock64();
     if (!__all_sync(0xffffffffu, mbar_test_wait(&sm->full[slot], par)))
       s.aborted = chunk_wait_slow(soff(&sm->full[slot]), par);
-    if (ctid() == 0) sm->trace_wait += clock64() - tw;
+    if (clane() == 0) sm->trace_wait[cwarp()] += clock64() - tw;
 #else
     if (!__all_sync(0xffffffffu, mbar_try_wait(&sm->full[slot], par)))
       s.aborted = chunk_wait_slow(soff(&sm->full[slot]), par);
@@ -728,9 +732,53 @@ __device__ __forceinline__ float dot8(const float (&w)[8], const float4& a, cons
 // all rows, and the NR T sums are reduced together so that their shuffle
 // chains overlap.  NR and T are compile-time: a guard on a runtime row count
 // inside an unrolled loop would issue the skipped rows' instructions anyway.
+// Four bf16 rows of 1024 against one token (the CodePredictor's QKV, head and
+// gate/up rows): every shared-memory load of the group -- the lane's 32
+// activations and its 4 x 4 weight vectors -- is issued before the first
+// multiply, so their latencies overlap (measured on GB300: 1,330 cycles per
+// 8 KB chunk and warp, against 2,270 for the block loop below).
+template <int NR>
+__device__ __forceinline__ void dots4_k1024(uint32_t w, const uint32_t (&ro)[NR], uint32_t xs, int lane,
+                                            float (&acc)[NR][1]) {
+  constexpr int K = 1024;
+  const uint32_t wl = w + (uint32_t)(lane * 16), xl = xs + (uint32_t)(lane * 16);
+  float4 xa[4], xc[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    xa[b] = lds_f4(xl + (uint32_t)(b * 512));
+    xc[b] = lds_f4(xl + (uint32_t)(b * 512 + K * 2));
+  }
+  uint4 wr[NR][4];
+#pragma unroll
+  for (int r = 0; r < NR; ++r)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) wr[r][b] = lds_u4(wl + ro[r] + (uint32_t)(b * 512));
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    float a = 0.f;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      float f[8];
+      unpack_bf16x8(wr[r][b], f);
+      a = dot8(f, xa[b], xc[b], a);
+    }
+    acc[r][0] = a;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int r = 0; r < NR; ++r) acc[r][0] += __shfl_xor_sync(0xffffffffu, acc[r][0], o);
+}
+
 template <class WT, int T, int NR>
 __device__ __forceinline__ void dots(uint32_t w, const uint32_t (&ro)[NR], int K, uint32_t xs, int lane,
                                      float (&acc)[NR][T]) {
+  if constexpr (T == 1 && NR == 4 && std::is_same<WT, bf16>::value) {
+    if (K == 1024) {
+      dots4_k1024<NR>(w, ro, xs, lane, acc);
+      return;
+    }
+  }
 #pragma unroll
   for (int r = 0; r < NR; ++r)
 #pragma unroll
@@ -805,8 +853,11 @@ __device__ __forceinline__ void rows_group(uint32_t buf, int rb, int r0, int K, 
 // Rows [r0, r1) of a row-major [*, K] matrix streamed from the ring (the
 // private chunks the producer cut them into) against T staged vectors at
 // shared offset xs: output row of token t = inv_t (row . x_t), placed as o
-// says.  A chunk's rows go in pairs (a ragged last row alone).  Advances the
-// ring position past the rows' chunks.
+// says.  A chunk's rows go in groups of four when it holds a multiple of four
+// rows (the activations are read from shared memory once per group, and they
+// are half of a group's shared-memory traffic at two rows), else in pairs (a
+// ragged last row computed with its neighbour's bytes and not stored).
+// Advances the ring position past the rows' chunks.
 template <class WT, int T>
 __device__ __forceinline__ void stream_rows_t(Cons c, int r0, int r1, int K, uint32_t xs, const RowsOut& o,
                                               const float (&inv)[T]) {
@@ -818,8 +869,13 @@ __device__ __forceinline__ void stream_rows_t(Cons c, int r0, int r1, int K, uin
   for (uint32_t n = first_chunk(n0, s.warp); n < n0 + nch; n += FK_CONSUMER_WARPS) {
     const uint32_t buf = chunk_wait(s, n);
     const int base = r0 + (int)(n - n0) * rpc, R = min(rpc, r1 - base);
+    if ((rpc & 3) == 0) {
 #pragma unroll 1
-    for (int r = 0; r < R; r += 2) rows_group<WT, T, 2>(buf, rb, r, K, xs, s.lane, o, base, inv, R - r);
+      for (int r = 0; r < R; r += 4) rows_group<WT, T, 4>(buf, rb, r, K, xs, s.lane, o, base, inv, R - r);
+    } else {
+#pragma unroll 1
+      for (int r = 0; r < R; r += 2) rows_group<WT, T, 2>(buf, rb, r, K, xs, s.lane, o, base, inv, R - r);
+    }
     release_private(s, n);
   }
   warp_set(cst().aborted, s.aborted ? 1 : 0);
@@ -2067,10 +2123,8 @@ __device__ void consumer() {
   }
   consumer_sync();
 #ifdef Q3TTS_TRACE
-  if (ctid() == 0) {
-    fk_sm()->trace_n = 0;
-    fk_sm()->trace_wait = 0;
-  }
+  if (ctid() == 0) fk_sm()->trace_n = 0;
+  if (clane() == 0) fk_sm()->trace_wait[cwarp()] = 0;
 #endif
   FK_MARK(TR_STEP, 15);
   ConsState& L = cst();
@@ -2097,11 +2151,14 @@ __device__ void consumer() {
   for (; L.j < Q3TTS_N_CODEBOOKS; next_step(L)) {
     const Step st = decode_step(*fk_prm(), L.j, L.k);
 #ifdef Q3TTS_TRACE
-    if (ctid() == 0) {  // the previous step's ring-wait cycles, in units of 16
-      const long long w = fk_sm()->trace_wait >> 4;
+    consumer_sync();  // (profiling builds) every warp's waits of the previous step are in
+    if (ctid() == 0) {  // the previous step's largest ring wait of a warp, in units of 16 cycles
+      long long w = 0;
+      for (int q = 0; q < FK_CONSUMER_WARPS; ++q) w = max(w, fk_sm()->trace_wait[q] >> 4);
       fk_mark(TR_CW0, (int)(w > 0xffff ? 0xffff : w));
-      fk_sm()->trace_wait = 0;
     }
+    consumer_sync();
+    if (clane() == 0) fk_sm()->trace_wait[cwarp()] = 0;
 #endif
     FK_MARK(TR_STEP, st.kind | (st.j << 4) | (st.l << 9));
     const bool cp = st.j < Q3TTS_N_CODEBOOKS - 1;
