@@ -54,6 +54,7 @@
 //    is bounded; on expiry the kernel records Q3TTS_ERR_TIMEOUT, raises an
 //    abort flag, stops waiting, lets in-flight copies land and returns.
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <mutex>
 #include <new>
@@ -107,12 +108,38 @@ struct LayerDev {
   const float* s_d;
 };
 
+// A CTA's share of every phase of a frame.  It depends only on the
+// configuration and the CTA's index, so the host computes it once
+// (frame_kernel_create) and each CTA copies its row into shared memory at the
+// start of a frame: no phase divides on its critical path.  Index s: 0 the
+// CodePredictor, 1 the Talker.
+struct FKRange {
+  int lo, hi, nch;  // items [lo, hi), in nch ring chunks
+};
+struct FKPlan {
+  FKRange qkv[2];   // rows of W_qkv
+  FKRange proj;     // rows of the CodePredictor input projection (width D_t)
+  FKRange head[2];  // rows of the CodePredictor head / of the Talker head
+  FKRange ffn[2];   // FFN units [f0, f1) in nch gate/up chunks
+  int ffn_nd[2];    // chunks of the units' W_down^T rows
+  int op_t0[2], op_t1[2], op_h0[2], op_h1[2];  // o_proj tiles [t0, t1) and the heads h0..h1 they cover
+  int sl_lo[3], sl_hi[3];  // the CTA's slice of a D_c-, D_t- and xstride-long vector
+  int rpc[2];       // rows of width D_c / D_t per ring chunk
+  int upc[2];       // FFN units of width D_c / D_t per ring chunk
+  float invD[2];    // 1 / D_c, 1 / D_t
+  float inv_nt[2];  // 1 / (o_proj tiles per head), for D_c / D_t
+  int cpg, tg, tch; // Talker attention: CTAs per kv group; this CTA's group and chunk
+  int hd_shift, rep_shift;   // log2 head_dim, log2 (q heads per kv head)
+  float inv_hd, attn_scale;  // 1 / head_dim, 1 / sqrt(head_dim)
+};
+
 struct FKParams {
   int ncta;
   int Dt, Dc, Ft, Fc, Hq, Hkv, hd, Vt, Vc, Lt, Lc, qkv_rows, has_proj, qk_norm, dmax;
   float eps;
   const LayerDev* tl;
   const LayerDev* cl;
+  const FKPlan* plan;  // [ncta]
   const void *t_head, *e_codec, *cp_heads, *cp_embeds, *cp_proj, *t_gfinal, *cp_gfinal;
   const float *s_head, *s_cp_heads, *s_cp_proj;  // FP8: the heads' and projection's row scales
   float* pending_h;
@@ -157,6 +184,7 @@ struct FKState {
   char* sideC;
   LayerDev* tl;
   LayerDev* cl;
+  FKPlan* plan;  // [ncta]
   float *xb, *xa, *xf;
   uint64_t *qkv, *z, *part, *cp_logits;
   uint32_t seq;  // launches of this handle with its workspace scratch
@@ -412,6 +440,8 @@ struct FKSmem {
   int flag;
   uint32_t pf_gate;  // chunks the ring's producer has issued (read by the prefetch warp)
   ConsState cs[FK_CONSUMER_WARPS];
+  FKPlan plan;  // this CTA's row of the plan
+  int ta_s0, ta_s1;  // this frame: the Talker positions [s0, s1) this CTA's attention chunk covers
 #ifdef Q3TTS_TRACE
   int trace_n;
   long long trace_wait[FK_CONSUMER_WARPS];  // clock64 cycles each consumer warp spent in ring waits this step
@@ -859,13 +889,13 @@ __device__ __forceinline__ void rows_group(uint32_t buf, int rb, int r0, int K, 
 // ragged last row computed with its neighbour's bytes and not stored).
 // Advances the ring position past the rows' chunks.
 template <class WT, int T>
-__device__ __forceinline__ void stream_rows_t(Cons c, int r0, int r1, int K, uint32_t xs, const RowsOut& o,
-                                              const float (&inv)[T]) {
+__device__ __forceinline__ void stream_rows_t(Cons c, const FKRange& rg, int rpc, int K, uint32_t xs,
+                                              const RowsOut& o, const float (&inv)[T]) {
   Stream s = stream_begin(c);
   const int rb = K * (int)sizeof(WT);
-  const int rpc = rows_per_chunk(rb);
+  const int r0 = rg.lo, r1 = rg.hi;
   const uint32_t n0 = cst().n;
-  const uint32_t nch = r1 > r0 ? (uint32_t)((r1 - r0 + rpc - 1) / rpc) : 0u;
+  const uint32_t nch = (uint32_t)rg.nch;
   for (uint32_t n = first_chunk(n0, s.warp); n < n0 + nch; n += FK_CONSUMER_WARPS) {
     const uint32_t buf = chunk_wait(s, n);
     const int base = r0 + (int)(n - n0) * rpc, R = min(rpc, r1 - base);
@@ -883,14 +913,14 @@ __device__ __forceinline__ void stream_rows_t(Cons c, int r0, int r1, int K, uin
 }
 
 template <class WT>
-__device__ __forceinline__ void stream_rows(Cons c, int r0, int r1, int K, int T, uint32_t xs, const RowsOut& o,
-                                            float inv0, float inv1) {
+__device__ __forceinline__ void stream_rows(Cons c, const FKRange& rg, int rpc, int K, int T, uint32_t xs,
+                                            const RowsOut& o, float inv0, float inv1) {
   if (T == 1) {
     const float inv[1] = {inv0};
-    stream_rows_t<WT, 1>(c, r0, r1, K, xs, o, inv);
+    stream_rows_t<WT, 1>(c, rg, rpc, K, xs, o, inv);
   } else {
     const float inv[2] = {inv0, inv1};
-    stream_rows_t<WT, 2>(c, r0, r1, K, xs, o, inv);
+    stream_rows_t<WT, 2>(c, rg, rpc, K, xs, o, inv);
   }
 }
 
@@ -932,20 +962,21 @@ __device__ __forceinline__ float4 gain4<float>(const float* g, int i) {
   return *reinterpret_cast<const float4*>(g + i);
 }
 
-// The CTA's slice [lo, hi) of a D-vector (32-bit arithmetic: D * ncta < 2^31).
-__device__ __forceinline__ void cta_slice(int D, int& lo, int& hi) {
-  const int nc = fk_prm()->ncta, cta = ccta();
-  lo = D * cta / nc;
-  hi = D * (cta + 1) / nc;
+// The CTA's slice [lo, hi) of a vector: which = 0 (D_c long), 1 (D_t), 2
+// (xstride), from the plan.
+__device__ __forceinline__ void cta_slice(int which, int& lo, int& hi) {
+  lo = fk_sm()->plan.sl_lo[which];
+  hi = fk_sm()->plan.sl_hi[which];
 }
 
-// 1 / rms of staged token t (width D), from load_norm's partial sums.
-__device__ __forceinline__ float norm_inv(int t, int D) {
+// 1 / rms of staged token t of stack s (width D_s), from load_norm's partial
+// sums (the mean square as sum * (1 / D_s); rsqrt within 2 ulp).
+__device__ __forceinline__ float norm_inv(int t, int s) {
   const float* r = fk_sm()->red[t];
   float a = 0.f;
 #pragma unroll
   for (int w = 0; w < FK_CONSUMER_WARPS; ++w) a += r[w];
-  return 1.0f / sqrtf(a / (float)D + fk_prm()->eps);
+  return rsqrtf(fmaf(a, fk_sm()->plan.invD[s], fk_prm()->eps));
 }
 
 // Stages y_t = g * x_t in xs (plane layout) for t < T, where x_t comes from
@@ -958,10 +989,10 @@ __device__ __forceinline__ float norm_inv(int t, int D) {
 // tokens, all of its loads issued together.  With fold >= 0 the CTA's slice of
 // each raw x_t goes to xbase(fold).  If out is given, the CTA's slice of the
 // normed x_0 goes there.  g points into shared memory (4-element aligned
-// groups).
+// groups).  sd: the stack (0 CodePredictor, 1 Talker) whose width D is.
 template <class WT>
-__device__ __noinline__ void load_norm(Cons c, int src, int kp, uint32_t ztag, int t0, int T, int D, const WT* g,
-                                          int fold, float* out) {
+__device__ __noinline__ void load_norm(Cons c, int src, int kp, uint32_t ztag, int t0, int T, int D, int sd,
+                                       const WT* g, int fold, float* out) {
   const FKParams& p = *fk_prm();
   float* xs = fk_sm()->u.g.xs;
   constexpr int PER = FK_DMAX / 4 / FK_CONSUMERS;  // float4 per thread: T D <= FK_DMAX (checked at create)
@@ -1034,7 +1065,7 @@ __device__ __noinline__ void load_norm(Cons c, int src, int kp, uint32_t ztag, i
     fk_sm()->red[1][cwarp()] = ss1;
   }
   int lo, hi;
-  cta_slice(D, lo, hi);
+  cta_slice(sd, lo, hi);
   if (fold >= 0) {
     float* fb = xbase(p, fold);
 #pragma unroll
@@ -1064,7 +1095,7 @@ __device__ __noinline__ void load_norm(Cons c, int src, int kp, uint32_t ztag, i
   }
   consumer_sync();
   if (out) {
-    const float iv = norm_inv(0, D);
+    const float iv = norm_inv(0, sd);
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
       const int e = tid + FK_CONSUMERS * u;
@@ -1102,7 +1133,7 @@ __device__ __forceinline__ void norm_rope_head(const FKParams& p, const FKSmem* 
     for (int j = 0; j < 4; ++j)
       if (j < J) ss = fmaf(v[j], v[j], ss);
     ss = warp_sum(ss);
-    const float inv = 1.0f / sqrtf(ss / (float)hd + p.eps);
+    const float inv = rsqrtf(fmaf(ss, sm->plan.inv_hd, p.eps));
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       if (j < J) v[j] = v[j] * inv * to_f(g[lane + 32 * j]);
@@ -1238,11 +1269,8 @@ __device__ __forceinline__ const WT* side_gk(Cons c, int D) { return side_cur<WT
 // (column 32 j + l of W_o, inputs h hd + 8 kb ..) sit at (kb 32 + l) 8, so a
 // warp reads a tile with conflict-free 16-byte loads and every lane owns one
 // output column -- no cross-lane reduction.  The CTA's tiles are [t0, t1)
-// of Hq * ceil(D / 32).
+// of Hq * ceil(D / 32) (the plan's op_t0, op_t1 for stack s).
 __device__ __forceinline__ int oproj_nt(int D) { return (D + 31) >> 5; }
-__device__ __forceinline__ void oproj_tiles(const FKParams& p, int D, int cta, int& t0, int& t1) {
-  split(p.Hq * oproj_nt(D), p.ncta, cta, t0, t1);
-}
 
 // The CTA's o_proj tiles, one per ring chunk and private to a warp, against
 // the attention outputs of the CTA's (<= 2) heads (os, plane layout) for T
@@ -1250,13 +1278,12 @@ __device__ __forceinline__ void oproj_tiles(const FKParams& p, int D, int cta, i
 // added into xattn(k).  Closes the attention phase of layer k with a grid
 // barrier.
 template <class WT>
-__device__ __forceinline__ void oproj_step(Cons c, int D, int T, int k, const float* so) {
+__device__ __forceinline__ void oproj_step(Cons c, int D, int sd, int T, int k, const float* so) {
   const FKParams& p = *fk_prm();
   Stream s = stream_begin(c);
   const int hd = p.hd, nt = oproj_nt(D), nkb = hd >> 3;
-  int t0, t1;
-  oproj_tiles(p, D, ccta(), t0, t1);
-  const int h_first = t0 / nt;
+  const int t0 = fk_sm()->plan.op_t0[sd], t1 = fk_sm()->plan.op_t1[sd];
+  const int h_first = fk_sm()->plan.op_h0[sd];
   float* XA = xattn(p, k);
   const uint32_t os0 = soff(fk_sm()->os[0][0]);
   constexpr uint32_t OS_HEAD = FK_TMAX * FK_HDMAX * 4, OS_TOK = FK_HDMAX * 4;
@@ -1264,7 +1291,9 @@ __device__ __forceinline__ void oproj_step(Cons c, int D, int T, int k, const fl
   const uint32_t nch = t1 > t0 ? (uint32_t)(t1 - t0) : 0u;
   for (uint32_t n = first_chunk(n0, s.warp); n < n0 + nch; n += FK_CONSUMER_WARPS) {
     const uint32_t buf = chunk_wait(s, n);
-    const int ti = t0 + (int)(n - n0), h = ti / nt, col = (ti - h * nt) * 32 + s.lane;
+    // head of tile ti: floor((ti + 0.5) / nt) in float is exact here (ti < 16 nt, nt <= 64)
+    const int ti = t0 + (int)(n - n0), h = (int)(((float)ti + 0.5f) * fk_sm()->plan.inv_nt[sd]);
+    const int col = (ti - h * nt) * 32 + s.lane;
     const uint32_t w = buf + (uint32_t)(s.lane * 8 * (int)sizeof(WT));
     float sc = 1.f;
     if constexpr (kFp8<WT>) sc = col < D ? __ldg(so + col) : 0.f;  // W_o row (output column) scale
@@ -1302,17 +1331,18 @@ __device__ __forceinline__ void store_head_plane(float* dst, int hd, const float
 template <class WT>
 __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0, int k, uint32_t qtag) {
   const FKParams& p = *fk_prm();
-  const int D = p.Dc, hd = p.hd, Hq = p.Hq, Hkv = p.Hkv, rep = Hq / Hkv, J = hd / 32;
-  const int nt = oproj_nt(D);
-  int v0, v1;  // the CTA's o_proj tiles
-  oproj_tiles(p, D, ccta(), v0, v1);
-  const int h_first = v0 / nt, h_last = (v1 - 1) / nt;
+  const FKPlan& pl = fk_sm()->plan;
+  const int D = p.Dc, hd = p.hd, Hq = p.Hq, Hkv = p.Hkv, rs = pl.rep_shift, rep = 1 << rs, J = hd >> 5;
+  const int nt = oproj_nt(D), ts = T - 1;  // tokens of the pass: 1 or 2 (shift ts)
+  const int v0 = pl.op_t0[0], v1 = pl.op_t1[0];  // the CTA's o_proj tiles
+  const int h_first = pl.op_h0[0], h_last = pl.op_h1[0];
   const int nh = v1 > v0 ? h_last - h_first + 1 : 0;
   const int npair = nh * T;
-  const int g_first = h_first / rep;
-  const int ng = nh ? h_last / rep - g_first + 1 : 0;  // kv groups touched (<= 2)
+  const int g_first = h_first >> rs;
+  const int ng = nh ? (h_last >> rs) - g_first + 1 : 0;  // kv groups touched (<= 2)
+  const int gs = ng > 1 ? 1 : 0;
   AttnScratch& as = fk_sm()->u.att;
-  const float scale = 1.0f / sqrtf((float)hd);
+  const float scale = pl.attn_scale;
   const int w = cwarp(), lane = clane();
   const float* ckb = (const float*)p.ckv.pool + ckv_base(p, layer, 0, g_first);  // group g_first, k, position 0
   const int gstride = p.ckv.page_size * hd, vstride = Hkv * gstride;  // next kv group; k -> v
@@ -1341,8 +1371,8 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
     const bool isq = w < npair, isk = w >= FK_CONSUMER_WARPS - FK_PAIRS && w - (FK_CONSUMER_WARPS - FK_PAIRS) < T * ng;
     if (isq || isk) {
       const int it = w - (FK_CONSUMER_WARPS - FK_PAIRS);
-      const int t = isq ? w % T : it / ng, gi = isq ? 0 : it % ng;
-      const int h = h_first + w / T, g = g_first + gi;
+      const int t = isq ? (w & ts) : it >> gs, gi = isq ? 0 : (it & gs);
+      const int h = h_first + (w >> ts), g = g_first + gi;
       const int so = t * p.qkv_rows + (isq ? h * hd : (Hq + g) * hd) + lane;
       const int vo = t * p.qkv_rows + (Hq + Hkv + g) * hd + lane;
       const bool app = isk && g * rep * nt >= v0 && g * rep * nt < v1;  // this CTA appends k, v
@@ -1388,7 +1418,7 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
   // 2) per-warp partial softmax over its positions, for every pair
 #pragma unroll 1
   for (int pr = 0; pr < npair; ++pr) {
-    const int h = h_first + pr / T, t = pr % T, gsel = h / rep - g_first;
+    const int h = h_first + (pr >> ts), t = pr & ts, gsel = (h >> rs) - g_first;
     float m = -INFINITY, l = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
     for (int np = 0; np < 2; ++np) {
@@ -1429,7 +1459,7 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
   consumer_sync();
   // 3) combine the warps: thread (pair, d)
   for (int e = ctid(); e < npair * hd; e += FK_CONSUMERS) {
-    const int pr = e / hd, d = e % hd;
+    const int pr = e >> pl.hd_shift, d = e & (hd - 1);
     float M = -INFINITY;
 #pragma unroll
     for (int q = 0; q < FK_CONSUMER_WARPS; ++q) M = fmaxf(M, as.m[q][pr]);
@@ -1440,11 +1470,11 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
       Ls += as.l[q][pr] * f;
       Os += as.o[q][pr][d] * f;
     }
-    put_plane(fk_sm()->os[pr / T][pr % T], hd, d, Os / Ls);
+    put_plane(fk_sm()->os[pr >> ts][pr & ts], hd, d, __fdividef(Os, Ls));  // Ls >= 1 (the max term)
   }
   consumer_sync();
   FK_MARK(TR_SUB, 6);
-  oproj_step<WT>(c, D, T, k, p.cl[layer].s_o);
+  oproj_step<WT>(c, D, 0, T, k, p.cl[layer].s_o);
 }
 
 // Talker phase B1: attention partials.  Work item = (kv group g, position
@@ -1491,14 +1521,14 @@ __device__ __forceinline__ void talker_kv_rows(const FKParams& p, int layer, int
 template <class WT, class KT>
 __device__ __forceinline__ void phase_talker_attn(Cons c, int layer, uint32_t qtag, uint32_t ptag) {
   const FKParams& p = *fk_prm();
-  const int hd = p.hd, Hq = p.Hq, Hkv = p.Hkv, rep = Hq / Hkv, J = hd / 32;
-  const int cpg = p.ncta / Hkv;
-  const int g = ccta() / cpg, ch = ccta() % cpg;
-  const int pos = p.pos, S = pos + 1;
+  const FKPlan& pl = fk_sm()->plan;
+  const int hd = p.hd, Hq = p.Hq, Hkv = p.Hkv, rep = 1 << pl.rep_shift, J = hd >> 5;
+  const int cpg = pl.cpg, g = pl.tg, ch = pl.tch;
+  const int pos = p.pos;
   AttnScratch& as = fk_sm()->u.att;
-  const float scale = 1.0f / sqrtf((float)hd);
+  const float scale = pl.attn_scale;
   if (g < Hkv) {
-    const int cs = (S + cpg - 1) / cpg, s0 = ch * cs, s1 = min(S, s0 + cs);
+    const int s0 = fk_sm()->ta_s0, s1 = fk_sm()->ta_s1;
     constexpr int BATCH = 2;
     float k[BATCH][4], v[BATCH][4];
     // the warp's first K/V rows are loaded before step 1 (they do not depend
@@ -1595,7 +1625,7 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer, uint32_t qt
     }
     consumer_sync();
     for (int e = ctid(); e < rep * hd; e += FK_CONSUMERS) {
-      const int r = e / hd, d = e % hd;
+      const int r = e >> pl.hd_shift, d = e & (hd - 1);
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < FK_CONSUMER_WARPS; ++w) M = fmaxf(M, as.m[w][r]);
@@ -1624,10 +1654,10 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer, uint32_t qt
 template <class WT>
 __device__ __forceinline__ void phase_talker_oproj(Cons c, int k, uint32_t ptag, int l) {
   const FKParams& p = *fk_prm();
-  const int D = p.Dt, hd = p.hd, cpg = p.ncta / p.Hkv, nt = oproj_nt(D);
-  int v0, v1;  // the CTA's o_proj tiles
-  oproj_tiles(p, D, ccta(), v0, v1);
-  const int h_first = v0 / nt, h_last = (v1 - 1) / nt;
+  const FKPlan& pl = fk_sm()->plan;
+  const int D = p.Dt, hd = p.hd, cpg = pl.cpg;
+  const int v0 = pl.op_t0[1], v1 = pl.op_t1[1];  // the CTA's o_proj tiles
+  const int h_first = pl.op_h0[1], h_last = pl.op_h1[1];
   const int nh = v1 > v0 ? h_last - h_first + 1 : 0;
   // warp-cooperative: thread (hh, d) = ctid() of the CTA's nh heads (whole
   // warps, as hd is a multiple of 32); lane c of a warp reads chunk c's
@@ -1636,7 +1666,7 @@ __device__ __forceinline__ void phase_talker_oproj(Cons c, int k, uint32_t ptag,
   // shuffle
   const int e = ctid();
   if (e < nh * hd) {
-    const int hh = e / hd, d = e % hd, lane = clane();
+    const int hh = e >> pl.hd_shift, d = e & (hd - 1), lane = clane();
     const uint64_t* base = p.part + (size_t)(h_first + hh) * cpg * (hd + 2);
     float M = -INFINITY;
     for (int c0 = 0; c0 < cpg; c0 += 32) {
@@ -1677,10 +1707,10 @@ __device__ __forceinline__ void phase_talker_oproj(Cons c, int k, uint32_t ptag,
         }
       }
     }
-    put_plane(fk_sm()->os[hh][0], hd, d, O / L);
+    put_plane(fk_sm()->os[hh][0], hd, d, __fdividef(O, L));  // L >= 1 (the max term)
   }
   consumer_sync();
-  oproj_step<WT>(c, D, 1, k, p.tl[l].s_o);
+  oproj_step<WT>(c, D, 1, 1, k, p.tl[l].s_o);  // the Talker's stack, one token
 }
 
 // Units u0 .. u0 + G - 1 of a chunk that holds the gate rows of U units and
@@ -1718,12 +1748,11 @@ __device__ __forceinline__ void ffn_units(uint32_t buf, int rb, int U, int u0, i
 // registers and adds the CTA's partial sums into copy CTA % FK_KC of
 // xffn(k) with float4 atomics.
 template <class WT, int T>
-__device__ __forceinline__ void ffn_down(Stream& s, int D, int f0, int f1, uint32_t n0, int k, const float* sd) {
+__device__ __forceinline__ void ffn_down(Stream& s, int D, int f0, int f1, int rpc, uint32_t nd, uint32_t n0, int k,
+                                         const float* sd) {
   const FKParams& p = *fk_prm();
   const float(*act)[FK_UMAX] = fk_sm()->act;
   const int rb = D * (int)sizeof(WT);
-  const int rpc = rows_per_chunk(rb);
-  const uint32_t nd = f1 > f0 ? (uint32_t)((f1 - f0 + rpc - 1) / rpc) : 0u;
   const int col = (s.warp * 32 + s.lane) * 8;  // the lane's first output column
   const bool active = col < D;
   float y[T][8];
@@ -1786,14 +1815,16 @@ __device__ __forceinline__ int units_per_chunk(int row_bytes) {
 // CTA % FK_KC of xffn(k) with float4 atomics.  The CTA also clears its slice
 // of layer k + 1's deltas (see xbase).
 template <class WT>
-__device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int k, const LayerDev* lw) {
+__device__ __forceinline__ void phase_ffn(Cons c, int sd, int T, int k, const LayerDev* lw) {
   using GT = typename GainOf<WT>::T;
   const FKParams& p = *fk_prm();
-  load_norm<GT>(c, SRC_RES_A, k, 0u, 0, T, D, side_cur<GT>(c) + D, -1, nullptr);
+  const FKPlan& pl = fk_sm()->plan;
+  const int D = sd ? p.Dt : p.Dc, F = sd ? p.Ft : p.Fc;
+  load_norm<GT>(c, SRC_RES_A, k, 0u, 0, T, D, sd, side_cur<GT>(c) + D, -1, nullptr);
   side_end(c);
   {
     int lo, hi;
-    cta_slice(p.xstride, lo, hi);
+    cta_slice(2, lo, hi);
     float* a1 = xattn(p, k + 1);
     float* f1 = xffn(p, k + 1, 0);
     for (int i = lo + ctid(); i < hi; i += FK_CONSUMERS) {
@@ -1802,16 +1833,15 @@ __device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int k, co
       for (int q = 0; q < FK_KC; ++q) f1[q * p.xstride + i] = 0.f;
     }
   }
-  const float inv0 = norm_inv(0, D), inv1 = T > 1 ? norm_inv(1, D) : 0.f;
-  int f0, f1;
-  split(F, p.ncta, ccta(), f0, f1);
+  const float inv0 = norm_inv(0, sd), inv1 = T > 1 ? norm_inv(1, sd) : 0.f;
+  const int f0 = pl.ffn[sd].lo, f1 = pl.ffn[sd].hi;
   const int rb = D * (int)sizeof(WT);
-  const int upc = units_per_chunk(rb);
+  const int upc = pl.upc[sd];
   FKSmem* sm = fk_sm();
   const uint32_t xs = soff(sm->u.g.xs);
   Stream s = stream_begin(c);
   uint32_t n0 = cst().n;
-  const uint32_t nch = f1 > f0 ? (uint32_t)((f1 - f0 + upc - 1) / upc) : 0u;
+  const uint32_t nch = (uint32_t)pl.ffn[sd].nch;
   for (uint32_t n = first_chunk(n0, s.warp); n < n0 + nch; n += FK_CONSUMER_WARPS) {
     const uint32_t buf = chunk_wait(s, n);
     const int fb = f0 + (int)(n - n0) * upc, U = min(upc, f1 - fb);
@@ -1835,9 +1865,9 @@ __device__ __forceinline__ void phase_ffn(Cons c, int D, int F, int T, int k, co
   n0 += nch;
   consumer_sync();  // act complete
   if (T == 1)
-    ffn_down<WT, 1>(s, D, f0, f1, n0, k, lw->s_d);
+    ffn_down<WT, 1>(s, D, f0, f1, pl.rpc[sd], (uint32_t)pl.ffn_nd[sd], n0, k, lw->s_d);
   else
-    ffn_down<WT, 2>(s, D, f0, f1, n0, k, lw->s_d);
+    ffn_down<WT, 2>(s, D, f0, f1, pl.rpc[sd], (uint32_t)pl.ffn_nd[sd], n0, k, lw->s_d);
   grid_sync(c);
 }
 
@@ -2016,7 +2046,10 @@ __device__ __forceinline__ void rows_step(Cons c, const Step& st) {
   const bool cp = st.j < Q3TTS_N_CODEBOOKS - 1;
   const int Tp = cp && st.j == 0 ? 2 : 1;  // tokens of the pass
   const uint32_t tag = tag_of(L.s);
-  int K, T, nrows;
+  const int sd = cp ? 0 : 1;  // the stack
+  const FKPlan& pl = fk_sm()->plan;
+  int K, T, rpc;
+  const FKRange* rg;
   RowsOut o;
   o.out = nullptr;
   o.out64 = nullptr;
@@ -2026,27 +2059,31 @@ __device__ __forceinline__ void rows_step(Cons c, const Step& st) {
   if (st.kind == S_QKV) {
     K = cp ? p.Dc : p.Dt;
     T = Tp;
-    nrows = p.qkv_rows;
+    rg = &pl.qkv[sd];
+    rpc = pl.rpc[sd];
     o.out64 = p.qkv;
     o.ts = p.qkv_rows;
     if constexpr (kFp8<WT>) o.sc = (cp ? p.cl : p.tl)[st.l].s_qkv;
   } else if (st.kind == S_PROJ) {
     K = p.Dt;
     T = Tp;
-    nrows = p.Dc;
+    rg = &pl.proj;
+    rpc = pl.rpc[1];
     o.out64 = p.z;
     o.ts = p.Dc;
     o.sc = p.s_cp_proj;
   } else if (st.kind == S_CP_HEAD) {
     K = p.Dc;
     T = 1;
-    nrows = p.Vc;
+    rg = &pl.head[0];
+    rpc = pl.rpc[0];
     o.out64 = p.cp_logits;
     if constexpr (kFp8<WT>) o.sc = p.s_cp_heads + (size_t)st.j * p.Vc;
   } else {
     K = p.Dt;
     T = 1;
-    nrows = p.Vt;
+    rg = &pl.head[1];
+    rpc = pl.rpc[1];
     o.out = p.pending_logits + (size_t)p.sid * p.Vt;
     o.sc = p.s_head;
   }
@@ -2067,13 +2104,11 @@ __device__ __forceinline__ void rows_step(Cons c, const Step& st) {
       t0 = Tp - 1;
       if (!cp) hout = p.pending_h + (size_t)p.sid * p.Dt;
     }
-    load_norm<GT>(c, src, k - 1, tag_of(L.s - 1), t0, T, K, g, fold, hout);
-    inv0 = norm_inv(0, K);
-    inv1 = T > 1 ? norm_inv(1, K) : 0.f;
+    load_norm<GT>(c, src, k - 1, tag_of(L.s - 1), t0, T, K, sd, g, fold, hout);
+    inv0 = norm_inv(0, sd);
+    inv1 = T > 1 ? norm_inv(1, sd) : 0.f;
   }
-  int lo, hi;
-  split(nrows, p.ncta, ccta(), lo, hi);
-  stream_rows<WT>(c, lo, hi, K, T, soff(fk_sm()->u.g.xs), o, inv0, inv1);
+  stream_rows<WT>(c, *rg, rpc, K, T, soff(fk_sm()->u.g.xs), o, inv0, inv1);
   FK_MARK(TR_SUB, 8);
   // no grid barrier after a row GEMV: its readers wait for the outputs' tags
   // (the Talker head is the frame's last step); the CTA's warps still meet,
@@ -2112,7 +2147,18 @@ __device__ void consumer() {
       for (int i = ctid(); i < tp; i += FK_CONSUMERS)
         sm->tpage[i] = (p.newpage >= 0 && i == (p.pos >> (__ffs(p.tkv.page_size) - 1))) ? p.newpage
                                                                          : p.tkv.page_table[p.sid * tp + i];
-    if (ctid() == 0) sm->cpage = p.ckv.page_table[p.sid * p.ckv.pages_per_stream];
+    if (ctid() == 0) {
+      sm->cpage = p.ckv.page_table[p.sid * p.ckv.pages_per_stream];
+      // this frame's Talker attention chunk of the CTA: positions [s0, s1)
+      const FKPlan& gp = p.plan[ccta()];
+      const int S = p.pos + 1, cs = (S + gp.cpg - 1) / gp.cpg;
+      sm->ta_s0 = gp.tch * cs;
+      sm->ta_s1 = min(S, sm->ta_s0 + cs);
+    }
+    // this CTA's plan row (read before any phase, after the barrier below)
+    static_assert(sizeof(FKPlan) % 4 == 0 && sizeof(FKPlan) / 4 <= FK_CONSUMERS, "one plan word per consumer thread");
+    if (ctid() < (int)(sizeof(FKPlan) / 4))
+      reinterpret_cast<int*>(&sm->plan)[ctid()] = reinterpret_cast<const int*>(p.plan + ccta())[ctid()];
     // rope rows: CodePredictor positions 0..15 and the Talker position
     const int half = p.hd / 2;
     for (int e = ctid(); e < 17 * half; e += FK_CONSUMERS) {
@@ -2138,7 +2184,7 @@ __device__ void consumer() {
     // before any CTA adds into them
     const FKParams& p = *fk_prm();
     int lo, hi;
-    cta_slice(p.xstride, lo, hi);
+    cta_slice(2, lo, hi);
     float* a0 = xattn(p, 0);
     float* f0 = xffn(p, 0, 0);
     for (int i = lo + ctid(); i < hi; i += FK_CONSUMERS) {
@@ -2177,8 +2223,7 @@ __device__ void consumer() {
         phase_talker_oproj<WT>(c, (int)L.layer, tag_of(L.s - 1), st.l);
         break;
       case S_FFN:
-        phase_ffn<WT>(c, cp ? fk_prm()->Dc : fk_prm()->Dt, cp ? fk_prm()->Fc : fk_prm()->Ft, T, (int)L.layer,
-                      (cp ? fk_prm()->cl : fk_prm()->tl) + st.l);
+        phase_ffn<WT>(c, cp ? 0 : 1, T, (int)L.layer, (cp ? fk_prm()->cl : fk_prm()->tl) + st.l);
         break;
       default:
         rows_step<WT>(c, st);
@@ -2544,6 +2589,7 @@ static size_t fk_layout(const q3tts_config& c, int ncta, FKState* st, char* base
   char* sideC = take((size_t)c.cp_layers * (2 * c.cp_hidden + 2 * hd) * gsz);
   char* tl = take(sizeof(LayerDev) * c.talker_layers);
   char* cl = take(sizeof(LayerDev) * c.cp_layers);
+  char* plan = take(sizeof(FKPlan) * ncta);
   char* xb = take(sizeof(float) * 2 * xst);
   char* xa = take(sizeof(float) * 2 * xst);
   char* xf = take(sizeof(float) * 2 * FK_KC * xst);
@@ -2556,6 +2602,7 @@ static size_t fk_layout(const q3tts_config& c, int ncta, FKState* st, char* base
     st->base = base;
     st->tl = (LayerDev*)tl;
     st->cl = (LayerDev*)cl;
+    st->plan = (FKPlan*)plan;
     st->xb = (float*)xb; st->xa = (float*)xa; st->xf = (float*)xf;
     st->qkv = (uint64_t*)qkv; st->z = (uint64_t*)z; st->part = (uint64_t*)part; st->cp_logits = (uint64_t*)lg;
     st->bar = (unsigned*)sync;
@@ -2570,6 +2617,65 @@ static size_t fk_layout(const q3tts_config& c, int ncta, FKState* st, char* base
 }
 
 size_t frame_kernel_workspace(const q3tts_config& c, int) { return fk_layout(c, FK_MAXCTA, nullptr, nullptr) + 256; }
+
+// The CTAs' plan rows: the producer's split of every phase (the same
+// arithmetic it does on the device), with the chunk counts the consumers walk.
+static void fk_plan(const q3tts_config& c, int ncta, std::vector<FKPlan>& plan) {
+  const int esz = mat_esz(c.weight_dtype);
+  const int D[2] = {c.cp_hidden, c.talker_hidden}, F[2] = {c.cp_ffn, c.talker_ffn},
+            V[2] = {c.cp_vocab, c.codec_vocab};
+  const int qkv_rows = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+  const int SL[3] = {c.cp_hidden, c.talker_hidden, fk_xstride(c)};
+  auto part = [&](int n, int i, int& lo, int& hi) {
+    lo = (int)((unsigned)n * (unsigned)i / (unsigned)ncta);
+    hi = (int)((unsigned)n * (unsigned)(i + 1) / (unsigned)ncta);
+  };
+  auto rows_pc = [](int rb) {
+    const int r = FK_STAGE / rb;
+    return r < 1 ? 1 : (r > FK_RMAX ? FK_RMAX : r);
+  };
+  auto units_pc = [](int rb) {
+    const int u = FK_STAGE / (2 * rb);
+    return u < 1 ? 1 : (u > FK_RMAX / 2 ? FK_RMAX / 2 : u);
+  };
+  auto range = [&](int n, int i, int per, FKRange& r) {
+    part(n, i, r.lo, r.hi);
+    r.nch = r.hi > r.lo ? (r.hi - r.lo + per - 1) / per : 0;
+  };
+  plan.assign(ncta, FKPlan{});
+  for (int i = 0; i < ncta; ++i) {
+    FKPlan& q = plan[i];
+    for (int sd = 0; sd < 2; ++sd) {
+      q.rpc[sd] = rows_pc(D[sd] * esz);
+      q.upc[sd] = units_pc(D[sd] * esz);
+      q.invD[sd] = 1.0f / (float)D[sd];
+      range(qkv_rows, i, q.rpc[sd], q.qkv[sd]);
+      range(V[sd], i, q.rpc[sd], q.head[sd]);
+      range(F[sd], i, q.upc[sd], q.ffn[sd]);
+      q.ffn_nd[sd] = q.ffn[sd].hi > q.ffn[sd].lo ? (q.ffn[sd].hi - q.ffn[sd].lo + q.rpc[sd] - 1) / q.rpc[sd] : 0;
+      const int nt = (D[sd] + 31) / 32;
+      part(c.n_q_heads * nt, i, q.op_t0[sd], q.op_t1[sd]);
+      q.op_h0[sd] = q.op_t0[sd] / nt;
+      q.op_h1[sd] = (q.op_t1[sd] - 1) / nt;
+      q.inv_nt[sd] = 1.0f / (float)nt;
+    }
+    q.cpg = std::max(1, ncta / c.n_kv_heads);  // as the partials' layout (fk_layout)
+    q.tg = i / q.cpg;
+    q.tch = i % q.cpg;
+    int hs = 0, rs = 0;
+    while ((1 << hs) < c.head_dim) ++hs;
+    while ((1 << rs) < c.n_q_heads / c.n_kv_heads) ++rs;
+    q.hd_shift = hs;
+    q.rep_shift = rs;
+    q.inv_hd = 1.0f / (float)c.head_dim;
+    q.attn_scale = 1.0f / std::sqrt((float)c.head_dim);
+    range(c.cp_hidden, i, q.rpc[1], q.proj);  // rows of width D_t
+    for (int w = 0; w < 3; ++w) {
+      q.sl_lo[w] = SL[w] * i / ncta;
+      q.sl_hi[w] = SL[w] * (i + 1) / ncta;
+    }
+  }
+}
 
 template <class WT, class KT>
 static void* kernel_ptr() {
@@ -2619,8 +2725,11 @@ int frame_kernel_create(q3tts_handle* h) {
   // RMSNorm staging holds at most FK_DMAX values: the CodePredictor's first
   // pass stages two tokens
   if (FK_TMAX * c.cp_hidden > FK_DMAX) return Q3TTS_OK;
-  // cache pages of a power-of-two size (positions split by shift and mask)
-  if (c.page_size & (c.page_size - 1)) return Q3TTS_OK;
+  // cache pages and heads of a power-of-two size (positions and head
+  // elements split by shift and mask), at least one warp wide
+  if ((c.page_size & (c.page_size - 1)) || (c.head_dim & (c.head_dim - 1)) || c.head_dim < 32 ||
+      c.n_q_heads % c.n_kv_heads)
+    return Q3TTS_OK;
   // tags number a frame's steps below FK_MAXSTEPS
   const int steps = (Q3TTS_N_CODEBOOKS - 1) * (2 + (c.talker_hidden != c.cp_hidden ? 1 : 0) + 3 * c.cp_layers) +
                     2 + 4 * c.talker_layers;
@@ -2693,7 +2802,10 @@ int frame_kernel_create(q3tts_handle* h) {
   for (int l = 0; l < c.cp_layers; ++l)
     if (!fill(h->cl[l], cl[l], c.cp_hidden, c.cp_ffn, st->sideC + (size_t)l * (2 * c.cp_hidden + 2 * hd) * gsz))
       return Q3TTS_ERR_CUDA;
-  if (cudaMemcpyAsync(st->tl, tl.data(), sizeof(LayerDev) * tl.size(), cudaMemcpyHostToDevice, h->s) != cudaSuccess ||
+  std::vector<FKPlan> plan;
+  fk_plan(c, ncta, plan);
+  if (cudaMemcpyAsync(st->plan, plan.data(), sizeof(FKPlan) * plan.size(), cudaMemcpyHostToDevice, h->s) != cudaSuccess ||
+      cudaMemcpyAsync(st->tl, tl.data(), sizeof(LayerDev) * tl.size(), cudaMemcpyHostToDevice, h->s) != cudaSuccess ||
       cudaMemcpyAsync(st->cl, cl.data(), sizeof(LayerDev) * cl.size(), cudaMemcpyHostToDevice, h->s) != cudaSuccess ||
       cudaMemsetAsync(st->bar, 0, sizeof(unsigned) * 4, h->s) != cudaSuccess ||
       cudaStreamSynchronize(h->s) != cudaSuccess)
@@ -2731,7 +2843,7 @@ static void frame_params(FKParams& p, const q3tts_handle* h, int sid, int pos, i
   p.Lt = c.talker_layers; p.Lc = c.cp_layers; p.qkv_rows = h->qkv_rows;
   p.has_proj = h->w.cp_w_proj != nullptr; p.qk_norm = c.qk_norm; p.dmax = st->dmax; p.eps = c.rms_eps;
   p.xstride = fk_xstride(c);
-  p.tl = st->tl; p.cl = st->cl;
+  p.tl = st->tl; p.cl = st->cl; p.plan = st->plan;
   p.t_head = h->w.talker_w_head; p.e_codec = h->w.talker_e_codec; p.cp_heads = h->w.cp_heads;
   p.cp_embeds = h->w.cp_embeds; p.cp_proj = h->w.cp_w_proj; p.t_gfinal = h->w.talker_g_final;
   p.cp_gfinal = h->w.cp_g_final;
