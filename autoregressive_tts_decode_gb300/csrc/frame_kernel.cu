@@ -73,7 +73,7 @@ constexpr int FK_PREFETCH_THREADS = 32;  // one warp; one thread issues L2 prefe
 constexpr int FK_THREADS = FK_PRODUCER_THREADS + FK_CONSUMERS + FK_PREFETCH_THREADS;
 constexpr int FK_STAGE = 8192;  // one ring chunk: 2 rows of 2048 bf16, one o_proj tile of 32 x 128 bf16
 constexpr int FK_NSTAGE = 20;
-constexpr int FK_PF_AHEAD = 0;  // default distance (chunks) the L2 prefetch runs ahead of the ring: off (deeper prefetch queues up memory traffic that delays the latency-bound phases)
+constexpr int FK_PF_AHEAD = 8;  // default distance (chunks) the L2 prefetch runs ahead of the ring (measured on GB300: 8 best of 0, 8, 24, 64; deeper prefetch queues up memory traffic that delays the latency-bound phases)
 constexpr int FK_TMAX = 2;     // tokens per pass (CodePredictor pass 0 carries two)
 constexpr int FK_DMAX = 2048;  // widest hidden state staged in shared memory
 constexpr int FK_HDMAX = 128;
@@ -1765,14 +1765,30 @@ __device__ __forceinline__ void ffn_down(Stream& s, int D, int f0, int f1, int r
     const int fb = f0 + (int)(n - n0) * rpc, R = min(rpc, f1 - fb);
     if (active) {
       const uint32_t w = buf + (uint32_t)(col * (int)sizeof(WT));
-      for (int r = 0; r < R; ++r) {
-        float d8[8];
-        lds_w8<WT>(w + (uint32_t)(r * rb), d8);
+      if (R == 4) {  // a full chunk of four rows: every load first, then the multiplies
+        float d8[4][8], a[4][T];
 #pragma unroll
-        for (int t = 0; t < T; ++t) {
-          const float a = act[t][fb - f0 + r];
+        for (int r = 0; r < 4; ++r) {
+          lds_w8<WT>(w + (uint32_t)(r * rb), d8[r]);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) y[t][k] = fmaf(a, d8[k], y[t][k]);
+          for (int t = 0; t < T; ++t) a[r][t] = act[t][fb - f0 + r];
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int t = 0; t < T; ++t)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) y[t][k] = fmaf(a[r][t], d8[r][k], y[t][k]);
+      } else {
+        for (int r = 0; r < R; ++r) {
+          float d8[8];
+          lds_w8<WT>(w + (uint32_t)(r * rb), d8);
+#pragma unroll
+          for (int t = 0; t < T; ++t) {
+            const float a = act[t][fb - f0 + r];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) y[t][k] = fmaf(a, d8[k], y[t][k]);
+          }
         }
       }
     }
@@ -1822,17 +1838,6 @@ __device__ __forceinline__ void phase_ffn(Cons c, int sd, int T, int k, const La
   const int D = sd ? p.Dt : p.Dc, F = sd ? p.Ft : p.Fc;
   load_norm<GT>(c, SRC_RES_A, k, 0u, 0, T, D, sd, side_cur<GT>(c) + D, -1, nullptr);
   side_end(c);
-  {
-    int lo, hi;
-    cta_slice(2, lo, hi);
-    float* a1 = xattn(p, k + 1);
-    float* f1 = xffn(p, k + 1, 0);
-    for (int i = lo + ctid(); i < hi; i += FK_CONSUMERS) {
-      a1[i] = 0.f;
-#pragma unroll
-      for (int q = 0; q < FK_KC; ++q) f1[q * p.xstride + i] = 0.f;
-    }
-  }
   const float inv0 = norm_inv(0, sd), inv1 = T > 1 ? norm_inv(1, sd) : 0.f;
   const int f0 = pl.ffn[sd].lo, f1 = pl.ffn[sd].hi;
   const int rb = D * (int)sizeof(WT);
@@ -1863,6 +1868,20 @@ __device__ __forceinline__ void phase_ffn(Cons c, int sd, int T, int k, const La
   }
   warp_set(cst().n, n0 + nch);
   n0 += nch;
+  if (s.warp == (int)(n0 % FK_CONSUMER_WARPS)) {
+    // the CTA's slice of layer k + 1's deltas is cleared here, by the warp
+    // the next chunk would have gone to: the round-robin gave it the fewest
+    // gate/up chunks, so it would wait below anyway
+    int lo, hi;
+    cta_slice(2, lo, hi);
+    float* a1 = xattn(p, k + 1);
+    float* f1 = xffn(p, k + 1, 0);
+    for (int i = lo + s.lane; i < hi; i += 32) {
+      a1[i] = 0.f;
+#pragma unroll
+      for (int q = 0; q < FK_KC; ++q) f1[q * p.xstride + i] = 0.f;
+    }
+  }
   consumer_sync();  // act complete
   if (T == 1)
     ffn_down<WT, 1>(s, D, f0, f1, pl.rpc[sd], (uint32_t)pl.ffn_nd[sd], n0, k, lw->s_d);
