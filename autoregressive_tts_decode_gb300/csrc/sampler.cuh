@@ -314,8 +314,8 @@ struct FastSamplerSmem {
   unsigned long long cand[FAST_CAP];
   unsigned long long top[FAST_NW * FAST_TOP];
   unsigned long long sorted[SAMPLER_KSMALL];
-  float w[SAMPLER_KSMALL];
-  float run[SAMPLER_KSMALL];
+  alignas(16) float w[SAMPLER_KSMALL];    // (read as float4 by the running sums)
+  alignas(16) float run[SAMPLER_KSMALL];
   uint32_t keys[SAMPLER_VMAX];  // the fallback selection's copy of the value keys
   int wc[2][FAST_NW];
   int wscan[FAST_NW];
@@ -425,7 +425,8 @@ __device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits
   const bool pen = history != nullptr && rep != 1.0f;
   // value keys of the thread's logits (float4 q: elements 4 (tid + FAST_NT q)
   // .. + 3) into sm.keys, the lane's largest (key, index) kept: rolled loops,
-  // so the float divisions of the rule appear once in the code
+  // so the float divisions of the rule appear once in the code (unrolling the
+  // inner loop measured slower)
   unsigned long long lm = 0ull;
 #pragma unroll 1
   for (int q = 0; q < FAST_V4; ++q) {
@@ -497,6 +498,7 @@ __device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits
   } else if (tid < C) {
     const unsigned long long my = sm.cand[tid];
     int rank = 0;
+#pragma unroll 8
     for (int j = 0; j < C; ++j) rank += sm.cand[j] > my ? 1 : 0;
     if (rank < K) sm.sorted[rank] = my;
   }
@@ -504,10 +506,22 @@ __device__ __noinline__ int fast_sample(FastSamplerSmem& sm, const float* logits
   if (tid < K) sm.w[tid] = exp_cw(__fsub_rn(key_value(sm.sorted[tid]), key_value(sm.sorted[0])));
   G::sync();
   if (warp == 0) {
-    // running sums in order (one thread: the float rule's summation order)
+    // running sums in order (one thread: the float rule's summation order);
+    // the weights are read in blocks of four ahead of the dependent adds
     if (lane == 0) {
       float run = 0.0f;
-      for (int i = 0; i < K; ++i) {
+      int i = 0;
+#pragma unroll 1
+      for (; i + 4 <= K; i += 4) {
+        const float4 wv = *reinterpret_cast<const float4*>(&sm.w[i]);
+        float4 rv;
+        rv.x = run = __fadd_rn(run, wv.x);
+        rv.y = run = __fadd_rn(run, wv.y);
+        rv.z = run = __fadd_rn(run, wv.z);
+        rv.w = run = __fadd_rn(run, wv.w);
+        *reinterpret_cast<float4*>(&sm.run[i]) = rv;
+      }
+      for (; i < K; ++i) {
         run = __fadd_rn(run, sm.w[i]);
         sm.run[i] = run;
       }
