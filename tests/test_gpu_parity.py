@@ -272,6 +272,31 @@ def test_persistent_kernel_matches_layered_step(q3, oracle_mod, shape_name):
         assert pu.sampler_replay(oracle_mod, shape, sp, codes[0], logits[0], out[True][0][0], u[0]) == 0
 
 
+def test_page_size_off_powers_of_two_takes_the_layered_step(q3, oracle_mod, tiny_weights):
+    """The persistent kernel splits cache positions by shift and mask, so it is
+    set up for power-of-two page sizes only; a 12-position page decodes through
+    the one-kernel-per-operation step, with the same greedy codes as the oracle
+    (the prompt spans two pages, the frames a third)."""
+    W, Wd = tiny_weights
+    p = synth.make_prompts(TINY.shape, [21])[0]
+    frames = 6
+    orc = oracle_mod.Oracle(TINY.shape, W, 1, 64)
+    oc, ol = pu.run_oracle(orc, 0, p.numpy(), synth.GREEDY, frames)
+    per_frame = {}
+    for ps in (16, 12):
+        eng = _engine(q3, TINY.shape, Wd, cap=64, page_size=ps)
+        eng.prefill(0, p.cuda())
+        eng.sync()
+        l0 = eng.kernel_launches()
+        codes, logits = pu.run_gpu(eng, [0], [p], synth.GREEDY, frames, prefill=False)
+        per_frame[ps] = (eng.kernel_launches() - l0) / frames
+        eng.close()
+        assert np.array_equal(codes[0], oc), ps
+        assert np.max(np.abs(logits[0] - ol)) < TOL_F32, ps
+    assert per_frame[16] == 1          # one persistent launch per frame
+    assert per_frame[12] > 1           # the layered step
+
+
 @pytest.mark.parametrize("kv", ["f32", "bf16"])
 def test_long_contexts_split_attention(q3, oracle_mod, tiny_weights, kv):
     """Streams whose contexts span several 64-position spans: the layered step and a
