@@ -129,18 +129,20 @@ TINY_SHAPE = ModelShape(talker_layers=2, talker_hidden=256, talker_ffn=768, cp_l
                         cp_hidden=256, cp_ffn=768, n_q_heads=4, n_kv_heads=2, head_dim=64,
                         codec_vocab=3072, cp_vocab=2048, weight_dtype=DTYPE_F32,
                         kv_dtype=DTYPE_F32)
-# The batch-1 and batched-16 workloads fix bf16 for the weights only; their
-# Talker KV cache stays fp32 (bf16 KV moves 1.7B logits by ~0.036 against the
-# fp64 oracle, over the 3e-2 tolerance).  The serving workload fixes bf16 KV.
+# The 0.6B, 1.7B, batched and serving workloads keep bf16 weights and a bf16
+# Talker KV cache (the oracle rounds its cached k, v to bf16 likewise); the
+# CodePredictor cache is fp32.  SHAPE_17B_KV32 is the 1.7B shape with an fp32
+# Talker cache, which the library also takes.
 SHAPE_06B = ModelShape(talker_layers=28, talker_hidden=1024, talker_ffn=3072, cp_layers=5,
                        cp_hidden=1024, cp_ffn=3072, n_q_heads=16, n_kv_heads=8, head_dim=128,
                        codec_vocab=3072, cp_vocab=2048, weight_dtype=DTYPE_BF16,
-                       kv_dtype=DTYPE_F32)
+                       kv_dtype=DTYPE_BF16)
 SHAPE_17B = ModelShape(talker_layers=28, talker_hidden=2048, talker_ffn=6144, cp_layers=5,
                        cp_hidden=1024, cp_ffn=3072, n_q_heads=16, n_kv_heads=8, head_dim=128,
                        codec_vocab=3072, cp_vocab=2048, weight_dtype=DTYPE_BF16,
-                       kv_dtype=DTYPE_F32)
-SHAPE_17B_KV16 = dataclasses.replace(SHAPE_17B, kv_dtype=DTYPE_BF16)
+                       kv_dtype=DTYPE_BF16)
+SHAPE_17B_KV16 = SHAPE_17B
+SHAPE_17B_KV32 = dataclasses.replace(SHAPE_17B, kv_dtype=DTYPE_F32)
 SHAPE_17B_FP8 = dataclasses.replace(SHAPE_17B, weight_dtype=DTYPE_FP8)
 
 WORKLOADS: Dict[str, Workload] = {

@@ -484,7 +484,9 @@ def main():
             "rtf": synth.FRAMES_PER_SECOND / (value / world),
             "config": {"workload": wl.name, "streams_per_gpu": B,
                        "prompt_len": lens if B > 1 else lens[0], "kv_cap": wl.kv_cap,
-                       "page_size": wl.page_size, "frames_per_episode": wl.frames,
+                       "page_size": wl.page_size,
+                       "kv_cache": {synth.DTYPE_F32: "fp32", synth.DTYPE_BF16: "bf16"}.get(s.kv_dtype, "?"),
+                       "frames_per_episode": wl.frames,
                        "sampling": "greedy" if not wl.sampling.do_sample else "top_k50_T0.9_rep1.05",
                        "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2: each step streams %.2f GB of weights"

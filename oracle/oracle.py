@@ -190,14 +190,20 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
     return o
 
 
+# The model shapes' code for a bf16 tensor (their weight_dtype / kv_dtype fields).
+DTYPE_BF16_KV = 1
+
+
 class Oracle:
     """The oracle model over CPU weight tensors (fp32 or bf16 torch tensors)."""
 
     def __init__(self, shape, weights: Dict[str, "object"], n_streams: int, kv_cap: int,
-                 kv_bf16: bool = False):
+                 kv_bf16: Optional[bool] = None):
         """kv_bf16: the Talker KV cache holds bf16 values (each cached k, v is
-        rounded to fp32 and then to the nearest bf16), as in the serving
-        configuration whose cache is bf16."""
+        rounded to fp32 and then to the nearest bf16), as in a configuration
+        whose cache is bf16.  None: as the shape's kv_dtype says."""
+        if kv_bf16 is None:
+            kv_bf16 = shape.kv_dtype == DTYPE_BF16_KV
         L = lib()
         self.shape = shape
         self.n_streams = n_streams

@@ -45,7 +45,7 @@ def test_page_closed_form_arithmetic():
 
 
 def test_algorithmic_frame_bytes_1p7b():
-    s = synth.SHAPE_17B
+    s = synth.SHAPE_17B_KV32  # the fp32 Talker cache; the bf16 one below
     fb = bm.frame_bytes(s, 128)
     # Talker: 28 layers x (QKV 16.8 + o 8.4 + gate/up 50.3 + down 25.2 MB) + head 12.6 MB
     assert fb.talker_weights / 1e9 == pytest.approx(2.831, abs=0.001)
@@ -55,7 +55,7 @@ def test_algorithmic_frame_bytes_1p7b():
     # + CodePredictor KV (fp32, 5 layers x 135 positions x 8 KB) ~ 5.5 MB
     run = bm.run_bytes(s, 128, 240) / 240
     assert run / 1e9 == pytest.approx(2.831 + 15 * 0.1657 + 0.0571 + 0.0055, abs=0.002)
-    kv16 = bm.run_bytes(synth.SHAPE_17B_KV16, 128, 240) / 240
+    kv16 = bm.run_bytes(synth.SHAPE_17B, 128, 240) / 240
     assert (run - kv16) / 1e9 == pytest.approx(0.0286, abs=0.001)
 
 
@@ -63,9 +63,9 @@ def test_algorithmic_frame_bytes_0p6b():
     s = synth.SHAPE_06B
     fb = bm.frame_bytes(s, 64)
     assert fb.cp_pass_weights / 1e6 == pytest.approx(161.5, abs=0.1)
-    # Talker 0.887 GB + 15 passes + fp32 Talker KV (~184 positions) + CodePredictor KV
+    # Talker 0.887 GB + 15 passes + bf16 Talker KV (~184 positions) + fp32 CodePredictor KV
     run = bm.run_bytes(s, 64, 240) / 240
-    assert run / 1e9 == pytest.approx(0.887 + 15 * 0.1615 + 0.0423 + 0.0055, abs=0.002)
+    assert run / 1e9 == pytest.approx(0.887 + 15 * 0.1615 + 0.0423 / 2 + 0.0055, abs=0.002)
 
 
 def test_talker_module_below_page_figure():

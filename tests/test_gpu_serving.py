@@ -40,7 +40,7 @@ FRAMES = 2
 CASES = {
     # name: (workload, oracle cache in bf16)
     "serving128": ("serving128", True),
-    "batched16": ("batched16", False),
+    "batched16": ("batched16", True),
 }
 
 
@@ -90,7 +90,11 @@ def test_many_streams_full_shapes(q3, oracle_mod, case):
         c1, l1 = pu.run_gpu(one, [0], [prompts[k]], wl.sampling, FRAMES, uniforms=u[k:k + 1],
                             forced=codes[k:k + 1])
         one.close()
-        assert float(np.max(np.abs(l1[0] - logits[k]))) < 2e-3
+        # the same arithmetic up to fp32 reassociation (split-K atomics); with a
+        # bf16 cache that can also send a cached k or v to the other bf16
+        # neighbour (2^-8 relative), which moves logits by a few 1e-3
+        same = 1e-2 if s.kv_dtype == synth.DTYPE_BF16 else 2e-3
+        assert float(np.max(np.abs(l1[0] - logits[k]))) < same
         assert pu.sampler_replay(oracle_mod, s, wl.sampling, c1[0], l1[0], codes[k], u[k]) == 0
         assert pu.sampler_replay(oracle_mod, s, wl.sampling, codes[k], logits[k], codes[k], u[k]) == 0
     del Wd

@@ -55,14 +55,18 @@ def _static(eng, sp, u, c, fc, lg):
     eng.step_frame_static(0, sp, u[0], c, forced=fc, logits=lg)
 
 
-@pytest.mark.parametrize("name,tol", [("tiny", 2e-5), ("0.6b", 1e-3)])
+@pytest.mark.parametrize("name,tol", [("tiny", 2e-5), ("0.6b", 1e-2)])
 def test_static_scratch_frame_matches_step_frame(q3, oracle_mod, name, tol):
     """Stream A runs two frames through q3tts_step_frame; stream B, on another
     handle with the same weights and prompt, runs them through
     q3tts_step_frame_static, teacher-forced with A's codes.  Both run the same
     kernel, so the logits agree up to float-atomic reassociation (tiny fp32:
-    2e-5; 0.6B bf16 weights: 1e-3, well inside the 3e-2 parity bound), the codes
-    agree, and B's draws follow the float sampling rule on B's own logits."""
+    2e-5; 0.6B, bf16 weights and Talker cache: 1e-2, as reassociation can also
+    send a cached k or v to the other bf16 neighbour -- measured 0.0026 -- well
+    inside the 3e-2 parity bound), and B's draws follow the float sampling rule
+    on B's own logits.  With an fp32 cache the codes agree too; with a bf16 one
+    a draw whose uniform sits near a boundary of the cumulative weights may go
+    the other way (B is teacher-forced, so its state does not follow its draws)."""
     wl = synth.WORKLOADS[name]
     shape = wl.shape
     W, Wd = pu.gpu_weights(shape, gen_device="cuda" if name != "tiny" else "cpu")
@@ -84,7 +88,8 @@ def test_static_scratch_frame_matches_step_frame(q3, oracle_mod, name, tol):
     assert lena == lenb == p.shape[0] + FRAMES
     err = float(np.max(np.abs(la - lb)))
     assert err < tol, err
-    assert np.array_equal(ca, cb)
+    if shape.kv_dtype == synth.DTYPE_F32:
+        assert np.array_equal(ca, cb)
     assert pu.sampler_replay(oracle_mod, shape, sp, cb, lb, ca, u[0]) == 0
 
 
