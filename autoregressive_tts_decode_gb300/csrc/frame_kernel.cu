@@ -1480,9 +1480,41 @@ __device__ __forceinline__ void phase_cp_attn(Cons c, int layer, int T, int pos0
 // Talker phase B1: attention partials.  Work item = (kv group g, position
 // chunk); the q heads of the group share the K/V reads.  The item holding the
 // current position appends its k, v to the cache.
-// K and v rows of Talker positions sb and sb + 8 of kv group g (cached
-// positions from the cache; the current position: v from the QKV rows and a
-// zero key, which the caller replaces; beyond it: zeros).
+// J (1, 2 or 4) consecutive elements of a cache row, widened: one vector load.
+template <class KT>
+__device__ __forceinline__ void ld_kv(const KT* p, int J, float (&o)[4]);
+template <>
+__device__ __forceinline__ void ld_kv<float>(const float* p, int J, float (&o)[4]) {
+  o[1] = o[2] = o[3] = 0.f;
+  if (J == 4) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  } else if (J == 2) {
+    const float2 a = *reinterpret_cast<const float2*>(p);
+    o[0] = a.x; o[1] = a.y;
+  } else {
+    o[0] = *p;
+  }
+}
+template <>
+__device__ __forceinline__ void ld_kv<bf16>(const bf16* p, int J, float (&o)[4]) {
+  o[1] = o[2] = o[3] = 0.f;
+  if (J == 4) {
+    const uint2 a = *reinterpret_cast<const uint2*>(p);
+    o[0] = __uint_as_float(a.x << 16); o[1] = __uint_as_float(a.x & 0xffff0000u);
+    o[2] = __uint_as_float(a.y << 16); o[3] = __uint_as_float(a.y & 0xffff0000u);
+  } else if (J == 2) {
+    const uint32_t a = *reinterpret_cast<const uint32_t*>(p);
+    o[0] = __uint_as_float(a << 16); o[1] = __uint_as_float(a & 0xffff0000u);
+  } else {
+    o[0] = to_f(*p);
+  }
+}
+
+// K and v rows of Talker positions sb and sb + 8 of kv group g, lane l holding
+// elements J l .. J l + J - 1 of each (cached positions from the cache; the
+// current position: v from the QKV rows and a zero key, which the caller
+// replaces; beyond it: zeros).
 template <class KT>
 __device__ __forceinline__ void talker_kv_rows(const FKParams& p, int layer, int g, int pos, int sb, int J,
                                                uint32_t qtag, float (&k)[2][4], float (&v)[2][4]) {
@@ -1490,24 +1522,21 @@ __device__ __forceinline__ void talker_kv_rows(const FKParams& p, int layer, int
   for (int b = 0; b < 2; ++b) {
     const int sp = sb + b * FK_CONSUMER_WARPS;
     if (sp < pos) {
-      const KT* kc = (const KT*)p.tkv.pool + tkv_offset(p, layer, sp, 0, g);
-      const KT* vc = (const KT*)p.tkv.pool + tkv_offset(p, layer, sp, 1, g);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        k[b][j] = j < J ? to_f(kc[clane() + 32 * j]) : 0.f;
-        v[b][j] = j < J ? to_f(vc[clane() + 32 * j]) : 0.f;
-      }
+      const KT* kc = (const KT*)p.tkv.pool + tkv_offset(p, layer, sp, 0, g) + J * clane();
+      const KT* vc = (const KT*)p.tkv.pool + tkv_offset(p, layer, sp, 1, g) + J * clane();
+      ld_kv<KT>(kc, J, k[b]);
+      ld_kv<KT>(vc, J, v[b]);
     } else {
 #pragma unroll
       for (int j = 0; j < 4; ++j) k[b][j] = v[b][j] = 0.f;
       if (sp == pos) {  // v of the current position: the tagged QKV rows
-        const int vo = (p.Hq + p.Hkv + g) * p.hd + clane();
+        const int vo = (p.Hq + p.Hkv + g) * p.hd + J * clane();
         uint64_t raw[4];
         int off[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          off[j] = vo + 32 * j;
-          raw[j] = j < J ? ld_relaxed64(p.qkv + vo + 32 * j) : tag_filler(qtag);
+          off[j] = vo + j;
+          raw[j] = j < J ? ld_relaxed64(p.qkv + vo + j) : tag_filler(qtag);
         }
         tag_resolve<4>(raw, p.qkv, off, qtag);
 #pragma unroll
@@ -1587,7 +1616,7 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer, uint32_t qt
         if (sb + b * FK_CONSUMER_WARPS == pos) {
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            if (j < J) k[b][j] = as.kcur[0][clane() + 32 * j];
+            if (j < J) k[b][j] = as.kcur[0][J * clane() + j];
         }
 #pragma unroll
       for (int b = 0; b < BATCH; ++b) {
@@ -1596,10 +1625,10 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer, uint32_t qt
 #pragma unroll
           for (int r = 0; r < FK_REPMAX; ++r) {
             if (r < rep) {
-              float d = 0.f;
+              float d = 0.f;  // lane l: elements J l .. J l + J - 1
 #pragma unroll
               for (int j = 0; j < 4; ++j)
-                if (j < J) d = fmaf(as.q[r][clane() + 32 * j], k[b][j], d);
+                if (j < J) d = fmaf(as.q[r][J * clane() + j], k[b][j], d);
               d = warp_sum(d) * scale;
               const float mn = fmaxf(m[r], d), corr = __expf(m[r] - mn), e = __expf(d - mn);
               l[r] = l[r] * corr + e;
@@ -1620,7 +1649,7 @@ __device__ __forceinline__ void phase_talker_attn(Cons c, int layer, uint32_t qt
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if (j < J) as.o[cwarp()][r][clane() + 32 * j] = o[r][j];
+          if (j < J) as.o[cwarp()][r][J * clane() + j] = o[r][j];
       }
     }
     consumer_sync();
