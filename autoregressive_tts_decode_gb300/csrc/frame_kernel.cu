@@ -17,9 +17,8 @@
 //    through a 20-deep ring of 8 KB chunks in shared memory with 1-D bulk
 //    copies (cp.async.bulk + mbarrier transaction counts, L2 evict-first).
 //    Weights do not depend on activations, so the stream runs ahead across
-//    phase boundaries.  An optional second warp prefetches further ahead
-//    into L2 (off by default: the extra traffic delays the latency-bound
-//    phases).
+//    phase boundaries.  A second warp prefetches 8 chunks further ahead into
+//    L2 (a deeper prefetch delays the latency-bound phases).
 //  * Eight consumer warps.  A private chunk (rows of a GEMV, an o_proj tile,
 //    gate and up rows) belongs to one warp, which computes whole dot
 //    products over it alone; a shared chunk (rows of the transposed down
@@ -46,9 +45,10 @@
 //  * Draws are made redundantly by every CTA from the full logit vector
 //    (sampler.cuh, fast_sample), so a sampled code needs no barrier.
 //  * The frame is a list of steps decoded from a (pass, step) position, each
-//    step kind with one call site, so every phase's code exists once (the
-//    kernel is sensitive to instruction-cache misses); the consumers' loop
-//    state and launch parameters live in shared memory.
+//    step kind with one call site, so every phase's code exists once; the
+//    consumers' loop state, the launch parameters and the CTA's share of
+//    every phase (the plan, computed on the host) live in shared memory, so
+//    that no phase starts with a division or a global load of its bounds.
 //  * The grid barrier is a release-add / acquire-load counter polled by one
 //    thread per CTA.  Every wait (ring slots, side slots, tags, grid barrier)
 //    is bounded; on expiry the kernel records Q3TTS_ERR_TIMEOUT, raises an
@@ -97,7 +97,7 @@ static_assert(FAST_NT == FK_CONSUMERS, "the register sampler runs on the consume
 struct LayerDev {
   const void* side;   // [g_attn D | g_ffn D | g_q hd | g_k hd], weight dtype, contiguous
   const void* w_qkv;
-  const void* w_oT;   // o_proj tiles [Hq][ceil(D/32)][hd/8][32][8] (see oproj_tiles)
+  const void* w_oT;   // o_proj tiles [Hq][ceil(D/32)][hd/8][32][8] (see oproj_step)
   const void* w_gu;   // [2F][D]: gate rows, then up rows (the caller's tensor)
   const void* w_dT;   // [F][D]: W_down transposed, row f = column f of W_down
   // FP8 matrices: per-output-row scales (W_qkv rows, W_o rows = output
