@@ -17,6 +17,7 @@ no exchange step); value = frames of all ranks / max-over-ranks time.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import json
 import math
 import os
@@ -219,6 +220,18 @@ def cpu_baseline(wl, sample_frames=3, prompt_len=16):
                          "sample": "the next 2 frames of the same stream on one thread"}}
 
 
+@contextlib.contextmanager
+def nvtx(name):
+    """A named NVTX range on the host timeline (prefill, warm-up, timed frames,
+    end-to-end frames, each frame), for timeline tools; it adds host work only."""
+    import torch
+    torch.cuda.nvtx.range_push(name)
+    try:
+        yield
+    finally:
+        torch.cuda.nvtx.range_pop()
+
+
 def prefill_and_ttfa(eng, stream, prompt, sampling, u_dev, codes, reps=5):
     """Prefill time of one prompt and the time to the first frame of codes.
 
@@ -239,9 +252,11 @@ def prefill_and_ttfa(eng, stream, prompt, sampling, u_dev, codes, reps=5):
         a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         torch.cuda.synchronize()
         a.record(st)
-        eng.prefill(stream, prompt)
+        with nvtx("prefill"):
+            eng.prefill(stream, prompt)
         b.record(st)
-        eng.step_frame([stream], sampling, u_dev, codes)
+        with nvtx("first frame"):
+            eng.step_frame([stream], sampling, u_dev, codes)
         c.record(st)
         eng.sync()
         torch.cuda.synchronize()
@@ -356,10 +371,11 @@ def main():
     eng = q3tts.Engine(s, W, max_streams=n_streams, kv_cap=wl.kv_cap, page_size=wl.page_size)
     # every episode's streams get their prompts before timing
     prompts = synth.make_prompts(s, lens, device="cuda")
-    for e in range(episodes):
-        for b in range(B):
-            eng.prefill(e * B + b, prompts[b])
-    torch.cuda.synchronize()
+    with nvtx("prefill"):
+        for e in range(episodes):
+            for b in range(B):
+                eng.prefill(e * B + b, prompts[b])
+        torch.cuda.synchronize()
     uni = synth.uniforms(list(range(n_streams)), wl.frames)  # [streams, frames, 16]
     uni_d = torch.from_numpy(uni).to("cuda")
     codes = torch.zeros((B, 16), dtype=torch.int32, device="cuda")
@@ -378,10 +394,11 @@ def main():
         return ids, u
 
     stream = eng.stream
-    for i in range(args.warmup):
-        ids, u = step_args(i)
-        eng.step_frame(ids, wl.sampling, u, codes)
-    eng.sync()
+    with nvtx("warm-up"):
+        for i in range(args.warmup):
+            ids, u = step_args(i)
+            eng.step_frame(ids, wl.sampling, u, codes)
+        eng.sync()
     # pre-build each step's uniforms so the timed loop does no host work
     pre = [step_args(args.warmup + i) for i in range(args.steps)]
     launches0 = eng.kernel_launches()
@@ -394,13 +411,15 @@ def main():
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
-        for i in range(args.steps):
-            ids, u = pre[i]
-            ev[i][0].record(stream)
-            eng.step_frame(ids, wl.sampling, u, codes)
-            ev[i][1].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
+        with nvtx("timed frames"):
+            for i in range(args.steps):
+                ids, u = pre[i]
+                ev[i][0].record(stream)
+                with nvtx("frame"):
+                    eng.step_frame(ids, wl.sampling, u, codes)
+                ev[i][1].record(stream)
+            t_end.record(stream)
+            torch.cuda.synchronize()
     eng.sync()
     launches = eng.kernel_launches() - launches0
     elapsed = t_start.elapsed_time(t_end) / 1e3
@@ -446,14 +465,15 @@ def main():
         plans = [plan(args.warmup + i) for i in range(args.steps)]
         srcs = [host_u[ids[0]:ids[-1] + 1, f] for ids, f in plans]
         torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for i in range(args.steps):
-            ids, f = plans[i]
-            dev_u.copy_(srcs[i], non_blocking=True)
-            eng.step_frame(ids, wl.sampling, dev_u, codes)
-            host_codes.copy_(codes, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
-        dt = time.perf_counter() - t0
+        with nvtx("end-to-end frames"):
+            t0 = time.perf_counter()
+            for i in range(args.steps):
+                ids, f = plans[i]
+                dev_u.copy_(srcs[i], non_blocking=True)
+                eng.step_frame(ids, wl.sampling, dev_u, codes)
+                host_codes.copy_(codes, non_blocking=True)
+                torch.cuda.current_stream().synchronize()
+            dt = time.perf_counter() - t0
         eng.sync()
         dt = slowest(dt, world, "cuda")
         e2e = {"value": job_rate(args.steps * B, world, dt), "unit": UNIT,

@@ -97,3 +97,17 @@ def test_recorded_traffic_only_for_matching_code(tmp_path, monkeypatch):
     assert bench.captured_traffic("1.7b") == 123.0
     src.write_text(src.read_text() + "\nconstexpr int changed = 2;\n")
     assert bench.captured_traffic("1.7b") is None           # the kernel changed since the capture
+
+
+def test_nvtx_ranges_nest_without_a_device():
+    """The bench's NVTX ranges (host timeline markers) open and close in order
+    even on a machine without a GPU, and pass exceptions through."""
+    import bench
+    with bench.nvtx("outer"):
+        with bench.nvtx("inner"):
+            pass
+    try:
+        with bench.nvtx("raises"):
+            raise ValueError("x")
+    except ValueError:
+        pass
