@@ -209,8 +209,13 @@ int q3tts_prefill(q3tts_handle* h, int stream_id, const float* embeds_dev, int l
  * Each stream advances by one Talker position.  Q3TTS_ERR_STATE if a stream
  * has no prompt, Q3TTS_ERR_CAPACITY if its cache is full.
  * Execution: one stream whose configuration and sampling settings the
- * persistent frame kernel covers runs as one launch of that kernel; otherwise
- * the frame runs layer by layer, and without a logits dump that sequence is
+ * persistent frame kernel covers runs as one launch of that kernel.  It covers
+ * hidden sizes up to 2048 (multiples of 8; the CodePredictor's up to 1024),
+ * at most 64 layers in all, power-of-two head sizes from 32 to 128 with at
+ * most 2 query heads per KV head, power-of-two page sizes,
+ * vocabularies up to 4096 (multiples of 4), and draws that are greedy or keep
+ * at most 64 candidates (top_k 1..64).  Otherwise the frame runs layer by
+ * layer, and without a logits dump that sequence is
  * captured into a CUDA graph on the first call for a given n_active (and
  * forced_dev NULL or not) and replayed on later calls, the inputs and codes
  * passing through buffers in the workspace.  Q3TTS_FRAME_KERNEL=0 and
