@@ -305,6 +305,28 @@ def streaming_chunks(eng, stream, prompt, sampling, uni_dev, frames=64, chunks=(
                     "enqueued before the host waits for chunk k"}
 
 
+L2_BYTES = 129e6  # GB300 L2
+
+
+def workload_config(wl, world):
+    """The `config` object of a bench line: the workload as both arms run it."""
+    from autoregressive_tts_decode_gb300 import bytes_model, synth
+    s = wl.shape
+    lens = wl.prompt_lengths()
+    B = wl.streams
+    fb = bytes_model.frame_bytes(s, lens[0])
+    weights = fb.talker_weights + (synth.N_CODEBOOKS - 1) * fb.cp_pass_weights
+    return {"workload": wl.name, "streams_per_gpu": B,
+            "prompt_len": lens if B > 1 else lens[0], "kv_cap": wl.kv_cap,
+            "page_size": wl.page_size,
+            "kv_cache": {synth.DTYPE_F32: "fp32", synth.DTYPE_BF16: "bf16"}.get(s.kv_dtype, "?"),
+            "frames_per_episode": wl.frames,
+            "sampling": "greedy" if not wl.sampling.do_sample else "top_k50_T0.9_rep1.05",
+            "parallelism": f"replicas x{world}",
+            "l2": ("inputs larger than L2: each step streams %.2f GB of weights" if weights > L2_BYTES
+                   else "inputs within L2 (%.2f GB of weights per step): not an L2-cold figure") % (weights / 1e9)}
+
+
 def run_reference(args):
     """The reference arm: the CPU oracle on this workload, bounded per step."""
     rank, world, _ = dist_env()
@@ -334,11 +356,12 @@ def run_reference(args):
             "steps": steps, "warmup": warm, "ms_per_step": 1e3 * dt / steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "rtf": synth.FRAMES_PER_SECOND / v,
-            "config": {"workload": wl.name, "streams": 1, "prompt_len": 16},
+            "config": workload_config(wl, world),
             "cpu_baseline": {"value": v, "unit": UNIT, "cores": oracle.max_threads(),
                              "kind": "oracle",
                              "sample": f"{steps} frames of one stream after a 16-position prompt "
-                                       f"(oracle steps capped at 8 to bound CPU time)"},
+                                       f"(oracle steps capped at 8 to bound CPU time; the workload's own "
+                                       f"prompt and streams are in config)"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -502,15 +525,7 @@ def main():
             "data": "synthetic (random N(0,0.02) weights of the named shapes, N(0,1) prompts, "
                     "seeded uniforms)",
             "rtf": synth.FRAMES_PER_SECOND / (value / world),
-            "config": {"workload": wl.name, "streams_per_gpu": B,
-                       "prompt_len": lens if B > 1 else lens[0], "kv_cap": wl.kv_cap,
-                       "page_size": wl.page_size,
-                       "kv_cache": {synth.DTYPE_F32: "fp32", synth.DTYPE_BF16: "bf16"}.get(s.kv_dtype, "?"),
-                       "frames_per_episode": wl.frames,
-                       "sampling": "greedy" if not wl.sampling.do_sample else "top_k50_T0.9_rep1.05",
-                       "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2: each step streams %.2f GB of weights"
-                             % (bytes_per_step / 1e9)},
+            "config": workload_config(wl, world),
             "roofline": {"bound": "hbm",
                          "kernel": ("frame_kernel (persistent, one launch per frame)"
                                     if launches == args.steps else
