@@ -59,6 +59,23 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     assert capsys.readouterr().out == ""
 
 
+def test_reference_arm_reports_the_workload_config(monkeypatch, capsys):
+    """The reference arm (the oracle on the host, a bounded sample) prints one
+    JSON line whose config is the workload's own -- the object the GPU arm
+    prints -- and describes its sample in cpu_baseline."""
+    import json
+    from autoregressive_tts_decode_gb300 import synth
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    args = types.SimpleNamespace(workload="tiny", steps=1, warmup=0, gpus=1)
+    bench.run_reference(args)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.workload_config(synth.WORKLOADS["tiny"], 1)
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
 def _sources():
     out = []
     for f in bench.KERNEL_SOURCES:
