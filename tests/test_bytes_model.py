@@ -73,3 +73,29 @@ def test_talker_module_below_page_figure():
     size; our counted Talker must stay below it."""
     t = bm.module_bytes(synth.SHAPE_17B)["talker"] / 1e9
     assert 2.8 < t < golden()["talker_gb_fp16"]
+
+
+def test_fp8_frame_bytes_are_codes_plus_row_scales():
+    """FP8 matrices cost one byte per weight plus an fp32 scale per output row
+    (the row scales of the E4M3 format this library reads); gains, embedding rows
+    and the KV cache are priced as in the bf16 shape."""
+    s = synth.SHAPE_17B
+    b = bm.frame_bytes(s, 200)
+    f = bm.frame_bytes(synth.SHAPE_17B_FP8, 200)
+    hq = s.n_q_heads * s.head_dim
+
+    def mats(D, F, L, V):  # (rows, cols) of a stack's matrices and its head
+        return [(s.qkv_rows, D), (D, hq), (2 * F, D), (D, F)] * L + [(V, D)]
+
+    talker = mats(s.talker_hidden, s.talker_ffn, s.talker_layers, s.codec_vocab)
+    cp = mats(s.cp_hidden, s.cp_ffn, s.cp_layers, s.cp_vocab) + [(s.cp_hidden, s.talker_hidden)]
+
+    def fp8_minus_bf16(m):
+        return sum(r * c + 4 * r - 2 * r * c for r, c in m)
+
+    assert f.talker_weights - b.talker_weights == fp8_minus_bf16(talker)
+    assert f.cp_pass_weights - b.cp_pass_weights == fp8_minus_bf16(cp)
+    assert (f.embed_rows, f.kv_read, f.kv_write) == (b.embed_rows, b.kv_read, b.kv_write)
+    # weights per frame: 2.66 GB in FP8 against 5.32 GB in bf16
+    assert (f.talker_weights + 15 * f.cp_pass_weights) / 1e9 == pytest.approx(2.66, abs=0.01)
+    assert (b.talker_weights + 15 * b.cp_pass_weights) / 1e9 == pytest.approx(5.32, abs=0.01)
