@@ -194,6 +194,9 @@ class Engine:
 
     def close(self):
         if getattr(self, "h", None) is not None and self.h.value:
+            # queued work still reads the workspace this object owns: wait for
+            # it (a recorded error was the caller's to collect) before release
+            load().q3tts_sync_status(self.h)
             load().q3tts_destroy(self.h)
             self.h = None
 

@@ -335,8 +335,14 @@ uint64_t q3tts_kernel_launches(const q3tts_handle* h);
  * persistent frame kernel. */
 int q3tts_debug_fail_barrier(q3tts_handle* h, int barrier, int wait_us);
 
+/* Releases the handle: its host state, events and captured graphs.  It does
+ * not wait for work queued on the handle's stream, so call q3tts_sync_status
+ * first if the workspace or the weights are freed right after; neither is
+ * touched by this call (both stay caller-owned).  NULL is a no-op. */
 void q3tts_destroy(q3tts_handle* h);
 
+/* A static, never-NULL description of a status code ("unknown error" for a
+ * code this library does not return). */
 const char* q3tts_strerror(int code);
 
 #ifdef __cplusplus
