@@ -175,7 +175,10 @@ int q3tts_stream_finished(q3tts_handle* h, int stream, int* finished);
 /* Bytes of workspace q3tts_create needs for cfg (0 if cfg is invalid). */
 size_t q3tts_workspace_size(const q3tts_config* cfg);
 
-/* Builds a handle over caller-owned weights and workspace (device memory of at
+/* Counterpart of loading the engine once with a fixed KV-cache capacity
+ * ("qwen3-tts-hip" README, "Library Usage": load_with_max_frames,
+ * EngineOptions::max_cache_steps).
+ * Builds a handle over caller-owned weights and workspace (device memory of at
  * least q3tts_workspace_size(cfg) bytes, 256-byte aligned).  cuda_stream is a
  * cudaStream_t (NULL = legacy default stream).  Uploads RoPE tables and the
  * library's re-laid-out weight copies into the workspace and synchronises
@@ -196,7 +199,13 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
  * is exhausted. */
 int q3tts_prefill(q3tts_handle* h, int stream_id, const float* embeds_dev, int len);
 
-/* Decodes one frame for each of n_active streams (distinct ids, host array
+/* One acoustic frame as defined at the top of this header ("Running Qwen3-TTS
+ * on an AMD R9700", section "Running Qwen3-TTS"): the semantic draw from the
+ * pending Talker logits, 15 CodePredictor passes each ending in a head and a
+ * draw, the sum of the 16 code embeddings, and one Talker step.  The draws
+ * follow the GenerateOptions controls ("qwen3-tts-hip" README, "Library
+ * Usage").
+ * Decodes one frame for each of n_active streams (distinct ids, host array
  * stream_ids[n_active]; params: host array [n_active]).
  *   uniforms_dev     device fp32 [n_active, 16]: the uniform in [0,1) for each
  *                    draw (codebook order); ignored by greedy draws.
