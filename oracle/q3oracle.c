@@ -36,6 +36,14 @@
  *   final-normed hidden and the semantic code's embedding); the repetition
  *   penalty follows the usual divide-positive / multiply-negative rule over
  *   the semantic codes already emitted in the stream.
+ *
+ * Pins: every function here is checked by CPU tests against something other
+ * than itself -- library routines (rms_norm, scaled_dot_product_attention,
+ * silu, linear, torch's bf16 and float8_e4m3fn conversions), closed forms (RoPE
+ * on basis vectors, one-position attention, identity-stack frames), invariants
+ * (incremental decode = one causal pass), an exhaustive sampler check on a
+ * fine grid of u, and the pages' frame constants and module sizes.  No
+ * function is left without a pin.
  */
 #include <math.h>
 #include <stdint.h>
