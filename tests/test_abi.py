@@ -1,6 +1,7 @@
 """The C ABI without a GPU: the library builds for sm_103a, loads, and exports
 every function include/q3tts.h declares; the binding mirrors the header's
-structs and constants."""
+structs and constants; the host-side argument checks (NULL handles, unaligned
+weights) answer before any device work; every status code has its text."""
 import ctypes
 import os
 import re
@@ -149,3 +150,53 @@ def test_create_rejects_unaligned_weight_pointers(lib):
         h = ctypes.c_void_p()
         rc = L.q3tts_create(ctypes.byref(cfg), ctypes.byref(w), ws, 1 << 60, None, ctypes.byref(h))
         assert rc == q3tts.ERR_CUDA
+
+
+def test_every_call_rejects_a_null_handle_on_the_host(lib):
+    """The calls' argument checks come before any device work: every function
+    the header declares, given a NULL handle (or NULL required pointers),
+    returns Q3TTS_ERR_ARG -- here, with no device at all.  kernel_launches(NULL)
+    is 0, destroy(NULL) is a no-op and create clears its output handle."""
+    L = q3tts.load(build.LIB)
+    N, E = None, q3tts.ERR_ARG
+    out = ctypes.c_void_p(0x1000)
+    fin = ctypes.c_int(7)
+    calls = {
+        "q3tts_workspace_size": (lambda: L.q3tts_workspace_size(N), 0),
+        "q3tts_create": (lambda: L.q3tts_create(N, N, N, 0, N, ctypes.byref(out)), E),
+        "q3tts_prefill": (lambda: L.q3tts_prefill(N, 0, N, 1), E),
+        "q3tts_step_frame": (lambda: L.q3tts_step_frame(N, N, N, 1, N, N, N, N), E),
+        "q3tts_step_frames": (lambda: L.q3tts_step_frames(N, N, N, 1, 1, N, N, N, N), E),
+        "q3tts_frames_ready": (lambda: L.q3tts_frames_ready(N), E),
+        "q3tts_step_frame_static": (lambda: L.q3tts_step_frame_static(N, N, 0, N, N, N, N), E),
+        "q3tts_read_pending": (lambda: L.q3tts_read_pending(N, 0, N, N), E),
+        "q3tts_reset": (lambda: L.q3tts_reset(N, -1), E),
+        "q3tts_stream_length": (lambda: L.q3tts_stream_length(N, 0), E),
+        "q3tts_stream_finished": (lambda: L.q3tts_stream_finished(N, 0, ctypes.byref(fin)), E),
+        "q3tts_sync_status": (lambda: L.q3tts_sync_status(N), E),
+        "q3tts_kernel_launches": (lambda: L.q3tts_kernel_launches(N), 0),
+        "q3tts_debug_fail_barrier": (lambda: L.q3tts_debug_fail_barrier(N, 0, 1000), E),
+        "q3tts_destroy": (lambda: L.q3tts_destroy(N), ...),  # void: only returns
+        "q3tts_strerror": (lambda: L.q3tts_strerror(q3tts.ERR_ARG), b"invalid argument"),
+    }
+    assert set(calls) == set(header_functions())
+    for name, (call, want) in calls.items():
+        got = call()
+        assert want is ... or got == want, name
+    assert out.value is None
+    assert fin.value == 7
+
+
+def test_strerror_describes_every_status_code(lib):
+    """Each status code the header defines has its own description; any other
+    value reads "unknown error" (a static string, never NULL)."""
+    L = q3tts.load(build.LIB)
+    src = open(HEADER).read()
+    codes = {k: int(v) for k, v in re.findall(r"#define (Q3TTS_(?:OK|ERR_[A-Z_]+)) \(?(-?\d+)\)?", src)}
+    assert len(codes) == 8
+    texts = {k: L.q3tts_strerror(v).decode() for k, v in codes.items()}
+    assert texts["Q3TTS_OK"] == "ok"
+    assert "unknown error" not in texts.values()
+    assert len(set(texts.values())) == len(texts)
+    for v in (-8, -99, 1, 1 << 30):
+        assert L.q3tts_strerror(v).decode() == "unknown error"
