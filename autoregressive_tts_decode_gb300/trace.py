@@ -10,8 +10,10 @@ spent waiting for ring data in the step before (aux in units of 16 clock64
 cycles).  This module builds that library beside the normal one (under
 _build/trace/), runs frames of a workload on it, and tabulates per step kind
 the median time from a step's start to its grid-barrier arrival (work) and
-from there to the next step's start (wait).  Each mark costs about 0.1 us, so
-a traced frame runs slower than a plain one.
+from there to the next step's start (wait), and per grid barrier the CTAs'
+arrival skew and the release time from the last arrival to the first pass
+(globaltimer, one clock for all SMs).  Each mark costs about 0.1 us, so a
+traced frame runs slower than a plain one.
 
     python -m autoregressive_tts_decode_gb300.trace --workload 1.7b --frames 12
 """
@@ -32,7 +34,7 @@ from . import build
 # the kernel's trace buffer: FK_MAXCTA rows of FK_TRACE_EV records of 4 words
 MAXCTA, TRACE_EV = 256, 8192
 # record tags (TR_* in csrc/frame_kernel.cu)
-TR_STEP, TR_ARRIVE, TR_END, TR_CW = 1, 3, 7, 8
+TR_STEP, TR_ARRIVE, TR_PASS, TR_END, TR_CW = 1, 3, 4, 7, 8
 FRAME_START = 15  # the aux of the frame's opening TR_STEP
 # step kinds in the kernel's order (enum StepKind); the Talker's draw, QKV and
 # FFN steps (pass 15) get a "_T" suffix
@@ -135,6 +137,52 @@ def step_table(trace: np.ndarray, mhz: float = 2070.0) -> Dict[str, Tuple[float,
                 float(np.median(ring[k]))) for k in work}
 
 
+def barrier_table(trace: np.ndarray) -> Dict[str, Tuple[float, float, float, float]]:
+    """Per kind of the step that a grid barrier ends ("START" for the frame's
+    first): (barriers per frame, median arrival skew us -- the last CTA's
+    arrival after the median CTA's --, median arrival spread us -- last minus
+    first --, median release us -- from the last arrival to the first CTA
+    that passes).  Times from the globaltimer, one clock for all SMs (ns);
+    every CTA passes the same barriers in the same order."""
+    tag = (trace[:, :, 3] >> 16).astype(np.int64)
+    aux = (trace[:, :, 3] & 0xFFFF).astype(np.int64)
+    g = trace[:, :, 0].astype(np.int64) | (trace[:, :, 1].astype(np.int64) << 32)
+    arr, pas, kinds = [], [], None
+    for c in range(trace.shape[0]):
+        n = int((tag[c] != 0).sum())
+        cur, a, p, k = None, [], [], []
+        for i in range(n):
+            t = int(tag[c, i])
+            if t == TR_STEP:
+                cur = "START" if aux[c, i] == FRAME_START else step_kind(int(aux[c, i]))
+            elif t == TR_ARRIVE:
+                a.append(int(g[c, i]))
+                k.append(cur)
+            elif t == TR_PASS:
+                p.append(int(g[c, i]))
+        if a:
+            arr.append(a)
+            pas.append(p)
+            kinds = kinds or k
+    if not arr:
+        return {}
+    nb = min(min(len(a) for a in arr), min(len(p) for p in pas))
+    # nanoseconds since the epoch exceed float64's exact range: subtract a base first
+    base = min(a[0] for a in arr)
+    A = np.array([a[:nb] for a in arr], dtype=np.int64) - base
+    P = np.array([p[:nb] for p in pas], dtype=np.int64) - base
+    A, P = A.astype(np.float64), P.astype(np.float64)
+    skew = (A.max(0) - np.median(A, 0)) / 1e3
+    spread = (A.max(0) - A.min(0)) / 1e3
+    release = (P.min(0) - A.max(0)) / 1e3
+    out = {}
+    for k in dict.fromkeys(kinds[:nb]):
+        sel = np.array([kk == k for kk in kinds[:nb]])
+        out[k] = (float(sel.sum()), float(np.median(skew[sel])), float(np.median(spread[sel])),
+                  float(np.median(release[sel])))
+    return out
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--workload", default="1.7b")
@@ -146,6 +194,9 @@ def main(argv=None):
     print("%-9s %6s %8s %8s %9s %10s" % ("step", "count", "work us", "wait us", "ring us", "total us"))
     for k, (n, w, q, r) in sorted(table.items(), key=lambda kv: -kv[1][0] * (kv[1][1] + kv[1][2])):
         print("%-9s %6.0f %8.2f %8.2f %9.2f %10.1f" % (k, n, w, q, r, n * (w + q)))
+    print("%-9s %6s %8s %9s %10s" % ("barrier", "count", "skew us", "spread us", "release us"))
+    for k, (n, sk, sp, rl) in barrier_table(trace).items():
+        print("%-9s %6.0f %8.2f %9.2f %10.2f" % (k, n, sk, sp, rl))
 
 
 if __name__ == "__main__":

@@ -1,7 +1,8 @@
 """The frame-kernel trace summary (autoregressive_tts_decode_gb300.trace) on a
 hand-built trace: step kinds decoded from the step marks, work = step start to
 grid-barrier arrival, wait = arrival to the next step, ring waits attributed to
-the step before their record."""
+the step before their record; grid-barrier skew and release times from the
+globaltimer."""
 import numpy as np
 
 from autoregressive_tts_decode_gb300 import trace as T
@@ -38,3 +39,33 @@ def test_step_table_on_a_hand_built_trace():
 def test_step_kinds_follow_the_kernel_enum():
     assert T.step_kind(0) == "DRAW" and T.step_kind(0 | (T.TALKER_PASS << 4)) == "DRAW_T"
     assert T.step_kind(8) == "T_HEAD" and T.step_kind(6 | (T.TALKER_PASS << 4)) == "T_ATTN"
+
+
+def _grec(tag, aux, ns):
+    return [ns & 0xFFFFFFFF, ns >> 32, 0, (tag << 16) | aux]
+
+
+def test_barrier_table_on_a_hand_built_trace():
+    """Skew, spread and release of grid barriers from globaltimer records of
+    three CTAs, with the timer's epoch-sized base (about 1.8e18 ns), which
+    float64 cannot hold to the nanosecond."""
+    base = 1_780_000_000_000_000_000
+    attn, ffn = 3 | (2 << 4), 4 | (2 << 4)
+    times = [  # per CTA: (arrive, pass) of the attention barrier, then of the FFN barrier
+        ((1000, 3000), (5000, 8000)),
+        ((1200, 3100), (5600, 8000)),
+        ((2000, 3050), (5200, 8100)),
+    ]
+    tr = np.zeros((4, T.TRACE_EV, 4), dtype=np.uint32)
+    for c, ((a0, p0), (a1, p1)) in enumerate(times):
+        rows = [_grec(T.TR_STEP, T.FRAME_START, base), _grec(T.TR_STEP, attn, base + 500),
+                _grec(T.TR_ARRIVE, 0, base + a0), _grec(T.TR_PASS, 0, base + p0),
+                _grec(T.TR_STEP, ffn, base + p0 + 10),
+                _grec(T.TR_ARRIVE, 0, base + a1), _grec(T.TR_PASS, 0, base + p1)]
+        tr[c, :len(rows)] = np.array(rows, dtype=np.uint64).astype(np.uint32)
+    tab = T.barrier_table(tr)
+    assert list(tab) == ["CP_ATTN", "FFN"]
+    # arrivals 1000/1200/2000 ns: skew 2000 - 1200, spread 1000, release 3000 - 2000
+    assert tab["CP_ATTN"] == (1.0, 0.8, 1.0, 1.0)
+    # arrivals 5000/5600/5200 ns: skew 5600 - 5200, spread 600, release 8000 - 5600
+    assert tab["FFN"] == (1.0, 0.4, 0.6, 2.4)
