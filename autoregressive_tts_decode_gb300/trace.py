@@ -12,7 +12,8 @@ _build/trace/), runs frames of a workload on it, and tabulates per step kind
 the median time from a step's start to its grid-barrier arrival (work) and
 from there to the next step's start (wait), and per grid barrier the CTAs'
 arrival skew and the release time from the last arrival to the first pass
-(globaltimer, one clock for all SMs).  Each mark costs about 0.1 us, so a
+(globaltimer, one clock for all SMs), and the frame split into the intervals
+between barriers, which add up to the whole frame.  Each mark costs about 0.1 us, so a
 traced frame runs slower than a plain one.
 
     python -m autoregressive_tts_decode_gb300.trace --workload 1.7b --frames 12
@@ -183,6 +184,56 @@ def barrier_table(trace: np.ndarray) -> Dict[str, Tuple[float, float, float, flo
     return out
 
 
+def interval_table(trace: np.ndarray) -> Tuple[Dict[str, Tuple[int, float, float]], float]:
+    """The frame split into barrier intervals, which add up to the whole frame:
+    from one grid barrier's first pass (the frame's first step for the first
+    interval) to the next barrier's last arrival -- the slowest CTA's work --
+    plus that barrier's release to its first pass.  Intervals are keyed by the
+    step kinds they hold, joined by "+", with (count, work us, release us)
+    summed per key; the second value is the tail from the last barrier's first
+    pass to the last CTA's end mark, us.  Globaltimer (ns), as barrier_table."""
+    tag = (trace[:, :, 3] >> 16).astype(np.int64)
+    aux = (trace[:, :, 3] & 0xFFFF).astype(np.int64)
+    g = trace[:, :, 0].astype(np.int64) | (trace[:, :, 1].astype(np.int64) << 32)
+    rows = []  # per CTA: (frame start, [(arrive, pass, step kinds)], end)
+    for c in range(trace.shape[0]):
+        n = int((tag[c] != 0).sum())
+        start = end = arrive = None
+        steps, bars = [], []
+        for i in range(n):
+            t, x, tm = int(tag[c, i]), int(aux[c, i]), int(g[c, i])
+            if t == TR_STEP:
+                if x == FRAME_START:
+                    start = tm
+                else:
+                    steps.append(step_kind(x))
+            elif t == TR_ARRIVE:
+                arrive = tm
+            elif t == TR_PASS:
+                bars.append((arrive, tm, "+".join(steps)))
+                steps = []
+            elif t == TR_END:
+                end = tm
+        if start is not None:
+            rows.append((start, bars, end))
+    if not rows:
+        return {}, 0.0
+    nb = min(len(r[1]) for r in rows)
+    prev = min(r[0] for r in rows)
+    out: Dict[str, list] = {}
+    for b in range(nb):
+        last_arrival = max(r[1][b][0] for r in rows)
+        first_pass = min(r[1][b][1] for r in rows)
+        e = out.setdefault(rows[0][1][b][2], [0, 0.0, 0.0])
+        e[0] += 1
+        e[1] += (last_arrival - prev) / 1e3
+        e[2] += (first_pass - last_arrival) / 1e3
+        prev = first_pass
+    ends = [r[2] for r in rows if r[2] is not None]
+    tail = (max(ends) - prev) / 1e3 if ends else 0.0
+    return {k: (v[0], v[1], v[2]) for k, v in out.items()}, tail
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--workload", default="1.7b")
@@ -194,6 +245,11 @@ def main(argv=None):
     print("%-9s %6s %8s %8s %9s %10s" % ("step", "count", "work us", "wait us", "ring us", "total us"))
     for k, (n, w, q, r) in sorted(table.items(), key=lambda kv: -kv[1][0] * (kv[1][1] + kv[1][2])):
         print("%-9s %6.0f %8.2f %8.2f %9.2f %10.1f" % (k, n, w, q, r, n * (w + q)))
+    intervals, tail = interval_table(trace)
+    print("%-44s %6s %9s %10s" % ("interval (steps between barriers)", "count", "work us", "release us"))
+    for k, (n, w, r) in sorted(intervals.items(), key=lambda kv: -(kv[1][1] + kv[1][2])):
+        print("%-44s %6d %9.1f %10.1f" % (k[:44] or "(none)", n, w, r))
+    print("%-44s %6s %9.1f" % ("tail after the last barrier", "", tail))
     print("%-9s %6s %8s %9s %10s" % ("barrier", "count", "skew us", "spread us", "release us"))
     for k, (n, sk, sp, rl) in barrier_table(trace).items():
         print("%-9s %6.0f %8.2f %9.2f %10.2f" % (k, n, sk, sp, rl))

@@ -69,3 +69,26 @@ def test_barrier_table_on_a_hand_built_trace():
     assert tab["CP_ATTN"] == (1.0, 0.8, 1.0, 1.0)
     # arrivals 5000/5600/5200 ns: skew 5600 - 5200, spread 600, release 8000 - 5600
     assert tab["FFN"] == (1.0, 0.4, 0.6, 2.4)
+
+
+def test_interval_table_adds_up_to_the_frame():
+    """Two CTAs, two barriers and an end mark: the intervals (slowest CTA's work
+    + release) and the tail add up to the frame, first start to last end."""
+    base = 1_780_000_000_000_000_000
+    qkv, attn, ffn, head = 2 | (3 << 4), 3 | (3 << 4), 4 | (3 << 4), 5 | (3 << 4)
+    ctas = [
+        [(T.TR_STEP, T.FRAME_START, 0), (T.TR_STEP, qkv, 10), (T.TR_STEP, attn, 100),
+         (T.TR_ARRIVE, 0, 300), (T.TR_PASS, 0, 500), (T.TR_STEP, ffn, 510),
+         (T.TR_ARRIVE, 0, 900), (T.TR_PASS, 0, 1200), (T.TR_STEP, head, 1210), (T.TR_END, 0, 1400)],
+        [(T.TR_STEP, T.FRAME_START, 5), (T.TR_STEP, qkv, 12), (T.TR_STEP, attn, 110),
+         (T.TR_ARRIVE, 0, 400), (T.TR_PASS, 0, 520), (T.TR_STEP, ffn, 530),
+         (T.TR_ARRIVE, 0, 1000), (T.TR_PASS, 0, 1210), (T.TR_STEP, head, 1220), (T.TR_END, 0, 1500)],
+    ]
+    tr = np.zeros((3, T.TRACE_EV, 4), dtype=np.uint32)
+    for c, recs in enumerate(ctas):
+        tr[c, :len(recs)] = np.array([_grec(t, a, base + ns) for t, a, ns in recs],
+                                     dtype=np.uint64).astype(np.uint32)
+    tab, tail = T.interval_table(tr)
+    assert tab == {"QKV+CP_ATTN": (1, 0.4, 0.1), "FFN": (1, 0.5, 0.2)}
+    assert tail == 0.3
+    assert sum(w + r for _, w, r in tab.values()) + tail == 1.5  # first start 0 to last end 1500 ns
