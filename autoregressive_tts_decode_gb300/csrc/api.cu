@@ -313,10 +313,11 @@ int q3tts_prefill(q3tts_handle* h, int sid, const float* embeds_dev, int len) {
   const int ps = h->c.page_size;
   const int need = (len + ps - 1) / ps;
   free_stream_pages(h, sid);
-  if ((int)h->free_pages.size() < need) {
-    h->len[sid] = -1;
-    return Q3TTS_ERR_CAPACITY;
-  }
+  // the stream has no prompt until this call succeeds: an error below (pool
+  // exhausted, a failed copy or launch) leaves it that way, never with its old
+  // length over pages it no longer holds
+  h->len[sid] = -1;
+  if ((int)h->free_pages.size() < need) return Q3TTS_ERR_CAPACITY;
   std::vector<int> row(need);
   for (int i = 0; i < need; ++i) {
     row[i] = h->free_pages.back();

@@ -196,7 +196,10 @@ int q3tts_create(const q3tts_config* cfg, const q3tts_weights* w, void* workspac
  * their KV and leaves the final-normed hidden and codec logits of position
  * len-1 as the stream's pending state, from which the next frame's semantic
  * token is drawn.  Q3TTS_ERR_CAPACITY if len >= kv_cap_steps or the page pool
- * is exhausted. */
+ * is exhausted.  Argument errors and len >= kv_cap_steps leave the stream as
+ * it was; any later error (page pool exhausted, a CUDA failure) leaves it
+ * without a prompt, so its frames get Q3TTS_ERR_STATE until a prefill
+ * succeeds. */
 int q3tts_prefill(q3tts_handle* h, int stream_id, const float* embeds_dev, int len);
 
 /* One acoustic frame as defined at the top of this header ("Running Qwen3-TTS
